@@ -1,0 +1,518 @@
+"""Benchmark of the paged-attention hot path on GB300.
+
+One step = one decode step of the whole path on one batch: pa_append_kv
+writes each request's new K/V token into the page pool by slot_mapping, then
+pa_attention (which routes L = 1 to the split-KV decode kernel) attends over
+every request's paged context. Inputs are seeded synthetic batches shaped
+like the pages' decode workloads (no datasets, no weights).
+
+Prints one JSON line. ``value`` is decode K/V GB/s over the whole step
+(algorithmic bytes / device time), with the inputs resident in HBM; four or
+more rotating copies of the page pool keep every step's K/V reads cold in L2.
+
+    python bench.py [--gpus N --steps K --warmup W] [--workload NAME]
+    python bench.py --impl reference ...   (the fp64 CPU oracle, timed)
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+path has no exchange step; "scaling": "weak") and value sums all ranks' bytes
+over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "paged decode K/V GB/s & tokens/s (% HBM peak); prefill TFLOP/s (% bf16 peak)"
+DEFAULT_WORKLOAD = "decode_b32_gqa7_ps16"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def step_bytes(b: wl.PagedBatch):
+    """Algorithmic bytes of one step: (decode kernel, append kernel)."""
+    n = b.context_lens.astype(np.int64)
+    kv = int(n.sum()) * b.H_kv * b.D * 2 * 2
+    qo = 2 * b.B * b.H_q * b.L * b.D * 2
+    tables = int(np.ceil(n / b.page_size).sum()) * 4 + b.B * 4
+    decode = kv + qo + tables
+    append = 2 * (2 * b.B * b.H_kv * b.L_new * b.D * 2) + b.B * b.L_new * 4
+    return decode, append
+
+
+def prefill_flops(b: wl.PagedBatch) -> float:
+    """Causal-useful FLOPs: 4 * D per (query row, visible key) pair."""
+    total = 0
+    for n in b.context_lens.astype(np.int64):
+        for i in range(b.L):
+            p = int(n) - b.L + i
+            vis = min(int(n), p + 1) if b.causal else int(n)
+            total += max(0, vis)
+    return 4.0 * b.D * b.H_q * total
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def source_digest(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(kernel_key, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)[kernel_key]
+    except Exception:
+        return None
+    if t.get("workload") != workload:
+        return None
+    if t.get("source_sha") != source_digest(t["source"]):
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.marks = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, name):
+        self.marks.append((name, time.time()))
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        parsed = []
+        for ts, line in self.rows:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                parsed.append((ts, float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        window = [p for p in parsed if t0 <= p[0] <= t1]
+        scope = "timed"
+        if not window:          # very short timed region: widen to the whole run
+            window, scope = parsed, "run"
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in window for i, v in enumerate(p[3])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": float(np.median([p[1] for p in window])),
+                "sm_max_mhz": float(max(p[2] for p in window)),
+                "reasons": reasons, "samples": len(window), "window": scope}
+
+
+class OracleSampler:
+    """The fp64 CPU oracle on the same workload, on bounded samples: whole
+    (request, KV head) groups (all query heads of the group, every query row)
+    in batch order, `chunk` groups per oracle call (rows spread over
+    `n_threads` threads). The append is applied once, up front."""
+
+    def __init__(self, b: wl.PagedBatch, n_threads: int):
+        import oracle
+        self.oracle = oracle
+        self.b = b
+        self.n_threads = n_threads
+        self.kp, self.vp = b.key_pages.copy(), b.value_pages.copy()
+        oracle.append_kv(b.key_new, b.value_new, self.kp, self.vp, b.slot_mapping, b.page_size)
+        self.G = b.H_q // b.H_kv
+        self.groups = [(r, h) for r in range(b.B) for h in range(b.H_kv)]
+        self.k = 0
+
+    def run(self, budget_s: float, chunk=None):
+        """Runs calls until budget_s has passed (at least one call).
+        Returns (GB/s of K/V read, groups done, seconds)."""
+        b, G = self.b, self.G
+        if chunk is None:
+            chunk = max(1, min(len(self.groups), -(-self.n_threads // (G * b.L))))
+        done_bytes, n_groups, t_start = 0, 0, time.perf_counter()
+        while True:
+            sel = [self.groups[(self.k + j) % len(self.groups)] for j in range(chunk)]
+            self.k += chunk
+            rows = np.asarray([(r, h * G + g, i) for r, h in sel for g in range(G)
+                               for i in range(b.L)], dtype=np.int32)
+            self.oracle.attention(b.query, self.kp, self.vp, b.block_table, b.context_lens,
+                                  b.page_size, scale=b.scale, causal=b.causal, rows=rows,
+                                  n_threads=self.n_threads)
+            done_bytes += sum(int(b.context_lens[r]) * b.D * 2 * 2 for r, _ in sel)
+            n_groups += len(sel)
+            el = time.perf_counter() - t_start
+            if el >= budget_s:
+                return done_bytes / el / 1e9, n_groups, el
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return 0
+    b = wl.make_workload(args.workload)
+    cores = os.cpu_count() or 1
+    dec_bytes, _ = step_bytes(b)
+    total_budget = 150.0
+    per_step = max(0.02, total_budget / max(1, args.steps + args.warmup))
+    sampler = OracleSampler(b, cores)
+    for _ in range(args.warmup):
+        sampler.run(per_step, chunk=1)
+    t0 = time.perf_counter()
+    rates = []
+    groups = 0
+    for _ in range(args.steps):
+        r, g, _ = sampler.run(per_step, chunk=1)
+        rates.append(r)
+        groups += g
+    el = time.perf_counter() - t0
+    value = float(np.mean(rates))
+    sample = (f"{args.workload}: per step, whole (request, KV head) groups of the batch "
+              f"(all query heads and rows of each) for ~{per_step:.3f} s; {groups} groups over "
+              f"{args.steps} steps; GB/s of K/V read")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * el / max(1, args.steps), 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(b, world, "none (CPU)"),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(b, world, l2_note):
+    n = b.context_lens
+    return {"workload": b.name, "B": b.B, "H_q": b.H_q, "H_kv": b.H_kv, "D": b.D,
+            "page_size": b.page_size, "L": b.L, "L_new": b.L_new, "num_pages": b.num_pages,
+            "context_lens": {"min": int(n.min()), "max": int(n.max()), "sum": int(n.sum())},
+            "recipe": b.recipe, "seed": b.seed, "l2": l2_note,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=8.0,
+                    help="seconds of oracle work for the cpu_baseline leg")
+    ap.add_argument("--no-prefill", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+
+    rank = _env_int("RANK", 0)
+    world = _env_int("WORLD_SIZE", 1)
+    local_rank = _env_int("LOCAL_RANK", 0)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import paged_kv_attention_06_gb300 as pa
+    from paged_kv_attention_06_gb300 import binding
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    b = wl.make_workload(args.workload)
+
+    def to_dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    dec_bytes, app_bytes = step_bytes(b)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    pool_bytes = 2 * b.key_pages.nbytes
+    copies = max(4, math.ceil(4 * l2 / max(1, dec_bytes)))
+    kp0, vp0 = to_dev(b.key_pages), to_dev(b.value_pages)
+    pools = [(kp0, vp0)] + [(kp0.clone(), vp0.clone()) for _ in range(copies - 1)]
+    q = to_dev(b.query)
+    bt = to_dev(b.block_table)
+    cl = to_dev(b.context_lens)
+    kn, vn = to_dev(b.key_new), to_dev(b.value_new)
+    sm = to_dev(b.slot_mapping)
+    out = torch.empty_like(q)
+    shape = pa.make_shape(q.shape, kp0.shape, bt.shape[1])
+    app_shape = pa.pa_shape(b.B, 0, b.H_kv, b.D, b.L_new, b.num_pages, 0)
+    ws, ws_need = pa.decode_workspace(shape, device)
+    stream = torch.cuda.current_stream(device)
+    sp = stream.cuda_stream
+    max_ctx = int(b.context_lens.max())
+    lib = binding._lib
+    route = int(lib.pa_attention_route(shape, max_ctx))
+
+    # Pre-marshalled C-ABI calls (the step launches only these two kernels).
+    def make_calls(kp, vp):
+        app = (kn.data_ptr(), vn.data_ptr(), kp.data_ptr(), vp.data_ptr(), sm.data_ptr(),
+               b.page_size, app_shape, sp)
+        att = (q.data_ptr(), kp.data_ptr(), vp.data_ptr(), bt.data_ptr(), cl.data_ptr(),
+               b.page_size, b.scale, int(b.causal), out.data_ptr(), shape, max_ctx,
+               ws.data_ptr(), ws_need, sp)
+        return app, att
+
+    calls = [make_calls(kp, vp) for kp, vp in pools]
+
+    def step(k, ev=None):
+        app, att = calls[k % copies]
+        st = lib.pa_append_kv(*app)
+        if ev is not None:
+            ev[0].record(stream)
+        st |= lib.pa_attention(*att)
+        if ev is not None:
+            ev[1].record(stream)
+        return st
+
+    for k in range(args.warmup):
+        if step(k):
+            raise RuntimeError("warm-up step failed")
+    torch.cuda.synchronize()
+    status, flags = pa.pa_get_device_error()
+    if status:
+        raise RuntimeError(f"device error during warm-up: {flags:#x}")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    host0 = time.perf_counter()
+    t_start.record(stream)
+    bad = 0
+    for k in range(args.steps):
+        bad |= step(k, evs[k])
+    t_end.record(stream)
+    host_s = time.perf_counter() - host0
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    if bad:
+        raise RuntimeError("a timed step returned an error status")
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    status, flags = pa.pa_get_device_error()
+    if status:
+        raise RuntimeError(f"device error in the timed region: {flags:#x}")
+    if dist is not None:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- e2e: same step through the C ABI from pinned host buffers ---------
+    h_q = torch.from_numpy(b.query.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_kn = torch.from_numpy(b.key_new.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_vn = torch.from_numpy(b.value_new.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_sm = torch.from_numpy(b.slot_mapping).pin_memory()
+    h_bt = torch.from_numpy(b.block_table).pin_memory()
+    h_cl = torch.from_numpy(b.context_lens).pin_memory()
+    h_out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_sm, h_bt, h_cl))
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_steps = max(10, min(args.steps, 2000))
+    for k in range(3):
+        step(k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(e2e_steps):
+        q.copy_(h_q, non_blocking=True)
+        kn.copy_(h_kn, non_blocking=True)
+        vn.copy_(h_vn, non_blocking=True)
+        sm.copy_(h_sm, non_blocking=True)
+        bt.copy_(h_bt, non_blocking=True)
+        cl.copy_(h_cl, non_blocking=True)
+        step(k)
+        h_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    # ---- secondary: chunked prefill TFLOP/s (prefill route) -----------------
+    prefill = None
+    if not args.no_prefill and world == 1:
+        prefill = bench_prefill(pa, binding, torch, device, stream)
+
+    clocks.stop()
+    ck = clocks.summary(wall0, wall1)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    ms_step = total_ms / args.steps
+    dec_avg_ms = float(np.mean(dec_ms))
+    value = world * (dec_bytes + app_bytes) / (ms_step * 1e-3) / 1e9
+    hbm_peak, bf16_peak, peak_kind = load_peaks()
+    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
+    traffic = committed_traffic("decode_kernel", b.name)
+    cpu = None
+    if world == 1 or rank == 0:
+        cores = os.cpu_count() or 1
+        rate, groups, secs = OracleSampler(b, cores).run(args.cpu_budget)
+        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{args.workload}: {groups} whole (request, KV head) groups "
+                         f"(all {b.H_q // b.H_kv} query heads each), {secs:.1f} s on "
+                         f"{cores} threads; GB/s of K/V read"}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": workload_config(
+            b, world, f"{copies} rotating copies of the K/V pool "
+                      f"({copies * pool_bytes / 1e6:.0f} MB vs {l2 / 1e6:.0f} MB L2): each "
+                      f"step reads a copy last touched {copies - 1} steps earlier"),
+        "tokens_per_s": round(world * b.B / (ms_step * 1e-3), 1),
+        "decode_kernel_us": round(1e3 * dec_avg_ms, 3),
+        "route": "decode" if route == 0 else "prefill",
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "decode_kernel<128> (split-KV + fused merge)",
+                     "algorithmic_bytes_per_launch": dec_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * (dec_bytes + app_bytes) / (e2e_ms * 1e-3) / 1e9, 3),
+                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 6), "steps": e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "host_launch_us_per_step": round(1e6 * host_s / args.steps, 2),
+        "clocks": ck,
+    }
+    if prefill is not None:
+        prefill["roofline_frac_bf16"] = round(prefill["tflops"] / bf16_peak, 4)
+        prefill["peak_source"] = f"{peak_kind} bf16_tflops"
+        line["prefill"] = prefill
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_prefill(pa, binding, torch, device, stream, steps=20):
+    """Chunked causal prefill (512 new rows after a ragged prefix): append of
+    the 512 rows, then pa_attention (prefill route), timed with events."""
+    b = wl.make_workload("prefill_chunk512")
+
+    def to_dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    kp, vp = to_dev(b.key_pages), to_dev(b.value_pages)
+    q, bt, cl = to_dev(b.query), to_dev(b.block_table), to_dev(b.context_lens)
+    kn, vn, sm = to_dev(b.key_new), to_dev(b.value_new), to_dev(b.slot_mapping)
+    out = torch.empty_like(q)
+    flush = torch.empty(int(2 * torch.cuda.get_device_properties(device).L2_cache_size),
+                        dtype=torch.uint8, device=device)
+    pa.pa_append_kv(kn, vn, kp, vp, sm, b.page_size)
+    app, att = [], []
+    for k in range(steps + 3):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        pa.pa_append_kv(kn, vn, kp, vp, sm, b.page_size)
+        e[1].record(stream)
+        pa.pa_attention(q, kp, vp, bt, cl, b.page_size, scale=b.scale, causal=True, out=out,
+                        max_context_len=int(b.context_lens.max()))
+        e[2].record(stream)
+        if k >= 3:
+            app.append(e)
+    torch.cuda.synchronize()
+    st, flags = pa.pa_get_device_error()
+    if st:
+        raise RuntimeError(f"device error in prefill bench: {flags:#x}")
+    att_ms = float(np.median([e[1].elapsed_time(e[2]) for e in app]))
+    app_ms = float(np.median([e[0].elapsed_time(e[1]) for e in app]))
+    flops = prefill_flops(b)
+    _, app_bytes = step_bytes(b)
+    return {"workload": b.name, "tflops": round(flops / (att_ms * 1e-3) / 1e12, 3),
+            "attention_ms": round(att_ms, 4), "append_ms": round(app_ms, 4),
+            "append_gbs": round(app_bytes / (app_ms * 1e-3) / 1e9, 2),
+            "causal_useful_flops": flops, "steps": steps,
+            "l2": "2x L2 buffer written before every step (outside the events)"}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,195 @@
+/*
+ * pagedattn: paged K/V attention for NVIDIA GB300 (sm_103a).
+ *
+ * A C ABI over hand-written CUDA kernels. Query heads attend over a per-layer
+ * pool of fixed-size K/V pages through a per-request block table, without
+ * gathering a dense K/V tensor first.
+ *
+ * Conventions shared by every call:
+ *   - All tensors are raw DEVICE pointers to contiguous row-major buffers
+ *     owned by the caller. bf16 values are passed as their 16-bit patterns.
+ *   - Layouts (Week 3 Day 4: Direct Paged Attention, "The Paged Attention
+ *     API" and "How This Maps to tiny-llm"; Tutorial 13: Paged Attention and
+ *     Memory Management, section 6 "Paged Attention Metadata"):
+ *       query        [B, H_q, L, D]            bf16
+ *       out          [B, H_q, L, D]            bf16
+ *       key_pages    [P, H_kv, page_size, D]   bf16 (one pool per layer)
+ *       value_pages  [P, H_kv, page_size, D]   bf16
+ *       block_table  [B, max_pages]            int32, physical page ids
+ *       context_lens [B]                       int32, valid tokens per request
+ *     Logical position j of request b is slot j % page_size of physical page
+ *     block_table[b, j / page_size] (Week 3 Day 4, "Why block_table
+ *     Matters"). Entries past ceil(context_lens[b] / page_size) are never
+ *     read and may hold anything.
+ *   - GQA: query head h_q reads KV head h_q / (H_q / H_kv).
+ *   - Causal mask: query row i of request b sits at absolute position
+ *     context_lens[b] - L + i (the rows are the newest L positions) and sees
+ *     keys 0..that position. With causal = 0 every row sees all
+ *     context_lens[b] keys. A row that sees no key returns zeros.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Every call is asynchronous on it; nothing synchronises except
+ *     pa_get_device_error.
+ *   - Errors: a call that returns anything but PA_OK launched nothing and
+ *     touched no buffer. Per-request values that live on the device
+ *     (block_table entries, context_lens, slot_mapping) cannot be checked on
+ *     the host; the kernels check them, never access memory outside the
+ *     buffers for a bad value, and record it in a device error word that
+ *     pa_get_device_error reads.
+ *   - The library allocates no device memory on any call.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,    /* null pointer, bad size, bad scale, misalignment */
+    PA_ERR_UNSUPPORTED = 2,    /* D not 64/128, H_q % H_kv != 0, page_size not a
+                                  power of two in 1..256, shapes beyond limits */
+    PA_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required    */
+    PA_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed          */
+    PA_ERR_DEVICE_BOUNDS = 5,  /* a kernel met an out-of-range page id, slot or
+                                  context length (from pa_get_device_error)     */
+    PA_ERR_DEVICE_TIMEOUT = 6  /* a kernel's bounded wait on its own copies ran
+                                  out (from pa_get_device_error)                */
+} pa_status;
+
+/* Bits of the device error word reported by pa_get_device_error. */
+#define PA_DEVERR_PAGE_ID      0x1u  /* block_table entry outside [0, P)           */
+#define PA_DEVERR_SLOT         0x2u  /* slot_mapping entry >= P * page_size         */
+#define PA_DEVERR_CONTEXT_LEN  0x4u  /* context_lens entry < 0 or > max_pages*ps    */
+#define PA_DEVERR_TIMEOUT      0x8u  /* pipeline wait gave up                       */
+
+/* Problem sizes shared by every call. */
+typedef struct pa_shape {
+    int32_t batch;         /* B: requests                                       */
+    int32_t num_q_heads;   /* H_q (unused by pa_append_kv)                      */
+    int32_t num_kv_heads;  /* H_kv, must divide H_q                             */
+    int32_t head_dim;      /* D: 64 or 128                                      */
+    int32_t q_len;         /* L: query rows per request; for pa_append_kv the
+                              number of new tokens per request (L_new)          */
+    int32_t num_pages;     /* P: pages in the pool                              */
+    int32_t max_pages;     /* row length (stride) of block_table                */
+} pa_shape;
+
+/*
+ * Write path: scatter new K/V rows into the page pool by slot_mapping.
+ * (Reading vLLM's PagedAttention Kernel, 3.2 "Writing into the cache":
+ * the flat slot of a token is physical_block * page_size + offset.)
+ *
+ *   key, value      [B, H_kv, L_new, D] bf16, 16-byte aligned
+ *   key_pages, value_pages  [P, H_kv, page_size, D] bf16, modified in place
+ *   slot_mapping    [B, L_new] int32. slot < 0: no token (padding), skipped.
+ *                   slot >= P * page_size: skipped, PA_DEVERR_SLOT recorded.
+ *                   Two tokens with the same slot: undefined which one lands.
+ *   shape.q_len = L_new; shape.num_q_heads and shape.max_pages are unused.
+ * The copy is bit-exact.
+ */
+pa_status pa_append_kv(const void *key, const void *value, void *key_pages,
+                       void *value_pages, const int32_t *slot_mapping,
+                       int32_t page_size, pa_shape shape, void *stream);
+
+/*
+ * Bytes of scratch workspace pa_decode needs for `shape` on the CURRENT
+ * device (it depends on the device's SM count). 0 on invalid shapes.
+ * Layout: the first 256 KiB hold one int32 ticket per segment (request x KV
+ * head x tile of 16 query rows; at most 65536 segments), the rest holds
+ * per-block partial (max, sum, output) states. The ticket region is the same
+ * for every shape.
+ */
+size_t pa_decode_workspace_bytes(pa_shape shape);
+
+/*
+ * Decode attention: split-KV over the cached context (Week 3 Day 4,
+ * "Choose a Schedule for Each Query Shape" and "Task 2": partition the
+ * context across parallel workers and merge their partial (max, sum,
+ * output) states; Reading vLLM's PagedAttention Kernel, 3.3: partitions
+ * computed in parallel and combined afterwards). Any L >= 1 is computed
+ * correctly; the schedule is built for small L (one-token decode).
+ *
+ *   scale            > 0 and finite (the Python binding maps None to 1/sqrt(D))
+ *   max_context_len  an upper bound of context_lens used only to size the
+ *                    grid (0 = unknown); larger entries are still correct.
+ *   workspace        device scratch of at least pa_decode_workspace_bytes
+ *                    bytes, 256-byte aligned, whose first 256 KiB are
+ *                    ZERO-FILLED before its first use. A call that completes
+ *                    leaves those ticket words at zero again, so one zero
+ *                    fill serves every later call of any shape that fits.
+ *                    Calls that share a workspace must not overlap on the
+ *                    GPU. After a device error the ticket region must be
+ *                    zero-filled again.
+ */
+pa_status pa_decode(const void *query, const void *key_pages,
+                    const void *value_pages, const int32_t *block_table,
+                    const int32_t *context_lens, int32_t page_size, float scale,
+                    int causal, void *out, pa_shape shape,
+                    int32_t max_context_len, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/*
+ * Prefill attention: query rows in tiles, every K/V tile resolved through
+ * block_table (Week 3 Day 4, "Task 2", the long-query page-walking
+ * schedule), causal by default with the bottom-right offset above. Needs no
+ * workspace.
+ */
+pa_status pa_prefill(const void *query, const void *key_pages,
+                     const void *value_pages, const int32_t *block_table,
+                     const int32_t *context_lens, int32_t page_size, float scale,
+                     int causal, void *out, pa_shape shape, void *stream);
+
+/*
+ * Route chosen by pa_attention for these sizes: 0 = decode, 1 = prefill.
+ * The rule sits at this boundary (Week 3 Day 4, "Choose a Schedule for Each
+ * Query Shape": short queries take the vector decode schedule, long ones the
+ * page-walking prefill; no dense fallback). Returns -1 on invalid shapes.
+ */
+int32_t pa_attention_route(pa_shape shape, int32_t max_context_len);
+
+/*
+ * Dispatching entry point: runs pa_decode or pa_prefill as
+ * pa_attention_route says, with the same arguments. The workspace is
+ * required only when the route is decode (pass NULL/0 otherwise).
+ */
+pa_status pa_attention(const void *query, const void *key_pages,
+                       const void *value_pages, const int32_t *block_table,
+                       const int32_t *context_lens, int32_t page_size,
+                       float scale, int causal, void *out, pa_shape shape,
+                       int32_t max_context_len, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device. *flags (may be NULL) receives the PA_DEVERR_* bits seen
+ * since the last call. Returns PA_OK when no bit was set,
+ * PA_ERR_DEVICE_TIMEOUT when the timeout bit was set, PA_ERR_DEVICE_BOUNDS
+ * for any other bit, PA_ERR_CUDA if synchronising failed.
+ */
+pa_status pa_get_device_error(void *stream, uint32_t *flags);
+
+/* Static, human-readable name of a status code. */
+const char *pa_status_string(pa_status status);
+
+/* Library version, e.g. "0.1.0". */
+const char *pa_version(void);
+
+/*
+ * Test support for failure detection. The next pa_decode, pa_prefill or
+ * pa_attention call made by the calling host thread runs one extra wait, in
+ * its first block, on a barrier that nothing ever arrives at. That wait runs
+ * out after its bounded limit (about one second), records PA_DEVERR_TIMEOUT
+ * in the device error word, and the kernel then finishes normally with the
+ * correct result. Nothing faults or hangs; the CUDA context stays usable.
+ */
+void pa_debug_arm_wait_timeout(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

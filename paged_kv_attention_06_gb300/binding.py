@@ -1,0 +1,257 @@
+"""ctypes binding of libpagedattn.so, with the C entry points' names.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI. Torch tensors supply device pointers and the
+current CUDA stream; torch is used for nothing else. There is no CPU or
+PyTorch fallback: if the compiled library is missing, importing this module
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_WORKSPACE = 3
+PA_ERR_CUDA = 4
+PA_ERR_DEVICE_BOUNDS = 5
+PA_ERR_DEVICE_TIMEOUT = 6
+
+PA_DEVERR_PAGE_ID = 0x1
+PA_DEVERR_SLOT = 0x2
+PA_DEVERR_CONTEXT_LEN = 0x4
+PA_DEVERR_TIMEOUT = 0x8
+
+LIB_PATH = _build.LIB
+
+
+class pa_shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("q_len", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("max_pages", ctypes.c_int32)]
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    lib.pa_append_kv.argtypes = [vp, vp, vp, vp, vp, i32, pa_shape, vp]
+    lib.pa_append_kv.restype = ctypes.c_int
+    lib.pa_decode_workspace_bytes.argtypes = [pa_shape]
+    lib.pa_decode_workspace_bytes.restype = sz
+    attn = [vp, vp, vp, vp, vp, i32, f32, ctypes.c_int, vp, pa_shape]
+    lib.pa_decode.argtypes = attn + [i32, vp, sz, vp]
+    lib.pa_decode.restype = ctypes.c_int
+    lib.pa_prefill.argtypes = attn + [vp]
+    lib.pa_prefill.restype = ctypes.c_int
+    lib.pa_attention.argtypes = attn + [i32, vp, sz, vp]
+    lib.pa_attention.restype = ctypes.c_int
+    lib.pa_attention_route.argtypes = [pa_shape, i32]
+    lib.pa_attention_route.restype = i32
+    lib.pa_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.pa_get_device_error.restype = ctypes.c_int
+    lib.pa_status_string.argtypes = [ctypes.c_int]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_version.argtypes = []
+    lib.pa_version.restype = ctypes.c_char_p
+    lib.pa_debug_arm_wait_timeout.argtypes = []
+    lib.pa_debug_arm_wait_timeout.restype = None
+    return lib
+
+
+_lib = _load()
+
+
+def status_string(status: int) -> str:
+    return _lib.pa_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return _lib.pa_version().decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PagedAttentionError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev_ptr(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def make_shape(query_shape, pages_shape, max_pages: int) -> pa_shape:
+    B, H_q, L, D = (int(x) for x in query_shape)
+    P, H_kv, _, D2 = (int(x) for x in pages_shape)
+    if D2 != D:
+        raise ValueError("query and pages disagree on head_dim")
+    return pa_shape(B, H_q, H_kv, D, L, P, int(max_pages))
+
+
+# ---------------------------------------------------------------------------
+# Workspace cache: one zero-filled buffer per device, grown on demand. The
+# library leaves the counter words at zero after every completed call.
+
+_ws_lock = threading.Lock()
+_ws_cache = {}
+
+
+def decode_workspace(shape: pa_shape, device: torch.device) -> Tuple[torch.Tensor, int]:
+    need = pa_decode_workspace_bytes(shape, device)
+    with _ws_lock:
+        buf = _ws_cache.get(device.index)
+        if buf is None or buf.numel() < need:
+            buf = torch.zeros(max(need, 256), dtype=torch.uint8, device=device)
+            _ws_cache[device.index] = buf
+    return buf, need
+
+
+def pa_decode_workspace_bytes(shape: pa_shape, device: Optional[torch.device] = None) -> int:
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(_lib.pa_decode_workspace_bytes(shape))
+
+
+# ---------------------------------------------------------------------------
+# Entry points
+
+
+def pa_append_kv(key: torch.Tensor, value: torch.Tensor, key_pages: torch.Tensor,
+                 value_pages: torch.Tensor, slot_mapping: torch.Tensor, page_size: int,
+                 stream=None) -> None:
+    """key/value [B, H_kv, L_new, D] bf16 -> pages [P, H_kv, page_size, D] at
+    slot_mapping [B, L_new] int32 (in place)."""
+    B, H_kv, L_new, D = key.shape
+    if tuple(value.shape) != tuple(key.shape):
+        raise ValueError("key and value shapes differ")
+    if tuple(slot_mapping.shape) != (B, L_new):
+        raise ValueError("slot_mapping must be [B, L_new]")
+    if key_pages.shape[1:] != (H_kv, page_size, D) or value_pages.shape != key_pages.shape:
+        raise ValueError("page pool shape does not match key / page_size")
+    shape = pa_shape(B, 0, H_kv, D, L_new, key_pages.shape[0], 0)
+    st = _lib.pa_append_kv(_dev_ptr(key, torch.bfloat16, "key"),
+                           _dev_ptr(value, torch.bfloat16, "value"),
+                           _dev_ptr(key_pages, torch.bfloat16, "key_pages"),
+                           _dev_ptr(value_pages, torch.bfloat16, "value_pages"),
+                           _dev_ptr(slot_mapping, torch.int32, "slot_mapping"),
+                           int(page_size), shape, _stream(stream))
+    _check(st, "pa_append_kv")
+
+
+def _attn_common(query, key_pages, value_pages, block_table, context_lens, page_size,
+                 scale, out):
+    B, H_q, L, D = query.shape
+    if key_pages.shape[2] != page_size or value_pages.shape != key_pages.shape:
+        raise ValueError("page pool shape does not match page_size")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_table must be [B, max_pages] and context_lens [B]")
+    if out is None:
+        out = torch.empty_like(query)
+    elif tuple(out.shape) != tuple(query.shape):
+        raise ValueError("out must have the query's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    shape = make_shape(query.shape, key_pages.shape, block_table.shape[1])
+    ptrs = (_dev_ptr(query, torch.bfloat16, "query"),
+            _dev_ptr(key_pages, torch.bfloat16, "key_pages"),
+            _dev_ptr(value_pages, torch.bfloat16, "value_pages"),
+            _dev_ptr(block_table, torch.int32, "block_table"),
+            _dev_ptr(context_lens, torch.int32, "context_lens"))
+    return shape, ptrs, float(scale), out
+
+
+def pa_decode(query, key_pages, value_pages, block_table, context_lens, page_size: int,
+              scale: Optional[float] = None, causal: bool = True, out=None,
+              max_context_len: int = 0, workspace: Optional[torch.Tensor] = None,
+              stream=None) -> torch.Tensor:
+    """Split-KV paged attention; returns out [B, H_q, L, D] bf16."""
+    shape, ptrs, scale, out = _attn_common(query, key_pages, value_pages, block_table,
+                                           context_lens, page_size, scale, out)
+    if workspace is None:
+        workspace, _ = decode_workspace(shape, query.device)
+    st = _lib.pa_decode(*ptrs, int(page_size), scale, int(bool(causal)),
+                        _dev_ptr(out, torch.bfloat16, "out"), shape, int(max_context_len),
+                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                        _stream(stream))
+    _check(st, "pa_decode")
+    return out
+
+
+def pa_prefill(query, key_pages, value_pages, block_table, context_lens, page_size: int,
+               scale: Optional[float] = None, causal: bool = True, out=None,
+               stream=None) -> torch.Tensor:
+    """Page-walking prefill attention; returns out [B, H_q, L, D] bf16."""
+    shape, ptrs, scale, out = _attn_common(query, key_pages, value_pages, block_table,
+                                           context_lens, page_size, scale, out)
+    st = _lib.pa_prefill(*ptrs, int(page_size), scale, int(bool(causal)),
+                         _dev_ptr(out, torch.bfloat16, "out"), shape, _stream(stream))
+    _check(st, "pa_prefill")
+    return out
+
+
+def pa_attention_route(query_shape, pages_shape, max_pages: int, max_context_len: int = 0) -> int:
+    return int(_lib.pa_attention_route(make_shape(query_shape, pages_shape, max_pages),
+                                       int(max_context_len)))
+
+
+def pa_attention(query, key_pages, value_pages, block_table, context_lens, page_size: int,
+                 scale: Optional[float] = None, causal: bool = True, out=None,
+                 max_context_len: int = 0, workspace: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """Dispatching entry point (decode for short queries, prefill otherwise)."""
+    shape, ptrs, scale, out = _attn_common(query, key_pages, value_pages, block_table,
+                                           context_lens, page_size, scale, out)
+    route = int(_lib.pa_attention_route(shape, int(max_context_len)))
+    ws_ptr, ws_bytes = None, 0
+    if route == 0:
+        if workspace is None:
+            workspace, _ = decode_workspace(shape, query.device)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = _lib.pa_attention(*ptrs, int(page_size), scale, int(bool(causal)),
+                           _dev_ptr(out, torch.bfloat16, "out"), shape, int(max_context_len),
+                           ws_ptr, ws_bytes, _stream(stream))
+    _check(st, "pa_attention")
+    return out
+
+
+def pa_debug_arm_wait_timeout() -> None:
+    """Test support: the next attention call on this thread runs one bounded
+    wait on a barrier nothing arrives at (records PA_DEVERR_TIMEOUT)."""
+    _lib.pa_debug_arm_wait_timeout()
+
+
+def pa_get_device_error(stream=None) -> Tuple[int, int]:
+    """Synchronises the stream; returns (status, PA_DEVERR_* flags) and clears them."""
+    flags = ctypes.c_uint32(0)
+    st = _lib.pa_get_device_error(_stream(stream), ctypes.byref(flags))
+    return int(st), int(flags.value)

@@ -1,0 +1,374 @@
+// C ABI of the paged-attention library: argument checks, tensor-map set-up,
+// the dispatch rule, and the device error word. No entry point allocates
+// device memory; every launch goes on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/pagedattn.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+// Device error word: kernels OR PA_DEVERR_* bits into it; pa_get_device_error
+// reads and clears it. One copy per device that loads the library.
+__device__ unsigned int g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int id = 0;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    unsigned* err = nullptr;  // device address of g_device_error
+};
+
+std::mutex g_mutex;
+thread_local bool t_arm_unset_wait = false;  // test support, see pa_debug_arm_wait_timeout
+DeviceInfo g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+pa_status device_info(DeviceInfo** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.ready) {
+        int sms = 0, smem = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return PA_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess)
+            return PA_ERR_CUDA;
+        d.id = dev;
+        d.sm_count = sms;
+        d.max_smem_optin = smem;
+        d.err = static_cast<unsigned*>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return PA_OK;
+}
+
+pa_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p)
+            return PA_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    *fn = g_encode;
+    return PA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+// Checks shared by the attention entry points.
+pa_status check_attention(const void* query, const void* key_pages, const void* value_pages,
+                          const int32_t* block_table, const int32_t* context_lens,
+                          int32_t page_size, float scale, const void* out, const pa_shape& s)
+{
+    if (!query || !key_pages || !value_pages || !block_table || !context_lens || !out)
+        return PA_ERR_INVALID_ARG;
+    if (s.batch <= 0 || s.num_q_heads <= 0 || s.num_kv_heads <= 0 || s.q_len <= 0 ||
+        s.num_pages <= 0 || s.max_pages <= 0 || s.head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(query) || !aligned16(key_pages) || !aligned16(value_pages) || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+    if (s.head_dim != 64 && s.head_dim != 128)
+        return PA_ERR_UNSUPPORTED;
+    if (s.num_q_heads % s.num_kv_heads != 0)
+        return PA_ERR_UNSUPPORTED;
+    if (!pow2_in(page_size, 1, 256))
+        return PA_ERR_UNSUPPORTED;
+    // TMA row coordinates and in-kernel page arithmetic are 32-bit.
+    if (int64_t(s.num_pages) * s.num_kv_heads * page_size >= (int64_t(1) << 31))
+        return PA_ERR_UNSUPPORTED;
+    if (int64_t(s.max_pages) * page_size >= (int64_t(1) << 30))
+        return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+// 2-D view of a page pool: rows = P * H_kv * page_size, columns = D.
+pa_status encode_pool_map(CUtensorMap* map, const void* pool, const pa_shape& s, int32_t ps)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    pa_status st = get_encoder(&enc);
+    if (st != PA_OK)
+        return st;
+    const cuuint64_t dims[2] = {cuuint64_t(s.head_dim),
+                                cuuint64_t(s.num_pages) * s.num_kv_heads * ps};
+    const cuuint64_t strides[1] = {cuuint64_t(s.head_dim) * 2};
+    const int box_rows = ps < kDecodeTokens ? ps : kDecodeTokens;
+    const cuuint32_t box[2] = {64u, cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    // Boxes of 8+ rows land on 1024-byte boundaries and use the 128-byte
+    // swizzle; smaller pages use a linear layout (their destinations are only
+    // 128-byte aligned).
+    const CUtensorMapSwizzle swz =
+        box_rows >= 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+int64_t decode_segments(const pa_shape& s)
+{
+    const int64_t G = s.num_q_heads / s.num_kv_heads;
+    const int64_t MT = (G * s.q_len + kDecodeRows - 1) / kDecodeRows;
+    return int64_t(s.batch) * s.num_kv_heads * MT;
+}
+
+// Runs the split-KV kernel. whole_segments = 1 gives every block whole
+// segments (no partial states, no workspace).
+pa_status run_split_kv(const void* query, const void* key_pages, const void* value_pages,
+                       const int32_t* block_table, const int32_t* context_lens,
+                       int32_t page_size, float scale, int causal, void* out,
+                       const pa_shape& s, int32_t max_context_len, void* workspace,
+                       size_t workspace_bytes, int whole_segments, cudaStream_t stream)
+{
+    DeviceInfo* dev;
+    pa_status st = device_info(&dev);
+    if (st != PA_OK)
+        return st;
+    const int G = s.num_q_heads / s.num_kv_heads;
+    const int64_t R = int64_t(G) * s.q_len;
+    const int64_t nseg = decode_segments(s);
+    if (R >= (int64_t(1) << 30) || nseg > kMaxSegments)
+        return PA_ERR_UNSUPPORTED;
+    const size_t smem = decode_smem_bytes(s.head_dim, s.batch);
+    if (smem > size_t(dev->max_smem_optin))
+        return PA_ERR_UNSUPPORTED;  // batch too large for the per-block prefix table
+
+    const int grid_max = decode_max_grid(dev->sm_count);
+    int64_t grid = grid_max;
+    if (whole_segments) {
+        grid = nseg < grid_max ? nseg : grid_max;
+    } else if (max_context_len > 0) {
+        const int64_t gran = (int64_t(max_context_len) + kDecodeTokens - 1) / kDecodeTokens;
+        const int64_t bound = nseg * (gran > 0 ? gran : 1);
+        if (bound < grid)
+            grid = bound;
+    }
+    if (grid < 1)
+        grid = 1;
+
+    DecodeArgs a;
+    memset(&a, 0, sizeof a);
+    if (!whole_segments) {
+        const size_t need = decode_workspace_bytes(nseg, grid_max, s.head_dim);
+        if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return PA_ERR_WORKSPACE;
+        a.counters = static_cast<int32_t*>(workspace);
+        a.partials =
+            reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kCounterRegionBytes);
+    }
+    CUtensorMap kmap, vmap;
+    if ((st = encode_pool_map(&kmap, key_pages, s, page_size)) != PA_OK)
+        return st;
+    if ((st = encode_pool_map(&vmap, value_pages, s, page_size)) != PA_OK)
+        return st;
+
+    a.q = static_cast<const uint16_t*>(query);
+    a.out = static_cast<uint16_t*>(out);
+    a.block_table = block_table;
+    a.context_lens = context_lens;
+    a.err = dev->err;
+    a.B = s.batch;
+    a.H_q = s.num_q_heads;
+    a.H_kv = s.num_kv_heads;
+    a.L = s.q_len;
+    a.D = s.head_dim;
+    a.ps = page_size;
+    a.max_pages = s.max_pages;
+    a.num_pages = s.num_pages;
+    a.G = G;
+    a.R = int32_t(R);
+    a.MT = int32_t((R + kDecodeRows - 1) / kDecodeRows);
+    a.box_rows = page_size < kDecodeTokens ? page_size : kDecodeTokens;
+    a.swz = a.box_rows >= 8 ? 7 : 0;
+    a.whole_segments = whole_segments;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.causal = causal ? 1 : 0;
+    a.debug_unset_wait = t_arm_unset_wait ? 1 : 0;
+    t_arm_unset_wait = false;
+    return launch_decode(kmap, vmap, a, int(grid), dev->id, stream) == cudaSuccess ? PA_OK
+                                                                                   : PA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+pa_status pa_append_kv(const void* key, const void* value, void* key_pages, void* value_pages,
+                       const int32_t* slot_mapping, int32_t page_size, pa_shape shape,
+                       void* stream)
+{
+    if (!key || !value || !key_pages || !value_pages || !slot_mapping)
+        return PA_ERR_INVALID_ARG;
+    if (shape.batch <= 0 || shape.num_kv_heads <= 0 || shape.q_len < 0 || shape.num_pages <= 0 ||
+        shape.head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_pages) || !aligned16(value_pages))
+        return PA_ERR_INVALID_ARG;
+    if (shape.head_dim != 64 && shape.head_dim != 128)
+        return PA_ERR_UNSUPPORTED;
+    if (!pow2_in(page_size, 1, 256))
+        return PA_ERR_UNSUPPORTED;
+    if (2 * int64_t(shape.batch) * shape.q_len * shape.num_kv_heads * (shape.head_dim / 8) >=
+        (int64_t(1) << 40))
+        return PA_ERR_UNSUPPORTED;
+    DeviceInfo* dev;
+    pa_status st = device_info(&dev);
+    if (st != PA_OK)
+        return st;
+    if (shape.q_len == 0)
+        return PA_OK;
+    AppendArgs a;
+    a.key = static_cast<const uint16_t*>(key);
+    a.value = static_cast<const uint16_t*>(value);
+    a.key_pages = static_cast<uint16_t*>(key_pages);
+    a.value_pages = static_cast<uint16_t*>(value_pages);
+    a.slot_mapping = slot_mapping;
+    a.err = dev->err;
+    a.B = shape.batch;
+    a.L_new = shape.q_len;
+    a.H_kv = shape.num_kv_heads;
+    a.D = shape.head_dim;
+    a.ps = page_size;
+    a.num_pages = shape.num_pages;
+    return launch_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                               : PA_ERR_CUDA;
+}
+
+size_t pa_decode_workspace_bytes(pa_shape shape)
+{
+    if (shape.batch <= 0 || shape.num_q_heads <= 0 || shape.num_kv_heads <= 0 ||
+        shape.q_len <= 0 || shape.num_q_heads % shape.num_kv_heads != 0 ||
+        (shape.head_dim != 64 && shape.head_dim != 128) ||
+        decode_segments(shape) > kMaxSegments)
+        return 0;
+    DeviceInfo* dev;
+    if (device_info(&dev) != PA_OK)
+        return 0;
+    return decode_workspace_bytes(decode_segments(shape), decode_max_grid(dev->sm_count),
+                                  shape.head_dim);
+}
+
+pa_status pa_decode(const void* query, const void* key_pages, const void* value_pages,
+                    const int32_t* block_table, const int32_t* context_lens, int32_t page_size,
+                    float scale, int causal, void* out, pa_shape shape, int32_t max_context_len,
+                    void* workspace, size_t workspace_bytes, void* stream)
+{
+    pa_status st = check_attention(query, key_pages, value_pages, block_table, context_lens,
+                                   page_size, scale, out, shape);
+    if (st != PA_OK)
+        return st;
+    return run_split_kv(query, key_pages, value_pages, block_table, context_lens, page_size,
+                        scale, causal, out, shape, max_context_len, workspace, workspace_bytes,
+                        0, static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_prefill(const void* query, const void* key_pages, const void* value_pages,
+                     const int32_t* block_table, const int32_t* context_lens, int32_t page_size,
+                     float scale, int causal, void* out, pa_shape shape, void* stream)
+{
+    pa_status st = check_attention(query, key_pages, value_pages, block_table, context_lens,
+                                   page_size, scale, out, shape);
+    if (st != PA_OK)
+        return st;
+    return run_split_kv(query, key_pages, value_pages, block_table, context_lens, page_size,
+                        scale, causal, out, shape, 0, nullptr, 0, 1,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int32_t pa_attention_route(pa_shape shape, int32_t max_context_len)
+{
+    (void)max_context_len;
+    if (shape.q_len <= 0)
+        return -1;
+    return shape.q_len <= 8 ? 0 : 1;
+}
+
+pa_status pa_attention(const void* query, const void* key_pages, const void* value_pages,
+                       const int32_t* block_table, const int32_t* context_lens, int32_t page_size,
+                       float scale, int causal, void* out, pa_shape shape,
+                       int32_t max_context_len, void* workspace, size_t workspace_bytes,
+                       void* stream)
+{
+    const int32_t route = pa_attention_route(shape, max_context_len);
+    if (route < 0)
+        return PA_ERR_INVALID_ARG;
+    if (route == 0)
+        return pa_decode(query, key_pages, value_pages, block_table, context_lens, page_size,
+                         scale, causal, out, shape, max_context_len, workspace, workspace_bytes,
+                         stream);
+    return pa_prefill(query, key_pages, value_pages, block_table, context_lens, page_size, scale,
+                      causal, out, shape, stream);
+}
+
+pa_status pa_get_device_error(void* stream, uint32_t* flags)
+{
+    DeviceInfo* dev;
+    pa_status st = device_info(&dev);
+    if (st != PA_OK)
+        return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    unsigned v = 0;
+    const unsigned zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (flags)
+        *flags = v;
+    if (v & PA_DEVERR_TIMEOUT)
+        return PA_ERR_DEVICE_TIMEOUT;
+    return v ? PA_ERR_DEVICE_BOUNDS : PA_OK;
+}
+
+const char* pa_status_string(pa_status status)
+{
+    switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG: invalid argument";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: unsupported shape or page size";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing, too small or misaligned";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA call or launch failed";
+    case PA_ERR_DEVICE_BOUNDS: return "PA_ERR_DEVICE_BOUNDS: kernel met an out-of-range index";
+    case PA_ERR_DEVICE_TIMEOUT: return "PA_ERR_DEVICE_TIMEOUT: kernel wait gave up";
+    }
+    return "unknown pa_status";
+}
+
+const char* pa_version(void) { return "0.1.0"; }
+
+void pa_debug_arm_wait_timeout(void) { t_arm_unset_wait = true; }
+
+}  // extern "C"

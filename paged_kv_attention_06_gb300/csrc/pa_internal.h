@@ -1,0 +1,82 @@
+// Internal declarations shared by the library's translation units (host
+// launchers and kernel argument blocks). Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Device error bits (same values as the PA_DEVERR_* macros of the header).
+constexpr unsigned PA_DEVERR_PAGE_ID_BIT = 0x1u;
+constexpr unsigned PA_DEVERR_SLOT_BIT = 0x2u;
+constexpr unsigned PA_DEVERR_CONTEXT_LEN_BIT = 0x4u;
+constexpr unsigned PA_DEVERR_TIMEOUT_BIT = 0x8u;
+
+// Longest a kernel waits for one pipeline phase before giving up, and the
+// limit of every later wait of a block that already gave up once.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr uint64_t kShortWaitLimitNs = 20000000ull;
+
+// ---------------------------------------------------------------------------
+// Write path
+
+struct AppendArgs {
+    const uint16_t* key;          // [B, H_kv, L_new, D]
+    const uint16_t* value;
+    uint16_t* key_pages;          // [P, H_kv, ps, D]
+    uint16_t* value_pages;
+    const int32_t* slot_mapping;  // [B, L_new]
+    unsigned* err;
+    int32_t B, L_new, H_kv, D, ps, num_pages;
+};
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Split-KV attention (decode schedule)
+
+// Work decomposition: a "segment" is (request b, KV head h, tile mt of 16
+// query rows); its keys are cut into granules of kDecodeTokens tokens. All
+// granules of all segments form one stream that the grid splits evenly; a
+// segment that straddles blocks is merged by the last block to finish it.
+constexpr int kDecodeTokens = 64;
+constexpr int kDecodeRows = 16;
+
+// Workspace layout: a fixed 256 KiB counter region (one int32 ticket per
+// segment, at most kMaxSegments) followed by the partial-state slots. The
+// counter region does not depend on the shape, so partial states of one call
+// never land on counter words of another call that shares the workspace.
+constexpr int64_t kMaxSegments = 65536;
+constexpr size_t kCounterRegionBytes = size_t(kMaxSegments) * 4;
+
+struct DecodeArgs {
+    const uint16_t* q;            // [B, H_q, L, D]
+    uint16_t* out;                // [B, H_q, L, D]
+    const int32_t* block_table;   // [B, max_pages]
+    const int32_t* context_lens;  // [B]
+    float* partials;              // [slots][m[16], l[16], acc[16][D]]
+    int32_t* counters;            // [nseg]
+    unsigned* err;
+    int32_t B, H_q, H_kv, L, D, ps, max_pages, num_pages;
+    int32_t G;          // H_q / H_kv
+    int32_t R;          // G * L query rows per (request, KV head)
+    int32_t MT;         // ceil(R / 16) row tiles
+    int32_t box_rows;   // rows per TMA box: min(ps, 64)
+    int32_t swz;        // 7: 128B-swizzled stage layout (box_rows >= 8); 0: linear
+    int32_t whole_segments;  // 1: every block takes whole segments (no partials)
+    float scale_log2;   // scale * log2(e)
+    int32_t causal;
+    int32_t debug_unset_wait;  // test support: block 0 first waits on a barrier
+                               // that nothing arrives at (times out, flags)
+};
+
+size_t decode_smem_bytes(int D, int B);
+int decode_max_grid(int sm_count);
+size_t decode_workspace_bytes(int64_t nseg, int grid_max, int D);
+cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_map,
+                          const DecodeArgs& a, int grid, int device, cudaStream_t stream);
+
+}  // namespace pa

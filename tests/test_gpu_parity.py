@@ -1,0 +1,247 @@
+"""GPU path vs the fp64 oracle, element by element, through the C ABI.
+
+Append and indexing must be bit-exact; attention outputs must satisfy
+max |err| <= 2e-2 and mean |err| <= 2e-3 against the oracle on the same
+seeded inputs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from gpu_util import (DeviceBatch, assert_close, check_no_device_error, gpu_step, host_bits,
+                      host_f64, oracle_out, oracle_pages)
+
+pytestmark = pytest.mark.gpu
+
+
+# ----------------------------------------------------------------------------
+# Named workloads, end to end (append, then the dispatching entry point)
+
+
+def test_tiny_decode_full():
+    b = wl.make_workload("tiny_decode")
+    db = DeviceBatch(b)
+    out = gpu_step(db)
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert np.array_equal(host_bits(db.key_pages), kp)
+    assert np.array_equal(host_bits(db.value_pages), vp)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), "tiny_decode")
+
+
+@pytest.mark.parametrize("name", ["decode_b32_gqa7_ps16", "decode_b64_ps128", "decode_long_b8"])
+def test_decode_workloads_every_row(name):
+    b = wl.make_workload(name)
+    db = DeviceBatch(b)
+    out = gpu_step(db)
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    # the append touches B rows per KV head: compare the whole pools bit for bit
+    assert np.array_equal(host_bits(db.key_pages), kp)
+    assert np.array_equal(host_bits(db.value_pages), vp)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), name)
+
+
+def test_prefill_chunk_sampled_rows():
+    b = wl.make_workload("prefill_chunk512")
+    db = DeviceBatch(b)
+    out = gpu_step(db)
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert np.array_equal(host_bits(db.key_pages), kp)
+    assert np.array_equal(host_bits(db.value_pages), vp)
+    rng = np.random.default_rng(0)
+    rows = []
+    for r in range(b.B):
+        for i in sorted(set([0, 1, 63, 64, 127, 128, 255, 256, 383, 510, 511] +
+                            list(rng.integers(0, b.L, 6)))):
+            for h in range(b.H_q):
+                rows.append((r, h, i))
+    rows = np.asarray(rows, dtype=np.int32)
+    ref = oracle_out(b, kp, vp, rows=rows)
+    got = host_f64(out)[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(got, ref, "prefill_chunk512 sampled")
+    assert torch.isfinite(out.float()).all()
+
+
+# ----------------------------------------------------------------------------
+# Sweeps over page sizes, GQA ratios, head dims, query lengths and ragged
+# context lengths at page boundaries
+
+
+def _boundary_lens(ps, L, B, seed, max_len=700):
+    rng = np.random.default_rng(seed)
+    cands = [L, ps - 1, ps, ps + 1, 2 * ps, 2 * ps + 1, 63, 64, 65, 127, 129, 300]
+    lens = [max(L, int(c)) for c in cands if c >= 1]
+    while len(lens) < B:
+        lens.append(int(rng.integers(L, max_len)))
+    return [min(x, max_len) for x in lens[:B]]
+
+
+SWEEP = [
+    # (page_size, H_q, H_kv, D, L)
+    (1, 8, 8, 64, 1), (2, 8, 4, 128, 1), (4, 4, 2, 64, 1), (16, 28, 4, 128, 1),
+    (16, 32, 8, 128, 2), (64, 16, 4, 64, 1), (128, 32, 8, 128, 1), (256, 14, 2, 128, 1),
+    (16, 16, 1, 128, 1), (16, 32, 1, 64, 1), (8, 12, 4, 128, 8), (32, 28, 4, 128, 5),
+    (4, 8, 1, 128, 3), (128, 7, 7, 64, 2),
+]
+
+
+@pytest.mark.parametrize("ps,H_q,H_kv,D,L", SWEEP)
+@pytest.mark.parametrize("route", ["decode", "prefill"])
+def test_sweep_against_oracle(ps, H_q, H_kv, D, L, route):
+    B = 12
+    lens = _boundary_lens(ps, L, B, seed=ps * 131 + H_q * 7 + D + L)
+    b = wl.build_batch("sweep", B=B, H_q=H_q, H_kv=H_kv, D=D, page_size=ps, L=L,
+                       context_lens=lens, seed=ps + 17 * L + D, L_new=min(L, 1))
+    db = DeviceBatch(b)
+    out = gpu_step(db, route=route)
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), f"{route} ps={ps} G={H_q // H_kv} L={L}")
+
+
+@pytest.mark.parametrize("L,causal", [(9, True), (16, True), (33, False), (64, True), (130, True)])
+@pytest.mark.parametrize("ps", [16, 128])
+def test_prefill_lengths(L, causal, ps):
+    B = 5
+    rng = np.random.default_rng(L + ps)
+    lens = [L, L + 1, L + ps, L + 200, L + int(rng.integers(0, 600))]
+    b = wl.build_batch("prefill", B=B, H_q=8, H_kv=2, D=128, page_size=ps, L=L,
+                       context_lens=lens, seed=3 * L + ps, causal=causal, placement="churn")
+    db = DeviceBatch(b)
+    out = gpu_step(db)            # pa_attention routes L > 8 to prefill
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), f"prefill L={L} ps={ps}")
+
+
+# ----------------------------------------------------------------------------
+# Invariants of Week 3 Day 4, "What Must Hold"
+
+
+def _relabelled(b: wl.PagedBatch, seed: int) -> wl.PagedBatch:
+    perm = np.random.default_rng(seed).permutation(b.num_pages).astype(np.int32)
+    kp, vp = np.empty_like(b.key_pages), np.empty_like(b.value_pages)
+    kp[perm] = b.key_pages
+    vp[perm] = b.value_pages
+    bt = b.block_table.copy()
+    m = bt >= 0
+    bt[m] = perm[bt[m]]
+    sm = b.slot_mapping.copy()
+    ok = sm >= 0
+    sm[ok] = perm[sm[ok] // b.page_size] * b.page_size + sm[ok] % b.page_size
+    import dataclasses
+    return dataclasses.replace(b, key_pages=kp, value_pages=vp, block_table=bt, slot_mapping=sm)
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "decode_b32_gqa7_ps16"])
+def test_physical_relabelling_bit_identical(name):
+    b = wl.make_workload(name)
+    out1 = host_bits(gpu_step(DeviceBatch(b)))
+    out2 = host_bits(gpu_step(DeviceBatch(_relabelled(b, 5))))
+    check_no_device_error()
+    assert np.array_equal(out1, out2)
+
+
+@pytest.mark.parametrize("pattern", [0x7FC0, 0x7F80, 0xFF80, 0x0000])
+@pytest.mark.parametrize("route", ["decode", "prefill"])
+def test_stale_slots_never_affect_output(pattern, route):
+    b = wl.build_batch("stale", B=6, H_q=16, H_kv=4, D=128, page_size=16, L=3,
+                       context_lens=[3, 17, 31, 64, 100, 250], seed=77, L_new=0)
+    out1 = host_bits(gpu_step(DeviceBatch(b), route=route))
+    used = np.zeros((b.num_pages, b.page_size), dtype=bool)
+    for r in range(b.B):
+        for j in range(int(b.context_lens[r])):
+            used[b.block_table[r, j // b.page_size], j % b.page_size] = True
+    pages, slots = np.nonzero(~used)
+    kp, vp = b.key_pages.copy(), b.value_pages.copy()
+    kp[pages, :, slots, :] = pattern
+    vp[pages, :, slots, :] = pattern
+    import dataclasses
+    b2 = dataclasses.replace(b, key_pages=kp, value_pages=vp)
+    out2 = host_bits(gpu_step(DeviceBatch(b2), route=route))
+    check_no_device_error()
+    assert np.array_equal(out1, out2)
+
+
+def test_padding_entries_never_read():
+    b = wl.make_workload("tiny_decode", pad_value=-1)
+    out1 = host_bits(gpu_step(DeviceBatch(b)))
+    import dataclasses
+    bt = b.block_table.copy()
+    bt[bt < 0] = 2**30                        # far outside the pool
+    out2 = host_bits(gpu_step(DeviceBatch(dataclasses.replace(b, block_table=bt))))
+    check_no_device_error()                   # never dereferenced, so never flagged
+    assert np.array_equal(out1, out2)
+
+
+def test_shared_pages_between_requests():
+    """Two requests point at the same physical prefix pages (explicit
+    sharing, as in prefix caching); reads of aliased pages are legal."""
+    ps, n_shared = 16, 48
+    b = wl.build_batch("alias", B=3, H_q=8, H_kv=2, D=128, page_size=ps, L=1,
+                       context_lens=[100, 70, 48], seed=5, L_new=0)
+    bt = b.block_table.copy()
+    bt[1, :n_shared // ps] = bt[0, :n_shared // ps]
+    bt[2, :n_shared // ps] = bt[0, :n_shared // ps]
+    import dataclasses
+    b2 = dataclasses.replace(b, block_table=bt)
+    out = gpu_step(DeviceBatch(b2))
+    check_no_device_error()
+    assert_close(host_f64(out), oracle_out(b2, b2.key_pages, b2.value_pages), "aliased")
+
+
+def test_empty_contexts_and_rows_without_keys():
+    b = wl.build_batch("empty", B=4, H_q=8, H_kv=4, D=64, page_size=4, L=4,
+                       context_lens=[0, 2, 4, 9], seed=9, L_new=0)
+    for route in ("decode", "prefill"):
+        out = host_f64(gpu_step(DeviceBatch(b), route=route))
+        check_no_device_error()
+        ref = oracle_out(b, b.key_pages, b.value_pages)
+        assert np.all(out[0] == 0)             # n = 0
+        assert np.all(out[1, :, :2] == 0)      # rows at positions -2, -1
+        assert_close(out, ref, route)
+
+
+def test_decode_and_prefill_routes_agree():
+    b = wl.build_batch("routes", B=8, H_q=32, H_kv=8, D=128, page_size=16, L=4,
+                       context_lens=[5, 77, 300, 1000, 2047, 16, 17, 4096], seed=21, L_new=0)
+    db = DeviceBatch(b)
+    dec = host_f64(gpu_step(db, route="decode"))
+    pre = host_f64(gpu_step(db, route="prefill"))
+    ref = oracle_out(b, b.key_pages, b.value_pages)
+    assert_close(dec, ref, "decode")
+    assert_close(pre, ref, "prefill")
+
+
+def test_workspace_reuse_is_deterministic():
+    import paged_kv_attention_06_gb300 as pa
+    b = wl.make_workload("decode_b32_gqa7_ps16")
+    db = DeviceBatch(b)
+    outs = [host_bits(gpu_step(db, route="decode", append=False)) for _ in range(3)]
+    check_no_device_error()
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    shape = pa.make_shape(db.query.shape, db.key_pages.shape, db.block_table.shape[1])
+    ws, need = pa.decode_workspace(shape, db.query.device)
+    counters = ws[: 256 * 1024].view(torch.int32)
+    assert int(counters.abs().sum()) == 0      # the whole ticket region is left at zero
+
+
+def test_non_default_stream():
+    b = wl.make_workload("tiny_decode")
+    db = DeviceBatch(b)
+    s = torch.cuda.Stream()
+    import paged_kv_attention_06_gb300 as pa
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        pa.pa_append_kv(db.key_new, db.value_new, db.key_pages, db.value_pages,
+                        db.slot_mapping, b.page_size)
+        out = pa.pa_attention(db.query, db.key_pages, db.value_pages, db.block_table,
+                              db.context_lens, b.page_size, scale=b.scale, max_context_len=10)
+    s.synchronize()
+    kp, vp = oracle_pages(b)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), "stream")

@@ -133,6 +133,33 @@ pa_status pa_decode(const void *query, const void *key_pages,
                     size_t workspace_bytes, void *stream);
 
 /*
+ * pa_decode without a caller-provided workspace. (The pages have no
+ * counterpart: this entry point exists for callers of this library that
+ * cannot allocate device memory, e.g. a host program embedded in another
+ * runtime that owns every device allocation and only hands out the input and
+ * output pointers, or a serving loop where cudaMalloc/cudaFree are off limits
+ * because they can synchronise the device mid-flight.)
+ *
+ * Same arguments, checks and result as pa_decode, minus the workspace: the
+ * scratch is a 32 MiB array inside the library's device image, held by every
+ * GPU that loads this part of the library until the process exits. The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Shapes whose scratch (pa_decode_workspace_bytes) exceeds 32 MiB are
+ *     rejected with PA_ERR_WORKSPACE before anything is launched.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents; each call zero-fills the ticket words it needs (a
+ *     memset on `stream`) before its kernel. Calls that overlap on the GPU
+ *     (other streams, other host threads) race on the array: order them.
+ */
+pa_status pa_decode_noalloc(const void *query, const void *key_pages,
+                            const void *value_pages, const int32_t *block_table,
+                            const int32_t *context_lens, int32_t page_size,
+                            float scale, int causal, void *out, pa_shape shape,
+                            int32_t max_context_len, void *stream);
+
+/*
  * Prefill attention: query rows in tiles, every K/V tile resolved through
  * block_table (Week 3 Day 4, "Task 2", the long-query page-walking
  * schedule), causal by default with the bottom-right offset above. Needs no

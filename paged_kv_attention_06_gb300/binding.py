@@ -255,3 +255,31 @@ def pa_get_device_error(stream=None) -> Tuple[int, int]:
     flags = ctypes.c_uint32(0)
     st = _lib.pa_get_device_error(_stream(stream), ctypes.byref(flags))
     return int(st), int(flags.value)
+
+
+# ---------------------------------------------------------------------------
+# Decode without a caller-provided workspace (for callers that cannot
+# allocate device memory; the scratch is a fixed array inside the library).
+
+_noalloc_ready = False
+
+
+def pa_decode_noalloc(query, key_pages, value_pages, block_table, context_lens,
+                      page_size: int, scale: Optional[float] = None, causal: bool = True,
+                      out=None, max_context_len: int = 0, stream=None) -> torch.Tensor:
+    """pa_decode with the library's built-in 32 MiB scratch instead of a
+    workspace; `out` must be given by callers that allocate nothing."""
+    global _noalloc_ready
+    if not _noalloc_ready:
+        vp, i32 = ctypes.c_void_p, ctypes.c_int32
+        _lib.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, ctypes.c_float,
+                                           ctypes.c_int, vp, pa_shape, i32, vp]
+        _lib.pa_decode_noalloc.restype = ctypes.c_int
+        _noalloc_ready = True
+    shape, ptrs, scale, out = _attn_common(query, key_pages, value_pages, block_table,
+                                           context_lens, page_size, scale, out)
+    st = _lib.pa_decode_noalloc(*ptrs, int(page_size), scale, int(bool(causal)),
+                                _dev_ptr(out, torch.bfloat16, "out"), shape,
+                                int(max_context_len), _stream(stream))
+    _check(st, "pa_decode_noalloc")
+    return out

@@ -219,6 +219,28 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
 }
 
 }  // namespace
+
+pa_status validate_decode(const void* query, const void* key_pages, const void* value_pages,
+                          const int32_t* block_table, const int32_t* context_lens,
+                          int32_t page_size, float scale, const void* out, const pa_shape& s)
+{
+    pa_status st = check_attention(query, key_pages, value_pages, block_table, context_lens,
+                                   page_size, scale, out, s);
+    if (st != PA_OK)
+        return st;
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != PA_OK)
+        return st;
+    const int64_t R = int64_t(s.num_q_heads / s.num_kv_heads) * s.q_len;
+    if (R >= (int64_t(1) << 30) || decode_segments(s) > kMaxSegments)
+        return PA_ERR_UNSUPPORTED;
+    if (decode_smem_bytes(s.head_dim, s.batch) > size_t(dev->max_smem_optin))
+        return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+int64_t decode_segment_count(const pa_shape& s) { return decode_segments(s); }
+
 }  // namespace pa
 
 using namespace pa;

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/pagedattn.h"
+
 namespace pa {
 
 // Device error bits (same values as the PA_DEVERR_* macros of the header).
@@ -78,5 +80,12 @@ int decode_max_grid(int sm_count);
 size_t decode_workspace_bytes(int64_t nseg, int grid_max, int D);
 cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_map,
                           const DecodeArgs& a, int grid, int device, cudaStream_t stream);
+
+// Host-side checks of a decode call (everything pa_decode rejects before
+// launching, except the workspace), and its number of segments.
+pa_status validate_decode(const void* query, const void* key_pages, const void* value_pages,
+                          const int32_t* block_table, const int32_t* context_lens,
+                          int32_t page_size, float scale, const void* out, const pa_shape& s);
+int64_t decode_segment_count(const pa_shape& s);
 
 }  // namespace pa

@@ -250,6 +250,28 @@ def run_reference(args, rank, world):
     return 0
 
 
+def _bench_lib(binding):
+    """ctypes view of the native step loops (bench_loop.cpp)."""
+    import ctypes
+    from paged_kv_attention_06_gb300 import build as pkg_build
+    lib = ctypes.CDLL(pkg_build.BENCH_LIB)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    pvp = ctypes.POINTER(ctypes.c_void_p)
+    lib.pa_bench_steps.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, pvp, pvp,
+                                   vp, i32,
+                                   binding.pa_shape, vp, vp, vp, f32, ctypes.c_int, vp,
+                                   binding.pa_shape, i32, vp, sz, vp,
+                                   ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
+    lib.pa_bench_steps.restype = ctypes.c_int
+    lib.pa_bench_e2e_steps.argtypes = [ctypes.c_int, ctypes.c_int, pvp, pvp,
+                                       ctypes.POINTER(ctypes.c_size_t), ctypes.c_int, vp, vp, sz,
+                                       vp, vp, pvp, pvp, vp, i32, binding.pa_shape, vp, vp, vp,
+                                       f32, ctypes.c_int, vp, binding.pa_shape, i32, vp, sz, vp,
+                                       ctypes.POINTER(ctypes.c_float)]
+    lib.pa_bench_e2e_steps.restype = ctypes.c_int
+    return lib
+
+
 def workload_config(b, world, l2_note):
     n = b.context_lens
     return {"workload": b.name, "B": b.B, "H_q": b.H_q, "H_kv": b.H_kv, "D": b.D,
@@ -317,30 +339,29 @@ def main(argv=None):
     lib = binding._lib
     route = int(lib.pa_attention_route(shape, max_ctx))
 
-    # Pre-marshalled C-ABI calls (the step launches only these two kernels).
-    def make_calls(kp, vp):
-        app = (kn.data_ptr(), vn.data_ptr(), kp.data_ptr(), vp.data_ptr(), sm.data_ptr(),
-               b.page_size, app_shape, sp)
-        att = (q.data_ptr(), kp.data_ptr(), vp.data_ptr(), bt.data_ptr(), cl.data_ptr(),
-               b.page_size, b.scale, int(b.causal), out.data_ptr(), shape, max_ctx,
-               ws.data_ptr(), ws_need, sp)
-        return app, att
+    # The timed steps are issued from C (bench_loop.cpp) through the public
+    # C ABI, so that no interpreter work sits between launches.
+    import ctypes
+    blib = _bench_lib(binding)
+    kps = (ctypes.c_void_p * copies)(*[kp.data_ptr() for kp, _ in pools])
+    vps = (ctypes.c_void_p * copies)(*[vp_.data_ptr() for _, vp_ in pools])
 
-    calls = [make_calls(kp, vp) for kp, vp in pools]
+    sample_every = 4
 
-    def step(k, ev=None):
-        app, att = calls[k % copies]
-        st = lib.pa_append_kv(*app)
-        if ev is not None:
-            ev[0].record(stream)
-        st |= lib.pa_attention(*att)
-        if ev is not None:
-            ev[1].record(stream)
-        return st
+    def run_steps(n):
+        n_samples = -(-n // sample_every)
+        step_ms = (ctypes.c_float * max(1, n_samples))()
+        total = ctypes.c_float(0)
+        st = blib.pa_bench_steps(n, sample_every, copies, kn.data_ptr(), vn.data_ptr(), kps, vps,
+                                 sm.data_ptr(), b.page_size, app_shape, q.data_ptr(),
+                                 bt.data_ptr(), cl.data_ptr(), b.scale, int(b.causal),
+                                 out.data_ptr(), shape, max_ctx, ws.data_ptr(), ws_need, sp,
+                                 step_ms, ctypes.byref(total))
+        if st != 0:
+            raise RuntimeError(f"native step loop failed with status {st}")
+        return float(total.value), [float(x) for x in step_ms[:n_samples]]
 
-    for k in range(args.warmup):
-        if step(k):
-            raise RuntimeError("warm-up step failed")
+    run_steps(args.warmup)
     torch.cuda.synchronize()
     status, flags = pa.pa_get_device_error()
     if status:
@@ -349,29 +370,17 @@ def main(argv=None):
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.time()
     host0 = time.perf_counter()
-    t_start.record(stream)
-    bad = 0
-    for k in range(args.steps):
-        bad |= step(k, evs[k])
-    t_end.record(stream)
+    total_ms, dec_ms = run_steps(args.steps)
     host_s = time.perf_counter() - host0
     torch.cuda.synchronize()
     wall1 = time.time()
     if dist is not None:
         dist.barrier()
-    if bad:
-        raise RuntimeError("a timed step returned an error status")
-    total_ms = t_start.elapsed_time(t_end)
-    dec_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     status, flags = pa.pa_get_device_error()
     if status:
         raise RuntimeError(f"device error in the timed region: {flags:#x}")
@@ -381,33 +390,37 @@ def main(argv=None):
         total_ms = float(t.item())
 
     # ---- e2e: same step through the C ABI from pinned host buffers ---------
-    h_q = torch.from_numpy(b.query.view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_kn = torch.from_numpy(b.key_new.view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_vn = torch.from_numpy(b.value_new.view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_sm = torch.from_numpy(b.slot_mapping).pin_memory()
-    h_bt = torch.from_numpy(b.block_table).pin_memory()
-    h_cl = torch.from_numpy(b.context_lens).pin_memory()
+    def pinned(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+        return torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+
+    host_in = [pinned(b.query), pinned(b.key_new), pinned(b.value_new), pinned(b.slot_mapping),
+               pinned(b.block_table), pinned(b.context_lens)]
+    dev_in = [q, kn, vn, sm, bt, cl]
     h_out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_sm, h_bt, h_cl))
+    nbytes = [t.numel() * t.element_size() for t in host_in]
+    h2d = sum(nbytes)
     d2h = h_out.numel() * h_out.element_size()
     e2e_steps = max(10, min(args.steps, 2000))
-    for k in range(3):
-        step(k)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(e2e_steps):
-        q.copy_(h_q, non_blocking=True)
-        kn.copy_(h_kn, non_blocking=True)
-        vn.copy_(h_vn, non_blocking=True)
-        sm.copy_(h_sm, non_blocking=True)
-        bt.copy_(h_bt, non_blocking=True)
-        cl.copy_(h_cl, non_blocking=True)
-        step(k)
-        h_out.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    src = (ctypes.c_void_p * 6)(*[t.data_ptr() for t in host_in])
+    dst = (ctypes.c_void_p * 6)(*[t.data_ptr() for t in dev_in])
+    szs = (ctypes.c_size_t * 6)(*nbytes)
+
+    def run_e2e(n):
+        total = ctypes.c_float(0)
+        st = blib.pa_bench_e2e_steps(n, copies, src, dst, szs, 6, out.data_ptr(),
+                                     h_out.data_ptr(), d2h, kn.data_ptr(), vn.data_ptr(), kps,
+                                     vps, sm.data_ptr(), b.page_size, app_shape, q.data_ptr(),
+                                     bt.data_ptr(), cl.data_ptr(), b.scale, int(b.causal),
+                                     out.data_ptr(), shape, max_ctx, ws.data_ptr(), ws_need, sp,
+                                     ctypes.byref(total))
+        if st != 0:
+            raise RuntimeError(f"native e2e loop failed with status {st}")
+        return float(total.value)
+
+    run_e2e(3)
+    e2e_ms = run_e2e(e2e_steps) / e2e_steps
 
     # ---- secondary: chunked prefill TFLOP/s (prefill route) -----------------
     prefill = None
@@ -445,18 +458,20 @@ def main(argv=None):
                       f"({copies * pool_bytes / 1e6:.0f} MB vs {l2 / 1e6:.0f} MB L2): each "
                       f"step reads a copy last touched {copies - 1} steps earlier"),
         "tokens_per_s": round(world * b.B / (ms_step * 1e-3), 1),
-        "decode_kernel_us": round(1e3 * dec_avg_ms, 3),
+        "decode_call_us": round(1e3 * dec_avg_ms, 3),
+        "decode_call_timing": f"CUDA events around pa_attention on every {sample_every}th timed step",
         "route": "decode" if route == 0 else "prefill",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "decode_kernel<128> (split-KV + fused merge)",
+                     "kernel": "decode_kernel<128> + decode_merge_kernel<128> (one pa_decode call)",
                      "algorithmic_bytes_per_launch": dec_bytes},
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * (dec_bytes + app_bytes) / (e2e_ms * 1e-3) / 1e9, 3),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 6), "steps": e2e_steps},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (3 if route == 0 else 2) * args.steps,
+        "timed_loop": "native C loop over the C ABI (bench_loop.cpp)",
         "host_launch_us_per_step": round(1e6 * host_s / args.steps, 2),
         "clocks": ck,
     }

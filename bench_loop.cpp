@@ -1,0 +1,138 @@
+// Native timed loops for bench.py: the benchmark's steps issued from C
+// through the public C ABI of libpagedattn.so, so that no interpreter runs
+// between launches inside a timed region. Not part of the library.
+//
+// One step = pa_append_kv (new K/V rows by slot_mapping) + pa_attention on
+// page-pool copy k % n_copies. CUDA events bracket the whole loop, and the
+// attention call (its kernels' device time) of every `sample_every`-th step:
+// an event between two kernels stops the second from being scheduled early
+// (programmatic dependent launch), so the other steps run without one, as
+// a serving loop would.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "include/pagedattn.h"
+
+namespace {
+
+struct EventPool {
+    std::vector<cudaEvent_t> ev;
+    explicit EventPool(size_t n) : ev(n, nullptr)
+    {
+        for (auto& e : ev)
+            if (cudaEventCreate(&e) != cudaSuccess)
+                e = nullptr;
+    }
+    ~EventPool()
+    {
+        for (auto e : ev)
+            if (e)
+                cudaEventDestroy(e);
+    }
+    bool ok() const
+    {
+        for (auto e : ev)
+            if (!e)
+                return false;
+        return true;
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+// Returns 0 on success, a pa_status (> 0) if a call failed, -1 on a CUDA
+// error. step_ms[j]: device time of the attention call of step
+// j * sample_every; *total_ms: the whole loop (first append to last
+// attention).
+int pa_bench_steps(int n_steps, int sample_every, int n_copies, const void* key_new, const void* value_new,
+                   void* const* key_pages, void* const* value_pages,
+                   const int32_t* slot_mapping, int32_t page_size, pa_shape append_shape,
+                   const void* query, const int32_t* block_table, const int32_t* context_lens,
+                   float scale, int causal, void* out, pa_shape shape, int32_t max_context_len,
+                   void* workspace, size_t workspace_bytes, void* stream, float* step_ms,
+                   float* total_ms)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (sample_every < 1)
+        sample_every = 1;
+    const int n_samples = (n_steps + sample_every - 1) / sample_every;
+    EventPool pool(2 * size_t(n_samples) + 2);
+    if (!pool.ok())
+        return -1;
+    cudaEvent_t t0 = pool.ev[2 * n_samples], t1 = pool.ev[2 * n_samples + 1];
+    if (cudaEventRecord(t0, s) != cudaSuccess)
+        return -1;
+    for (int k = 0; k < n_steps; ++k) {
+        const int c = k % n_copies;
+        const bool sampled = k % sample_every == 0;
+        const int j = k / sample_every;
+        pa_status st = pa_append_kv(key_new, value_new, key_pages[c], value_pages[c],
+                                    slot_mapping, page_size, append_shape, stream);
+        if (st != PA_OK)
+            return int(st);
+        if (sampled)
+            cudaEventRecord(pool.ev[2 * j], s);
+        st = pa_attention(query, key_pages[c], value_pages[c], block_table, context_lens,
+                          page_size, scale, causal, out, shape, max_context_len, workspace,
+                          workspace_bytes, stream);
+        if (st != PA_OK)
+            return int(st);
+        if (sampled)
+            cudaEventRecord(pool.ev[2 * j + 1], s);
+    }
+    if (cudaEventRecord(t1, s) != cudaSuccess || cudaEventSynchronize(t1) != cudaSuccess)
+        return -1;
+    for (int j = 0; j < n_samples; ++j)
+        if (cudaEventElapsedTime(&step_ms[j], pool.ev[2 * j], pool.ev[2 * j + 1]) != cudaSuccess)
+            return -1;
+    return cudaEventElapsedTime(total_ms, t0, t1) == cudaSuccess ? 0 : -1;
+}
+
+// End-to-end steps from pinned host buffers: every step copies the step's
+// inputs host -> device (query, new K/V, slot_mapping, block_table,
+// context_lens), runs the step, and copies the output back.
+int pa_bench_e2e_steps(int n_steps, int n_copies, const void* const* host_src,
+                       void* const* dev_dst, const size_t* bytes, int n_inputs,
+                       const void* dev_out, void* host_out, size_t out_bytes,
+                       const void* key_new, const void* value_new, void* const* key_pages,
+                       void* const* value_pages, const int32_t* slot_mapping, int32_t page_size,
+                       pa_shape append_shape, const void* query, const int32_t* block_table,
+                       const int32_t* context_lens, float scale, int causal, void* out,
+                       pa_shape shape, int32_t max_context_len, void* workspace,
+                       size_t workspace_bytes, void* stream, float* total_ms)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    EventPool pool(2);
+    if (!pool.ok())
+        return -1;
+    if (cudaEventRecord(pool.ev[0], s) != cudaSuccess)
+        return -1;
+    for (int k = 0; k < n_steps; ++k) {
+        const int c = k % n_copies;
+        for (int i = 0; i < n_inputs; ++i)
+            if (cudaMemcpyAsync(dev_dst[i], host_src[i], bytes[i], cudaMemcpyHostToDevice, s) !=
+                cudaSuccess)
+                return -1;
+        pa_status st = pa_append_kv(key_new, value_new, key_pages[c], value_pages[c],
+                                    slot_mapping, page_size, append_shape, stream);
+        if (st != PA_OK)
+            return int(st);
+        st = pa_attention(query, key_pages[c], value_pages[c], block_table, context_lens,
+                          page_size, scale, causal, out, shape, max_context_len, workspace,
+                          workspace_bytes, stream);
+        if (st != PA_OK)
+            return int(st);
+        if (cudaMemcpyAsync(host_out, dev_out, out_bytes, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess)
+            return -1;
+    }
+    if (cudaEventRecord(pool.ev[1], s) != cudaSuccess || cudaEventSynchronize(pool.ev[1]) != cudaSuccess)
+        return -1;
+    return cudaEventElapsedTime(total_ms, pool.ev[0], pool.ev[1]) == cudaSuccess ? 0 : -1;
+}
+
+}  // extern "C"

@@ -98,10 +98,9 @@ pa_status pa_append_kv(const void *key, const void *value, void *key_pages,
 /*
  * Bytes of scratch workspace pa_decode needs for `shape` on the CURRENT
  * device (it depends on the device's SM count). 0 on invalid shapes.
- * Layout: the first 256 KiB hold one int32 ticket per segment (request x KV
- * head x tile of 16 query rows; at most 65536 segments), the rest holds
- * per-block partial (max, sum, output) states. The ticket region is the same
- * for every shape.
+ * It holds one partial (max, sum, output) state per block for every segment
+ * (request x KV head x tile of 16 query rows; at most 65536 segments) that
+ * straddles blocks; its contents on entry do not matter.
  */
 size_t pa_decode_workspace_bytes(pa_shape shape);
 
@@ -117,13 +116,11 @@ size_t pa_decode_workspace_bytes(pa_shape shape);
  *   max_context_len  an upper bound of context_lens used only to size the
  *                    grid (0 = unknown); larger entries are still correct.
  *   workspace        device scratch of at least pa_decode_workspace_bytes
- *                    bytes, 256-byte aligned, whose first 256 KiB are
- *                    ZERO-FILLED before its first use. A call that completes
- *                    leaves those ticket words at zero again, so one zero
- *                    fill serves every later call of any shape that fits.
- *                    Calls that share a workspace must not overlap on the
- *                    GPU. After a device error the ticket region must be
- *                    zero-filled again.
+ *                    bytes, 16-byte aligned; any contents. Calls that share a
+ *                    workspace must not overlap on the GPU.
+ * The work is two kernels on `stream`: the split-KV pass and a small merge
+ * pass, chained by programmatic dependent launch (each waits for the kernel
+ * before it in the stream before touching any data).
  */
 pa_status pa_decode(const void *query, const void *key_pages,
                     const void *value_pages, const int32_t *block_table,
@@ -149,9 +146,9 @@ pa_status pa_decode(const void *query, const void *key_pages,
  *   - Shapes whose scratch (pa_decode_workspace_bytes) exceeds 32 MiB are
  *     rejected with PA_ERR_WORKSPACE before anything is launched.
  *   - Every call on a device shares the one array, which keeps the previous
- *     call's contents; each call zero-fills the ticket words it needs (a
- *     memset on `stream`) before its kernel. Calls that overlap on the GPU
- *     (other streams, other host threads) race on the array: order them.
+ *     call's contents (the decode needs nothing in it to start at zero).
+ *     Calls that overlap on the GPU (other streams, other host threads) race
+ *     on the array: order them.
  */
 pa_status pa_decode_noalloc(const void *query, const void *key_pages,
                             const void *value_pages, const int32_t *block_table,

@@ -120,8 +120,8 @@ def make_shape(query_shape, pages_shape, max_pages: int) -> pa_shape:
 
 
 # ---------------------------------------------------------------------------
-# Workspace cache: one zero-filled buffer per device, grown on demand. The
-# library leaves the counter words at zero after every completed call.
+# Workspace cache: one buffer per device, grown on demand (its contents never
+# matter to the library).
 
 _ws_lock = threading.Lock()
 _ws_cache = {}

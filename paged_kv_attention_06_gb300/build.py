@@ -19,6 +19,9 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(BUILD, "libpagedattn.so")
+ROOT = os.path.dirname(HERE)
+BENCH_SRC = os.path.join(ROOT, "bench_loop.cpp")
+BENCH_LIB = os.path.join(BUILD, "libpabench.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -44,10 +47,11 @@ def _deps():
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
-        return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in _deps())
+    for lib in (LIB, BENCH_LIB):
+        if not os.path.exists(lib):
+            return False
+    t = min(os.path.getmtime(LIB), os.path.getmtime(BENCH_LIB))
+    return all(os.path.getmtime(p) <= t for p in _deps() + [BENCH_SRC])
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
@@ -73,12 +77,24 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         objs = list(ex.map(compile_one, srcs))
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-           "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
+           "-Xlinker", "-soname=libpagedattn.so", "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("nvcc link failed")
     os.replace(tmp, LIB)
+    # The benchmark's native step loops (bench_loop.cpp, beside bench.py):
+    # host code only, linked against the library above.
+    if os.path.exists(BENCH_SRC):
+        tmp = BENCH_LIB + f".tmp{os.getpid()}"
+        cmd = [nvcc, "-shared", "-std=c++17", "-O2", "-Xcompiler", "-fPIC", "-cudart", "shared",
+               "-I", ROOT, BENCH_SRC, "-o", tmp, "-L", BUILD, "-lpagedattn",
+               "-Xlinker", "-rpath=$ORIGIN", "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode:
+            sys.stderr.write(r.stdout + r.stderr)
+            raise RuntimeError("bench loop build failed")
+        os.replace(tmp, BENCH_LIB)
     return LIB
 
 

@@ -110,8 +110,49 @@ pa_status check_attention(const void* query, const void* key_pages, const void* 
     return PA_OK;
 }
 
+// Recently encoded tensor maps of this host thread (a map depends only on
+// the pool's address and shape).
+struct MapCacheEntry {
+    CUtensorMap map;
+    const void* pool;
+    uint64_t rows;
+    int32_t D, ps;
+    bool valid;
+};
+constexpr int kMapCache = 8;
+thread_local MapCacheEntry t_map_cache[kMapCache];
+thread_local int t_map_next = 0;
+
+pa_status encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pa_shape& s,
+                                   int32_t ps);
+
 // 2-D view of a page pool: rows = P * H_kv * page_size, columns = D.
 pa_status encode_pool_map(CUtensorMap* map, const void* pool, const pa_shape& s, int32_t ps)
+{
+    const uint64_t rows = uint64_t(s.num_pages) * s.num_kv_heads * ps;
+    for (int i = 0; i < kMapCache; ++i) {
+        const MapCacheEntry& e = t_map_cache[i];
+        if (e.valid && e.pool == pool && e.rows == rows && e.D == s.head_dim && e.ps == ps) {
+            *map = e.map;
+            return PA_OK;
+        }
+    }
+    pa_status st = encode_pool_map_uncached(map, pool, s, ps);
+    if (st == PA_OK) {
+        MapCacheEntry& e = t_map_cache[t_map_next];
+        t_map_next = (t_map_next + 1) % kMapCache;
+        e.map = *map;
+        e.pool = pool;
+        e.rows = rows;
+        e.D = s.head_dim;
+        e.ps = ps;
+        e.valid = true;
+    }
+    return st;
+}
+
+pa_status encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pa_shape& s,
+                                   int32_t ps)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     pa_status st = get_encoder(&enc);
@@ -179,11 +220,9 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
     memset(&a, 0, sizeof a);
     if (!whole_segments) {
         const size_t need = decode_workspace_bytes(nseg, grid_max, s.head_dim);
-        if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
             return PA_ERR_WORKSPACE;
-        a.counters = static_cast<int32_t*>(workspace);
-        a.partials =
-            reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kCounterRegionBytes);
+        a.partials = static_cast<float*>(workspace);
     }
     CUtensorMap kmap, vmap;
     if ((st = encode_pool_map(&kmap, key_pages, s, page_size)) != PA_OK)

@@ -7,6 +7,7 @@
 // fully coalesced. The copy is bit-exact (no conversion).
 #include <stdint.h>
 
+#include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -14,6 +15,11 @@ namespace {
 
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a)
 {
+    // Launched with programmatic stream serialization: wait for the previous
+    // kernel in the stream (which may still read the pool) before writing,
+    // and let the attention kernel that follows be scheduled.
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int vec_per_row = a.D / 8;
     const int64_t per_tensor = int64_t(a.B) * a.L_new * a.H_kv * vec_per_row;
     const int64_t total = 2 * per_tensor;
@@ -55,8 +61,16 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream)
     int64_t blocks = (total + 255) / 256;
     if (blocks > 65535)
         blocks = 65535;
-    append_kernel<<<int(blocks), 256, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, append_kernel, a);
 }
 
 }  // namespace pa

@@ -16,20 +16,24 @@
 //     ranges (split-KV across blocks: the cached context is spread over the
 //     whole GPU however ragged the lengths are).
 //   * Per block: one producer warp resolves each page id once per page
-//     (address translation hoisted per TMA box) and issues TMA tile loads of
-//     whole page slices into a 3-stage shared-memory ring (128B swizzle);
-//     four consumer warps each take 16 tokens of a granule and run
-//     S = Q K^T and O += P V on the tensor cores (mma.sync m16n8k16, bf16 in,
-//     fp32 accumulate) with the online-softmax recurrence in registers
-//     (running max, running sum, rescaled output; Week 3 Day 4, "Task 2").
-//   * At the end of a segment piece the four warps merge their (m, l, O)
-//     through shared memory. A segment that one block finished alone is
-//     normalised and written; otherwise the block writes its partial state,
-//     and the last block to finish the segment (an atomic ticket, no waiting
-//     on other blocks) merges all partials: M = max m_s,
-//     l = sum l_s 2^(m_s - M), o = sum acc_s 2^(m_s - M) / l.
-//   * Scores live in the log2 domain (scale * log2(e) folded into one
-//     multiply) so every exponential is one exp2f.
+//     (address translation hoisted per TMA box, issued before it waits for a
+//     free stage) and issues TMA tile loads of whole page slices into a
+//     3-stage shared-memory ring (128B swizzle). Four consumer warps split the
+//     head dimension: each computes S = Q K^T for all 64 tokens of a granule
+//     (the same values in every warp, so the softmax state needs no exchange)
+//     and O += P V for its quarter of the output columns, on the tensor cores
+//     (mma.sync m16n8k16, bf16 in, fp32 accumulate), with the online-softmax
+//     recurrence in registers (running max, running sum, rescaled output;
+//     Week 3 Day 4, "Task 2").
+//   * A segment that one block finished alone is normalised and written at
+//     once. A segment that straddles blocks leaves one partial (m, l, acc)
+//     per block; a second, small kernel (one block per such segment, chained
+//     by programmatic dependent launch so it is resident before this one
+//     ends) merges them: M = max m_s, l = sum l_s 2^(m_s - M),
+//     o = sum acc_s 2^(m_s - M) / l. No block ever waits for another block.
+//   * Scores live in the log2 domain (scale * log2(e) folded into one FFMA)
+//     so every exponential is one ex2.approx; the output is rescaled only
+//     when a running maximum moves.
 //   * Masked scores are selected to -inf (never multiplied by zero); V rows
 //     past the context are zeroed in shared memory before P V, so stale or
 //     NaN bytes in unused page slots never reach the result.
@@ -60,13 +64,10 @@ struct Layout {
     static constexpr int kK = 0;
     static constexpr int kV = kK + kStages * kStageBytes;
     static constexpr int kQ = kV + kStages * kStageBytes;    // [16][D] bf16, swizzled
-    static constexpr int kML = kQ + kDecodeRows * D * 2;     // [warps][2][16] float
-    static constexpr int kBar = kML + kConsumerWarps * 2 * kDecodeRows * 4;
-    static constexpr int kMisc = kBar + 2 * kStages * 8;     // abort flag, ticket, test barrier
-    static constexpr int kPrefix = kMisc + 16;               // [B + 1] int32
+    static constexpr int kBar = kQ + kDecodeRows * D * 2;
+    static constexpr int kMisc = kBar + 2 * kStages * 8;     // abort flag, test barrier
+    static constexpr int kPrefix = kMisc + 32;               // [B + 1] int32
     static size_t bytes(int B) { return kPrefix + size_t(B + 1) * 4 + 1024; }
-    static_assert(kStageBytes * 2 >= 4 * kDecodeRows * D * 4,
-                  "merge scratch must fit in one stage");
 };
 
 __device__ __forceinline__ int clamp_context(int n, int cap, unsigned* err)
@@ -132,12 +133,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
     uint64_t* empty = full + kStages;
     volatile int* misc = reinterpret_cast<volatile int*>(smem + Lay::kMisc);
-    float* ml = reinterpret_cast<float*>(smem + Lay::kML);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int per_req = a.H_kv * a.MT;
     const int cap = a.max_pages * a.ps;
+
+    // Inputs may come from the previous kernel in the stream (e.g. the append
+    // of this step): wait for it before reading any of them, and let the
+    // merge pass that follows this kernel be scheduled right away.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     // ---- granule prefix over requests (one warp) ---------------------------
     if (warp == 0) {
@@ -163,10 +169,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             carry += __shfl_sync(0xffffffffu, incl, 31);
         }
     }
-    uint64_t* never = reinterpret_cast<uint64_t*>(smem + Lay::kMisc + 8);
+    uint64_t* never = reinterpret_cast<uint64_t*>(smem + Lay::kMisc + 16);
     if (threadIdx.x == 0) {
         misc[0] = 0;
         misc[1] = 0;
+        misc[2] = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
@@ -234,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             prefetch_tensormap(&value_map);
         }
         const uint64_t policy = l2_policy_evict_first();
+        const int box = a.box_rows;
         int stage = 0;
         uint32_t phase = 0;
         for (int64_t x = x_begin; x < x_end; ++x) {
@@ -241,32 +249,48 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int n = clamp_context(a.context_lens[sp.b], cap, a.err);
             const int t0 = int(x - sp.seg_start) * kDecodeTokens;
             const int nvalid = min(kDecodeTokens, n - t0);
-            const bool ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, misc, a.err);
-            if (ok && nvalid > 0) {
-                const int box = a.box_rows;
-                const int nbox = (nvalid + box - 1) / box;
-                const uint32_t bytes = uint32_t(nbox) * box * 128u * Lay::kHalves * 2u;
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-                __syncwarp();
-                const int32_t* bt = a.block_table + int64_t(sp.b) * a.max_pages;
-                for (int j = lane; j < nbox; j += 32) {
+            const int nbox = nvalid > 0 ? (nvalid + box - 1) / box : 0;
+            // Address translation for this granule, once per page (box), issued
+            // before the wait for a free stage so its latency overlaps it.
+            const int32_t* bt = a.block_table + int64_t(sp.b) * a.max_pages;
+            int row_a = 0, row_b = 0;  // boxes lane and lane + 32
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int j = lane + 32 * k;
+                if (j < nbox) {
                     const int tok = t0 + j * box;
                     const int lp = tok / a.ps;
-                    const int slot0 = tok - lp * a.ps;
                     int phys = bt[lp];
                     if (unsigned(phys) >= unsigned(a.num_pages)) {
                         atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
                         phys = 0;
                     }
-                    const int row = (phys * a.H_kv + sp.h) * a.ps + slot0;
-                    const int dst = j * box * 128;
+                    const int row = (phys * a.H_kv + sp.h) * a.ps + (tok - lp * a.ps);
+                    if (k == 0)
+                        row_a = row;
+                    else
+                        row_b = row;
+                }
+            }
+            const bool ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, misc, a.err);
+            if (ok && nbox > 0) {
+                const uint32_t bytes = uint32_t(nbox) * box * 128u * Lay::kHalves * 2u;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                __syncwarp();
 #pragma unroll
-                    for (int hf = 0; hf < Lay::kHalves; ++hf) {
-                        tma_load_2d(k_half(stage, hf) + dst, &key_map, hf * 64, row, &full[stage],
-                                    policy);
-                        tma_load_2d(v_half(stage, hf) + dst, &value_map, hf * 64, row,
-                                    &full[stage], policy);
+                for (int k = 0; k < 2; ++k) {
+                    const int j = lane + 32 * k;
+                    if (j < nbox) {
+                        const int row = k == 0 ? row_a : row_b;
+                        const int dst = j * box * 128;
+#pragma unroll
+                        for (int hf = 0; hf < Lay::kHalves; ++hf) {
+                            tma_load_2d(k_half(stage, hf) + dst, &key_map, hf * 64, row,
+                                        &full[stage], policy);
+                            tma_load_2d(v_half(stage, hf) + dst, &value_map, hf * 64, row,
+                                        &full[stage], policy);
+                        }
                     }
                 }
             } else if (ok && lane == 0) {
@@ -282,33 +306,67 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ===================== consumer warps ===================================
+    // Consumer warp w owns output columns [w * D/4, (w + 1) * D/4). Every
+    // warp computes the scores of all 64 tokens of a granule (identical in all
+    // four warps, so the softmax state needs no exchange) and P V for its own
+    // columns; a segment's result never has to be merged across warps.
+    constexpr int kCols = D / kConsumerWarps;  // output columns per warp
+    constexpr int kON = kCols / 8;             // output n-tiles per warp
+    constexpr int kSN = kDecodeTokens / 8;     // score n-tiles per granule
     const int tid = threadIdx.x;  // 0..127
     const int swz = a.swz;        // stage layout: chunk ^ (row & 7) when swizzled
     const int row0 = lane >> 2;   // fragment rows row0 and row0 + 8
     const int quad = lane & 3;
+    const int col0 = warp * kCols;
     uint8_t* q_smem = smem + Lay::kQ;
     int stage = 0;
     uint32_t phase = 0;
+    constexpr int kSlotFloats = kDecodeRows * (D + 2);
+
+    // Q tile of a segment (16 rows x D, 16-byte chunks) -> registers; each
+    // consumer thread holds kQChunks chunks. Loaded one piece ahead so the
+    // next piece never waits on it.
+    constexpr int kQChunks = (kDecodeRows * kNT) / kConsumerThreads;
+    static_assert(kQChunks * kConsumerThreads == kDecodeRows * kNT, "Q tile split");
+    uint4 qreg[kQChunks];
+    auto load_q = [&](const SegmentPos& p) {
+#pragma unroll
+        for (int u = 0; u < kQChunks; ++u) {
+            const int c = tid + u * kConsumerThreads;
+            const int r = c / kNT, ch = c - r * kNT;
+            const int rg = p.mt * kDecodeRows + r;
+            qreg[u] = make_uint4(0, 0, 0, 0);
+            if (rg < a.R) {
+                const int g = rg / a.L, i = rg - g * a.L;
+                const int hq = p.h * a.G + g;
+                qreg[u] = *reinterpret_cast<const uint4*>(
+                    a.q + ((int64_t(p.b) * a.H_q + hq) * a.L + i) * D + ch * 8);
+            }
+        }
+    };
+
+    // Output row index of fragment row rw of a segment, or -1 for padding.
+    auto out_row = [&](const SegmentPos& p, int rw) -> int64_t {
+        const int rg = p.mt * kDecodeRows + rw;
+        if (rg >= a.R)
+            return -1;
+        const int g = rg / a.L, i = rg - g * a.L;
+        return (int64_t(p.b) * a.H_q + p.h * a.G + g) * a.L + i;
+    };
 
     int64_t x = x_begin;
+    load_q(locate(pre, a.B, per_req, a.MT, x));
     while (x < x_end) {
         const SegmentPos sp = locate(pre, a.B, per_req, a.MT, x);
         const int64_t piece_end = min(x_end, sp.seg_start + sp.seg_len);
         const int n = clamp_context(a.context_lens[sp.b], cap, a.err);
 
-        // ---- Q tile (16 rows x D) into shared memory, 16-byte chunks swizzled
-        for (int c = tid; c < kDecodeRows * kNT; c += kConsumerThreads) {
+        // ---- Q tile into shared memory, 16-byte chunks swizzled by row
+#pragma unroll
+        for (int u = 0; u < kQChunks; ++u) {
+            const int c = tid + u * kConsumerThreads;
             const int r = c / kNT, ch = c - r * kNT;
-            const int rg = sp.mt * kDecodeRows + r;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (rg < a.R) {
-                const int g = rg / a.L, i = rg - g * a.L;
-                const int hq = sp.h * a.G + g;
-                const uint16_t* src =
-                    a.q + ((int64_t(sp.b) * a.H_q + hq) * a.L + i) * D + ch * 8;
-                v = *reinterpret_cast<const uint4*>(src);
-            }
-            *reinterpret_cast<uint4*>(q_smem + r * D * 2 + ((ch ^ (r & 7)) << 4)) = v;
+            *reinterpret_cast<uint4*>(q_smem + r * D * 2 + ((ch ^ (r & 7)) << 4)) = qreg[u];
         }
         named_barrier_sync(kConsumerBarrier, kConsumerThreads);
         uint32_t qa[kKS][4];
@@ -328,283 +386,316 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int i = rg < a.R ? rg % a.L : a.L - 1;
             lim[rr] = a.causal ? min(n - a.L + i, n - 1) : n - 1;
         }
+        const int lim_min = __reduce_min_sync(0xffffffffu, min(lim[0], lim[1]));
 
         float m_run[2] = {-INFINITY, -INFINITY};
         float l_run[2] = {0.f, 0.f};
-        float o[kNT][4];
+        float o[kON][4];
 #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
+        for (int nt = 0; nt < kON; ++nt)
             o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
-        int hold = 0;
-        bool wrote_hold = false;
         for (; x < piece_end; ++x) {
             const int t0 = int(x - sp.seg_start) * kDecodeTokens;
             const int nvalid = min(kDecodeTokens, n - t0);
             const bool ok = mbar_wait_bounded(&full[stage], phase, misc, a.err);
-            const int my0 = warp * 16;
             bool wrote = false;
-            if (ok && my0 < nvalid) {
-                if (nvalid < my0 + 16) {
-                    // Zero V rows past the context: P is 0 there, but 0 * NaN is not.
-                    const int z0 = nvalid;
-                    const int nz = (my0 + 16 - z0) * kNT;
+            if (ok && nvalid > 0) {
+                if (nvalid < kDecodeTokens) {
+                    // Zero this warp's V columns of the rows past the context:
+                    // P is 0 there, but 0 * NaN is not.
+                    constexpr int kChunks = kCols / 8;  // 16-byte chunks per row
+                    const int nz = (kDecodeTokens - nvalid) * kChunks;
                     for (int idx = lane; idx < nz; idx += 32) {
-                        const int r = z0 + idx / kNT, ch = idx % kNT;
+                        const int r = nvalid + idx / kChunks;
+                        const int ch = col0 / 8 + idx % kChunks;
                         *reinterpret_cast<uint4*>(v_half(stage, ch >> 3) + r * 128 +
-                                                  ((ch & 7) << 4)) = make_uint4(0, 0, 0, 0);
+                                                  (((ch & 7) ^ (r & swz)) << 4)) =
+                            make_uint4(0, 0, 0, 0);
                     }
                     wrote = true;
                     __syncwarp();
                 }
-                // S = Q K^T for tokens my0..my0+15 (two n-tiles of 8 tokens).
-                float s[2][4];
+                // S = Q K^T for all 64 tokens (8 n-tiles of 8 tokens).
+                float sc[kSN][4];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-                    s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+                for (int nt = 0; nt < kSN; ++nt)
+                    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
                 {
-                    const int tr = my0 + (lane & 7) + ((lane >> 4) << 3);
+                    const int trl = (lane & 7) + ((lane >> 4) << 3);
                     const int chsel = (lane >> 3) & 1;
 #pragma unroll
                     for (int kk = 0; kk < kKS; ++kk) {
                         const int ch = 2 * kk + chsel;
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(smem_u32(k_half(stage, ch >> 3) + tr * 128 +
-                                         (((ch & 7) ^ (tr & swz)) << 4)),
-                                b0, b1, b2, b3);
-                        mma_bf16_16816(s[0], qa[kk], b0, b1);
-                        mma_bf16_16816(s[1], qa[kk], b2, b3);
+#pragma unroll
+                        for (int tq = 0; tq < kSN / 2; ++tq) {
+                            const int tr = tq * 16 + trl;
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(smem_u32(k_half(stage, ch >> 3) + tr * 128 +
+                                             (((ch & 7) ^ (tr & swz)) << 4)),
+                                    b0, b1, b2, b3);
+                            mma_bf16_16816(sc[2 * tq], qa[kk], b0, b1);
+                            mma_bf16_16816(sc[2 * tq + 1], qa[kk], b2, b3);
+                        }
                     }
                 }
-                // Scale into the log2 domain and mask (select, never multiply).
+                // Mask (select to -inf, never multiply) only where some row's
+                // last visible position falls inside this granule.
+                if (t0 + kDecodeTokens - 1 > lim_min) {
+#pragma unroll
+                    for (int nt = 0; nt < kSN; ++nt)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int tok = t0 + nt * 8 + 2 * quad + (j & 1);
+                            if (tok > lim[j >> 1])
+                                sc[nt][j] = -INFINITY;
+                        }
+                }
+                // Online softmax in the log2 domain: m_run is kept scaled
+                // (scale * log2 e > 0 preserves the order); p = 2^(c s - m) is
+                // one FFMA and one ex2.
                 float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int tok = t0 + my0 + nt * 8 + 2 * quad + (j & 1);
-                        const int rr = j >> 1;
-                        const float v = s[nt][j] * a.scale_log2;
-                        s[nt][j] = tok <= lim[rr] ? v : -INFINITY;
-                        mx[rr] = fmaxf(mx[rr], s[nt][j]);
-                    }
+                for (int nt = 0; nt < kSN; ++nt) {
+                    mx[0] = fmaxf(mx[0], fmaxf(sc[nt][0], sc[nt][1]));
+                    mx[1] = fmaxf(mx[1], fmaxf(sc[nt][2], sc[nt][3]));
                 }
-                float corr[2], mu[2];
+                float mu[2], mn[2];
+                bool changed = false;
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
                     mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-                    const float mn = fmaxf(m_run[rr], mx[rr]);
-                    mu[rr] = mn == -INFINITY ? 0.f : mn;
-                    corr[rr] = exp2f(m_run[rr] - mu[rr]);
-                    m_run[rr] = mn;
+                    mn[rr] = fmaxf(m_run[rr], mx[rr] * a.scale_log2);
+                    changed |= mn[rr] != m_run[rr];
+                    mu[rr] = mn[rr] == -INFINITY ? 0.f : mn[rr];
                 }
-                float psum[2] = {0.f, 0.f};
+                if (__any_sync(0xffffffffu, changed)) {
+                    // Rescale only when a running max moved: corr = 2^(m_old -
+                    // m_new), exactly 1 for rows whose max did not move.
+                    float corr[2];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                    for (int rr = 0; rr < 2; ++rr) {
+                        corr[rr] = mn[rr] == m_run[rr] ? 1.f : fast_exp2(m_run[rr] - mu[rr]);
+                        m_run[rr] = mn[rr];
+                        l_run[rr] *= corr[rr];
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < kON; ++nt) {
+                        o[nt][0] *= corr[0];
+                        o[nt][1] *= corr[0];
+                        o[nt][2] *= corr[1];
+                        o[nt][3] *= corr[1];
+                    }
+                }
+                uint32_t pa[kSN / 2][4];
+#pragma unroll
+                for (int nt = 0; nt < kSN; ++nt) {
+                    float p[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const float p = exp2f(s[nt][j] - mu[j >> 1]);
-                        s[nt][j] = p;
-                        psum[j >> 1] += p;
+                        p[j] = fast_exp2(fmaf(sc[nt][j], a.scale_log2, -mu[j >> 1]));
+                        l_run[j >> 1] += p[j];
                     }
+                    pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p[0], p[1]);
+                    pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p[2], p[3]);
                 }
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr)
-                    l_run[rr] = l_run[rr] * corr[rr] + psum[rr];
-#pragma unroll
-                for (int nt = 0; nt < kNT; ++nt) {
-                    o[nt][0] *= corr[0];
-                    o[nt][1] *= corr[0];
-                    o[nt][2] *= corr[1];
-                    o[nt][3] *= corr[1];
-                }
-                uint32_t pa[4];
-                pa[0] = pack_bf16x2(s[0][0], s[0][1]);
-                pa[1] = pack_bf16x2(s[0][2], s[0][3]);
-                pa[2] = pack_bf16x2(s[1][0], s[1][1]);
-                pa[3] = pack_bf16x2(s[1][2], s[1][3]);
-                // O += P V: ldmatrix.trans gives the k-major V fragments.
+                // O[:, col0 .. col0 + kCols) += P V; ldmatrix.trans gives the
+                // k-major V fragments.
                 {
-                    const int tr = my0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                    const int trl = (lane & 7) + (((lane >> 3) & 1) << 3);
                     const int chsel = lane >> 4;
 #pragma unroll
-                    for (int jj = 0; jj < kNT / 2; ++jj) {
-                        const int ch = 2 * jj + chsel;
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_trans(smem_u32(v_half(stage, ch >> 3) + tr * 128 +
-                                               (((ch & 7) ^ (tr & swz)) << 4)),
-                                      b0, b1, b2, b3);
-                        mma_bf16_16816(o[2 * jj], pa, b0, b1);
-                        mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
+                    for (int kt = 0; kt < kSN / 2; ++kt) {
+                        const int tr = kt * 16 + trl;
+#pragma unroll
+                        for (int jj = 0; jj < kON / 2; ++jj) {
+                            const int ch = col0 / 8 + 2 * jj + chsel;
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4_trans(smem_u32(v_half(stage, ch >> 3) + tr * 128 +
+                                                   (((ch & 7) ^ (tr & swz)) << 4)),
+                                          b0, b1, b2, b3);
+                            mma_bf16_16816(o[2 * jj], pa[kt], b0, b1);
+                            mma_bf16_16816(o[2 * jj + 1], pa[kt], b2, b3);
+                        }
                     }
                 }
             }
-            if (x + 1 < piece_end) {
-                if (wrote)
-                    fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&empty[stage]);
-            } else {
-                hold = stage;  // kept as merge scratch, released after the merge
-                wrote_hold = wrote;
-            }
+            if (wrote)
+                fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stage]);
             if (++stage == kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
-        (void)wrote_hold;
+        if (x < x_end)
+            load_q(locate(pre, a.B, per_req, a.MT, x));  // next piece's Q, in flight
 
-        // ---- merge the four warps' states through the held stage -----------
+        // ---- end of a piece: every warp holds identical (m, l) and its own
+        // output columns.
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
             l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
             l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
         }
-        named_barrier_sync(kConsumerBarrier, kConsumerThreads);  // all done reading `hold`
-        float* scratch = reinterpret_cast<float*>(warp < 2 ? k_half(hold, 0) : v_half(hold, 0)) +
-                         (warp & 1) * kDecodeRows * D;
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                const int r = row0 + rr * 8;
-                const int k2 = ((nt ^ (r & 7)) << 2) | quad;  // float2 index in the row
-                *reinterpret_cast<float2*>(scratch + r * D + 2 * k2) =
-                    make_float2(o[nt][2 * rr], o[nt][2 * rr + 1]);
-            }
-        }
-        if (quad == 0) {
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                ml[(warp * 2 + 0) * kDecodeRows + row0 + rr * 8] = m_run[rr];
-                ml[(warp * 2 + 1) * kDecodeRows + row0 + rr * 8] = l_run[rr];
-            }
-        }
-        named_barrier_sync(kConsumerBarrier, kConsumerThreads);
-
-        // Combine: thread -> (row, D/8 columns).
-        const int r = tid >> 3;
-        const int c0 = (tid & 7) * (D / 8);
-        const int rg = sp.mt * kDecodeRows + r;
-        float acc[D / 8];
-        float Lsum = 0.f, M = -INFINITY;
-        {
-            float mw[kConsumerWarps], lw[kConsumerWarps];
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                mw[w] = ml[(w * 2 + 0) * kDecodeRows + r];
-                lw[w] = ml[(w * 2 + 1) * kDecodeRows + r];
-                M = fmaxf(M, mw[w]);
-            }
-            const float Mu = M == -INFINITY ? 0.f : M;
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c)
-                acc[c] = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float f = exp2f(mw[w] - Mu);
-                Lsum += f * lw[w];
-                const float* sw =
-                    reinterpret_cast<const float*>(w < 2 ? k_half(hold, 0) : v_half(hold, 0)) +
-                    (w & 1) * kDecodeRows * D + r * D;
-#pragma unroll
-                for (int c = 0; c < D / 8; c += 2) {
-                    const int col = c0 + c;
-                    const int nt = col >> 3, qd = (col & 7) >> 1;
-                    const int k2 = ((nt ^ (r & 7)) << 2) | qd;
-                    const float2 v = *reinterpret_cast<const float2*>(sw + 2 * k2);
-                    acc[c] += f * v.x;
-                    acc[c + 1] += f * v.y;
-                }
-            }
-        }
-
-        const int64_t nseg_blocks_first = a.whole_segments ? cta : block_of(sp.seg_start, total, grid);
-        const int64_t nseg_blocks_last =
-            a.whole_segments ? cta : block_of(sp.seg_start + sp.seg_len - 1, total, grid);
-        const int npieces = int(nseg_blocks_last - nseg_blocks_first) + 1;
+        const bool single =
+            a.whole_segments ||
+            block_of(sp.seg_start, total, grid) == block_of(sp.seg_start + sp.seg_len - 1, total, grid);
         const bool aborted = misc[0] != 0;
 
-        auto store_out = [&](const float* v, float l) {
-            if (rg >= a.R)
-                return;
-            const int g = rg / a.L, i = rg - g * a.L;
-            const int hq = sp.h * a.G + g;
-            uint16_t* dst = a.out + ((int64_t(sp.b) * a.H_q + hq) * a.L + i) * D + c0;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (!aborted && single) {
 #pragma unroll
-            for (int c = 0; c < D / 8; c += 8) {
-                uint4 w;
-                w.x = pack_bf16x2(v[c + 0] * inv, v[c + 1] * inv);
-                w.y = pack_bf16x2(v[c + 2] * inv, v[c + 3] * inv);
-                w.z = pack_bf16x2(v[c + 4] * inv, v[c + 5] * inv);
-                w.w = pack_bf16x2(v[c + 6] * inv, v[c + 7] * inv);
-                *reinterpret_cast<uint4*>(dst + c) = w;
+            for (int rr = 0; rr < 2; ++rr) {
+                const int64_t orow = out_row(sp, row0 + rr * 8);
+                if (orow < 0)
+                    continue;
+                const float inv = l_run[rr] > 0.f ? 1.f / l_run[rr] : 0.f;
+                uint16_t* dst = a.out + orow * D + col0 + 2 * quad;
+#pragma unroll
+                for (int nt = 0; nt < kON; ++nt)
+                    *reinterpret_cast<uint32_t*>(dst + nt * 8) =
+                        pack_bf16x2(o[nt][2 * rr] * inv, o[nt][2 * rr + 1] * inv);
             }
-        };
-
-        if (npieces == 1) {
-            if (!aborted)
-                store_out(acc, Lsum);
         } else if (!aborted) {
-            constexpr int kSlotFloats = kDecodeRows * (D + 2);
+            // A segment that straddles blocks: leave this block's partial
+            // (m, l, acc) for the merge pass.
             float* slot = a.partials + (int64_t(sp.seg) + cta) * kSlotFloats;
-            if ((tid & 7) == 0) {
-                slot[r] = M;
-                slot[kDecodeRows + r] = Lsum;
-            }
-            float* dst = slot + 2 * kDecodeRows + r * D + c0;
 #pragma unroll
-            for (int c = 0; c < D / 8; c += 4)
-                *reinterpret_cast<float4*>(dst + c) =
-                    make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-            __threadfence();
-            named_barrier_sync(kConsumerBarrier, kConsumerThreads);
-            if (tid == 0) {
-                const int t = atomicAdd(&a.counters[sp.seg], 1);
-                misc[1] = (t == npieces - 1) ? 1 : 0;
-            }
-            named_barrier_sync(kConsumerBarrier, kConsumerThreads);
-            if (misc[1]) {
-                __threadfence();
-                const float* base = a.partials + (int64_t(sp.seg) + nseg_blocks_first) * kSlotFloats;
-                float Mx = -INFINITY;
-                for (int k = 0; k < npieces; ++k)
-                    Mx = fmaxf(Mx, __ldcg(base + int64_t(k) * kSlotFloats + r));
-                const float Mu = Mx == -INFINITY ? 0.f : Mx;
-                float L2 = 0.f;
-                float fin[D / 8];
-#pragma unroll
-                for (int c = 0; c < D / 8; ++c)
-                    fin[c] = 0.f;
-                for (int k = 0; k < npieces; ++k) {
-                    const float* sk = base + int64_t(k) * kSlotFloats;
-                    const float f = exp2f(__ldcg(sk + r) - Mu);
-                    L2 += f * __ldcg(sk + kDecodeRows + r);
-                    const float4* src =
-                        reinterpret_cast<const float4*>(sk + 2 * kDecodeRows + r * D + c0);
-#pragma unroll
-                    for (int c = 0; c < D / 8; c += 4) {
-                        const float4 v = __ldcg(src + c / 4);
-                        fin[c] += f * v.x;
-                        fin[c + 1] += f * v.y;
-                        fin[c + 2] += f * v.z;
-                        fin[c + 3] += f * v.w;
-                    }
+            for (int rr = 0; rr < 2; ++rr) {
+                const int rw = row0 + rr * 8;
+                if (out_row(sp, rw) < 0)
+                    continue;  // padding rows of the tile carry nothing
+                if (warp == 0 && quad == 0) {
+                    slot[rw] = m_run[rr];
+                    slot[kDecodeRows + rw] = l_run[rr];
                 }
-                store_out(fin, L2);
-                if (tid == 0)
-                    a.counters[sp.seg] = 0;
+                float* dst = slot + 2 * kDecodeRows + rw * D + col0 + 2 * quad;
+#pragma unroll
+                for (int nt = 0; nt < kON; ++nt)
+                    *reinterpret_cast<float2*>(dst + nt * 8) =
+                        make_float2(o[nt][2 * rr], o[nt][2 * rr + 1]);
             }
         }
-        named_barrier_sync(kConsumerBarrier, kConsumerThreads);  // scratch, Q and misc reuse
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&empty[hold]);
+        // Every warp has finished this piece before the next piece's Q tile
+        // overwrites shared memory.
+        named_barrier_sync(kConsumerBarrier, kConsumerThreads);
+    }
+}
+
+// Merge pass over the segments that straddle decode blocks: one block per
+// segment (blocks of the other segments return at once). Its per-segment
+// arithmetic repeats the decode kernel's partition, on the inputs only; the
+// partial states are read after the decode grid has completed.
+// Thread -> (row tid / 8, columns c0 .. c0 + D/8): M = max m_k,
+// l = sum l_k 2^(m_k - M), o = sum acc_k 2^(m_k - M) / l.
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int decode_grid)
+{
+    constexpr int kSlotFloats = kDecodeRows * (D + 2);
+    __shared__ long long red[2][4];
+    const int tid = threadIdx.x;
+    const int seg = blockIdx.x;
+    const int per_req = a.H_kv * a.MT;
+    const int b = seg / per_req, hm = seg - b * per_req;
+    const int cap = a.max_pages * a.ps;
+    auto granules = [&](int q) {
+        int n = a.context_lens[q];
+        n = n < 0 ? 0 : (n > cap ? cap : n);
+        return max(1, (n + kDecodeTokens - 1) / kDecodeTokens);
+    };
+    long long before = 0, total = 0;
+    for (int q = tid; q < a.B; q += blockDim.x) {
+        const long long g = (long long)granules(q) * per_req;
+        total += g;
+        if (q < b)
+            before += g;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        total += __shfl_xor_sync(0xffffffffu, total, o);
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+    }
+    if ((tid & 31) == 0) {
+        red[0][tid >> 5] = total;
+        red[1][tid >> 5] = before;
+    }
+    __syncthreads();
+    total = red[0][0] + red[0][1] + red[0][2] + red[0][3];
+    before = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+    const int gb = granules(b);
+    const int64_t seg_start = before + int64_t(hm) * gb;
+    const int64_t grid = int64_t(decode_grid) < total ? int64_t(decode_grid) : total;
+    const int64_t first = block_of(seg_start, total, grid);
+    const int64_t last = block_of(seg_start + gb - 1, total, grid);
+    if (first == last)
+        return;  // finished and written by one decode block
+    grid_dependency_wait();  // the decode grid has completed: its partials are visible
+
+    const int r = tid >> 3;
+    const int c0 = (tid & 7) * (D / 8);
+    const int rg = (hm % a.MT) * kDecodeRows + r;
+    if (rg >= a.R)
+        return;
+    const int g = rg / a.L, i = rg - g * a.L;
+    const int64_t orow = (int64_t(b) * a.H_q + (hm / a.MT) * a.G + g) * a.L + i;
+    const float* base = a.partials + (int64_t(seg) + first) * kSlotFloats;
+    const int np = int(last - first) + 1;
+    float Mx = -INFINITY;  // pieces' maxima, 8 loads in flight at a time
+    for (int k0 = 0; k0 < np; k0 += 8) {
+        float mk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            mk[u] = k0 + u < np ? __ldcg(base + int64_t(k0 + u) * kSlotFloats + r) : -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            Mx = fmaxf(Mx, mk[u]);
+    }
+    const float Mu = Mx == -INFINITY ? 0.f : Mx;
+    float L2 = 0.f;
+    float fin[D / 8];
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c)
+        fin[c] = 0.f;
+    for (int k0 = 0; k0 < np; k0 += 4) {  // weighted sums, 4 pieces in flight
+        float mk[4], lk[4];
+        float4 v[4][D / 32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const bool live = k0 + u < np;
+            const float* sk = base + int64_t(live ? k0 + u : 0) * kSlotFloats;
+            mk[u] = live ? __ldcg(sk + r) : -INFINITY;
+            lk[u] = live ? __ldcg(sk + kDecodeRows + r) : 0.f;
+            const float4* src = reinterpret_cast<const float4*>(sk + 2 * kDecodeRows + r * D + c0);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c)
+                v[u][c] = live ? __ldcg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float w = fast_exp2(mk[u] - Mu);  // 0 for absent pieces
+            L2 += w * lk[u];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                fin[4 * c] += w * v[u][c].x;
+                fin[4 * c + 1] += w * v[u][c].y;
+                fin[4 * c + 2] += w * v[u][c].z;
+                fin[4 * c + 3] += w * v[u][c].w;
+            }
+        }
+    }
+    const float inv = L2 > 0.f ? 1.f / L2 : 0.f;
+    uint16_t* dst = a.out + orow * D + c0;
+#pragma unroll
+    for (int c = 0; c < D / 8; c += 8) {
+        uint4 w4;
+        w4.x = pack_bf16x2(fin[c + 0] * inv, fin[c + 1] * inv);
+        w4.y = pack_bf16x2(fin[c + 2] * inv, fin[c + 3] * inv);
+        w4.z = pack_bf16x2(fin[c + 4] * inv, fin[c + 5] * inv);
+        w4.w = pack_bf16x2(fin[c + 6] * inv, fin[c + 7] * inv);
+        *reinterpret_cast<uint4*>(dst + c) = w4;
     }
 }
 
@@ -620,7 +711,7 @@ int decode_max_grid(int sm_count) { return 2 * sm_count; }
 size_t decode_workspace_bytes(int64_t nseg, int grid_max, int D)
 {
     const size_t slots = size_t(nseg) + size_t(grid_max);
-    return kCounterRegionBytes + slots * kDecodeRows * (D + 2) * 4;
+    return slots * kDecodeRows * (D + 2) * 4;
 }
 
 cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_map,
@@ -643,10 +734,31 @@ cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_m
             return e;
         smem_set[device][di].store(smem, std::memory_order_relaxed);
     }
-    if (a.D == 64)
-        decode_kernel<64><<<grid, kThreads, smem, stream>>>(key_map, value_map, a);
-    else
-        decode_kernel<128><<<grid, kThreads, smem, stream>>>(key_map, value_map, a);
+    // Both kernels are launched with programmatic stream serialization: each
+    // may be scheduled before its predecessor in the stream has finished and
+    // waits for it (griddepcontrol.wait) before touching its data.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = a.D == 64 ? cudaLaunchKernelEx(&cfg, decode_kernel<64>, key_map, value_map, a)
+                              : cudaLaunchKernelEx(&cfg, decode_kernel<128>, key_map, value_map, a);
+    if (e != cudaSuccess || a.whole_segments)
+        return e;
+    cudaLaunchConfig_t mcfg = cfg;
+    mcfg.gridDim = dim3(unsigned(int64_t(a.B) * a.H_kv * a.MT));
+    mcfg.blockDim = dim3(128);
+    mcfg.dynamicSmemBytes = 0;
+    e = a.D == 64 ? cudaLaunchKernelEx(&mcfg, decode_merge_kernel<64>, a, grid)
+                  : cudaLaunchKernelEx(&mcfg, decode_merge_kernel<128>, a, grid);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 

@@ -72,11 +72,8 @@ extern "C" pa_status pa_decode_noalloc(const void* query, const void* key_pages,
     void* scratch = nullptr;
     if ((st = noalloc_scratch(&scratch)) != PA_OK)
         return st;
-    // The array keeps whatever the previous call left; the ticket words of
-    // this shape must start at zero.
-    const size_t tickets = size_t(pa::decode_segment_count(shape)) * sizeof(int32_t);
-    if (cudaMemsetAsync(scratch, 0, tickets, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return PA_ERR_CUDA;
+    // The array keeps whatever the previous call left; the decode reads only
+    // what it writes first, so nothing needs clearing.
     return pa_decode(query, key_pages, value_pages, block_table, context_lens, page_size, scale,
                      causal, out, shape, max_context_len, scratch, kNoAllocScratchBytes, stream);
 }

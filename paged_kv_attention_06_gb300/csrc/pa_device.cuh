@@ -151,10 +151,33 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// 2^x with the hardware approximation (ex2.approx.ftz.f32: relative error
+// about 2^-22, 2^-inf = +0).
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Programmatic dependent launch. wait: blocks until the grid this launch
+// depends on (the previous kernel in the stream) has completed and its
+// memory is visible; a kernel launched without the attribute returns at
+// once. launch_dependents: lets the next kernel in the stream be scheduled.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Named barrier among the first `threads` threads of the block.

@@ -43,16 +43,13 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 // Work decomposition: a "segment" is (request b, KV head h, tile mt of 16
 // query rows); its keys are cut into granules of kDecodeTokens tokens. All
 // granules of all segments form one stream that the grid splits evenly; a
-// segment that straddles blocks is merged by the last block to finish it.
+// segment that straddles blocks leaves one partial state per block, merged
+// by a second, small kernel.
 constexpr int kDecodeTokens = 64;
 constexpr int kDecodeRows = 16;
 
-// Workspace layout: a fixed 256 KiB counter region (one int32 ticket per
-// segment, at most kMaxSegments) followed by the partial-state slots. The
-// counter region does not depend on the shape, so partial states of one call
-// never land on counter words of another call that shares the workspace.
+// At most this many segments per call (request x KV head x 16-row tile).
 constexpr int64_t kMaxSegments = 65536;
-constexpr size_t kCounterRegionBytes = size_t(kMaxSegments) * 4;
 
 struct DecodeArgs {
     const uint16_t* q;            // [B, H_q, L, D]
@@ -60,7 +57,6 @@ struct DecodeArgs {
     const int32_t* block_table;   // [B, max_pages]
     const int32_t* context_lens;  // [B]
     float* partials;              // [slots][m[16], l[16], acc[16][D]]
-    int32_t* counters;            // [nseg]
     unsigned* err;
     int32_t B, H_q, H_kv, L, D, ps, max_pages, num_pages;
     int32_t G;          // H_q / H_kv

@@ -218,17 +218,22 @@ def test_decode_and_prefill_routes_agree():
     assert_close(pre, ref, "prefill")
 
 
-def test_workspace_reuse_is_deterministic():
+def test_workspace_contents_do_not_matter():
+    """Repeated calls are bit-identical, whatever the workspace held before
+    (the decode reads only partial states it wrote in the same call)."""
     import paged_kv_attention_06_gb300 as pa
     b = wl.make_workload("decode_b32_gqa7_ps16")
     db = DeviceBatch(b)
-    outs = [host_bits(gpu_step(db, route="decode", append=False)) for _ in range(3)]
-    check_no_device_error()
-    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    outs = [host_bits(gpu_step(db, route="decode", append=False)) for _ in range(2)]
     shape = pa.make_shape(db.query.shape, db.key_pages.shape, db.block_table.shape[1])
     ws, need = pa.decode_workspace(shape, db.query.device)
-    counters = ws[: 256 * 1024].view(torch.int32)
-    assert int(counters.abs().sum()) == 0      # the whole ticket region is left at zero
+    ws.fill_(0xFF)                              # NaN patterns everywhere
+    outs.append(host_bits(gpu_step(db, route="decode", append=False)))
+    ws.random_(0, 256)
+    outs.append(host_bits(gpu_step(db, route="decode", append=False)))
+    check_no_device_error()
+    for o in outs[1:]:
+        assert np.array_equal(outs[0], o)
 
 
 def test_non_default_stream():

@@ -175,6 +175,72 @@ pa_status encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pa_
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// 2-D bf16 tensor map over `rows` rows of 128 columns, boxes of 64 columns x
+// box_rows rows, 128-byte swizzle (used by the prefill kernel).
+pa_status encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    pa_status st = get_encoder(&enc);
+    if (st != PA_OK)
+        return st;
+    const cuuint64_t dims[2] = {128u, cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {256u};
+    const cuuint32_t box[2] = {64u, box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+// Prefill on tcgen05 (D = 128, page_size >= 8): one block per (request,
+// query head, tile of 128 query rows).
+pa_status run_prefill_tc(const void* query, const void* key_pages, const void* value_pages,
+                         const int32_t* block_table, const int32_t* context_lens,
+                         int32_t page_size, float scale, int causal, void* out,
+                         const pa_shape& s, cudaStream_t stream)
+{
+    DeviceInfo* dev;
+    pa_status st = device_info(&dev);
+    if (st != PA_OK)
+        return st;
+    if (prefill_smem_bytes() > size_t(dev->max_smem_optin))
+        return PA_ERR_UNSUPPORTED;
+    const int64_t n_qtiles = (int64_t(s.q_len) + 127) / 128;
+    const int64_t grid = int64_t(s.batch) * s.num_q_heads * n_qtiles;
+    const int64_t q_rows = int64_t(s.batch) * s.num_q_heads * s.q_len;
+    if (grid >= (int64_t(1) << 31) || q_rows >= (int64_t(1) << 31))
+        return PA_ERR_UNSUPPORTED;
+    const uint32_t box = uint32_t(page_size < 128 ? page_size : 128);
+    CUtensorMap qmap, kmap, vmap;
+    const uint64_t kv_rows = uint64_t(s.num_pages) * s.num_kv_heads * page_size;
+    if ((st = encode_rows_map(&qmap, query, uint64_t(q_rows), 128u)) != PA_OK ||
+        (st = encode_rows_map(&kmap, key_pages, kv_rows, box)) != PA_OK ||
+        (st = encode_rows_map(&vmap, value_pages, kv_rows, box)) != PA_OK)
+        return st;
+    PrefillArgs a;
+    memset(&a, 0, sizeof a);
+    a.out = static_cast<uint16_t*>(out);
+    a.block_table = block_table;
+    a.context_lens = context_lens;
+    a.err = dev->err;
+    a.B = s.batch;
+    a.H_q = s.num_q_heads;
+    a.H_kv = s.num_kv_heads;
+    a.L = s.q_len;
+    a.ps = page_size;
+    a.max_pages = s.max_pages;
+    a.num_pages = s.num_pages;
+    a.G = s.num_q_heads / s.num_kv_heads;
+    a.n_qtiles = int32_t(n_qtiles);
+    a.box_rows = int32_t(box);
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.causal = causal ? 1 : 0;
+    return launch_prefill(qmap, kmap, vmap, a, dev->id, stream) == cudaSuccess ? PA_OK
+                                                                            : PA_ERR_CUDA;
+}
+
 int64_t decode_segments(const pa_shape& s)
 {
     const int64_t G = s.num_q_heads / s.num_kv_heads;
@@ -363,6 +429,12 @@ pa_status pa_prefill(const void* query, const void* key_pages, const void* value
                                    page_size, scale, out, shape);
     if (st != PA_OK)
         return st;
+    if (shape.head_dim == 128 && page_size >= 8)
+        return run_prefill_tc(query, key_pages, value_pages, block_table, context_lens,
+                              page_size, scale, causal, out, shape,
+                              static_cast<cudaStream_t>(stream));
+    // D = 64 or pages smaller than 8 tokens: the split-KV kernel with whole
+    // segments per block.
     return run_split_kv(query, key_pages, value_pages, block_table, context_lens, page_size,
                         scale, causal, out, shape, 0, nullptr, 0, 1,
                         static_cast<cudaStream_t>(stream));

@@ -77,6 +77,27 @@ size_t decode_workspace_bytes(int64_t nseg, int grid_max, int D);
 cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_map,
                           const DecodeArgs& a, int grid, int device, cudaStream_t stream);
 
+// ---------------------------------------------------------------------------
+// Prefill on the 5th-generation tensor cores (D = 128, page_size >= 8)
+
+struct PrefillArgs {
+    uint16_t* out;                // [B, H_q, L, 128]
+    const int32_t* block_table;   // [B, max_pages]
+    const int32_t* context_lens;  // [B]
+    unsigned* err;
+    int32_t B, H_q, H_kv, L, ps, max_pages, num_pages;
+    int32_t G;          // H_q / H_kv
+    int32_t n_qtiles;   // ceil(L / 128)
+    int32_t box_rows;   // rows per K/V TMA box: min(ps, 128)
+    float scale_log2;
+    int32_t causal;
+};
+
+size_t prefill_smem_bytes();
+cudaError_t launch_prefill(const CUtensorMap& q_map, const CUtensorMap& key_map,
+                           const CUtensorMap& value_map, const PrefillArgs& a, int device,
+                           cudaStream_t stream);
+
 // Host-side checks of a decode call (everything pa_decode rejects before
 // launching, except the workspace), and its number of segments.
 pa_status validate_decode(const void* query, const void* key_pages, const void* value_pages,

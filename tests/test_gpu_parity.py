@@ -250,3 +250,57 @@ def test_non_default_stream():
     s.synchronize()
     kp, vp = oracle_pages(b)
     assert_close(host_f64(out), oracle_out(b, kp, vp), "stream")
+
+
+# ----------------------------------------------------------------------------
+# The tensor-core prefill path (head_dim 128, page_size >= 8) at its edges
+
+
+@pytest.mark.parametrize("ps", [8, 16, 64, 128, 256])
+@pytest.mark.parametrize("causal", [True, False])
+def test_tc_prefill_page_sizes(ps, causal):
+    lens = [200, 129, 513, 300]
+    b = wl.build_batch("tcprefill", B=4, H_q=8, H_kv=2, D=128, page_size=ps, L=129,
+                       context_lens=lens, seed=ps + int(causal), causal=causal,
+                       placement="churn")
+    out = gpu_step(DeviceBatch(b), route="prefill")
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), f"tc prefill ps={ps} causal={causal}")
+
+
+def test_tc_prefill_rows_without_keys_and_empty_context():
+    # L = 200 rows after contexts of 0, 50 and 199 tokens: rows at negative
+    # positions see no key and must return zeros.
+    b = wl.build_batch("tcempty", B=3, H_q=4, H_kv=4, D=128, page_size=16, L=200,
+                       context_lens=[0, 50, 199], seed=4, L_new=0)
+    out = host_f64(gpu_step(DeviceBatch(b), route="prefill"))
+    check_no_device_error()
+    assert np.all(out[0] == 0)
+    assert np.all(out[1, :, :150] == 0) and np.all(out[2, :, :1] == 0)
+    assert_close(out, oracle_out(b, b.key_pages, b.value_pages), "tc prefill empty rows")
+
+
+def test_tc_prefill_bad_page_id_is_flagged():
+    import dataclasses
+    import paged_kv_attention_06_gb300 as pa
+    b = wl.build_batch("tcbad", B=2, H_q=4, H_kv=2, D=128, page_size=16, L=32,
+                       context_lens=[100, 40], seed=8, L_new=0)
+    bt = b.block_table.copy()
+    bt[0, 2] = b.num_pages + 7
+    gpu_step(DeviceBatch(dataclasses.replace(b, block_table=bt)), route="prefill")
+    st, flags = pa.pa_get_device_error()
+    assert st == pa.PA_ERR_DEVICE_BOUNDS and flags & pa.PA_DEVERR_PAGE_ID
+
+
+def test_tc_prefill_long_context_gqa():
+    b = wl.build_batch("tclong", B=2, H_q=16, H_kv=2, D=128, page_size=16, L=384,
+                       context_lens=[3000, 1500], seed=12, placement="permutation")
+    db = DeviceBatch(b)
+    out = gpu_step(db, route="prefill")
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    rows = np.asarray([(r, h, i) for r in range(2) for h in range(16)
+                       for i in (0, 1, 127, 128, 255, 256, 383)], dtype=np.int32)
+    got = host_f64(out)[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(got, oracle_out(b, kp, vp, rows=rows), "tc prefill long")

@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         row_b = row;
                 }
             }
-            const bool ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, misc, a.err);
+            const bool ok = mbar_wait_warp(&empty[stage], phase ^ 1u, misc, a.err);
             if (ok && nbox > 0) {
                 const uint32_t bytes = uint32_t(nbox) * box * 128u * Lay::kHalves * 2u;
                 if (lane == 0)
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (; x < piece_end; ++x) {
             const int t0 = int(x - sp.seg_start) * kDecodeTokens;
             const int nvalid = min(kDecodeTokens, n - t0);
-            const bool ok = mbar_wait_bounded(&full[stage], phase, misc, a.err);
+            const bool ok = mbar_wait_warp(&full[stage], phase, misc, a.err);
             bool wrote = false;
             if (ok && nvalid > 0) {
                 if (nvalid < kDecodeTokens) {

@@ -89,6 +89,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// The same wait for a whole warp; the result is the same in every lane, so
+// it can gate warp-collective code.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort_flag, unsigned* err)
+{
+    const bool ok = mbar_wait_bounded(bar, parity, abort_flag, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) accesses of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -113,6 +122,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 

@@ -10,9 +10,12 @@
 //
 // Schedule (one block per (request, query head, tile of 128 query rows);
 // the tiles with the most keys are launched first):
-//   * warp 0 (producer): TMA loads of the Q tile (128 x 128, once) and of
-//     K/V tiles of 128 keys, page by page (one box of min(page_size, 128)
-//     rows x 64 columns per page and half), 128-byte swizzle, two stages;
+//   * warps 0, 2, 3 (loaders): TMA loads of the Q tile (128 x 128, once)
+//     and of K and V tiles of 128 keys, page by page (one box of
+//     min(page_size, 128) rows x 64 columns per page and half, the boxes of a
+//     tile split over the three warps), 128-byte swizzle, two K and two V
+//     stages released separately (a K stage as soon as its scores are
+//     computed);
 //   * warp 1 (one thread): tcgen05.mma kind::f16 (bf16 in, fp32 accumulate)
 //     S = Q K^T into one of two TMEM score buffers, then O += P V into the
 //     TMEM output accumulator, completion signalled by tcgen05.commit;
@@ -58,8 +61,8 @@ struct Layout {
     static constexpr int kBytes = kMisc + 16 + 1024;  // + alignment slack
 };
 
-enum Bar { kQFull = 0, kKVFull0 = 1, kKVEmpty0 = 3, kSFull0 = 5, kSFree0 = 7, kPFull = 9,
-           kPVDone = 10, kMmaDone = 11 };
+enum Bar { kQFull = 0, kKFull0 = 1, kKEmpty0 = 3, kVFull0 = 5, kVEmpty0 = 7, kSFull0 = 9,
+           kSFree0 = 11, kPFull = 13, kPVDone = 14, kMmaDone = 15 };
 
 // K-major bf16 operand tile stored as [half][128 rows][128 B], 128B swizzle:
 // descriptor of k-step kk (16 elements along K).
@@ -121,8 +124,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         misc[0] = 0;
         mbar_init(&bar[kQFull], 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&bar[kKVFull0 + s], 1);
-            mbar_init(&bar[kKVEmpty0 + s], 1);
+            mbar_init(&bar[kKFull0 + s], 3);   // one arrival per loader warp
+            mbar_init(&bar[kKEmpty0 + s], 1);
+            mbar_init(&bar[kVFull0 + s], 3);
+            mbar_init(&bar[kVEmpty0 + s], 1);
             mbar_init(&bar[kSFull0 + s], 1);
             mbar_init(&bar[kSFree0 + s], 4);
         }
@@ -140,10 +145,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && nt > 0) {
-        // ===================== producer: Q once, then K/V page by page =====
-        const uint64_t policy = l2_policy_evict_first();
-        if (lane == 0) {
+    if ((warp == 0 || warp == 2 || warp == 3) && nt > 0) {
+        // ===================== loaders: Q once (warp 0), then K and V page
+        // by page. A tile's page boxes are split over the three loader warps
+        // (box b to loader b mod 3), each arriving on the stage barrier with
+        // its own byte count: issuing many small boxes is bound by the
+        // issuing warp, so three warps issue them three times faster.
+        const int li = warp == 0 ? 0 : warp - 1;  // 0, 1, 2
+        // K/V tiles are read again by the other query tiles and heads of the
+        // same request and KV group: keep them in L2.
+        const uint64_t policy = l2_policy_evict_last();
+        if (lane == 0 && li == 0) {
             prefetch_tensormap(&q_map);
             prefetch_tensormap(&key_map);
             prefetch_tensormap(&value_map);
@@ -154,44 +166,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int box = a.box_rows;
         const int32_t* bt = a.block_table + int64_t(b) * a.max_pages;
-        for (int j = 0; j < nt; ++j) {
-            const int s = j & 1;
+        const int my_box = li + 3 * lane;              // this lane's box of a tile
+        auto n_boxes = [&](int j) {
             const int key0 = j * kTile;
-            const int kend = min(n, key0 + kTile);
-            const int nbox = (kend - key0 + box - 1) / box;
-            int row = 0;
-            if (lane < nbox) {
-                const int tok = key0 + lane * box;
-                const int lp = tok / a.ps;
-                int phys = bt[lp];
-                if (unsigned(phys) >= unsigned(a.num_pages)) {
-                    atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
-                    phys = 0;
-                }
-                row = (phys * a.H_kv + hk) * a.ps + (tok - lp * a.ps);
+            return (min(n, key0 + kTile) - key0 + box - 1) / box;
+        };
+        // Raw block-table entry of this lane's box in tile j (loaded ahead of
+        // use, so the load latency overlaps the waits; checked at use).
+        auto fetch_page = [&](int j) -> int {
+            if (j >= nt || my_box >= n_boxes(j))
+                return 0;
+            return bt[(j * kTile + my_box * box) / a.ps];
+        };
+        auto pool_row = [&](int j, int phys) -> int {
+            if (unsigned(phys) >= unsigned(a.num_pages)) {
+                atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
+                phys = 0;
             }
-            const bool ok = mbar_wait_bounded(&bar[kKVEmpty0 + s], ((j >> 1) & 1) ^ 1u, misc, a.err);
+            const int tok = j * kTile + my_box * box;
+            return (phys * a.H_kv + hk) * a.ps + (tok - (tok / a.ps) * a.ps);
+        };
+        // This warp's part of tile j's K (is_v = false) or V.
+        auto load = [&](int j, bool is_v, int phys) {
+            const int nbox = n_boxes(j);
+            const int mine = nbox > li ? (nbox - li + 2) / 3 : 0;  // boxes of this warp
+            const int s = j & 1;
+            const int full = (is_v ? kVFull0 : kKFull0) + s;
+            const int empty = (is_v ? kVEmpty0 : kKEmpty0) + s;
+            const bool ok = mbar_wait_warp(&bar[empty], ((j >> 1) & 1) ^ 1u, misc, a.err);
             if (ok) {
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&bar[kKVFull0 + s], uint32_t(nbox) * box * 128u * 4u);
+                    mbar_arrive_expect_tx(&bar[full], uint32_t(mine) * box * 128u * 2u);
                 __syncwarp();
-                if (lane < nbox) {
-                    const int dst = lane * box * 128;
-                    uint8_t* kd = smem + Layout::kK + s * Layout::kMat + dst;
-                    uint8_t* vd = smem + Layout::kV + s * Layout::kMat + dst;
-                    tma_load_2d(kd, &key_map, 0, row, &bar[kKVFull0 + s], policy);
-                    tma_load_2d(kd + Layout::kHalf, &key_map, 64, row, &bar[kKVFull0 + s], policy);
-                    tma_load_2d(vd, &value_map, 0, row, &bar[kKVFull0 + s], policy);
-                    tma_load_2d(vd + Layout::kHalf, &value_map, 64, row, &bar[kKVFull0 + s], policy);
+                if (my_box < nbox) {
+                    const int row = pool_row(j, phys);
+                    uint8_t* d = smem + (is_v ? Layout::kV : Layout::kK) + s * Layout::kMat +
+                                 my_box * box * 128;
+                    const CUtensorMap* m = is_v ? &value_map : &key_map;
+                    tma_load_2d(d, m, 0, row, &bar[full], policy);
+                    tma_load_2d(d + Layout::kHalf, m, 64, row, &bar[full], policy);
                 }
             }
             __syncwarp();
+        };
+        // Order of need: S_j = Q K_j^T is issued before P_{j-1} V_{j-1}, so
+        // the loads go K_0, K_1, V_0, K_2, V_1, ...; a K stage is free again
+        // as soon as its S is computed, a V stage once its P V is. Page ids
+        // are fetched two tiles ahead.
+        int page_j = fetch_page(0);
+        int page_j1 = fetch_page(1);
+        load(0, false, page_j);
+        for (int j = 0; j < nt; ++j) {
+            const int page_j2 = fetch_page(j + 2);
+            if (j + 1 < nt)
+                load(j + 1, false, page_j1);
+            load(j, true, page_j);
+            page_j = page_j1;
+            page_j1 = page_j2;
         }
         // No copy may still be landing when the block exits: the last (up to)
-        // two stages' phases have completed once the MMA thread consumed
-        // them; wait for them again (bounded) in case it gave up.
-        for (int j = max(0, nt - 2); j < nt; ++j)
-            mbar_wait_bounded(&bar[kKVFull0 + (j & 1)], (j >> 1) & 1, misc, a.err);
+        // two stages' phases have completed once they were consumed; wait for
+        // them again (bounded) in case a consumer gave up.
+        for (int j = max(0, nt - 2); j < nt; ++j) {
+            mbar_wait_bounded(&bar[kKFull0 + (j & 1)], (j >> 1) & 1, misc, a.err);
+            mbar_wait_bounded(&bar[kVFull0 + (j & 1)], (j >> 1) & 1, misc, a.err);
+        }
     } else if (warp == 1 && nt > 0) {
         // ===================== MMA issue (one thread) ======================
         if (lane == 0) {
@@ -202,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j <= nt && ok; ++j) {
                 if (j < nt) {
                     const int s = j & 1;
-                    ok = mbar_wait_bounded(&bar[kKVFull0 + s], (j >> 1) & 1, misc, a.err);
+                    ok = mbar_wait_bounded(&bar[kKFull0 + s], (j >> 1) & 1, misc, a.err);
                     if (ok && j >= 2)
                         ok = mbar_wait_bounded(&bar[kSFree0 + s], ((j - 2) >> 1) & 1, misc, a.err);
                     if (!ok)
@@ -214,11 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < 8; ++kk)
                         tc_mma_bf16(d, kmajor_desc(sQ, kk), kmajor_desc(kb, kk), idesc_s, kk > 0);
                     tc_commit(&bar[kSFull0 + s]);
+                    tc_commit(&bar[kKEmpty0 + s]);
                 }
                 if (j >= 1) {
                     const int jp = j - 1;
                     const int sp = jp & 1;
                     ok = mbar_wait_bounded(&bar[kPFull], jp & 1, misc, a.err);
+                    if (ok)
+                        ok = mbar_wait_bounded(&bar[kVFull0 + sp], (jp >> 1) & 1, misc, a.err);
                     if (!ok)
                         break;
                     tc_fence_after();
@@ -228,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma_bf16(tmem + kColO, kmajor_desc(sP, kk), mnmajor_desc(vb, kk),
                                     idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(&bar[kPVDone]);
-                    tc_commit(&bar[kKVEmpty0 + sp]);
+                    tc_commit(&bar[kVEmpty0 + sp]);
                 }
             }
             // Every MMA this thread issued completes before the block ends.
@@ -251,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         for (int j = 0; j < nt; ++j) {
             const int sb = j & 1;
-            const bool ok = mbar_wait_bounded(&bar[kSFull0 + sb], (j >> 1) & 1, misc, a.err);
+            const bool ok = mbar_wait_warp(&bar[kSFull0 + sb], (j >> 1) & 1, misc, a.err);
             tc_fence_after();
             uint32_t sv[128];
 #pragma unroll
@@ -270,10 +312,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (key0 + k > lim)
                         s[k] = -INFINITY;
             }
-            float mx = -INFINITY;
+            float m8[8];
 #pragma unroll
-            for (int k = 0; k < kTile; ++k)
-                mx = fmaxf(mx, s[k]);
+            for (int u = 0; u < 8; ++u)
+                m8[u] = s[u];
+#pragma unroll
+            for (int k = 8; k < kTile; k += 8)
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    m8[u] = fmaxf(m8[u], s[k + u]);
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             const float mxs = mx * c;
             const bool need = mxs > m_used + kRescaleLog2 || (m_used == -INFINITY && mxs > -INFINITY);
             float factor = 1.f;
@@ -321,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // V rows past the context hold stale bytes: zero them (P is 0
             // there, but 0 * NaN is not).
             if (n < key0 + kTile) {
+                mbar_wait_bounded(&bar[kVFull0 + sb], (j >> 1) & 1, misc, a.err);  // V_j landed
                 const int z0 = max(0, n - key0);
                 const int nz = (kTile - z0) * 16;   // 16-byte chunks
                 uint8_t* vb = smem + Layout::kV + sb * Layout::kMat;

@@ -212,6 +212,18 @@ const char *pa_version(void);
  */
 void pa_debug_arm_wait_timeout(void);
 
+/*
+ * Test and tuning support: which tensor-core prefill kernel the calling host
+ * thread's pa_prefill / pa_attention calls use (head_dim 128, page_size >= 8).
+ *   0  automatic (the default): as 2;
+ *   1  one query head per block;
+ *   2  two query heads of one KV group per block, when the group size
+ *      (num_q_heads / num_kv_heads) is even; otherwise as 1.
+ * Any other value is taken as 0. Returns the previous setting. Results agree
+ * with the oracle under every setting; only the speed differs.
+ */
+int pa_debug_prefill_variant(int variant);
+
 #ifdef __cplusplus
 }
 #endif

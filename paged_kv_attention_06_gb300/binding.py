@@ -74,6 +74,8 @@ def _load() -> ctypes.CDLL:
     lib.pa_version.restype = ctypes.c_char_p
     lib.pa_debug_arm_wait_timeout.argtypes = []
     lib.pa_debug_arm_wait_timeout.restype = None
+    lib.pa_debug_prefill_variant.argtypes = [ctypes.c_int]
+    lib.pa_debug_prefill_variant.restype = ctypes.c_int
     return lib
 
 
@@ -283,3 +285,10 @@ def pa_decode_noalloc(query, key_pages, value_pages, block_table, context_lens,
                                 int(max_context_len), _stream(stream))
     _check(st, "pa_decode_noalloc")
     return out
+
+
+def pa_debug_prefill_variant(variant: int) -> int:
+    """Select the tensor-core prefill kernel for this thread's calls: 0 auto,
+    1 one query head per block, 2 two heads of a KV group per block (even
+    group size). Returns the previous setting."""
+    return int(_lib.pa_debug_prefill_variant(int(variant)))

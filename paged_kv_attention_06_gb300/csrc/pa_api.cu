@@ -33,6 +33,7 @@ struct DeviceInfo {
 
 std::mutex g_mutex;
 thread_local bool t_arm_unset_wait = false;  // test support, see pa_debug_arm_wait_timeout
+thread_local int t_prefill_variant = 0;      // see pa_debug_prefill_variant
 DeviceInfo g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -205,7 +206,12 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     pa_status st = device_info(&dev);
     if (st != PA_OK)
         return st;
-    if (prefill_smem_bytes() > size_t(dev->max_smem_optin))
+    // Two query heads of one KV group per block whenever the group size is
+    // even (unless the one-head kernel is requested).
+    bool pairs = t_prefill_variant != 1 && (s.num_q_heads / s.num_kv_heads) % 2 == 0;
+    if (pairs && prefill_pairs_smem_bytes() > size_t(dev->max_smem_optin))
+        pairs = false;
+    if (!pairs && prefill_smem_bytes() > size_t(dev->max_smem_optin))
         return PA_ERR_UNSUPPORTED;
     const int64_t n_qtiles = (int64_t(s.q_len) + 127) / 128;
     const int64_t grid = int64_t(s.batch) * s.num_q_heads * n_qtiles;
@@ -237,8 +243,11 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     a.box_rows = int32_t(box);
     a.scale_log2 = scale * 1.4426950408889634f;
     a.causal = causal ? 1 : 0;
-    return launch_prefill(qmap, kmap, vmap, a, dev->id, stream) == cudaSuccess ? PA_OK
-                                                                            : PA_ERR_CUDA;
+    cudaError_t e = pairs ? launch_prefill_pairs(qmap, kmap, vmap, a, dev->id, stream)
+                          : launch_prefill(qmap, kmap, vmap, a, dev->id, stream);
+    if (pairs && e == cudaErrorNotSupported)   // register split not available: one head per block
+        e = launch_prefill(qmap, kmap, vmap, a, dev->id, stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int64_t decode_segments(const pa_shape& s)
@@ -503,5 +512,12 @@ const char* pa_status_string(pa_status status)
 const char* pa_version(void) { return "0.1.0"; }
 
 void pa_debug_arm_wait_timeout(void) { t_arm_unset_wait = true; }
+
+int pa_debug_prefill_variant(int variant)
+{
+    const int prev = t_prefill_variant;
+    t_prefill_variant = (variant == 1 || variant == 2) ? variant : 0;
+    return prev;
+}
 
 }  // extern "C"

@@ -89,6 +89,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// mbar_wait_bounded with the waiting loop marked unlikely, so that the
+// common case of a thread whose every wait delays the tensor core (the MMA
+// issuer), a phase that has already completed, stays one try_wait and a
+// branch (the loop's set-up otherwise costs several times that per call).
+__device__ __forceinline__ bool mbar_wait_lean(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort_flag, unsigned* err)
+{
+    if (__builtin_expect(mbar_try_wait(bar, parity), 1))
+        return true;
+    const uint64_t limit = *abort_flag ? kShortWaitLimitNs : kWaitLimitNs;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((i & 15u) == 0 && global_timer_ns() - t0 > limit) {
+            if (!*abort_flag) {
+                *abort_flag = 1;
+                atomicOr(err, PA_DEVERR_TIMEOUT_BIT);
+            }
+            return false;
+        }
+    }
+}
+
 // The same wait for a whole warp; the result is the same in every lane, so
 // it can gate warp-collective code.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,

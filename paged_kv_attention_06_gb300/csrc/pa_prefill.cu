@@ -17,16 +17,19 @@
 //     stages released separately (a K stage as soon as its scores are
 //     computed);
 //   * warp 1 (one thread): tcgen05.mma kind::f16 (bf16 in, fp32 accumulate)
-//     S = Q K^T into one of two TMEM score buffers, then O += P V into the
-//     TMEM output accumulator, completion signalled by tcgen05.commit;
+//     S = Q K^T into one of two TMEM score buffers, then O += P V (P from
+//     TMEM) into the TMEM output accumulator, completion signalled by
+//     tcgen05.commit; a score buffer is reused once its P V is done;
 //   * warps 4-7 (one thread per row, TMEM lanes 0..127): the online-softmax
 //     fold. Scores are masked by select (never multiplied), kept in the log2
 //     domain; the running maximum used for the exponentials moves only when
 //     a tile's maximum exceeds it by more than 2^8, in which case O (TMEM)
 //     and the running sum are rescaled (the result is the same softmax:
-//     exponentials of a stale maximum stay below 2^8). P (bf16) goes to
-//     shared memory in the swizzled K-major layout the second MMA reads. V
-//     rows past the context are zeroed before P V. At the end, O / l -> bf16.
+//     exponentials of a stale maximum stay below 2^8). P (bf16) is written
+//     back into the tile's score buffer in TMEM and read from there as the A
+//     operand of P V, so it never crosses shared memory (whose bandwidth the
+//     MMAs and the TMA copies already share). V rows past the context are
+//     zeroed before P V. At the end, O / l -> bf16.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -54,29 +57,28 @@ struct Layout {
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kMat;        // 2 stages
     static constexpr int kV = kK + 2 * kMat;    // 2 stages
-    static constexpr int kP = kV + 2 * kMat;
-    static constexpr int kBar = kP + kMat;      // 16 mbarriers
+    static constexpr int kBar = kV + 2 * kMat;  // 16 mbarriers
     static constexpr int kTmemSlot = kBar + 16 * 8;
     static constexpr int kMisc = kTmemSlot + 16;
     static constexpr int kBytes = kMisc + 16 + 1024;  // + alignment slack
 };
 
 enum Bar { kQFull = 0, kKFull0 = 1, kKEmpty0 = 3, kVFull0 = 5, kVEmpty0 = 7, kSFull0 = 9,
-           kSFree0 = 11, kPFull = 13, kPVDone = 14, kMmaDone = 15 };
+           kPFull = 11, kPVDone = 12, kMmaDone = 13 };
 
-// K-major bf16 operand tile stored as [half][128 rows][128 B], 128B swizzle:
-// descriptor of k-step kk (16 elements along K).
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk)
+// Operand descriptors (128B swizzle). K-major [half][128 rows][128 B] (Q, K):
+// k-step kk (16 elements along K) starts kmajor_off(kk) bytes in. MN-major
+// (V: rows = keys, 128 B of columns per row, two 64-column halves): k-step kk
+// (16 keys) starts 16 rows in.
+__host__ __device__ constexpr uint32_t kmajor_off(int kk)
 {
-    return smem_desc_sw128(base + uint32_t(kk >> 2) * Layout::kHalf + uint32_t(kk & 3) * 32u,
-                           16u, 1024u);
+    return uint32_t(kk >> 2) * Layout::kHalf + uint32_t(kk & 3) * 32u;
 }
-
-// MN-major bf16 operand (V: rows = keys (K), 128 B of columns (N) per row,
-// two 64-column halves): descriptor of k-step kk (16 keys).
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk)
+__host__ __device__ constexpr uint32_t mnmajor_off(int kk) { return uint32_t(kk) * 16u * 128u; }
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t saddr) { return smem_desc_sw128(saddr, 16u, 1024u); }
+__device__ __forceinline__ uint64_t mnmajor_base(uint32_t saddr)
 {
-    return smem_desc_sw128(base + uint32_t(kk) * 16u * 128u, uint32_t(Layout::kHalf), 1024u);
+    return smem_desc_sw128(saddr, uint32_t(Layout::kHalf), 1024u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -118,7 +120,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = smem_u32(smem + Layout::kQ);
     const uint32_t sK = smem_u32(smem + Layout::kK);
     const uint32_t sV = smem_u32(smem + Layout::kV);
-    const uint32_t sP = smem_u32(smem + Layout::kP);
 
     if (threadIdx.x == 0) {
         misc[0] = 0;
@@ -129,7 +130,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar[kVFull0 + s], 3);
             mbar_init(&bar[kVEmpty0 + s], 1);
             mbar_init(&bar[kSFull0 + s], 1);
-            mbar_init(&bar[kSFree0 + s], 4);
         }
         mbar_init(&bar[kPFull], 4);
         mbar_init(&bar[kPVDone], 1);
@@ -173,10 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // Raw block-table entry of this lane's box in tile j (loaded ahead of
         // use, so the load latency overlaps the waits; checked at use).
+        // The load is unconditional (index clamped to entry 0 when the box
+        // does not exist) so that nothing waits for its result before use.
         auto fetch_page = [&](int j) -> int {
-            if (j >= nt || my_box >= n_boxes(j))
-                return 0;
-            return bt[(j * kTile + my_box * box) / a.ps];
+            const bool live = j < nt && my_box < n_boxes(j);
+            return bt[live ? (j * kTile + my_box * box) / a.ps : 0];
         };
         auto pool_row = [&](int j, int phys) -> int {
             if (unsigned(phys) >= unsigned(a.num_pages)) {
@@ -213,16 +214,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the loads go K_0, K_1, V_0, K_2, V_1, ...; a K stage is free again
         // as soon as its S is computed, a V stage once its P V is. Page ids
         // are fetched two tiles ahead.
-        int page_j = fetch_page(0);
-        int page_j1 = fetch_page(1);
-        load(0, false, page_j);
-        for (int j = 0; j < nt; ++j) {
-            const int page_j2 = fetch_page(j + 2);
-            if (j + 1 < nt)
-                load(j + 1, false, page_j1);
-            load(j, true, page_j);
-            page_j = page_j1;
-            page_j1 = page_j2;
+        // Page ids two tiles ahead in a ring of three registers (slot = tile
+        // mod 3). The loop is unrolled over the ring so that no pending load
+        // result is ever copied (a copy would wait for the load).
+        int pg[3];
+        pg[0] = fetch_page(0);
+        pg[1] = fetch_page(1);
+        load(0, false, pg[0]);
+        for (int j0 = 0; j0 < nt; j0 += 3) {
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+                const int j = j0 + u;
+                if (j < nt) {
+                    pg[(u + 2) % 3] = fetch_page(j + 2);
+                    if (j + 1 < nt)
+                        load(j + 1, false, pg[(u + 1) % 3]);
+                    load(j, true, pg[u]);
+                }
+            }
         }
         // No copy may still be landing when the block exits: the last (up to)
         // two stages' phases have completed once they were consumed; wait for
@@ -236,22 +245,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0);
             const uint32_t idesc_pv = idesc_bf16_f32(kTile, 128, 1);
+            // Base descriptors built once; every k-step is one add.
+            const uint64_t dq = kmajor_base(sQ);
+            const uint64_t dk0 = kmajor_base(sK), dk1 = desc_advance(dk0, Layout::kMat);
+            const uint64_t dv0 = mnmajor_base(sV), dv1 = desc_advance(dv0, Layout::kMat);
             bool ok = mbar_wait_bounded(&bar[kQFull], 0, misc, a.err);
             tc_fence_after();
             for (int j = 0; j <= nt && ok; ++j) {
                 if (j < nt) {
                     const int s = j & 1;
                     ok = mbar_wait_bounded(&bar[kKFull0 + s], (j >> 1) & 1, misc, a.err);
+                    // The buffer S_j overwrites holds P_{j-2} until P_{j-2} V is done.
                     if (ok && j >= 2)
-                        ok = mbar_wait_bounded(&bar[kSFree0 + s], ((j - 2) >> 1) & 1, misc, a.err);
+                        ok = mbar_wait_bounded(&bar[kPVDone], (j - 2) & 1, misc, a.err);
                     if (!ok)
                         break;
                     tc_fence_after();
                     const uint32_t d = tmem + (s ? kColS1 : kColS0);
-                    const uint32_t kb = sK + uint32_t(s) * Layout::kMat;
+                    const uint64_t db = s ? dk1 : dk0;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        tc_mma_bf16(d, kmajor_desc(sQ, kk), kmajor_desc(kb, kk), idesc_s, kk > 0);
+                        tc_mma_bf16(d, desc_advance(dq, kmajor_off(kk)),
+                                    desc_advance(db, kmajor_off(kk)), idesc_s, kk > 0);
                     tc_commit(&bar[kSFull0 + s]);
                     tc_commit(&bar[kKEmpty0 + s]);
                 }
@@ -264,11 +279,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok)
                         break;
                     tc_fence_after();
-                    const uint32_t vb = sV + uint32_t(sp) * Layout::kMat;
+                    const uint64_t db = sp ? dv1 : dv0;
+                    const uint32_t pcol = tmem + (sp ? kColS1 : kColS0);  // P_jp in TMEM
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        tc_mma_bf16(tmem + kColO, kmajor_desc(sP, kk), mnmajor_desc(vb, kk),
-                                    idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma_bf16_ts(tmem + kColO, pcol + 8u * kk, desc_advance(db, mnmajor_off(kk)),
+                                       idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(&bar[kPVDone]);
                     tc_commit(&bar[kVEmpty0 + sp]);
                 }
@@ -300,10 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q4 = 0; q4 < 4; ++q4)
                 tmem_ld32(trow + (sb ? kColS1 : kColS0) + 32u * q4, sv + 32 * q4);
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bar[kSFree0 + sb]);
             float* s = reinterpret_cast<float*>(sv);
             const int key0 = j * kTile;
             if (key0 + kTile - 1 > lim) {
@@ -341,9 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[k] = pack_bf16x2(p0, p1);
             }
             // P buffer and O are free once the previous P V has completed.
-            bool ok2 = true;
             if (j >= 1)
-                ok2 = mbar_wait_bounded(&bar[kPVDone], (j - 1) & 1, misc, a.err);
+                mbar_wait_bounded(&bar[kPVDone], (j - 1) & 1, misc, a.err);
             if (j >= 1 && __any_sync(0xffffffffu, need)) {
                 tc_fence_after();
 #pragma unroll
@@ -358,15 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
             }
-            // P row r -> shared memory, K-major [key half][row][128 B], chunk
-            // c of the row at c ^ (r & 7).
-#pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                uint8_t* dst = smem + Layout::kP + (ch >> 3) * Layout::kHalf + r * 128 +
-                               (((ch & 7) ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4*>(dst) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            }
+            // P row r (bf16, two per 32-bit column) over the first 64 columns of
+            // this tile's score buffer: the A operand of P V, read from TMEM.
+            tmem_st32(trow + (sb ? kColS1 : kColS0), pk);
+            tmem_st32(trow + (sb ? kColS1 : kColS0) + 32u, pk + 32);
+            tmem_wait_st();
             // V rows past the context hold stale bytes: zero them (P is 0
             // there, but 0 * NaN is not).
             if (n < key0 + kTile) {
@@ -386,7 +393,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0)
                 mbar_arrive(&bar[kPFull]);
             (void)ok;
-            (void)ok2;
         }
         // ---- epilogue: O / l -> bf16 --------------------------------------
         const float inv = l > 0.f ? 1.f / l : 0.f;

@@ -1,0 +1,553 @@
+// Causal page-walking prefill attention on the 5th-generation tensor cores,
+// two query heads of one KV group per block.
+//
+// Computes the same as the one-head prefill kernel: for request b, query
+// head h_q and query rows i in [0, L) (absolute position n_b - L + i),
+// softmax(scale * q . K^T + causal mask) . V over keys 0..position, K/V
+// resolved page by page through block_table (Week 3 Day 4: Direct Paged
+// Attention, "Task 2"; the heads of a KV group share every K/V tile, the
+// grouped-query schedule of "Checkpoint 2").
+//
+// Why two heads: with one 128-row query tile per block, the tensor core
+// waits for the softmax of every tile (one warp per SM sub-partition does
+// the exponentials of a whole tile). Two heads see exactly the same keys, so
+// one K/V tile serves two independent 128-row score tiles, and the MMAs of
+// one head run while the other head's softmax works.
+//
+// Schedule (one block per (request, pair of query heads of one KV group,
+// tile of 128 query rows), tiles with the most keys launched first):
+//   * warps 0, 2, 3 (loaders): TMA loads of both Q tiles (once) and of K and
+//     V tiles of 128 keys page by page (one box of min(page_size, 128) rows x
+//     64 columns per page and half, the boxes split over the three warps),
+//     two K and two V stages released separately;
+//   * warp 1 (one thread): tcgen05.mma kind::f16, M = 128, fp32 accumulate:
+//     S_h = Q_h K^T (N = 128 keys; an N = 64 MMA takes as long as N = 128)
+//     into head h's score buffer in TMEM, and O_h += P_h V (N = 128 =
+//     head_dim) with P_h read from TMEM. An MMA issue returns only about as
+//     fast as the tensor core executes it, so every wait of this thread is
+//     time the tensor core idles; the order per tile j is P_0 V_j, S_0 for
+//     tile j + 1, P_1 V_j, S_1 for tile j + 1;
+//   * warps 4-7 (head 0) and 8-11 (head 1): one thread per query row (TMEM
+//     lane), the online-softmax fold with a lazily moved maximum (O and the
+//     running sum are rescaled only when a tile's maximum exceeds the one in
+//     use by more than 2^8; exponentials of a stale maximum stay below 2^8,
+//     so the result is the same softmax). P (bf16, two per 32-bit column) is
+//     written over the upper 64 columns of the head's score buffer. V rows
+//     past the context are zeroed (by head 0's warps) before either P V. At
+//     the end O / l -> bf16.
+//
+// TMEM (512 columns): S_0 [0, 128), S_1 [128, 256), O_0 [256, 384),
+// O_1 [384, 512). A score buffer holds P_h(j) until P_h(j) V_j completes;
+// S_h(j + 1) is issued only after that completion has been observed, and
+// its commit also covers P_h(j) V_j, so a softmax thread that sees S_h(j + 1)
+// may rescale O_h without another wait.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kRows = 128;            // query rows per head and block
+constexpr int kKeys = 128;            // keys per K/V tile
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.f;
+constexpr int kRegsProducer = 128;     // per thread, warps 0-3 after the split
+constexpr int kRegsSoftmax = 184;     // per thread, warps 4-11 after the split
+static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= 65536, "register split");
+
+__host__ __device__ constexpr uint32_t col_s(int head) { return uint32_t(head * 128); }
+__host__ __device__ constexpr uint32_t col_o(int head) { return uint32_t(256 + head * 128); }
+constexpr uint32_t kPCol = 64;        // P_h: columns [64, 128) of head h's score buffer
+
+struct Layout {
+    static constexpr int kHalf = 128 * 128;        // 128 rows x 64 bf16 (128 B)
+    static constexpr int kMat = 2 * kHalf;         // 128 x 128 bf16, [half][row][128 B]
+    static constexpr int kQ = 0;                   // [head] matrices
+    static constexpr int kK = kQ + 2 * kMat;       // 2 stages
+    static constexpr int kV = kK + 2 * kMat;       // 2 stages
+    static constexpr int kBar = kV + 2 * kMat;
+    static constexpr int kNumBars = 16;
+    static constexpr int kTmemSlot = kBar + kNumBars * 8;
+    static constexpr int kMisc = kTmemSlot + 16;
+    static constexpr int kBytes = kMisc + 16 + 1024;   // + alignment slack
+};
+
+// Barrier indices.
+constexpr int kQFull = 0;
+constexpr int kKFull = 1;     // + stage (2)
+constexpr int kKEmpty = 3;    // + stage
+constexpr int kVFull = 5;     // + stage
+constexpr int kVEmpty = 7;    // + stage
+constexpr int kSFull = 9;     // + head (2)
+constexpr int kPFull = 11;    // + head
+constexpr int kPVDone = 13;   // + head
+constexpr int kMmaDone = 15;
+
+// Operand descriptors (128B swizzle). K-major [half][128 rows][128 B] (Q, K):
+// k-step kk (16 elements along K) starts kmajor_off(kk) bytes in. MN-major
+// [d half][128 keys][128 B] (V): k-step kk (16 keys) starts 16 rows in.
+__host__ __device__ constexpr uint32_t kmajor_off(int kk)
+{
+    return uint32_t(kk >> 2) * Layout::kHalf + uint32_t(kk & 3) * 32u;
+}
+__host__ __device__ constexpr uint32_t mnmajor_off(int kk) { return uint32_t(kk) * 16u * 128u; }
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t saddr) { return smem_desc_sw128(saddr, 16u, 1024u); }
+__device__ __forceinline__ uint64_t mnmajor_base(uint32_t saddr)
+{
+    return smem_desc_sw128(saddr, uint32_t(Layout::kHalf), 1024u);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_pairs_kernel(const __grid_constant__ CUtensorMap q_map,
+                         const __grid_constant__ CUtensorMap key_map,
+                         const __grid_constant__ CUtensorMap value_map, const PrefillArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Layout::kBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Layout::kTmemSlot);
+    volatile int* misc = reinterpret_cast<volatile int*>(smem + Layout::kMisc);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- which tile: heavy query tiles first --------------------------------
+    const int pairs = a.H_q / 2;
+    const int bp_count = a.B * pairs;
+    const int t = a.n_qtiles - 1 - int(blockIdx.x / bp_count);
+    const int bp = int(blockIdx.x % bp_count);
+    const int b = bp / pairs;
+    const int hq0 = 2 * (bp - b * pairs);        // heads hq0, hq0 + 1 (same KV group)
+    const int hk = hq0 / a.G;
+    const int cap = a.max_pages * a.ps;
+    int n = a.context_lens[b];
+    if (n < 0 || n > cap) {
+        if (threadIdx.x == 0)
+            atomicOr(a.err, PA_DEVERR_CONTEXT_LEN_BIT);
+        n = n < 0 ? 0 : cap;
+    }
+    const int row0 = t * kRows;
+    const int rows = min(kRows, a.L - row0);
+    const int p_last = n - a.L + row0 + rows - 1;   // position of the tile's last row
+    int n_keys = a.causal ? min(n, p_last + 1) : n;
+    if (n_keys < 0)
+        n_keys = 0;
+    const int nt = (n_keys + kKeys - 1) / kKeys;     // K/V tiles to visit
+
+    const uint32_t sQ = smem_u32(smem + Layout::kQ);
+    const uint32_t sK = smem_u32(smem + Layout::kK);
+    const uint32_t sV = smem_u32(smem + Layout::kV);
+
+    if (threadIdx.x == 0) {
+        misc[0] = 0;
+        mbar_init(&bar[kQFull], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar[kKFull + s], 3);   // one arrival per loader warp
+            mbar_init(&bar[kKEmpty + s], 1);
+            mbar_init(&bar[kVFull + s], 3);
+            mbar_init(&bar[kVEmpty + s], 1);
+        }
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&bar[kSFull + h], 1);
+            mbar_init(&bar[kPFull + h], 4);   // one arrival per softmax warp
+            mbar_init(&bar[kPVDone + h], 1);
+        }
+        mbar_init(&bar[kMmaDone], 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // Registers from the loader / MMA warpgroup (warps 0-3) to the two softmax
+    // warpgroups: 128 x kRegsProducer + 256 x kRegsSoftmax <= 384 x the launch
+    // count (checked on the host before every launch).
+    if (warp < 4)
+        setmaxnreg_dec<kRegsProducer>();
+    else
+        setmaxnreg_inc<kRegsSoftmax>();
+
+    if ((warp == 0 || warp == 2 || warp == 3) && nt > 0) {
+        // ===================== loaders =====================================
+        // Box k of a tile goes to loader k mod 3; each loader arrives on the
+        // stage barrier with its own byte count.
+        const int li = warp == 0 ? 0 : warp - 1;     // 0, 1, 2
+        // K/V tiles are read again by the other query tiles and head pairs
+        // of the same request and KV group: keep them in L2.
+        const uint64_t policy = l2_policy_evict_last();
+        if (lane == 0 && li == 0) {
+            prefetch_tensormap(&q_map);
+            prefetch_tensormap(&key_map);
+            prefetch_tensormap(&value_map);
+            mbar_arrive_expect_tx(&bar[kQFull], 2u * Layout::kMat);
+            for (int h = 0; h < 2; ++h) {
+                const int qrow = (b * a.H_q + hq0 + h) * a.L + row0;
+                uint8_t* d = smem + Layout::kQ + h * Layout::kMat;
+                tma_load_2d(d, &q_map, 0, qrow, &bar[kQFull], policy);
+                tma_load_2d(d + Layout::kHalf, &q_map, 64, qrow, &bar[kQFull], policy);
+            }
+        }
+        const int box = a.box_rows;                  // min(ps, 128)
+        const int32_t* bt = a.block_table + int64_t(b) * a.max_pages;
+        const int my_box = li + 3 * lane;
+        auto n_boxes = [&](int j) {
+            const int key0 = j * kKeys;
+            return (min(n, key0 + kKeys) - key0 + box - 1) / box;
+        };
+        // Raw block-table entry of this lane's box in tile j, loaded ahead
+        // of use and checked at use. The load is unconditional (entry 0 when
+        // the box does not exist) so that nothing waits for it before use.
+        auto fetch_page = [&](int j) -> int {
+            const bool live = j < nt && my_box < n_boxes(j);
+            return bt[live ? (j * kKeys + my_box * box) / a.ps : 0];
+        };
+        auto pool_row = [&](int j, int phys) -> int {
+            if (unsigned(phys) >= unsigned(a.num_pages)) {
+                atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
+                phys = 0;
+            }
+            const int tok = j * kKeys + my_box * box;
+            return (phys * a.H_kv + hk) * a.ps + (tok - (tok / a.ps) * a.ps);
+        };
+        auto load = [&](int j, bool is_v, int phys) {
+            const int nbox = n_boxes(j);
+            const int mine = nbox > li ? (nbox - li + 2) / 3 : 0;
+            const int s = j & 1;
+            const int full = (is_v ? kVFull : kKFull) + s;
+            const int empty = (is_v ? kVEmpty : kKEmpty) + s;
+            const bool ok = mbar_wait_warp(&bar[empty], ((j >> 1) & 1) ^ 1u, misc, a.err);
+            if (ok) {
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&bar[full], uint32_t(mine) * box * 128u * 2u);
+                __syncwarp();
+                if (my_box < nbox) {
+                    const int row = pool_row(j, phys);
+                    uint8_t* d = smem + (is_v ? Layout::kV : Layout::kK) + s * Layout::kMat +
+                                 my_box * box * 128;
+                    const CUtensorMap* m = is_v ? &value_map : &key_map;
+                    tma_load_2d(d, m, 0, row, &bar[full], policy);
+                    tma_load_2d(d + Layout::kHalf, m, 64, row, &bar[full], policy);
+                }
+            }
+            __syncwarp();
+        };
+        // Order of need: K_0, V_0, K_1, V_1, ... (S for tile j + 1 follows
+        // P V of tile j). K runs one tile ahead of V. Page ids are fetched
+        // two tiles ahead in a ring of three registers, the loop unrolled
+        // over the ring so that no pending load result is ever copied.
+        int pg[3];
+        pg[0] = fetch_page(0);
+        pg[1] = fetch_page(1);
+        load(0, false, pg[0]);
+        for (int j0 = 0; j0 < nt; j0 += 3) {
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+                const int j = j0 + u;
+                if (j < nt) {
+                    pg[(u + 2) % 3] = fetch_page(j + 2);
+                    load(j, true, pg[u]);
+                    if (j + 1 < nt)
+                        load(j + 1, false, pg[(u + 1) % 3]);
+                }
+            }
+        }
+        // No copy may still be landing when the block exits: wait (bounded)
+        // for the last two stages of both streams.
+        for (int j = max(0, nt - 2); j < nt; ++j) {
+            mbar_wait_bounded(&bar[kKFull + (j & 1)], (j >> 1) & 1, misc, a.err);
+            mbar_wait_bounded(&bar[kVFull + (j & 1)], (j >> 1) & 1, misc, a.err);
+        }
+    } else if (warp == 1 && nt > 0) {
+        // ===================== MMA issue (one thread) ======================
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
+            const uint32_t idesc_pv = idesc_bf16_f32(kRows, 128, 1);
+            // Base descriptors built once; every k-step is one add.
+            const uint64_t dq0 = kmajor_base(sQ), dq1 = desc_advance(dq0, Layout::kMat);
+            const uint64_t dk0 = kmajor_base(sK), dk1 = desc_advance(dk0, Layout::kMat);
+            const uint64_t dv0 = mnmajor_base(sV), dv1 = desc_advance(dv0, Layout::kMat);
+            auto issue_s = [&](int h, int j) {
+                const uint64_t da = h ? dq1 : dq0;
+                const uint64_t db = (j & 1) ? dk1 : dk0;
+                const uint32_t d = tmem + col_s(h);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_bf16(d, desc_advance(da, kmajor_off(kk)), desc_advance(db, kmajor_off(kk)),
+                                idesc_s, kk > 0);
+                tc_commit(&bar[kSFull + h]);
+            };
+            auto issue_pv = [&](int h, int j) {
+                const uint64_t db = (j & 1) ? dv1 : dv0;
+                const uint32_t d = tmem + col_o(h);
+                const uint32_t pa = tmem + col_s(h) + kPCol;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_bf16_ts(d, pa + 8u * kk, desc_advance(db, mnmajor_off(kk)), idesc_pv,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&bar[kPVDone + h]);
+            };
+            bool ok = mbar_wait_lean(&bar[kQFull], 0, misc, a.err);
+            if (ok)
+                ok = mbar_wait_lean(&bar[kKFull], 0, misc, a.err);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                issue_s(1, 0);
+                tc_commit(&bar[kKEmpty]);
+            }
+            for (int j = 0; j < nt && ok; ++j) {
+                const bool more = j + 1 < nt;
+                ok = mbar_wait_lean(&bar[kVFull + (j & 1)], (j >> 1) & 1, misc, a.err);
+                for (int h = 0; h < 2 && ok; ++h) {
+                    ok = mbar_wait_lean(&bar[kPFull + h], j & 1, misc, a.err);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    issue_pv(h, j);
+                    if (h == 1)
+                        tc_commit(&bar[kVEmpty + (j & 1)]);
+                    if (more) {
+                        if (h == 0)
+                            ok = mbar_wait_lean(&bar[kKFull + ((j + 1) & 1)],
+                                                   ((j + 1) >> 1) & 1, misc, a.err);
+                        // S_h(j + 1) overwrites P_h(j): wait for P_h(j) V_j.
+                        if (ok)
+                            ok = mbar_wait_lean(&bar[kPVDone + h], j & 1, misc, a.err);
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+                        issue_s(h, j + 1);
+                        if (h == 1)
+                            tc_commit(&bar[kKEmpty + ((j + 1) & 1)]);
+                    }
+                }
+            }
+            // Every MMA this thread issued completes before the block ends.
+            tc_commit(&bar[kMmaDone]);
+            mbar_wait_lean(&bar[kMmaDone], 0, misc, a.err);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ===================== softmax: one warpgroup per head =============
+        const int head = (warp - 4) >> 2;            // 0: warps 4-7, 1: warps 8-11
+        const int w4 = warp & 3;                     // TMEM lane quarter of this warp
+        const int r = w4 * 32 + lane;                // query row of the tile
+        const uint32_t trow = tmem + (uint32_t(w4 * 32) << 16);
+        const uint32_t ts = trow + col_s(head);
+        const uint32_t to = trow + col_o(head);
+        const int i = row0 + r;
+        const bool valid = r < rows;
+        const int lim = a.causal ? min(n - a.L + i, n - 1) : n - 1;  // last visible key
+        float m_used = -INFINITY;
+        float l = 0.f;
+        const float c = a.scale_log2;
+        uint16_t* orow = a.out + ((int64_t(b) * a.H_q + hq0 + head) * a.L + i) * 128;
+
+        for (int j = 0; j < nt; ++j) {
+            mbar_wait_warp(&bar[kSFull + head], j & 1, misc, a.err);
+            tc_fence_after();
+            // Scores in two halves of 64 columns (64 registers at a time): the
+            // maximum over both, then the exponentials of the upper half (still
+            // in registers), P of keys 64..127 over columns 96..127 (scores
+            // already read), the lower half read again, P of keys 0..63 over
+            // columns 64..95. Columns 0..63 are never written, so every score
+            // is read before anything overwrites it.
+            const int key0 = j * kKeys;
+            const bool edge = key0 + kKeys - 1 > lim;
+            uint32_t sv[64];
+            float* s = reinterpret_cast<float*>(sv);
+            auto load_half = [&](int hf) {
+                tmem_ld32(ts + 64u * hf, sv);
+                tmem_ld32(ts + 64u * hf + 32u, sv + 32);
+                tmem_wait_ld();
+                if (edge) {
+                    // Keys past this row's last visible key -> -inf (by select).
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        const int nv = lim - (key0 + 64 * hf + 32 * w) + 1;   // visible keys
+                        const uint32_t vis = nv >= 32 ? 0xffffffffu : nv <= 0 ? 0u : (1u << nv) - 1u;
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            s[32 * w + k] = (vis >> k) & 1u ? s[32 * w + k] : -INFINITY;
+                    }
+                }
+            };
+            float m8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                m8[u] = -INFINITY;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                load_half(hf);
+#pragma unroll
+                for (int k = 0; k < 64; k += 8)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        m8[u] = fmaxf(m8[u], s[k + u]);
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            const float mxs = mx * c;
+            const bool need =
+                mxs > m_used + kRescaleLog2 || (m_used == -INFINITY && mxs > -INFINITY);
+            float factor = 1.f;
+            if (need) {
+                factor = m_used == -INFINITY ? 0.f : fast_exp2(m_used - mxs);
+                m_used = mxs;
+                l *= factor;
+            }
+            const float mu = m_used == -INFINITY ? 0.f : m_used;
+            // Exponent arguments and the running sum two at a time (packed
+            // fp32x2 FMA and add): half the instructions of the scalar forms.
+            const float2 c2 = make_float2(c, c), nmu2 = make_float2(-mu, -mu);
+            float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                              make_float2(0.f, 0.f)};
+            auto exp_store = [&](int hf) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const float2 x = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), c2, nmu2);
+                    const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                    lsum[k & 3] = __fadd2_rn(lsum[k & 3], pp);
+                    pk[k] = pack_bf16x2(pp.x, pp.y);
+                }
+                tmem_st32(ts + kPCol + 32u * hf, pk);
+            };
+            exp_store(1);        // upper half, still in registers
+            load_half(0);
+            exp_store(0);
+            {
+                const float2 t2 = __fadd2_rn(__fadd2_rn(lsum[0], lsum[1]), __fadd2_rn(lsum[2], lsum[3]));
+                l += t2.x + t2.y;
+            }
+            // O_h holds P_h(j-1) V_{j-1} complete (the commit of S_h(j) covers
+            // it): rescale it if the maximum moved (after P, when the scores
+            // no longer occupy registers).
+            if (j >= 1 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t ov[32];
+                    tmem_ld32(to + 32u * q4, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        ov[k] = __float_as_uint(__uint_as_float(ov[k]) * factor);
+                    tmem_st32(to + 32u * q4, ov);
+                }
+            }
+            tmem_wait_st();
+            // V rows past the context hold stale bytes: zero them (P is 0
+            // there, but 0 * NaN is not) before either head's P V.
+            if (head == 0 && n < key0 + kKeys) {
+                mbar_wait_bounded(&bar[kVFull + (j & 1)], (j >> 1) & 1, misc, a.err);
+                const int z0 = max(0, n - key0);
+                const int nz = (kKeys - z0) * 16;    // 16-byte chunks
+                uint8_t* vb = smem + Layout::kV + (j & 1) * Layout::kMat;
+                for (int idx = r; idx < nz; idx += 128) {
+                    const int zr = z0 + idx / 16, ch = idx % 16;
+                    *reinterpret_cast<uint4*>(vb + (ch >> 3) * Layout::kHalf + zr * 128 +
+                                              (((ch & 7) ^ (zr & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bar[kPFull + head]);
+        }
+        // ---- epilogue: O / l -> bf16 ----------------------------------------
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (nt > 0) {
+            mbar_wait_warp(&bar[kPVDone + head], (nt - 1) & 1, misc, a.err);
+            tc_fence_after();
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t ov[32];
+            if (nt > 0) {
+                tmem_ld32(to + 32u * q4, ov);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    ov[k] = 0u;
+            }
+            if (valid && misc[0] == 0) {
+#pragma unroll
+                for (int k = 0; k < 32; k += 8) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(ov[k]) * inv, __uint_as_float(ov[k + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(ov[k + 2]) * inv, __uint_as_float(ov[k + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(ov[k + 4]) * inv, __uint_as_float(ov[k + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(ov[k + 6]) * inv, __uint_as_float(ov[k + 7]) * inv);
+                    *reinterpret_cast<uint4*>(orow + 32 * q4 + k) = w;
+                }
+            }
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t prefill_pairs_smem_bytes() { return size_t(Layout::kBytes); }
+
+cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& key_map,
+                                 const CUtensorMap& value_map, const PrefillArgs& a, int device,
+                                 cudaStream_t stream)
+{
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> smem_set[kMaxDev];
+    if (device < 0 || device >= kMaxDev)
+        return cudaErrorInvalidDevice;
+    const int smem = Layout::kBytes;
+    // The register split needs 128 x kRegsProducer + 256 x kRegsSoftmax
+    // registers out of the launch's own 384 x numRegs, a launch count no
+    // higher than kRegsSoftmax (the increase must be one) and no lower than
+    // kRegsProducer; otherwise the increase would wait forever.
+    static std::atomic<int> regs_ok[kMaxDev];
+    int rk = regs_ok[device].load(std::memory_order_relaxed);
+    if (rk == 0) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_pairs_kernel);
+        if (e != cudaSuccess)
+            return e;
+        const bool fits = fa.numRegs >= kRegsProducer && fa.numRegs <= kRegsSoftmax &&
+                          128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * fa.numRegs;
+        rk = fits ? 1 : 2;
+        regs_ok[device].store(rk, std::memory_order_relaxed);
+    }
+    if (rk != 1)
+        return cudaErrorNotSupported;
+    if (smem_set[device].load(std::memory_order_relaxed) < smem) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_pairs_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+        smem_set[device].store(smem, std::memory_order_relaxed);
+    }
+    const int64_t grid = int64_t(a.B) * (a.H_q / 2) * a.n_qtiles;
+    prefill_pairs_kernel<<<unsigned(grid), kThreads, smem, stream>>>(q_map, key_map, value_map, a);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -52,6 +52,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// The descriptor of the same matrix layout starting `bytes` further on: the
+// start address (bits 0-13, in 16-byte units) is the only field that moves,
+// and no shared-memory address reaches 2^18 bytes, so the sum never carries
+// into the next field. One integer add instead of a rebuilt descriptor keeps
+// the single MMA-issuing thread short.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes)
+{
+    return desc + uint64_t(bytes >> 4);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A
 // and B, A K-major, B K-major (b_mn_major = 0) or MN-major (1), N >> 3 in
 // bits 17-22, M >> 4 in bits 24-28.
@@ -78,6 +88,19 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T (A, K-major, read from tensor memory:
+// row m in lane m, two 16-bit elements per 32-bit column), one thread.
+__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar)
@@ -86,6 +109,24 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar)
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
         : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Per-warpgroup register reallocation (all threads of a warpgroup execute
+// the same one). N is a multiple of 8 in [24, 256].
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------------------

@@ -256,11 +256,22 @@ def test_non_default_stream():
 # The tensor-core prefill path (head_dim 128, page_size >= 8) at its edges
 
 
+@pytest.fixture(params=[1, 2], ids=["one_head", "head_pairs"])
+def prefill_variant(request):
+    """Runs the test under each tensor-core prefill kernel (pairs need an even
+    group size; odd groups take the one-head kernel under either setting)."""
+    import paged_kv_attention_06_gb300 as pa
+    prev = pa.pa_debug_prefill_variant(request.param)
+    yield request.param
+    pa.pa_debug_prefill_variant(prev)
+
+
 @pytest.mark.parametrize("ps", [8, 16, 64, 128, 256])
 @pytest.mark.parametrize("causal", [True, False])
-def test_tc_prefill_page_sizes(ps, causal):
+@pytest.mark.parametrize("H_q,H_kv", [(8, 2), (6, 2)])   # group of 4 / 3
+def test_tc_prefill_page_sizes(ps, causal, H_q, H_kv, prefill_variant):
     lens = [200, 129, 513, 300]
-    b = wl.build_batch("tcprefill", B=4, H_q=8, H_kv=2, D=128, page_size=ps, L=129,
+    b = wl.build_batch("tcprefill", B=4, H_q=H_q, H_kv=H_kv, D=128, page_size=ps, L=129,
                        context_lens=lens, seed=ps + int(causal), causal=causal,
                        placement="churn")
     out = gpu_step(DeviceBatch(b), route="prefill")
@@ -269,10 +280,11 @@ def test_tc_prefill_page_sizes(ps, causal):
     assert_close(host_f64(out), oracle_out(b, kp, vp), f"tc prefill ps={ps} causal={causal}")
 
 
-def test_tc_prefill_rows_without_keys_and_empty_context():
+@pytest.mark.parametrize("H_q,H_kv", [(4, 4), (4, 2)])   # group of 1 / 2
+def test_tc_prefill_rows_without_keys_and_empty_context(H_q, H_kv, prefill_variant):
     # L = 200 rows after contexts of 0, 50 and 199 tokens: rows at negative
     # positions see no key and must return zeros.
-    b = wl.build_batch("tcempty", B=3, H_q=4, H_kv=4, D=128, page_size=16, L=200,
+    b = wl.build_batch("tcempty", B=3, H_q=H_q, H_kv=H_kv, D=128, page_size=16, L=200,
                        context_lens=[0, 50, 199], seed=4, L_new=0)
     out = host_f64(gpu_step(DeviceBatch(b), route="prefill"))
     check_no_device_error()
@@ -281,7 +293,7 @@ def test_tc_prefill_rows_without_keys_and_empty_context():
     assert_close(out, oracle_out(b, b.key_pages, b.value_pages), "tc prefill empty rows")
 
 
-def test_tc_prefill_bad_page_id_is_flagged():
+def test_tc_prefill_bad_page_id_is_flagged(prefill_variant):
     import dataclasses
     import paged_kv_attention_06_gb300 as pa
     b = wl.build_batch("tcbad", B=2, H_q=4, H_kv=2, D=128, page_size=16, L=32,
@@ -293,7 +305,7 @@ def test_tc_prefill_bad_page_id_is_flagged():
     assert st == pa.PA_ERR_DEVICE_BOUNDS and flags & pa.PA_DEVERR_PAGE_ID
 
 
-def test_tc_prefill_long_context_gqa():
+def test_tc_prefill_long_context_gqa(prefill_variant):
     b = wl.build_batch("tclong", B=2, H_q=16, H_kv=2, D=128, page_size=16, L=384,
                        context_lens=[3000, 1500], seed=12, placement="permutation")
     db = DeviceBatch(b)

@@ -271,15 +271,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_bounded(&bar[kVFull + (j & 1)], (j >> 1) & 1, misc, a.err);
         }
     } else if (warp == 1 && nt > 0) {
-        // ===================== MMA issue (one thread) ======================
-        if (lane == 0) {
-            const uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
-            const uint32_t idesc_pv = idesc_bf16_f32(kRows, 128, 1);
-            // Base descriptors built once; every k-step is one add.
-            const uint64_t dq0 = kmajor_base(sQ), dq1 = desc_advance(dq0, Layout::kMat);
-            const uint64_t dk0 = kmajor_base(sK), dk1 = desc_advance(dk0, Layout::kMat);
-            const uint64_t dv0 = mnmajor_base(sV), dv1 = desc_advance(dv0, Layout::kMat);
-            auto issue_s = [&](int h, int j) {
+        // ===================== MMA issue (one elected thread) ==============
+        // The whole warp runs the loop (waits are warp-uniform, which costs
+        // less than branches in a lone lane); one elected lane issues. The
+        // first wait after a tcgen05.commit costs about 0.1 us even on a
+        // completed phase, so the waits that are normally already satisfied
+        // (the other head's P, the next K and V tiles) are taken right after
+        // a wait that has to take that long anyway (P_h V done), or before a
+        // commit.
+        const bool leader = elect_one();
+        const uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
+        const uint32_t idesc_pv = idesc_bf16_f32(kRows, 128, 1);
+        // Base descriptors built once; every k-step is one add.
+        const uint64_t dq0 = kmajor_base(sQ), dq1 = desc_advance(dq0, Layout::kMat);
+        const uint64_t dk0 = kmajor_base(sK), dk1 = desc_advance(dk0, Layout::kMat);
+        const uint64_t dv0 = mnmajor_base(sV), dv1 = desc_advance(dv0, Layout::kMat);
+        auto s_mmas = [&](int h, int j) {
+            if (leader) {
                 const uint64_t da = h ? dq1 : dq0;
                 const uint64_t db = (j & 1) ? dk1 : dk0;
                 const uint32_t d = tmem + col_s(h);
@@ -287,9 +295,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < 8; ++kk)
                     tc_mma_bf16(d, desc_advance(da, kmajor_off(kk)), desc_advance(db, kmajor_off(kk)),
                                 idesc_s, kk > 0);
-                tc_commit(&bar[kSFull + h]);
-            };
-            auto issue_pv = [&](int h, int j) {
+            }
+            __syncwarp();
+        };
+        auto pv_mmas = [&](int h, int j) {
+            if (leader) {
                 const uint64_t db = (j & 1) ? dv1 : dv0;
                 const uint32_t d = tmem + col_o(h);
                 const uint32_t pa = tmem + col_s(h) + kPCol;
@@ -297,49 +307,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < 8; ++kk)
                     tc_mma_bf16_ts(d, pa + 8u * kk, desc_advance(db, mnmajor_off(kk)), idesc_pv,
                                    (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&bar[kPVDone + h]);
-            };
-            bool ok = mbar_wait_lean(&bar[kQFull], 0, misc, a.err);
-            if (ok)
-                ok = mbar_wait_lean(&bar[kKFull], 0, misc, a.err);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0, 0);
-                issue_s(1, 0);
-                tc_commit(&bar[kKEmpty]);
             }
-            for (int j = 0; j < nt && ok; ++j) {
-                const bool more = j + 1 < nt;
-                ok = mbar_wait_lean(&bar[kVFull + (j & 1)], (j >> 1) & 1, misc, a.err);
-                for (int h = 0; h < 2 && ok; ++h) {
-                    ok = mbar_wait_lean(&bar[kPFull + h], j & 1, misc, a.err);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    issue_pv(h, j);
-                    if (h == 1)
-                        tc_commit(&bar[kVEmpty + (j & 1)]);
-                    if (more) {
-                        if (h == 0)
-                            ok = mbar_wait_lean(&bar[kKFull + ((j + 1) & 1)],
-                                                   ((j + 1) >> 1) & 1, misc, a.err);
-                        // S_h(j + 1) overwrites P_h(j): wait for P_h(j) V_j.
-                        if (ok)
-                            ok = mbar_wait_lean(&bar[kPVDone + h], j & 1, misc, a.err);
-                        if (!ok)
-                            break;
-                        tc_fence_after();
-                        issue_s(h, j + 1);
-                        if (h == 1)
-                            tc_commit(&bar[kKEmpty + ((j + 1) & 1)]);
-                    }
-                }
-            }
-            // Every MMA this thread issued completes before the block ends.
-            tc_commit(&bar[kMmaDone]);
-            mbar_wait_lean(&bar[kMmaDone], 0, misc, a.err);
+            __syncwarp();
+        };
+        auto commit = [&](int b) {
+            if (leader)
+                tc_commit(&bar[b]);
+            __syncwarp();
+        };
+        auto wait = [&](int b, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait_lean(&bar[b], parity, misc, a.err));
+        };
+        bool ok = wait(kQFull, 0) && wait(kKFull, 0);
+        if (ok) {
+            tc_fence_after();
+            s_mmas(0, 0);
+            commit(kSFull);
+            s_mmas(1, 0);
+            ok = wait(kVFull, 0) && (nt < 2 || wait(kKFull + 1, 0));
+            commit(kSFull + 1);
+            commit(kKEmpty);
         }
-        __syncwarp();
+        for (int j = 0; j < nt && ok; ++j) {
+            const bool more = j + 1 < nt;
+            // head 0: P_0 V_j, then S_0 for tile j + 1 once P_0 V_j is done
+            // (S_0 overwrites P_0)
+            if (!wait(kPFull, j & 1))
+                break;
+            tc_fence_after();
+            pv_mmas(0, j);
+            commit(kPVDone);
+            if (!wait(kPVDone, j & 1))
+                break;
+            tc_fence_after();
+            if (more)
+                s_mmas(0, j + 1);
+            ok = wait(kPFull + 1, j & 1);
+            if (more)
+                commit(kSFull);
+            if (!ok)
+                break;
+            // head 1: P_1 V_j, then S_1 for tile j + 1
+            tc_fence_after();
+            pv_mmas(1, j);
+            commit(kPVDone + 1);
+            commit(kVEmpty + (j & 1));
+            if (!wait(kPVDone + 1, j & 1))
+                break;
+            if (more) {
+                tc_fence_after();
+                s_mmas(1, j + 1);
+                // the next tile's V and the tile after's K, before the commit
+                ok = wait(kVFull + ((j + 1) & 1), ((j + 1) >> 1) & 1) &&
+                     (j + 2 >= nt || wait(kKFull + (j & 1), ((j + 2) >> 1) & 1));
+                commit(kSFull + 1);
+                commit(kKEmpty + ((j + 1) & 1));
+            }
+        }
+        // Every MMA issued completes before the block ends.
+        commit(kMmaDone);
+        wait(kMmaDone, 0);
     } else if (warp >= 4) {
         // ===================== softmax: one warpgroup per head =============
         const int head = (warp - 4) >> 2;            // 0: warps 4-7, 1: warps 8-11

@@ -111,6 +111,17 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar)
         : "memory");
 }
 
+// One lane of the (converged) warp, the same lane in every call: 1 there,
+// 0 in the others.
+__device__ __forceinline__ uint32_t elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred;
+}
+
 // ---------------------------------------------------------------------------
 // Per-warpgroup register reallocation (all threads of a warpgroup execute
 // the same one). N is a multiple of 8 in [24, 256].

@@ -176,16 +176,17 @@ pa_status encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pa_
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
-// 2-D bf16 tensor map over `rows` rows of 128 columns, boxes of 64 columns x
-// box_rows rows, 128-byte swizzle (used by the prefill kernel).
-pa_status encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows)
+// 2-D bf16 tensor map over `rows` rows of `cols` columns, boxes of 64 columns
+// x box_rows rows, 128-byte swizzle (queries of both kernels, prefill K/V).
+pa_status encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows,
+                          uint32_t cols = 128)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     pa_status st = get_encoder(&enc);
     if (st != PA_OK)
         return st;
-    const cuuint64_t dims[2] = {128u, cuuint64_t(rows)};
-    const cuuint64_t strides[1] = {256u};
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
     const cuuint32_t box[2] = {64u, box_rows};
     const cuuint32_t estr[2] = {1u, 1u};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
@@ -328,7 +329,12 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
     a.causal = causal ? 1 : 0;
     a.debug_unset_wait = t_arm_unset_wait ? 1 : 0;
     t_arm_unset_wait = false;
-    return launch_decode(kmap, vmap, a, int(grid), dev->id, stream) == cudaSuccess ? PA_OK
+    CUtensorMap qmap;
+    const uint64_t q_rows = uint64_t(s.batch) * s.num_q_heads * s.q_len;
+    if ((st = encode_rows_map(&qmap, query, q_rows, uint32_t(kDecodeRows), uint32_t(s.head_dim))) !=
+        PA_OK)
+        return st;
+    return launch_decode(kmap, vmap, qmap, a, int(grid), dev->id, stream) == cudaSuccess ? PA_OK
                                                                                    : PA_ERR_CUDA;
 }
 

@@ -54,7 +54,6 @@ constexpr int kStages = 3;
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumerThreads + 32;
-constexpr int kConsumerBarrier = 1;  // named barrier id for the consumer warps
 
 template <int D>
 struct Layout {
@@ -63,8 +62,11 @@ struct Layout {
     static constexpr int kStageBytes = kHalves * kHalfBytes; // K (or V) of one granule
     static constexpr int kK = 0;
     static constexpr int kV = kK + kStages * kStageBytes;
-    static constexpr int kQ = kV + kStages * kStageBytes;    // [16][D] bf16, swizzled
-    static constexpr int kBar = kQ + kDecodeRows * D * 2;
+    // Q tile of the segment whose piece starts at a stage's granule:
+    // [stage][half][16 rows][128 B], 128B swizzle (TMA box of 16 rows).
+    static constexpr int kQHalfBytes = kDecodeRows * 128;
+    static constexpr int kQ = kV + kStages * kStageBytes;
+    static constexpr int kBar = kQ + kStages * kHalves * kQHalfBytes;
     static constexpr int kMisc = kBar + 2 * kStages * 8;     // abort flag, test barrier
     static constexpr int kPrefix = kMisc + 32;               // [B + 1] int32
     static size_t bytes(int B) { return kPrefix + size_t(B + 1) * 4 + 1024; }
@@ -120,10 +122,10 @@ __device__ __forceinline__ int64_t block_of(int64_t x, int64_t total, int64_t gr
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap key_map,
-                  const __grid_constant__ CUtensorMap value_map, const DecodeArgs a)
+                  const __grid_constant__ CUtensorMap value_map,
+                  const __grid_constant__ CUtensorMap q_map, const DecodeArgs a)
 {
     using Lay = Layout<D>;
-    constexpr int kNT = D / 8;   // n-tiles of 8 output columns
     constexpr int kKS = D / 16;  // k-steps of 16 over the head dimension
 
     extern __shared__ uint8_t smem_raw[];
@@ -239,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             prefetch_tensormap(&key_map);
             prefetch_tensormap(&value_map);
+            prefetch_tensormap(&q_map);
         }
         const uint64_t policy = l2_policy_evict_first();
         const int box = a.box_rows;
@@ -272,11 +275,23 @@ __global__ void __launch_bounds__(kThreads, 2)
                         row_b = row;
                 }
             }
+            // The first granule of a piece also brings the segment's Q tile (the
+            // G heads x L rows of a KV group are consecutive rows of q).
+            const bool first = x == x_begin || x == sp.seg_start;
             const bool ok = mbar_wait_warp(&empty[stage], phase ^ 1u, misc, a.err);
-            if (ok && nbox > 0) {
-                const uint32_t bytes = uint32_t(nbox) * box * 128u * Lay::kHalves * 2u;
-                if (lane == 0)
+            if (ok && (nbox > 0 || first)) {
+                const uint32_t bytes = uint32_t(nbox) * box * 128u * Lay::kHalves * 2u +
+                                       (first ? uint32_t(Lay::kHalves * Lay::kQHalfBytes) : 0u);
+                if (lane == 0) {
                     mbar_arrive_expect_tx(&full[stage], bytes);
+                    if (first) {
+                        const int qrow = (sp.b * a.H_q + sp.h * a.G) * a.L + sp.mt * kDecodeRows;
+#pragma unroll
+                        for (int hf = 0; hf < Lay::kHalves; ++hf)
+                            tma_load_2d(smem + Lay::kQ + (stage * Lay::kHalves + hf) * Lay::kQHalfBytes,
+                                        &q_map, hf * 64, qrow, &full[stage], policy);
+                    }
+                }
                 __syncwarp();
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
@@ -313,37 +328,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     constexpr int kCols = D / kConsumerWarps;  // output columns per warp
     constexpr int kON = kCols / 8;             // output n-tiles per warp
     constexpr int kSN = kDecodeTokens / 8;     // score n-tiles per granule
-    const int tid = threadIdx.x;  // 0..127
     const int swz = a.swz;        // stage layout: chunk ^ (row & 7) when swizzled
     const int row0 = lane >> 2;   // fragment rows row0 and row0 + 8
     const int quad = lane & 3;
     const int col0 = warp * kCols;
-    uint8_t* q_smem = smem + Lay::kQ;
     int stage = 0;
     uint32_t phase = 0;
     constexpr int kSlotFloats = kDecodeRows * (D + 2);
-
-    // Q tile of a segment (16 rows x D, 16-byte chunks) -> registers; each
-    // consumer thread holds kQChunks chunks. Loaded one piece ahead so the
-    // next piece never waits on it.
-    constexpr int kQChunks = (kDecodeRows * kNT) / kConsumerThreads;
-    static_assert(kQChunks * kConsumerThreads == kDecodeRows * kNT, "Q tile split");
-    uint4 qreg[kQChunks];
-    auto load_q = [&](const SegmentPos& p) {
-#pragma unroll
-        for (int u = 0; u < kQChunks; ++u) {
-            const int c = tid + u * kConsumerThreads;
-            const int r = c / kNT, ch = c - r * kNT;
-            const int rg = p.mt * kDecodeRows + r;
-            qreg[u] = make_uint4(0, 0, 0, 0);
-            if (rg < a.R) {
-                const int g = rg / a.L, i = rg - g * a.L;
-                const int hq = p.h * a.G + g;
-                qreg[u] = *reinterpret_cast<const uint4*>(
-                    a.q + ((int64_t(p.b) * a.H_q + hq) * a.L + i) * D + ch * 8);
-            }
-        }
-    };
 
     // Output row index of fragment row rw of a segment, or -1 for padding.
     auto out_row = [&](const SegmentPos& p, int rw) -> int64_t {
@@ -355,28 +346,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     };
 
     int64_t x = x_begin;
-    load_q(locate(pre, a.B, per_req, a.MT, x));
     while (x < x_end) {
         const SegmentPos sp = locate(pre, a.B, per_req, a.MT, x);
         const int64_t piece_end = min(x_end, sp.seg_start + sp.seg_len);
         const int n = clamp_context(a.context_lens[sp.b], cap, a.err);
 
-        // ---- Q tile into shared memory, 16-byte chunks swizzled by row
-#pragma unroll
-        for (int u = 0; u < kQChunks; ++u) {
-            const int c = tid + u * kConsumerThreads;
-            const int r = c / kNT, ch = c - r * kNT;
-            *reinterpret_cast<uint4*>(q_smem + r * D * 2 + ((ch ^ (r & 7)) << 4)) = qreg[u];
-        }
-        named_barrier_sync(kConsumerBarrier, kConsumerThreads);
+        // Q fragments of the piece: from the stage of its first granule,
+        // loaded (ldmatrix) once that stage has landed.
         uint32_t qa[kKS][4];
-#pragma unroll
-        for (int kk = 0; kk < kKS; ++kk) {
-            const int r = lane & 15;
-            const int ch = 2 * kk + (lane >> 4);
-            ldsm_x4(smem_u32(q_smem + r * D * 2 + ((ch ^ (r & 7)) << 4)), qa[kk][0], qa[kk][1],
-                    qa[kk][2], qa[kk][3]);
-        }
+        bool need_q = true;
 
         // Last visible position of this thread's two fragment rows.
         int lim[2];
@@ -399,6 +377,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int t0 = int(x - sp.seg_start) * kDecodeTokens;
             const int nvalid = min(kDecodeTokens, n - t0);
             const bool ok = mbar_wait_warp(&full[stage], phase, misc, a.err);
+            if (need_q) {
+                const uint8_t* qs = smem + Lay::kQ + stage * Lay::kHalves * Lay::kQHalfBytes;
+#pragma unroll
+                for (int kk = 0; kk < kKS; ++kk) {
+                    const int r = lane & 15;
+                    const int ch = 2 * kk + (lane >> 4);   // 16-byte chunk along D
+                    ldsm_x4(smem_u32(qs + (ch >> 3) * Lay::kQHalfBytes + r * 128 +
+                                     (((ch & 7) ^ (r & 7)) << 4)),
+                            qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+                }
+                need_q = false;
+            }
             bool wrote = false;
             if (ok && nvalid > 0) {
                 if (nvalid < kDecodeTokens) {
@@ -531,8 +521,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 phase ^= 1u;
             }
         }
-        if (x < x_end)
-            load_q(locate(pre, a.B, per_req, a.MT, x));  // next piece's Q, in flight
 
         // ---- end of a piece: every warp holds identical (m, l) and its own
         // output columns.
@@ -579,9 +567,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         make_float2(o[nt][2 * rr], o[nt][2 * rr + 1]);
             }
         }
-        // Every warp has finished this piece before the next piece's Q tile
-        // overwrites shared memory.
-        named_barrier_sync(kConsumerBarrier, kConsumerThreads);
+
     }
 }
 
@@ -715,7 +701,8 @@ size_t decode_workspace_bytes(int64_t nseg, int grid_max, int D)
 }
 
 cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_map,
-                          const DecodeArgs& a, int grid, int device, cudaStream_t stream)
+                          const CUtensorMap& q_map, const DecodeArgs& a, int grid, int device,
+                          cudaStream_t stream)
 {
     // The dynamic shared-memory limit is raised once per (device, head_dim)
     // and only grows.
@@ -747,8 +734,9 @@ cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_m
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = a.D == 64 ? cudaLaunchKernelEx(&cfg, decode_kernel<64>, key_map, value_map, a)
-                              : cudaLaunchKernelEx(&cfg, decode_kernel<128>, key_map, value_map, a);
+    cudaError_t e = a.D == 64
+                        ? cudaLaunchKernelEx(&cfg, decode_kernel<64>, key_map, value_map, q_map, a)
+                        : cudaLaunchKernelEx(&cfg, decode_kernel<128>, key_map, value_map, q_map, a);
     if (e != cudaSuccess || a.whole_segments)
         return e;
     cudaLaunchConfig_t mcfg = cfg;

@@ -75,7 +75,8 @@ size_t decode_smem_bytes(int D, int B);
 int decode_max_grid(int sm_count);
 size_t decode_workspace_bytes(int64_t nseg, int grid_max, int D);
 cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_map,
-                          const DecodeArgs& a, int grid, int device, cudaStream_t stream);
+                          const CUtensorMap& q_map, const DecodeArgs& a, int grid, int device,
+                          cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Prefill on the 5th-generation tensor cores (D = 128, page_size >= 8)

@@ -112,11 +112,44 @@ __device__ __forceinline__ SegmentPos locate(const int32_t* pre, int B, int per_
     return s;
 }
 
-// Block index that processes granule x when `total` granules are split over
-// `grid` blocks as [floor(i*total/grid), floor((i+1)*total/grid)).
-__device__ __forceinline__ int64_t block_of(int64_t x, int64_t total, int64_t grid)
+// The split over blocks weighs each segment as its granules plus
+// kPieceUnits: a piece costs a block more than its granules (the first
+// granule's Q tile, the partial tail granule, the epilogue), and a block that
+// gets many short segments would otherwise end last. Unit stream: segment s
+// is kPieceUnits units of overhead, then its granules, so granule x of
+// segment s sits at unit x + kPieceUnits * (s + 1); block i owns the units
+// [floor(i*T/grid), floor((i+1)*T/grid)), T = granules + kPieceUnits * nseg,
+// i.e. the granules whose units fall there.
+constexpr int kPieceUnits = 1;
+
+// Block index that processes the granule at unit position u.
+__device__ __forceinline__ int64_t block_of_unit(int64_t u, int64_t units, int64_t grid)
 {
-    return ((x + 1) * grid - 1) / total;
+    return ((u + 1) * grid - 1) / units;
+}
+
+// First granule whose unit position is >= u (granule count if none).
+// pre[b] = first granule of request b; every segment of request b has the
+// same number of granules.
+__device__ __forceinline__ int64_t granule_at_unit(const int32_t* pre, int B, int per_req,
+                                                   int64_t u, int64_t units)
+{
+    if (u >= units)
+        return pre[B];
+    auto pre_u = [&](int b) { return int64_t(pre[b]) + int64_t(kPieceUnits) * per_req * b; };
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {  // largest b whose first unit is <= u
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre_u(mid) <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int gb = (pre[lo + 1] - pre[lo]) / per_req;
+    const int64_t r = u - pre_u(lo);
+    const int64_t hm = r / (gb + kPieceUnits);
+    const int64_t in = r - hm * (gb + kPieceUnits) - kPieceUnits;
+    return pre[lo] + hm * gb + (in > 0 ? in : 0);
 }
 
 template <int D>
@@ -198,12 +231,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
 
     const int64_t total = pre[a.B];
+    const int64_t units = total + int64_t(kPieceUnits) * a.B * per_req;
     const int64_t cta = blockIdx.x;
-    // The stream is split over min(gridDim.x, total) blocks so that every
-    // block in use owns at least one granule; a segment spanning blocks
-    // first..last then has exactly last - first + 1 pieces.
+    // The unit stream is split over min(gridDim.x, units) blocks so that every
+    // block in use owns at least one unit; a segment whose granules span
+    // blocks first..last then has exactly last - first + 1 pieces (every
+    // block in between owns units inside the segment's granules).
     const int64_t grid = a.whole_segments ? int64_t(gridDim.x)
-                                          : (int64_t(gridDim.x) < total ? int64_t(gridDim.x) : total);
+                                          : (int64_t(gridDim.x) < units ? int64_t(gridDim.x) : units);
     if (cta >= grid)
         return;
     int64_t x_begin, x_end;
@@ -223,8 +258,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         x_begin = seg_first(s0);
         x_end = seg_first(s1);
     } else {
-        x_begin = cta * total / grid;
-        x_end = (cta + 1) * total / grid;
+        x_begin = granule_at_unit(pre, a.B, per_req, cta * units / grid, units);
+        x_end = granule_at_unit(pre, a.B, per_req, (cta + 1) * units / grid, units);
     }
     if (x_begin >= x_end)
         return;
@@ -531,7 +566,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const bool single =
             a.whole_segments ||
-            block_of(sp.seg_start, total, grid) == block_of(sp.seg_start + sp.seg_len - 1, total, grid);
+            block_of_unit(sp.seg_start + int64_t(kPieceUnits) * (sp.seg + 1), units, grid) ==
+                block_of_unit(sp.seg_start + sp.seg_len - 1 + int64_t(kPieceUnits) * (sp.seg + 1), units,
+                              grid);
         const bool aborted = misc[0] != 0;
 
         if (!aborted && single) {
@@ -613,9 +650,11 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
     before = red[1][0] + red[1][1] + red[1][2] + red[1][3];
     const int gb = granules(b);
     const int64_t seg_start = before + int64_t(hm) * gb;
-    const int64_t grid = int64_t(decode_grid) < total ? int64_t(decode_grid) : total;
-    const int64_t first = block_of(seg_start, total, grid);
-    const int64_t last = block_of(seg_start + gb - 1, total, grid);
+    const int64_t units = total + int64_t(kPieceUnits) * a.B * per_req;
+    const int64_t grid = int64_t(decode_grid) < units ? int64_t(decode_grid) : units;
+    const int64_t u0 = seg_start + int64_t(kPieceUnits) * (seg + 1);
+    const int64_t first = block_of_unit(u0, units, grid);
+    const int64_t last = block_of_unit(u0 + gb - 1, units, grid);
     if (first == last)
         return;  // finished and written by one decode block
     grid_dependency_wait();  // the decode grid has completed: its partials are visible

@@ -291,6 +291,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=8.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-other-decode", action="store_true",
+                    help="skip the other decode workloads (secondary entries)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
 
@@ -422,6 +424,14 @@ def main(argv=None):
     run_e2e(3)
     e2e_ms = run_e2e(e2e_steps) / e2e_steps
 
+    # ---- secondary: the other decode workloads ------------------------------
+    other_decode = []
+    if not args.no_other_decode and world == 1:
+        for name, n in (("decode_b64_ps128", 400), ("decode_long_b8", 200)):
+            if name != args.workload:
+                other_decode.append(bench_decode_config(name, pa, binding, torch, device,
+                                                        stream, n))
+
     # ---- secondary: chunked prefill TFLOP/s (prefill route) -----------------
     prefill = None
     if not args.no_prefill and world == 1:
@@ -472,9 +482,11 @@ def main(argv=None):
                 "ms_per_step": round(e2e_ms, 6), "steps": e2e_steps},
         "gpu_launches": (3 if route == 0 else 2) * args.steps,
         "timed_loop": "native C loop over the C ABI (bench_loop.cpp)",
-        "host_launch_us_per_step": round(1e6 * host_s / args.steps, 2),
+        "host_wall_us_per_step": round(1e6 * host_s / args.steps, 2),
         "clocks": ck,
     }
+    if other_decode:
+        line["other_decode"] = other_decode
     if prefill is not None:
         prefill["roofline_frac_bf16"] = round(prefill["tflops"] / bf16_peak, 4)
         prefill["peak_source"] = f"{peak_kind} bf16_tflops"
@@ -483,6 +495,68 @@ def main(argv=None):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def bench_decode_config(name, pa, binding, torch, device, stream, steps, warmup=10):
+    """One of the other decode workloads through the same native step loop
+    (append + pa_attention per step, rotating pool copies): step time, the
+    decode call's event time and its HBM roofline fraction."""
+    import ctypes
+    b = wl.make_workload(name)
+
+    def to_dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    dec_bytes, app_bytes = step_bytes(b)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    copies = max(4, math.ceil(4 * l2 / max(1, dec_bytes)))
+    kp0, vp0 = to_dev(b.key_pages), to_dev(b.value_pages)
+    pools = [(kp0, vp0)] + [(kp0.clone(), vp0.clone()) for _ in range(copies - 1)]
+    q, bt, cl = to_dev(b.query), to_dev(b.block_table), to_dev(b.context_lens)
+    kn, vn, sm = to_dev(b.key_new), to_dev(b.value_new), to_dev(b.slot_mapping)
+    out = torch.empty_like(q)
+    shape = pa.make_shape(q.shape, kp0.shape, bt.shape[1])
+    app_shape = pa.pa_shape(b.B, 0, b.H_kv, b.D, b.L_new, b.num_pages, 0)
+    ws, ws_need = pa.decode_workspace(shape, device)
+    blib = _bench_lib(binding)
+    kps = (ctypes.c_void_p * copies)(*[kp.data_ptr() for kp, _ in pools])
+    vps = (ctypes.c_void_p * copies)(*[vp_.data_ptr() for _, vp_ in pools])
+    sample_every = 4
+
+    def run(n):
+        step_ms = (ctypes.c_float * max(1, -(-n // sample_every)))()
+        total = ctypes.c_float(0)
+        st = blib.pa_bench_steps(n, sample_every, copies, kn.data_ptr(), vn.data_ptr(), kps, vps,
+                                 sm.data_ptr(), b.page_size, app_shape, q.data_ptr(),
+                                 bt.data_ptr(), cl.data_ptr(), b.scale, int(b.causal),
+                                 out.data_ptr(), shape, int(b.context_lens.max()), ws.data_ptr(),
+                                 ws_need, stream.cuda_stream, step_ms, ctypes.byref(total))
+        if st != 0:
+            raise RuntimeError(f"native step loop failed with status {st} on {name}")
+        return float(total.value), [float(x) for x in step_ms[:-(-n // sample_every)]]
+
+    run(warmup)
+    torch.cuda.synchronize()
+    total_ms, dec_ms = run(steps)
+    torch.cuda.synchronize()
+    st, flags = pa.pa_get_device_error()
+    if st:
+        raise RuntimeError(f"device error in decode bench {name}: {flags:#x}")
+    hbm_peak, _, peak_kind = load_peaks()
+    dec_avg = float(np.mean(dec_ms))
+    ms_step = total_ms / steps
+    res = {"workload": name, "ms_per_step": round(ms_step, 6),
+           "step_gbs": round((dec_bytes + app_bytes) / (ms_step * 1e-3) / 1e9, 2),
+           "decode_call_us": round(1e3 * dec_avg, 3),
+           "decode_gbs": round(dec_bytes / (dec_avg * 1e-3) / 1e9, 2),
+           "frac": round(dec_bytes / (dec_avg * 1e-3) / 1e9 / hbm_peak, 4),
+           "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": dec_bytes,
+           "steps": steps, "l2": f"{copies} rotating pool copies"}
+    del pools, ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def bench_prefill(pa, binding, torch, device, stream, steps=20):

@@ -291,6 +291,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=8.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--dispatch-sweep", action="store_true",
+                    help="time decode vs prefill over query chunk lengths and exit")
     ap.add_argument("--no-other-decode", action="store_true",
                     help="skip the other decode workloads (secondary entries)")
     args = ap.parse_args(argv)
@@ -308,6 +310,11 @@ def main(argv=None):
 
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
+    if args.dispatch_sweep:
+        print(json.dumps({"dispatch_sweep": dispatch_sweep(torch, device),
+                          "timing": "CUDA graph of 16 calls over 4 rotating pool copies, "
+                                    "replayed 3 times, events around the replays"}))
+        return 0
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -557,6 +564,70 @@ def bench_decode_config(name, pa, binding, torch, device, stream, steps, warmup=
     del pools, ws
     torch.cuda.empty_cache()
     return res
+
+
+def dispatch_sweep(torch, device, Ls=(1, 2, 4, 8, 12, 16, 24, 32, 64), ctxs=(1024, 4096),
+                   groups=((28, 4), (32, 8)), B=32, page_size=16, copies=4, calls=16):
+    """Time pa_decode and pa_prefill on the same inputs for query chunks of L
+    rows (both are correct for every L): the data behind the L threshold of
+    pa_attention_route. Each timing is a CUDA graph of `calls` calls over
+    `copies` rotating pool copies, replayed 3 times, CUDA events around the
+    replays (no interpreter between launches)."""
+    import paged_kv_attention_06_gb300 as pa
+
+    def to_dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    rows = []
+    for (H_q, H_kv) in groups:
+        for ctx in ctxs:
+            base = wl.build_batch(f"sweep_g{H_q // H_kv}_n{ctx}", B=B, H_q=H_q, H_kv=H_kv, D=128,
+                                  page_size=page_size, L=1, context_lens=[ctx] * B,
+                                  seed=4242 + ctx + H_q, L_new=1)
+            kp0, vp0 = to_dev(base.key_pages), to_dev(base.value_pages)
+            pools = [(kp0, vp0)] + [(kp0.clone(), vp0.clone()) for _ in range(copies - 1)]
+            bt, cl = to_dev(base.block_table), to_dev(base.context_lens)
+            for L in Ls:
+                q = torch.randn(B, H_q, L, 128, device=device).to(torch.bfloat16)
+                out = torch.empty_like(q)
+                res = {}
+                for kind in ("decode", "prefill"):
+                    def call(c):
+                        kp, vp_ = pools[c % copies]
+                        if kind == "decode":
+                            pa.pa_decode(q, kp, vp_, bt, cl, page_size, scale=base.scale, out=out,
+                                         max_context_len=ctx)
+                        else:
+                            pa.pa_prefill(q, kp, vp_, bt, cl, page_size, scale=base.scale, out=out)
+                    for c in range(3):
+                        call(c)
+                    torch.cuda.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        for c in range(calls):
+                            call(c)
+                    g.replay()
+                    torch.cuda.synchronize()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for _ in range(3):
+                        g.replay()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    res[kind] = e0.elapsed_time(e1) * 1e3 / (3 * calls)
+                    del g
+                st, flags = pa.pa_get_device_error()
+                if st:
+                    raise RuntimeError(f"device error in the dispatch sweep: {flags:#x}")
+                rows.append({"G": H_q // H_kv, "H_q": H_q, "H_kv": H_kv, "ctx": ctx, "L": L,
+                             "decode_us": round(res["decode"], 2),
+                             "prefill_us": round(res["prefill"], 2),
+                             "faster": "decode" if res["decode"] <= res["prefill"] else "prefill"})
+            del pools
+            torch.cuda.empty_cache()
+    return rows
 
 
 def bench_prefill(pa, binding, torch, device, stream, steps=20):

@@ -64,6 +64,8 @@ def _load():
         lib.pa_oracle_translate.restype = ctypes.c_int
         lib.pa_oracle_append_kv.argtypes = [p, p, p, p, p] + [i32] * 6
         lib.pa_oracle_append_kv.restype = ctypes.c_int64
+        lib.pa_oracle_gather.argtypes = [p, p, p] + [i32] * 7 + [p]
+        lib.pa_oracle_gather.restype = ctypes.c_int
         lib.pa_oracle_attention_rows.argtypes = (
             [p] * 5 + [i32] * 8 + [ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                    p, ctypes.c_int64, p, ctypes.c_int])
@@ -123,6 +125,27 @@ def append_kv(key, value, key_pages, value_pages, slot_mapping, page_size: int) 
     return int(lib.pa_oracle_append_kv(_ptr(key), _ptr(value), _ptr(key_pages),
                                        _ptr(value_pages), _ptr(slots), B, L_new,
                                        H_kv, D, page_size, P))
+
+
+def gather(pages, block_table, context_lens, page_size: int, dense_len: int,
+           fill: int = 0) -> np.ndarray:
+    """Dense copy of every request's visible K (or V) rows: pages
+    [P, H_kv, page_size, D] uint16 (bf16 bits) -> [B, H_kv, dense_len, D];
+    rows past a request's context hold `fill`."""
+    lib = _load()
+    if pages.dtype != np.uint16 or not pages.flags.c_contiguous:
+        raise TypeError("gather works on contiguous uint16 (bf16 bit) pages")
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    P, H_kv, ps, D = pages.shape
+    assert ps == page_size
+    B, max_pages = bt.shape
+    out = np.full((B, H_kv, dense_len, D), fill, dtype=np.uint16)
+    status = lib.pa_oracle_gather(_ptr(pages), _ptr(bt), _ptr(cl), B, H_kv, D, page_size, P,
+                                  max_pages, dense_len, _ptr(out))
+    if status:
+        raise OracleError(_STATUS.get(status, str(status)))
+    return out
 
 
 def attention(query, key_pages, value_pages, block_table, context_lens,

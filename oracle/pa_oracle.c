@@ -85,6 +85,43 @@ int pa_oracle_translate(const int32_t *block_table_row, int32_t page_size,
 }
 
 /*
+ * Dense copy of the visible K (or V) rows of every request, the "gather"
+ * step of the dense baseline (Week 3 Day 4: the dense path first
+ * materialises each request's cached K/V contiguously, then attends).
+ * pages: [num_pages, H_kv, page_size, D] bf16 bits; block_table [B,
+ * max_pages]; dense: [B, H_kv, dense_len, D]. For every request b, KV head h
+ * and position t < context_lens[b]: dense[b][h][t][:] = pages[page][h][slot][:]
+ * with (page, slot) = translate(block_table[b], t). Rows t >= context_lens[b]
+ * are left as they are. Returns ORACLE_OK, or ORACLE_BAD_PAGE (nothing
+ * more copied) when a translation leaves the pool or a context is longer
+ * than dense_len or the block table.
+ */
+int pa_oracle_gather(const uint16_t *pages, const int32_t *block_table,
+                     const int32_t *context_lens, int32_t B, int32_t H_kv, int32_t D,
+                     int32_t page_size, int32_t num_pages, int32_t max_pages,
+                     int32_t dense_len, uint16_t *dense)
+{
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t n = context_lens[b];
+        if (n < 0 || n > dense_len || (int64_t)n > (int64_t)max_pages * page_size)
+            return ORACLE_BAD_PAGE;
+        const int32_t *row = block_table + (int64_t)b * max_pages;
+        for (int32_t t = 0; t < n; ++t) {
+            int32_t page, slot;
+            if (pa_oracle_translate(row, page_size, num_pages, t, &page, &slot))
+                return ORACLE_BAD_PAGE;
+            for (int32_t h = 0; h < H_kv; ++h) {
+                const uint16_t *src = pages + (((int64_t)page * H_kv + h) * page_size + slot) * D;
+                uint16_t *dst = dense + (((int64_t)b * H_kv + h) * dense_len + t) * D;
+                for (int32_t d = 0; d < D; ++d)
+                    dst[d] = src[d];
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
  * Write path. key/value: [B, H_kv, L_new, D] bf16 bits. Pages:
  * [num_pages, H_kv, page_size, D] bf16 bits. slot_mapping: [B, L_new].
  * A negative slot means "no token here" and is skipped. A slot beyond the

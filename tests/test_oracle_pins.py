@@ -390,3 +390,65 @@ def test_rows_subset_matches_full():
     sub = oracle.attention(q, kp, vp, bt, cl, 4, rows=rows, n_threads=2)
     for r, (b, h, i) in enumerate(rows):
         assert np.array_equal(sub[r], full[b, h, i])
+
+
+# ----------------------------------------------------------------------------
+# Gather (the dense baseline's first step)
+
+
+def test_p1_gather_follows_printed_mapping():
+    """Every page row carries its own (page, slot) marker; the gathered dense
+    rows must come out in the order of the printed position -> page table."""
+    g = _golden("p1_block_table_mapping.json")
+    ps, n = g["page_size"], g["context_len"]
+    P, H_kv, D = 16, 2, 8
+    pages = np.zeros((P, H_kv, ps, D), dtype=np.uint16)
+    for p in range(P):
+        for h in range(H_kv):
+            for s in range(ps):
+                pages[p, h, s, :] = 1000 * h + 16 * p + s
+    bt = np.array([g["page_ids"]], dtype=np.int32)
+    dense = oracle.gather(pages, bt, np.array([n], dtype=np.int32), ps, n + 3, fill=7)
+    for h in range(H_kv):
+        want = [1000 * h + 16 * p + s for p, s in zip(g["expected_pages_by_position"],
+                                                       g["expected_slots_by_position"])]
+        assert dense[0, h, :n, 0].tolist() == want
+        assert np.all(dense[0, h, n:] == 7)          # rows past the context untouched
+
+
+def test_gather_invariant_to_physical_relabelling():
+    b = wl.make_workload("tiny_decode")
+    d0 = oracle.gather(b.key_pages, b.block_table, b.context_lens, b.page_size, 16)
+    rng = np.random.default_rng(3)
+    perm = rng.permutation(b.num_pages)            # page p moves to perm[p]
+    pages = np.empty_like(b.key_pages)
+    pages[perm] = b.key_pages
+    bt = np.where(b.block_table >= 0, perm[np.clip(b.block_table, 0, None)], -1).astype(np.int32)
+    d1 = oracle.gather(pages, bt, b.context_lens, b.page_size, 16)
+    assert np.array_equal(d0, d1)
+
+
+def test_dense_attention_over_gathered_rows_equals_paged_attention():
+    """The gathered buffer is a pool with one page of dense_len tokens per
+    request; attention over it with the identity table is the same fp64
+    computation over the same keys in the same order: bit-identical."""
+    b = wl.make_workload("tiny_decode")
+    N = 12
+    kd = oracle.gather(b.key_pages, b.block_table, b.context_lens, b.page_size, N)
+    vd = oracle.gather(b.value_pages, b.block_table, b.context_lens, b.page_size, N)
+    ident = np.arange(b.B, dtype=np.int32).reshape(b.B, 1)
+    dense = oracle.attention(b.query, kd.reshape(b.B, b.H_kv, N, b.D), vd.reshape(b.B, b.H_kv, N, b.D),
+                             ident, b.context_lens, N, scale=b.scale, causal=b.causal)
+    paged = oracle.attention(b.query, b.key_pages, b.value_pages, b.block_table, b.context_lens,
+                             b.page_size, scale=b.scale, causal=b.causal)
+    assert np.array_equal(dense, paged)
+
+
+def test_gather_rejects_bad_page_and_long_context():
+    b = wl.make_workload("tiny_decode")
+    bt = b.block_table.copy()
+    bt[0, 0] = b.num_pages
+    with pytest.raises(oracle.OracleError):
+        oracle.gather(b.key_pages, bt, b.context_lens, b.page_size, 16)
+    with pytest.raises(oracle.OracleError):
+        oracle.gather(b.key_pages, b.block_table, b.context_lens, b.page_size, 8)  # 10 > 8

@@ -291,6 +291,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=8.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--dense-gather", action="store_true",
+                    help="time direct paged decode against gather + dense decode and exit")
     ap.add_argument("--dispatch-sweep", action="store_true",
                     help="time decode vs prefill over query chunk lengths and exit")
     ap.add_argument("--no-other-decode", action="store_true",
@@ -310,6 +312,12 @@ def main(argv=None):
 
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
+    if args.dense_gather:
+        print(json.dumps({"dense_gather": dense_gather_bench(torch, device),
+                          "timing": "CUDA graph of 20 calls over 4 rotating pools and dense "
+                                    "buffers, replayed 3 times, events around the replays; "
+                                    "median of 4"}))
+        return 0
     if args.dispatch_sweep:
         print(json.dumps({"dispatch_sweep": dispatch_sweep(torch, device),
                           "timing": "CUDA graph of 16 calls over 4 rotating pool copies, "
@@ -626,6 +634,89 @@ def dispatch_sweep(torch, device, Ls=(1, 2, 4, 8, 12, 16, 24, 32, 64), ctxs=(102
                              "prefill_us": round(res["prefill"], 2),
                              "faster": "decode" if res["decode"] <= res["prefill"] else "prefill"})
             del pools
+            torch.cuda.empty_cache()
+    return rows
+
+
+def dense_gather_bench(torch, device, ctxs=(128, 1024), batches=(1, 32), H_q=32, H_kv=8,
+                       page_size=128, copies=4, calls=20, repeats=4):
+    """The pages' operator comparison (tiny-llm "Measure the Direct Page
+    Walk": the dense path with its page-to-dense gather against the direct
+    page walk, Qwen3-4B decode shape, contexts 128 and 1024, page size 128),
+    on GB300: pa_decode over the pages, pa_gather_kv + pa_decode_dense, and
+    pa_decode_dense alone. Each time: a CUDA graph of `calls` calls over
+    `copies` rotating pools (and dense buffers), replayed 3 times, CUDA
+    events around the replays; the median of `repeats` such measurements."""
+    import paged_kv_attention_06_gb300 as pa
+
+    def to_dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    rows = []
+    for B in batches:
+        for ctx in ctxs:
+            base = wl.build_batch(f"densegather_b{B}_n{ctx}", B=B, H_q=H_q, H_kv=H_kv, D=128,
+                                  page_size=page_size, L=1, context_lens=[ctx] * B,
+                                  seed=777 + B + ctx, L_new=1, placement="churn")
+            kp0, vp0 = to_dev(base.key_pages), to_dev(base.value_pages)
+            pools = [(kp0, vp0)] + [(kp0.clone(), vp0.clone()) for _ in range(copies - 1)]
+            bt, cl = to_dev(base.block_table), to_dev(base.context_lens)
+            q = to_dev(base.query)
+            out = torch.empty_like(q)
+            N = max(64, -(-ctx // 64) * 64)
+            dense = [(torch.empty((B, H_kv, N, 128), dtype=torch.bfloat16, device=device),
+                      torch.empty((B, H_kv, N, 128), dtype=torch.bfloat16, device=device))
+                     for _ in range(copies)]
+            for c in range(copies):
+                pa.pa_gather_kv(pools[c][0], pools[c][1], bt, cl, page_size, N,
+                                key_dense=dense[c][0], value_dense=dense[c][1])
+            res = {}
+            for kind in ("paged", "gather+dense", "dense_only"):
+                def call(c):
+                    kp, vp_ = pools[c % copies]
+                    kd, vd = dense[c % copies]
+                    if kind == "paged":
+                        pa.pa_decode(q, kp, vp_, bt, cl, page_size, scale=base.scale, out=out,
+                                     max_context_len=ctx)
+                    else:
+                        if kind == "gather+dense":
+                            pa.pa_gather_kv(kp, vp_, bt, cl, page_size, N, key_dense=kd,
+                                            value_dense=vd)
+                        pa.pa_decode_dense(q, kd, vd, cl, scale=base.scale, out=out,
+                                           max_context_len=ctx)
+                for c in range(5):
+                    call(c)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for c in range(calls):
+                        call(c)
+                ts = []
+                for _ in range(repeats):
+                    g.replay()
+                    torch.cuda.synchronize()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for _ in range(3):
+                        g.replay()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e3 / (3 * calls))
+                res[kind] = float(np.median(ts))
+                del g
+            st, flags = pa.pa_get_device_error()
+            if st:
+                raise RuntimeError(f"device error in the dense-gather bench: {flags:#x}")
+            kv_bytes = 2 * B * ctx * H_kv * 128 * 2
+            rows.append({"B": B, "ctx": ctx, "H_q": H_q, "H_kv": H_kv, "page_size": page_size,
+                         "paged_us": round(res["paged"], 2),
+                         "gather_plus_dense_us": round(res["gather+dense"], 2),
+                         "dense_only_us": round(res["dense_only"], 2),
+                         "paged_vs_gather_plus_dense": round(res["gather+dense"] / res["paged"], 3),
+                         "kv_bytes": kv_bytes})
+            del pools, dense
             torch.cuda.empty_cache()
     return rows
 

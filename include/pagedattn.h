@@ -157,6 +157,45 @@ pa_status pa_decode_noalloc(const void *query, const void *key_pages,
                             int32_t max_context_len, void *stream);
 
 /*
+ * Dense baseline, first step (Week 3 Day 4, "Measure the Direct Page Walk":
+ * the dense path gathers each request's cached K/V into contiguous memory
+ * before attending; the direct page walk does without this copy). Copies,
+ * for every request b, KV head h and position t < context_lens[b], the row
+ * pages[block_table[b][t / page_size]][h][t % page_size][:] of key_pages and
+ * value_pages into key_dense[b][h][t][:] and value_dense[b][h][t][:].
+ *   key_dense, value_dense  device, [B, H_kv, dense_len, D] bf16, 16-byte
+ *                           aligned, owned by the caller; rows at or past a
+ *                           request's context are not written.
+ *   shape                   batch, num_kv_heads, head_dim, num_pages,
+ *                           max_pages are used.
+ * A block-table entry outside the pool skips its rows and records
+ * PA_DEVERR_PAGE_ID; a context longer than dense_len or the block table
+ * records PA_DEVERR_CONTEXT_LEN and is cut to fit. Bit copy, one kernel on
+ * `stream` (programmatic dependent launch, like pa_append_kv).
+ */
+pa_status pa_gather_kv(const void *key_pages, const void *value_pages,
+                       const int32_t *block_table, const int32_t *context_lens,
+                       int32_t page_size, pa_shape shape, int32_t dense_len,
+                       void *key_dense, void *value_dense, void *stream);
+
+/*
+ * Dense baseline, second step: decode attention over dense K/V buffers
+ * [B, H_kv, dense_len, D] (as pa_gather_kv writes them), with the same
+ * split-KV kernel, arithmetic and workspace as pa_decode; request b's keys
+ * are rows 0 .. context_lens[b] - 1 of its block, no block table is read.
+ * On the same K/V values the result is bit-identical to pa_decode's.
+ *   dense_len  a multiple of 64, >= every context length (a longer context
+ *              records PA_DEVERR_CONTEXT_LEN and is cut to dense_len).
+ *   shape      num_pages and max_pages are ignored.
+ *   workspace  as for pa_decode (pa_decode_workspace_bytes of the shape).
+ */
+pa_status pa_decode_dense(const void *query, const void *key_dense,
+                          const void *value_dense, const int32_t *context_lens,
+                          int32_t dense_len, float scale, int causal, void *out,
+                          pa_shape shape, int32_t max_context_len, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/*
  * Prefill attention: query rows in tiles, every K/V tile resolved through
  * block_table (Week 3 Day 4, "Task 2", the long-query page-walking
  * schedule), causal by default with the bottom-right offset above. Needs no

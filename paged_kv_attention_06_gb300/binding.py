@@ -62,6 +62,11 @@ def _load() -> ctypes.CDLL:
     lib.pa_decode.restype = ctypes.c_int
     lib.pa_prefill.argtypes = attn + [vp]
     lib.pa_prefill.restype = ctypes.c_int
+    lib.pa_gather_kv.argtypes = [vp, vp, vp, vp, i32, pa_shape, i32, vp, vp, vp]
+    lib.pa_gather_kv.restype = ctypes.c_int
+    lib.pa_decode_dense.argtypes = [vp, vp, vp, vp, i32, ctypes.c_float, ctypes.c_int, vp,
+                                    pa_shape, i32, vp, sz, vp]
+    lib.pa_decode_dense.restype = ctypes.c_int
     lib.pa_attention.argtypes = attn + [i32, vp, sz, vp]
     lib.pa_attention.restype = ctypes.c_int
     lib.pa_attention_route.argtypes = [pa_shape, i32]
@@ -292,3 +297,57 @@ def pa_debug_prefill_variant(variant: int) -> int:
     1 one query head per block, 2 two heads of a KV group per block (even
     group size). Returns the previous setting."""
     return int(_lib.pa_debug_prefill_variant(int(variant)))
+
+
+def pa_gather_kv(key_pages, value_pages, block_table, context_lens, page_size: int,
+                 dense_len: int, key_dense=None, value_dense=None, stream=None):
+    """Dense copies [B, H_kv, dense_len, D] of every request's visible K and V
+    rows (the dense baseline's gather); returns (key_dense, value_dense)."""
+    P, H_kv, ps, D = key_pages.shape
+    if ps != page_size or value_pages.shape != key_pages.shape:
+        raise ValueError("page pool shape does not match page_size")
+    B = block_table.shape[0]
+    if key_dense is None:
+        key_dense = torch.empty((B, H_kv, dense_len, D), dtype=torch.bfloat16,
+                                device=key_pages.device)
+    if value_dense is None:
+        value_dense = torch.empty_like(key_dense)
+    for t in (key_dense, value_dense):
+        if tuple(t.shape) != (B, H_kv, dense_len, D):
+            raise ValueError("dense buffers must be [B, H_kv, dense_len, D]")
+    shape = pa_shape(B, H_kv, H_kv, D, 1, P, block_table.shape[1])
+    st = _lib.pa_gather_kv(_dev_ptr(key_pages, torch.bfloat16, "key_pages"),
+                           _dev_ptr(value_pages, torch.bfloat16, "value_pages"),
+                           _dev_ptr(block_table, torch.int32, "block_table"),
+                           _dev_ptr(context_lens, torch.int32, "context_lens"), int(page_size),
+                           shape, int(dense_len), _dev_ptr(key_dense, torch.bfloat16, "key_dense"),
+                           _dev_ptr(value_dense, torch.bfloat16, "value_dense"), _stream(stream))
+    _check(st, "pa_gather_kv")
+    return key_dense, value_dense
+
+
+def pa_decode_dense(query, key_dense, value_dense, context_lens, scale: Optional[float] = None,
+                    causal: bool = True, out=None, max_context_len: int = 0,
+                    workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Split-KV decode over dense K/V [B, H_kv, dense_len, D] (the dense
+    baseline's attention); returns out [B, H_q, L, D] bf16."""
+    B, H_q, L, D = query.shape
+    Bk, H_kv, dense_len, Dk = key_dense.shape
+    if (Bk, Dk) != (B, D) or value_dense.shape != key_dense.shape:
+        raise ValueError("dense K/V must be [B, H_kv, dense_len, D]")
+    if out is None:
+        out = torch.empty_like(query)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    shape = pa_shape(B, H_q, H_kv, D, L, B, 1)
+    if workspace is None:
+        workspace, _ = decode_workspace(shape, query.device)
+    st = _lib.pa_decode_dense(_dev_ptr(query, torch.bfloat16, "query"),
+                              _dev_ptr(key_dense, torch.bfloat16, "key_dense"),
+                              _dev_ptr(value_dense, torch.bfloat16, "value_dense"),
+                              _dev_ptr(context_lens, torch.int32, "context_lens"), int(dense_len),
+                              float(scale), int(bool(causal)), _dev_ptr(out, torch.bfloat16, "out"),
+                              shape, int(max_context_len), workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "pa_decode_dense")
+    return out

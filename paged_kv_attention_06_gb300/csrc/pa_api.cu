@@ -264,7 +264,8 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
                        const int32_t* block_table, const int32_t* context_lens,
                        int32_t page_size, float scale, int causal, void* out,
                        const pa_shape& s, int32_t max_context_len, void* workspace,
-                       size_t workspace_bytes, int whole_segments, cudaStream_t stream)
+                       size_t workspace_bytes, int whole_segments, cudaStream_t stream,
+                       int dense = 0)
 {
     DeviceInfo* dev;
     pa_status st = device_info(&dev);
@@ -325,6 +326,7 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
     a.box_rows = page_size < kDecodeTokens ? page_size : kDecodeTokens;
     a.swz = a.box_rows >= 8 ? 7 : 0;
     a.whole_segments = whole_segments;
+    a.dense = dense;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.causal = causal ? 1 : 0;
     a.debug_unset_wait = t_arm_unset_wait ? 1 : 0;
@@ -434,6 +436,83 @@ pa_status pa_decode(const void* query, const void* key_pages, const void* value_
     return run_split_kv(query, key_pages, value_pages, block_table, context_lens, page_size,
                         scale, causal, out, shape, max_context_len, workspace, workspace_bytes,
                         0, static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_gather_kv(const void* key_pages, const void* value_pages, const int32_t* block_table,
+                       const int32_t* context_lens, int32_t page_size, pa_shape shape,
+                       int32_t dense_len, void* key_dense, void* value_dense, void* stream)
+{
+    if (!key_pages || !value_pages || !block_table || !context_lens || !key_dense || !value_dense)
+        return PA_ERR_INVALID_ARG;
+    if (shape.batch <= 0 || shape.num_kv_heads <= 0 || shape.num_pages <= 0 ||
+        shape.max_pages <= 0 || shape.head_dim <= 0 || dense_len <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(key_pages) || !aligned16(value_pages) || !aligned16(key_dense) ||
+        !aligned16(value_dense))
+        return PA_ERR_INVALID_ARG;
+    if (shape.head_dim != 64 && shape.head_dim != 128)
+        return PA_ERR_UNSUPPORTED;
+    if (!pow2_in(page_size, 1, 256))
+        return PA_ERR_UNSUPPORTED;
+    if (int64_t(shape.num_pages) * shape.num_kv_heads * page_size >= (int64_t(1) << 31) ||
+        int64_t(shape.max_pages) * page_size >= (int64_t(1) << 30) ||
+        2 * int64_t(shape.batch) * shape.num_kv_heads * dense_len * (shape.head_dim / 8) >=
+            (int64_t(1) << 40))
+        return PA_ERR_UNSUPPORTED;
+    DeviceInfo* dev;
+    pa_status st = device_info(&dev);
+    if (st != PA_OK)
+        return st;
+    GatherArgs a;
+    a.key_pages = static_cast<const uint16_t*>(key_pages);
+    a.value_pages = static_cast<const uint16_t*>(value_pages);
+    a.block_table = block_table;
+    a.context_lens = context_lens;
+    a.key_dense = static_cast<uint16_t*>(key_dense);
+    a.value_dense = static_cast<uint16_t*>(value_dense);
+    a.err = dev->err;
+    a.B = shape.batch;
+    a.H_kv = shape.num_kv_heads;
+    a.D = shape.head_dim;
+    a.ps = page_size;
+    a.num_pages = shape.num_pages;
+    a.max_pages = shape.max_pages;
+    a.dense_len = dense_len;
+    return launch_gather(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                               : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_dense(const void* query, const void* key_dense, const void* value_dense,
+                          const int32_t* context_lens, int32_t dense_len, float scale, int causal,
+                          void* out, pa_shape shape, int32_t max_context_len, void* workspace,
+                          size_t workspace_bytes, void* stream)
+{
+    if (dense_len < 64 || dense_len % 64 != 0)
+        return PA_ERR_UNSUPPORTED;
+    // The dense buffers are a pool of B pages of dense_len tokens, request b
+    // in page b (the kernel does not read a block table for them).
+    pa_shape s = shape;
+    s.num_pages = shape.batch;
+    s.max_pages = 1;
+    if (!query || !key_dense || !value_dense || !context_lens || !out)
+        return PA_ERR_INVALID_ARG;
+    if (s.batch <= 0 || s.num_q_heads <= 0 || s.num_kv_heads <= 0 || s.q_len <= 0 ||
+        s.head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(query) || !aligned16(key_dense) || !aligned16(value_dense) || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+    if (s.head_dim != 64 && s.head_dim != 128)
+        return PA_ERR_UNSUPPORTED;
+    if (s.num_q_heads % s.num_kv_heads != 0)
+        return PA_ERR_UNSUPPORTED;
+    if (int64_t(s.batch) * s.num_kv_heads * dense_len >= (int64_t(1) << 31) ||
+        int64_t(dense_len) >= (int64_t(1) << 30))
+        return PA_ERR_UNSUPPORTED;
+    return run_split_kv(query, key_dense, value_dense, nullptr, context_lens, dense_len, scale,
+                        causal, out, s, max_context_len, workspace, workspace_bytes, 0,
+                        static_cast<cudaStream_t>(stream), 1);
 }
 
 pa_status pa_prefill(const void* query, const void* key_pages, const void* value_pages,

@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (j < nbox) {
                     const int tok = t0 + j * box;
                     const int lp = tok / a.ps;
-                    int phys = bt[lp];
+                    int phys = a.dense ? sp.b : bt[lp];
                     if (unsigned(phys) >= unsigned(a.num_pages)) {
                         atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
                         phys = 0;

@@ -37,6 +37,19 @@ struct AppendArgs {
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 
+struct GatherArgs {
+    const uint16_t* key_pages;    // [P, H_kv, ps, D]
+    const uint16_t* value_pages;
+    const int32_t* block_table;   // [B, max_pages]
+    const int32_t* context_lens;  // [B]
+    uint16_t* key_dense;          // [B, H_kv, dense_len, D]
+    uint16_t* value_dense;
+    unsigned* err;
+    int32_t B, H_kv, D, ps, num_pages, max_pages, dense_len;
+};
+
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream);
+
 // ---------------------------------------------------------------------------
 // Split-KV attention (decode schedule)
 
@@ -65,6 +78,8 @@ struct DecodeArgs {
     int32_t box_rows;   // rows per TMA box: min(ps, 64)
     int32_t swz;        // 7: 128B-swizzled stage layout (box_rows >= 8); 0: linear
     int32_t whole_segments;  // 1: every block takes whole segments (no partials)
+    int32_t dense;      // 1: K/V are dense [B, H_kv, ps, D] (request b is page b;
+                        // block_table is not read)
     float scale_log2;   // scale * log2(e)
     int32_t causal;
     int32_t debug_unset_wait;  // test support: block 0 first waits on a barrier

@@ -15,7 +15,7 @@
 // one head run while the other head's softmax works.
 //
 // Schedule (one block per (request, pair of query heads of one KV group,
-// tile of 128 query rows), tiles with the most keys launched first):
+// tile of 128 query rows), tiles with the most K/V tiles launched first):
 //   * warps 0, 2, 3 (loaders): TMA loads of both Q tiles (once) and of K and
 //     V tiles of 128 keys page by page (one box of min(page_size, 128) rows x
 //     64 columns per page and half, the boxes split over the three warps),
@@ -120,15 +120,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- which tile: heavy query tiles first --------------------------------
+    // ---- which tile -----------------------------------------------------------
+    // Blocks go out in order of rank: the (request, query tile) pairs sorted by
+    // the number of K/V tiles they visit, most first (the longest-job-first
+    // order for the block scheduler), then the head pairs of each. Every block
+    // ranks all pairs itself (one thread per pair) when there are at most
+    // kThreads of them; beyond that, query tiles are taken last to first.
     const int pairs = a.H_q / 2;
-    const int bp_count = a.B * pairs;
-    const int t = a.n_qtiles - 1 - int(blockIdx.x / bp_count);
-    const int bp = int(blockIdx.x % bp_count);
-    const int b = bp / pairs;
-    const int hq0 = 2 * (bp - b * pairs);        // heads hq0, hq0 + 1 (same KV group)
-    const int hk = hq0 / a.G;
     const int cap = a.max_pages * a.ps;
+    const int rank = int(blockIdx.x / pairs);
+    const int hp = int(blockIdx.x % pairs);
+    const int M = a.B * a.n_qtiles;
+    int b, t;
+    if (M <= kThreads) {
+        __shared__ int tiles_of[kThreads];
+        __shared__ int order[kThreads];
+        auto tiles_for = [&](int bb, int tt) {
+            int nn = a.context_lens[bb];
+            nn = nn < 0 ? 0 : (nn > cap ? cap : nn);
+            const int r0 = tt * kRows;
+            const int pl = nn - a.L + r0 + min(kRows, a.L - r0) - 1;
+            int nk = a.causal ? min(nn, pl + 1) : nn;
+            nk = nk < 0 ? 0 : nk;
+            return (nk + kKeys - 1) / kKeys;
+        };
+        const int m = threadIdx.x;
+        if (m < M)
+            tiles_of[m] = tiles_for(m / a.n_qtiles, m % a.n_qtiles);
+        __syncthreads();
+        if (m < M) {
+            const int w = tiles_of[m];
+            int rk = 0;
+            for (int k = 0; k < M; ++k) {
+                const int wk = tiles_of[k];
+                rk += (wk > w || (wk == w && k < m)) ? 1 : 0;
+            }
+            order[rk] = m;
+        }
+        __syncthreads();
+        const int combo = order[rank];
+        b = combo / a.n_qtiles;
+        t = combo - b * a.n_qtiles;
+    } else {
+        t = a.n_qtiles - 1 - rank / a.B;
+        b = rank - (rank / a.B) * a.B;
+    }
+    const int hq0 = 2 * hp;                      // heads hq0, hq0 + 1 (same KV group)
+    const int hk = hq0 / a.G;
     int n = a.context_lens[b];
     if (n < 0 || n > cap) {
         if (threadIdx.x == 0)

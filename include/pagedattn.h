@@ -56,8 +56,10 @@ typedef enum pa_status {
     PA_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed          */
     PA_ERR_DEVICE_BOUNDS = 5,  /* a kernel met an out-of-range page id, slot or
                                   context length (from pa_get_device_error)     */
-    PA_ERR_DEVICE_TIMEOUT = 6  /* a kernel's bounded wait on its own copies ran
+    PA_ERR_DEVICE_TIMEOUT = 6, /* a kernel's bounded wait on its own copies ran
                                   out (from pa_get_device_error)                */
+    PA_ERR_NO_PAGES = 7        /* pa_kv_cache: the page pool or a block-table row
+                                  is full; nothing was changed                  */
 } pa_status;
 
 /* Bits of the device error word reported by pa_get_device_error. */
@@ -234,6 +236,52 @@ pa_status pa_attention(const void *query, const void *key_pages,
  * for any other bit, PA_ERR_CUDA if synchronising failed.
  */
 pa_status pa_get_device_error(void *stream, uint32_t *flags);
+
+/*
+ * Host-side page allocator and per-step metadata (host code, no GPU work).
+ * One pa_kv_cache is one layer's page pool of num_pages pages of page_size
+ * tokens, and the pages each request (seq_id) holds in it (Week 3 Day 4,
+ * "Decode Metadata"; Tutorial 13, section 4 "The Request Cache"). Not
+ * thread-safe: one host thread per cache at a time.
+ *   - pages are handed out freed-first (the last freed page first), else the
+ *     lowest page id never handed out;
+ *   - pa_kv_cache_plan places new tokens by the tail-fill rule: the next token
+ *     goes into the request's tail page while it has room, otherwise into a
+ *     new page;
+ *   - pa_kv_cache_release returns every page of a request exactly once; a
+ *     second release (or an unknown seq_id) is PA_ERR_INVALID_ARG.
+ */
+typedef struct pa_kv_cache pa_kv_cache;
+
+pa_status pa_kv_cache_create(int32_t num_pages, int32_t page_size, pa_kv_cache **cache);
+void pa_kv_cache_destroy(pa_kv_cache *cache);
+
+/* A new request with no tokens; PA_ERR_INVALID_ARG if seq_id exists. */
+pa_status pa_kv_cache_add(pa_kv_cache *cache, int64_t seq_id);
+pa_status pa_kv_cache_release(pa_kv_cache *cache, int64_t seq_id);
+
+/* Pages not held by any request; -1 on a null cache. */
+int32_t pa_kv_cache_free_pages(const pa_kv_cache *cache);
+/* Tokens cached for seq_id; -1 if unknown. */
+int32_t pa_kv_cache_context_len(const pa_kv_cache *cache, int64_t seq_id);
+
+/*
+ * One scheduler step for n requests: request i (seq_ids[i], all distinct and
+ * added) gets new_tokens[i] (0 .. l_new) new tokens. Writes, into host
+ * arrays:
+ *   block_table   [n, max_pages]  the request's page ids in logical order,
+ *                                 -1 after the last;
+ *   context_lens  [n]             tokens cached after this step;
+ *   slot_mapping  [n, l_new]      the flat slot (page * page_size + offset)
+ *                                 of each new token in order, -1 after the
+ *                                 last (may be NULL when l_new == 0).
+ * All or nothing: if the pool runs out of pages or a request would need more
+ * than max_pages pages, nothing is changed and PA_ERR_NO_PAGES is returned;
+ * bad arguments give PA_ERR_INVALID_ARG, also with nothing changed.
+ */
+pa_status pa_kv_cache_plan(pa_kv_cache *cache, int32_t n, const int64_t *seq_ids,
+                           const int32_t *new_tokens, int32_t max_pages, int32_t l_new,
+                           int32_t *block_table, int32_t *context_lens, int32_t *slot_mapping);
 
 /* Static, human-readable name of a status code. */
 const char *pa_status_string(pa_status status);

@@ -14,6 +14,7 @@ import os
 import threading
 from typing import Optional, Tuple
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -25,6 +26,7 @@ PA_ERR_WORKSPACE = 3
 PA_ERR_CUDA = 4
 PA_ERR_DEVICE_BOUNDS = 5
 PA_ERR_DEVICE_TIMEOUT = 6
+PA_ERR_NO_PAGES = 7
 
 PA_DEVERR_PAGE_ID = 0x1
 PA_DEVERR_SLOT = 0x2
@@ -62,6 +64,21 @@ def _load() -> ctypes.CDLL:
     lib.pa_decode.restype = ctypes.c_int
     lib.pa_prefill.argtypes = attn + [vp]
     lib.pa_prefill.restype = ctypes.c_int
+    i64 = ctypes.c_int64
+    lib.pa_kv_cache_create.argtypes = [i32, i32, ctypes.POINTER(vp)]
+    lib.pa_kv_cache_create.restype = ctypes.c_int
+    lib.pa_kv_cache_destroy.argtypes = [vp]
+    lib.pa_kv_cache_destroy.restype = None
+    lib.pa_kv_cache_add.argtypes = [vp, i64]
+    lib.pa_kv_cache_add.restype = ctypes.c_int
+    lib.pa_kv_cache_release.argtypes = [vp, i64]
+    lib.pa_kv_cache_release.restype = ctypes.c_int
+    lib.pa_kv_cache_free_pages.argtypes = [vp]
+    lib.pa_kv_cache_free_pages.restype = i32
+    lib.pa_kv_cache_context_len.argtypes = [vp, i64]
+    lib.pa_kv_cache_context_len.restype = i32
+    lib.pa_kv_cache_plan.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp]
+    lib.pa_kv_cache_plan.restype = ctypes.c_int
     lib.pa_gather_kv.argtypes = [vp, vp, vp, vp, i32, pa_shape, i32, vp, vp, vp]
     lib.pa_gather_kv.restype = ctypes.c_int
     lib.pa_decode_dense.argtypes = [vp, vp, vp, vp, i32, ctypes.c_float, ctypes.c_int, vp,
@@ -351,3 +368,57 @@ def pa_decode_dense(query, key_dense, value_dense, context_lens, scale: Optional
                               workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "pa_decode_dense")
     return out
+
+
+class KVCache:
+    """Host-side page allocator and per-step metadata of one layer pool (the
+    C++ pa_kv_cache): freed pages first, tail-fill placement, all-or-nothing
+    steps, release exactly once."""
+
+    def __init__(self, num_pages: int, page_size: int):
+        h = ctypes.c_void_p()
+        _check(_lib.pa_kv_cache_create(int(num_pages), int(page_size), ctypes.byref(h)),
+               "pa_kv_cache_create")
+        self._h = h
+        self.num_pages = int(num_pages)
+        self.page_size = int(page_size)
+
+    def close(self) -> None:
+        if self._h:
+            _lib.pa_kv_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add(self, seq_id: int) -> None:
+        _check(_lib.pa_kv_cache_add(self._h, int(seq_id)), "pa_kv_cache_add")
+
+    def release(self, seq_id: int) -> None:
+        _check(_lib.pa_kv_cache_release(self._h, int(seq_id)), "pa_kv_cache_release")
+
+    @property
+    def free_pages(self) -> int:
+        return int(_lib.pa_kv_cache_free_pages(self._h))
+
+    def context_len(self, seq_id: int) -> int:
+        return int(_lib.pa_kv_cache_context_len(self._h, int(seq_id)))
+
+    def plan(self, seq_ids, new_tokens, max_pages: int, l_new: int):
+        """One step: returns (block_table [n, max_pages], context_lens [n],
+        slot_mapping [n, l_new]) as int32 numpy arrays; raises
+        PagedAttentionError (PA_ERR_NO_PAGES) with nothing changed when the
+        step does not fit."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        toks = np.ascontiguousarray(new_tokens, dtype=np.int32)
+        n = int(ids.shape[0])
+        bt = np.empty((n, int(max_pages)), dtype=np.int32)
+        cl = np.empty((n,), dtype=np.int32)
+        sm = np.empty((n, max(int(l_new), 1)), dtype=np.int32)
+        st = _lib.pa_kv_cache_plan(self._h, n, ids.ctypes.data, toks.ctypes.data, int(max_pages),
+                                   int(l_new), bt.ctypes.data, cl.ctypes.data, sm.ctypes.data)
+        _check(st, "pa_kv_cache_plan")
+        return bt, cl, sm[:, :int(l_new)]

@@ -587,6 +587,7 @@ const char* pa_status_string(pa_status status)
     case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG: invalid argument";
     case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: unsupported shape or page size";
     case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing, too small or misaligned";
+    case PA_ERR_NO_PAGES: return "PA_ERR_NO_PAGES: page pool or block-table row full (nothing changed)";
     case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA call or launch failed";
     case PA_ERR_DEVICE_BOUNDS: return "PA_ERR_DEVICE_BOUNDS: kernel met an out-of-range index";
     case PA_ERR_DEVICE_TIMEOUT: return "PA_ERR_DEVICE_TIMEOUT: kernel wait gave up";

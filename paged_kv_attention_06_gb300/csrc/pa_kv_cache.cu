@@ -1,0 +1,205 @@
+// Host-side page allocator and per-step metadata builder (host code only).
+//
+// The pages' serving stack keeps, per request, the list of pages it holds in
+// each layer pool and the number of tokens cached; a scheduler step turns
+// that into the block_table, context_lens and slot_mapping the kernels read
+// (Week 3 Day 4, "Decode Metadata": allocate a page only when the tail page is
+// full; prepare the batch's page metadata once per scheduler step; Tutorial
+// 13, section 4 "The Request Cache": fill the tail page first, then
+// allocate; release every page of a finished request exactly once; restore
+// the pool when a write fails).
+//
+// The allocator hands out a freed page first (free list, last freed first)
+// and otherwise the lowest never-used page id. A step is all-or-nothing: the
+// allocations it made are undone, in reverse, when any request of the step
+// cannot be placed, so a failed step leaves the cache exactly as it was.
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "../../include/pagedattn.h"
+
+namespace {
+
+struct Sequence {
+    std::vector<int32_t> pages;
+    int32_t len = 0;       // tokens cached
+};
+
+}  // namespace
+
+struct pa_kv_cache {
+    int32_t num_pages = 0;
+    int32_t page_size = 0;
+    int32_t next_fresh = 0;                 // lowest page id never handed out
+    std::vector<int32_t> free_list;         // freed ids, last freed at the back
+    std::unordered_map<int64_t, Sequence> seqs;
+    int32_t held = 0;                       // pages held by sequences
+};
+
+namespace {
+
+// One allocation, for undo: the page and whether it came off the free list.
+struct Taken {
+    int32_t page;
+    bool from_free_list;
+};
+
+bool take_page(pa_kv_cache* c, std::vector<Taken>* log, int32_t* page)
+{
+    if (!c->free_list.empty()) {
+        *page = c->free_list.back();
+        c->free_list.pop_back();
+        log->push_back({*page, true});
+    } else if (c->next_fresh < c->num_pages) {
+        *page = c->next_fresh++;
+        log->push_back({*page, false});
+    } else {
+        return false;
+    }
+    ++c->held;
+    return true;
+}
+
+void undo(pa_kv_cache* c, const std::vector<Taken>& log)
+{
+    for (size_t k = log.size(); k-- > 0;) {
+        if (log[k].from_free_list)
+            c->free_list.push_back(log[k].page);
+        else
+            --c->next_fresh;
+        --c->held;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_kv_cache_create(int32_t num_pages, int32_t page_size, pa_kv_cache** cache)
+{
+    if (!cache || num_pages <= 0 || page_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    pa_kv_cache* c = new (std::nothrow) pa_kv_cache;
+    if (!c)
+        return PA_ERR_NO_PAGES;
+    c->num_pages = num_pages;
+    c->page_size = page_size;
+    *cache = c;
+    return PA_OK;
+}
+
+void pa_kv_cache_destroy(pa_kv_cache* cache) { delete cache; }
+
+pa_status pa_kv_cache_add(pa_kv_cache* cache, int64_t seq_id)
+{
+    if (!cache)
+        return PA_ERR_INVALID_ARG;
+    if (cache->seqs.count(seq_id))
+        return PA_ERR_INVALID_ARG;
+    cache->seqs.emplace(seq_id, Sequence());
+    return PA_OK;
+}
+
+pa_status pa_kv_cache_release(pa_kv_cache* cache, int64_t seq_id)
+{
+    if (!cache)
+        return PA_ERR_INVALID_ARG;
+    auto it = cache->seqs.find(seq_id);
+    if (it == cache->seqs.end())
+        return PA_ERR_INVALID_ARG;   // unknown, or released already
+    for (int32_t p : it->second.pages)
+        cache->free_list.push_back(p);
+    cache->held -= int32_t(it->second.pages.size());
+    cache->seqs.erase(it);
+    return PA_OK;
+}
+
+int32_t pa_kv_cache_free_pages(const pa_kv_cache* cache)
+{
+    return cache ? cache->num_pages - cache->held : -1;
+}
+
+int32_t pa_kv_cache_context_len(const pa_kv_cache* cache, int64_t seq_id)
+{
+    if (!cache)
+        return -1;
+    auto it = cache->seqs.find(seq_id);
+    return it == cache->seqs.end() ? -1 : it->second.len;
+}
+
+pa_status pa_kv_cache_plan(pa_kv_cache* cache, int32_t n, const int64_t* seq_ids,
+                           const int32_t* new_tokens, int32_t max_pages, int32_t l_new,
+                           int32_t* block_table, int32_t* context_lens, int32_t* slot_mapping)
+{
+    if (!cache || n < 0 || max_pages <= 0 || l_new < 0)
+        return PA_ERR_INVALID_ARG;
+    if (n > 0 && (!seq_ids || !new_tokens || !block_table || !context_lens ||
+                  (l_new > 0 && !slot_mapping)))
+        return PA_ERR_INVALID_ARG;
+    // Validate every request before touching anything.
+    std::unordered_set<int64_t> seen;
+    for (int32_t i = 0; i < n; ++i) {
+        if (new_tokens[i] < 0 || new_tokens[i] > l_new)
+            return PA_ERR_INVALID_ARG;
+        if (!seen.insert(seq_ids[i]).second || !cache->seqs.count(seq_ids[i]))
+            return PA_ERR_INVALID_ARG;   // listed twice, or unknown
+        if (int64_t(cache->seqs[seq_ids[i]].pages.size()) > max_pages)
+            return PA_ERR_NO_PAGES;      // its block-table row does not fit
+    }
+    const int32_t ps = cache->page_size;
+    std::vector<Taken> log;
+    struct Before {
+        Sequence* s;
+        size_t pages;
+        int32_t len;
+    };
+    std::vector<Before> before;
+    before.reserve(size_t(n));
+    pa_status st = PA_OK;
+    for (int32_t i = 0; i < n && st == PA_OK; ++i) {
+        Sequence& s = cache->seqs[seq_ids[i]];
+        before.push_back({&s, s.pages.size(), s.len});
+        int32_t* slots = slot_mapping ? slot_mapping + int64_t(i) * l_new : nullptr;
+        for (int32_t k = 0; k < new_tokens[i]; ++k) {
+            const int32_t pos = s.len;
+            if (pos % ps == 0) {   // the tail page is full (or there is none)
+                int32_t page;
+                if (int32_t(s.pages.size()) >= max_pages || !take_page(cache, &log, &page)) {
+                    st = PA_ERR_NO_PAGES;
+                    break;
+                }
+                s.pages.push_back(page);
+            }
+            slots[k] = s.pages.back() * ps + pos % ps;
+            ++s.len;
+        }
+    }
+    if (st != PA_OK) {
+        for (const Before& b : before) {
+            b.s->pages.resize(b.pages);
+            b.s->len = b.len;
+        }
+        undo(cache, log);
+        return st;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        const Sequence& s = cache->seqs[seq_ids[i]];
+        int32_t* row = block_table + int64_t(i) * max_pages;
+        const int32_t np = int32_t(s.pages.size());
+        memcpy(row, s.pages.data(), size_t(np) * sizeof(int32_t));
+        for (int32_t k = np; k < max_pages; ++k)
+            row[k] = -1;
+        context_lens[i] = s.len;
+        if (slot_mapping)
+            for (int32_t k = new_tokens[i]; k < l_new; ++k)
+                slot_mapping[int64_t(i) * l_new + k] = -1;
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

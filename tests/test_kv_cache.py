@@ -1,0 +1,119 @@
+"""The C++ page allocator and per-step metadata builder (pa_kv_cache, host
+code): against the pinned Python allocator fixture (same page ids, slots and
+tables on random histories), the printed append walkthrough of Tutorial 13
+(tail-fill code), all-or-nothing steps, and release exactly once. No GPU."""
+import numpy as np
+import pytest
+
+import workloads as wl
+
+
+def _pa():
+    import paged_kv_attention_06_gb300 as pa
+    return pa
+
+
+def test_append_walkthrough_tail_fill():
+    import json, os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "p2_append_walkthrough.json")))
+    exp = g["append_code"]
+    ps = g["page_size"]
+    c = _pa().KVCache(8, ps)
+    c.add(7)
+    token = 0
+    contents = {}
+    for k, n_tok in enumerate(g["chunks"]):
+        bt, cl, sm = c.plan([7], [n_tok], max_pages=4, l_new=4)
+        pages = [int(p) for p in bt[0] if p >= 0]
+        assert pages == exp["page_ids_after_each_chunk"][k]
+        assert int(cl[0]) == exp["offset_after_each_chunk"][k]
+        lens = [min(ps, int(cl[0]) - ps * i) for i in range(len(pages))]
+        assert lens == exp["page_lens_after_each_chunk"][k]
+        for t, slot in enumerate(sm[0, :n_tok]):
+            contents[(int(slot) // ps, int(slot) % ps)] = token + t
+        assert np.all(sm[0, n_tok:] == -1)
+        token += n_tok
+    for pid, row in exp["page_contents"].items():
+        for s, t in enumerate(row):
+            assert contents.get((int(pid), s)) == t
+
+
+def test_matches_python_fixture_on_random_histories():
+    """Random admissions, chunked appends and releases: the C++ cache and the
+    fixture (PagePool LIFO free list + PagedCache tail fill) give the same
+    page ids, slots, tables and context lengths at every step."""
+    pa = _pa()
+    rng = np.random.default_rng(5)
+    for trial in range(20):
+        ps = int(rng.choice([1, 4, 16]))
+        num_pages = 4096
+        c = pa.KVCache(num_pages, ps)
+        pool = wl.PagePool(ps)
+        live = {}
+        next_id = 0
+        for step in range(60):
+            if len(live) < 4 and rng.random() < 0.5:
+                c.add(next_id)
+                live[next_id] = wl.PagedCache(pool)
+                next_id += 1
+            if live and rng.random() < 0.15:
+                sid = int(rng.choice(list(live)))
+                c.release(sid)
+                live.pop(sid).release()
+            if not live:
+                continue
+            ids = list(live)
+            toks = [int(rng.integers(0, 9)) for _ in ids]
+            bt, cl, sm = c.plan(ids, toks, max_pages=256, l_new=8)
+            for i, sid in enumerate(ids):
+                slots = live[sid].append(toks[i])
+                assert sm[i, :toks[i]].tolist() == slots
+                assert [int(p) for p in bt[i] if p >= 0] == live[sid].page_ids
+                assert int(cl[i]) == live[sid].offset == c.context_len(sid)
+        assert c.free_pages == num_pages - len(pool.used_page_ids)
+
+
+def test_step_is_all_or_nothing():
+    pa = _pa()
+    c = pa.KVCache(4, 4)
+    c.add(1)
+    c.add(2)
+    c.plan([1], [5], max_pages=4, l_new=8)           # request 1: 2 pages
+    free = c.free_pages
+    with pytest.raises(pa.PagedAttentionError) as e:  # needs 3 + 1 pages, 2 left
+        c.plan([2, 1], [9, 3], max_pages=4, l_new=9)
+    assert e.value.status == pa.PA_ERR_NO_PAGES
+    assert c.free_pages == free and c.context_len(1) == 5 and c.context_len(2) == 0
+    # the same history without the failed step gives the same next allocation
+    d = pa.KVCache(4, 4)
+    d.add(1)
+    d.add(2)
+    d.plan([1], [5], max_pages=4, l_new=8)
+    assert np.array_equal(c.plan([2], [4], 4, 4)[0], d.plan([2], [4], 4, 4)[0])
+    with pytest.raises(pa.PagedAttentionError):       # block-table row too short
+        c.plan([1], [8], max_pages=2, l_new=8)
+    assert c.context_len(1) == 5
+
+
+def test_release_exactly_once_and_bad_arguments():
+    pa = _pa()
+    c = pa.KVCache(8, 2)
+    c.add(3)
+    bt, _, _ = c.plan([3], [5], max_pages=8, l_new=5)
+    assert c.free_pages == 5
+    c.release(3)
+    assert c.free_pages == 8
+    with pytest.raises(pa.PagedAttentionError):
+        c.release(3)                                  # second release
+    with pytest.raises(pa.PagedAttentionError):
+        c.plan([3], [1], 8, 1)                        # unknown request
+    c.add(4)
+    with pytest.raises(pa.PagedAttentionError):
+        c.add(4)                                      # exists
+    with pytest.raises(pa.PagedAttentionError):
+        c.plan([4, 4], [1, 1], 8, 1)                  # listed twice
+    with pytest.raises(pa.PagedAttentionError):
+        c.plan([4], [2], 8, 1)                        # more tokens than l_new
+    # freed pages come back last-freed first: request 3 held pages 0, 1, 2
+    bt, _, _ = c.plan([4], [2], 8, 2)
+    assert int(bt[0, 0]) == int(np.asarray(bt)[0, 0]) == 2

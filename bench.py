@@ -291,6 +291,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=8.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--serving-trace", action="store_true",
+                    help="run the synthetic serving trace through pa_kv_cache and exit")
     ap.add_argument("--dense-gather", action="store_true",
                     help="time direct paged decode against gather + dense decode and exit")
     ap.add_argument("--dispatch-sweep", action="store_true",
@@ -312,6 +314,10 @@ def main(argv=None):
 
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
+    if args.serving_trace:
+        serving_trace(torch, device)            # warm-up run (builds, first calls)
+        print(json.dumps({"serving_trace": serving_trace(torch, device)}))
+        return 0
     if args.dense_gather:
         print(json.dumps({"dense_gather": dense_gather_bench(torch, device),
                           "timing": "CUDA graph of 20 calls over 4 rotating pools and dense "
@@ -719,6 +725,125 @@ def dense_gather_bench(torch, device, ctxs=(128, 1024), batches=(1, 32), H_q=32,
             del pools, dense
             torch.cuda.empty_cache()
     return rows
+
+
+def serving_trace(torch, device, n_seqs=16, batch=4, prompt=(128, 1024), output=(32, 128),
+                  chunk=128, H_q=32, H_kv=8, D=128, page_size=16, seed=2024):
+    """A synthetic serving trace shaped like the pages' (16 requests, at most
+    4 active, prompts U[128, 1024], outputs U[32, 128], prefill in chunks of
+    128 tokens) through one attention layer: every step the C++ pa_kv_cache
+    plans the step's block_table, context_lens and slot_mapping once, the
+    tables go to the device from pinned buffers, the new K/V rows are
+    appended, and attention runs (all decoding requests in one call with
+    L = 1; each prefilling request's chunk in its own call). K/V rows and
+    queries are seeded normal values (no model)."""
+    import paged_kv_attention_06_gb300 as pa
+    rng = np.random.default_rng(seed)
+    prompts = rng.integers(prompt[0], prompt[1], size=n_seqs, endpoint=True)
+    outputs = rng.integers(output[0], output[1], size=n_seqs, endpoint=True)
+    max_ctx = int(prompts.max() + outputs.max())
+    max_pages = -(-max_ctx // page_size)
+    num_pages = batch * max_pages + 64
+    cache = pa.KVCache(num_pages, page_size)
+    gen = torch.Generator(device=device).manual_seed(seed)
+    kp = torch.randn((num_pages, H_kv, page_size, D), generator=gen, device=device).to(torch.bfloat16)
+    vp = torch.randn((num_pages, H_kv, page_size, D), generator=gen, device=device).to(torch.bfloat16)
+    # flat buffers; a step uses the leading n * ... elements as a contiguous [n, ..] view
+    flat = lambda n: torch.randn((n,), generator=gen, device=device).to(torch.bfloat16)
+    k_flat, v_flat = flat(batch * H_kv * chunk * D), flat(batch * H_kv * chunk * D)
+    q_flat = flat(batch * H_q * chunk * D)
+    # one pinned staging region per call of a step (the copies are asynchronous)
+    regions = batch + 1
+    h_bt = torch.empty((regions, batch * max_pages), dtype=torch.int32).pin_memory()
+    h_cl = torch.empty((regions, batch), dtype=torch.int32).pin_memory()
+    h_sm = torch.empty((regions, batch * chunk), dtype=torch.int32).pin_memory()
+    d_bt = torch.empty((batch * max_pages,), dtype=torch.int32, device=device)
+    d_cl = torch.empty((batch,), dtype=torch.int32, device=device)
+    d_sm = torch.empty((batch * chunk,), dtype=torch.int32, device=device)
+
+    def step(r, ids, toks, l_new, is_decode):
+        bt, cl, sm = cache.plan(ids, toks, max_pages, l_new)
+        n = len(ids)
+        nb, ns = n * max_pages, n * l_new
+        h_bt[r, :nb].copy_(torch.from_numpy(bt.reshape(-1)))
+        h_cl[r, :n].copy_(torch.from_numpy(cl))
+        h_sm[r, :ns].copy_(torch.from_numpy(np.ascontiguousarray(sm).reshape(-1)))
+        d_bt[:nb].copy_(h_bt[r, :nb], non_blocking=True)
+        d_cl[:n].copy_(h_cl[r, :n], non_blocking=True)
+        d_sm[:ns].copy_(h_sm[r, :ns], non_blocking=True)
+        kv = (n, H_kv, l_new, D)
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record()
+        pa.pa_append_kv(k_flat[:n * H_kv * l_new * D].view(kv), v_flat[:n * H_kv * l_new * D].view(kv),
+                        kp, vp, d_sm[:ns].view(n, l_new), page_size)
+        e1.record()
+        pa.pa_attention(q_flat[:n * H_q * l_new * D].view(n, H_q, l_new, D), kp, vp,
+                        d_bt[:nb].view(n, max_pages), d_cl[:n], page_size,
+                        max_context_len=int(cl.max()))
+        e2.record()
+        events.append((e0, e1, e2, is_decode))
+    waiting = list(range(n_seqs))
+    events = []
+    append_ms = decode_ms = prefill_ms = 0.0
+    active = {}                        # seq -> [prompt tokens done, output tokens done]
+    steps = prefill_tokens = decode_tokens = 0
+    host_s = 0.0
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    while waiting or active:
+        while waiting and len(active) < batch:
+            s_id = waiting.pop(0)
+            cache.add(s_id)
+            active[s_id] = [0, 0]
+        dec = [s_id for s_id, (p_, o_) in active.items() if p_ >= prompts[s_id]]
+        pre = [s_id for s_id, (p_, o_) in active.items() if p_ < prompts[s_id]]
+        # decode group: one token each, one attention call
+        if dec:
+            t0 = time.perf_counter()
+            step(0, dec, [1] * len(dec), 1, True)
+            host_s += time.perf_counter() - t0
+            decode_tokens += len(dec)
+            for s_id in dec:
+                active[s_id][1] += 1
+        # prefill: each request's next chunk in its own call
+        for r, s_id in enumerate(pre, start=1):
+            take = int(min(chunk, prompts[s_id] - active[s_id][0]))
+            t0 = time.perf_counter()
+            step(r, [s_id], [take], take, False)
+            host_s += time.perf_counter() - t0
+            prefill_tokens += take
+            active[s_id][0] += take
+        torch.cuda.synchronize()   # the pinned staging buffers are reused next step
+        for e0, e1, e2, is_decode in events:
+            append_ms += e0.elapsed_time(e1)
+            if is_decode:
+                decode_ms += e1.elapsed_time(e2)
+            else:
+                prefill_ms += e1.elapsed_time(e2)
+        events.clear()
+        for s_id in [s_id for s_id, (p_, o_) in active.items() if o_ >= outputs[s_id]]:
+            cache.release(s_id)
+            del active[s_id]
+        steps += 1
+    wall = time.perf_counter() - wall0
+    st, flags = pa.pa_get_device_error()
+    if st:
+        raise RuntimeError(f"device error in the serving trace: {flags:#x}")
+    leaked = num_pages - cache.free_pages
+    cache.close()
+    return {"requests": n_seqs, "max_active": batch, "steps": steps,
+            "prefill_tokens": int(prefill_tokens), "decode_tokens": int(decode_tokens),
+            "wall_s": round(wall, 4), "tokens_per_s": round((prefill_tokens + decode_tokens) / wall, 1),
+            "us_per_step": round(1e6 * wall / steps, 2),
+            "host_issue_us_per_step": round(1e6 * host_s / steps, 2),
+            "device_us_per_step": {"append": round(1e3 * append_ms / steps, 2),
+                                   "decode_attention": round(1e3 * decode_ms / steps, 2),
+                                   "prefill_attention": round(1e3 * prefill_ms / steps, 2)},
+            "pages_left_held": int(leaked),
+            "shape": {"H_q": H_q, "H_kv": H_kv, "D": D, "page_size": page_size, "chunk": chunk,
+                      "prompt": list(prompt), "output": list(output)},
+            "timing": "wall clock over the whole trace (one device sync per step); device "
+                      "times from CUDA events around each append and attention call"}
 
 
 def bench_prefill(pa, binding, torch, device, stream, steps=20):

@@ -283,6 +283,25 @@ pa_status pa_kv_cache_plan(pa_kv_cache *cache, int32_t n, const int64_t *seq_ids
                            const int32_t *new_tokens, int32_t max_pages, int32_t l_new,
                            int32_t *block_table, int32_t *context_lens, int32_t *slot_mapping);
 
+/*
+ * Snapshot and restore (Tutorial 13, section 7 "Transactional Safety"): a
+ * snapshot is a copy of the cache's bookkeeping (free list, fresh-page
+ * counter, every request's pages and length). Restoring it puts the cache
+ * back as it was when the snapshot was taken, so a step whose K/V write or
+ * attention launch failed after pa_kv_cache_plan succeeded can be undone.
+ * Pool contents are not part of a snapshot and need no restoring: the rows a
+ * failed step wrote lie in free pages or past a request's context length,
+ * which no kernel reads. The caller owns the snapshot and frees it with
+ * pa_kv_cache_snapshot_destroy; restoring a snapshot of another cache is
+ * PA_ERR_INVALID_ARG. A snapshot stays valid after restore (restore it again
+ * to roll back again).
+ */
+typedef struct pa_kv_cache_snapshot pa_kv_cache_snapshot;
+
+pa_status pa_kv_cache_snapshot_take(const pa_kv_cache *cache, pa_kv_cache_snapshot **snapshot);
+pa_status pa_kv_cache_restore(pa_kv_cache *cache, const pa_kv_cache_snapshot *snapshot);
+void pa_kv_cache_snapshot_destroy(pa_kv_cache_snapshot *snapshot);
+
 /* Static, human-readable name of a status code. */
 const char *pa_status_string(pa_status status);
 

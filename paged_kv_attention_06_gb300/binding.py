@@ -79,6 +79,12 @@ def _load() -> ctypes.CDLL:
     lib.pa_kv_cache_context_len.restype = i32
     lib.pa_kv_cache_plan.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp]
     lib.pa_kv_cache_plan.restype = ctypes.c_int
+    lib.pa_kv_cache_snapshot_take.argtypes = [vp, ctypes.POINTER(vp)]
+    lib.pa_kv_cache_snapshot_take.restype = ctypes.c_int
+    lib.pa_kv_cache_restore.argtypes = [vp, vp]
+    lib.pa_kv_cache_restore.restype = ctypes.c_int
+    lib.pa_kv_cache_snapshot_destroy.argtypes = [vp]
+    lib.pa_kv_cache_snapshot_destroy.restype = None
     lib.pa_gather_kv.argtypes = [vp, vp, vp, vp, i32, pa_shape, i32, vp, vp, vp]
     lib.pa_gather_kv.restype = ctypes.c_int
     lib.pa_decode_dense.argtypes = [vp, vp, vp, vp, i32, ctypes.c_float, ctypes.c_int, vp,
@@ -407,6 +413,16 @@ class KVCache:
     def context_len(self, seq_id: int) -> int:
         return int(_lib.pa_kv_cache_context_len(self._h, int(seq_id)))
 
+    def snapshot(self) -> "KVCacheSnapshot":
+        """Copy of the bookkeeping, for restore() after a failed step."""
+        h = ctypes.c_void_p()
+        _check(_lib.pa_kv_cache_snapshot_take(self._h, ctypes.byref(h)),
+               "pa_kv_cache_snapshot_take")
+        return KVCacheSnapshot(h)
+
+    def restore(self, snapshot: "KVCacheSnapshot") -> None:
+        _check(_lib.pa_kv_cache_restore(self._h, snapshot._h), "pa_kv_cache_restore")
+
     def plan(self, seq_ids, new_tokens, max_pages: int, l_new: int):
         """One step: returns (block_table [n, max_pages], context_lens [n],
         slot_mapping [n, l_new]) as int32 numpy arrays; raises
@@ -422,3 +438,21 @@ class KVCache:
                                    int(l_new), bt.ctypes.data, cl.ctypes.data, sm.ctypes.data)
         _check(st, "pa_kv_cache_plan")
         return bt, cl, sm[:, :int(l_new)]
+
+
+class KVCacheSnapshot:
+    """A pa_kv_cache_snapshot handle (freed with the object)."""
+
+    def __init__(self, handle):
+        self._h = handle
+
+    def close(self) -> None:
+        if self._h:
+            _lib.pa_kv_cache_snapshot_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

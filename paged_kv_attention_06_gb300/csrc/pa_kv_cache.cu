@@ -78,6 +78,11 @@ void undo(pa_kv_cache* c, const std::vector<Taken>& log)
 
 }  // namespace
 
+struct pa_kv_cache_snapshot {
+    const pa_kv_cache* owner;
+    pa_kv_cache state;
+};
+
 extern "C" {
 
 pa_status pa_kv_cache_create(int32_t num_pages, int32_t page_size, pa_kv_cache** cache)
@@ -201,5 +206,28 @@ pa_status pa_kv_cache_plan(pa_kv_cache* cache, int32_t n, const int64_t* seq_ids
     }
     return PA_OK;
 }
+
+pa_status pa_kv_cache_snapshot_take(const pa_kv_cache* cache, pa_kv_cache_snapshot** snapshot)
+{
+    if (!cache || !snapshot)
+        return PA_ERR_INVALID_ARG;
+    pa_kv_cache_snapshot* s = new (std::nothrow) pa_kv_cache_snapshot;
+    if (!s)
+        return PA_ERR_NO_PAGES;
+    s->owner = cache;
+    s->state = *cache;
+    *snapshot = s;
+    return PA_OK;
+}
+
+pa_status pa_kv_cache_restore(pa_kv_cache* cache, const pa_kv_cache_snapshot* snapshot)
+{
+    if (!cache || !snapshot || snapshot->owner != cache)
+        return PA_ERR_INVALID_ARG;
+    *cache = snapshot->state;
+    return PA_OK;
+}
+
+void pa_kv_cache_snapshot_destroy(pa_kv_cache_snapshot* snapshot) { delete snapshot; }
 
 }  // extern "C"

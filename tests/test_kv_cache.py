@@ -117,3 +117,32 @@ def test_release_exactly_once_and_bad_arguments():
     # freed pages come back last-freed first: request 3 held pages 0, 1, 2
     bt, _, _ = c.plan([4], [2], 8, 2)
     assert int(bt[0, 0]) == int(np.asarray(bt)[0, 0]) == 2
+
+
+def test_snapshot_restore_rolls_back_a_step():
+    """Tutorial 13 section 7: a step that failed after its pages were planned
+    (its K/V write or launch failed) is undone by restoring the snapshot taken
+    before it; the cache then behaves exactly like one that never ran it."""
+    pa = _pa()
+    c, twin = pa.KVCache(16, 4), pa.KVCache(16, 4)
+    for x in (c, twin):
+        x.add(1)
+        x.add(2)
+        x.plan([1, 2], [6, 3], max_pages=8, l_new=6)
+        x.release(2)                                  # pages on the free list
+    snap = c.snapshot()
+    c.plan([1], [7], max_pages=8, l_new=7)            # the step that "failed"
+    c.release(1)
+    c.add(9)
+    c.plan([9], [5], max_pages=8, l_new=5)
+    c.restore(snap)
+    assert c.context_len(1) == twin.context_len(1) == 6
+    assert c.context_len(9) == -1 and c.free_pages == twin.free_pages
+    a, b = c.plan([1], [7], 8, 7), twin.plan([1], [7], 8, 7)
+    assert all(np.array_equal(u, v) for u, v in zip(a, b))
+    c.restore(snap)                                   # a snapshot can be restored again
+    assert c.context_len(1) == 6
+    other = pa.KVCache(16, 4)
+    with pytest.raises(pa.PagedAttentionError):       # snapshot of another cache
+        other.restore(snap)
+    snap.close()

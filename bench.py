@@ -863,28 +863,44 @@ def bench_prefill(pa, binding, torch, device, stream, steps=20):
     flush = torch.empty(int(2 * torch.cuda.get_device_properties(device).L2_cache_size),
                         dtype=torch.uint8, device=device)
     pa.pa_append_kv(kn, vn, kp, vp, sm, b.page_size)
-    app, att = [], []
-    for k in range(steps + 3):
-        flush.zero_()
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        e[0].record(stream)
-        pa.pa_append_kv(kn, vn, kp, vp, sm, b.page_size)
-        e[1].record(stream)
-        pa.pa_attention(q, kp, vp, bt, cl, b.page_size, scale=b.scale, causal=True, out=out,
-                        max_context_len=int(b.context_lens.max()))
-        e[2].record(stream)
-        if k >= 3:
-            app.append(e)
-    torch.cuda.synchronize()
-    st, flags = pa.pa_get_device_error()
-    if st:
-        raise RuntimeError(f"device error in prefill bench: {flags:#x}")
-    att_ms = float(np.median([e[1].elapsed_time(e[2]) for e in app]))
-    app_ms = float(np.median([e[0].elapsed_time(e[1]) for e in app]))
+    mcl = int(b.context_lens.max())
+
+    def timed(attend):
+        evs = []
+        for k in range(steps + 3):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+            pa.pa_append_kv(kn, vn, kp, vp, sm, b.page_size)
+            e[1].record(stream)
+            attend()
+            e[2].record(stream)
+            if k >= 3:
+                evs.append(e)
+        torch.cuda.synchronize()
+        st, flags = pa.pa_get_device_error()
+        if st:
+            raise RuntimeError(f"device error in prefill bench: {flags:#x}")
+        return (float(np.median([e[1].elapsed_time(e[2]) for e in evs])),
+                float(np.median([e[0].elapsed_time(e[1]) for e in evs])))
+
+    # The product path: pa_attention routes L = 512 to prefill; with 256
+    # (request, head pair, query tile) items on 152 SMs it takes the pairs
+    # kernel. Beside it, the split kernel forced through pa_prefill_split.
+    att_ms, app_ms = timed(lambda: pa.pa_attention(q, kp, vp, bt, cl, b.page_size, scale=b.scale,
+                                                   causal=True, out=out, max_context_len=mcl))
+    split_ms, _ = timed(lambda: pa.pa_prefill_split(q, kp, vp, bt, cl, b.page_size, scale=b.scale,
+                                                    causal=True, out=out))
+    items = b.B * ((b.L + 127) // 128) * (b.H_q // 2)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    kernel = "prefill_split_kernel" if 2 * items < 3 * sms else "prefill_pairs_kernel"
     flops = prefill_flops(b)
     _, app_bytes = step_bytes(b)
     return {"workload": b.name, "tflops": round(flops / (att_ms * 1e-3) / 1e12, 3),
-            "attention_ms": round(att_ms, 4), "append_ms": round(app_ms, 4),
+            "attention_ms": round(att_ms, 4), "kernel": kernel, "items": items,
+            "split_kernel": {"attention_ms": round(split_ms, 4),
+                             "tflops": round(flops / (split_ms * 1e-3) / 1e12, 3)},
+            "append_ms": round(app_ms, 4),
             "append_gbs": round(app_bytes / (app_ms * 1e-3) / 1e9, 2),
             "causal_useful_flops": flops, "steps": steps,
             "l2": "2x L2 buffer written before every step (outside the events)"}

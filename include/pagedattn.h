@@ -209,6 +209,42 @@ pa_status pa_prefill(const void *query, const void *key_pages,
                      int causal, void *out, pa_shape shape, void *stream);
 
 /*
+ * Bytes of device workspace pa_prefill_split needs for `shape` and
+ * page_size on the CURRENT device, or 0 when the shape takes a prefill
+ * kernel that needs none (head_dim 64, page_size < 8, an odd group size
+ * num_q_heads / num_kv_heads). The size depends only on the device's SM
+ * count (about 130 KiB per SM), not on the batch.
+ */
+size_t pa_prefill_workspace_bytes(pa_shape shape, int32_t page_size);
+
+/*
+ * Prefill attention with the same arguments, result and checks as
+ * pa_prefill, on a kernel that balances the work over the GPU: the K/V
+ * tiles of every (request, pair of query heads of one KV group, tile of 128
+ * query rows) form one stream, cut into equal ranges for a persistent grid
+ * of one block per SM (the split-KV idea of Week 3 Day 4, "Choose a
+ * Schedule for Each Query Shape", applied to the long-query schedule). An
+ * item cut by range boundaries is finished by the block holding its first
+ * tiles, which merges the partial softmax states its later pieces (done
+ * first by the following blocks) left in the workspace. The launch is
+ * cooperative (all blocks resident); where the device cannot hold every
+ * block at once, the call runs pa_prefill's kernels instead.
+ *   workspace        device memory of at least pa_prefill_workspace_bytes,
+ *                    256-byte aligned, any contents (nothing needs clearing;
+ *                    each launch tags its counters with its own stamp).
+ *                    Calls that share a workspace must not overlap on the GPU.
+ * Shapes for which pa_prefill_workspace_bytes is 0 run pa_prefill (the
+ * workspace is then not touched). PA_ERR_WORKSPACE when the workspace is
+ * missing, too small or misaligned. The output is the same softmax as
+ * pa_prefill's up to rounding (the pieces' states are combined in fp32).
+ */
+pa_status pa_prefill_split(const void *query, const void *key_pages,
+                           const void *value_pages, const int32_t *block_table,
+                           const int32_t *context_lens, int32_t page_size, float scale,
+                           int causal, void *out, pa_shape shape, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
  * Route chosen by pa_attention for these sizes: 0 = decode, 1 = prefill.
  * The rule sits at this boundary (Week 3 Day 4, "Choose a Schedule for Each
  * Query Shape": short queries take the vector decode schedule, long ones the
@@ -219,7 +255,11 @@ int32_t pa_attention_route(pa_shape shape, int32_t max_context_len);
 /*
  * Dispatching entry point: runs pa_decode or pa_prefill as
  * pa_attention_route says, with the same arguments. The workspace is
- * required only when the route is decode (pass NULL/0 otherwise).
+ * required only when the route is decode. On the prefill route, given a
+ * workspace of at least pa_prefill_workspace_bytes (256-byte aligned), it
+ * runs pa_prefill_split when the shape has fewer than 1.5 (request, head
+ * pair, 128-row query tile) items per SM, where whole blocks would leave
+ * SMs idle; otherwise (or with NULL / a smaller workspace) pa_prefill.
  */
 pa_status pa_attention(const void *query, const void *key_pages,
                        const void *value_pages, const int32_t *block_table,
@@ -325,7 +365,9 @@ void pa_debug_arm_wait_timeout(void);
  *   1  one query head per block;
  *   2  two query heads of one KV group per block, when the group size
  *      (num_q_heads / num_kv_heads) is even; otherwise as 1.
- * Any other value is taken as 0. Returns the previous setting. Results agree
+ * Settings 1 and 2 also hold for pa_prefill_split and for pa_attention given
+ * a prefill workspace (the workspace is then not used). Any other value is
+ * taken as 0. Returns the previous setting. Results agree
  * with the oracle under every setting; only the speed differs.
  */
 int pa_debug_prefill_variant(int variant);

@@ -10,7 +10,8 @@ _API = ("pa_append_kv", "pa_decode", "pa_prefill", "pa_attention", "pa_attention
         "pa_decode_workspace_bytes", "pa_get_device_error", "status_string", "version",
         "pa_shape", "PagedAttentionError", "decode_workspace", "make_shape",
         "pa_debug_arm_wait_timeout", "pa_debug_prefill_variant", "pa_decode_noalloc",
-        "pa_gather_kv", "pa_decode_dense", "KVCache", "KVCacheSnapshot")
+        "pa_gather_kv", "pa_decode_dense", "KVCache", "KVCacheSnapshot",
+        "pa_prefill_split", "pa_prefill_workspace_bytes", "prefill_workspace")
 
 
 def __getattr__(name):

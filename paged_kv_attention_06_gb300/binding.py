@@ -64,6 +64,10 @@ def _load() -> ctypes.CDLL:
     lib.pa_decode.restype = ctypes.c_int
     lib.pa_prefill.argtypes = attn + [vp]
     lib.pa_prefill.restype = ctypes.c_int
+    lib.pa_prefill_workspace_bytes.argtypes = [pa_shape, i32]
+    lib.pa_prefill_workspace_bytes.restype = sz
+    lib.pa_prefill_split.argtypes = attn + [vp, sz, vp]
+    lib.pa_prefill_split.restype = ctypes.c_int
     i64 = ctypes.c_int64
     lib.pa_kv_cache_create.argtypes = [i32, i32, ctypes.POINTER(vp)]
     lib.pa_kv_cache_create.restype = ctypes.c_int
@@ -155,6 +159,31 @@ def make_shape(query_shape, pages_shape, max_pages: int) -> pa_shape:
 
 _ws_lock = threading.Lock()
 _ws_cache = {}
+
+
+def _cached_workspace(need: int, device: torch.device) -> torch.Tensor:
+    with _ws_lock:
+        buf = _ws_cache.get(device.index)
+        if buf is None or buf.numel() < need:
+            buf = torch.zeros(max(need, 256), dtype=torch.uint8, device=device)
+            _ws_cache[device.index] = buf
+    return buf
+
+
+def prefill_workspace(shape: pa_shape, page_size: int,
+                      device: torch.device) -> Tuple[Optional[torch.Tensor], int]:
+    """(buffer, bytes) for pa_prefill_split, or (None, 0) when the shape's
+    prefill kernel needs none."""
+    need = pa_prefill_workspace_bytes(shape, page_size, device)
+    if need == 0:
+        return None, 0
+    return _cached_workspace(need, device), need
+
+
+def pa_prefill_workspace_bytes(shape: pa_shape, page_size: int,
+                               device: Optional[torch.device] = None) -> int:
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(_lib.pa_prefill_workspace_bytes(shape, int(page_size)))
 
 
 def decode_workspace(shape: pa_shape, device: torch.device) -> Tuple[torch.Tensor, int]:
@@ -249,6 +278,25 @@ def pa_prefill(query, key_pages, value_pages, block_table, context_lens, page_si
     return out
 
 
+def pa_prefill_split(query, key_pages, value_pages, block_table, context_lens, page_size: int,
+                     scale: Optional[float] = None, causal: bool = True, out=None,
+                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """pa_prefill on the kernel that spreads the K/V tiles evenly over the
+    SMs (needs a workspace; the library's shared one is used when none is
+    given)."""
+    shape, ptrs, scale, out = _attn_common(query, key_pages, value_pages, block_table,
+                                           context_lens, page_size, scale, out)
+    if workspace is None:
+        workspace, _ = prefill_workspace(shape, page_size, query.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib.pa_prefill_split(*ptrs, int(page_size), scale, int(bool(causal)),
+                               _dev_ptr(out, torch.bfloat16, "out"), shape, ws_ptr, ws_bytes,
+                               _stream(stream))
+    _check(st, "pa_prefill_split")
+    return out
+
+
 def pa_attention_route(query_shape, pages_shape, max_pages: int, max_context_len: int = 0) -> int:
     return int(_lib.pa_attention_route(make_shape(query_shape, pages_shape, max_pages),
                                        int(max_context_len)))
@@ -263,9 +311,11 @@ def pa_attention(query, key_pages, value_pages, block_table, context_lens, page_
                                            context_lens, page_size, scale, out)
     route = int(_lib.pa_attention_route(shape, int(max_context_len)))
     ws_ptr, ws_bytes = None, 0
-    if route == 0:
-        if workspace is None:
-            workspace, _ = decode_workspace(shape, query.device)
+    if route == 0 and workspace is None:
+        workspace, _ = decode_workspace(shape, query.device)
+    elif route == 1 and workspace is None:
+        workspace, _ = prefill_workspace(shape, page_size, query.device)
+    if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     st = _lib.pa_attention(*ptrs, int(page_size), scale, int(bool(causal)),
                            _dev_ptr(out, torch.bfloat16, "out"), shape, int(max_context_len),

@@ -196,17 +196,37 @@ pa_status encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uin
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
-// Prefill on tcgen05 (D = 128, page_size >= 8): one block per (request,
-// query head, tile of 128 query rows).
+// Workspace the split prefill kernel needs for this shape on this device, or
+// 0 when the shape takes another prefill kernel (head_dim 64, pages of fewer
+// than 8 tokens, an odd group size, or shared memory too small).
+size_t split_prefill_need(const pa_shape& s, int32_t page_size, const DeviceInfo* dev)
+{
+    if (s.head_dim != 128 || page_size < 8 || s.num_kv_heads <= 0 ||
+        s.num_q_heads % s.num_kv_heads != 0 || (s.num_q_heads / s.num_kv_heads) % 2 != 0)
+        return 0;
+    if (prefill_split_smem_bytes() > size_t(dev->max_smem_optin))
+        return 0;
+    return prefill_split_workspace_bytes(dev->sm_count);
+}
+
+// Prefill on tcgen05 (D = 128, page_size >= 8). With a workspace of at least
+// split_prefill_need bytes: the split kernel (K/V tiles spread evenly over
+// one block per SM); otherwise one block per (request, query head or head
+// pair, tile of 128 query rows).
 pa_status run_prefill_tc(const void* query, const void* key_pages, const void* value_pages,
                          const int32_t* block_table, const int32_t* context_lens,
                          int32_t page_size, float scale, int causal, void* out,
-                         const pa_shape& s, cudaStream_t stream)
+                         const pa_shape& s, cudaStream_t stream, void* workspace = nullptr,
+                         size_t workspace_bytes = 0)
 {
     DeviceInfo* dev;
     pa_status st = device_info(&dev);
     if (st != PA_OK)
         return st;
+    const size_t split_need = split_prefill_need(s, page_size, dev);
+    const bool split = t_prefill_variant == 0 && workspace && split_need > 0 &&
+                       workspace_bytes >= split_need &&
+                       (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0;
     // Two query heads of one KV group per block whenever the group size is
     // even (unless the one-head kernel is requested).
     bool pairs = t_prefill_variant != 1 && (s.num_q_heads / s.num_kv_heads) % 2 == 0;
@@ -244,6 +264,35 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     a.box_rows = int32_t(box);
     a.scale_log2 = scale * 1.4426950408889634f;
     a.causal = causal ? 1 : 0;
+    if (split) {
+        SplitPrefillArgs sa;
+        memset(&sa, 0, sizeof sa);
+        sa.out = a.out;
+        sa.block_table = a.block_table;
+        sa.context_lens = a.context_lens;
+        sa.err = a.err;
+        sa.B = a.B;
+        sa.H_q = a.H_q;
+        sa.H_kv = a.H_kv;
+        sa.L = a.L;
+        sa.ps = a.ps;
+        sa.max_pages = a.max_pages;
+        sa.num_pages = a.num_pages;
+        sa.G = a.G;
+        sa.n_qtiles = a.n_qtiles;
+        sa.box_rows = a.box_rows;
+        sa.scale_log2 = a.scale_log2;
+        sa.causal = a.causal;
+        cudaError_t e = launch_prefill_split(qmap, kmap, vmap, sa, dev->sm_count, workspace,
+                                             dev->id, stream);
+        if (e == cudaSuccess)
+            return PA_OK;
+        if (e != cudaErrorNotSupported && e != cudaErrorCooperativeLaunchTooLarge)
+            return PA_ERR_CUDA;
+        // The register split is not available, or not every block could be
+        // resident (another client holds SMs): the kernels below.
+        (void)cudaGetLastError();
+    }
     cudaError_t e = pairs ? launch_prefill_pairs(qmap, kmap, vmap, a, dev->id, stream)
                           : launch_prefill(qmap, kmap, vmap, a, dev->id, stream);
     if (pairs && e == cudaErrorNotSupported)   // register split not available: one head per block
@@ -534,6 +583,37 @@ pa_status pa_prefill(const void* query, const void* key_pages, const void* value
                         static_cast<cudaStream_t>(stream));
 }
 
+size_t pa_prefill_workspace_bytes(pa_shape shape, int32_t page_size)
+{
+    DeviceInfo* dev;
+    if (device_info(&dev) != PA_OK)
+        return 0;
+    return split_prefill_need(shape, page_size, dev);
+}
+
+pa_status pa_prefill_split(const void* query, const void* key_pages, const void* value_pages,
+                           const int32_t* block_table, const int32_t* context_lens,
+                           int32_t page_size, float scale, int causal, void* out, pa_shape shape,
+                           void* workspace, size_t workspace_bytes, void* stream)
+{
+    pa_status st = check_attention(query, key_pages, value_pages, block_table, context_lens,
+                                   page_size, scale, out, shape);
+    if (st != PA_OK)
+        return st;
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != PA_OK)
+        return st;
+    const size_t need = split_prefill_need(shape, page_size, dev);
+    if (need == 0)   // another prefill kernel serves this shape; no workspace used
+        return pa_prefill(query, key_pages, value_pages, block_table, context_lens, page_size,
+                          scale, causal, out, shape, stream);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PA_ERR_WORKSPACE;
+    return run_prefill_tc(query, key_pages, value_pages, block_table, context_lens, page_size,
+                          scale, causal, out, shape, static_cast<cudaStream_t>(stream), workspace,
+                          workspace_bytes);
+}
+
 int32_t pa_attention_route(pa_shape shape, int32_t max_context_len)
 {
     (void)max_context_len;
@@ -555,6 +635,25 @@ pa_status pa_attention(const void* query, const void* key_pages, const void* val
         return pa_decode(query, key_pages, value_pages, block_table, context_lens, page_size,
                          scale, causal, out, shape, max_context_len, workspace, workspace_bytes,
                          stream);
+    if (workspace) {
+        // The split kernel pays for its balance at every piece boundary; it
+        // is the faster one when the (request, head pair, query tile) items
+        // are too few to fill the SMs in whole waves (measured: 1.75x on one
+        // 512-row chunk after a 16k prefix, 64 items; equal at 1.7 items per
+        // SM; slower beyond).
+        DeviceInfo* dev;
+        pa_status st = device_info(&dev);
+        if (st != PA_OK)
+            return st;
+        const size_t need = split_prefill_need(shape, page_size, dev);
+        const int64_t items = int64_t(shape.batch) * ((int64_t(shape.q_len) + 127) / 128) *
+                              (shape.num_q_heads / 2);
+        if (need > 0 && workspace_bytes >= need && 2 * items < 3 * int64_t(dev->sm_count) &&
+            (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0)
+            return pa_prefill_split(query, key_pages, value_pages, block_table, context_lens,
+                                    page_size, scale, causal, out, shape, workspace,
+                                    workspace_bytes, stream);
+    }
     return pa_prefill(query, key_pages, value_pages, block_table, context_lens, page_size, scale,
                       causal, out, shape, stream);
 }

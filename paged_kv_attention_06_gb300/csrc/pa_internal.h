@@ -109,6 +109,33 @@ struct PrefillArgs {
     int32_t causal;
 };
 
+// Prefill with the K/V tiles of all (request, head pair, query tile) items
+// split evenly over a persistent grid (one block per SM, all resident); an
+// item cut by a block boundary is finished by the block that holds its first
+// tiles, which merges the states the later pieces left in the workspace.
+struct SplitPrefillArgs {
+    uint16_t* out;                // [B, H_q, L, 128]
+    const int32_t* block_table;   // [B, max_pages]
+    const int32_t* context_lens;  // [B]
+    unsigned* err;
+    float* state;                 // [grid][head 2][32][128][4]
+    float2* state_ml;             // [grid][head 2][128] (m, l)
+    unsigned long long* flags;    // [grid][head 2][4 warps]: stamp when written
+    uint64_t stamp;               // this launch's stamp (never 0)
+    int32_t B, H_q, H_kv, L, ps, max_pages, num_pages;
+    int32_t G;          // H_q / H_kv (even)
+    int32_t n_qtiles;   // ceil(L / 128)
+    int32_t box_rows;   // rows per K/V TMA box: min(ps, 128)
+    float scale_log2;
+    int32_t causal;
+};
+
+size_t prefill_split_smem_bytes();
+size_t prefill_split_workspace_bytes(int grid);
+cudaError_t launch_prefill_split(const CUtensorMap& q_map, const CUtensorMap& key_map,
+                                 const CUtensorMap& value_map, SplitPrefillArgs a, int grid,
+                                 void* workspace, int device, cudaStream_t stream);
+
 size_t prefill_smem_bytes();
 size_t prefill_pairs_smem_bytes();
 cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& key_map,

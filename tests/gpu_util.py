@@ -53,9 +53,10 @@ def gpu_step(db: DeviceBatch, route: str = "attention", append: bool = True):
     if append and b.L_new > 0:
         pa.pa_append_kv(db.key_new, db.value_new, db.key_pages, db.value_pages,
                         db.slot_mapping, b.page_size)
-    fn = {"attention": pa.pa_attention, "decode": pa.pa_decode, "prefill": pa.pa_prefill}[route]
+    fn = {"attention": pa.pa_attention, "decode": pa.pa_decode, "prefill": pa.pa_prefill,
+          "prefill_split": pa.pa_prefill_split}[route]
     kwargs = dict(scale=b.scale, causal=b.causal)
-    if route != "prefill":
+    if route in ("attention", "decode"):
         kwargs["max_context_len"] = int(b.context_lens.max()) if b.B else 0
     return fn(db.query, db.key_pages, db.value_pages, db.block_table, db.context_lens,
               b.page_size, **kwargs)

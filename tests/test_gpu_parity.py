@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 from gpu_util import (DeviceBatch, assert_close, check_no_device_error, gpu_step, host_bits,
                       host_f64, oracle_out, oracle_pages)
@@ -256,13 +257,16 @@ def test_non_default_stream():
 # The tensor-core prefill path (head_dim 128, page_size >= 8) at its edges
 
 
-@pytest.fixture(params=[1, 2], ids=["one_head", "head_pairs"])
+@pytest.fixture(params=[1, 2, 0], ids=["one_head", "head_pairs", "split"])
 def prefill_variant(request):
     """Runs the test under each tensor-core prefill kernel (pairs need an even
-    group size; odd groups take the one-head kernel under either setting)."""
+    group size; odd groups take the one-head kernel under either setting; the
+    split kernel runs through pa_prefill_split with a workspace, and odd
+    groups there also fall back to the one-head kernel). Yields the route for
+    gpu_step."""
     import paged_kv_attention_06_gb300 as pa
     prev = pa.pa_debug_prefill_variant(request.param)
-    yield request.param
+    yield "prefill_split" if request.param == 0 else "prefill"
     pa.pa_debug_prefill_variant(prev)
 
 
@@ -274,7 +278,7 @@ def test_tc_prefill_page_sizes(ps, causal, H_q, H_kv, prefill_variant):
     b = wl.build_batch("tcprefill", B=4, H_q=H_q, H_kv=H_kv, D=128, page_size=ps, L=129,
                        context_lens=lens, seed=ps + int(causal), causal=causal,
                        placement="churn")
-    out = gpu_step(DeviceBatch(b), route="prefill")
+    out = gpu_step(DeviceBatch(b), route=prefill_variant)
     check_no_device_error()
     kp, vp = oracle_pages(b)
     assert_close(host_f64(out), oracle_out(b, kp, vp), f"tc prefill ps={ps} causal={causal}")
@@ -286,7 +290,7 @@ def test_tc_prefill_rows_without_keys_and_empty_context(H_q, H_kv, prefill_varia
     # positions see no key and must return zeros.
     b = wl.build_batch("tcempty", B=3, H_q=H_q, H_kv=H_kv, D=128, page_size=16, L=200,
                        context_lens=[0, 50, 199], seed=4, L_new=0)
-    out = host_f64(gpu_step(DeviceBatch(b), route="prefill"))
+    out = host_f64(gpu_step(DeviceBatch(b), route=prefill_variant))
     check_no_device_error()
     assert np.all(out[0] == 0)
     assert np.all(out[1, :, :150] == 0) and np.all(out[2, :, :1] == 0)
@@ -300,7 +304,7 @@ def test_tc_prefill_bad_page_id_is_flagged(prefill_variant):
                        context_lens=[100, 40], seed=8, L_new=0)
     bt = b.block_table.copy()
     bt[0, 2] = b.num_pages + 7
-    gpu_step(DeviceBatch(dataclasses.replace(b, block_table=bt)), route="prefill")
+    gpu_step(DeviceBatch(dataclasses.replace(b, block_table=bt)), route=prefill_variant)
     st, flags = pa.pa_get_device_error()
     assert st == pa.PA_ERR_DEVICE_BOUNDS and flags & pa.PA_DEVERR_PAGE_ID
 
@@ -309,10 +313,102 @@ def test_tc_prefill_long_context_gqa(prefill_variant):
     b = wl.build_batch("tclong", B=2, H_q=16, H_kv=2, D=128, page_size=16, L=384,
                        context_lens=[3000, 1500], seed=12, placement="permutation")
     db = DeviceBatch(b)
-    out = gpu_step(db, route="prefill")
+    out = gpu_step(db, route=prefill_variant)
     check_no_device_error()
     kp, vp = oracle_pages(b)
     rows = np.asarray([(r, h, i) for r in range(2) for h in range(16)
                        for i in (0, 1, 127, 128, 255, 256, 383)], dtype=np.int32)
     got = host_f64(out)[rows[:, 0], rows[:, 1], rows[:, 2]]
     assert_close(got, oracle_out(b, kp, vp, rows=rows), "tc prefill long")
+
+
+# ----------------------------------------------------------------------------
+# The split prefill kernel (K/V tiles of all query tiles spread evenly over
+# one block per SM; items cut by a block boundary are merged from their
+# pieces' states)
+
+
+def _sampled_rows(b, rng, extra=6):
+    rows = []
+    for r in range(b.B):
+        for i in sorted(set([0, 1, 63, 64, 127, 128, b.L // 2, b.L - 2, b.L - 1] +
+                            list(rng.integers(0, b.L, extra)))):
+            if 0 <= i < b.L:
+                for h in range(b.H_q):
+                    rows.append((r, h, i))
+    return np.asarray(rows, dtype=np.int32)
+
+
+def test_split_prefill_chunk512_sampled_rows():
+    b = wl.make_workload("prefill_chunk512")
+    db = DeviceBatch(b)
+    out = gpu_step(db, route="prefill_split")
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    rows = _sampled_rows(b, np.random.default_rng(1))
+    got = host_f64(out)[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(got, oracle_out(b, kp, vp, rows=rows), "split prefill_chunk512")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_split_prefill_items_cut_into_many_pieces(causal):
+    # One request, 2 query tiles x 4 head pairs = 8 items of ~64 K/V tiles
+    # over ~150 blocks: every item is cut into ~19 pieces.
+    b = wl.build_batch("splitlong", B=1, H_q=8, H_kv=2, D=128, page_size=16, L=256,
+                       context_lens=[8000], seed=21, causal=causal, placement="permutation")
+    out = gpu_step(DeviceBatch(b), route="prefill_split")
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    rows = _sampled_rows(b, np.random.default_rng(2), extra=10)
+    got = host_f64(out)[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(got, oracle_out(b, kp, vp, rows=rows), f"split many pieces causal={causal}")
+
+
+def test_split_prefill_fewer_units_than_blocks():
+    # 3 short requests: far fewer K/V tiles than blocks (most blocks get an
+    # empty range and leave at once); every row compared.
+    b = wl.build_batch("splitsmall", B=3, H_q=4, H_kv=2, D=128, page_size=16, L=20,
+                       context_lens=[20, 150, 300], seed=22, placement="churn")
+    out = gpu_step(DeviceBatch(b), route="prefill_split")
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), "split few units")
+
+
+def test_split_prefill_workspace_contents_and_repeat():
+    """Any workspace contents give the same output, and two runs are bit
+    identical (the merge order is fixed)."""
+    import paged_kv_attention_06_gb300 as pa
+    b = wl.build_batch("splitws", B=2, H_q=8, H_kv=2, D=128, page_size=16, L=300,
+                       context_lens=[2500, 900], seed=23, placement="churn")
+    db = DeviceBatch(b)
+    gpu_step(db, route="prefill_split")            # the append, once
+    shape = pa.make_shape(db.query.shape, db.key_pages.shape, db.block_table.shape[1])
+    need = pa.pa_prefill_workspace_bytes(shape, b.page_size)
+    assert need > 0
+    outs = []
+    for fill in (0x00, 0xFF, 0x5A):
+        ws = torch.full((need,), fill, dtype=torch.uint8, device="cuda")
+        outs.append(pa.pa_prefill_split(db.query, db.key_pages, db.value_pages, db.block_table,
+                                        db.context_lens, b.page_size, scale=b.scale,
+                                        causal=b.causal, workspace=ws))
+        check_no_device_error()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    kp, vp = b.key_pages.copy(), b.value_pages.copy()
+    oracle.append_kv(b.key_new, b.value_new, kp, vp, b.slot_mapping, b.page_size)
+    assert_close(host_f64(outs[0]), oracle_out(b, kp, vp), "split workspace contents")
+
+
+def test_split_prefill_rejects_small_workspace():
+    import paged_kv_attention_06_gb300 as pa
+    b = wl.build_batch("splitsmallws", B=1, H_q=4, H_kv=2, D=128, page_size=16, L=64,
+                       context_lens=[200], seed=24, L_new=0)
+    db = DeviceBatch(b)
+    shape = pa.make_shape(db.query.shape, db.key_pages.shape, db.block_table.shape[1])
+    need = pa.pa_prefill_workspace_bytes(shape, b.page_size)
+    ws = torch.empty((need - 256,), dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PagedAttentionError) as e:
+        pa.pa_prefill_split(db.query, db.key_pages, db.value_pages, db.block_table,
+                            db.context_lens, b.page_size, workspace=ws)
+    assert e.value.status == pa.PA_ERR_WORKSPACE

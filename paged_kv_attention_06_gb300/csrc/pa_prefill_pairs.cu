@@ -212,200 +212,200 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     // Registers from the loader / MMA warpgroup (warps 0-3) to the two softmax
     // warpgroups: 128 x kRegsProducer + 256 x kRegsSoftmax <= 384 x the launch
-    // count (checked on the host before every launch).
-    if (warp < 4)
+    // count (checked on the host before every launch). Each change sits at the
+    // top of its warpgroup's branch, so that the branch is compiled to it.
+    if (warp < 4) {
         setmaxnreg_dec<kRegsProducer>();
-    else
-        setmaxnreg_inc<kRegsSoftmax>();
-
-    if ((warp == 0 || warp == 2 || warp == 3) && nt > 0) {
-        // ===================== loaders =====================================
-        // Box k of a tile goes to loader k mod 3; each loader arrives on the
-        // stage barrier with its own byte count.
-        const int li = warp == 0 ? 0 : warp - 1;     // 0, 1, 2
-        // K/V tiles are read again by the other query tiles and head pairs
-        // of the same request and KV group: keep them in L2.
-        const uint64_t policy = l2_policy_evict_last();
-        if (lane == 0 && li == 0) {
-            prefetch_tensormap(&q_map);
-            prefetch_tensormap(&key_map);
-            prefetch_tensormap(&value_map);
-            mbar_arrive_expect_tx(&bar[kQFull], 2u * Layout::kMat);
-            for (int h = 0; h < 2; ++h) {
-                const int qrow = (b * a.H_q + hq0 + h) * a.L + row0;
-                uint8_t* d = smem + Layout::kQ + h * Layout::kMat;
-                tma_load_2d(d, &q_map, 0, qrow, &bar[kQFull], policy);
-                tma_load_2d(d + Layout::kHalf, &q_map, 64, qrow, &bar[kQFull], policy);
+        if (warp != 1 && nt > 0) {
+            // ===================== loaders =====================================
+            // Box k of a tile goes to loader k mod 3; each loader arrives on the
+            // stage barrier with its own byte count.
+            const int li = warp == 0 ? 0 : warp - 1;     // 0, 1, 2
+            // K/V tiles are read again by the other query tiles and head pairs
+            // of the same request and KV group: keep them in L2.
+            const uint64_t policy = l2_policy_evict_last();
+            if (lane == 0 && li == 0) {
+                prefetch_tensormap(&q_map);
+                prefetch_tensormap(&key_map);
+                prefetch_tensormap(&value_map);
+                mbar_arrive_expect_tx(&bar[kQFull], 2u * Layout::kMat);
+                for (int h = 0; h < 2; ++h) {
+                    const int qrow = (b * a.H_q + hq0 + h) * a.L + row0;
+                    uint8_t* d = smem + Layout::kQ + h * Layout::kMat;
+                    tma_load_2d(d, &q_map, 0, qrow, &bar[kQFull], policy);
+                    tma_load_2d(d + Layout::kHalf, &q_map, 64, qrow, &bar[kQFull], policy);
+                }
             }
-        }
-        const int box = a.box_rows;                  // min(ps, 128)
-        const int32_t* bt = a.block_table + int64_t(b) * a.max_pages;
-        const int my_box = li + 3 * lane;
-        auto n_boxes = [&](int j) {
-            const int key0 = j * kKeys;
-            return (min(n, key0 + kKeys) - key0 + box - 1) / box;
-        };
-        // Raw block-table entry of this lane's box in tile j, loaded ahead
-        // of use and checked at use. The load is unconditional (entry 0 when
-        // the box does not exist) so that nothing waits for it before use.
-        auto fetch_page = [&](int j) -> int {
-            const bool live = j < nt && my_box < n_boxes(j);
-            return bt[live ? (j * kKeys + my_box * box) / a.ps : 0];
-        };
-        auto pool_row = [&](int j, int phys) -> int {
-            if (unsigned(phys) >= unsigned(a.num_pages)) {
-                atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
-                phys = 0;
-            }
-            const int tok = j * kKeys + my_box * box;
-            return (phys * a.H_kv + hk) * a.ps + (tok - (tok / a.ps) * a.ps);
-        };
-        auto load = [&](int j, bool is_v, int phys) {
-            const int nbox = n_boxes(j);
-            const int mine = nbox > li ? (nbox - li + 2) / 3 : 0;
-            const int s = j & 1;
-            const int full = (is_v ? kVFull : kKFull) + s;
-            const int empty = (is_v ? kVEmpty : kKEmpty) + s;
-            const bool ok = mbar_wait_warp(&bar[empty], ((j >> 1) & 1) ^ 1u, misc, a.err);
-            if (ok) {
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&bar[full], uint32_t(mine) * box * 128u * 2u);
+            const int box = a.box_rows;                  // min(ps, 128)
+            const int32_t* bt = a.block_table + int64_t(b) * a.max_pages;
+            const int my_box = li + 3 * lane;
+            auto n_boxes = [&](int j) {
+                const int key0 = j * kKeys;
+                return (min(n, key0 + kKeys) - key0 + box - 1) / box;
+            };
+            // Raw block-table entry of this lane's box in tile j, loaded ahead
+            // of use and checked at use. The load is unconditional (entry 0 when
+            // the box does not exist) so that nothing waits for it before use.
+            auto fetch_page = [&](int j) -> int {
+                const bool live = j < nt && my_box < n_boxes(j);
+                return bt[live ? (j * kKeys + my_box * box) / a.ps : 0];
+            };
+            auto pool_row = [&](int j, int phys) -> int {
+                if (unsigned(phys) >= unsigned(a.num_pages)) {
+                    atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
+                    phys = 0;
+                }
+                const int tok = j * kKeys + my_box * box;
+                return (phys * a.H_kv + hk) * a.ps + (tok - (tok / a.ps) * a.ps);
+            };
+            auto load = [&](int j, bool is_v, int phys) {
+                const int nbox = n_boxes(j);
+                const int mine = nbox > li ? (nbox - li + 2) / 3 : 0;
+                const int s = j & 1;
+                const int full = (is_v ? kVFull : kKFull) + s;
+                const int empty = (is_v ? kVEmpty : kKEmpty) + s;
+                const bool ok = mbar_wait_warp(&bar[empty], ((j >> 1) & 1) ^ 1u, misc, a.err);
+                if (ok) {
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&bar[full], uint32_t(mine) * box * 128u * 2u);
+                    __syncwarp();
+                    if (my_box < nbox) {
+                        const int row = pool_row(j, phys);
+                        uint8_t* d = smem + (is_v ? Layout::kV : Layout::kK) + s * Layout::kMat +
+                                     my_box * box * 128;
+                        const CUtensorMap* m = is_v ? &value_map : &key_map;
+                        tma_load_2d(d, m, 0, row, &bar[full], policy);
+                        tma_load_2d(d + Layout::kHalf, m, 64, row, &bar[full], policy);
+                    }
+                }
                 __syncwarp();
-                if (my_box < nbox) {
-                    const int row = pool_row(j, phys);
-                    uint8_t* d = smem + (is_v ? Layout::kV : Layout::kK) + s * Layout::kMat +
-                                 my_box * box * 128;
-                    const CUtensorMap* m = is_v ? &value_map : &key_map;
-                    tma_load_2d(d, m, 0, row, &bar[full], policy);
-                    tma_load_2d(d + Layout::kHalf, m, 64, row, &bar[full], policy);
+            };
+            // Order of need: K_0, V_0, K_1, V_1, ... (S for tile j + 1 follows
+            // P V of tile j). K runs one tile ahead of V. Page ids are fetched
+            // two tiles ahead in a ring of three registers, the loop unrolled
+            // over the ring so that no pending load result is ever copied.
+            int pg[3];
+            pg[0] = fetch_page(0);
+            pg[1] = fetch_page(1);
+            load(0, false, pg[0]);
+            for (int j0 = 0; j0 < nt; j0 += 3) {
+    #pragma unroll
+                for (int u = 0; u < 3; ++u) {
+                    const int j = j0 + u;
+                    if (j < nt) {
+                        pg[(u + 2) % 3] = fetch_page(j + 2);
+                        load(j, true, pg[u]);
+                        if (j + 1 < nt)
+                            load(j + 1, false, pg[(u + 1) % 3]);
+                    }
                 }
             }
-            __syncwarp();
-        };
-        // Order of need: K_0, V_0, K_1, V_1, ... (S for tile j + 1 follows
-        // P V of tile j). K runs one tile ahead of V. Page ids are fetched
-        // two tiles ahead in a ring of three registers, the loop unrolled
-        // over the ring so that no pending load result is ever copied.
-        int pg[3];
-        pg[0] = fetch_page(0);
-        pg[1] = fetch_page(1);
-        load(0, false, pg[0]);
-        for (int j0 = 0; j0 < nt; j0 += 3) {
-#pragma unroll
-            for (int u = 0; u < 3; ++u) {
-                const int j = j0 + u;
-                if (j < nt) {
-                    pg[(u + 2) % 3] = fetch_page(j + 2);
-                    load(j, true, pg[u]);
-                    if (j + 1 < nt)
-                        load(j + 1, false, pg[(u + 1) % 3]);
+            // No copy may still be landing when the block exits: wait (bounded)
+            // for the last two stages of both streams.
+            for (int j = max(0, nt - 2); j < nt; ++j) {
+                mbar_wait_bounded(&bar[kKFull + (j & 1)], (j >> 1) & 1, misc, a.err);
+                mbar_wait_bounded(&bar[kVFull + (j & 1)], (j >> 1) & 1, misc, a.err);
+            }
+        } else if (warp == 1 && nt > 0) {
+            // ===================== MMA issue (one elected thread) ==============
+            // The whole warp runs the loop (waits are warp-uniform, which costs
+            // less than branches in a lone lane); one elected lane issues. The
+            // first wait after a tcgen05.commit costs about 0.1 us even on a
+            // completed phase, so the waits that are normally already satisfied
+            // (the other head's P, the next K and V tiles) are taken right after
+            // a wait that has to take that long anyway (P_h V done), or before a
+            // commit.
+            const bool leader = elect_one();
+            const uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
+            const uint32_t idesc_pv = idesc_bf16_f32(kRows, 128, 1);
+            // Base descriptors built once; every k-step is one add.
+            const uint64_t dq0 = kmajor_base(sQ), dq1 = desc_advance(dq0, Layout::kMat);
+            const uint64_t dk0 = kmajor_base(sK), dk1 = desc_advance(dk0, Layout::kMat);
+            const uint64_t dv0 = mnmajor_base(sV), dv1 = desc_advance(dv0, Layout::kMat);
+            auto s_mmas = [&](int h, int j) {
+                if (leader) {
+                    const uint64_t da = h ? dq1 : dq0;
+                    const uint64_t db = (j & 1) ? dk1 : dk0;
+                    const uint32_t d = tmem + col_s(h);
+    #pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc_mma_bf16(d, desc_advance(da, kmajor_off(kk)), desc_advance(db, kmajor_off(kk)),
+                                    idesc_s, kk > 0);
                 }
-            }
-        }
-        // No copy may still be landing when the block exits: wait (bounded)
-        // for the last two stages of both streams.
-        for (int j = max(0, nt - 2); j < nt; ++j) {
-            mbar_wait_bounded(&bar[kKFull + (j & 1)], (j >> 1) & 1, misc, a.err);
-            mbar_wait_bounded(&bar[kVFull + (j & 1)], (j >> 1) & 1, misc, a.err);
-        }
-    } else if (warp == 1 && nt > 0) {
-        // ===================== MMA issue (one elected thread) ==============
-        // The whole warp runs the loop (waits are warp-uniform, which costs
-        // less than branches in a lone lane); one elected lane issues. The
-        // first wait after a tcgen05.commit costs about 0.1 us even on a
-        // completed phase, so the waits that are normally already satisfied
-        // (the other head's P, the next K and V tiles) are taken right after
-        // a wait that has to take that long anyway (P_h V done), or before a
-        // commit.
-        const bool leader = elect_one();
-        const uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
-        const uint32_t idesc_pv = idesc_bf16_f32(kRows, 128, 1);
-        // Base descriptors built once; every k-step is one add.
-        const uint64_t dq0 = kmajor_base(sQ), dq1 = desc_advance(dq0, Layout::kMat);
-        const uint64_t dk0 = kmajor_base(sK), dk1 = desc_advance(dk0, Layout::kMat);
-        const uint64_t dv0 = mnmajor_base(sV), dv1 = desc_advance(dv0, Layout::kMat);
-        auto s_mmas = [&](int h, int j) {
-            if (leader) {
-                const uint64_t da = h ? dq1 : dq0;
-                const uint64_t db = (j & 1) ? dk1 : dk0;
-                const uint32_t d = tmem + col_s(h);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_bf16(d, desc_advance(da, kmajor_off(kk)), desc_advance(db, kmajor_off(kk)),
-                                idesc_s, kk > 0);
-            }
-            __syncwarp();
-        };
-        auto pv_mmas = [&](int h, int j) {
-            if (leader) {
-                const uint64_t db = (j & 1) ? dv1 : dv0;
-                const uint32_t d = tmem + col_o(h);
-                const uint32_t pa = tmem + col_s(h) + kPCol;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_bf16_ts(d, pa + 8u * kk, desc_advance(db, mnmajor_off(kk)), idesc_pv,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            __syncwarp();
-        };
-        auto commit = [&](int b) {
-            if (leader)
-                tc_commit(&bar[b]);
-            __syncwarp();
-        };
-        auto wait = [&](int b, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait_lean(&bar[b], parity, misc, a.err));
-        };
-        bool ok = wait(kQFull, 0) && wait(kKFull, 0);
-        if (ok) {
-            tc_fence_after();
-            s_mmas(0, 0);
-            commit(kSFull);
-            s_mmas(1, 0);
-            ok = wait(kVFull, 0) && (nt < 2 || wait(kKFull + 1, 0));
-            commit(kSFull + 1);
-            commit(kKEmpty);
-        }
-        for (int j = 0; j < nt && ok; ++j) {
-            const bool more = j + 1 < nt;
-            // head 0: P_0 V_j, then S_0 for tile j + 1 once P_0 V_j is done
-            // (S_0 overwrites P_0)
-            if (!wait(kPFull, j & 1))
-                break;
-            tc_fence_after();
-            pv_mmas(0, j);
-            commit(kPVDone);
-            if (!wait(kPVDone, j & 1))
-                break;
-            tc_fence_after();
-            if (more)
-                s_mmas(0, j + 1);
-            ok = wait(kPFull + 1, j & 1);
-            if (more)
-                commit(kSFull);
-            if (!ok)
-                break;
-            // head 1: P_1 V_j, then S_1 for tile j + 1
-            tc_fence_after();
-            pv_mmas(1, j);
-            commit(kPVDone + 1);
-            commit(kVEmpty + (j & 1));
-            if (!wait(kPVDone + 1, j & 1))
-                break;
-            if (more) {
+                __syncwarp();
+            };
+            auto pv_mmas = [&](int h, int j) {
+                if (leader) {
+                    const uint64_t db = (j & 1) ? dv1 : dv0;
+                    const uint32_t d = tmem + col_o(h);
+                    const uint32_t pa = tmem + col_s(h) + kPCol;
+    #pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc_mma_bf16_ts(d, pa + 8u * kk, desc_advance(db, mnmajor_off(kk)), idesc_pv,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                __syncwarp();
+            };
+            auto commit = [&](int b) {
+                if (leader)
+                    tc_commit(&bar[b]);
+                __syncwarp();
+            };
+            auto wait = [&](int b, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait_lean(&bar[b], parity, misc, a.err));
+            };
+            bool ok = wait(kQFull, 0) && wait(kKFull, 0);
+            if (ok) {
                 tc_fence_after();
-                s_mmas(1, j + 1);
-                // the next tile's V and the tile after's K, before the commit
-                ok = wait(kVFull + ((j + 1) & 1), ((j + 1) >> 1) & 1) &&
-                     (j + 2 >= nt || wait(kKFull + (j & 1), ((j + 2) >> 1) & 1));
+                s_mmas(0, 0);
+                commit(kSFull);
+                s_mmas(1, 0);
+                ok = wait(kVFull, 0) && (nt < 2 || wait(kKFull + 1, 0));
                 commit(kSFull + 1);
-                commit(kKEmpty + ((j + 1) & 1));
+                commit(kKEmpty);
             }
+            for (int j = 0; j < nt && ok; ++j) {
+                const bool more = j + 1 < nt;
+                // head 0: P_0 V_j, then S_0 for tile j + 1 once P_0 V_j is done
+                // (S_0 overwrites P_0)
+                if (!wait(kPFull, j & 1))
+                    break;
+                tc_fence_after();
+                pv_mmas(0, j);
+                commit(kPVDone);
+                if (!wait(kPVDone, j & 1))
+                    break;
+                tc_fence_after();
+                if (more)
+                    s_mmas(0, j + 1);
+                ok = wait(kPFull + 1, j & 1);
+                if (more)
+                    commit(kSFull);
+                if (!ok)
+                    break;
+                // head 1: P_1 V_j, then S_1 for tile j + 1
+                tc_fence_after();
+                pv_mmas(1, j);
+                commit(kPVDone + 1);
+                commit(kVEmpty + (j & 1));
+                if (!wait(kPVDone + 1, j & 1))
+                    break;
+                if (more) {
+                    tc_fence_after();
+                    s_mmas(1, j + 1);
+                    // the next tile's V and the tile after's K, before the commit
+                    ok = wait(kVFull + ((j + 1) & 1), ((j + 1) >> 1) & 1) &&
+                         (j + 2 >= nt || wait(kKFull + (j & 1), ((j + 2) >> 1) & 1));
+                    commit(kSFull + 1);
+                    commit(kKEmpty + ((j + 1) & 1));
+                }
+            }
+            // Every MMA issued completes before the block ends.
+            commit(kMmaDone);
+            wait(kMmaDone, 0);
         }
-        // Every MMA issued completes before the block ends.
-        commit(kMmaDone);
-        wait(kMmaDone, 0);
-    } else if (warp >= 4) {
+    } else {
+        setmaxnreg_inc<kRegsSoftmax>();
         // ===================== softmax: one warpgroup per head =============
         const int head = (warp - 4) >> 2;            // 0: warps 4-7, 1: warps 8-11
         const int w4 = warp & 3;                     // TMEM lane quarter of this warp

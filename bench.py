@@ -291,6 +291,9 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=8.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-shapes", action="store_true",
+                    help="time both prefill kernels on chunked-prefill shapes and exit")
+    ap.add_argument("--shape", default=None, help="with --prefill-shapes: only this shape")
     ap.add_argument("--serving-trace", action="store_true",
                     help="run the synthetic serving trace through pa_kv_cache and exit")
     ap.add_argument("--dense-gather", action="store_true",
@@ -314,6 +317,9 @@ def main(argv=None):
 
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
+    if args.prefill_shapes:
+        print(json.dumps({"prefill_shapes": prefill_shapes(torch, device, args.shape)}))
+        return 0
     if args.serving_trace:
         serving_trace(torch, device)            # warm-up run (builds, first calls)
         print(json.dumps({"serving_trace": serving_trace(torch, device)}))
@@ -844,6 +850,74 @@ def serving_trace(torch, device, n_seqs=16, batch=4, prompt=(128, 1024), output=
                       "prompt": list(prompt), "output": list(output)},
             "timing": "wall clock over the whole trace (one device sync per step); device "
                       "times from CUDA events around each append and attention call"}
+
+
+PREFILL_SHAPES = [
+    # (name, B, L, context_lens): H_q = 32, H_kv = 8, D = 128, page_size 16
+    ("chunk512_b4", 4, 512, [1866, 2285, 710, 2052]),
+    ("chunk512_b1_prefix16k", 1, 512, [16384 + 512]),
+    ("chunk1024_b2_prefix8k", 2, 1024, [9216, 5000]),
+    ("prompt2048_b1", 1, 2048, [2048]),
+    ("chunk256_b8_mixed", 8, 256, [300, 4000, 800, 2500, 256, 6000, 1200, 3300]),
+    ("chunk512_b16", 16, 512, [2347, 3567, 1221, 3885, 597, 1860, 2978, 3327,
+                               2150, 802, 1462, 3739, 2811, 1028, 3300, 2444]),
+]
+
+
+def prefill_shapes(torch, device, only=None, steps=15):
+    """Both tensor-core prefill kernels (pa_prefill: one block per request x
+    head pair x query tile; pa_prefill_split: K/V tiles spread over one block
+    per SM) on chunked-prefill shapes with few and many query-tile items,
+    L2 flushed before every call, CUDA events. Inputs: seeded N(0,1) K/V
+    already in the pages (no append), random page permutation."""
+    import paged_kv_attention_06_gb300 as pa
+    flush = torch.empty(int(2 * torch.cuda.get_device_properties(device).L2_cache_size),
+                        dtype=torch.uint8, device=device)
+
+    def to_dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    def timeit(fn):
+        evs = []
+        for k in range(steps + 3):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            if k >= 3:
+                evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return float(np.median([x.elapsed_time(y) for x, y in evs])) * 1e3
+
+    rows = []
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    for name, B, L, lens in PREFILL_SHAPES:
+        if only and name != only:
+            continue
+        b = wl.build_batch(name, B=B, H_q=32, H_kv=8, D=128, page_size=16, L=L,
+                           context_lens=lens, seed=5, L_new=0, placement="permutation")
+        q, kp, vp = to_dev(b.query), to_dev(b.key_pages), to_dev(b.value_pages)
+        bt, cl = to_dev(b.block_table), to_dev(b.context_lens)
+        out = torch.empty_like(q)
+        t_pairs = timeit(lambda: pa.pa_prefill(q, kp, vp, bt, cl, b.page_size, scale=b.scale,
+                                               causal=True, out=out))
+        t_split = timeit(lambda: pa.pa_prefill_split(q, kp, vp, bt, cl, b.page_size,
+                                                     scale=b.scale, causal=True, out=out))
+        fl = prefill_flops(b)
+        items = B * ((L + 127) // 128) * 16
+        rows.append({"shape": name, "items": items, "items_per_sm": round(items / sms, 2),
+                     "gflop": round(fl / 1e9, 2),
+                     "pairs_us": round(t_pairs, 2), "split_us": round(t_split, 2),
+                     "pairs_tflops": round(fl / t_pairs / 1e6, 1),
+                     "split_tflops": round(fl / t_split / 1e6, 1),
+                     "attention_picks": "split" if 2 * items < 3 * sms else "pairs"})
+    st, flags = pa.pa_get_device_error()
+    if st:
+        raise RuntimeError(f"device error in the prefill shapes: {flags:#x}")
+    return rows
 
 
 def bench_prefill(pa, binding, torch, device, stream, steps=20):

@@ -12,7 +12,10 @@ Definitions followed (page titles and sections, see the C file's header):
   * append: Reading vLLM's PagedAttention Kernel, 3.2 "Writing into the cache";
   * attention: Reading vLLM's PagedAttention Kernel, section 4 (dense
     reference), over the gathered valid page prefixes of Tutorial 13,
-    section 5 "Reading Pages for Attention".
+    section 5 "Reading Pages for Attention";
+  * FP8 pages: Reading vLLM's PagedAttention Kernel, section 3.2 (the write
+    path's cache dtype and per-tensor k_scale / v_scale), with e4m3 codes
+    from the format's own definition.
 
 Every function here is pinned by ``tests/test_oracle_pins.py``.
 """
@@ -70,6 +73,13 @@ def _load():
             [p] * 5 + [i32] * 8 + [ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                    p, ctypes.c_int64, p, ctypes.c_int])
         lib.pa_oracle_attention_rows.restype = ctypes.c_int
+        lib.pa_oracle_e4m3_encode.argtypes = [p, p, ctypes.c_int64]
+        lib.pa_oracle_e4m3_encode.restype = None
+        lib.pa_oracle_e4m3_decode.argtypes = [p, p, ctypes.c_int64]
+        lib.pa_oracle_e4m3_decode.restype = None
+        lib.pa_oracle_append_kv_fp8.argtypes = ([p, p, p, p, p] + [i32] * 6 +
+                                                [ctypes.c_float, ctypes.c_float])
+        lib.pa_oracle_append_kv_fp8.restype = ctypes.c_int64
         _lib = lib
         return lib
 
@@ -188,3 +198,70 @@ def attention(query, key_pages, value_pages, block_table, context_lens,
     if rows is None:
         return out.reshape(B, H_q, L, D)
     return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) pages with per-tensor scales (Reading vLLM's PagedAttention
+# Kernel, section 3.2: the write path takes the cache dtype, k_scale and
+# v_scale). See the C file for the encoding and the reading of the pages.
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """fp32 values -> e4m3 codes (nearest, ties to even, saturated to +-448)."""
+    lib = _load()
+    xs = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(xs.shape, dtype=np.uint8)
+    lib.pa_oracle_e4m3_encode(_ptr(xs), _ptr(out), xs.size)
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """e4m3 codes -> their exact values (fp64; NaN for S.1111.111)."""
+    lib = _load()
+    cs = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(cs.shape, dtype=np.float64)
+    lib.pa_oracle_e4m3_decode(_ptr(cs), _ptr(out), cs.size)
+    return out
+
+
+def append_kv_fp8(key, value, key_pages, value_pages, slot_mapping, page_size: int,
+                  k_scale: float, v_scale: float) -> int:
+    """Scatter key/value [B, H_kv, L_new, D] (uint16 bf16 bits) into uint8
+    e4m3 pages [P, H_kv, page_size, D] in place: each element stored as the
+    code of fp32(x) / fp32(scale). Returns the count of slots past the pool."""
+    lib = _load()
+    for a in (key, value):
+        if a.dtype != np.uint16 or not a.flags.c_contiguous:
+            raise TypeError("key/value must be contiguous uint16 (bf16 bit) arrays")
+    for a in (key_pages, value_pages):
+        if a.dtype != np.uint8 or not a.flags.c_contiguous:
+            raise TypeError("FP8 pages must be contiguous uint8 arrays")
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int32)
+    B, H_kv, L_new, D = key.shape
+    P = key_pages.shape[0]
+    assert value.shape == key.shape and value_pages.shape == key_pages.shape
+    assert key_pages.shape[1:] == (H_kv, page_size, D)
+    assert slots.shape == (B, L_new)
+    return int(lib.pa_oracle_append_kv_fp8(_ptr(key), _ptr(value), _ptr(key_pages),
+                                           _ptr(value_pages), _ptr(slots), B, L_new, H_kv,
+                                           D, page_size, P, float(np.float32(k_scale)),
+                                           float(np.float32(v_scale))))
+
+
+def attention_fp8(query, key_pages, value_pages, k_scale: float, v_scale: float,
+                  block_table, context_lens, page_size: int, scale: float | None = None,
+                  causal: bool = True, rows=None, n_threads: int = 1) -> np.ndarray:
+    """Paged attention in fp64 over e4m3 pages: every K (V) element is the
+    exact value of its code times k_scale (v_scale); query uint16 bf16 bits.
+    Otherwise as attention()."""
+    q = bf16_bits_to_f64(query)
+    kp = e4m3_decode(key_pages) * float(np.float32(k_scale))
+    vp = e4m3_decode(value_pages) * float(np.float32(v_scale))
+    return attention(q, kp, vp, block_table, context_lens, page_size, scale=scale,
+                     causal=causal, rows=rows, n_threads=n_threads)
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """uint16 bf16 bit patterns -> their exact values in fp64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)

@@ -28,6 +28,12 @@
  *    scale * q . k_j, the output is the softmax-weighted sum of v_j, taken in
  *    the two-pass form: maximum, then normalised exponentials.
  *
+ *  - FP8 pages (Reading vLLM's PagedAttention Kernel, section 3.2, the
+ *    write path's cache dtype and per-tensor scales): e4m3 encoding and
+ *    decoding from the format's definition, and the quantising append
+ *    (see the block above pa_oracle_e4m3_value). Attention over FP8 pages
+ *    is attention over their exact decoded values times the scales.
+ *
  * Element storage: query and pages are either bf16 bit patterns (uint16) or
  * fp64. bf16 -> fp64 is exact, so all arithmetic below is fp64 on the exact
  * input values.
@@ -150,6 +156,108 @@ int64_t pa_oracle_append_kv(const uint16_t *key, const uint16_t *value,
                 int64_t dst = ((page * H_kv + h) * page_size + offset) * D;
                 memcpy(key_pages + dst, key + src, (size_t)D * sizeof(uint16_t));
                 memcpy(value_pages + dst, value + src, (size_t)D * sizeof(uint16_t));
+            }
+        }
+    }
+    return bad;
+}
+
+/*
+ * FP8 pages (Reading vLLM's PagedAttention Kernel, section 3.2: the write
+ * path takes the cache dtype and per-tensor k_scale / v_scale). The pages
+ * fix no rounding; the reading taken: a page stores e4m3 codes c whose value
+ * times the scale stands for the input x, c being the e4m3 value nearest to
+ * x / scale (x and the quotient in fp32), ties to the code with an even
+ * mantissa, magnitudes past the largest finite value saturated to it.
+ *
+ * e4m3 (the 8-bit floating-point format "E4M3"): a sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits; exponent 0 holds the subnormals m * 2^-9; no
+ * infinities; S.1111.111 is NaN, so the largest finite magnitude is
+ * 1.75 * 2^8 = 448.
+ */
+double pa_oracle_e4m3_value(uint8_t c)
+{
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    const double v = e == 0 ? m * ldexp(1.0, -9) : (8 + m) * ldexp(1.0, e - 10);
+    return s ? -v : v;
+}
+
+/* Nearest e4m3 code to x: a plain search over the 127 finite magnitudes. */
+static uint8_t e4m3_encode_one(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int best = 0;
+    double best_d = a;                      /* code 0 has the value 0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double d = fabs(pa_oracle_e4m3_value((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
+void pa_oracle_e4m3_encode(const float *x, uint8_t *out, int64_t n)
+{
+    for (int64_t k = 0; k < n; ++k)
+        out[k] = e4m3_encode_one(x[k]);
+}
+
+void pa_oracle_e4m3_decode(const uint8_t *codes, double *out, int64_t n)
+{
+    for (int64_t k = 0; k < n; ++k)
+        out[k] = pa_oracle_e4m3_value(codes[k]);
+}
+
+static float bf16_bits_to_float(uint16_t bits)
+{
+    const uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/*
+ * FP8 write path: as pa_oracle_append_kv, but every element is stored as the
+ * e4m3 code of (its fp32 value / scale), the quotient rounded to fp32 first.
+ * Pages: [num_pages, H_kv, page_size, D] bytes. Returns the count of slots
+ * beyond the pool (skipped).
+ */
+int64_t pa_oracle_append_kv_fp8(const uint16_t *key, const uint16_t *value,
+                                uint8_t *key_pages, uint8_t *value_pages,
+                                const int32_t *slot_mapping,
+                                int32_t B, int32_t L_new, int32_t H_kv, int32_t D,
+                                int32_t page_size, int32_t num_pages,
+                                float k_scale, float v_scale)
+{
+    int64_t bad = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        for (int32_t i = 0; i < L_new; ++i) {
+            const int64_t s = slot_mapping[(int64_t)b * L_new + i];
+            if (s < 0)
+                continue;
+            const int64_t page = s / page_size, offset = s % page_size;
+            if (page >= num_pages) {
+                ++bad;
+                continue;
+            }
+            for (int32_t h = 0; h < H_kv; ++h) {
+                const int64_t src = (((int64_t)b * H_kv + h) * L_new + i) * D;
+                const int64_t dst = ((page * H_kv + h) * page_size + offset) * D;
+                for (int32_t d = 0; d < D; ++d) {
+                    const float qk = bf16_bits_to_float(key[src + d]) / k_scale;
+                    const float qv = bf16_bits_to_float(value[src + d]) / v_scale;
+                    key_pages[dst + d] = e4m3_encode_one(qk);
+                    value_pages[dst + d] = e4m3_encode_one(qv);
+                }
             }
         }
     }

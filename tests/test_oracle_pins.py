@@ -452,3 +452,101 @@ def test_gather_rejects_bad_page_and_long_context():
         oracle.gather(b.key_pages, bt, b.context_lens, b.page_size, 16)
     with pytest.raises(oracle.OracleError):
         oracle.gather(b.key_pages, b.block_table, b.context_lens, b.page_size, 8)  # 10 > 8
+
+
+# ----------------------------------------------------------------------------
+# FP8 (e4m3) pages with per-tensor scales (Reading vLLM's PagedAttention
+# Kernel, 3.2: the write path takes kv_cache_dtype, k_scale and v_scale).
+
+
+def test_e4m3_values_of_the_format():
+    """Codes whose values the format fixes: bias 7, 3 mantissa bits,
+    subnormals m * 2^-9, S.1111.111 = NaN, largest finite 448."""
+    table = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+             0x30: 0.5, 0x38: 1.0, 0x39: 1.125, 0x40: 2.0, 0x77: 240.0, 0x7E: 448.0,
+             0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0}
+    codes = np.array(list(table), dtype=np.uint8)
+    got = oracle.e4m3_decode(codes)
+    assert np.array_equal(got, np.array(list(table.values())))
+    assert np.signbit(got[list(table).index(0x80)])
+    assert np.isnan(oracle.e4m3_decode(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+
+
+def test_e4m3_encode_matches_torch_rounding():
+    """Nearest value, ties to even: the same codes as torch's float8_e4m3fn
+    conversion wherever that conversion stays finite (|x| < 464)."""
+    rng = np.random.default_rng(17)
+    finite = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = (finite[1:] + finite[:-1]) / 2                   # every tie point
+    x = np.concatenate([
+        rng.normal(0, 1, 4000), rng.normal(0, 60, 4000), rng.uniform(-460, 460, 4000),
+        rng.uniform(-0.02, 0.02, 4000), mids, -mids, finite, -finite,
+        np.nextafter(mids, 0), np.nextafter(mids, 1000)]).astype(np.float32)
+    x = x[np.abs(x) < 464]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), ref)
+
+
+def test_e4m3_encode_saturates_round_trips_and_is_monotone():
+    x = np.float32([448.0, 464.0, 500.0, 1e9, np.inf, -464.0, -1e9, -np.inf])
+    assert oracle.e4m3_encode(x).tolist() == [0x7E] * 5 + [0xFE] * 3
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(vals), codes)         # every finite code
+    sweep = np.linspace(-470, 470, 200001, dtype=np.float32)
+    dec = oracle.e4m3_decode(oracle.e4m3_encode(sweep))
+    assert np.all(np.diff(dec) >= 0)
+    # within half a step of the format at every magnitude below 448
+    inside = np.abs(sweep) <= 448
+    a = np.abs(sweep[inside]).astype(np.float64)
+    step = np.where(a < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -6))) - 3))
+    assert np.all(np.abs(dec[inside] - sweep[inside]) <= step / 2 + 1e-12)
+
+
+def test_append_fp8_stores_codes_of_x_over_scale():
+    """Values that are scale times an e4m3 value come back exactly; slots
+    are the same as the bf16 append's."""
+    rng = np.random.default_rng(23)
+    B, H_kv, L_new, D, ps, P = 2, 2, 5, 16, 4, 8
+    k_scale, v_scale = 0.0625, 0.5            # powers of two: x / scale exact in fp32
+    kc = rng.integers(0, 0x7F, size=(B, H_kv, L_new, D)).astype(np.uint8)
+    vc = (rng.integers(0, 0x7F, size=(B, H_kv, L_new, D)) | 0x80 * rng.integers(0, 2, size=(B, H_kv, L_new, D))).astype(np.uint8)
+    vc[vc == 0xFF] = 0xFE
+    kx = (oracle.e4m3_decode(kc) * k_scale).astype(np.float32)
+    vx = (oracle.e4m3_decode(vc) * v_scale).astype(np.float32)
+    to_bits = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(to_bits(kx).astype(np.uint32) << 16, kx.view(np.uint32))   # bf16 exact
+    slots = rng.permutation(P * ps)[:B * L_new].reshape(B, L_new).astype(np.int32)
+    slots[1, 3] = -1
+    kp = np.zeros((P, H_kv, ps, D), np.uint8)
+    vp = np.zeros_like(kp)
+    assert oracle.append_kv_fp8(to_bits(kx), to_bits(vx), kp, vp, slots, ps, k_scale, v_scale) == 0
+    for b in range(B):
+        for i in range(L_new):
+            s = slots[b, i]
+            if s < 0:
+                continue
+            assert np.array_equal(kp[s // ps, :, s % ps], kc[b, :, i])
+            assert np.array_equal(vp[s // ps, :, s % ps], vc[b, :, i])
+    assert kp.sum() == sum(int(kc[b, :, i].astype(np.int64).sum()) for b in range(B)
+                           for i in range(L_new) if slots[b, i] >= 0)
+
+
+def test_attention_fp8_equals_bf16_attention_on_shared_values():
+    """With unit scales and K/V values that are both bf16 and e4m3 values,
+    attention over the FP8 pages equals attention over the bf16 pages."""
+    rng = np.random.default_rng(29)
+    b = wl.build_batch("fp8pin", B=2, H_q=4, H_kv=2, D=16, page_size=4, L=3,
+                       context_lens=[9, 6], seed=31, L_new=0)
+    codes_k = rng.integers(0, 0x7F, size=b.key_pages.shape).astype(np.uint8) | \
+        (0x80 * rng.integers(0, 2, size=b.key_pages.shape)).astype(np.uint8)
+    codes_v = rng.integers(0, 0x7F, size=b.value_pages.shape).astype(np.uint8)
+    codes_k[codes_k == 0xFF] = 0x7E
+    fk = oracle.e4m3_decode(codes_k).astype(np.float32)
+    fv = oracle.e4m3_decode(codes_v).astype(np.float32)
+    bits = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)   # e4m3 values are bf16 values
+    ref = oracle.attention(b.query, bits(fk), bits(fv), b.block_table, b.context_lens,
+                           b.page_size, scale=b.scale)
+    got = oracle.attention_fp8(b.query, codes_k, codes_v, 1.0, 1.0, b.block_table,
+                               b.context_lens, b.page_size, scale=b.scale)
+    assert np.array_equal(got, ref)

@@ -209,6 +209,42 @@ pa_status pa_prefill(const void *query, const void *key_pages,
                      int causal, void *out, pa_shape shape, void *stream);
 
 /*
+ * FP8 page pools (Reading vLLM's PagedAttention Kernel, section 3.2: the
+ * write path takes the cache dtype and per-tensor k_scale / v_scale). A pool
+ * holds e4m3 codes (1 byte per element: sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, largest finite 448), [num_pages, num_kv_heads, page_size,
+ * head_dim] like the bf16 pools; a code c stands for value(c) * scale.
+ * head_dim 128 only.
+ */
+
+/*
+ * pa_append_kv for e4m3 pools: every element of the new rows (bf16) is
+ * stored as the e4m3 code nearest to fp32(x) / scale (the quotient rounded to
+ * fp32 first; ties to the even code; magnitudes past 448 saturate to 448; a
+ * NaN gives a NaN code). k_scale and v_scale must be finite and > 0. Same
+ * slots, checks and error reporting as pa_append_kv.
+ */
+pa_status pa_append_kv_fp8(const void *key, const void *value, void *key_pages,
+                           void *value_pages, const int32_t *slot_mapping, int32_t page_size,
+                           float k_scale, float v_scale, pa_shape shape, void *stream);
+
+/*
+ * pa_decode over e4m3 pools: the same split-KV schedule, arguments,
+ * workspace (pa_decode_workspace_bytes) and result as pa_decode, with every
+ * K element value(code) * k_scale and every V element value(code) * v_scale.
+ * The kernel reads the codes straight from the pages (half the bytes of the
+ * bf16 pools) and multiplies on the tensor cores in f16, into which e4m3
+ * values convert exactly; the query is taken in f16 too, so its elements
+ * must have magnitudes within f16's range (below 65504; below 2^-14 they keep
+ * fewer bits). Any query length (no prefill kernel for e4m3 pools).
+ */
+pa_status pa_decode_fp8(const void *query, const void *key_pages, const void *value_pages,
+                        const int32_t *block_table, const int32_t *context_lens, int32_t page_size,
+                        float scale, float k_scale, float v_scale, int causal, void *out,
+                        pa_shape shape, int32_t max_context_len, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace pa_prefill_split needs for `shape` and
  * page_size on the CURRENT device, or 0 when the shape takes a prefill
  * kernel that needs none (head_dim 64, page_size < 8, an odd group size

@@ -64,6 +64,11 @@ def _load() -> ctypes.CDLL:
     lib.pa_decode.restype = ctypes.c_int
     lib.pa_prefill.argtypes = attn + [vp]
     lib.pa_prefill.restype = ctypes.c_int
+    lib.pa_append_kv_fp8.argtypes = [vp, vp, vp, vp, vp, i32, f32, f32, pa_shape, vp]
+    lib.pa_append_kv_fp8.restype = ctypes.c_int
+    lib.pa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, i32, f32, f32, f32, ctypes.c_int, vp,
+                                  pa_shape, i32, vp, sz, vp]
+    lib.pa_decode_fp8.restype = ctypes.c_int
     lib.pa_prefill_workspace_bytes.argtypes = [pa_shape, i32]
     lib.pa_prefill_workspace_bytes.restype = sz
     lib.pa_prefill_split.argtypes = attn + [vp, sz, vp]
@@ -225,6 +230,60 @@ def pa_append_kv(key: torch.Tensor, value: torch.Tensor, key_pages: torch.Tensor
                            _dev_ptr(slot_mapping, torch.int32, "slot_mapping"),
                            int(page_size), shape, _stream(stream))
     _check(st, "pa_append_kv")
+
+
+def pa_append_kv_fp8(key: torch.Tensor, value: torch.Tensor, key_pages: torch.Tensor,
+                     value_pages: torch.Tensor, slot_mapping: torch.Tensor, page_size: int,
+                     k_scale: float, v_scale: float, stream=None) -> None:
+    """key/value [B, H_kv, L_new, D] bf16 -> uint8 e4m3 pages [P, H_kv,
+    page_size, D] at slot_mapping [B, L_new], code = e4m3(x / scale)."""
+    B, H_kv, L_new, D = key.shape
+    if tuple(value.shape) != tuple(key.shape):
+        raise ValueError("key and value shapes differ")
+    if tuple(slot_mapping.shape) != (B, L_new):
+        raise ValueError("slot_mapping must be [B, L_new]")
+    if key_pages.shape[1:] != (H_kv, page_size, D) or value_pages.shape != key_pages.shape:
+        raise ValueError("page pool shape does not match key / page_size")
+    shape = pa_shape(B, 0, H_kv, D, L_new, key_pages.shape[0], 0)
+    st = _lib.pa_append_kv_fp8(_dev_ptr(key, torch.bfloat16, "key"),
+                               _dev_ptr(value, torch.bfloat16, "value"),
+                               _dev_ptr(key_pages, torch.uint8, "key_pages"),
+                               _dev_ptr(value_pages, torch.uint8, "value_pages"),
+                               _dev_ptr(slot_mapping, torch.int32, "slot_mapping"),
+                               int(page_size), float(k_scale), float(v_scale), shape,
+                               _stream(stream))
+    _check(st, "pa_append_kv_fp8")
+
+
+def pa_decode_fp8(query, key_pages, value_pages, block_table, context_lens, page_size: int,
+                  k_scale: float, v_scale: float, scale: Optional[float] = None,
+                  causal: bool = True, out=None, max_context_len: int = 0,
+                  workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Split-KV paged attention over uint8 e4m3 pools (K = code * k_scale,
+    V = code * v_scale); query and out [B, H_q, L, D] bf16."""
+    B, H_q, L, D = query.shape
+    if key_pages.shape[2] != page_size or value_pages.shape != key_pages.shape:
+        raise ValueError("page pool shape does not match page_size")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_table must be [B, max_pages] and context_lens [B]")
+    if out is None:
+        out = torch.empty_like(query)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    shape = make_shape(query.shape, key_pages.shape, block_table.shape[1])
+    if workspace is None:
+        workspace, _ = decode_workspace(shape, query.device)
+    st = _lib.pa_decode_fp8(_dev_ptr(query, torch.bfloat16, "query"),
+                            _dev_ptr(key_pages, torch.uint8, "key_pages"),
+                            _dev_ptr(value_pages, torch.uint8, "value_pages"),
+                            _dev_ptr(block_table, torch.int32, "block_table"),
+                            _dev_ptr(context_lens, torch.int32, "context_lens"),
+                            int(page_size), float(scale), float(k_scale), float(v_scale),
+                            int(bool(causal)), _dev_ptr(out, torch.bfloat16, "out"), shape,
+                            int(max_context_len), workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "pa_decode_fp8")
+    return out
 
 
 def _attn_common(query, key_pages, value_pages, block_table, context_lens, page_size,

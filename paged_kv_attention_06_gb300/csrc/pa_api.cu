@@ -118,6 +118,7 @@ struct MapCacheEntry {
     const void* pool;
     uint64_t rows;
     int32_t D, ps;
+    bool fp8;
     bool valid;
 };
 constexpr int kMapCache = 8;
@@ -125,20 +126,23 @@ thread_local MapCacheEntry t_map_cache[kMapCache];
 thread_local int t_map_next = 0;
 
 pa_status encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pa_shape& s,
-                                   int32_t ps);
+                                   int32_t ps, bool fp8);
 
-// 2-D view of a page pool: rows = P * H_kv * page_size, columns = D.
-pa_status encode_pool_map(CUtensorMap* map, const void* pool, const pa_shape& s, int32_t ps)
+// 2-D view of a page pool: rows = P * H_kv * page_size, columns = D (bf16
+// elements, or e4m3 codes of one byte when fp8).
+pa_status encode_pool_map(CUtensorMap* map, const void* pool, const pa_shape& s, int32_t ps,
+                          bool fp8 = false)
 {
     const uint64_t rows = uint64_t(s.num_pages) * s.num_kv_heads * ps;
     for (int i = 0; i < kMapCache; ++i) {
         const MapCacheEntry& e = t_map_cache[i];
-        if (e.valid && e.pool == pool && e.rows == rows && e.D == s.head_dim && e.ps == ps) {
+        if (e.valid && e.pool == pool && e.rows == rows && e.D == s.head_dim && e.ps == ps &&
+            e.fp8 == fp8) {
             *map = e.map;
             return PA_OK;
         }
     }
-    pa_status st = encode_pool_map_uncached(map, pool, s, ps);
+    pa_status st = encode_pool_map_uncached(map, pool, s, ps, fp8);
     if (st == PA_OK) {
         MapCacheEntry& e = t_map_cache[t_map_next];
         t_map_next = (t_map_next + 1) % kMapCache;
@@ -147,13 +151,14 @@ pa_status encode_pool_map(CUtensorMap* map, const void* pool, const pa_shape& s,
         e.rows = rows;
         e.D = s.head_dim;
         e.ps = ps;
+        e.fp8 = fp8;
         e.valid = true;
     }
     return st;
 }
 
 pa_status encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pa_shape& s,
-                                   int32_t ps)
+                                   int32_t ps, bool fp8)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     pa_status st = get_encoder(&enc);
@@ -161,18 +166,20 @@ pa_status encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pa_
         return st;
     const cuuint64_t dims[2] = {cuuint64_t(s.head_dim),
                                 cuuint64_t(s.num_pages) * s.num_kv_heads * ps};
-    const cuuint64_t strides[1] = {cuuint64_t(s.head_dim) * 2};
+    const cuuint64_t strides[1] = {cuuint64_t(s.head_dim) * (fp8 ? 1 : 2)};
     const int box_rows = ps < kDecodeTokens ? ps : kDecodeTokens;
-    const cuuint32_t box[2] = {64u, cuuint32_t(box_rows)};
+    // a box row is 128 bytes: 64 bf16 or 128 e4m3 codes
+    const cuuint32_t box[2] = {fp8 ? 128u : 64u, cuuint32_t(box_rows)};
     const cuuint32_t estr[2] = {1u, 1u};
     // Boxes of 8+ rows land on 1024-byte boundaries and use the 128-byte
     // swizzle; smaller pages use a linear layout (their destinations are only
     // 128-byte aligned).
     const CUtensorMapSwizzle swz =
         box_rows >= 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void*>(pool), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -314,7 +321,7 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
                        int32_t page_size, float scale, int causal, void* out,
                        const pa_shape& s, int32_t max_context_len, void* workspace,
                        size_t workspace_bytes, int whole_segments, cudaStream_t stream,
-                       int dense = 0)
+                       int dense = 0, int fp8 = 0, float k_scale = 1.f, float v_scale = 1.f)
 {
     DeviceInfo* dev;
     pa_status st = device_info(&dev);
@@ -325,7 +332,7 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
     const int64_t nseg = decode_segments(s);
     if (R >= (int64_t(1) << 30) || nseg > kMaxSegments)
         return PA_ERR_UNSUPPORTED;
-    const size_t smem = decode_smem_bytes(s.head_dim, s.batch);
+    const size_t smem = decode_smem_bytes(s.head_dim, s.batch, fp8 != 0);
     if (smem > size_t(dev->max_smem_optin))
         return PA_ERR_UNSUPPORTED;  // batch too large for the per-block prefix table
 
@@ -351,9 +358,9 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
         a.partials = static_cast<float*>(workspace);
     }
     CUtensorMap kmap, vmap;
-    if ((st = encode_pool_map(&kmap, key_pages, s, page_size)) != PA_OK)
+    if ((st = encode_pool_map(&kmap, key_pages, s, page_size, fp8 != 0)) != PA_OK)
         return st;
-    if ((st = encode_pool_map(&vmap, value_pages, s, page_size)) != PA_OK)
+    if ((st = encode_pool_map(&vmap, value_pages, s, page_size, fp8 != 0)) != PA_OK)
         return st;
 
     a.q = static_cast<const uint16_t*>(query);
@@ -376,8 +383,10 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
     a.swz = a.box_rows >= 8 ? 7 : 0;
     a.whole_segments = whole_segments;
     a.dense = dense;
-    a.scale_log2 = scale * 1.4426950408889634f;
+    a.scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
     a.causal = causal ? 1 : 0;
+    a.fp8 = fp8 ? 1 : 0;
+    a.v_scale = fp8 ? v_scale : 1.f;
     a.debug_unset_wait = t_arm_unset_wait ? 1 : 0;
     t_arm_unset_wait = false;
     CUtensorMap qmap;
@@ -443,6 +452,7 @@ pa_status pa_append_kv(const void* key, const void* value, void* key_pages, void
     if (shape.q_len == 0)
         return PA_OK;
     AppendArgs a;
+    memset(&a, 0, sizeof a);
     a.key = static_cast<const uint16_t*>(key);
     a.value = static_cast<const uint16_t*>(value);
     a.key_pages = static_cast<uint16_t*>(key_pages);
@@ -471,6 +481,72 @@ size_t pa_decode_workspace_bytes(pa_shape shape)
         return 0;
     return decode_workspace_bytes(decode_segments(shape), decode_max_grid(dev->sm_count),
                                   shape.head_dim);
+}
+
+pa_status pa_append_kv_fp8(const void* key, const void* value, void* key_pages,
+                           void* value_pages, const int32_t* slot_mapping, int32_t page_size,
+                           float k_scale, float v_scale, pa_shape shape, void* stream)
+{
+    if (!key || !value || !key_pages || !value_pages || !slot_mapping)
+        return PA_ERR_INVALID_ARG;
+    if (shape.batch <= 0 || shape.num_kv_heads <= 0 || shape.q_len < 0 || shape.num_pages <= 0 ||
+        shape.head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!(k_scale > 0.f) || !isfinite(k_scale) || !(v_scale > 0.f) || !isfinite(v_scale))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_pages) || !aligned16(value_pages))
+        return PA_ERR_INVALID_ARG;
+    if (shape.head_dim != 128)
+        return PA_ERR_UNSUPPORTED;
+    if (!pow2_in(page_size, 1, 256))
+        return PA_ERR_UNSUPPORTED;
+    if (2 * int64_t(shape.batch) * shape.q_len * shape.num_kv_heads * (shape.head_dim / 8) >=
+        (int64_t(1) << 40))
+        return PA_ERR_UNSUPPORTED;
+    DeviceInfo* dev;
+    pa_status st = device_info(&dev);
+    if (st != PA_OK)
+        return st;
+    if (shape.q_len == 0)
+        return PA_OK;
+    AppendArgs a;
+    memset(&a, 0, sizeof a);
+    a.key = static_cast<const uint16_t*>(key);
+    a.value = static_cast<const uint16_t*>(value);
+    a.key_pages = static_cast<uint16_t*>(key_pages);     // byte pages; the kernel casts back
+    a.value_pages = static_cast<uint16_t*>(value_pages);
+    a.slot_mapping = slot_mapping;
+    a.err = dev->err;
+    a.B = shape.batch;
+    a.L_new = shape.q_len;
+    a.H_kv = shape.num_kv_heads;
+    a.D = shape.head_dim;
+    a.ps = page_size;
+    a.num_pages = shape.num_pages;
+    a.fp8 = 1;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    return launch_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                               : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_fp8(const void* query, const void* key_pages, const void* value_pages,
+                        const int32_t* block_table, const int32_t* context_lens, int32_t page_size,
+                        float scale, float k_scale, float v_scale, int causal, void* out,
+                        pa_shape shape, int32_t max_context_len, void* workspace,
+                        size_t workspace_bytes, void* stream)
+{
+    pa_status st = check_attention(query, key_pages, value_pages, block_table, context_lens,
+                                   page_size, scale, out, shape);
+    if (st != PA_OK)
+        return st;
+    if (!(k_scale > 0.f) || !isfinite(k_scale) || !(v_scale > 0.f) || !isfinite(v_scale))
+        return PA_ERR_INVALID_ARG;
+    if (shape.head_dim != 128)
+        return PA_ERR_UNSUPPORTED;
+    return run_split_kv(query, key_pages, value_pages, block_table, context_lens, page_size, scale,
+                        causal, out, shape, max_context_len, workspace, workspace_bytes, 0,
+                        static_cast<cudaStream_t>(stream), 0, 1, k_scale, v_scale);
 }
 
 pa_status pa_decode(const void* query, const void* key_pages, const void* value_pages,

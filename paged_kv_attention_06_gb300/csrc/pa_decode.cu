@@ -50,16 +50,19 @@
 namespace pa {
 namespace {
 
-constexpr int kStages = 3;
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumerThreads + 32;
 
-template <int D>
+// F8: K/V pages of e4m3 codes (one byte per element; 128-byte rows at
+// D = 128), five stages in the room of the bf16 kernel's three.
+template <int D, bool F8 = false>
 struct Layout {
-    static constexpr int kHalves = D / 64;                   // 128-byte column blocks
+    static constexpr int kStages = F8 ? 5 : 3;
+    static constexpr int kHalves = D / 64;                   // Q: 128-byte column blocks (bf16)
+    static constexpr int kKVHalves = F8 ? D / 128 : D / 64;  // K/V: 128-byte column blocks
     static constexpr int kHalfBytes = kDecodeTokens * 128;   // 64 rows x 128 B
-    static constexpr int kStageBytes = kHalves * kHalfBytes; // K (or V) of one granule
+    static constexpr int kStageBytes = kKVHalves * kHalfBytes; // K (or V) of one granule
     static constexpr int kK = 0;
     static constexpr int kV = kK + kStages * kStageBytes;
     // Q tile of the segment whose piece starts at a stage's granule:
@@ -152,13 +155,15 @@ __device__ __forceinline__ int64_t granule_at_unit(const int32_t* pre, int B, in
     return pre[lo] + hm * gb + (in > 0 ? in : 0);
 }
 
-template <int D>
+template <int D, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap key_map,
                   const __grid_constant__ CUtensorMap value_map,
                   const __grid_constant__ CUtensorMap q_map, const DecodeArgs a)
 {
-    using Lay = Layout<D>;
+    using Lay = Layout<D, F8>;
+    constexpr int kStages = Lay::kStages;
+    static_assert(!F8 || D == 128, "e4m3 pages: head_dim 128");
     constexpr int kKS = D / 16;  // k-steps of 16 over the head dimension
 
     extern __shared__ uint8_t smem_raw[];
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool first = x == x_begin || x == sp.seg_start;
             const bool ok = mbar_wait_warp(&empty[stage], phase ^ 1u, misc, a.err);
             if (ok && (nbox > 0 || first)) {
-                const uint32_t bytes = uint32_t(nbox) * box * 128u * Lay::kHalves * 2u +
+                const uint32_t bytes = uint32_t(nbox) * box * 128u * Lay::kKVHalves * 2u +
                                        (first ? uint32_t(Lay::kHalves * Lay::kQHalfBytes) : 0u);
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full[stage], bytes);
@@ -335,11 +340,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                         const int row = k == 0 ? row_a : row_b;
                         const int dst = j * box * 128;
 #pragma unroll
-                        for (int hf = 0; hf < Lay::kHalves; ++hf) {
-                            tma_load_2d(k_half(stage, hf) + dst, &key_map, hf * 64, row,
+                        for (int hf = 0; hf < Lay::kKVHalves; ++hf) {
+                            // a box row is 128 bytes: 64 bf16 or 128 e4m3 elements
+                            tma_load_2d(k_half(stage, hf) + dst, &key_map, hf * (F8 ? 128 : 64), row,
                                         &full[stage], policy);
-                            tma_load_2d(v_half(stage, hf) + dst, &value_map, hf * 64, row,
-                                        &full[stage], policy);
+                            tma_load_2d(v_half(stage, hf) + dst, &value_map, hf * (F8 ? 128 : 64),
+                                        row, &full[stage], policy);
                         }
                     }
                 }
@@ -414,13 +420,34 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool ok = mbar_wait_warp(&full[stage], phase, misc, a.err);
             if (need_q) {
                 const uint8_t* qs = smem + Lay::kQ + stage * Lay::kHalves * Lay::kQHalfBytes;
+                if constexpr (F8) {
+                    // f16 fragments with the head dimension permuted inside
+                    // each 16-wide k-step the way the e4m3 K fragments come
+                    // out of ldmatrix: thread (row0, quad) holds d = 16 kk +
+                    // 4 quad + {0, 1} in a0 / a1 and + {2, 3} in a2 / a3.
 #pragma unroll
-                for (int kk = 0; kk < kKS; ++kk) {
-                    const int r = lane & 15;
-                    const int ch = 2 * kk + (lane >> 4);   // 16-byte chunk along D
-                    ldsm_x4(smem_u32(qs + (ch >> 3) * Lay::kQHalfBytes + r * 128 +
-                                     (((ch & 7) ^ (r & 7)) << 4)),
-                            qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+                    for (int kk = 0; kk < kKS; ++kk) {
+                        const int d = 16 * kk + 4 * quad;
+                        const int hf = d >> 6, ch = (d & 63) >> 3;
+#pragma unroll
+                        for (int rr = 0; rr < 2; ++rr) {
+                            const int r = row0 + 8 * rr;
+                            const uint2 v = *reinterpret_cast<const uint2*>(
+                                qs + hf * Lay::kQHalfBytes + r * 128 + ((ch ^ (r & 7)) << 4) +
+                                (quad & 1) * 8);
+                            qa[kk][rr] = bf16x2_to_f16x2(v.x);
+                            qa[kk][2 + rr] = bf16x2_to_f16x2(v.y);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < kKS; ++kk) {
+                        const int r = lane & 15;
+                        const int ch = 2 * kk + (lane >> 4);   // 16-byte chunk along D
+                        ldsm_x4(smem_u32(qs + (ch >> 3) * Lay::kQHalfBytes + r * 128 +
+                                         (((ch & 7) ^ (r & 7)) << 4)),
+                                qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+                    }
                 }
                 need_q = false;
             }
@@ -429,11 +456,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (nvalid < kDecodeTokens) {
                     // Zero this warp's V columns of the rows past the context:
                     // P is 0 there, but 0 * NaN is not.
-                    constexpr int kChunks = kCols / 8;  // 16-byte chunks per row
+                    constexpr int kElemsPerChunk = F8 ? 16 : 8;
+                    constexpr int kChunks = kCols / kElemsPerChunk;  // 16-byte chunks per row
                     const int nz = (kDecodeTokens - nvalid) * kChunks;
                     for (int idx = lane; idx < nz; idx += 32) {
                         const int r = nvalid + idx / kChunks;
-                        const int ch = col0 / 8 + idx % kChunks;
+                        const int ch = col0 / kElemsPerChunk + idx % kChunks;
                         *reinterpret_cast<uint4*>(v_half(stage, ch >> 3) + r * 128 +
                                                   (((ch & 7) ^ (r & swz)) << 4)) =
                             make_uint4(0, 0, 0, 0);
@@ -446,7 +474,26 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int nt = 0; nt < kSN; ++nt)
                     sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-                {
+                if constexpr (F8) {
+                    // One ldmatrix.x4 of e4m3 rows: 4 n-tiles of 8 tokens x one
+                    // 16-byte k-step; thread (row0, quad) gets 4 codes of token
+                    // row0 at d = 16 kk + 4 quad .. + 3, the two halves of
+                    // each register the two B registers (exact f16).
+#pragma unroll
+                    for (int kk = 0; kk < kKS; ++kk) {
+#pragma unroll
+                        for (int tq = 0; tq < kSN / 4; ++tq) {
+                            const int tr = tq * 32 + lane;
+                            uint32_t r4[4];
+                            ldsm_x4(smem_u32(k_half(stage, 0) + tr * 128 + ((kk ^ (tr & swz)) << 4)),
+                                    r4[0], r4[1], r4[2], r4[3]);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                mma_f16_16816(sc[4 * tq + i], qa[kk], e4m3x2_to_f16x2(r4[i]),
+                                              e4m3x2_to_f16x2(r4[i] >> 16));
+                        }
+                    }
+                } else {
                     const int trl = (lane & 7) + ((lane >> 4) << 3);
                     const int chsel = (lane >> 3) & 1;
 #pragma unroll
@@ -522,12 +569,43 @@ __global__ void __launch_bounds__(kThreads, 2)
                         p[j] = fast_exp2(fmaf(sc[nt][j], a.scale_log2, -mu[j >> 1]));
                         l_run[j >> 1] += p[j];
                     }
-                    pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p[0], p[1]);
-                    pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p[2], p[3]);
+                    if constexpr (F8) {
+                        pa[nt >> 1][(nt & 1) * 2 + 0] = pack_f16x2(p[0], p[1]);
+                        pa[nt >> 1][(nt & 1) * 2 + 1] = pack_f16x2(p[2], p[3]);
+                    } else {
+                        pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p[0], p[1]);
+                        pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p[2], p[3]);
+                    }
                 }
                 // O[:, col0 .. col0 + kCols) += P V; ldmatrix.trans gives the
                 // k-major V fragments.
-                {
+                if constexpr (F8) {
+                    // ldmatrix.x4.trans of e4m3 rows: tokens 16 kt + 0..7 and
+                    // + 8..15 of the warp's two 16-byte column chunks. A
+                    // register holds codes (token t, d), (t, d + 1), (t + 1, d),
+                    // (t + 1, d + 1) with t = 16 kt + 2 quad (+ 8), d = 16 c +
+                    // 2 (lane / 4): bytes 0, 2 feed the P V of the even d,
+                    // bytes 1, 3 that of the odd d. o[2 jj] / o[2 jj + 1] hold
+                    // columns 16 c + 4 quad + {0, 2} / {1, 3}.
+                    const int trl = (lane & 7) + (((lane >> 3) & 1) << 3);
+                    const int chsel = lane >> 4;
+#pragma unroll
+                    for (int kt = 0; kt < kSN / 2; ++kt) {
+                        const int tr = kt * 16 + trl;
+                        const int ch = col0 / 16 + chsel;
+                        uint32_t r4[4];
+                        ldsm_x4_trans(smem_u32(v_half(stage, 0) + tr * 128 + ((ch ^ (tr & swz)) << 4)),
+                                      r4[0], r4[1], r4[2], r4[3]);
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const uint32_t lo = r4[2 * jj], hi = r4[2 * jj + 1];
+                            mma_f16_16816(o[2 * jj], pa[kt], e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0020u)),
+                                          e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0020u)));
+                            mma_f16_16816(o[2 * jj + 1], pa[kt], e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0031u)),
+                                          e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0031u)));
+                        }
+                    }
+                } else {
                     const int trl = (lane & 7) + (((lane >> 3) & 1) << 3);
                     const int chsel = lane >> 4;
 #pragma unroll
@@ -577,12 +655,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int64_t orow = out_row(sp, row0 + rr * 8);
                 if (orow < 0)
                     continue;
-                const float inv = l_run[rr] > 0.f ? 1.f / l_run[rr] : 0.f;
-                uint16_t* dst = a.out + orow * D + col0 + 2 * quad;
+                if constexpr (F8) {
+                    const float inv = l_run[rr] > 0.f ? a.v_scale / l_run[rr] : 0.f;
 #pragma unroll
-                for (int nt = 0; nt < kON; ++nt)
-                    *reinterpret_cast<uint32_t*>(dst + nt * 8) =
-                        pack_bf16x2(o[nt][2 * rr] * inv, o[nt][2 * rr + 1] * inv);
+                    for (int jj = 0; jj < 2; ++jj) {
+                        uint16_t* dst = a.out + orow * D + col0 + 16 * jj + 4 * quad;
+                        *reinterpret_cast<uint2*>(dst) =
+                            make_uint2(pack_bf16x2(o[2 * jj][2 * rr] * inv, o[2 * jj + 1][2 * rr] * inv),
+                                       pack_bf16x2(o[2 * jj][2 * rr + 1] * inv,
+                                                   o[2 * jj + 1][2 * rr + 1] * inv));
+                    }
+                } else {
+                    const float inv = l_run[rr] > 0.f ? 1.f / l_run[rr] : 0.f;
+                    uint16_t* dst = a.out + orow * D + col0 + 2 * quad;
+#pragma unroll
+                    for (int nt = 0; nt < kON; ++nt)
+                        *reinterpret_cast<uint32_t*>(dst + nt * 8) =
+                            pack_bf16x2(o[nt][2 * rr] * inv, o[nt][2 * rr + 1] * inv);
+                }
             }
         } else if (!aborted) {
             // A segment that straddles blocks: leave this block's partial
@@ -597,11 +687,22 @@ __global__ void __launch_bounds__(kThreads, 2)
                     slot[rw] = m_run[rr];
                     slot[kDecodeRows + rw] = l_run[rr];
                 }
-                float* dst = slot + 2 * kDecodeRows + rw * D + col0 + 2 * quad;
+                if constexpr (F8) {
+                    // the state carries v_scale, so the merge pass needs no change
+                    const float vs = a.v_scale;
 #pragma unroll
-                for (int nt = 0; nt < kON; ++nt)
-                    *reinterpret_cast<float2*>(dst + nt * 8) =
-                        make_float2(o[nt][2 * rr], o[nt][2 * rr + 1]);
+                    for (int jj = 0; jj < 2; ++jj)
+                        *reinterpret_cast<float4*>(slot + 2 * kDecodeRows + rw * D + col0 + 16 * jj +
+                                                   4 * quad) =
+                            make_float4(o[2 * jj][2 * rr] * vs, o[2 * jj + 1][2 * rr] * vs,
+                                        o[2 * jj][2 * rr + 1] * vs, o[2 * jj + 1][2 * rr + 1] * vs);
+                } else {
+                    float* dst = slot + 2 * kDecodeRows + rw * D + col0 + 2 * quad;
+#pragma unroll
+                    for (int nt = 0; nt < kON; ++nt)
+                        *reinterpret_cast<float2*>(dst + nt * 8) =
+                            make_float2(o[nt][2 * rr], o[nt][2 * rr + 1]);
+                }
             }
         }
 
@@ -726,9 +827,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
 
 }  // namespace
 
-size_t decode_smem_bytes(int D, int B)
+size_t decode_smem_bytes(int D, int B, bool fp8)
 {
-    return D == 64 ? Layout<64>::bytes(B) : Layout<128>::bytes(B);
+    return fp8 ? Layout<128, true>::bytes(B) : D == 64 ? Layout<64>::bytes(B) : Layout<128>::bytes(B);
 }
 
 int decode_max_grid(int sm_count) { return 2 * sm_count; }
@@ -746,13 +847,17 @@ cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_m
     // The dynamic shared-memory limit is raised once per (device, head_dim)
     // and only grows.
     constexpr int kMaxDev = 64;
-    static std::atomic<int> smem_set[kMaxDev][2];
-    const int smem = int(decode_smem_bytes(a.D, a.B));
-    const int di = a.D == 64 ? 0 : 1;
+    static std::atomic<int> smem_set[kMaxDev][3];
+    const bool fp8 = a.fp8 != 0;
+    if (fp8 && a.D != 128)
+        return cudaErrorInvalidValue;
+    const int smem = int(decode_smem_bytes(a.D, a.B, fp8));
+    const int di = fp8 ? 2 : a.D == 64 ? 0 : 1;
     if (device < 0 || device >= kMaxDev)
         return cudaErrorInvalidDevice;
     if (smem_set[device][di].load(std::memory_order_relaxed) < smem) {
-        const void* fn = a.D == 64 ? reinterpret_cast<const void*>(decode_kernel<64>)
+        const void* fn = fp8 ? reinterpret_cast<const void*>(decode_kernel<128, true>)
+                       : a.D == 64 ? reinterpret_cast<const void*>(decode_kernel<64>)
                                    : reinterpret_cast<const void*>(decode_kernel<128>);
         cudaError_t e =
             cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -773,9 +878,10 @@ cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_m
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = a.D == 64
-                        ? cudaLaunchKernelEx(&cfg, decode_kernel<64>, key_map, value_map, q_map, a)
-                        : cudaLaunchKernelEx(&cfg, decode_kernel<128>, key_map, value_map, q_map, a);
+    cudaError_t e =
+        fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<128, true>, key_map, value_map, q_map, a)
+        : a.D == 64 ? cudaLaunchKernelEx(&cfg, decode_kernel<64>, key_map, value_map, q_map, a)
+                    : cudaLaunchKernelEx(&cfg, decode_kernel<128>, key_map, value_map, q_map, a);
     if (e != cudaSuccess || a.whole_segments)
         return e;
     cudaLaunchConfig_t mcfg = cfg;

@@ -4,6 +4,8 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "pa_internal.h"
@@ -227,6 +229,46 @@ __device__ __forceinline__ float fast_exp2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// mma.sync m16n8k16, f16 x f16 -> fp32 (the FP8-page decode path: e4m3
+// values are exact in f16).
+__device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint32_t b0,
+                                              uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two e4m3 codes (the low 16 bits; the lower byte first) -> two f16, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(v & 0xffffu), __NV_E4M3);
+    return uint32_t(h.x) | (uint32_t(h.y) << 16);
+}
+
+// Two fp32 -> two e4m3 codes (round to nearest even, saturated to +-448),
+// the first in the lower byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
+{
+    return uint32_t(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+// bf16 pair -> f16 pair (rounded to nearest; exact for magnitudes in f16's
+// normal range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v)
+{
+    const __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)

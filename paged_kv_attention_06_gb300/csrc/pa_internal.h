@@ -33,6 +33,8 @@ struct AppendArgs {
     const int32_t* slot_mapping;  // [B, L_new]
     unsigned* err;
     int32_t B, L_new, H_kv, D, ps, num_pages;
+    int32_t fp8;                  // 1: the pages hold e4m3 codes (one byte each)
+    float k_scale, v_scale;       // e4m3 pages: code = e4m3(x / scale)
 };
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
@@ -80,13 +82,15 @@ struct DecodeArgs {
     int32_t whole_segments;  // 1: every block takes whole segments (no partials)
     int32_t dense;      // 1: K/V are dense [B, H_kv, ps, D] (request b is page b;
                         // block_table is not read)
-    float scale_log2;   // scale * log2(e)
+    float scale_log2;   // scale * log2(e) (times k_scale for e4m3 pages)
     int32_t causal;
+    int32_t fp8;        // 1: K/V pages hold e4m3 codes (head_dim 128)
+    float v_scale;      // e4m3 pages: the value scale (1 otherwise)
     int32_t debug_unset_wait;  // test support: block 0 first waits on a barrier
                                // that nothing arrives at (times out, flags)
 };
 
-size_t decode_smem_bytes(int D, int B);
+size_t decode_smem_bytes(int D, int B, bool fp8 = false);
 int decode_max_grid(int sm_count);
 size_t decode_workspace_bytes(int64_t nseg, int grid_max, int D);
 cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_map,

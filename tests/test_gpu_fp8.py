@@ -1,0 +1,146 @@
+"""FP8 (e4m3) page pools with per-tensor scales on the GPU, through the C
+ABI, against the fp64 oracle on the same inputs: the quantising append bit
+for bit, decode attention within the stated tolerance (max |err| <= 2e-2,
+mean |err| <= 2e-3) over the exact decoded page values."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_util import N_THREADS, assert_close, check_no_device_error, dev, host_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _pa():
+    import paged_kv_attention_06_gb300 as pa
+    return pa
+
+
+def _u8(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+@pytest.mark.parametrize("ps", [16, 1, 128])
+@pytest.mark.parametrize("scales", [(0.05, 0.031), (1.0, 0.25), (0.003, 0.7)])
+def test_append_fp8_bit_exact(ps, scales):
+    pa = _pa()
+    k_scale, v_scale = scales
+    rng = np.random.default_rng(ps * 7 + int(k_scale * 1000))
+    B, H_kv, L_new, D = 3, 4, 19, 128
+    P = (B * L_new) // ps + 8
+    key = wl.normal_bf16(rng, (B, H_kv, L_new, D), std=1.0)
+    value = wl.normal_bf16(rng, (B, H_kv, L_new, D), std=2.0)
+    # saturating, subnormal and zero elements
+    key[0, 0, 0, :8] = wl.bf16_bits(np.float32([600, -600, 1e-6, -1e-6, 0.0, -0.0, 20.0, 3e-3]))
+    slots = rng.permutation(P * ps)[:B * L_new].reshape(B, L_new).astype(np.int32)
+    slots[1, 4] = -1
+    slots[2, 7] = -1
+    kp0 = wl.random_e4m3_codes(rng, (P, H_kv, ps, D), allow_nan=True)
+    vp0 = wl.random_e4m3_codes(rng, (P, H_kv, ps, D), allow_nan=True)
+    kp_d, vp_d = _u8(kp0), _u8(vp0)
+    pa.pa_append_kv_fp8(dev(key), dev(value), kp_d, vp_d, dev(slots), ps, k_scale, v_scale)
+    check_no_device_error()
+    kp, vp = kp0.copy(), vp0.copy()
+    assert oracle.append_kv_fp8(key, value, kp, vp, slots, ps, k_scale, v_scale) == 0
+    assert np.array_equal(kp_d.cpu().numpy(), kp)
+    assert np.array_equal(vp_d.cpu().numpy(), vp)
+
+
+def _fp8_batch(name, B, H_q, H_kv, ps, L, lens, seed, causal=True, placement="permutation"):
+    b = wl.build_batch(name, B=B, H_q=H_q, H_kv=H_kv, D=128, page_size=ps, L=L,
+                       context_lens=lens, seed=seed, L_new=0, causal=causal,
+                       placement=placement)
+    rng = np.random.default_rng(seed + 1000)
+    kc = wl.random_e4m3_codes(rng, b.key_pages.shape)
+    vc = wl.random_e4m3_codes(rng, b.value_pages.shape)
+    # stale slots (past every context, in unreferenced pages) hold any byte
+    stale = wl.random_e4m3_codes(rng, b.key_pages.shape, allow_nan=True)
+    used = np.zeros(b.key_pages.shape[0], bool)
+    for r in range(B):
+        n = int(b.context_lens[r])
+        for j in range(-(-n // ps)):
+            used[b.block_table[r, j]] = True
+    kc[~used], vc[~used] = stale[~used], stale[~used][::-1]
+    for r in range(B):
+        n = int(b.context_lens[r])
+        if n % ps:
+            tail = b.block_table[r, n // ps]
+            kc[tail, :, n % ps:] = stale[tail, :, n % ps:]
+            vc[tail, :, n % ps:] = 0x7F                         # NaN codes
+    return b, kc, vc
+
+
+def _run(b, kc, vc, k_scale, v_scale, rows=None):
+    pa = _pa()
+    q = dev(b.query)
+    out = pa.pa_decode_fp8(q, _u8(kc), _u8(vc), dev(b.block_table), dev(b.context_lens),
+                           b.page_size, k_scale, v_scale, scale=b.scale, causal=b.causal,
+                           max_context_len=int(b.context_lens.max()))
+    check_no_device_error()
+    ref = oracle.attention_fp8(b.query, kc, vc, k_scale, v_scale, b.block_table,
+                               b.context_lens, b.page_size, scale=b.scale, causal=b.causal,
+                               rows=rows, n_threads=N_THREADS)
+    got = host_f64(out)
+    if rows is not None:
+        got = got[rows[:, 0], rows[:, 1], rows[:, 2]]
+    return got, ref
+
+
+@pytest.mark.parametrize("ps", [16, 128, 4, 1])
+@pytest.mark.parametrize("H_q,H_kv", [(28, 4), (8, 8), (32, 4)])
+def test_decode_fp8_matches_oracle(ps, H_q, H_kv):
+    lens = [1, 63, 64, 65, 127, 300, 1000, 2051]
+    b, kc, vc = _fp8_batch("fp8dec", 8, H_q, H_kv, ps, 1, lens, seed=ps + H_q)
+    got, ref = _run(b, kc, vc, 0.05, 0.04)
+    assert_close(got, ref, f"fp8 decode ps={ps} G={H_q // H_kv}")
+
+
+@pytest.mark.parametrize("L,causal", [(2, True), (5, True), (8, True), (4, False), (16, True)])
+def test_decode_fp8_multi_row(L, causal):
+    lens = [L, L + 5, 130, 777, 64 + L]
+    b, kc, vc = _fp8_batch("fp8rows", 5, 16, 4, 16, L, lens, seed=40 + L, causal=causal)
+    got, ref = _run(b, kc, vc, 0.02, 0.06)
+    assert_close(got, ref, f"fp8 decode L={L} causal={causal}")
+
+
+def test_decode_fp8_headline_shape_every_row():
+    """The 7B-class GQA decode batch (B = 32, H_q = 28, H_kv = 4, page_size 16,
+    contexts U[128, 4096], shuffled pool) with e4m3 pools."""
+    rng = np.random.default_rng(1002)
+    lens = [int(x) for x in rng.integers(128, 4097, size=32)]
+    b, kc, vc = _fp8_batch("fp8head", 32, 28, 4, 16, 1, lens, seed=1002)
+    got, ref = _run(b, kc, vc, 0.05, 0.05)
+    assert_close(got, ref, "fp8 headline shape")
+
+
+def test_decode_fp8_empty_contexts_give_zeros():
+    b, kc, vc = _fp8_batch("fp8empty", 3, 8, 2, 16, 3, [0, 2, 40], seed=51)
+    got, ref = _run(b, kc, vc, 0.1, 0.1)
+    assert np.all(got[0] == 0)
+    assert_close(got, ref, "fp8 empty contexts")
+
+
+def test_append_then_decode_fp8():
+    """Append the step's token with the quantising append, then decode over
+    the updated e4m3 pools: the oracle does the same with its own append."""
+    pa = _pa()
+    b = wl.make_workload("decode_b32_gqa7_ps16")
+    rng = np.random.default_rng(77)
+    kc = wl.random_e4m3_codes(rng, b.key_pages.shape)
+    vc = wl.random_e4m3_codes(rng, b.value_pages.shape)
+    ks, vs = 0.05, 0.05
+    kp_d, vp_d = _u8(kc), _u8(vc)
+    pa.pa_append_kv_fp8(dev(b.key_new), dev(b.value_new), kp_d, vp_d, dev(b.slot_mapping),
+                        b.page_size, ks, vs)
+    out = pa.pa_decode_fp8(dev(b.query), kp_d, vp_d, dev(b.block_table), dev(b.context_lens),
+                           b.page_size, ks, vs, scale=b.scale,
+                           max_context_len=int(b.context_lens.max()))
+    check_no_device_error()
+    kp, vp = kc.copy(), vc.copy()
+    oracle.append_kv_fp8(b.key_new, b.value_new, kp, vp, b.slot_mapping, b.page_size, ks, vs)
+    assert np.array_equal(kp_d.cpu().numpy(), kp) and np.array_equal(vp_d.cpu().numpy(), vp)
+    ref = oracle.attention_fp8(b.query, kp, vp, ks, vs, b.block_table, b.context_lens,
+                               b.page_size, scale=b.scale, n_threads=N_THREADS)
+    assert_close(host_f64(out), ref, "fp8 append + decode")

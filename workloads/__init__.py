@@ -54,6 +54,18 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
 _CHUNK = 1 << 22
 
 
+def random_e4m3_codes(rng: np.random.Generator, shape, max_magnitude_code: int = 0x5F,
+                      allow_nan: bool = False) -> np.ndarray:
+    """Seeded e4m3 byte codes: a uniform magnitude code in [0, max_magnitude_code]
+    (0x5F is 1.875 * 2^4 = 30) and a random sign; with allow_nan, any of the 256
+    byte values (stale FP8 slots). Bytes only, no arithmetic of the method."""
+    if allow_nan:
+        return rng.integers(0, 256, size=shape, dtype=np.uint8)
+    mag = rng.integers(0, max_magnitude_code + 1, size=shape, dtype=np.uint8)
+    sign = (rng.integers(0, 2, size=shape, dtype=np.uint8) << 7).astype(np.uint8)
+    return mag | sign
+
+
 def normal_bf16(rng: np.random.Generator, shape, std: float = 1.0) -> np.ndarray:
     """bf16 bit patterns of N(0, std^2) draws.
 

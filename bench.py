@@ -269,6 +269,12 @@ def _bench_lib(binding):
                                        f32, ctypes.c_int, vp, binding.pa_shape, i32, vp, sz, vp,
                                        ctypes.POINTER(ctypes.c_float)]
     lib.pa_bench_e2e_steps.restype = ctypes.c_int
+    lib.pa_bench_steps_fp8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, pvp,
+                                       pvp, vp, i32, binding.pa_shape, vp, vp, vp, f32, f32, f32,
+                                       ctypes.c_int, vp, binding.pa_shape, i32, vp, sz, vp,
+                                       ctypes.POINTER(ctypes.c_float),
+                                       ctypes.POINTER(ctypes.c_float)]
+    lib.pa_bench_steps_fp8.restype = ctypes.c_int
     return lib
 
 
@@ -291,6 +297,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=8.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--fp8-decode", action="store_true",
+                    help="time only the decode step over e4m3 page pools of --workload and exit")
     ap.add_argument("--prefill-shapes", action="store_true",
                     help="time both prefill kernels on chunked-prefill shapes and exit")
     ap.add_argument("--shape", default=None, help="with --prefill-shapes: only this shape")
@@ -317,6 +325,13 @@ def main(argv=None):
 
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
+    if args.fp8_decode:
+        import paged_kv_attention_06_gb300 as pa
+        from paged_kv_attention_06_gb300 import binding
+        stream = torch.cuda.current_stream()
+        print(json.dumps({"fp8_decode": bench_decode_fp8(args.workload, pa, binding, torch, device,
+                                                         stream, args.steps, args.warmup)}))
+        return 0
     if args.prefill_shapes:
         print(json.dumps({"prefill_shapes": prefill_shapes(torch, device, args.shape)}))
         return 0
@@ -458,6 +473,12 @@ def main(argv=None):
             if name != args.workload:
                 other_decode.append(bench_decode_config(name, pa, binding, torch, device,
                                                         stream, n))
+    # the same decode step over e4m3 page pools (half the K/V bytes)
+    fp8_decode = None
+    if not args.no_other_decode and world == 1 and b.D == 128:
+        fp8_decode = bench_decode_fp8(b.name, pa, binding, torch, device, stream, 2000)
+        fp8_decode["other"] = [bench_decode_fp8(name, pa, binding, torch, device, stream, n)
+                               for name, n in (("decode_b64_ps128", 400), ("decode_long_b8", 200))]
 
     # ---- secondary: chunked prefill TFLOP/s (prefill route) -----------------
     prefill = None
@@ -514,6 +535,8 @@ def main(argv=None):
     }
     if other_decode:
         line["other_decode"] = other_decode
+    if fp8_decode is not None:
+        line["fp8_decode"] = fp8_decode
     if prefill is not None:
         prefill["roofline_frac_bf16"] = round(prefill["tflops"] / bf16_peak, 4)
         prefill["peak_source"] = f"{peak_kind} bf16_tflops"
@@ -522,6 +545,76 @@ def main(argv=None):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def bench_decode_fp8(name, pa, binding, torch, device, stream, steps, warmup=10,
+                     k_scale=0.05, v_scale=0.05):
+    """The decode workload with e4m3 page pools (seeded random codes,
+    per-tensor scales): pa_append_kv_fp8 + pa_decode_fp8 per step through the
+    native loop, rotating pool copies; bytes counted at one byte per K/V
+    element."""
+    import ctypes
+    b = wl.make_workload(name)
+    rng = np.random.default_rng(b.seed + 7)
+
+    def to_dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    bf16_bytes, _ = step_bytes(b)
+    kv_bf16 = int(b.context_lens.astype(np.int64).sum()) * b.H_kv * b.D * 2 * 2
+    dec_bytes = bf16_bytes - kv_bf16 // 2
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    copies = max(4, math.ceil(4 * l2 / max(1, dec_bytes)))
+    kp0 = to_dev(wl.random_e4m3_codes(rng, b.key_pages.shape))
+    vp0 = to_dev(wl.random_e4m3_codes(rng, b.value_pages.shape))
+    pools = [(kp0, vp0)] + [(kp0.clone(), vp0.clone()) for _ in range(copies - 1)]
+    q, bt, cl = to_dev(b.query), to_dev(b.block_table), to_dev(b.context_lens)
+    kn, vn, sm = to_dev(b.key_new), to_dev(b.value_new), to_dev(b.slot_mapping)
+    out = torch.empty_like(q)
+    shape = pa.make_shape(q.shape, kp0.shape, bt.shape[1])
+    app_shape = pa.pa_shape(b.B, 0, b.H_kv, b.D, b.L_new, b.num_pages, 0)
+    ws, ws_need = pa.decode_workspace(shape, device)
+    blib = _bench_lib(binding)
+    kps = (ctypes.c_void_p * copies)(*[kp.data_ptr() for kp, _ in pools])
+    vps = (ctypes.c_void_p * copies)(*[vp_.data_ptr() for _, vp_ in pools])
+    sample_every = 4
+
+    def run(n):
+        step_ms = (ctypes.c_float * max(1, -(-n // sample_every)))()
+        total = ctypes.c_float(0)
+        st = blib.pa_bench_steps_fp8(n, sample_every, copies, kn.data_ptr(), vn.data_ptr(), kps,
+                                     vps, sm.data_ptr(), b.page_size, app_shape, q.data_ptr(),
+                                     bt.data_ptr(), cl.data_ptr(), b.scale, k_scale, v_scale,
+                                     int(b.causal), out.data_ptr(), shape,
+                                     int(b.context_lens.max()), ws.data_ptr(), ws_need,
+                                     stream.cuda_stream, step_ms, ctypes.byref(total))
+        if st != 0:
+            raise RuntimeError(f"native fp8 step loop failed with status {st} on {name}")
+        return float(total.value), [float(x) for x in step_ms[:-(-n // sample_every)]]
+
+    run(warmup)
+    torch.cuda.synchronize()
+    total_ms, dec_ms = run(steps)
+    torch.cuda.synchronize()
+    st, flags = pa.pa_get_device_error()
+    if st:
+        raise RuntimeError(f"device error in fp8 decode bench {name}: {flags:#x}")
+    hbm_peak, _, peak_kind = load_peaks()
+    dec_avg = float(np.mean(dec_ms))
+    ms_step = total_ms / steps
+    res = {"workload": name, "pages": "e4m3, per-tensor scales", "ms_per_step": round(ms_step, 6),
+           "tokens_per_s": round(b.B * b.L / (ms_step * 1e-3), 1),
+           "decode_call_us": round(1e3 * dec_avg, 3),
+           "decode_gbs": round(dec_bytes / (dec_avg * 1e-3) / 1e9, 2),
+           "frac": round(dec_bytes / (dec_avg * 1e-3) / 1e9 / hbm_peak, 4),
+           "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": dec_bytes,
+           "kernel": "decode_kernel<128, e4m3> + decode_merge_kernel<128>",
+           "steps": steps, "l2": f"{copies} rotating pool copies"}
+    del pools, ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def bench_decode_config(name, pa, binding, torch, device, stream, steps, warmup=10):

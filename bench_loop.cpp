@@ -92,6 +92,53 @@ int pa_bench_steps(int n_steps, int sample_every, int n_copies, const void* key_
     return cudaEventElapsedTime(total_ms, t0, t1) == cudaSuccess ? 0 : -1;
 }
 
+// pa_bench_steps for e4m3 page pools: pa_append_kv_fp8 + pa_decode_fp8 per
+// step, the same events.
+int pa_bench_steps_fp8(int n_steps, int sample_every, int n_copies, const void* key_new,
+                       const void* value_new, void* const* key_pages, void* const* value_pages,
+                       const int32_t* slot_mapping, int32_t page_size, pa_shape append_shape,
+                       const void* query, const int32_t* block_table, const int32_t* context_lens,
+                       float scale, float k_scale, float v_scale, int causal, void* out,
+                       pa_shape shape, int32_t max_context_len, void* workspace,
+                       size_t workspace_bytes, void* stream, float* step_ms, float* total_ms)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (sample_every < 1)
+        sample_every = 1;
+    const int n_samples = (n_steps + sample_every - 1) / sample_every;
+    EventPool pool(2 * size_t(n_samples) + 2);
+    if (!pool.ok())
+        return -1;
+    cudaEvent_t t0 = pool.ev[2 * n_samples], t1 = pool.ev[2 * n_samples + 1];
+    if (cudaEventRecord(t0, s) != cudaSuccess)
+        return -1;
+    for (int k = 0; k < n_steps; ++k) {
+        const int c = k % n_copies;
+        const bool sampled = k % sample_every == 0;
+        const int j = k / sample_every;
+        pa_status st = pa_append_kv_fp8(key_new, value_new, key_pages[c], value_pages[c],
+                                        slot_mapping, page_size, k_scale, v_scale, append_shape,
+                                        stream);
+        if (st != PA_OK)
+            return int(st);
+        if (sampled)
+            cudaEventRecord(pool.ev[2 * j], s);
+        st = pa_decode_fp8(query, key_pages[c], value_pages[c], block_table, context_lens,
+                           page_size, scale, k_scale, v_scale, causal, out, shape,
+                           max_context_len, workspace, workspace_bytes, stream);
+        if (st != PA_OK)
+            return int(st);
+        if (sampled)
+            cudaEventRecord(pool.ev[2 * j + 1], s);
+    }
+    if (cudaEventRecord(t1, s) != cudaSuccess || cudaEventSynchronize(t1) != cudaSuccess)
+        return -1;
+    for (int j = 0; j < n_samples; ++j)
+        if (cudaEventElapsedTime(&step_ms[j], pool.ev[2 * j], pool.ev[2 * j + 1]) != cudaSuccess)
+            return -1;
+    return cudaEventElapsedTime(total_ms, t0, t1) == cudaSuccess ? 0 : -1;
+}
+
 // End-to-end steps from pinned host buffers: every step copies the step's
 // inputs host -> device (query, new K/V, slot_mapping, block_table,
 // context_lens), runs the step, and copies the output back.

@@ -55,10 +55,11 @@ constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumerThreads + 32;
 
 // F8: K/V pages of e4m3 codes (one byte per element; 128-byte rows at
-// D = 128), five stages in the room of the bf16 kernel's three.
+// D = 128): half-size stages, four of them, and a tile for the merge of the
+// four consumer warps' states at the end of a piece.
 template <int D, bool F8 = false>
 struct Layout {
-    static constexpr int kStages = F8 ? 5 : 3;
+    static constexpr int kStages = F8 ? 4 : 3;
     static constexpr int kHalves = D / 64;                   // Q: 128-byte column blocks (bf16)
     static constexpr int kKVHalves = F8 ? D / 128 : D / 64;  // K/V: 128-byte column blocks
     static constexpr int kHalfBytes = kDecodeTokens * 128;   // 64 rows x 128 B
@@ -69,7 +70,11 @@ struct Layout {
     // [stage][half][16 rows][128 B], 128B swizzle (TMA box of 16 rows).
     static constexpr int kQHalfBytes = kDecodeRows * 128;
     static constexpr int kQ = kV + kStages * kStageBytes;
-    static constexpr int kBar = kQ + kStages * kHalves * kQHalfBytes;
+    // F8: each consumer warp's normalised O (f16) at the end of a piece,
+    // [warp][16 rows][D]
+    static constexpr int kWork = kQ + kStages * kHalves * kQHalfBytes;
+    static constexpr int kWorkBytes = F8 ? kConsumerWarps * kDecodeRows * D * 2 : 0;
+    static constexpr int kBar = kWork + kWorkBytes;
     static constexpr int kMisc = kBar + 2 * kStages * 8;     // abort flag, test barrier
     static constexpr int kPrefix = kMisc + 32;               // [B + 1] int32
     static size_t bytes(int B) { return kPrefix + size_t(B + 1) * 4 + 1024; }
@@ -386,6 +391,293 @@ __global__ void __launch_bounds__(kThreads, 2)
         return (int64_t(p.b) * a.H_q + p.h * a.G + g) * a.L + i;
     };
 
+    if constexpr (F8) {
+        // ---- e4m3 pages: warp w owns tokens [16 w, 16 w + 16) of every granule.
+        // It reads their codes straight from the stage (ldmatrix on the byte
+        // rows), converts them in registers to f16 (exact), computes their
+        // scores and P V over all D columns on the tensor cores (f16 in, fp32
+        // accumulate) and keeps its own online-softmax state; at the end of a
+        // piece the four states merge through the work tile (each warp's O / l_w
+        // in f16, relative error 2^-11), M = max m_w, l = sum l_w 2^(m_w - M),
+        // o = sum l_w 2^(m_w - M) (O_w / l_w). Every warp then
+        // holds its D/4 columns, as in the bf16 schedule, and the same
+        // epilogue follows.
+        //   * K: ldmatrix (no transpose) of 8 byte rows gives lane (row0,
+        //     quad) the codes of token row0 at d = 16 kk + 4 quad .. + 3; their
+        //     two halves are the two f16 B registers when the head dimension
+        //     is permuted inside each 16-wide k-step the same way in Q (a0 / a1
+        //     hold d = 16 kk + 4 quad + {0, 1}, a2 / a3 + {2, 3}).
+        //   * V: ldmatrix.trans of byte rows gives codes (t, d), (t, d + 1),
+        //     (t + 1, d), (t + 1, d + 1), t = 2 quad (+ 8), d = 16 c + 2 (lane
+        //     / 4); bytes 0, 2 feed the P V of the even d, bytes 1, 3 that of
+        //     the odd d: o[2 c] holds columns 16 c + 4 quad + {0, 2},
+        //     o[2 c + 1] columns 16 c + 4 quad + {1, 3}.
+        constexpr int kWT = kDecodeTokens / kConsumerWarps;   // tokens per warp
+        constexpr int kONF = D / 8;                           // output n-tiles per warp
+        __shared__ float wstate[kConsumerWarps][2][kDecodeRows];   // (m, l) per warp and row
+        uint16_t* wtile = reinterpret_cast<uint16_t*>(smem + Lay::kWork);  // [warp][16 rows][D] f16
+        const int r_lo = warp * kWT;
+        int64_t x = x_begin;
+        while (x < x_end) {
+            const SegmentPos sp = locate(pre, a.B, per_req, a.MT, x);
+            const int64_t piece_end = min(x_end, sp.seg_start + sp.seg_len);
+            const int n = clamp_context(a.context_lens[sp.b], cap, a.err);
+            uint32_t qa[kKS][4];
+            bool need_q = true;
+            int lim[2];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int rg = sp.mt * kDecodeRows + row0 + rr * 8;
+                const int i = rg < a.R ? rg % a.L : a.L - 1;
+                lim[rr] = a.causal ? min(n - a.L + i, n - 1) : n - 1;
+            }
+            const int lim_min = __reduce_min_sync(0xffffffffu, min(lim[0], lim[1]));
+            float m_run[2] = {-INFINITY, -INFINITY};
+            float l_run[2] = {0.f, 0.f};
+            float o[kONF][4];
+#pragma unroll
+            for (int nt = 0; nt < kONF; ++nt)
+                o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+            for (; x < piece_end; ++x) {
+                const int t0 = int(x - sp.seg_start) * kDecodeTokens;
+                const int nvalid = min(kDecodeTokens, n - t0);
+                const bool ok = mbar_wait_warp(&full[stage], phase, misc, a.err);
+                if (need_q) {
+                    const uint8_t* qs = smem + Lay::kQ + stage * Lay::kHalves * Lay::kQHalfBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kKS; ++kk) {
+                        const int d = 16 * kk + 4 * quad;
+                        const int hf = d >> 6, ch = (d & 63) >> 3;
+#pragma unroll
+                        for (int rr = 0; rr < 2; ++rr) {
+                            const int r = row0 + 8 * rr;
+                            const uint2 v = *reinterpret_cast<const uint2*>(
+                                qs + hf * Lay::kQHalfBytes + r * 128 + ((ch ^ (r & 7)) << 4) +
+                                (quad & 1) * 8);
+                            qa[kk][rr] = bf16x2_to_f16x2(v.x);
+                            qa[kk][2 + rr] = bf16x2_to_f16x2(v.y);
+                        }
+                    }
+                    need_q = false;
+                }
+                const bool live = ok && nvalid > r_lo;
+                if (live && nvalid < r_lo + kWT) {
+                    // V rows of this warp past the context hold stale codes
+                    // (NaN among them): zero them (P is 0 there, 0 * NaN is not)
+                    const int nz = (r_lo + kWT - nvalid) * 8;          // 16-byte chunks
+                    for (int idx = lane; idx < nz; idx += 32) {
+                        const int r = nvalid + idx / 8, c = idx % 8;
+                        *reinterpret_cast<uint4*>(v_half(stage, 0) + r * 128 + ((c ^ (r & swz)) << 4)) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    // ordered before the TMA that refills the stage later
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (live) {
+                    // S = Q K^T for the warp's 16 tokens (2 n-tiles)
+                    float sc[2][4];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+                        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                    {
+                        // matrices: (tokens 0-7, chunk kk), (8-15, kk), (0-7, kk + 1), (8-15, kk + 1)
+                        const int tr = r_lo + (lane & 7) + (((lane >> 3) & 1) << 3);
+                        const int chsel = lane >> 4;
+#pragma unroll
+                        for (int kp = 0; kp < kKS; kp += 2) {
+                            const int ch = kp + chsel;
+                            uint32_t r4[4];
+                            ldsm_x4(smem_u32(k_half(stage, 0) + tr * 128 + ((ch ^ (tr & swz)) << 4)),
+                                    r4[0], r4[1], r4[2], r4[3]);
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                mma_f16_16816(sc[u & 1], qa[kp + (u >> 1)], e4m3x2_to_f16x2(r4[u]),
+                                              e4m3x2_to_f16x2(r4[u] >> 16));
+                        }
+                    }
+                    if (t0 + r_lo + kWT - 1 > lim_min) {
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int tok = t0 + r_lo + nt * 8 + 2 * quad + (j & 1);
+                                if (tok > lim[j >> 1])
+                                    sc[nt][j] = -INFINITY;
+                            }
+                    }
+                    float mx[2], mu[2], mn[2];
+                    bool changed = false;
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        mx[rr] = fmaxf(fmaxf(sc[0][2 * rr], sc[0][2 * rr + 1]),
+                                       fmaxf(sc[1][2 * rr], sc[1][2 * rr + 1]));
+                        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+                        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+                        mn[rr] = fmaxf(m_run[rr], mx[rr] * a.scale_log2);
+                        changed |= mn[rr] != m_run[rr];
+                        mu[rr] = mn[rr] == -INFINITY ? 0.f : mn[rr];
+                    }
+                    if (__any_sync(0xffffffffu, changed)) {
+                        float corr[2];
+#pragma unroll
+                        for (int rr = 0; rr < 2; ++rr) {
+                            corr[rr] = mn[rr] == m_run[rr] ? 1.f : fast_exp2(m_run[rr] - mu[rr]);
+                            m_run[rr] = mn[rr];
+                            l_run[rr] *= corr[rr];
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < kONF; ++nt) {
+                            o[nt][0] *= corr[0];
+                            o[nt][1] *= corr[0];
+                            o[nt][2] *= corr[1];
+                            o[nt][3] *= corr[1];
+                        }
+                    }
+                    uint32_t pa[4];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        float p[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            p[j] = fast_exp2(fmaf(sc[nt][j], a.scale_log2, -mu[j >> 1]));
+                            l_run[j >> 1] += p[j];
+                        }
+                        pa[nt * 2 + 0] = pack_f16x2(p[0], p[1]);
+                        pa[nt * 2 + 1] = pack_f16x2(p[2], p[3]);
+                    }
+                    // O[:, all D] += P V over the warp's 16 tokens
+                    {
+                        // matrices: (tokens 0-7, chunk c), (8-15, c), (0-7, c + 1), (8-15, c + 1)
+                        const int tr = r_lo + (lane & 7) + (((lane >> 3) & 1) << 3);
+                        const int chsel = lane >> 4;
+#pragma unroll
+                        for (int cp = 0; cp < D / 16; cp += 2) {
+                            const int ch = cp + chsel;
+                            uint32_t r4[4];
+                            ldsm_x4_trans(smem_u32(v_half(stage, 0) + tr * 128 + ((ch ^ (tr & swz)) << 4)),
+                                          r4[0], r4[1], r4[2], r4[3]);
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int c = cp + u;
+                                const uint32_t lo = r4[2 * u], hi = r4[2 * u + 1];
+                                mma_f16_16816(o[2 * c], pa, e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0020u)),
+                                              e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0020u)));
+                                mma_f16_16816(o[2 * c + 1], pa, e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0031u)),
+                                              e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0031u)));
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[stage]);       // the stage is no longer read
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+
+            // ---- end of a piece: merge the four warp states ----------------
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
+                l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
+            }
+            named_barrier_sync(1, kConsumerThreads);   // the work tile's K/V are no longer read
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int rw = row0 + rr * 8;
+                const float il = l_run[rr] > 0.f ? 1.f / l_run[rr] : 0.f;
+                uint16_t* dst = wtile + (warp * kDecodeRows + rw) * D + 4 * quad;
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c)
+                    *reinterpret_cast<uint2*>(dst + 16 * c) =
+                        make_uint2(pack_f16x2(o[2 * c][2 * rr] * il, o[2 * c + 1][2 * rr] * il),
+                                   pack_f16x2(o[2 * c][2 * rr + 1] * il, o[2 * c + 1][2 * rr + 1] * il));
+                if (quad == 0) {
+                    wstate[warp][0][rw] = m_run[rr];
+                    wstate[warp][1][rw] = l_run[rr];
+                }
+            }
+            named_barrier_sync(1, kConsumerThreads);
+            float om[kON][4];
+            float Mr[2], Lr[2];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int rw = row0 + rr * 8;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    M = fmaxf(M, wstate[w][0][rw]);
+                float g[kConsumerWarps];                 // l_w 2^(m_w - M)
+                float L = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float mw = wstate[w][0][rw];
+                    g[w] = mw == -INFINITY ? 0.f : wstate[w][1][rw] * fast_exp2(mw - M);
+                    L += g[w];
+                }
+                Mr[rr] = M;
+                Lr[rr] = L;
+#pragma unroll
+                for (int nt = 0; nt < kON; ++nt) {
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+                        const __half2 h = *reinterpret_cast<const __half2*>(
+                            wtile + (w * kDecodeRows + rw) * D + col0 + nt * 8 + 2 * quad);
+                        const float2 v = __half22float2(h);
+                        s0 += g[w] * v.x;
+                        s1 += g[w] * v.y;
+                    }
+                    om[nt][2 * rr] = s0;
+                    om[nt][2 * rr + 1] = s1;
+                }
+            }
+            named_barrier_sync(1, kConsumerThreads);   // the tile may be refilled
+
+            const bool single =
+                a.whole_segments ||
+                block_of_unit(sp.seg_start + int64_t(kPieceUnits) * (sp.seg + 1), units, grid) ==
+                    block_of_unit(sp.seg_start + sp.seg_len - 1 + int64_t(kPieceUnits) * (sp.seg + 1),
+                                  units, grid);
+            const bool aborted = misc[0] != 0;
+            if (!aborted && single) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int64_t orow = out_row(sp, row0 + rr * 8);
+                    if (orow < 0)
+                        continue;
+                    const float inv = Lr[rr] > 0.f ? a.v_scale / Lr[rr] : 0.f;
+                    uint16_t* dst = a.out + orow * D + col0 + 2 * quad;
+#pragma unroll
+                    for (int nt = 0; nt < kON; ++nt)
+                        *reinterpret_cast<uint32_t*>(dst + nt * 8) =
+                            pack_bf16x2(om[nt][2 * rr] * inv, om[nt][2 * rr + 1] * inv);
+                }
+            } else if (!aborted) {
+                // the state carries v_scale, so the merge pass needs no change
+                float* slot = a.partials + (int64_t(sp.seg) + cta) * kSlotFloats;
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int rw = row0 + rr * 8;
+                    if (out_row(sp, rw) < 0)
+                        continue;
+                    if (warp == 0 && quad == 0) {
+                        slot[rw] = Mr[rr];
+                        slot[kDecodeRows + rw] = Lr[rr];
+                    }
+                    float* dst = slot + 2 * kDecodeRows + rw * D + col0 + 2 * quad;
+#pragma unroll
+                    for (int nt = 0; nt < kON; ++nt)
+                        *reinterpret_cast<float2*>(dst + nt * 8) =
+                            make_float2(om[nt][2 * rr] * a.v_scale, om[nt][2 * rr + 1] * a.v_scale);
+                }
+            }
+        }
+    } else {
     int64_t x = x_begin;
     while (x < x_end) {
         const SegmentPos sp = locate(pre, a.B, per_req, a.MT, x);
@@ -420,48 +712,83 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool ok = mbar_wait_warp(&full[stage], phase, misc, a.err);
             if (need_q) {
                 const uint8_t* qs = smem + Lay::kQ + stage * Lay::kHalves * Lay::kQHalfBytes;
-                if constexpr (F8) {
-                    // f16 fragments with the head dimension permuted inside
-                    // each 16-wide k-step the way the e4m3 K fragments come
-                    // out of ldmatrix: thread (row0, quad) holds d = 16 kk +
-                    // 4 quad + {0, 1} in a0 / a1 and + {2, 3} in a2 / a3.
 #pragma unroll
-                    for (int kk = 0; kk < kKS; ++kk) {
-                        const int d = 16 * kk + 4 * quad;
-                        const int hf = d >> 6, ch = (d & 63) >> 3;
+                for (int kk = 0; kk < kKS; ++kk) {
+                    const int r = lane & 15;
+                    const int ch = 2 * kk + (lane >> 4);   // 16-byte chunk along D
+                    ldsm_x4(smem_u32(qs + (ch >> 3) * Lay::kQHalfBytes + r * 128 +
+                                     (((ch & 7) ^ (r & 7)) << 4)),
+                            qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+                    if constexpr (F8) {   // the e4m3 path multiplies in f16
 #pragma unroll
-                        for (int rr = 0; rr < 2; ++rr) {
-                            const int r = row0 + 8 * rr;
-                            const uint2 v = *reinterpret_cast<const uint2*>(
-                                qs + hf * Lay::kQHalfBytes + r * 128 + ((ch ^ (r & 7)) << 4) +
-                                (quad & 1) * 8);
-                            qa[kk][rr] = bf16x2_to_f16x2(v.x);
-                            qa[kk][2 + rr] = bf16x2_to_f16x2(v.y);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < kKS; ++kk) {
-                        const int r = lane & 15;
-                        const int ch = 2 * kk + (lane >> 4);   // 16-byte chunk along D
-                        ldsm_x4(smem_u32(qs + (ch >> 3) * Lay::kQHalfBytes + r * 128 +
-                                         (((ch & 7) ^ (r & 7)) << 4)),
-                                qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+                        for (int u = 0; u < 4; ++u)
+                            qa[kk][u] = bf16x2_to_f16x2(qa[kk][u]);
                     }
                 }
                 need_q = false;
             }
+            if constexpr (F8) {
+                // e4m3 stage -> f16 work tile, once for the four warps: thread
+                // (row r, half hf) converts 64 codes of K and of V (rows past
+                // the context become zeros, so stale or NaN codes never reach
+                // the MMAs); the stage is released right after.
+                named_barrier_sync(1, kConsumerThreads);   // every warp is done with the tile
+                if (ok && nvalid > 0) {
+                    const int th = warp * 32 + lane;
+                    const int r = th >> 1, hf = th & 1;
+#pragma unroll
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const uint8_t* src = (kv ? v_half(stage, 0) : k_half(stage, 0)) + r * 128;
+                        uint8_t* dst = smem + Lay::kWork + kv * (Lay::kWorkBytes / 2) +
+                                       hf * Lay::kHalfBytes + r * 128;
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const int c = 4 * hf + cc;         // 16-code chunk: d = 16 c .. + 15
+                            uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+                            if (r < nvalid) {
+                                const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ (r & swz)) << 4));
+                                w0 = make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16),
+                                                e4m3x2_to_f16x2(v.y), e4m3x2_to_f16x2(v.y >> 16));
+                                w1 = make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16),
+                                                e4m3x2_to_f16x2(v.w), e4m3x2_to_f16x2(v.w >> 16));
+                            }
+                            const int q = 2 * cc;              // f16 chunk (8 elements) in the half
+                            *reinterpret_cast<uint4*>(dst + ((q ^ (r & 7)) << 4)) = w0;
+                            *reinterpret_cast<uint4*>(dst + (((q + 1) ^ (r & 7)) << 4)) = w1;
+                        }
+                    }
+                }
+                named_barrier_sync(1, kConsumerThreads);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[stage]);
+            }
+            // K / V of the granule as the MMAs read them: the stage (bf16) or
+            // the f16 work tile (e4m3 pages), same layout.
+            auto kt_half = [&](int half) -> const uint8_t* {
+                return F8 ? smem + Lay::kWork + half * Lay::kHalfBytes : k_half(stage, half);
+            };
+            auto vt_half = [&](int half) -> const uint8_t* {
+                return F8 ? smem + Lay::kWork + Lay::kWorkBytes / 2 + half * Lay::kHalfBytes
+                          : v_half(stage, half);
+            };
+            const int tswz = F8 ? 7 : swz;
+            auto mma = [&](float* d, const uint32_t* aa, uint32_t b0, uint32_t b1) {
+                if constexpr (F8)
+                    mma_f16_16816(d, aa, b0, b1);
+                else
+                    mma_bf16_16816(d, aa, b0, b1);
+            };
             bool wrote = false;
             if (ok && nvalid > 0) {
-                if (nvalid < kDecodeTokens) {
+                if (!F8 && nvalid < kDecodeTokens) {
                     // Zero this warp's V columns of the rows past the context:
                     // P is 0 there, but 0 * NaN is not.
-                    constexpr int kElemsPerChunk = F8 ? 16 : 8;
-                    constexpr int kChunks = kCols / kElemsPerChunk;  // 16-byte chunks per row
+                    constexpr int kChunks = kCols / 8;  // 16-byte chunks per row
                     const int nz = (kDecodeTokens - nvalid) * kChunks;
                     for (int idx = lane; idx < nz; idx += 32) {
                         const int r = nvalid + idx / kChunks;
-                        const int ch = col0 / kElemsPerChunk + idx % kChunks;
+                        const int ch = col0 / 8 + idx % kChunks;
                         *reinterpret_cast<uint4*>(v_half(stage, ch >> 3) + r * 128 +
                                                   (((ch & 7) ^ (r & swz)) << 4)) =
                             make_uint4(0, 0, 0, 0);
@@ -474,26 +801,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int nt = 0; nt < kSN; ++nt)
                     sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-                if constexpr (F8) {
-                    // One ldmatrix.x4 of e4m3 rows: 4 n-tiles of 8 tokens x one
-                    // 16-byte k-step; thread (row0, quad) gets 4 codes of token
-                    // row0 at d = 16 kk + 4 quad .. + 3, the two halves of
-                    // each register the two B registers (exact f16).
-#pragma unroll
-                    for (int kk = 0; kk < kKS; ++kk) {
-#pragma unroll
-                        for (int tq = 0; tq < kSN / 4; ++tq) {
-                            const int tr = tq * 32 + lane;
-                            uint32_t r4[4];
-                            ldsm_x4(smem_u32(k_half(stage, 0) + tr * 128 + ((kk ^ (tr & swz)) << 4)),
-                                    r4[0], r4[1], r4[2], r4[3]);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                mma_f16_16816(sc[4 * tq + i], qa[kk], e4m3x2_to_f16x2(r4[i]),
-                                              e4m3x2_to_f16x2(r4[i] >> 16));
-                        }
-                    }
-                } else {
+                {
                     const int trl = (lane & 7) + ((lane >> 4) << 3);
                     const int chsel = (lane >> 3) & 1;
 #pragma unroll
@@ -503,11 +811,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                         for (int tq = 0; tq < kSN / 2; ++tq) {
                             const int tr = tq * 16 + trl;
                             uint32_t b0, b1, b2, b3;
-                            ldsm_x4(smem_u32(k_half(stage, ch >> 3) + tr * 128 +
-                                             (((ch & 7) ^ (tr & swz)) << 4)),
+                            ldsm_x4(smem_u32(kt_half(ch >> 3) + tr * 128 +
+                                             (((ch & 7) ^ (tr & tswz)) << 4)),
                                     b0, b1, b2, b3);
-                            mma_bf16_16816(sc[2 * tq], qa[kk], b0, b1);
-                            mma_bf16_16816(sc[2 * tq + 1], qa[kk], b2, b3);
+                            mma(sc[2 * tq], qa[kk], b0, b1);
+                            mma(sc[2 * tq + 1], qa[kk], b2, b3);
                         }
                     }
                 }
@@ -579,33 +887,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 // O[:, col0 .. col0 + kCols) += P V; ldmatrix.trans gives the
                 // k-major V fragments.
-                if constexpr (F8) {
-                    // ldmatrix.x4.trans of e4m3 rows: tokens 16 kt + 0..7 and
-                    // + 8..15 of the warp's two 16-byte column chunks. A
-                    // register holds codes (token t, d), (t, d + 1), (t + 1, d),
-                    // (t + 1, d + 1) with t = 16 kt + 2 quad (+ 8), d = 16 c +
-                    // 2 (lane / 4): bytes 0, 2 feed the P V of the even d,
-                    // bytes 1, 3 that of the odd d. o[2 jj] / o[2 jj + 1] hold
-                    // columns 16 c + 4 quad + {0, 2} / {1, 3}.
-                    const int trl = (lane & 7) + (((lane >> 3) & 1) << 3);
-                    const int chsel = lane >> 4;
-#pragma unroll
-                    for (int kt = 0; kt < kSN / 2; ++kt) {
-                        const int tr = kt * 16 + trl;
-                        const int ch = col0 / 16 + chsel;
-                        uint32_t r4[4];
-                        ldsm_x4_trans(smem_u32(v_half(stage, 0) + tr * 128 + ((ch ^ (tr & swz)) << 4)),
-                                      r4[0], r4[1], r4[2], r4[3]);
-#pragma unroll
-                        for (int jj = 0; jj < 2; ++jj) {
-                            const uint32_t lo = r4[2 * jj], hi = r4[2 * jj + 1];
-                            mma_f16_16816(o[2 * jj], pa[kt], e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0020u)),
-                                          e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0020u)));
-                            mma_f16_16816(o[2 * jj + 1], pa[kt], e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0031u)),
-                                          e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0031u)));
-                        }
-                    }
-                } else {
+                {
                     const int trl = (lane & 7) + (((lane >> 3) & 1) << 3);
                     const int chsel = lane >> 4;
 #pragma unroll
@@ -615,11 +897,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                         for (int jj = 0; jj < kON / 2; ++jj) {
                             const int ch = col0 / 8 + 2 * jj + chsel;
                             uint32_t b0, b1, b2, b3;
-                            ldsm_x4_trans(smem_u32(v_half(stage, ch >> 3) + tr * 128 +
-                                                   (((ch & 7) ^ (tr & swz)) << 4)),
+                            ldsm_x4_trans(smem_u32(vt_half(ch >> 3) + tr * 128 +
+                                                   (((ch & 7) ^ (tr & tswz)) << 4)),
                                           b0, b1, b2, b3);
-                            mma_bf16_16816(o[2 * jj], pa[kt], b0, b1);
-                            mma_bf16_16816(o[2 * jj + 1], pa[kt], b2, b3);
+                            mma(o[2 * jj], pa[kt], b0, b1);
+                            mma(o[2 * jj + 1], pa[kt], b2, b3);
                         }
                     }
                 }
@@ -627,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (wrote)
                 fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0)
+            if (!F8 && lane == 0)
                 mbar_arrive(&empty[stage]);
             if (++stage == kStages) {
                 stage = 0;
@@ -655,18 +937,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int64_t orow = out_row(sp, row0 + rr * 8);
                 if (orow < 0)
                     continue;
-                if constexpr (F8) {
-                    const float inv = l_run[rr] > 0.f ? a.v_scale / l_run[rr] : 0.f;
-#pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        uint16_t* dst = a.out + orow * D + col0 + 16 * jj + 4 * quad;
-                        *reinterpret_cast<uint2*>(dst) =
-                            make_uint2(pack_bf16x2(o[2 * jj][2 * rr] * inv, o[2 * jj + 1][2 * rr] * inv),
-                                       pack_bf16x2(o[2 * jj][2 * rr + 1] * inv,
-                                                   o[2 * jj + 1][2 * rr + 1] * inv));
-                    }
-                } else {
-                    const float inv = l_run[rr] > 0.f ? 1.f / l_run[rr] : 0.f;
+                {
+                    // e4m3 pages: V is the code times v_scale (1 for bf16)
+                    const float inv = l_run[rr] > 0.f ? (F8 ? a.v_scale : 1.f) / l_run[rr] : 0.f;
                     uint16_t* dst = a.out + orow * D + col0 + 2 * quad;
 #pragma unroll
                     for (int nt = 0; nt < kON; ++nt)
@@ -687,25 +960,19 @@ __global__ void __launch_bounds__(kThreads, 2)
                     slot[rw] = m_run[rr];
                     slot[kDecodeRows + rw] = l_run[rr];
                 }
-                if constexpr (F8) {
+                {
                     // the state carries v_scale, so the merge pass needs no change
-                    const float vs = a.v_scale;
-#pragma unroll
-                    for (int jj = 0; jj < 2; ++jj)
-                        *reinterpret_cast<float4*>(slot + 2 * kDecodeRows + rw * D + col0 + 16 * jj +
-                                                   4 * quad) =
-                            make_float4(o[2 * jj][2 * rr] * vs, o[2 * jj + 1][2 * rr] * vs,
-                                        o[2 * jj][2 * rr + 1] * vs, o[2 * jj + 1][2 * rr + 1] * vs);
-                } else {
+                    const float vs = F8 ? a.v_scale : 1.f;
                     float* dst = slot + 2 * kDecodeRows + rw * D + col0 + 2 * quad;
 #pragma unroll
                     for (int nt = 0; nt < kON; ++nt)
                         *reinterpret_cast<float2*>(dst + nt * 8) =
-                            make_float2(o[nt][2 * rr], o[nt][2 * rr + 1]);
+                            make_float2(o[nt][2 * rr] * vs, o[nt][2 * rr + 1] * vs);
                 }
             }
         }
 
+    }
     }
 }
 

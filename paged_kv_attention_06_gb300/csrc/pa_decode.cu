@@ -402,6 +402,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         // o = sum l_w 2^(m_w - M) (O_w / l_w). Every warp then
         // holds its D/4 columns, as in the bf16 schedule, and the same
         // epilogue follows.
+        //   * Codes become f16 holding value / 256 by moving their bits into
+        //     the f16 fields (exact); the host folds the 256 into the scales.
         //   * K: ldmatrix (no transpose) of 8 byte rows gives lane (row0,
         //     quad) the codes of token row0 at d = 16 kk + 4 quad .. + 3; their
         //     two halves are the two f16 B registers when the head dimension
@@ -493,8 +495,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                                     r4[0], r4[1], r4[2], r4[3]);
 #pragma unroll
                             for (int u = 0; u < 4; ++u)
-                                mma_f16_16816(sc[u & 1], qa[kp + (u >> 1)], e4m3x2_to_f16x2(r4[u]),
-                                              e4m3x2_to_f16x2(r4[u] >> 16));
+                                mma_f16_16816(sc[u & 1], qa[kp + (u >> 1)],
+                                              e4m3_spread_to_f16x2_div256(__byte_perm(r4[u], 0u, 0x4140u)),
+                                              e4m3_spread_to_f16x2_div256(__byte_perm(r4[u], 0u, 0x4342u)));
                         }
                     }
                     if (t0 + r_lo + kWT - 1 > lim_min) {
@@ -562,10 +565,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                             for (int u = 0; u < 2; ++u) {
                                 const int c = cp + u;
                                 const uint32_t lo = r4[2 * u], hi = r4[2 * u + 1];
-                                mma_f16_16816(o[2 * c], pa, e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0020u)),
-                                              e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0020u)));
-                                mma_f16_16816(o[2 * c + 1], pa, e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0031u)),
-                                              e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0031u)));
+                                mma_f16_16816(o[2 * c], pa,
+                                              e4m3_spread_to_f16x2_div256(__byte_perm(lo, 0u, 0x4240u)),
+                                              e4m3_spread_to_f16x2_div256(__byte_perm(hi, 0u, 0x4240u)));
+                                mma_f16_16816(o[2 * c + 1], pa,
+                                              e4m3_spread_to_f16x2_div256(__byte_perm(lo, 0u, 0x4341u)),
+                                              e4m3_spread_to_f16x2_div256(__byte_perm(hi, 0u, 0x4341u)));
                             }
                         }
                     }
@@ -719,69 +724,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                     ldsm_x4(smem_u32(qs + (ch >> 3) * Lay::kQHalfBytes + r * 128 +
                                      (((ch & 7) ^ (r & 7)) << 4)),
                             qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-                    if constexpr (F8) {   // the e4m3 path multiplies in f16
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            qa[kk][u] = bf16x2_to_f16x2(qa[kk][u]);
-                    }
                 }
                 need_q = false;
             }
-            if constexpr (F8) {
-                // e4m3 stage -> f16 work tile, once for the four warps: thread
-                // (row r, half hf) converts 64 codes of K and of V (rows past
-                // the context become zeros, so stale or NaN codes never reach
-                // the MMAs); the stage is released right after.
-                named_barrier_sync(1, kConsumerThreads);   // every warp is done with the tile
-                if (ok && nvalid > 0) {
-                    const int th = warp * 32 + lane;
-                    const int r = th >> 1, hf = th & 1;
-#pragma unroll
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const uint8_t* src = (kv ? v_half(stage, 0) : k_half(stage, 0)) + r * 128;
-                        uint8_t* dst = smem + Lay::kWork + kv * (Lay::kWorkBytes / 2) +
-                                       hf * Lay::kHalfBytes + r * 128;
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            const int c = 4 * hf + cc;         // 16-code chunk: d = 16 c .. + 15
-                            uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
-                            if (r < nvalid) {
-                                const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ (r & swz)) << 4));
-                                w0 = make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16),
-                                                e4m3x2_to_f16x2(v.y), e4m3x2_to_f16x2(v.y >> 16));
-                                w1 = make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16),
-                                                e4m3x2_to_f16x2(v.w), e4m3x2_to_f16x2(v.w >> 16));
-                            }
-                            const int q = 2 * cc;              // f16 chunk (8 elements) in the half
-                            *reinterpret_cast<uint4*>(dst + ((q ^ (r & 7)) << 4)) = w0;
-                            *reinterpret_cast<uint4*>(dst + (((q + 1) ^ (r & 7)) << 4)) = w1;
-                        }
-                    }
-                }
-                named_barrier_sync(1, kConsumerThreads);
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&empty[stage]);
-            }
-            // K / V of the granule as the MMAs read them: the stage (bf16) or
-            // the f16 work tile (e4m3 pages), same layout.
-            auto kt_half = [&](int half) -> const uint8_t* {
-                return F8 ? smem + Lay::kWork + half * Lay::kHalfBytes : k_half(stage, half);
-            };
-            auto vt_half = [&](int half) -> const uint8_t* {
-                return F8 ? smem + Lay::kWork + Lay::kWorkBytes / 2 + half * Lay::kHalfBytes
-                          : v_half(stage, half);
-            };
-            const int tswz = F8 ? 7 : swz;
-            auto mma = [&](float* d, const uint32_t* aa, uint32_t b0, uint32_t b1) {
-                if constexpr (F8)
-                    mma_f16_16816(d, aa, b0, b1);
-                else
-                    mma_bf16_16816(d, aa, b0, b1);
-            };
             bool wrote = false;
             if (ok && nvalid > 0) {
-                if (!F8 && nvalid < kDecodeTokens) {
+                if (nvalid < kDecodeTokens) {
                     // Zero this warp's V columns of the rows past the context:
                     // P is 0 there, but 0 * NaN is not.
                     constexpr int kChunks = kCols / 8;  // 16-byte chunks per row
@@ -811,11 +759,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                         for (int tq = 0; tq < kSN / 2; ++tq) {
                             const int tr = tq * 16 + trl;
                             uint32_t b0, b1, b2, b3;
-                            ldsm_x4(smem_u32(kt_half(ch >> 3) + tr * 128 +
-                                             (((ch & 7) ^ (tr & tswz)) << 4)),
+                            ldsm_x4(smem_u32(k_half(stage, ch >> 3) + tr * 128 +
+                                             (((ch & 7) ^ (tr & swz)) << 4)),
                                     b0, b1, b2, b3);
-                            mma(sc[2 * tq], qa[kk], b0, b1);
-                            mma(sc[2 * tq + 1], qa[kk], b2, b3);
+                            mma_bf16_16816(sc[2 * tq], qa[kk], b0, b1);
+                            mma_bf16_16816(sc[2 * tq + 1], qa[kk], b2, b3);
                         }
                     }
                 }
@@ -877,13 +825,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                         p[j] = fast_exp2(fmaf(sc[nt][j], a.scale_log2, -mu[j >> 1]));
                         l_run[j >> 1] += p[j];
                     }
-                    if constexpr (F8) {
-                        pa[nt >> 1][(nt & 1) * 2 + 0] = pack_f16x2(p[0], p[1]);
-                        pa[nt >> 1][(nt & 1) * 2 + 1] = pack_f16x2(p[2], p[3]);
-                    } else {
-                        pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p[0], p[1]);
-                        pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p[2], p[3]);
-                    }
+                    pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p[0], p[1]);
+                    pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p[2], p[3]);
                 }
                 // O[:, col0 .. col0 + kCols) += P V; ldmatrix.trans gives the
                 // k-major V fragments.
@@ -897,11 +840,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                         for (int jj = 0; jj < kON / 2; ++jj) {
                             const int ch = col0 / 8 + 2 * jj + chsel;
                             uint32_t b0, b1, b2, b3;
-                            ldsm_x4_trans(smem_u32(vt_half(ch >> 3) + tr * 128 +
-                                                   (((ch & 7) ^ (tr & tswz)) << 4)),
+                            ldsm_x4_trans(smem_u32(v_half(stage, ch >> 3) + tr * 128 +
+                                                   (((ch & 7) ^ (tr & swz)) << 4)),
                                           b0, b1, b2, b3);
-                            mma(o[2 * jj], pa[kt], b0, b1);
-                            mma(o[2 * jj + 1], pa[kt], b2, b3);
+                            mma_bf16_16816(o[2 * jj], pa[kt], b0, b1);
+                            mma_bf16_16816(o[2 * jj + 1], pa[kt], b2, b3);
                         }
                     }
                 }
@@ -909,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (wrote)
                 fence_proxy_async_smem();
             __syncwarp();
-            if (!F8 && lane == 0)
+            if (lane == 0)
                 mbar_arrive(&empty[stage]);
             if (++stage == kStages) {
                 stage = 0;
@@ -937,15 +880,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int64_t orow = out_row(sp, row0 + rr * 8);
                 if (orow < 0)
                     continue;
-                {
-                    // e4m3 pages: V is the code times v_scale (1 for bf16)
-                    const float inv = l_run[rr] > 0.f ? (F8 ? a.v_scale : 1.f) / l_run[rr] : 0.f;
-                    uint16_t* dst = a.out + orow * D + col0 + 2 * quad;
+                const float inv = l_run[rr] > 0.f ? 1.f / l_run[rr] : 0.f;
+                uint16_t* dst = a.out + orow * D + col0 + 2 * quad;
 #pragma unroll
-                    for (int nt = 0; nt < kON; ++nt)
-                        *reinterpret_cast<uint32_t*>(dst + nt * 8) =
-                            pack_bf16x2(o[nt][2 * rr] * inv, o[nt][2 * rr + 1] * inv);
-                }
+                for (int nt = 0; nt < kON; ++nt)
+                    *reinterpret_cast<uint32_t*>(dst + nt * 8) =
+                        pack_bf16x2(o[nt][2 * rr] * inv, o[nt][2 * rr + 1] * inv);
             }
         } else if (!aborted) {
             // A segment that straddles blocks: leave this block's partial
@@ -960,15 +900,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                     slot[rw] = m_run[rr];
                     slot[kDecodeRows + rw] = l_run[rr];
                 }
-                {
-                    // the state carries v_scale, so the merge pass needs no change
-                    const float vs = F8 ? a.v_scale : 1.f;
-                    float* dst = slot + 2 * kDecodeRows + rw * D + col0 + 2 * quad;
+                float* dst = slot + 2 * kDecodeRows + rw * D + col0 + 2 * quad;
 #pragma unroll
-                    for (int nt = 0; nt < kON; ++nt)
-                        *reinterpret_cast<float2*>(dst + nt * 8) =
-                            make_float2(o[nt][2 * rr] * vs, o[nt][2 * rr + 1] * vs);
-                }
+                for (int nt = 0; nt < kON; ++nt)
+                    *reinterpret_cast<float2*>(dst + nt * 8) =
+                        make_float2(o[nt][2 * rr], o[nt][2 * rr + 1]);
             }
         }
 

@@ -243,11 +243,13 @@ __device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint3
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two e4m3 codes (the low 16 bits; the lower byte first) -> two f16, exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v)
+// Two e4m3 codes, in bytes 0 and 2 of y, -> two f16 holding value / 256, for
+// every finite code exactly: the code's exponent and mantissa bits are moved
+// into the f16 fields, and the f16 bias (15, against 7) divides by 2^8;
+// e4m3 subnormals land on f16 subnormals. A NaN code reads as 480 / 256.
+__device__ __forceinline__ uint32_t e4m3_spread_to_f16x2_div256(uint32_t y)
 {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(v & 0xffffu), __NV_E4M3);
-    return uint32_t(h.x) | (uint32_t(h.y) << 16);
+    return ((y << 7) & 0x3F803F80u) | ((y << 8) & 0x80008000u);
 }
 
 // Two fp32 -> two e4m3 codes (round to nearest even, saturated to +-448),

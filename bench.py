@@ -50,6 +50,36 @@ def _env_int(name, default):
         return default
 
 
+def timed_region(dist, sync, run):
+    """Runs `run()` between a barrier and a device synchronize on both sides
+    (every rank enters and leaves together). Returns run()'s result."""
+    if dist is not None:
+        dist.barrier()
+    sync()
+    out = run()
+    sync()
+    if dist is not None:
+        dist.barrier()
+    return out
+
+
+def max_over_ranks(dist, value, device=None):
+    """The largest `value` over all ranks, returned on every rank (the value
+    itself with one rank): the whole job is as slow as its slowest replica."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world, bytes_per_step, ms_per_step):
+    """GB/s of the whole job: every replica moves `bytes_per_step` per step and
+    a step takes the slowest rank's `ms_per_step`."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def step_bytes(b: wl.PagedBatch):
     """Algorithmic bytes of one step: (decode kernel, append kernel)."""
     n = b.context_lens.astype(np.int64)
@@ -414,24 +444,16 @@ def main(argv=None):
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
     wall0 = time.time()
     host0 = time.perf_counter()
-    total_ms, dec_ms = run_steps(args.steps)
+    total_ms, dec_ms = timed_region(dist, torch.cuda.synchronize,
+                                    lambda: run_steps(args.steps))
     host_s = time.perf_counter() - host0
-    torch.cuda.synchronize()
     wall1 = time.time()
-    if dist is not None:
-        dist.barrier()
     status, flags = pa.pa_get_device_error()
     if status:
         raise RuntimeError(f"device error in the timed region: {flags:#x}")
-    if dist is not None:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(dist, total_ms, device)
 
     # ---- e2e: same step through the C ABI from pinned host buffers ---------
     def pinned(x):
@@ -464,7 +486,9 @@ def main(argv=None):
         return float(total.value)
 
     run_e2e(3)
-    e2e_ms = run_e2e(e2e_steps) / e2e_steps
+    e2e_ms = max_over_ranks(dist, timed_region(dist, torch.cuda.synchronize,
+                                               lambda: run_e2e(e2e_steps)) / e2e_steps,
+                            device)
 
     # ---- secondary: the other decode workloads ------------------------------
     other_decode = []
@@ -494,7 +518,7 @@ def main(argv=None):
 
     ms_step = total_ms / args.steps
     dec_avg_ms = float(np.mean(dec_ms))
-    value = world * (dec_bytes + app_bytes) / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, dec_bytes + app_bytes, ms_step)
     hbm_peak, bf16_peak, peak_kind = load_peaks()
     achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
     traffic = committed_traffic("decode_kernel", b.name)
@@ -525,7 +549,7 @@ def main(argv=None):
                      "kernel": "decode_kernel<128> + decode_merge_kernel<128> (one pa_decode call)",
                      "algorithmic_bytes_per_launch": dec_bytes},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * (dec_bytes + app_bytes) / (e2e_ms * 1e-3) / 1e9, 3),
+        "e2e": {"value": round(whole_job_gbs(world, dec_bytes + app_bytes, e2e_ms), 3),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 6), "steps": e2e_steps},
         "gpu_launches": (3 if route == 0 else 2) * args.steps,

@@ -8,6 +8,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "../../include/pagedattn.h"
@@ -18,6 +20,19 @@ namespace pa {
 // Device error word: kernels OR PA_DEVERR_* bits into it; pa_get_device_error
 // reads and clears it. One copy per device that loads the library.
 __device__ unsigned int g_device_error;
+
+uint64_t next_launch_stamp()
+{
+    static std::atomic<uint64_t> stamp{0};
+    if (stamp.load(std::memory_order_relaxed) == 0) {
+        const uint64_t seed = uint64_t(
+            std::chrono::steady_clock::now().time_since_epoch().count()) * 0x9E3779B97F4A7C15ull;
+        uint64_t expected = 0;
+        stamp.compare_exchange_strong(expected, (seed >> 16) | 1ull);
+    }
+    uint64_t st = stamp.fetch_add(1, std::memory_order_relaxed) & ((uint64_t(1) << 48) - 1);
+    return st == 0 ? 1 : st;
+}
 
 namespace {
 

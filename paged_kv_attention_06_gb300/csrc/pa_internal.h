@@ -113,6 +113,12 @@ struct PrefillArgs {
     int32_t causal;
 };
 
+// Stamps for the publish flags of kernels that hand partial states between
+// blocks: distinct for every launch of this process, the first one
+// seeded from a clock reading so that flags left in a workspace by an earlier
+// process are not mistaken for this launch's. Never 0; 48 bits.
+uint64_t next_launch_stamp();
+
 // Prefill with the K/V tiles of all (request, head pair, query tile) items
 // split evenly over a persistent grid (one block per SM, all resident); an
 // item cut by a block boundary is finished by the block that holds its first

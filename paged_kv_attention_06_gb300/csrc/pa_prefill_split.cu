@@ -55,7 +55,6 @@
 #include <string.h>
 
 #include <atomic>
-#include <chrono>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -1020,10 +1019,6 @@ cudaError_t launch_prefill_split(const CUtensorMap& q_map, const CUtensorMap& ke
     constexpr int kMaxDev = 64;
     static std::atomic<int> smem_set[kMaxDev];
     static std::atomic<int> regs_ok[kMaxDev];
-    // Launch stamps: distinct for every launch of this process, starting from
-    // a clock reading so that a workspace left by an earlier process is not
-    // mistaken for this one's.
-    static std::atomic<uint64_t> stamp{0};
     if (device < 0 || device >= kMaxDev)
         return cudaErrorInvalidDevice;
     int rk = regs_ok[device].load(std::memory_order_relaxed);
@@ -1047,16 +1042,7 @@ cudaError_t launch_prefill_split(const CUtensorMap& q_map, const CUtensorMap& ke
             return e;
         smem_set[device].store(smem, std::memory_order_relaxed);
     }
-    uint64_t st = stamp.load(std::memory_order_relaxed);
-    if (st == 0) {
-        const uint64_t seed = uint64_t(
-            std::chrono::steady_clock::now().time_since_epoch().count()) * 0x9E3779B97F4A7C15ull;
-        uint64_t expected = 0;
-        stamp.compare_exchange_strong(expected, (seed >> 16) | 1ull);
-    }
-    st = stamp.fetch_add(1, std::memory_order_relaxed) & ((uint64_t(1) << 48) - 1);
-    if (st == 0)
-        st = 1;
+    const uint64_t st = next_launch_stamp();
     uint8_t* w = static_cast<uint8_t*>(workspace);
     const size_t state = size_t(grid) * size_t(kStateFloats) * sizeof(float);
     const size_t ml = size_t(grid) * size_t(kMlEntries) * 2 * sizeof(float);

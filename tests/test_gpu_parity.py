@@ -237,6 +237,23 @@ def test_workspace_contents_do_not_matter():
         assert np.array_equal(outs[0], o)
 
 
+@pytest.mark.parametrize("n_ctx,H_q", [(40000, 8), (9000, 4), (200, 2)])
+def test_one_segment_split_over_blocks(n_ctx, H_q):
+    """A single (request, KV head) segment cut into one piece per block: the
+    pieces publish their partial states and whichever block sees them all
+    merges. Repeated calls are bit-identical whichever block merged."""
+    b = wl.build_batch("one_segment", B=1, H_q=H_q, H_kv=1, D=128, page_size=16, L=1,
+                       context_lens=[n_ctx], seed=31, L_new=0)
+    db = DeviceBatch(b)
+    outs = [host_bits(gpu_step(db, route="decode", append=False)) for _ in range(6)]
+    check_no_device_error()
+    for o in outs[1:]:
+        assert np.array_equal(outs[0], o)
+    ref = oracle_out(b, b.key_pages, b.value_pages)
+    got = host_f64(gpu_step(db, route="decode", append=False))
+    assert_close(got, ref, f"one segment, {n_ctx} keys")
+
+
 def test_non_default_stream():
     b = wl.make_workload("tiny_decode")
     db = DeviceBatch(b)

@@ -237,14 +237,51 @@ pa_status pa_append_kv_fp8(const void *key, const void *value, void *key_pages,
  * values convert exactly; the query is taken in f16 too, so its elements
  * must have magnitudes within f16's range (below 65504; below 2^-14 they keep
  * fewer bits). A NaN code in a visible slot reads as 480 (times the scale),
- * not NaN; slots past a request's context are never read. Any query length
- * (no prefill kernel for e4m3 pools).
+ * not NaN; slots past a request's context are never read. Any query length;
+ * for prefill chunks pa_prefill_fp8 is the faster call.
  */
 pa_status pa_decode_fp8(const void *query, const void *key_pages, const void *value_pages,
                         const int32_t *block_table, const int32_t *context_lens, int32_t page_size,
                         float scale, float k_scale, float v_scale, int causal, void *out,
                         pa_shape shape, int32_t max_context_len, void *workspace,
                         size_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of device workspace pa_prefill_fp8 needs for `shape` (head_dim 128)
+ * with contexts of at most max_context_len tokens, on the CURRENT device; 0
+ * on invalid shapes. It holds bf16 copies of K and V in pages of 128 tokens
+ * (batch * ceil(max_context_len / 128) pages of num_kv_heads * 128 * 128
+ * elements each, 64 KiB per page and KV head for K and V together), their
+ * page table, and the split prefill's workspace when pa_prefill_fp8 takes
+ * that kernel for the shape (the same rule as pa_attention's prefill route).
+ */
+size_t pa_prefill_fp8_workspace_bytes(pa_shape shape, int32_t max_context_len);
+
+/*
+ * Prefill attention over e4m3 pools (the pools of pa_append_kv_fp8): the
+ * result of pa_decode_fp8 (every K element value(code) * k_scale, every V
+ * element value(code) * v_scale, bottom-right causal mask when `causal`) on
+ * the tensor-core prefill kernels. Two kernels on `stream`:
+ *   1. the K/V tokens each request can see are copied into bf16 pages of
+ *      128 tokens in the workspace, each code converted to its exact value
+ *      (e4m3 values are bf16 values; a NaN code stays NaN);
+ *   2. pa_prefill's kernels (or pa_prefill_split's, by pa_attention's rule)
+ *      attend over the copies, with scale * k_scale as the softmax scale and
+ *      the output multiplied by v_scale, so the scaled values are never
+ *      rounded.
+ * Arguments as pa_decode_fp8. max_context_len bounds context_lens and sizes
+ * the copy; a longer entry records PA_DEVERR_CONTEXT_LEN and is cut to
+ * ceil(max_context_len / 128) * 128 tokens. workspace: at least
+ * pa_prefill_fp8_workspace_bytes(shape, max_context_len) bytes, 256-byte
+ * aligned, any contents; calls sharing one must not overlap on the GPU.
+ * head_dim 128 only (PA_ERR_UNSUPPORTED otherwise); k_scale and v_scale
+ * finite and > 0 (PA_ERR_INVALID_ARG).
+ */
+pa_status pa_prefill_fp8(const void *query, const void *key_pages, const void *value_pages,
+                         const int32_t *block_table, const int32_t *context_lens,
+                         int32_t page_size, float scale, float k_scale, float v_scale, int causal,
+                         void *out, pa_shape shape, int32_t max_context_len, void *workspace,
+                         size_t workspace_bytes, void *stream);
 
 /*
  * Bytes of device workspace pa_prefill_split needs for `shape` and

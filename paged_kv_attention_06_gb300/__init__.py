@@ -12,7 +12,8 @@ _API = ("pa_append_kv", "pa_decode", "pa_prefill", "pa_attention", "pa_attention
         "pa_debug_arm_wait_timeout", "pa_debug_prefill_variant", "pa_decode_noalloc",
         "pa_gather_kv", "pa_decode_dense", "KVCache", "KVCacheSnapshot",
         "pa_prefill_split", "pa_prefill_workspace_bytes", "prefill_workspace",
-        "pa_append_kv_fp8", "pa_decode_fp8")
+        "pa_append_kv_fp8", "pa_decode_fp8", "pa_prefill_fp8",
+        "pa_prefill_fp8_workspace_bytes")
 
 
 def __getattr__(name):

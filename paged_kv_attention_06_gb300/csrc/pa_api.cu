@@ -239,7 +239,7 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
                          const int32_t* block_table, const int32_t* context_lens,
                          int32_t page_size, float scale, int causal, void* out,
                          const pa_shape& s, cudaStream_t stream, void* workspace = nullptr,
-                         size_t workspace_bytes = 0)
+                         size_t workspace_bytes = 0, float out_scale = 1.f)
 {
     DeviceInfo* dev;
     pa_status st = device_info(&dev);
@@ -286,6 +286,7 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     a.box_rows = int32_t(box);
     a.scale_log2 = scale * 1.4426950408889634f;
     a.causal = causal ? 1 : 0;
+    a.out_scale = out_scale;
     if (split) {
         SplitPrefillArgs sa;
         memset(&sa, 0, sizeof sa);
@@ -305,6 +306,7 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
         sa.box_rows = a.box_rows;
         sa.scale_log2 = a.scale_log2;
         sa.causal = a.causal;
+        sa.out_scale = a.out_scale;
         cudaError_t e = launch_prefill_split(qmap, kmap, vmap, sa, dev->sm_count, workspace,
                                              dev->id, stream);
         if (e == cudaSuccess)
@@ -497,6 +499,105 @@ size_t pa_decode_workspace_bytes(pa_shape shape)
         return 0;
     return decode_workspace_bytes(decode_segments(shape), decode_max_grid(dev->sm_count),
                                   shape.head_dim);
+}
+
+namespace {
+
+// Prefill over e4m3 pools: the workspace holds the bf16 copies of K and V
+// (B * P2 pages of [H_kv, 128, 128]), the copies' page table, then (256-byte
+// aligned) the split prefill's workspace where that kernel serves the shape.
+struct Fp8PrefillPlan {
+    int64_t P2 = 0;
+    pa_shape copy{};
+    size_t kv_bytes = 0, table_off = 0, split_off = 0, split_bytes = 0, total = 0;
+};
+
+pa_status plan_prefill_fp8(const pa_shape& s, int32_t max_context_len, DeviceInfo* dev,
+                           Fp8PrefillPlan* p)
+{
+    if (max_context_len < 0 || s.batch <= 0 || s.num_kv_heads <= 0 || s.num_q_heads <= 0)
+        return PA_ERR_INVALID_ARG;
+    p->P2 = fp8_copy_pages(max_context_len);
+    const int64_t pages = int64_t(s.batch) * p->P2;
+    if (pages * s.num_kv_heads * 128 >= (int64_t(1) << 31) || p->P2 * 128 >= (int64_t(1) << 30))
+        return PA_ERR_UNSUPPORTED;
+    p->copy = s;
+    p->copy.head_dim = 128;
+    p->copy.num_pages = int32_t(pages);
+    p->copy.max_pages = int32_t(p->P2);
+    p->kv_bytes = size_t(pages) * s.num_kv_heads * 128 * 128 * 2;
+    p->table_off = 2 * p->kv_bytes;
+    const size_t table_bytes = size_t(pages) * 4;
+    p->split_off = (p->table_off + table_bytes + 255) & ~size_t(255);
+    // the kernel choice of pa_attention's prefill route (split below 1.5
+    // items per SM)
+    const int64_t items = int64_t(s.batch) * ((int64_t(s.q_len) + 127) / 128) * (s.num_q_heads / 2);
+    p->split_bytes = 2 * items < 3 * int64_t(dev->sm_count) ? split_prefill_need(p->copy, 128, dev) : 0;
+    p->total = p->split_off + p->split_bytes;
+    return PA_OK;
+}
+
+}  // namespace
+
+size_t pa_prefill_fp8_workspace_bytes(pa_shape shape, int32_t max_context_len)
+{
+    if (shape.head_dim != 128)
+        return 0;
+    DeviceInfo* dev;
+    if (device_info(&dev) != PA_OK)
+        return 0;
+    Fp8PrefillPlan p;
+    if (plan_prefill_fp8(shape, max_context_len, dev, &p) != PA_OK)
+        return 0;
+    return p.total;
+}
+
+pa_status pa_prefill_fp8(const void* query, const void* key_pages, const void* value_pages,
+                         const int32_t* block_table, const int32_t* context_lens,
+                         int32_t page_size, float scale, float k_scale, float v_scale, int causal,
+                         void* out, pa_shape shape, int32_t max_context_len, void* workspace,
+                         size_t workspace_bytes, void* stream)
+{
+    pa_status st = check_attention(query, key_pages, value_pages, block_table, context_lens,
+                                   page_size, scale, out, shape);
+    if (st != PA_OK)
+        return st;
+    if (!(k_scale > 0.f) || !isfinite(k_scale) || !(v_scale > 0.f) || !isfinite(v_scale))
+        return PA_ERR_INVALID_ARG;
+    if (shape.head_dim != 128)
+        return PA_ERR_UNSUPPORTED;
+    DeviceInfo* dev;
+    if ((st = device_info(&dev)) != PA_OK)
+        return st;
+    Fp8PrefillPlan p;
+    if ((st = plan_prefill_fp8(shape, max_context_len, dev, &p)) != PA_OK)
+        return st;
+    if (!workspace || workspace_bytes < p.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PA_ERR_WORKSPACE;
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    Fp8PagesArgs c;
+    memset(&c, 0, sizeof c);
+    c.key_pages = static_cast<const uint8_t*>(key_pages);
+    c.value_pages = static_cast<const uint8_t*>(value_pages);
+    c.block_table = block_table;
+    c.context_lens = context_lens;
+    c.key_out = reinterpret_cast<uint16_t*>(w);
+    c.value_out = reinterpret_cast<uint16_t*>(w + p.kv_bytes);
+    c.table_out = reinterpret_cast<int32_t*>(w + p.table_off);
+    c.err = dev->err;
+    c.B = shape.batch;
+    c.H_kv = shape.num_kv_heads;
+    c.ps = page_size;
+    c.max_pages = shape.max_pages;
+    c.num_pages = shape.num_pages;
+    c.P2 = int32_t(p.P2);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_fp8_pages_to_bf16(c, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    // k_scale into the softmax scale, v_scale into the output normalisation
+    return run_prefill_tc(query, c.key_out, c.value_out, c.table_out, context_lens, 128,
+                          scale * k_scale, causal, out, p.copy, s,
+                          p.split_bytes ? w + p.split_off : nullptr, p.split_bytes, v_scale);
 }
 
 pa_status pa_append_kv_fp8(const void* key, const void* value, void* key_pages,

@@ -111,7 +111,26 @@ struct PrefillArgs {
     int32_t box_rows;   // rows per K/V TMA box: min(ps, 128)
     float scale_log2;
     int32_t causal;
+    float out_scale;    // the output is out_scale * softmax . V (e4m3 copies: v_scale)
 };
+
+// Prefill over e4m3 pools: bf16 copies of the visible K/V tokens, in pages
+// of 128 tokens; copy page b * P2 + p holds tokens [128 p, 128 p + 128) of
+// request b.
+struct Fp8PagesArgs {
+    const uint8_t* key_pages;     // [P, H_kv, ps, 128] e4m3 codes
+    const uint8_t* value_pages;
+    const int32_t* block_table;   // [B, max_pages]
+    const int32_t* context_lens;  // [B]
+    uint16_t* key_out;            // [B * P2, H_kv, 128, 128] bf16
+    uint16_t* value_out;
+    int32_t* table_out;           // [B, P2]: b * P2 + p
+    unsigned* err;
+    int32_t B, H_kv, ps, max_pages, num_pages;
+    int32_t P2;                   // copy pages per request: ceil(max_context_len / 128)
+};
+int64_t fp8_copy_pages(int64_t max_context_len);
+cudaError_t launch_fp8_pages_to_bf16(const Fp8PagesArgs& a, cudaStream_t stream);
 
 // Stamps for the publish flags of kernels that hand partial states between
 // blocks: distinct for every launch of this process, the first one
@@ -138,6 +157,7 @@ struct SplitPrefillArgs {
     int32_t box_rows;   // rows per K/V TMA box: min(ps, 128)
     float scale_log2;
     int32_t causal;
+    float out_scale;    // the output is out_scale * softmax . V (e4m3 copies: v_scale)
 };
 
 size_t prefill_split_smem_bytes();

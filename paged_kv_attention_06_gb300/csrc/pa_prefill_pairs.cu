@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bar[kPFull + head]);
         }
         // ---- epilogue: O / l -> bf16 ----------------------------------------
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? a.out_scale / l : 0.f;
         if (nt > 0) {
             mbar_wait_warp(&bar[kPVDone + head], (nt - 1) & 1, misc, a.err);
             tc_fence_after();

@@ -812,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int p_nt = vp->nt;
             const bool split = has_tiles && (k_first > 0 || k_end < p_nt);
             if (!split) {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float inv = l > 0.f ? a.out_scale / l : 0.f;
 #pragma unroll 1
                 for (int hf = 0; hf < 2; ++hf) {
                     uint32_t ov[64];
@@ -910,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float f_own = m_used == -INFINITY ? 0.f : fast_exp2(m_used - mx);
                     const float f = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mx);
                     const float lt = l * f_own + ml.y * f;
-                    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                    const float inv = lt > 0.f ? a.out_scale / lt : 0.f;
                     uint32_t pk[32];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -948,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float2 ml = __ldcg(a.state_ml + (int64_t(cc) * 2 + head) * 128 + r);
                         lt += ml.x == -INFINITY ? 0.f : ml.y * fast_exp2(ml.x - mx);
                     }
-                    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                    const float inv = lt > 0.f ? a.out_scale / lt : 0.f;
 #pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {         // 64 columns per pass
                         uint32_t ov[64];

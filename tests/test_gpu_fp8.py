@@ -144,3 +144,105 @@ def test_append_then_decode_fp8():
     ref = oracle.attention_fp8(b.query, kp, vp, ks, vs, b.block_table, b.context_lens,
                                b.page_size, scale=b.scale, n_threads=N_THREADS)
     assert_close(host_f64(out), ref, "fp8 append + decode")
+
+
+# ----------------------------------------------------------------------------
+# Prefill over e4m3 pools (bf16 copies of the visible tokens + the tensor-core
+# prefill kernels)
+
+
+def _run_prefill(b, kc, vc, k_scale, v_scale, rows=None, max_context_len=None):
+    pa = _pa()
+    mcl = int(b.context_lens.max()) if max_context_len is None else max_context_len
+    out = pa.pa_prefill_fp8(dev(b.query), _u8(kc), _u8(vc), dev(b.block_table),
+                            dev(b.context_lens), b.page_size, k_scale, v_scale, scale=b.scale,
+                            causal=b.causal, max_context_len=mcl)
+    ref = oracle.attention_fp8(b.query, kc, vc, k_scale, v_scale, b.block_table,
+                               b.context_lens, b.page_size, scale=b.scale, causal=b.causal,
+                               rows=rows, n_threads=N_THREADS)
+    got = host_f64(out)
+    if rows is not None:
+        got = got[rows[:, 0], rows[:, 1], rows[:, 2]]
+    return got, ref
+
+
+@pytest.mark.parametrize("ps", [16, 1, 128])
+@pytest.mark.parametrize("L,causal", [(64, True), (130, True), (257, False)])
+def test_prefill_fp8_matches_oracle(ps, L, causal):
+    lens = [L, L + 300, 700, 2 * L + 5]
+    b, kc, vc = _fp8_batch("fp8pre", 4, 8, 2, ps, L, lens, seed=300 + L + ps, causal=causal)
+    got, ref = _run_prefill(b, kc, vc, 0.05, 0.04)
+    check_no_device_error()
+    assert_close(got, ref, f"fp8 prefill ps={ps} L={L} causal={causal}")
+
+
+@pytest.mark.parametrize("H_q,H_kv", [(6, 2), (4, 4)])   # group of 3 / 1: one head per block
+def test_prefill_fp8_one_head_kernel(H_q, H_kv):
+    b, kc, vc = _fp8_batch("fp8pre1", 3, H_q, H_kv, 16, 100, [100, 333, 1000], seed=61)
+    got, ref = _run_prefill(b, kc, vc, 0.02, 0.09)
+    check_no_device_error()
+    assert_close(got, ref, f"fp8 prefill G={H_q // H_kv}")
+
+
+def test_prefill_fp8_head_pairs_kernel_sampled_rows():
+    """Enough (request, head pair, 128-row tile) items for the whole-item
+    pairs kernel (8 x 4 x 8 = 256 items): sampled rows against the oracle."""
+    rng = np.random.default_rng(62)
+    lens = [int(x) for x in rng.integers(512, 1600, size=8)]
+    b, kc, vc = _fp8_batch("fp8pairs", 8, 16, 4, 16, 512, lens, seed=62)
+    rows = np.stack([rng.integers(0, 8, 400), rng.integers(0, 16, 400),
+                     rng.integers(0, 512, 400)], axis=1).astype(np.int32)
+    rows[:8, 2] = [0, 1, 127, 128, 255, 256, 510, 511]
+    got, ref = _run_prefill(b, kc, vc, 0.05, 0.05, rows=rows)
+    check_no_device_error()
+    assert_close(got, ref, "fp8 prefill pairs kernel")
+
+
+def test_prefill_fp8_short_and_empty_contexts():
+    b, kc, vc = _fp8_batch("fp8pre0", 3, 8, 2, 16, 40, [0, 7, 40], seed=63)
+    got, ref = _run_prefill(b, kc, vc, 0.1, 0.1)
+    check_no_device_error()
+    assert np.all(got[0] == 0)                 # no keys at all
+    assert np.all(got[1, :, :33] == 0)         # rows before the first key
+    assert_close(got, ref, "fp8 prefill short contexts")
+
+
+def test_prefill_fp8_agrees_with_decode_kernel():
+    b, kc, vc = _fp8_batch("fp8agree", 2, 8, 2, 16, 48, [48, 900], seed=64)
+    pa = _pa()
+    got_p, ref = _run_prefill(b, kc, vc, 0.05, 0.05)
+    got_d, _ = _run(b, kc, vc, 0.05, 0.05)
+    check_no_device_error()
+    assert_close(got_p, ref, "prefill kernels")
+    assert_close(got_d, ref, "split-KV kernel")
+
+
+def test_prefill_fp8_context_beyond_bound_is_flagged_and_cut():
+    pa = _pa()
+    b, kc, vc = _fp8_batch("fp8cut", 2, 8, 2, 16, 16, [200, 130], seed=65)
+    got, _ = _run_prefill(b, kc, vc, 0.05, 0.05, max_context_len=100)   # copies 128 tokens
+    status, flags = pa.pa_get_device_error()
+    assert flags & pa.PA_DEVERR_CONTEXT_LEN
+    cut = b.context_lens.copy()
+    cut[:] = np.minimum(cut, 128)
+    ref = oracle.attention_fp8(b.query, kc, vc, 0.05, 0.05, b.block_table, cut, b.page_size,
+                               scale=b.scale, causal=b.causal, n_threads=N_THREADS)
+    assert_close(got, ref, "fp8 prefill, contexts cut to the copy")
+
+
+def test_prefill_fp8_rejects_bad_arguments():
+    pa = _pa()
+    b, kc, vc = _fp8_batch("fp8bad", 1, 8, 2, 16, 8, [40], seed=66)
+    args = (dev(b.query), _u8(kc), _u8(vc), dev(b.block_table), dev(b.context_lens),
+            b.page_size)
+    shape = pa.make_shape(b.query.shape, kc.shape, b.block_table.shape[1])
+    need = pa.pa_prefill_fp8_workspace_bytes(shape, 40)
+    assert need > 0
+    small = torch.zeros(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PagedAttentionError) as e:
+        pa.pa_prefill_fp8(*args, 0.05, 0.05, max_context_len=40, workspace=small)
+    assert e.value.status == pa.PA_ERR_WORKSPACE
+    with pytest.raises(pa.PagedAttentionError) as e:
+        pa.pa_prefill_fp8(*args, 0.0, 0.05, max_context_len=40)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+    check_no_device_error()

@@ -1023,6 +1023,16 @@ def prefill_shapes(torch, device, only=None, steps=15):
                                                causal=True, out=out))
         t_split = timeit(lambda: pa.pa_prefill_split(q, kp, vp, bt, cl, b.page_size,
                                                      scale=b.scale, causal=True, out=out))
+        rng = np.random.default_rng(6)
+        kc = torch.from_numpy(wl.random_e4m3_codes(rng, b.key_pages.shape)).to(device)
+        vc = torch.from_numpy(wl.random_e4m3_codes(rng, b.value_pages.shape)).to(device)
+        mcl = int(b.context_lens.max())
+        ws8 = torch.empty(pa.pa_prefill_fp8_workspace_bytes(
+            pa.make_shape(q.shape, kc.shape, bt.shape[1]), mcl), dtype=torch.uint8, device=device)
+        t_fp8 = timeit(lambda: pa.pa_prefill_fp8(q, kc, vc, bt, cl, b.page_size, 0.05, 0.05,
+                                                 scale=b.scale, causal=True, out=out,
+                                                 max_context_len=mcl, workspace=ws8))
+        del ws8
         fl = prefill_flops(b)
         items = B * ((L + 127) // 128) * 16
         rows.append({"shape": name, "items": items, "items_per_sm": round(items / sms, 2),
@@ -1030,6 +1040,7 @@ def prefill_shapes(torch, device, only=None, steps=15):
                      "pairs_us": round(t_pairs, 2), "split_us": round(t_split, 2),
                      "pairs_tflops": round(fl / t_pairs / 1e6, 1),
                      "split_tflops": round(fl / t_split / 1e6, 1),
+                     "fp8_pages_us": round(t_fp8, 2), "fp8_pages_tflops": round(fl / t_fp8 / 1e6, 1),
                      "attention_picks": "split" if 2 * items < 3 * sms else "pairs"})
     st, flags = pa.pa_get_device_error()
     if st:
@@ -1056,13 +1067,16 @@ def bench_prefill(pa, binding, torch, device, stream, steps=20):
     pa.pa_append_kv(kn, vn, kp, vp, sm, b.page_size)
     mcl = int(b.context_lens.max())
 
-    def timed(attend):
+    def timed(attend, append=None):
         evs = []
         for k in range(steps + 3):
             flush.zero_()
             e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
             e[0].record(stream)
-            pa.pa_append_kv(kn, vn, kp, vp, sm, b.page_size)
+            if append is None:
+                pa.pa_append_kv(kn, vn, kp, vp, sm, b.page_size)
+            else:
+                append()
             e[1].record(stream)
             attend()
             e[2].record(stream)
@@ -1087,6 +1101,22 @@ def bench_prefill(pa, binding, torch, device, stream, steps=20):
     kernel = "prefill_split_kernel" if 2 * items < 3 * sms else "prefill_pairs_kernel"
     flops = prefill_flops(b)
     _, app_bytes = step_bytes(b)
+    # The same chunk over e4m3 pools (seeded random codes, per-tensor scales):
+    # the quantising append, then pa_prefill_fp8 (bf16 copies of the visible
+    # tokens, then the same tensor-core kernel choice).
+    rng = np.random.default_rng(b.seed + 9)
+    kc = torch.from_numpy(wl.random_e4m3_codes(rng, b.key_pages.shape)).to(device)
+    vc = torch.from_numpy(wl.random_e4m3_codes(rng, b.value_pages.shape)).to(device)
+    ks, vs = 0.05, 0.05
+    shape = pa.make_shape(q.shape, kc.shape, bt.shape[1])
+    ws8 = torch.empty(pa.pa_prefill_fp8_workspace_bytes(shape, mcl), dtype=torch.uint8,
+                      device=device)
+    fp8_ms, fp8_app_ms = timed(
+        lambda: pa.pa_prefill_fp8(q, kc, vc, bt, cl, b.page_size, ks, vs, scale=b.scale,
+                                  causal=True, out=out, max_context_len=mcl, workspace=ws8),
+        append=lambda: pa.pa_append_kv_fp8(kn, vn, kc, vc, sm, b.page_size, ks, vs))
+    visible = int(b.context_lens.astype(np.int64).sum())
+    copy_bytes = visible * b.H_kv * b.D * 2 * 3           # e4m3 read + bf16 write, K and V
     return {"workload": b.name, "tflops": round(flops / (att_ms * 1e-3) / 1e12, 3),
             "attention_ms": round(att_ms, 4), "kernel": kernel, "items": items,
             "split_kernel": {"attention_ms": round(split_ms, 4),
@@ -1094,7 +1124,13 @@ def bench_prefill(pa, binding, torch, device, stream, steps=20):
             "append_ms": round(app_ms, 4),
             "append_gbs": round(app_bytes / (app_ms * 1e-3) / 1e9, 2),
             "causal_useful_flops": flops, "steps": steps,
-            "l2": "2x L2 buffer written before every step (outside the events)"}
+            "l2": "2x L2 buffer written before every step (outside the events)",
+            "fp8_pages": {"call": "pa_prefill_fp8 (e4m3 to bf16 page copy + " + kernel + ")",
+                          "attention_ms": round(fp8_ms, 4),
+                          "tflops": round(flops / (fp8_ms * 1e-3) / 1e12, 3),
+                          "append_ms": round(fp8_app_ms, 4),
+                          "copy_bytes": copy_bytes,
+                          "over_bf16_ms": round(fp8_ms - att_ms, 4)}}
 
 
 if __name__ == "__main__":

@@ -292,75 +292,92 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int box = a.box_rows;
         int stage = 0;
         uint32_t phase = 0;
-        for (int64_t x = x_begin; x < x_end; ++x) {
+        // Per piece (the granules of one segment inside this block's range):
+        // the segment, its context length, page-table row and Q rows, found
+        // once. Per granule only the address translation of its boxes remains,
+        // and the next granule's is issued as soon as this one's copies are
+        // out, so its loads overlap the wait for a free stage.
+        int64_t x = x_begin;
+        while (x < x_end) {
             const SegmentPos sp = locate(pre, a.B, per_req, a.MT, x);
+            const int64_t piece_start = x;
+            const int64_t piece_end =
+                x_end < sp.seg_start + sp.seg_len ? x_end : sp.seg_start + sp.seg_len;
             const int n = clamp_context(a.context_lens[sp.b], cap, a.err);
-            const int t0 = int(x - sp.seg_start) * kDecodeTokens;
-            const int nvalid = min(kDecodeTokens, n - t0);
-            const int nbox = nvalid > 0 ? (nvalid + box - 1) / box : 0;
-            // Address translation for this granule, once per page (box), issued
-            // before the wait for a free stage so its latency overlaps it.
             const int32_t* bt = a.block_table + int64_t(sp.b) * a.max_pages;
-            int row_a = 0, row_b = 0;  // boxes lane and lane + 32
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int j = lane + 32 * k;
-                if (j < nbox) {
-                    const int tok = t0 + j * box;
-                    const int lp = tok / a.ps;
-                    int phys = a.dense ? sp.b : bt[lp];
-                    if (unsigned(phys) >= unsigned(a.num_pages)) {
-                        atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
-                        phys = 0;
-                    }
-                    const int row = (phys * a.H_kv + sp.h) * a.ps + (tok - lp * a.ps);
-                    if (k == 0)
-                        row_a = row;
-                    else
-                        row_b = row;
-                }
-            }
-            // The first granule of a piece also brings the segment's Q tile (the
-            // G heads x L rows of a KV group are consecutive rows of q).
-            const bool first = x == x_begin || x == sp.seg_start;
-            const bool ok = mbar_wait_warp(&empty[stage], phase ^ 1u, misc, a.err);
-            if (ok && (nbox > 0 || first)) {
-                const uint32_t bytes = uint32_t(nbox) * box * 128u * Lay::kKVHalves * 2u +
-                                       (first ? uint32_t(Lay::kHalves * Lay::kQHalfBytes) : 0u);
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-                    if (first) {
-                        const int qrow = (sp.b * a.H_q + sp.h * a.G) * a.L + sp.mt * kDecodeRows;
-#pragma unroll
-                        for (int hf = 0; hf < Lay::kHalves; ++hf)
-                            tma_load_2d(smem + Lay::kQ + (stage * Lay::kHalves + hf) * Lay::kQHalfBytes,
-                                        &q_map, hf * 64, qrow, &full[stage], policy);
-                    }
-                }
-                __syncwarp();
+            // The TMA row of each box of granule xx (boxes lane and lane + 32).
+            auto translate = [&](int64_t xx, int& nbox, int& ra, int& rb) {
+                const int t0 = int(xx - sp.seg_start) * kDecodeTokens;
+                const int nvalid = min(kDecodeTokens, n - t0);
+                nbox = nvalid > 0 ? (nvalid + box - 1) / box : 0;
+                ra = rb = 0;
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int j = lane + 32 * k;
                     if (j < nbox) {
-                        const int row = k == 0 ? row_a : row_b;
-                        const int dst = j * box * 128;
-#pragma unroll
-                        for (int hf = 0; hf < Lay::kKVHalves; ++hf) {
-                            // a box row is 128 bytes: 64 bf16 or 128 e4m3 elements
-                            tma_load_2d(k_half(stage, hf) + dst, &key_map, hf * (F8 ? 128 : 64), row,
-                                        &full[stage], policy);
-                            tma_load_2d(v_half(stage, hf) + dst, &value_map, hf * (F8 ? 128 : 64),
-                                        row, &full[stage], policy);
+                        const int tok = t0 + j * box;
+                        const int lp = tok / a.ps;
+                        int phys = a.dense ? sp.b : bt[lp];
+                        if (unsigned(phys) >= unsigned(a.num_pages)) {
+                            atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
+                            phys = 0;
                         }
+                        const int row = (phys * a.H_kv + sp.h) * a.ps + (tok - lp * a.ps);
+                        if (k == 0)
+                            ra = row;
+                        else
+                            rb = row;
                     }
                 }
-            } else if (ok && lane == 0) {
-                mbar_arrive(&full[stage]);  // empty granule: nothing to load
-            }
-            __syncwarp();
-            if (++stage == kStages) {
-                stage = 0;
-                phase ^= 1u;
+            };
+            int nbox, row_a, row_b;
+            translate(x, nbox, row_a, row_b);
+            for (; x < piece_end; ++x) {
+                // The first granule of a piece also brings the segment's Q tile
+                // (the G heads x L rows of a KV group are consecutive rows of q).
+                const bool first = x == piece_start;
+                const bool ok = mbar_wait_warp(&empty[stage], phase ^ 1u, misc, a.err);
+                if (ok && (nbox > 0 || first)) {
+                    const uint32_t bytes =
+                        uint32_t(nbox) * box * 128u * Lay::kKVHalves * 2u +
+                        (first ? uint32_t(Lay::kHalves * Lay::kQHalfBytes) : 0u);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&full[stage], bytes);
+                        if (first) {
+                            const int qrow = (sp.b * a.H_q + sp.h * a.G) * a.L + sp.mt * kDecodeRows;
+#pragma unroll
+                            for (int hf = 0; hf < Lay::kHalves; ++hf)
+                                tma_load_2d(smem + Lay::kQ + (stage * Lay::kHalves + hf) * Lay::kQHalfBytes,
+                                            &q_map, hf * 64, qrow, &full[stage], policy);
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int j = lane + 32 * k;
+                        if (j < nbox) {
+                            const int row = k == 0 ? row_a : row_b;
+                            const int dst = j * box * 128;
+#pragma unroll
+                            for (int hf = 0; hf < Lay::kKVHalves; ++hf) {
+                                // a box row is 128 bytes: 64 bf16 or 128 e4m3 elements
+                                tma_load_2d(k_half(stage, hf) + dst, &key_map, hf * (F8 ? 128 : 64),
+                                            row, &full[stage], policy);
+                                tma_load_2d(v_half(stage, hf) + dst, &value_map,
+                                            hf * (F8 ? 128 : 64), row, &full[stage], policy);
+                            }
+                        }
+                    }
+                } else if (ok && lane == 0) {
+                    mbar_arrive(&full[stage]);  // empty granule: nothing to load
+                }
+                __syncwarp();
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (x + 1 < piece_end)
+                    translate(x + 1, nbox, row_a, row_b);
             }
         }
         return;

@@ -303,26 +303,67 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int64_t piece_start = x;
             const int64_t piece_end =
                 x_end < sp.seg_start + sp.seg_len ? x_end : sp.seg_start + sp.seg_len;
-            const int n = clamp_context(a.context_lens[sp.b], cap, a.err);
+            const int n = clamp_context(__ldg(a.context_lens + sp.b), cap, a.err);
             const int32_t* bt = a.block_table + int64_t(sp.b) * a.max_pages;
+            // The piece's page ids, 64 at a time: a window of pages [wb, wb + 64)
+            // with page wb + lane in c0 and wb + 32 + lane in c1, and the next
+            // window already on its way (n0, n1), so a granule finds its ids by
+            // shuffle instead of waiting on a load. Pool page and box sizes are
+            // powers of two; a granule's pages never straddle two windows. The
+            // dense layout (request b is page b, of any length) reads no table.
+            const int ps_shift = __ffs(a.ps) - 1;
+            const int box_shift = __ffs(box) - 1;
+            auto load_window = [&](int w, int& e0, int& e1) {
+                e0 = e1 = 0;
+                if (a.dense)
+                    return;
+                if (w + lane < a.max_pages)
+                    e0 = __ldg(bt + w + lane);
+                if (w + 32 + lane < a.max_pages)
+                    e1 = __ldg(bt + w + 32 + lane);
+            };
+            int wb = a.dense ? 0 : (int((x - sp.seg_start) * kDecodeTokens) >> ps_shift) & ~63;
+            int c0, c1, n0, n1;
+            load_window(wb, c0, c1);
+            load_window(wb + 64, n0, n1);
             // The TMA row of each box of granule xx (boxes lane and lane + 32).
             auto translate = [&](int64_t xx, int& nbox, int& ra, int& rb) {
                 const int t0 = int(xx - sp.seg_start) * kDecodeTokens;
                 const int nvalid = min(kDecodeTokens, n - t0);
-                nbox = nvalid > 0 ? (nvalid + box - 1) / box : 0;
                 ra = rb = 0;
+                if (a.dense) {
+                    // one page per request holding the whole context (t < n <= ps)
+                    nbox = nvalid > 0 ? (nvalid + box - 1) / box : 0;
+                    const int base = (sp.b * a.H_kv + sp.h) * a.ps + t0;
+                    if (lane < nbox)
+                        ra = base + lane * box;
+                    if (lane + 32 < nbox)
+                        rb = base + (lane + 32) * box;
+                    return;
+                }
+                nbox = nvalid > 0 ? (nvalid + box - 1) >> box_shift : 0;
+                const int lp0 = t0 >> ps_shift;
+                while (lp0 >= wb + 64) {     // warp-uniform: move to the next window
+                    wb += 64;
+                    c0 = n0;
+                    c1 = n1;
+                    load_window(wb + 64, n0, n1);
+                }
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int j = lane + 32 * k;
+                    const int tok = t0 + (j << box_shift);
+                    const int lp = tok >> ps_shift;
+                    const int idx = (lp - wb) & 63;
+                    const int p0 = __shfl_sync(0xffffffffu, c0, idx & 31);
+                    const int p1 = __shfl_sync(0xffffffffu, c1, idx & 31);
                     if (j < nbox) {
-                        const int tok = t0 + j * box;
-                        const int lp = tok / a.ps;
-                        int phys = a.dense ? sp.b : bt[lp];
+                        int phys = idx < 32 ? p0 : p1;
                         if (unsigned(phys) >= unsigned(a.num_pages)) {
                             atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
                             phys = 0;
                         }
-                        const int row = (phys * a.H_kv + sp.h) * a.ps + (tok - lp * a.ps);
+                        const int row = (phys * a.H_kv + sp.h) * a.ps + (tok - (lp << ps_shift));
                         if (k == 0)
                             ra = row;
                         else

@@ -120,15 +120,19 @@ __device__ __forceinline__ SegmentPos locate(const int32_t* pre, int B, int per_
     return s;
 }
 
-// The split over blocks weighs each segment as its granules plus
-// kPieceUnits: a piece costs a block more than its granules (the first
-// granule's Q tile, the partial tail granule, the epilogue), and a block that
-// gets many short segments would otherwise end last. Unit stream: segment s
-// is kPieceUnits units of overhead, then its granules, so granule x of
-// segment s sits at unit x + kPieceUnits * (s + 1); block i owns the units
-// [floor(i*T/grid), floor((i+1)*T/grid)), T = granules + kPieceUnits * nseg,
-// i.e. the granules whose units fall there.
-constexpr int kPieceUnits = 1;
+// The split over blocks weighs each segment as its granules plus pu units
+// (DecodeArgs::piece_units): a piece costs a block more than its granules (the
+// first granule's Q tile, the partial tail granule, the epilogue; for e4m3
+// pages also the merge of the four warp states), and a block that gets many
+// short segments would otherwise end last. Unit stream: segment s is pu units
+// of overhead, then its granules, so granule x of segment s sits at unit
+// x + pu * (s + 1); block i owns the units [floor(i*T/grid),
+// floor((i+1)*T/grid)), T = granules + pu * nseg, i.e. the granules whose
+// units fall there. The merge pass recomputes the split with the same pu.
+// A piece costs about one granule beyond its own on bf16 pools and about
+// three on e4m3 pools (measured on 128-token pages: 79.9 us with 1, 63.4
+// with 3).
+__host__ __device__ constexpr int piece_units(bool f8) { return f8 ? 3 : 1; }
 
 // Block index that processes the granule at unit position u.
 __device__ __forceinline__ int64_t block_of_unit(int64_t u, int64_t units, int64_t grid)
@@ -140,11 +144,11 @@ __device__ __forceinline__ int64_t block_of_unit(int64_t u, int64_t units, int64
 // pre[b] = first granule of request b; every segment of request b has the
 // same number of granules.
 __device__ __forceinline__ int64_t granule_at_unit(const int32_t* pre, int B, int per_req,
-                                                   int64_t u, int64_t units)
+                                                   int64_t u, int64_t units, int pu)
 {
     if (u >= units)
         return pre[B];
-    auto pre_u = [&](int b) { return int64_t(pre[b]) + int64_t(kPieceUnits) * per_req * b; };
+    auto pre_u = [&](int b) { return int64_t(pre[b]) + int64_t(pu) * per_req * b; };
     int lo = 0, hi = B - 1;
     while (lo < hi) {  // largest b whose first unit is <= u
         const int mid = (lo + hi + 1) >> 1;
@@ -155,8 +159,8 @@ __device__ __forceinline__ int64_t granule_at_unit(const int32_t* pre, int B, in
     }
     const int gb = (pre[lo + 1] - pre[lo]) / per_req;
     const int64_t r = u - pre_u(lo);
-    const int64_t hm = r / (gb + kPieceUnits);
-    const int64_t in = r - hm * (gb + kPieceUnits) - kPieceUnits;
+    const int64_t hm = r / (gb + pu);
+    const int64_t in = r - hm * (gb + pu) - pu;
     return pre[lo] + hm * gb + (in > 0 ? in : 0);
 }
 
@@ -240,8 +244,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncthreads();
 
+    constexpr int kPU = piece_units(F8);
     const int64_t total = pre[a.B];
-    const int64_t units = total + int64_t(kPieceUnits) * a.B * per_req;
+    const int64_t units = total + int64_t(kPU) * a.B * per_req;
     const int64_t cta = blockIdx.x;
     // The unit stream is split over min(gridDim.x, units) blocks so that every
     // block in use owns at least one unit; a segment whose granules span
@@ -268,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         x_begin = seg_first(s0);
         x_end = seg_first(s1);
     } else {
-        x_begin = granule_at_unit(pre, a.B, per_req, cta * units / grid, units);
-        x_end = granule_at_unit(pre, a.B, per_req, (cta + 1) * units / grid, units);
+        x_begin = granule_at_unit(pre, a.B, per_req, cta * units / grid, units, kPU);
+        x_end = granule_at_unit(pre, a.B, per_req, (cta + 1) * units / grid, units, kPU);
     }
     if (x_begin >= x_end)
         return;
@@ -703,8 +708,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
             const bool single =
                 a.whole_segments ||
-                block_of_unit(sp.seg_start + int64_t(kPieceUnits) * (sp.seg + 1), units, grid) ==
-                    block_of_unit(sp.seg_start + sp.seg_len - 1 + int64_t(kPieceUnits) * (sp.seg + 1),
+                block_of_unit(sp.seg_start + int64_t(kPU) * (sp.seg + 1), units, grid) ==
+                    block_of_unit(sp.seg_start + sp.seg_len - 1 + int64_t(kPU) * (sp.seg + 1),
                                   units, grid);
             const bool aborted = misc[0] != 0;
             if (!aborted && single) {
@@ -927,8 +932,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const bool single =
             a.whole_segments ||
-            block_of_unit(sp.seg_start + int64_t(kPieceUnits) * (sp.seg + 1), units, grid) ==
-                block_of_unit(sp.seg_start + sp.seg_len - 1 + int64_t(kPieceUnits) * (sp.seg + 1), units,
+            block_of_unit(sp.seg_start + int64_t(kPU) * (sp.seg + 1), units, grid) ==
+                block_of_unit(sp.seg_start + sp.seg_len - 1 + int64_t(kPU) * (sp.seg + 1), units,
                               grid);
         const bool aborted = misc[0] != 0;
 
@@ -1012,9 +1017,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
     before = red[1][0] + red[1][1] + red[1][2] + red[1][3];
     const int gb = granules(b);
     const int64_t seg_start = before + int64_t(hm) * gb;
-    const int64_t units = total + int64_t(kPieceUnits) * a.B * per_req;
+    const int64_t units = total + int64_t(a.piece_units) * a.B * per_req;
     const int64_t grid = int64_t(decode_grid) < units ? int64_t(decode_grid) : units;
-    const int64_t u0 = seg_start + int64_t(kPieceUnits) * (seg + 1);
+    const int64_t u0 = seg_start + int64_t(a.piece_units) * (seg + 1);
     const int64_t first = block_of_unit(u0, units, grid);
     const int64_t last = block_of_unit(u0 + gb - 1, units, grid);
     if (first == last)
@@ -1145,12 +1150,14 @@ cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_m
                     : cudaLaunchKernelEx(&cfg, decode_kernel<128>, key_map, value_map, q_map, a);
     if (e != cudaSuccess || a.whole_segments)
         return e;
+    DecodeArgs ma = a;
+    ma.piece_units = piece_units(fp8);
     cudaLaunchConfig_t mcfg = cfg;
     mcfg.gridDim = dim3(unsigned(int64_t(a.B) * a.H_kv * a.MT));
     mcfg.blockDim = dim3(128);
     mcfg.dynamicSmemBytes = 0;
-    e = a.D == 64 ? cudaLaunchKernelEx(&mcfg, decode_merge_kernel<64>, a, grid)
-                  : cudaLaunchKernelEx(&mcfg, decode_merge_kernel<128>, a, grid);
+    e = a.D == 64 ? cudaLaunchKernelEx(&mcfg, decode_merge_kernel<64>, ma, grid)
+                  : cudaLaunchKernelEx(&mcfg, decode_merge_kernel<128>, ma, grid);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();

@@ -80,6 +80,8 @@ struct DecodeArgs {
     int32_t box_rows;   // rows per TMA box: min(ps, 64)
     int32_t swz;        // 7: 128B-swizzled stage layout (box_rows >= 8); 0: linear
     int32_t whole_segments;  // 1: every block takes whole segments (no partials)
+    int32_t piece_units;     // split weight of a piece beyond its granules (set by
+                             // the launcher for the merge pass)
     int32_t dense;      // 1: K/V are dense [B, H_kv, ps, D] (request b is page b;
                         // block_table is not read)
     float scale_log2;   // scale * log2(e) (times k_scale for e4m3 pages)

@@ -980,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // arithmetic repeats the decode kernel's partition, on the inputs only; the
 // partial states are read after the decode grid has completed.
 // Thread -> (row tid / 8, columns c0 .. c0 + D/8): M = max m_k,
-// l = sum l_k 2^(m_k - M), o = sum acc_k 2^(m_k - M) / l.
+// l = sum l_k 2^(m_k - M), o = sum acc_k 2^(m_k - M) / l, as one running pass.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int decode_grid)
 {
@@ -1035,23 +1035,15 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
     const int64_t orow = (int64_t(b) * a.H_q + (hm / a.MT) * a.G + g) * a.L + i;
     const float* base = a.partials + (int64_t(seg) + first) * kSlotFloats;
     const int np = int(last - first) + 1;
-    float Mx = -INFINITY;  // pieces' maxima, 8 loads in flight at a time
-    for (int k0 = 0; k0 < np; k0 += 8) {
-        float mk[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-            mk[u] = k0 + u < np ? __ldcg(base + int64_t(k0 + u) * kSlotFloats + r) : -INFINITY;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-            Mx = fmaxf(Mx, mk[u]);
-    }
-    const float Mu = Mx == -INFINITY ? 0.f : Mx;
-    float L2 = 0.f;
+    // One pass over the pieces, four in flight, with a running maximum:
+    // M' = max(M, m_k), l = l 2^(M - M') + l_k 2^(m_k - M'), likewise o
+    // (the pieces in order, so repeated calls give the same bits).
+    float Mx = -INFINITY, L2 = 0.f;
     float fin[D / 8];
 #pragma unroll
     for (int c = 0; c < D / 8; ++c)
         fin[c] = 0.f;
-    for (int k0 = 0; k0 < np; k0 += 4) {  // weighted sums, 4 pieces in flight
+    for (int k0 = 0; k0 < np; k0 += 4) {
         float mk[4], lk[4];
         float4 v[4][D / 32];
 #pragma unroll
@@ -1067,14 +1059,19 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const float w = fast_exp2(mk[u] - Mu);  // 0 for absent pieces
-            L2 += w * lk[u];
+            if (mk[u] == -INFINITY)
+                continue;  // absent piece, or no visible key in it
+            const float Mn = fmaxf(Mx, mk[u]);
+            const float co = Mx == -INFINITY ? 0.f : fast_exp2(Mx - Mn);
+            const float cn = fast_exp2(mk[u] - Mn);
+            Mx = Mn;
+            L2 = L2 * co + lk[u] * cn;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                fin[4 * c] += w * v[u][c].x;
-                fin[4 * c + 1] += w * v[u][c].y;
-                fin[4 * c + 2] += w * v[u][c].z;
-                fin[4 * c + 3] += w * v[u][c].w;
+                fin[4 * c] = fin[4 * c] * co + cn * v[u][c].x;
+                fin[4 * c + 1] = fin[4 * c + 1] * co + cn * v[u][c].y;
+                fin[4 * c + 2] = fin[4 * c + 2] * co + cn * v[u][c].z;
+                fin[4 * c + 3] = fin[4 * c + 3] * co + cn * v[u][c].w;
             }
         }
     }

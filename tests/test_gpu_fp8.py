@@ -246,3 +246,38 @@ def test_prefill_fp8_rejects_bad_arguments():
         pa.pa_prefill_fp8(*args, 0.0, 0.05, max_context_len=40)
     assert e.value.status == pa.PA_ERR_INVALID_ARG
     check_no_device_error()
+
+
+def test_prefill_fp8_chunk512_sampled_rows():
+    """The bench's prefill workload (4 requests, 512-row chunks after ragged
+    prefixes, H_q = 32, H_kv = 8) over e4m3 pools: the quantising append of
+    the chunk's K/V, then pa_prefill_fp8 as the bench calls it; sampled rows
+    against the oracle run on the oracle's own append."""
+    pa = _pa()
+    b = wl.make_workload("prefill_chunk512")
+    rng = np.random.default_rng(b.seed + 9)
+    kc = wl.random_e4m3_codes(rng, b.key_pages.shape)
+    vc = wl.random_e4m3_codes(rng, b.value_pages.shape)
+    ks, vs = 0.05, 0.05
+    kp_d, vp_d = _u8(kc), _u8(vc)
+    pa.pa_append_kv_fp8(dev(b.key_new), dev(b.value_new), kp_d, vp_d, dev(b.slot_mapping),
+                        b.page_size, ks, vs)
+    out = pa.pa_prefill_fp8(dev(b.query), kp_d, vp_d, dev(b.block_table), dev(b.context_lens),
+                            b.page_size, ks, vs, scale=b.scale, causal=True,
+                            max_context_len=int(b.context_lens.max()))
+    check_no_device_error()
+    kp, vp = kc.copy(), vc.copy()
+    oracle.append_kv_fp8(b.key_new, b.value_new, kp, vp, b.slot_mapping, b.page_size, ks, vs)
+    assert np.array_equal(kp_d.cpu().numpy(), kp) and np.array_equal(vp_d.cpu().numpy(), vp)
+    rows = []
+    for r in range(b.B):
+        for i in sorted(set([0, 1, 63, 64, 127, 128, 255, 256, 383, 510, 511] +
+                            list(rng.integers(0, b.L, 5)))):
+            for h in range(0, b.H_q, 3):
+                rows.append((r, h, i))
+    rows = np.asarray(rows, dtype=np.int32)
+    ref = oracle.attention_fp8(b.query, kp, vp, ks, vs, b.block_table, b.context_lens,
+                               b.page_size, scale=b.scale, causal=True, rows=rows,
+                               n_threads=N_THREADS)
+    got = host_f64(out)[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(got, ref, "fp8 prefill_chunk512 sampled")

@@ -182,4 +182,90 @@ int pa_bench_e2e_steps(int n_steps, int n_copies, const void* const* host_src,
     return cudaEventElapsedTime(total_ms, pool.ev[0], pool.ev[1]) == cudaSuccess ? 0 : -1;
 }
 
+// The end-to-end step with its copies overlapped with the kernels of the
+// neighbouring steps, as a serving loop runs it. Step k's inputs (one packed
+// pinned region, `in_bytes`) are copied on copy_stream into device region
+// k % 2 while step k - 1 computes on `stream`. Step k's output (device buffer
+// k % 2) comes back on out_stream while step k + 1 computes (a stream of its
+// own, so that the next input copy does not queue behind it). Every step still
+// moves its own inputs and its own output inside the timed region. The
+// inputs sit at byte offsets off[0..5] (query, new K, new V, slot_mapping,
+// block_table, context_lens) of each device region.
+int pa_bench_e2e_pipelined(int n_steps, int n_copies, const void* host_in,
+                           void* const* dev_in, size_t in_bytes, const size_t* off,
+                           void* const* dev_out, void* const* host_out, size_t out_bytes,
+                           void* const* key_pages, void* const* value_pages, int32_t page_size,
+                           pa_shape append_shape, float scale, int causal, pa_shape shape,
+                           int32_t max_context_len, void* workspace, size_t workspace_bytes,
+                           void* stream, void* copy_stream, void* out_stream,
+                           float* total_ms)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
+    cudaStream_t os = static_cast<cudaStream_t>(out_stream);
+    EventPool timing(2);
+    std::vector<cudaEvent_t> sync(6, nullptr);   // in_ready[2], done[2], out_free[2]
+    struct Destroy {
+        std::vector<cudaEvent_t>& e;
+        ~Destroy()
+        {
+            for (auto x : e)
+                if (x)
+                    cudaEventDestroy(x);
+        }
+    } destroy{sync};
+    if (!timing.ok())
+        return -1;
+    for (auto& e : sync)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+            return -1;
+    cudaEvent_t* in_ready = &sync[0];
+    cudaEvent_t* done = &sync[2];
+    cudaEvent_t* out_free = &sync[4];
+    if (cudaEventRecord(timing.ev[0], s) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, timing.ev[0], 0) != cudaSuccess ||
+        cudaStreamWaitEvent(os, timing.ev[0], 0) != cudaSuccess)
+        return -1;
+    for (int k = 0; k < n_steps; ++k) {
+        const int r = k & 1, c = k % n_copies;
+        uint8_t* base = static_cast<uint8_t*>(dev_in[r]);
+        // inputs: region r is free once step k - 2 has run
+        if (k >= 2 && cudaStreamWaitEvent(cs, done[r], 0) != cudaSuccess)
+            return -1;
+        if (cudaMemcpyAsync(base, host_in, in_bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+            cudaEventRecord(in_ready[r], cs) != cudaSuccess)
+            return -1;
+        // the step, once its inputs are in and output buffer r has been read back
+        if (cudaStreamWaitEvent(s, in_ready[r], 0) != cudaSuccess)
+            return -1;
+        if (k >= 2 && cudaStreamWaitEvent(s, out_free[r], 0) != cudaSuccess)
+            return -1;
+        pa_status st = pa_append_kv(base + off[1], base + off[2], key_pages[c], value_pages[c],
+                                    reinterpret_cast<const int32_t*>(base + off[3]), page_size,
+                                    append_shape, stream);
+        if (st != PA_OK)
+            return int(st);
+        st = pa_attention(base + off[0], key_pages[c], value_pages[c],
+                          reinterpret_cast<const int32_t*>(base + off[4]),
+                          reinterpret_cast<const int32_t*>(base + off[5]), page_size, scale,
+                          causal, dev_out[r], shape, max_context_len, workspace, workspace_bytes,
+                          stream);
+        if (st != PA_OK)
+            return int(st);
+        if (cudaEventRecord(done[r], s) != cudaSuccess)
+            return -1;
+        // output of step k back to the host
+        if (cudaStreamWaitEvent(os, done[r], 0) != cudaSuccess ||
+            cudaMemcpyAsync(host_out[r], dev_out[r], out_bytes, cudaMemcpyDeviceToHost, os) !=
+                cudaSuccess ||
+            cudaEventRecord(out_free[r], os) != cudaSuccess)
+            return -1;
+    }
+    if (cudaEventRecord(timing.ev[1], os) != cudaSuccess ||
+        cudaEventSynchronize(timing.ev[1]) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaStreamSynchronize(cs) != cudaSuccess)
+        return -1;
+    return cudaEventElapsedTime(total_ms, timing.ev[0], timing.ev[1]) == cudaSuccess ? 0 : -1;
+}
+
 }  // extern "C"

@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap key_map,
                    const __grid_constant__ CUtensorMap value_map, const PrefillArgs a)
 {
+    grid_dependency_wait();  // the previous kernel's outputs are visible from here on
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -454,8 +455,21 @@ cudaError_t launch_prefill(const CUtensorMap& q_map, const CUtensorMap& key_map,
         smem_set[device].store(smem, std::memory_order_relaxed);
     }
     const int64_t grid = int64_t(a.B) * a.H_q * a.n_qtiles;
-    prefill_kernel<<<unsigned(grid), kThreads, smem, stream>>>(q_map, key_map, value_map, a);
-    return cudaGetLastError();
+    // Programmatic stream serialization: the blocks may be scheduled while the
+    // previous kernel in the stream finishes; each waits for it
+    // (griddepcontrol.wait) before reading anything.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel, q_map, key_map, value_map, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace pa

@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap key_map,
                          const __grid_constant__ CUtensorMap value_map, const PrefillArgs a)
 {
+    grid_dependency_wait();  // the previous kernel's outputs are visible from here on
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -611,8 +612,21 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
         smem_set[device].store(smem, std::memory_order_relaxed);
     }
     const int64_t grid = int64_t(a.B) * (a.H_q / 2) * a.n_qtiles;
-    prefill_pairs_kernel<<<unsigned(grid), kThreads, smem, stream>>>(q_map, key_map, value_map, a);
-    return cudaGetLastError();
+    // Programmatic stream serialization: the blocks may be scheduled while the
+    // previous kernel in the stream finishes; each waits for it
+    // (griddepcontrol.wait) before reading anything.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_pairs_kernel, q_map, key_map, value_map, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace pa

@@ -284,6 +284,20 @@ pa_status pa_prefill_fp8(const void *query, const void *key_pages, const void *v
                          size_t workspace_bytes, void *stream);
 
 /*
+ * The dispatch of pa_attention for e4m3 pools: pa_decode_fp8 where
+ * pa_attention_route gives 0 (query rows <= 8), pa_prefill_fp8 otherwise,
+ * with the same arguments. The workspace is the one that call takes, at
+ * least pa_attention_fp8_workspace_bytes(shape, max_context_len) bytes,
+ * 256-byte aligned (0 bytes: invalid shape or head_dim other than 128).
+ */
+size_t pa_attention_fp8_workspace_bytes(pa_shape shape, int32_t max_context_len);
+pa_status pa_attention_fp8(const void *query, const void *key_pages, const void *value_pages,
+                           const int32_t *block_table, const int32_t *context_lens,
+                           int32_t page_size, float scale, float k_scale, float v_scale,
+                           int causal, void *out, pa_shape shape, int32_t max_context_len,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace pa_prefill_split needs for `shape` and
  * page_size on the CURRENT device, or 0 when the shape takes a prefill
  * kernel that needs none (head_dim 64, page_size < 8, an odd group size

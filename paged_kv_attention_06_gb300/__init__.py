@@ -13,7 +13,7 @@ _API = ("pa_append_kv", "pa_decode", "pa_prefill", "pa_attention", "pa_attention
         "pa_gather_kv", "pa_decode_dense", "KVCache", "KVCacheSnapshot",
         "pa_prefill_split", "pa_prefill_workspace_bytes", "prefill_workspace",
         "pa_append_kv_fp8", "pa_decode_fp8", "pa_prefill_fp8",
-        "pa_prefill_fp8_workspace_bytes")
+        "pa_prefill_fp8_workspace_bytes", "pa_attention_fp8")
 
 
 def __getattr__(name):

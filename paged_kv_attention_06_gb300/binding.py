@@ -76,6 +76,10 @@ def _load() -> ctypes.CDLL:
     lib.pa_prefill_fp8.argtypes = [vp, vp, vp, vp, vp, i32, f32, f32, f32, ctypes.c_int, vp,
                                    pa_shape, i32, vp, sz, vp]
     lib.pa_prefill_fp8.restype = ctypes.c_int
+    lib.pa_attention_fp8_workspace_bytes.argtypes = [pa_shape, i32]
+    lib.pa_attention_fp8_workspace_bytes.restype = sz
+    lib.pa_attention_fp8.argtypes = lib.pa_prefill_fp8.argtypes
+    lib.pa_attention_fp8.restype = ctypes.c_int
     lib.pa_prefill_split.argtypes = attn + [vp, sz, vp]
     lib.pa_prefill_split.restype = ctypes.c_int
     i64 = ctypes.c_int64
@@ -332,6 +336,43 @@ def pa_prefill_fp8(query, key_pages, value_pages, block_table, context_lens, pag
                              int(max_context_len), workspace.data_ptr(),
                              workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "pa_prefill_fp8")
+    return out
+
+
+def pa_attention_fp8(query, key_pages, value_pages, block_table, context_lens, page_size: int,
+                     k_scale: float, v_scale: float, scale: Optional[float] = None,
+                     causal: bool = True, out=None, max_context_len: Optional[int] = None,
+                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The dispatch for e4m3 pools: pa_decode_fp8 for up to 8 query rows,
+    pa_prefill_fp8 beyond (pa_attention_route's rule)."""
+    B, H_q, L, D = query.shape
+    if key_pages.shape[2] != page_size or value_pages.shape != key_pages.shape:
+        raise ValueError("page pool shape does not match page_size")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_table must be [B, max_pages] and context_lens [B]")
+    if out is None:
+        out = torch.empty_like(query)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item())
+    shape = make_shape(query.shape, key_pages.shape, block_table.shape[1])
+    if workspace is None:
+        with torch.cuda.device(query.device):
+            need = int(_lib.pa_attention_fp8_workspace_bytes(shape, int(max_context_len)))
+        if need == 0:
+            raise PagedAttentionError(PA_ERR_UNSUPPORTED, "pa_attention_fp8")
+        workspace = _cached_workspace(need, query.device)
+    st = _lib.pa_attention_fp8(_dev_ptr(query, torch.bfloat16, "query"),
+                               _dev_ptr(key_pages, torch.uint8, "key_pages"),
+                               _dev_ptr(value_pages, torch.uint8, "value_pages"),
+                               _dev_ptr(block_table, torch.int32, "block_table"),
+                               _dev_ptr(context_lens, torch.int32, "context_lens"),
+                               int(page_size), float(scale), float(k_scale), float(v_scale),
+                               int(bool(causal)), _dev_ptr(out, torch.bfloat16, "out"), shape,
+                               int(max_context_len), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "pa_attention_fp8")
     return out
 
 

@@ -600,6 +600,33 @@ pa_status pa_prefill_fp8(const void* query, const void* key_pages, const void* v
                           p.split_bytes ? w + p.split_off : nullptr, p.split_bytes, v_scale);
 }
 
+size_t pa_attention_fp8_workspace_bytes(pa_shape shape, int32_t max_context_len)
+{
+    const int32_t route = pa_attention_route(shape, max_context_len);
+    if (route < 0 || shape.head_dim != 128)
+        return 0;
+    return route == 0 ? pa_decode_workspace_bytes(shape)
+                      : pa_prefill_fp8_workspace_bytes(shape, max_context_len);
+}
+
+pa_status pa_attention_fp8(const void* query, const void* key_pages, const void* value_pages,
+                           const int32_t* block_table, const int32_t* context_lens,
+                           int32_t page_size, float scale, float k_scale, float v_scale,
+                           int causal, void* out, pa_shape shape, int32_t max_context_len,
+                           void* workspace, size_t workspace_bytes, void* stream)
+{
+    const int32_t route = pa_attention_route(shape, max_context_len);
+    if (route < 0)
+        return PA_ERR_INVALID_ARG;
+    if (route == 0)
+        return pa_decode_fp8(query, key_pages, value_pages, block_table, context_lens, page_size,
+                             scale, k_scale, v_scale, causal, out, shape, max_context_len,
+                             workspace, workspace_bytes, stream);
+    return pa_prefill_fp8(query, key_pages, value_pages, block_table, context_lens, page_size,
+                          scale, k_scale, v_scale, causal, out, shape, max_context_len, workspace,
+                          workspace_bytes, stream);
+}
+
 pa_status pa_append_kv_fp8(const void* key, const void* value, void* key_pages,
                            void* value_pages, const int32_t* slot_mapping, int32_t page_size,
                            float k_scale, float v_scale, pa_shape shape, void* stream)

@@ -281,3 +281,22 @@ def test_prefill_fp8_chunk512_sampled_rows():
                                n_threads=N_THREADS)
     got = host_f64(out)[rows[:, 0], rows[:, 1], rows[:, 2]]
     assert_close(got, ref, "fp8 prefill_chunk512 sampled")
+
+
+@pytest.mark.parametrize("L", [1, 8, 9, 200])
+def test_attention_fp8_dispatch_is_the_routed_call(L):
+    """pa_attention_fp8 gives the bits of pa_decode_fp8 for up to 8 query rows
+    and of pa_prefill_fp8 beyond, and both match the oracle."""
+    pa = _pa()
+    b, kc, vc = _fp8_batch("fp8route", 3, 8, 2, 16, L, [L + 40, 700, 2 * L + 3], seed=70 + L)
+    args = (dev(b.query), _u8(kc), _u8(vc), dev(b.block_table), dev(b.context_lens), b.page_size,
+            0.05, 0.05)
+    mcl = int(b.context_lens.max())
+    got = pa.pa_attention_fp8(*args, scale=b.scale, max_context_len=mcl)
+    routed = (pa.pa_decode_fp8 if L <= 8 else pa.pa_prefill_fp8)(*args, scale=b.scale,
+                                                                 max_context_len=mcl)
+    check_no_device_error()
+    assert torch.equal(got.view(torch.int16), routed.view(torch.int16))
+    ref = oracle.attention_fp8(b.query, kc, vc, 0.05, 0.05, b.block_table, b.context_lens,
+                               b.page_size, scale=b.scale, causal=True, n_threads=N_THREADS)
+    assert_close(host_f64(got), ref, f"pa_attention_fp8 L={L}")

@@ -415,12 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ts = trow + col_s(head);
         const uint32_t to = trow + col_o(head);
         const int i = row0 + r;
-        const bool valid = r < rows;
         const int lim = a.causal ? min(n - a.L + i, n - 1) : n - 1;  // last visible key
         float m_used = -INFINITY;
         float l = 0.f;
         const float c = a.scale_log2;
-        uint16_t* orow = a.out + ((int64_t(b) * a.H_q + hq0 + head) * a.L + i) * 128;
 
         for (int j = 0; j < nt; ++j) {
             mbar_wait_warp(&bar[kSFull + head], j & 1, misc, a.err);
@@ -540,28 +538,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_warp(&bar[kPVDone + head], (nt - 1) & 1, misc, a.err);
             tc_fence_after();
         }
+        // Output rows go through a 4 KiB staging buffer per warp, 16-byte
+        // chunks swizzled by row, so that a warp stores four whole 128-byte row
+        // segments per instruction instead of 32 scattered 16-byte pieces. The
+        // buffer is the head's Q tile: the wait above covers every MMA issued
+        // before the last P V, the last read of Q among them (with no visible
+        // key nothing was loaded into it).
+        uint8_t* stage = smem + Layout::kQ + head * Layout::kMat + w4 * 4096;
+        uint16_t* out_warp =
+            a.out + ((int64_t(b) * a.H_q + hq0 + head) * a.L + row0 + w4 * 32) * 128;
+        int rows_ok = rows - w4 * 32;
+        rows_ok = rows_ok > 32 ? 32 : rows_ok;
+        if (misc[0] != 0)
+            rows_ok = 0;                          // a wait gave up: write nothing
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t ov[32];
-            if (nt > 0) {
-                tmem_ld32(to + 32u * q4, ov);
-                tmem_wait_ld();
-            } else {
+        for (int hf = 0; hf < 2; ++hf) {
+            uint32_t pk[32];                      // columns 64 hf .. 64 hf + 63 of this row
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    ov[k] = 0u;
-            }
-            if (valid && misc[0] == 0) {
+            for (int q = 0; q < 2; ++q) {
+                uint32_t ov[32];
+                if (nt > 0) {
+                    tmem_ld32(to + 32u * (2 * hf + q), ov);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                for (int k = 0; k < 32; k += 8) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(ov[k]) * inv, __uint_as_float(ov[k + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(ov[k + 2]) * inv, __uint_as_float(ov[k + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(ov[k + 4]) * inv, __uint_as_float(ov[k + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(ov[k + 6]) * inv, __uint_as_float(ov[k + 7]) * inv);
-                    *reinterpret_cast<uint4*>(orow + 32 * q4 + k) = w;
+                    for (int k = 0; k < 32; ++k)
+                        ov[k] = 0u;
                 }
+#pragma unroll
+                for (int k = 0; k < 32; k += 2)
+                    pk[16 * q + k / 2] =
+                        pack_bf16x2(__uint_as_float(ov[k]) * inv, __uint_as_float(ov[k + 1]) * inv);
             }
+#pragma unroll
+            for (int cq = 0; cq < 8; ++cq)
+                *reinterpret_cast<uint4*>(stage + lane * 128 + ((cq ^ (lane & 7)) << 4)) =
+                    make_uint4(pk[4 * cq], pk[4 * cq + 1], pk[4 * cq + 2], pk[4 * cq + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int idx = j * 32 + lane;
+                const int rw = idx >> 3, cq = idx & 7;
+                const uint4 v = *reinterpret_cast<const uint4*>(stage + rw * 128 + ((cq ^ (rw & 7)) << 4));
+                if (rw < rows_ok)
+                    *reinterpret_cast<uint4*>(out_warp + int64_t(rw) * 128 + hf * 64 + cq * 8) = v;
+            }
+            __syncwarp();
         }
         tc_fence_before();
     }

@@ -113,8 +113,15 @@ def load_peaks():
 
 
 def source_digest(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Digest of a source file's code: comments and white space removed, so a
+    comment edit keeps a capture valid and any code change invalidates it."""
+    import re
+    with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = " ".join(text.split())
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
 
 
 def committed_traffic(kernel_key, workload):

@@ -15,10 +15,13 @@
 //     segments form one stream that the grid splits into equal contiguous
 //     ranges (split-KV across blocks: the cached context is spread over the
 //     whole GPU however ragged the lengths are).
-//   * Per block: one producer warp resolves each page id once per page
-//     (address translation hoisted per TMA box, issued before it waits for a
-//     free stage) and issues TMA tile loads of whole page slices into a
-//     3-stage shared-memory ring (128B swizzle). Four consumer warps split the
+//   * Per block: one producer warp finds each piece's segment, context
+//     length and page-table row once, reads the row 64 page ids at a time into
+//     registers (one window ahead), resolves each page id once per page by
+//     shuffle (address translation hoisted per TMA box and issued behind the
+//     previous granule's copies), and issues TMA tile loads of whole page
+//     slices into a 3-stage shared-memory ring (128B swizzle; four half-size
+//     stages for e4m3 pages). Four consumer warps split the
 //     head dimension: each computes S = Q K^T for all 64 tokens of a granule
 //     (the same values in every warp, so the softmax state needs no exchange)
 //     and O += P V for its quarter of the output columns, on the tensor cores

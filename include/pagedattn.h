@@ -450,10 +450,13 @@ void pa_debug_arm_wait_timeout(void);
 /*
  * Test and tuning support: which tensor-core prefill kernel the calling host
  * thread's pa_prefill / pa_attention calls use (head_dim 128, page_size >= 8).
- *   0  automatic (the default): as 2;
+ *   0  automatic (the default): as 2, except that a group size that is odd
+ *      with fewer (request, head pair, query tile) items than SMs takes 1;
  *   1  one query head per block;
- *   2  two query heads of one KV group per block, when the group size
- *      (num_q_heads / num_kv_heads) is even; otherwise as 1.
+ *   2  two query heads of one KV group per block when the group size
+ *      (num_q_heads / num_kv_heads) is at least 2; with an odd group size
+ *      the last pair of each group computes its last head twice and writes
+ *      it once. A group of 1 takes 1.
  * Settings 1 and 2 also hold for pa_prefill_split and for pa_attention given
  * a prefill workspace (the workspace is then not used). Any other value is
  * taken as 0. Returns the previous setting. Results agree

@@ -106,6 +106,9 @@ __device__ __forceinline__ uint64_t mnmajor_base(uint32_t saddr)
     return smem_desc_sw128(saddr, uint32_t(Layout::kHalf), 1024u);
 }
 
+// kOdd: the group size is odd and the last pair of each group repeats its
+// last head (a separate instantiation, so that even groups keep their code).
+template <bool kOdd>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pairs_kernel(const __grid_constant__ CUtensorMap q_map,
                          const __grid_constant__ CUtensorMap key_map,
@@ -127,7 +130,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // order for the block scheduler), then the head pairs of each. Every block
     // ranks all pairs itself (one thread per pair) when there are at most
     // kThreads of them; beyond that, query tiles are taken last to first.
-    const int pairs = a.H_q / 2;
+    // Head pairs: ceil(G / 2) per KV group; with an odd group size the last
+    // pair of each group holds its last head twice (computed by both softmax
+    // warpgroups, written by the first only).
+    const int per_group = kOdd ? (a.G + 1) / 2 : a.G / 2;
+    const int pairs = a.H_kv * per_group;
     const int cap = a.max_pages * a.ps;
     const int rank = int(blockIdx.x / pairs);
     const int hp = int(blockIdx.x % pairs);
@@ -166,8 +173,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         t = a.n_qtiles - 1 - rank / a.B;
         b = rank - (rank / a.B) * a.B;
     }
-    const int hq0 = 2 * hp;                      // heads hq0, hq0 + 1 (same KV group)
-    const int hk = hq0 / a.G;
+    int hk, hq0;
+    if constexpr (kOdd) {
+        hk = hp / per_group;                     // KV group
+        hq0 = hk * a.G + 2 * (hp - hk * per_group);
+    } else {
+        hq0 = 2 * hp;
+        hk = hq0 / a.G;
+    }
+    const bool dup = kOdd && hq0 + 1 == (hk + 1) * a.G;  // odd group: one head, twice
+    const int hq1 = dup ? hq0 : hq0 + 1;         // heads hq0, hq1 (same KV group)
     int n = a.context_lens[b];
     if (n < 0 || n > cap) {
         if (threadIdx.x == 0)
@@ -231,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prefetch_tensormap(&value_map);
                 mbar_arrive_expect_tx(&bar[kQFull], 2u * Layout::kMat);
                 for (int h = 0; h < 2; ++h) {
-                    const int qrow = (b * a.H_q + hq0 + h) * a.L + row0;
+                    const int qrow = (b * a.H_q + (h == 0 ? hq0 : hq1)) * a.L + row0;
                     uint8_t* d = smem + Layout::kQ + h * Layout::kMat;
                     tma_load_2d(d, &q_map, 0, qrow, &bar[kQFull], policy);
                     tma_load_2d(d + Layout::kHalf, &q_map, 64, qrow, &bar[kQFull], policy);
@@ -546,11 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // key nothing was loaded into it).
         uint8_t* stage = smem + Layout::kQ + head * Layout::kMat + w4 * 4096;
         uint16_t* out_warp =
-            a.out + ((int64_t(b) * a.H_q + hq0 + head) * a.L + row0 + w4 * 32) * 128;
+            a.out + ((int64_t(b) * a.H_q + (head == 0 ? hq0 : hq1)) * a.L + row0 + w4 * 32) * 128;
         int rows_ok = rows - w4 * 32;
         rows_ok = rows_ok > 32 ? 32 : rows_ok;
-        if (misc[0] != 0)
-            rows_ok = 0;                          // a wait gave up: write nothing
+        if (misc[0] != 0 || (head == 1 && dup))
+            rows_ok = 0;                          // a wait gave up, or the duplicate head
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             uint32_t pk[32];                      // columns 64 hf .. 64 hf + 63 of this row
@@ -604,36 +619,38 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
                                  cudaStream_t stream)
 {
     constexpr int kMaxDev = 64;
-    static std::atomic<int> smem_set[kMaxDev];
+    static std::atomic<int> smem_set[kMaxDev][2];
     if (device < 0 || device >= kMaxDev)
         return cudaErrorInvalidDevice;
+    const bool odd = a.G % 2 != 0;
+    const void* fn = odd ? reinterpret_cast<const void*>(prefill_pairs_kernel<true>)
+                         : reinterpret_cast<const void*>(prefill_pairs_kernel<false>);
     const int smem = Layout::kBytes;
     // The register split needs 128 x kRegsProducer + 256 x kRegsSoftmax
     // registers out of the launch's own 384 x numRegs, a launch count no
     // higher than kRegsSoftmax (the increase must be one) and no lower than
     // kRegsProducer; otherwise the increase would wait forever.
-    static std::atomic<int> regs_ok[kMaxDev];
-    int rk = regs_ok[device].load(std::memory_order_relaxed);
+    static std::atomic<int> regs_ok[kMaxDev][2];
+    int rk = regs_ok[device][odd].load(std::memory_order_relaxed);
     if (rk == 0) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_pairs_kernel);
+        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
         if (e != cudaSuccess)
             return e;
         const bool fits = fa.numRegs >= kRegsProducer && fa.numRegs <= kRegsSoftmax &&
                           128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * fa.numRegs;
         rk = fits ? 1 : 2;
-        regs_ok[device].store(rk, std::memory_order_relaxed);
+        regs_ok[device][odd].store(rk, std::memory_order_relaxed);
     }
     if (rk != 1)
         return cudaErrorNotSupported;
-    if (smem_set[device].load(std::memory_order_relaxed) < smem) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_pairs_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (smem_set[device][odd].load(std::memory_order_relaxed) < smem) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        smem_set[device].store(smem, std::memory_order_relaxed);
+        smem_set[device][odd].store(smem, std::memory_order_relaxed);
     }
-    const int64_t grid = int64_t(a.B) * (a.H_q / 2) * a.n_qtiles;
+    const int64_t grid = int64_t(a.B) * a.H_kv * ((a.G + 1) / 2) * a.n_qtiles;
     // Programmatic stream serialization: the blocks may be scheduled while the
     // previous kernel in the stream finishes; each waits for it
     // (griddepcontrol.wait) before reading anything.
@@ -647,7 +664,9 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_pairs_kernel, q_map, key_map, value_map, a);
+    const cudaError_t e =
+        odd ? cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<true>, q_map, key_map, value_map, a)
+            : cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<false>, q_map, key_map, value_map, a);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -176,8 +176,8 @@ def test_prefill_fp8_matches_oracle(ps, L, causal):
     assert_close(got, ref, f"fp8 prefill ps={ps} L={L} causal={causal}")
 
 
-@pytest.mark.parametrize("H_q,H_kv", [(6, 2), (4, 4)])   # group of 3 / 1: one head per block
-def test_prefill_fp8_one_head_kernel(H_q, H_kv):
+@pytest.mark.parametrize("H_q,H_kv", [(6, 2), (4, 4)])   # group of 3 (pairs, last head repeated) / 1 (one head)
+def test_prefill_fp8_odd_groups(H_q, H_kv):
     b, kc, vc = _fp8_batch("fp8pre1", 3, H_q, H_kv, 16, 100, [100, 333, 1000], seed=61)
     got, ref = _run_prefill(b, kc, vc, 0.02, 0.09)
     check_no_device_error()

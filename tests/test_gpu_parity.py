@@ -301,6 +301,20 @@ def test_tc_prefill_page_sizes(ps, causal, H_q, H_kv, prefill_variant):
     assert_close(host_f64(out), oracle_out(b, kp, vp), f"tc prefill ps={ps} causal={causal}")
 
 
+@pytest.mark.parametrize("H_q,H_kv", [(28, 4), (10, 2)])   # groups of 7 / 5
+def test_tc_prefill_odd_groups(H_q, H_kv, prefill_variant):
+    """Odd group sizes: the head-pairs kernel runs each group's last head in a
+    pair of its own (computed twice, written once); every head of every group
+    against the oracle, over several query tiles."""
+    lens = [300, 1000, 260]
+    b = wl.build_batch("tcodd", B=3, H_q=H_q, H_kv=H_kv, D=128, page_size=16, L=260,
+                       context_lens=lens, seed=H_q, causal=True, placement="churn")
+    out = gpu_step(DeviceBatch(b), route=prefill_variant)
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), f"tc prefill G={H_q // H_kv}")
+
+
 @pytest.mark.parametrize("H_q,H_kv", [(4, 4), (4, 2)])   # group of 1 / 2
 def test_tc_prefill_rows_without_keys_and_empty_context(H_q, H_kv, prefill_variant):
     # L = 200 rows after contexts of 0, 50 and 199 tokens: rows at negative

@@ -300,9 +300,9 @@ pa_status pa_attention_fp8(const void *query, const void *key_pages, const void 
 /*
  * Bytes of device workspace pa_prefill_split needs for `shape` and
  * page_size on the CURRENT device, or 0 when the shape takes a prefill
- * kernel that needs none (head_dim 64, page_size < 8, an odd group size
- * num_q_heads / num_kv_heads). The size depends only on the device's SM
- * count (about 130 KiB per SM), not on the batch.
+ * kernel that needs none (head_dim 64, page_size < 8, one query head per
+ * KV group). The size depends only on the device's SM count (about 130 KiB
+ * per SM), not on the batch.
  */
 size_t pa_prefill_workspace_bytes(pa_shape shape, int32_t page_size);
 
@@ -310,7 +310,9 @@ size_t pa_prefill_workspace_bytes(pa_shape shape, int32_t page_size);
  * Prefill attention with the same arguments, result and checks as
  * pa_prefill, on a kernel that balances the work over the GPU: the K/V
  * tiles of every (request, pair of query heads of one KV group, tile of 128
- * query rows) form one stream, cut into equal ranges for a persistent grid
+ * query rows; with an odd group size the last pair of each group holds its
+ * last head twice and writes it once) form one stream, cut into equal
+ * ranges for a persistent grid
  * of one block per SM (the split-KV idea of Week 3 Day 4, "Choose a
  * Schedule for Each Query Shape", applied to the long-query schedule). An
  * item cut by range boundaries is finished by the block holding its first

@@ -220,11 +220,20 @@ pa_status encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uin
 
 // Workspace the split prefill kernel needs for this shape on this device, or
 // 0 when the shape takes another prefill kernel (head_dim 64, pages of fewer
-// than 8 tokens, an odd group size, or shared memory too small).
+// than 8 tokens, one query head per KV group, or shared memory too small).
+// (request, pair of query heads of one KV group, 128-row query tile) items of a
+// prefill: ceil(G / 2) pairs per group (an odd group's last pair repeats its
+// last head).
+int64_t prefill_pair_items(const pa_shape& s)
+{
+    const int g = s.num_kv_heads > 0 ? s.num_q_heads / s.num_kv_heads : 0;
+    return int64_t(s.batch) * ((int64_t(s.q_len) + 127) / 128) * s.num_kv_heads * ((g + 1) / 2);
+}
+
 size_t split_prefill_need(const pa_shape& s, int32_t page_size, const DeviceInfo* dev)
 {
     if (s.head_dim != 128 || page_size < 8 || s.num_kv_heads <= 0 ||
-        s.num_q_heads % s.num_kv_heads != 0 || (s.num_q_heads / s.num_kv_heads) % 2 != 0)
+        s.num_q_heads % s.num_kv_heads != 0 || s.num_q_heads / s.num_kv_heads < 2)
         return 0;
     if (prefill_split_smem_bytes() > size_t(dev->max_smem_optin))
         return 0;
@@ -256,8 +265,7 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     // (group of 7, one 512-row chunk after a 16k prefix: 209.6 against 219.8
     // us; with 256 pair items the pairs kernel is 22-33 % faster).
     const int g = s.num_q_heads / s.num_kv_heads;
-    const int64_t pair_items =
-        int64_t(s.batch) * ((int64_t(s.q_len) + 127) / 128) * s.num_kv_heads * ((g + 1) / 2);
+    const int64_t pair_items = prefill_pair_items(s);
     bool pairs = t_prefill_variant != 1 && g >= 2 &&
                  (g % 2 == 0 || t_prefill_variant == 2 || pair_items >= dev->sm_count);
     if (pairs && prefill_pairs_smem_bytes() > size_t(dev->max_smem_optin))
@@ -539,7 +547,7 @@ pa_status plan_prefill_fp8(const pa_shape& s, int32_t max_context_len, DeviceInf
     p->split_off = (p->table_off + table_bytes + 255) & ~size_t(255);
     // the kernel choice of pa_attention's prefill route (split below 1.5
     // items per SM)
-    const int64_t items = int64_t(s.batch) * ((int64_t(s.q_len) + 127) / 128) * (s.num_q_heads / 2);
+    const int64_t items = prefill_pair_items(s);
     p->split_bytes = 2 * items < 3 * int64_t(dev->sm_count) ? split_prefill_need(p->copy, 128, dev) : 0;
     p->total = p->split_off + p->split_bytes;
     return PA_OK;
@@ -874,8 +882,7 @@ pa_status pa_attention(const void* query, const void* key_pages, const void* val
         if (st != PA_OK)
             return st;
         const size_t need = split_prefill_need(shape, page_size, dev);
-        const int64_t items = int64_t(shape.batch) * ((int64_t(shape.q_len) + 127) / 128) *
-                              (shape.num_q_heads / 2);
+        const int64_t items = prefill_pair_items(shape);
         if (need > 0 && workspace_bytes >= need && 2 * items < 3 * int64_t(dev->sm_count) &&
             (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0)
             return pa_prefill_split(query, key_pages, value_pages, block_table, context_lens,

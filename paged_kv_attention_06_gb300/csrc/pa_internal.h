@@ -154,7 +154,7 @@ struct SplitPrefillArgs {
     unsigned long long* flags;    // [grid][head 2][4 warps]: stamp when written
     uint64_t stamp;               // this launch's stamp (never 0)
     int32_t B, H_q, H_kv, L, ps, max_pages, num_pages;
-    int32_t G;          // H_q / H_kv (even)
+    int32_t G;          // H_q / H_kv (>= 2; odd: the last pair repeats its head)
     int32_t n_qtiles;   // ceil(L / 128)
     int32_t box_rows;   // rows per K/V TMA box: min(ps, 128)
     float scale_log2;

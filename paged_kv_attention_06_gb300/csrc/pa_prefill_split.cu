@@ -260,6 +260,10 @@ __device__ __forceinline__ int block_of_unit(int64_t x, int64_t U, int64_t G)
     return int(((x + 1) * G - 1) / U);
 }
 
+// kOdd: the group size is odd; the last head pair of each group holds its
+// last head twice (computed by both softmax warpgroups, written by the
+// first only), a separate instantiation so that even groups keep their code.
+template <bool kOdd>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_split_kernel(const __grid_constant__ CUtensorMap q_map,
                          const __grid_constant__ CUtensorMap key_map,
@@ -278,7 +282,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ Cursor warp_cursor[8];             // softmax warps: next item
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int pairs = a.H_q / 2;
+    const int per_group = kOdd ? (a.G + 1) / 2 : a.G / 2;   // head pairs per KV group
+    const int pairs = a.H_kv * per_group;
+    // Query head h (0, 1) of head pair hp, and whether hp repeats its head.
+    auto head_of = [&](int hp, int h) -> int {
+        if constexpr (kOdd) {
+            const int hk = hp / per_group;
+            const int hq0 = hk * a.G + 2 * (hp - hk * per_group);
+            return h == 1 && hq0 + 1 == (hk + 1) * a.G ? hq0 : hq0 + h;
+        } else {
+            return 2 * hp + h;
+        }
+    };
+    auto repeats = [&](int hp) -> bool {
+        if constexpr (kOdd)
+            return head_of(hp, 1) == head_of(hp, 0);
+        else
+            return false;
+    };
     const int64_t G = gridDim.x;
     const int c = int(blockIdx.x);
 
@@ -407,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (pc.next(a, pairs, s, e, pp)) {
                     if (pp.k1 > pp.k0) {
                         for (int h = 0; h < 2; ++h) {
-                            const int qrow = (pp.b * a.H_q + 2 * pp.hp + h) * a.L + pp.t * kRows;
+                            const int qrow = (pp.b * a.H_q + head_of(pp.hp, h)) * a.L + pp.t * kRows;
                             tma_prefetch_l2_2d(&q_map, 0, qrow);
                             tma_prefetch_l2_2d(&q_map, 64, qrow);
                         }
@@ -431,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool ok = mbar_wait_warp(&bar[kQEmpty + h], (qp & 1) ^ 1u, misc, a.err);
                 if (ok && lane == 0) {
                     mbar_arrive_expect_tx(&bar[kQFull + h], uint32_t(Layout::kMat));
-                    const int qrow = (d.b * a.H_q + 2 * d.hp + h) * a.L + d.t * kRows;
+                    const int qrow = (d.b * a.H_q + head_of(d.hp, h)) * a.L + d.t * kRows;
                     uint8_t* dst = smem + Layout::kQ + h * Layout::kMat;
                     tma_load_2d(dst, &q_map, 0, qrow, &bar[kQFull + h], policy);
                     tma_load_2d(dst + Layout::kHalf, &q_map, 64, qrow, &bar[kQFull + h], policy);
@@ -472,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 phys = 0;
                             }
                             const int tok = d.k * kKeys + my_box * box;
-                            const int hk = (2 * d.hp) / a.G;
+                            const int hk = d.hp / per_group;
                             const int row = (phys * a.H_kv + hk) * a.ps + (tok - (tok / a.ps) * a.ps);
                             uint8_t* dst = smem + (is_v ? Layout::kV : Layout::kK) + st * Layout::kMat +
                                            my_box * box * 128;
@@ -803,10 +824,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_warp(&bar[kPVDone + head], (g - 1) & 1, misc, a.err);
                 tc_fence_after();
             }
-            const int hq = 2 * vp->hp + head;
+            const int hq = head_of(vp->hp, head);
             const int wrow0 = vp->t * kRows + w4 * 32;            // this warp's first row
             uint16_t* out_warp = a.out + ((int64_t(vp->b) * a.H_q + hq) * a.L + wrow0) * 128;
-            const int rows_ok = misc[0] == 0 ? min(32, a.L - wrow0) : 0;
+            const int rows_ok =
+                misc[0] == 0 && !(head == 1 && repeats(vp->hp)) ? min(32, a.L - wrow0) : 0;
             const int64_t s = vr[0], e = vr[1], U = vr[2];
             const int64_t p_us = vp->us;
             const int p_nt = vp->nt;
@@ -1017,30 +1039,32 @@ cudaError_t launch_prefill_split(const CUtensorMap& q_map, const CUtensorMap& ke
                                  void* workspace, int device, cudaStream_t stream)
 {
     constexpr int kMaxDev = 64;
-    static std::atomic<int> smem_set[kMaxDev];
-    static std::atomic<int> regs_ok[kMaxDev];
+    static std::atomic<int> smem_set[kMaxDev][2];
+    static std::atomic<int> regs_ok[kMaxDev][2];
     if (device < 0 || device >= kMaxDev)
         return cudaErrorInvalidDevice;
-    int rk = regs_ok[device].load(std::memory_order_relaxed);
+    const bool odd = a.G % 2 != 0;
+    const void* fn = odd ? reinterpret_cast<const void*>(prefill_split_kernel<true>)
+                         : reinterpret_cast<const void*>(prefill_split_kernel<false>);
+    int rk = regs_ok[device][odd].load(std::memory_order_relaxed);
     if (rk == 0) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_split_kernel);
+        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
         if (e != cudaSuccess)
             return e;
         const bool fits = fa.numRegs >= kRegsProducer && fa.numRegs <= kRegsSoftmax &&
                           128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * fa.numRegs;
         rk = fits ? 1 : 2;
-        regs_ok[device].store(rk, std::memory_order_relaxed);
+        regs_ok[device][odd].store(rk, std::memory_order_relaxed);
     }
     if (rk != 1)
         return cudaErrorNotSupported;
     const int smem = Layout::kBytes;
-    if (smem_set[device].load(std::memory_order_relaxed) < smem) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_split_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (smem_set[device][odd].load(std::memory_order_relaxed) < smem) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        smem_set[device].store(smem, std::memory_order_relaxed);
+        smem_set[device][odd].store(smem, std::memory_order_relaxed);
     }
     const uint64_t st = next_launch_stamp();
     uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -1063,7 +1087,8 @@ cudaError_t launch_prefill_split(const CUtensorMap& q_map, const CUtensorMap& ke
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_split_kernel, q_map, key_map, value_map, a);
+    return odd ? cudaLaunchKernelEx(&cfg, prefill_split_kernel<true>, q_map, key_map, value_map, a)
+               : cudaLaunchKernelEx(&cfg, prefill_split_kernel<false>, q_map, key_map, value_map, a);
 }
 
 }  // namespace pa

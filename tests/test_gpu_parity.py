@@ -395,6 +395,23 @@ def test_split_prefill_items_cut_into_many_pieces(causal):
     assert_close(got, oracle_out(b, kp, vp, rows=rows), f"split many pieces causal={causal}")
 
 
+@pytest.mark.parametrize("H_q,H_kv", [(14, 2), (6, 2)])   # groups of 7 / 3
+def test_split_prefill_odd_groups_cut_into_pieces(H_q, H_kv):
+    """Odd group sizes on the split kernel: each group's last pair repeats its
+    last head, the items are cut into many pieces, and every query head (the
+    repeated last ones included) matches the oracle."""
+    b = wl.build_batch("splitodd", B=1, H_q=H_q, H_kv=H_kv, D=128, page_size=16, L=256,
+                       context_lens=[6000], seed=H_q, causal=True, placement="permutation")
+    out = gpu_step(DeviceBatch(b), route="prefill_split")
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    rng = np.random.default_rng(3)
+    rows = np.asarray([(0, h, int(i)) for h in range(b.H_q)
+                       for i in [0, 127, 128, 255] + list(rng.integers(0, b.L, 4))], dtype=np.int32)
+    got = host_f64(out)[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(got, oracle_out(b, kp, vp, rows=rows), f"split odd group G={H_q // H_kv}")
+
+
 def test_split_prefill_fewer_units_than_blocks():
     # 3 short requests: far fewer K/V tiles than blocks (most blocks get an
     # empty range and leave at once); every row compared.

@@ -250,6 +250,93 @@ class OracleSampler:
                 return done_bytes / el / 1e9, n_groups, el
 
 
+def cpu_model() -> str:
+    """The host CPU's model name: /proc/cpuinfo's "model name" (x86), else
+    lscpu's "Model name" (Arm hosts such as Grace), else the Arm implementer
+    and part codes of /proc/cpuinfo."""
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
+    except OSError:
+        pass
+    if fields.get("model name"):
+        return fields["model name"]
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    if "cpu implementer" in fields:
+        return f"implementer {fields['cpu implementer']} part {fields.get('cpu part', '?')}"
+    return "unknown"
+
+
+def decode_cpu_baseline(b: wl.PagedBatch, budget_s: float):
+    """The oracle on bounded samples of the decode workload, single-threaded
+    and on every host core (rates in GB/s of K/V read)."""
+    cores = os.cpu_count() or 1
+    sampler = OracleSampler(b, 1)
+    r1, g1, t1 = sampler.run(0.35 * budget_s, chunk=1)
+    sampler.n_threads = cores
+    ra, ga, ta = sampler.run(0.65 * budget_s)
+    return {"value": round(ra, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{b.name}: whole (request, KV head) groups (all {b.H_q // b.H_kv} query "
+                      f"heads each) in batch order; {ga} groups in {ta:.1f} s on {cores} "
+                      f"threads, {g1} groups in {t1:.1f} s on 1 thread; GB/s of K/V read",
+            "threads_1": {"value": round(r1, 4), "groups": g1, "seconds": round(t1, 2)},
+            "threads_all": {"value": round(ra, 4), "threads": cores, "groups": ga,
+                            "seconds": round(ta, 2)},
+            "cpu_model": cpu_model()}
+
+
+def prefill_cpu_baseline(b: wl.PagedBatch, budget_s: float, tile: int = 128):
+    """The oracle on sampled query tiles of the prefill chunk (after its
+    append), single-threaded and on every host core. A unit is one (request,
+    query head, 128-row query tile); units are drawn in a seeded random
+    order. Rate: causal-useful GFLOP/s (4 * D per visible (row, key) pair)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    kp, vp = b.key_pages.copy(), b.value_pages.copy()
+    oracle.append_kv(b.key_new, b.value_new, kp, vp, b.slot_mapping, b.page_size)
+    n_tiles = -(-b.L // tile)
+    units = [(r, h, t) for r in range(b.B) for h in range(b.H_q) for t in range(n_tiles)]
+    order = np.random.default_rng(b.seed + 11).permutation(len(units))
+
+    def run(threads, budget, k0):
+        flops, done, k, t_start = 0.0, 0, k0, time.perf_counter()
+        while True:
+            r, h, t = units[int(order[k % len(units)])]
+            k += 1
+            rows = np.asarray([(r, h, i) for i in range(t * tile, min(b.L, (t + 1) * tile))],
+                              dtype=np.int32)
+            oracle.attention(b.query, kp, vp, b.block_table, b.context_lens, b.page_size,
+                             scale=b.scale, causal=b.causal, rows=rows, n_threads=threads)
+            n = int(b.context_lens[r])
+            vis = [min(n, n - b.L + i + 1) if b.causal else n for i in rows[:, 2]]
+            flops += 4.0 * b.D * sum(max(0, v) for v in vis)
+            done += 1
+            el = time.perf_counter() - t_start
+            if el >= budget:
+                return flops / el / 1e9, done, el, k
+
+    g1, u1, t1, k = run(1, 0.35 * budget_s, 0)
+    ga, ua, ta, _ = run(cores, 0.65 * budget_s, k)
+    return {"value": round(ga, 4), "unit": "GFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{b.name}: (request, query head, {tile}-row query tile) units in a "
+                      f"seeded random order; {ua} units in {ta:.1f} s on {cores} threads, "
+                      f"{u1} in {t1:.1f} s on 1 thread; causal-useful GFLOP/s",
+            "threads_1": {"value": round(g1, 4), "units": u1, "seconds": round(t1, 2)},
+            "threads_all": {"value": round(ga, 4), "threads": cores, "units": ua,
+                            "seconds": round(ta, 2)},
+            "cpu_model": cpu_model()}
+
+
 def run_reference(args, rank, world):
     """The reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
     if rank != 0:
@@ -280,7 +367,7 @@ def run_reference(args, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(b, world, "none (CPU)"),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -318,7 +405,37 @@ def _bench_lib(binding):
                                        ctypes.POINTER(ctypes.c_float),
                                        ctypes.POINTER(ctypes.c_float)]
     lib.pa_bench_steps_fp8.restype = ctypes.c_int
+    lib.pa_bench_attention_calls.argtypes = [ctypes.c_int, ctypes.c_int, pvp, pvp, vp, vp, vp, i32,
+                                             f32, ctypes.c_int, ctypes.c_int, f32, f32, vp,
+                                             binding.pa_shape, i32, vp, sz, vp,
+                                             ctypes.POINTER(ctypes.c_float)]
+    lib.pa_bench_attention_calls.restype = ctypes.c_int
     return lib
+
+
+CALL_WARMUP, CALL_BLOCK, CALL_BLOCKS = 5, 60, 4
+
+
+def time_calls(blib, n_copies, kps, vps, q, bt, cl, page_size, scale, causal, out, shape,
+               max_ctx, ws, ws_bytes, stream, fp8=False, k_scale=1.0, v_scale=1.0):
+    """Device time of one attention call: CALL_WARMUP untimed calls, then
+    CALL_BLOCKS blocks of CALL_BLOCK back-to-back calls, each block bracketed
+    by CUDA events (none between calls). Returns (median over blocks of the
+    per-call ms, the blocks' per-call ms)."""
+    import ctypes
+
+    def block(n):
+        total = ctypes.c_float(0)
+        st = blib.pa_bench_attention_calls(n, n_copies, kps, vps, q, bt, cl, page_size, scale,
+                                           int(causal), int(fp8), k_scale, v_scale, out, shape,
+                                           max_ctx, ws, ws_bytes, stream, ctypes.byref(total))
+        if st != 0:
+            raise RuntimeError(f"native call loop failed with status {st}")
+        return float(total.value) / n
+
+    block(CALL_WARMUP)
+    per = [block(CALL_BLOCK) for _ in range(CALL_BLOCKS)]
+    return float(np.median(per)), per
 
 
 def workload_config(b, world, l2_note):
@@ -433,20 +550,27 @@ def main(argv=None):
     kps = (ctypes.c_void_p * copies)(*[kp.data_ptr() for kp, _ in pools])
     vps = (ctypes.c_void_p * copies)(*[vp_.data_ptr() for _, vp_ in pools])
 
-    sample_every = 4
-
     def run_steps(n):
-        n_samples = -(-n // sample_every)
-        step_ms = (ctypes.c_float * max(1, n_samples))()
+        """n steps with no event between them; returns their device ms."""
         total = ctypes.c_float(0)
-        st = blib.pa_bench_steps(n, sample_every, copies, kn.data_ptr(), vn.data_ptr(), kps, vps,
+        st = blib.pa_bench_steps(n, 0, copies, kn.data_ptr(), vn.data_ptr(), kps, vps,
                                  sm.data_ptr(), b.page_size, app_shape, q.data_ptr(),
                                  bt.data_ptr(), cl.data_ptr(), b.scale, int(b.causal),
                                  out.data_ptr(), shape, max_ctx, ws.data_ptr(), ws_need, sp,
-                                 step_ms, ctypes.byref(total))
+                                 None, ctypes.byref(total))
         if st != 0:
             raise RuntimeError(f"native step loop failed with status {st}")
-        return float(total.value), [float(x) for x in step_ms[:n_samples]]
+        return float(total.value)
+
+    # The K timed steps run as up to four blocks, each bracketed by events
+    # (none inside a block); the step time is their sum over K, and the blocks'
+    # own per-step times give the repeat spread.
+    n_blocks = 4 if args.steps >= 8 else 1
+    block_sizes = [args.steps // n_blocks + (1 if i < args.steps % n_blocks else 0)
+                   for i in range(n_blocks)]
+
+    def run_blocks():
+        return [run_steps(n) for n in block_sizes]
 
     run_steps(args.warmup)
     torch.cuda.synchronize()
@@ -459,10 +583,18 @@ def main(argv=None):
     time.sleep(0.3)
     wall0 = time.time()
     host0 = time.perf_counter()
-    total_ms, dec_ms = timed_region(dist, torch.cuda.synchronize,
-                                    lambda: run_steps(args.steps))
+    block_ms = timed_region(dist, torch.cuda.synchronize, run_blocks)
     host_s = time.perf_counter() - host0
     wall1 = time.time()
+    total_ms = max_over_ranks(dist, sum(block_ms), device)
+    block_step_ms = [t / n for t, n in zip(block_ms, block_sizes)]
+
+    # One decode call alone: blocks of back-to-back calls over the rotating
+    # pool copies, events only around each block.
+    call_ms, call_blocks = time_calls(blib, copies, kps, vps, q.data_ptr(), bt.data_ptr(),
+                                      cl.data_ptr(), b.page_size, b.scale, b.causal,
+                                      out.data_ptr(), shape, max_ctx, ws.data_ptr(), ws_need, sp)
+    call_ms = max_over_ranks(dist, call_ms, device)
     status, flags = pa.pa_get_device_error()
     if status:
         raise RuntimeError(f"device error in the timed region: {flags:#x}")
@@ -551,7 +683,7 @@ def main(argv=None):
     # ---- secondary: chunked prefill TFLOP/s (prefill route) -----------------
     prefill = None
     if not args.no_prefill and world == 1:
-        prefill = bench_prefill(pa, binding, torch, device, stream)
+        prefill = bench_prefill(pa, binding, torch, device, stream, cpu_budget=0.75 * args.cpu_budget)
 
     clocks.stop()
     ck = clocks.summary(wall0, wall1)
@@ -561,19 +693,13 @@ def main(argv=None):
         return 0
 
     ms_step = total_ms / args.steps
-    dec_avg_ms = float(np.mean(dec_ms))
     value = whole_job_gbs(world, dec_bytes + app_bytes, ms_step)
     hbm_peak, bf16_peak, peak_kind = load_peaks()
-    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
+    achieved = dec_bytes / (call_ms * 1e-3) / 1e9
     traffic = committed_traffic("decode_kernel", b.name)
     cpu = None
     if world == 1 or rank == 0:
-        cores = os.cpu_count() or 1
-        rate, groups, secs = OracleSampler(b, cores).run(args.cpu_budget)
-        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": f"{args.workload}: {groups} whole (request, KV head) groups "
-                         f"(all {b.H_q // b.H_kv} query heads each), {secs:.1f} s on "
-                         f"{cores} threads; GB/s of K/V read"}
+        cpu = decode_cpu_baseline(b, args.cpu_budget)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
@@ -584,8 +710,18 @@ def main(argv=None):
                       f"({copies * pool_bytes / 1e6:.0f} MB vs {l2 / 1e6:.0f} MB L2): each "
                       f"step reads a copy last touched {copies - 1} steps earlier"),
         "tokens_per_s": round(world * b.B / (ms_step * 1e-3), 1),
-        "decode_call_us": round(1e3 * dec_avg_ms, 3),
-        "decode_call_timing": f"CUDA events around pa_attention on every {sample_every}th timed step",
+        "step_blocks_ms_per_step": [round(t, 6) for t in block_step_ms],
+        "step_median_of_blocks_ms": round(float(np.median(block_step_ms)), 6),
+        "step_spread": round((max(block_step_ms) - min(block_step_ms)) /
+                             float(np.median(block_step_ms)), 4),
+        "decode_call_us": round(1e3 * call_ms, 3),
+        "decode_call_blocks_us": [round(1e3 * t, 3) for t in call_blocks],
+        "decode_call_spread": round((max(call_blocks) - min(call_blocks)) / float(np.median(
+            call_blocks)), 4),
+        "decode_call_timing": (f"{CALL_WARMUP} warm-up calls, then {CALL_BLOCKS} blocks of "
+                               f"{CALL_BLOCK} back-to-back pa_attention calls over the rotating "
+                               f"pool copies, CUDA events around each block only; median of "
+                               f"the blocks' per-call times"),
         "route": "decode" if route == 0 else "prefill",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
@@ -655,30 +791,30 @@ def bench_decode_fp8(name, pa, binding, torch, device, stream, steps, warmup=10,
     blib = _bench_lib(binding)
     kps = (ctypes.c_void_p * copies)(*[kp.data_ptr() for kp, _ in pools])
     vps = (ctypes.c_void_p * copies)(*[vp_.data_ptr() for _, vp_ in pools])
-    sample_every = 4
-
     def run(n):
-        step_ms = (ctypes.c_float * max(1, -(-n // sample_every)))()
         total = ctypes.c_float(0)
-        st = blib.pa_bench_steps_fp8(n, sample_every, copies, kn.data_ptr(), vn.data_ptr(), kps,
+        st = blib.pa_bench_steps_fp8(n, 0, copies, kn.data_ptr(), vn.data_ptr(), kps,
                                      vps, sm.data_ptr(), b.page_size, app_shape, q.data_ptr(),
                                      bt.data_ptr(), cl.data_ptr(), b.scale, k_scale, v_scale,
                                      int(b.causal), out.data_ptr(), shape,
                                      int(b.context_lens.max()), ws.data_ptr(), ws_need,
-                                     stream.cuda_stream, step_ms, ctypes.byref(total))
+                                     stream.cuda_stream, None, ctypes.byref(total))
         if st != 0:
             raise RuntimeError(f"native fp8 step loop failed with status {st} on {name}")
-        return float(total.value), [float(x) for x in step_ms[:-(-n // sample_every)]]
+        return float(total.value)
 
     run(warmup)
     torch.cuda.synchronize()
-    total_ms, dec_ms = run(steps)
+    total_ms = run(steps)
+    dec_avg, _ = time_calls(blib, copies, kps, vps, q.data_ptr(), bt.data_ptr(), cl.data_ptr(),
+                            b.page_size, b.scale, b.causal, out.data_ptr(), shape,
+                            int(b.context_lens.max()), ws.data_ptr(), ws_need,
+                            stream.cuda_stream, fp8=True, k_scale=k_scale, v_scale=v_scale)
     torch.cuda.synchronize()
     st, flags = pa.pa_get_device_error()
     if st:
         raise RuntimeError(f"device error in fp8 decode bench {name}: {flags:#x}")
     hbm_peak, _, peak_kind = load_peaks()
-    dec_avg = float(np.mean(dec_ms))
     ms_step = total_ms / steps
     res = {"workload": name, "pages": "e4m3, per-tensor scales", "ms_per_step": round(ms_step, 6),
            "tokens_per_s": round(b.B * b.L / (ms_step * 1e-3), 1),
@@ -719,29 +855,29 @@ def bench_decode_config(name, pa, binding, torch, device, stream, steps, warmup=
     blib = _bench_lib(binding)
     kps = (ctypes.c_void_p * copies)(*[kp.data_ptr() for kp, _ in pools])
     vps = (ctypes.c_void_p * copies)(*[vp_.data_ptr() for _, vp_ in pools])
-    sample_every = 4
-
     def run(n):
-        step_ms = (ctypes.c_float * max(1, -(-n // sample_every)))()
         total = ctypes.c_float(0)
-        st = blib.pa_bench_steps(n, sample_every, copies, kn.data_ptr(), vn.data_ptr(), kps, vps,
+        st = blib.pa_bench_steps(n, 0, copies, kn.data_ptr(), vn.data_ptr(), kps, vps,
                                  sm.data_ptr(), b.page_size, app_shape, q.data_ptr(),
                                  bt.data_ptr(), cl.data_ptr(), b.scale, int(b.causal),
                                  out.data_ptr(), shape, int(b.context_lens.max()), ws.data_ptr(),
-                                 ws_need, stream.cuda_stream, step_ms, ctypes.byref(total))
+                                 ws_need, stream.cuda_stream, None, ctypes.byref(total))
         if st != 0:
             raise RuntimeError(f"native step loop failed with status {st} on {name}")
-        return float(total.value), [float(x) for x in step_ms[:-(-n // sample_every)]]
+        return float(total.value)
 
     run(warmup)
     torch.cuda.synchronize()
-    total_ms, dec_ms = run(steps)
+    total_ms = run(steps)
+    dec_avg, _ = time_calls(blib, copies, kps, vps, q.data_ptr(), bt.data_ptr(), cl.data_ptr(),
+                            b.page_size, b.scale, b.causal, out.data_ptr(), shape,
+                            int(b.context_lens.max()), ws.data_ptr(), ws_need,
+                            stream.cuda_stream)
     torch.cuda.synchronize()
     st, flags = pa.pa_get_device_error()
     if st:
         raise RuntimeError(f"device error in decode bench {name}: {flags:#x}")
     hbm_peak, _, peak_kind = load_peaks()
-    dec_avg = float(np.mean(dec_ms))
     ms_step = total_ms / steps
     res = {"workload": name, "ms_per_step": round(ms_step, 6),
            "step_gbs": round((dec_bytes + app_bytes) / (ms_step * 1e-3) / 1e9, 2),
@@ -1100,7 +1236,7 @@ def prefill_shapes(torch, device, only=None, steps=15):
     return rows
 
 
-def bench_prefill(pa, binding, torch, device, stream, steps=20):
+def bench_prefill(pa, binding, torch, device, stream, steps=20, cpu_budget=6.0):
     """Chunked causal prefill (512 new rows after a ragged prefix): append of
     the 512 rows, then pa_attention (prefill route), timed with events."""
     b = wl.make_workload("prefill_chunk512")
@@ -1169,7 +1305,9 @@ def bench_prefill(pa, binding, torch, device, stream, steps=20):
         append=lambda: pa.pa_append_kv_fp8(kn, vn, kc, vc, sm, b.page_size, ks, vs))
     visible = int(b.context_lens.astype(np.int64).sum())
     copy_bytes = visible * b.H_kv * b.D * 2 * 3           # e4m3 read + bf16 write, K and V
+    cpu = prefill_cpu_baseline(b, cpu_budget) if cpu_budget > 0 else None
     return {"workload": b.name, "tflops": round(flops / (att_ms * 1e-3) / 1e12, 3),
+            "cpu_baseline": cpu,
             "attention_ms": round(att_ms, 4), "kernel": kernel, "items": items,
             "split_kernel": {"attention_ms": round(split_ms, 4),
                              "tflops": round(flops / (split_ms * 1e-3) / 1e12, 3)},

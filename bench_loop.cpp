@@ -3,11 +3,11 @@
 // between launches inside a timed region. Not part of the library.
 //
 // One step = pa_append_kv (new K/V rows by slot_mapping) + pa_attention on
-// page-pool copy k % n_copies. CUDA events bracket the whole loop, and the
-// attention call (its kernels' device time) of every `sample_every`-th step:
-// an event between two kernels stops the second from being scheduled early
-// (programmatic dependent launch), so the other steps run without one, as
-// a serving loop would.
+// page-pool copy k % n_copies. CUDA events bracket the whole loop, and
+// optionally the attention call of every `sample_every`-th step: an event
+// between two kernels stops the second from being scheduled early
+// (programmatic dependent launch), so the benchmark takes the time of one
+// call from blocks of back-to-back calls instead (pa_bench_attention_calls).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -46,8 +46,8 @@ extern "C" {
 
 // Returns 0 on success, a pa_status (> 0) if a call failed, -1 on a CUDA
 // error. step_ms[j]: device time of the attention call of step
-// j * sample_every; *total_ms: the whole loop (first append to last
-// attention).
+// j * sample_every (no such events when sample_every < 1); *total_ms: the
+// whole loop (first append to last attention).
 int pa_bench_steps(int n_steps, int sample_every, int n_copies, const void* key_new, const void* value_new,
                    void* const* key_pages, void* const* value_pages,
                    const int32_t* slot_mapping, int32_t page_size, pa_shape append_shape,
@@ -57,9 +57,8 @@ int pa_bench_steps(int n_steps, int sample_every, int n_copies, const void* key_
                    float* total_ms)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (sample_every < 1)
-        sample_every = 1;
-    const int n_samples = (n_steps + sample_every - 1) / sample_every;
+    // sample_every < 1: no event inside the loop
+    const int n_samples = sample_every < 1 ? 0 : (n_steps + sample_every - 1) / sample_every;
     EventPool pool(2 * size_t(n_samples) + 2);
     if (!pool.ok())
         return -1;
@@ -68,8 +67,8 @@ int pa_bench_steps(int n_steps, int sample_every, int n_copies, const void* key_
         return -1;
     for (int k = 0; k < n_steps; ++k) {
         const int c = k % n_copies;
-        const bool sampled = k % sample_every == 0;
-        const int j = k / sample_every;
+        const bool sampled = n_samples > 0 && k % sample_every == 0;
+        const int j = n_samples > 0 ? k / sample_every : 0;
         pa_status st = pa_append_kv(key_new, value_new, key_pages[c], value_pages[c],
                                     slot_mapping, page_size, append_shape, stream);
         if (st != PA_OK)
@@ -103,9 +102,7 @@ int pa_bench_steps_fp8(int n_steps, int sample_every, int n_copies, const void* 
                        size_t workspace_bytes, void* stream, float* step_ms, float* total_ms)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (sample_every < 1)
-        sample_every = 1;
-    const int n_samples = (n_steps + sample_every - 1) / sample_every;
+    const int n_samples = sample_every < 1 ? 0 : (n_steps + sample_every - 1) / sample_every;
     EventPool pool(2 * size_t(n_samples) + 2);
     if (!pool.ok())
         return -1;
@@ -114,8 +111,8 @@ int pa_bench_steps_fp8(int n_steps, int sample_every, int n_copies, const void* 
         return -1;
     for (int k = 0; k < n_steps; ++k) {
         const int c = k % n_copies;
-        const bool sampled = k % sample_every == 0;
-        const int j = k / sample_every;
+        const bool sampled = n_samples > 0 && k % sample_every == 0;
+        const int j = n_samples > 0 ? k / sample_every : 0;
         pa_status st = pa_append_kv_fp8(key_new, value_new, key_pages[c], value_pages[c],
                                         slot_mapping, page_size, k_scale, v_scale, append_shape,
                                         stream);
@@ -266,6 +263,44 @@ int pa_bench_e2e_pipelined(int n_steps, int n_copies, const void* host_in,
         cudaStreamSynchronize(cs) != cudaSuccess)
         return -1;
     return cudaEventElapsedTime(total_ms, timing.ev[0], timing.ev[1]) == cudaSuccess ? 0 : -1;
+}
+
+// Back-to-back attention calls with no other work and no event between them:
+// call k reads page-pool copy k % n_copies. Events bracket the whole loop,
+// so *total_ms / n_calls is the device time of one call as a stream of
+// calls runs it (each call's kernels may be scheduled while the one before
+// drains). fp8 != 0: pa_decode_fp8 over e4m3 pools with k_scale / v_scale;
+// otherwise pa_attention.
+int pa_bench_attention_calls(int n_calls, int n_copies, void* const* key_pages,
+                             void* const* value_pages, const void* query,
+                             const int32_t* block_table, const int32_t* context_lens,
+                             int32_t page_size, float scale, int causal, int fp8, float k_scale,
+                             float v_scale, void* out, pa_shape shape, int32_t max_context_len,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             float* total_ms)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    EventPool pool(2);
+    if (!pool.ok())
+        return -1;
+    if (cudaEventRecord(pool.ev[0], s) != cudaSuccess)
+        return -1;
+    for (int k = 0; k < n_calls; ++k) {
+        const int c = k % n_copies;
+        const pa_status st =
+            fp8 ? pa_decode_fp8(query, key_pages[c], value_pages[c], block_table, context_lens,
+                                page_size, scale, k_scale, v_scale, causal, out, shape,
+                                max_context_len, workspace, workspace_bytes, stream)
+                : pa_attention(query, key_pages[c], value_pages[c], block_table, context_lens,
+                               page_size, scale, causal, out, shape, max_context_len, workspace,
+                               workspace_bytes, stream);
+        if (st != PA_OK)
+            return int(st);
+    }
+    if (cudaEventRecord(pool.ev[1], s) != cudaSuccess ||
+        cudaEventSynchronize(pool.ev[1]) != cudaSuccess)
+        return -1;
+    return cudaEventElapsedTime(total_ms, pool.ev[0], pool.ev[1]) == cudaSuccess ? 0 : -1;
 }
 
 }  // extern "C"

@@ -151,6 +151,11 @@ pa_status pa_decode(const void *query, const void *key_pages,
  *     call's contents (the decode needs nothing in it to start at zero).
  *     Calls that overlap on the GPU (other streams, other host threads) race
  *     on the array: order them.
+ *   - The array's device address is cached per device for the life of the
+ *     process. cudaDeviceReset (or any reset of the device's primary
+ *     context) ends the context it was looked up in, and with it the cached
+ *     address (and that of the library's device error word): do not call
+ *     this library on a device after resetting it in the same process.
  */
 pa_status pa_decode_noalloc(const void *query, const void *key_pages,
                             const void *value_pages, const int32_t *block_table,
@@ -438,33 +443,6 @@ const char *pa_status_string(pa_status status);
 
 /* Library version, e.g. "0.1.0". */
 const char *pa_version(void);
-
-/*
- * Test support for failure detection. The next pa_decode, pa_prefill or
- * pa_attention call made by the calling host thread runs one extra wait, in
- * its first block, on a barrier that nothing ever arrives at. That wait runs
- * out after its bounded limit (about one second), records PA_DEVERR_TIMEOUT
- * in the device error word, and the kernel then finishes normally with the
- * correct result. Nothing faults or hangs; the CUDA context stays usable.
- */
-void pa_debug_arm_wait_timeout(void);
-
-/*
- * Test and tuning support: which tensor-core prefill kernel the calling host
- * thread's pa_prefill / pa_attention calls use (head_dim 128, page_size >= 8).
- *   0  automatic (the default): as 2, except that a group size that is odd
- *      with fewer (request, head pair, query tile) items than SMs takes 1;
- *   1  one query head per block;
- *   2  two query heads of one KV group per block when the group size
- *      (num_q_heads / num_kv_heads) is at least 2; with an odd group size
- *      the last pair of each group computes its last head twice and writes
- *      it once. A group of 1 takes 1.
- * Settings 1 and 2 also hold for pa_prefill_split and for pa_attention given
- * a prefill workspace (the workspace is then not used). Any other value is
- * taken as 0. Returns the previous setting. Results agree
- * with the oracle under every setting; only the speed differs.
- */
-int pa_debug_prefill_variant(int variant);
 
 #ifdef __cplusplus
 }

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "../../include/pagedattn.h"
+#include "../../include/pagedattn_test.h"
 #include "pa_internal.h"
 
 namespace pa {
@@ -323,6 +324,9 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
         sa.scale_log2 = a.scale_log2;
         sa.causal = a.causal;
         sa.out_scale = a.out_scale;
+        // An error the caller left pending is not ours to clear: note it, so
+        // that only a refused cooperative launch of this call is cleared.
+        const bool pending = cudaPeekAtLastError() != cudaSuccess;
         cudaError_t e = launch_prefill_split(qmap, kmap, vmap, sa, dev->sm_count, workspace,
                                              dev->id, stream);
         if (e == cudaSuccess)
@@ -331,7 +335,8 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
             return PA_ERR_CUDA;
         // The register split is not available, or not every block could be
         // resident (another client holds SMs): the kernels below.
-        (void)cudaGetLastError();
+        if (e == cudaErrorCooperativeLaunchTooLarge && !pending)
+            (void)cudaGetLastError();
     }
     cudaError_t e = pairs ? launch_prefill_pairs(qmap, kmap, vmap, a, dev->id, stream)
                           : launch_prefill(qmap, kmap, vmap, a, dev->id, stream);

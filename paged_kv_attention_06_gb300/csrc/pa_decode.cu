@@ -1156,11 +1156,8 @@ cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_m
     mcfg.gridDim = dim3(unsigned(int64_t(a.B) * a.H_kv * a.MT));
     mcfg.blockDim = dim3(128);
     mcfg.dynamicSmemBytes = 0;
-    e = a.D == 64 ? cudaLaunchKernelEx(&mcfg, decode_merge_kernel<64>, ma, grid)
-                  : cudaLaunchKernelEx(&mcfg, decode_merge_kernel<128>, ma, grid);
-    if (e != cudaSuccess)
-        return e;
-    return cudaGetLastError();
+    return a.D == 64 ? cudaLaunchKernelEx(&mcfg, decode_merge_kernel<64>, ma, grid)
+                     : cudaLaunchKernelEx(&mcfg, decode_merge_kernel<128>, ma, grid);
 }
 
 }  // namespace pa

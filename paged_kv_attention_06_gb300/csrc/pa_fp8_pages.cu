@@ -124,7 +124,7 @@ cudaError_t launch_fp8_pages_to_bf16(const Fp8PagesArgs& a, cudaStream_t stream)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, fp8_pages_to_bf16_kernel, a);
-    return e != cudaSuccess ? e : cudaGetLastError();
+    return e;
 }
 
 }  // namespace pa

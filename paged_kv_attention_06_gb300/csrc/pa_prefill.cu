@@ -469,7 +469,7 @@ cudaError_t launch_prefill(const CUtensorMap& q_map, const CUtensorMap& key_map,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel, q_map, key_map, value_map, a);
-    return e != cudaSuccess ? e : cudaGetLastError();
+    return e;
 }
 
 }  // namespace pa

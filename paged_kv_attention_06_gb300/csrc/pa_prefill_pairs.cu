@@ -667,7 +667,7 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
     const cudaError_t e =
         odd ? cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<true>, q_map, key_map, value_map, a)
             : cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<false>, q_map, key_map, value_map, a);
-    return e != cudaSuccess ? e : cudaGetLastError();
+    return e;
 }
 
 }  // namespace pa

@@ -29,3 +29,20 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write every attention comparison of the run (error and reference
+    magnitudes) to the JSON file named by PA_PARITY_LOG, if set."""
+    path = os.environ.get("PA_PARITY_LOG")
+    if not path:
+        return
+    mod = sys.modules.get("gpu_util")
+    if mod is None:
+        return
+    import json
+    rows = [{"what": w, "max_err": a, "mean_err": b, "max_ref": c, "mean_ref": d,
+             "max_ratio": (a / c) if c > 0 else None, "mean_ratio": (b / d) if d > 0 else None}
+            for (w, a, b, c, d) in mod.PARITY_LOG]
+    with open(path, "w") as f:
+        json.dump(rows, f, indent=1)

@@ -13,6 +13,23 @@ import workloads as wl
 MAX_ERR = 2e-2
 MEAN_ERR = 2e-3
 
+# The same comparison relative to the size of the reference: max |err| <=
+# REL * max |ref| and mean |err| <= REL * mean |ref|. With N(0,1) values and
+# 16k-40k visible keys an output element is about 0.01, so the absolute bounds
+# alone cannot fail there. The kernels' own error is the bf16 rounding of the
+# output (relative 2^-9 at most) and of the probabilities fed to P.V (relative
+# 2^-9 per term, zero-mean, so about 2^-9/sqrt(3) of the output's size), with
+# fp32 accumulation far below both; 2^-6 leaves a margin of 8x over the
+# worst element. Dropping a fraction f of a row's keys moves its output by
+# about sqrt(f) of its size, so a row that loses more than ~0.03 % of its keys
+# fails the mean bound.
+REL = 2.0 ** -6
+
+# Every comparison made in this process: (what, max|err|, mean|err|,
+# max|ref|, mean|ref|), written out by the session hook in conftest.py when
+# PA_PARITY_LOG names a file.
+PARITY_LOG = []
+
 N_THREADS = os.cpu_count() or 1
 
 
@@ -78,9 +95,17 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     err = np.abs(got - ref)
-    assert err.max() <= MAX_ERR, f"{what}: max|err| {err.max():.3e} > {MAX_ERR}"
-    assert err.mean() <= MEAN_ERR, f"{what}: mean|err| {err.mean():.3e} > {MEAN_ERR}"
-    return float(err.max()), float(err.mean())
+    mag = np.abs(ref)
+    emax, emean = float(err.max()), float(err.mean())
+    rmax, rmean = float(mag.max()), float(mag.mean())
+    PARITY_LOG.append((what, emax, emean, rmax, rmean))
+    assert emax <= MAX_ERR, f"{what}: max|err| {emax:.3e} > {MAX_ERR}"
+    assert emean <= MEAN_ERR, f"{what}: mean|err| {emean:.3e} > {MEAN_ERR}"
+    assert emax <= REL * rmax, \
+        f"{what}: max|err| {emax:.3e} > 2^-6 * max|ref| ({REL * rmax:.3e})"
+    assert emean <= REL * rmean, \
+        f"{what}: mean|err| {emean:.3e} > 2^-6 * mean|ref| ({REL * rmean:.3e})"
+    return emax, emean
 
 
 def check_no_device_error():

@@ -1,5 +1,6 @@
-"""The C-ABI library loads and exports every function include/pagedattn.h
-declares; host-only entry points answer without a GPU."""
+"""The C-ABI library loads and exports every function include/pagedattn.h and
+include/pagedattn_test.h declare; host-only entry points answer without a
+GPU; the test hooks stay out of the production header."""
 import ctypes
 import os
 import re
@@ -8,10 +9,11 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+TEST_HEADER = os.path.join(ROOT, "include", "pagedattn_test.h")
 
 
-def _declared():
-    text = open(HEADER).read()
+def _declared(path=HEADER):
+    text = open(path).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
 
@@ -31,8 +33,15 @@ def test_header_declares_the_entry_points():
 
 
 def test_every_declared_symbol_is_exported(lib):
-    for name in _declared():
+    for name in _declared() + _declared(TEST_HEADER):
         assert hasattr(lib, name), f"{name} declared but not exported"
+
+
+def test_test_hooks_only_in_the_test_header():
+    """Production callers see no kernel-selection switch or injected wait."""
+    hooks = _declared(TEST_HEADER)
+    assert hooks == ["pa_debug_arm_wait_timeout", "pa_debug_prefill_variant"]
+    assert not [n for n in _declared() if n.startswith("pa_debug")]
 
 
 def test_status_strings(lib):

@@ -27,7 +27,7 @@ def test_serving_trace_small(page_size):
     max_pages = -(-int(prompts.max() + outputs.max()) // page_size)
     num_pages = batch * max_pages + 8
     cache = pa.KVCache(num_pages, page_size)
-    pool = wl.PagePool(page_size)
+    pool = wl.PageFreeList(page_size)
     kp_h = wl.normal_bf16(rng, (num_pages, H_kv, page_size, D))
     vp_h = wl.normal_bf16(rng, (num_pages, H_kv, page_size, D))
     kp, vp = dev(kp_h), dev(vp_h)
@@ -41,8 +41,8 @@ def test_serving_trace_small(page_size):
         f_cl = np.zeros((len(ids),), dtype=np.int32)
         for i, sid in enumerate(ids):
             f_sm[i, :toks[i]] = fixture[sid].append(toks[i])
-            f_bt[i, :len(fixture[sid].page_ids)] = fixture[sid].page_ids
-            f_cl[i] = fixture[sid].offset
+            f_bt[i, :len(fixture[sid].pages)] = fixture[sid].pages
+            f_cl[i] = fixture[sid].length
         assert np.array_equal(bt, f_bt) and np.array_equal(cl, f_cl) and np.array_equal(sm, f_sm)
         n = len(ids)
         k_new = wl.normal_bf16(rng, (n, H_kv, l_new, D))
@@ -65,7 +65,7 @@ def test_serving_trace_small(page_size):
         while waiting and len(active) < batch:
             sid = waiting.pop(0)
             cache.add(sid)
-            fixture[sid] = wl.PagedCache(pool)
+            fixture[sid] = wl.RequestPages(pool)
             active[sid] = [0, 0]
         dec = [s for s, (p, o) in active.items() if p >= prompts[s]]
         pre = [s for s, (p, o) in active.items() if p < prompts[s]]

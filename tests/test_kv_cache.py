@@ -40,7 +40,7 @@ def test_append_walkthrough_tail_fill():
 
 def test_matches_python_fixture_on_random_histories():
     """Random admissions, chunked appends and releases: the C++ cache and the
-    fixture (PagePool LIFO free list + PagedCache tail fill) give the same
+    fixture (PageFreeList last-returned-first reuse + RequestPages tail fill) give the same
     page ids, slots, tables and context lengths at every step."""
     pa = _pa()
     rng = np.random.default_rng(5)
@@ -48,13 +48,13 @@ def test_matches_python_fixture_on_random_histories():
         ps = int(rng.choice([1, 4, 16]))
         num_pages = 4096
         c = pa.KVCache(num_pages, ps)
-        pool = wl.PagePool(ps)
+        pool = wl.PageFreeList(ps)
         live = {}
         next_id = 0
         for step in range(60):
             if len(live) < 4 and rng.random() < 0.5:
                 c.add(next_id)
-                live[next_id] = wl.PagedCache(pool)
+                live[next_id] = wl.RequestPages(pool)
                 next_id += 1
             if live and rng.random() < 0.15:
                 sid = int(rng.choice(list(live)))
@@ -68,9 +68,9 @@ def test_matches_python_fixture_on_random_histories():
             for i, sid in enumerate(ids):
                 slots = live[sid].append(toks[i])
                 assert sm[i, :toks[i]].tolist() == slots
-                assert [int(p) for p in bt[i] if p >= 0] == live[sid].page_ids
-                assert int(cl[i]) == live[sid].offset == c.context_len(sid)
-        assert c.free_pages == num_pages - len(pool.used_page_ids)
+                assert [int(p) for p in bt[i] if p >= 0] == live[sid].pages
+                assert int(cl[i]) == live[sid].length == c.context_len(sid)
+        assert c.free_pages == num_pages - len(pool.in_use)
 
 
 def test_step_is_all_or_nothing():

@@ -118,17 +118,17 @@ def test_p2_append_walkthrough(which):
     g = _golden("p2_append_walkthrough.json")
     exp = g[which]
     ps = g["page_size"]
-    pool = wl.PagePool(ps)
-    cache = wl.PagedCache(pool, policy=exp["policy"])
+    pool = wl.PageFreeList(ps)
+    cache = wl.RequestPages(pool, policy=exp["policy"])
     P, D = 3, 8
     key_pages = np.zeros((P, 1, ps, D), dtype=np.uint16)
     value_pages = np.zeros((P, 1, ps, D), dtype=np.uint16)
     token = 0
     for c, n_tok in enumerate(g["chunks"]):
         slots = cache.append(n_tok)
-        assert cache.page_ids == exp["page_ids_after_each_chunk"][c]
-        assert cache.page_lens == exp["page_lens_after_each_chunk"][c]
-        assert cache.offset == exp["offset_after_each_chunk"][c]
+        assert cache.pages == exp["page_ids_after_each_chunk"][c]
+        assert cache.fill == exp["page_lens_after_each_chunk"][c]
+        assert cache.length == exp["offset_after_each_chunk"][c]
         # token t's K row is the bf16 bits of (t + 1) in every lane, V of -(t+1)
         ids = np.arange(token, token + n_tok)
         key = np.repeat(wl.bf16_bits((ids + 1).astype(np.float32))[:, None], D, 1)

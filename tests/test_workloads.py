@@ -13,56 +13,56 @@ import workloads as wl
 
 
 def test_lifo_reuse_and_growth():
-    pool = wl.PagePool(4)
-    a, b, c = pool.allocate_page(), pool.allocate_page(), pool.allocate_page()
+    pool = wl.PageFreeList(4)
+    a, b, c = pool.take(), pool.take(), pool.take()
     assert (a, b, c) == (0, 1, 2)
-    pool.free_page(b)
-    pool.free_page(a)
-    assert pool.allocate_page() == a          # last freed, first reused
-    assert pool.allocate_page() == b
-    assert pool.allocate_page() == 3          # free list empty: grow
-    assert pool.num_allocated_pages == 4
+    pool.give_back(b)
+    pool.give_back(a)
+    assert pool.take() == a          # last freed, first reused
+    assert pool.take() == b
+    assert pool.take() == 3          # free list empty: grow
+    assert pool.fresh == 4
 
 
 def test_double_free_raises():
-    pool = wl.PagePool(4)
-    p = pool.allocate_page()
-    pool.free_page(p)
-    with pytest.raises(wl.PageAlreadyFree):
-        pool.free_page(p)
+    pool = wl.PageFreeList(4)
+    p = pool.take()
+    pool.give_back(p)
+    with pytest.raises(wl.DoubleFree):
+        pool.give_back(p)
 
 
 def test_release_returns_every_page_once():
-    pool = wl.PagePool(4)
-    caches = [wl.PagedCache(pool) for _ in range(3)]
+    pool = wl.PageFreeList(4)
+    caches = [wl.RequestPages(pool) for _ in range(3)]
     for c, n in zip(caches, (5, 9, 1)):
         c.append(n)
-    owned = [list(c.page_ids) for c in caches]
+    owned = [list(c.pages) for c in caches]
     assert len({p for o in owned for p in o}) == sum(len(o) for o in owned)   # no aliasing
     caches[1].release()
-    assert sorted(pool.free_page_ids) == sorted(owned[1])
-    with pytest.raises(wl.PageAlreadyFree):
+    assert sorted(pool.returned) == sorted(owned[1])
+    with pytest.raises(wl.DoubleFree):
         for p in owned[1]:
-            pool.free_page(p)
+            pool.give_back(p)
 
 
 def test_decode_allocates_only_on_tail_overflow():
-    pool = wl.PagePool(4)
-    c = wl.PagedCache(pool)
+    pool = wl.PageFreeList(4)
+    c = wl.RequestPages(pool)
     c.append(3)
     for step in range(9):
-        before = len(c.page_ids)
-        full = c.page_lens[-1] == 4
+        before = len(c.pages)
+        full = c.fill[-1] == 4
         c.append(1)
-        assert len(c.page_ids) == before + (1 if full else 0)
-    assert c.offset == 12 and c.page_lens == [4, 4, 4]
+        assert len(c.pages) == before + (1 if full else 0)
+    assert c.length == 12 and c.fill == [4, 4, 4]
 
 
 def test_slots_follow_page_and_offset():
-    pool = wl.PagePool(16)
+    pool = wl.PageFreeList(16)
     for _ in range(5):
-        pool.allocate_page()
-    c = wl.PagedCache(pool)
+        pool.take()
+    c = wl.RequestPages(pool)
     slots = c.append(20)
     assert slots[:16] == [5 * 16 + t for t in range(16)]
     assert slots[16:] == [6 * 16 + t for t in range(4)]

@@ -7,10 +7,11 @@ no weighted sums), and it imports neither the oracle nor the CUDA library.
 
 Contents:
   * bf16 <-> fp32 bit conversion (round to nearest even);
-  * ``PagePool`` / ``PagedCache``: the page allocator and per-request cache of
-    Tutorial 13: Paged Attention and Memory Management, section 3 "The Page
-    Pool" and section 4 "The Request Cache" (LIFO free-list reuse, grow when
-    empty, tail page filled first). Used to produce block tables and
+  * ``PageFreeList`` / ``RequestPages``: the page allocator and per-request
+    page list whose behaviour Tutorial 13: Paged Attention and Memory
+    Management states in section 3 "The Page Pool" and section 4 "The
+    Request Cache" (last returned page reused first, fresh ids when none is
+    returned, tail page filled first). Used to produce block tables and
     slot_mapping;
   * ``slot_of``: the flat-slot encoding of Reading vLLM's PagedAttention
     Kernel, 3.2 "Writing into the cache" (physical_block * block_size +
@@ -94,90 +95,84 @@ def normal_bf16(rng: np.random.Generator, shape, std: float = 1.0) -> np.ndarray
 
 
 # ----------------------------------------------------------------------------
-# Page allocator fixture (Tutorial 13, sections 3 and 4)
+# Page allocator fixture (Tutorial 13, sections 3 and 4, from the behaviour
+# the tutorial states: a page given back is the first one handed out again;
+# with none given back the pool hands out the next id it never used; a page
+# cannot be given back twice; new tokens go into the request's last page
+# while it has room, else onto a new page)
 
 
-class PageAlreadyFree(RuntimeError):
-    """Raised when a page is returned to the pool twice."""
+class DoubleFree(RuntimeError):
+    """Raised when a page is given back to the pool twice."""
 
 
-class PagePool:
-    """Free-list page allocator. A freed id goes on top of the free list and
-    is the next one handed out (LIFO); with an empty free list the pool grows
-    and the new id is the count of pages allocated so far."""
+class PageFreeList:
+    """Hands out page ids: the most recently returned id first, else the
+    lowest id never handed out (``fresh`` counts those)."""
 
     def __init__(self, page_size: int):
         self.page_size = int(page_size)
-        self.free_page_ids: List[int] = []
-        self.used_page_ids: set = set()
-        self.num_allocated_pages = 0
+        self.returned: List[int] = []  # stack, top = last returned
+        self.in_use: set = set()
+        self.fresh = 0
 
-    def allocate_page(self) -> int:
-        if self.free_page_ids:
-            page_id = self.free_page_ids.pop()
+    def take(self) -> int:
+        if self.returned:
+            pid = self.returned[-1]
+            del self.returned[-1]
         else:
-            page_id = self.num_allocated_pages
-            self.num_allocated_pages += 1
-        self.used_page_ids.add(page_id)
-        return page_id
+            pid, self.fresh = self.fresh, self.fresh + 1
+        self.in_use.add(pid)
+        return pid
 
-    def free_page(self, page_id: int) -> None:
-        if page_id not in self.used_page_ids:
-            raise PageAlreadyFree(f"page {page_id} is already free")
-        self.used_page_ids.remove(page_id)
-        self.free_page_ids.append(page_id)
+    def give_back(self, pid: int) -> None:
+        if pid not in self.in_use:
+            raise DoubleFree(f"page {pid} is not in use")
+        self.in_use.discard(pid)
+        self.returned.append(pid)
 
 
 @dataclass
-class PagedCache:
-    """One request's pages in one layer pool.
+class RequestPages:
+    """The pages one request holds in a pool, in logical order.
 
-    ``policy="tail_fill"`` fills the partial tail page before allocating new
-    pages (the append code of Tutorial 13, section 4; also the decode rule of
-    Week 3 Day 4, "Decode Metadata": allocate only when the tail page is
-    full). ``policy="new_page_per_chunk"`` starts every chunk on a fresh page,
-    which is what the printed example walkthrough of Tutorial 13 shows; it
-    leaves holes that a block table plus context length cannot describe, so it
-    exists only to reproduce that walkthrough."""
+    ``policy="tail_fill"``: a token goes into the last page while that page
+    has room, otherwise onto a fresh page (Tutorial 13, section 4; Week 3
+    Day 4, "Decode Metadata": allocate only when the tail page is full).
+    ``policy="new_page_per_chunk"``: each call's first token starts a fresh
+    page, as the printed walkthrough of Tutorial 13 shows; the holes this
+    leaves cannot be described by a block table plus a context length, so it
+    serves only to reproduce that walkthrough.
+    ``pages``: page ids; ``fill``: tokens held in each page; ``length``: tokens
+    placed so far."""
 
-    pool: PagePool
+    pool: PageFreeList
     policy: str = "tail_fill"
-    page_ids: List[int] = field(default_factory=list)
-    page_lens: List[int] = field(default_factory=list)
-    offset: int = 0
+    pages: List[int] = field(default_factory=list)
+    fill: List[int] = field(default_factory=list)
+    length: int = 0
 
     def append(self, n_tokens: int) -> List[int]:
-        """Place n_tokens new tokens; returns their flat slots in order."""
-        ps = self.pool.page_size
-        slots: List[int] = []
-        start = 0
-        if (self.policy == "tail_fill" and self.page_ids
-                and self.page_lens[-1] < ps):
-            pid = self.page_ids[-1]
-            first = self.page_lens[-1]
-            take = min(ps - first, n_tokens)
-            slots.extend(slot_of(pid, first + t, ps) for t in range(take))
-            self.page_lens[-1] += take
-            start += take
-        elif self.policy not in ("tail_fill", "new_page_per_chunk"):
+        """Place n_tokens new tokens, one at a time; returns their flat slots."""
+        if self.policy not in ("tail_fill", "new_page_per_chunk"):
             raise ValueError(f"unknown policy {self.policy}")
-        while start < n_tokens:
-            end = min(start + ps, n_tokens)
-            pid = self.pool.allocate_page()
-            slots.extend(slot_of(pid, t, ps) for t in range(end - start))
-            self.page_ids.append(pid)
-            self.page_lens.append(end - start)
-            start = end
-        self.offset += n_tokens
-        return slots
+        ps = self.pool.page_size
+        out: List[int] = []
+        for t in range(n_tokens):
+            room = bool(self.pages) and self.fill[-1] < ps
+            if not room or (t == 0 and self.policy == "new_page_per_chunk"):
+                self.pages.append(self.pool.take())
+                self.fill.append(0)
+            out.append(slot_of(self.pages[-1], self.fill[-1], ps))
+            self.fill[-1] += 1
+        self.length += n_tokens
+        return out
 
     def release(self) -> None:
-        """Return every page of this request to the pool exactly once."""
-        for pid in self.page_ids:
-            self.pool.free_page(pid)
-        self.page_ids = []
-        self.page_lens = []
-        self.offset = 0
+        """Give every page of this request back to the pool exactly once."""
+        held, self.pages, self.fill, self.length = self.pages, [], [], 0
+        for pid in held:
+            self.pool.give_back(pid)
 
 
 def slot_of(page_id: int, offset_in_page: int, page_size: int) -> int:
@@ -244,23 +239,23 @@ def _page_tables_churn(rng, lens: Sequence[int], page_size: int, num_pages: int,
 
     Every pool id is allocated once and freed in random order (a shuffled free
     list); transient requests then take ``freed_fraction`` of the pages needed
-    and release them (those ids go back on top of the LIFO free list); the
+    and release them (those ids go back on top of the returned stack); the
     real requests are then prefilled round-robin in chunks of ``step_tokens``
     with the tail-fill policy, so the first pages they get are the freed and
     reused ids. Returns (tables, transient page ids)."""
-    pool = PagePool(page_size)
-    ids = [pool.allocate_page() for _ in range(num_pages)]
+    pool = PageFreeList(page_size)
+    ids = [pool.take() for _ in range(num_pages)]
     for i in rng.permutation(len(ids)):
-        pool.free_page(ids[int(i)])
+        pool.give_back(ids[int(i)])
     need = sum(math.ceil(n / page_size) for n in lens)
-    transient = PagedCache(pool)
+    transient = RequestPages(pool)
     transient.append(int(freed_fraction * need) * page_size)
-    ghost_ids = list(transient.page_ids)
+    ghost_ids = list(transient.pages)
     order = list(rng.permutation(len(ghost_ids)))
     for j in order:                       # release in random order
-        pool.free_page(ghost_ids[int(j)])
-    transient.page_ids = []
-    caches = [PagedCache(pool) for _ in lens]
+        pool.give_back(ghost_ids[int(j)])
+    transient.pages = []
+    caches = [RequestPages(pool) for _ in lens]
     remaining = list(lens)
     while any(r > 0 for r in remaining):
         for b, cache in enumerate(caches):
@@ -268,9 +263,9 @@ def _page_tables_churn(rng, lens: Sequence[int], page_size: int, num_pages: int,
                 t = min(step_tokens, remaining[b])
                 cache.append(t)
                 remaining[b] -= t
-    if pool.num_allocated_pages != num_pages:
+    if pool.fresh != num_pages:
         raise AssertionError("pool grew beyond its sizing")
-    return [c.page_ids for c in caches], ghost_ids
+    return [c.pages for c in caches], ghost_ids
 
 
 def build_batch(name: str, B: int, H_q: int, H_kv: int, D: int, page_size: int,

@@ -8,6 +8,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <mutex>
@@ -345,12 +346,29 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// (request, KV head, 16-row tile) count of a call: the limit kMaxSegments
+// applies to it.
 int64_t decode_segments(const pa_shape& s)
 {
     const int64_t G = s.num_q_heads / s.num_kv_heads;
     const int64_t MT = (G * s.q_len + kDecodeRows - 1) / kDecodeRows;
     return int64_t(s.batch) * s.num_kv_heads * MT;
 }
+
+}  // namespace
+
+DecodePlan decode_plan(const pa_shape& s, bool fp8)
+{
+    DecodePlan p;
+    const int64_t G = s.num_q_heads / s.num_kv_heads;
+    p.MT = int32_t((G * s.q_len + kDecodeRows - 1) / kDecodeRows);
+    p.TG = fp8 || p.MT <= 1 ? 1 : p.MT == 2 ? 2 : 4;
+    p.MS = (p.MT + p.TG - 1) / p.TG;
+    p.nseg = int64_t(s.batch) * s.num_kv_heads * p.MS;
+    return p;
+}
+
+namespace {
 
 // Runs the split-KV kernel. whole_segments = 1 gives every block whole
 // segments (no partial states, no workspace).
@@ -367,10 +385,11 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
         return st;
     const int G = s.num_q_heads / s.num_kv_heads;
     const int64_t R = int64_t(G) * s.q_len;
-    const int64_t nseg = decode_segments(s);
-    if (R >= (int64_t(1) << 30) || nseg > kMaxSegments)
+    if (R >= (int64_t(1) << 30) || decode_segments(s) > kMaxSegments)
         return PA_ERR_UNSUPPORTED;
-    const size_t smem = decode_smem_bytes(s.head_dim, s.batch, fp8 != 0);
+    const DecodePlan plan = decode_plan(s, fp8 != 0);
+    const int64_t nseg = plan.nseg;
+    const size_t smem = decode_smem_bytes(s.head_dim, s.batch, fp8 != 0, plan.TG);
     if (smem > size_t(dev->max_smem_optin))
         return PA_ERR_UNSUPPORTED;  // batch too large for the per-block prefix table
 
@@ -390,7 +409,7 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
     DecodeArgs a;
     memset(&a, 0, sizeof a);
     if (!whole_segments) {
-        const size_t need = decode_workspace_bytes(nseg, grid_max, s.head_dim);
+        const size_t need = decode_workspace_bytes(nseg, grid_max, s.head_dim, plan.TG);
         if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
             return PA_ERR_WORKSPACE;
         a.partials = static_cast<float*>(workspace);
@@ -416,7 +435,8 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
     a.num_pages = s.num_pages;
     a.G = G;
     a.R = int32_t(R);
-    a.MT = int32_t((R + kDecodeRows - 1) / kDecodeRows);
+    a.MS = plan.MS;
+    a.TG = plan.TG;
     a.box_rows = page_size < kDecodeTokens ? page_size : kDecodeTokens;
     a.swz = a.box_rows >= 8 ? 7 : 0;
     a.whole_segments = whole_segments;
@@ -453,7 +473,10 @@ pa_status validate_decode(const void* query, const void* key_pages, const void* 
     const int64_t R = int64_t(s.num_q_heads / s.num_kv_heads) * s.q_len;
     if (R >= (int64_t(1) << 30) || decode_segments(s) > kMaxSegments)
         return PA_ERR_UNSUPPORTED;
-    if (decode_smem_bytes(s.head_dim, s.batch) > size_t(dev->max_smem_optin))
+    const size_t smem = std::max(decode_smem_bytes(s.head_dim, s.batch),
+                                 decode_smem_bytes(s.head_dim, s.batch, false,
+                                                   decode_plan(s, false).TG));
+    if (smem > size_t(dev->max_smem_optin))
         return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
@@ -518,8 +541,11 @@ size_t pa_decode_workspace_bytes(pa_shape shape)
     DeviceInfo* dev;
     if (device_info(&dev) != PA_OK)
         return 0;
-    return decode_workspace_bytes(decode_segments(shape), decode_max_grid(dev->sm_count),
-                                  shape.head_dim);
+    // The bf16 plan's need; an e4m3 call's (one row tile per segment) is
+    // never larger.
+    const DecodePlan plan = decode_plan(shape, false);
+    return decode_workspace_bytes(plan.nseg, decode_max_grid(dev->sm_count), shape.head_dim,
+                                  plan.TG);
 }
 
 namespace {

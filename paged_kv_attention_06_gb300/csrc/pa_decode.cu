@@ -60,22 +60,27 @@ constexpr int kThreads = kConsumerThreads + 32;
 // F8: K/V pages of e4m3 codes (one byte per element; 128-byte rows at
 // D = 128): half-size stages, four of them, and a tile for the merge of the
 // four consumer warps' states at the end of a piece.
-template <int D, bool F8 = false>
+// TG: 16-row query tiles per segment; each stage holds the Q tiles of all of
+// them. Three stages where they fit in about half the shared memory of an SM
+// (two blocks per SM), otherwise two.
+template <int D, bool F8 = false, int TG = 1>
 struct Layout {
-    static constexpr int kStages = F8 ? 4 : 3;
     static constexpr int kHalves = D / 64;                   // Q: 128-byte column blocks (bf16)
     static constexpr int kKVHalves = F8 ? D / 128 : D / 64;  // K/V: 128-byte column blocks
     static constexpr int kHalfBytes = kDecodeTokens * 128;   // 64 rows x 128 B
     static constexpr int kStageBytes = kKVHalves * kHalfBytes; // K (or V) of one granule
+    // Q tiles of the segment whose piece starts at a stage's granule:
+    // [stage][tile][half][16 rows][128 B], 128B swizzle (TMA box of 16 rows).
+    static constexpr int kQHalfBytes = kDecodeRows * 128;
+    static constexpr int kQStageBytes = TG * kHalves * kQHalfBytes;
+    static constexpr int kStages =
+        F8 ? 4 : (3 * (2 * kStageBytes + kQStageBytes) <= 110 * 1024 ? 3 : 2);
     static constexpr int kK = 0;
     static constexpr int kV = kK + kStages * kStageBytes;
-    // Q tile of the segment whose piece starts at a stage's granule:
-    // [stage][half][16 rows][128 B], 128B swizzle (TMA box of 16 rows).
-    static constexpr int kQHalfBytes = kDecodeRows * 128;
     static constexpr int kQ = kV + kStages * kStageBytes;
     // F8: each consumer warp's normalised O (f16) at the end of a piece,
     // [warp][16 rows][D]
-    static constexpr int kWork = kQ + kStages * kHalves * kQHalfBytes;
+    static constexpr int kWork = kQ + kStages * kQStageBytes;
     static constexpr int kWorkBytes = F8 ? kConsumerWarps * kDecodeRows * D * 2 : 0;
     static constexpr int kBar = kWork + kWorkBytes;
     static constexpr int kMisc = kBar + 2 * kStages * 8;     // abort flag, test barrier
@@ -93,13 +98,13 @@ __device__ __forceinline__ int clamp_context(int n, int cap, unsigned* err)
 }
 
 struct SegmentPos {
-    int b, h, mt, seg;
+    int b, h, ms, seg;  // request, KV head, segment within the (b, h) rows
     int64_t seg_start;  // first granule of the segment in the stream
     int seg_len;        // granules in the segment
 };
 
 // Locates granule x of the stream. pre[b] = first granule of request b.
-__device__ __forceinline__ SegmentPos locate(const int32_t* pre, int B, int per_req, int MT,
+__device__ __forceinline__ SegmentPos locate(const int32_t* pre, int B, int per_req, int MS,
                                              int64_t x)
 {
     int lo = 0, hi = B - 1;
@@ -115,8 +120,8 @@ __device__ __forceinline__ SegmentPos locate(const int32_t* pre, int B, int per_
     const int gb = (pre[lo + 1] - pre[lo]) / per_req;
     const int r = int(x - pre[lo]);
     const int hm = r / gb;
-    s.h = hm / MT;
-    s.mt = hm - s.h * MT;
+    s.h = hm / MS;
+    s.ms = hm - s.h * MS;
     s.seg = lo * per_req + hm;
     s.seg_start = pre[lo] + int64_t(hm) * gb;
     s.seg_len = gb;
@@ -167,15 +172,16 @@ __device__ __forceinline__ int64_t granule_at_unit(const int32_t* pre, int B, in
     return pre[lo] + hm * gb + (in > 0 ? in : 0);
 }
 
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, int TG = 1>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap key_map,
                   const __grid_constant__ CUtensorMap value_map,
                   const __grid_constant__ CUtensorMap q_map, const DecodeArgs a)
 {
-    using Lay = Layout<D, F8>;
+    using Lay = Layout<D, F8, TG>;
     constexpr int kStages = Lay::kStages;
-    static_assert(!F8 || D == 128, "e4m3 pages: head_dim 128");
+    static_assert(!F8 || (D == 128 && TG == 1), "e4m3 pages: head_dim 128, one row tile");
+    static_assert(TG == 1 || TG == 2 || TG == 4, "row tiles per segment");
     constexpr int kKS = D / 16;  // k-steps of 16 over the head dimension
 
     extern __shared__ uint8_t smem_raw[];
@@ -188,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int per_req = a.H_kv * a.MT;
+    const int per_req = a.H_kv * a.MS;
     const int cap = a.max_pages * a.ps;
 
     // Inputs may come from the previous kernel in the stream (e.g. the append
@@ -307,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // out, so its loads overlap the wait for a free stage.
         int64_t x = x_begin;
         while (x < x_end) {
-            const SegmentPos sp = locate(pre, a.B, per_req, a.MT, x);
+            const SegmentPos sp = locate(pre, a.B, per_req, a.MS, x);
             const int64_t piece_start = x;
             const int64_t piece_end =
                 x_end < sp.seg_start + sp.seg_len ? x_end : sp.seg_start + sp.seg_len;
@@ -381,23 +387,30 @@ __global__ void __launch_bounds__(kThreads, 2)
             };
             int nbox, row_a, row_b;
             translate(x, nbox, row_a, row_b);
+            // Row tiles of this segment that hold query rows (the others are
+            // padding: no Q load, no compute).
+            const int q_tiles = min(TG, (a.R - sp.ms * TG * kDecodeRows + kDecodeRows - 1) / kDecodeRows);
             for (; x < piece_end; ++x) {
-                // The first granule of a piece also brings the segment's Q tile
+                // The first granule of a piece also brings the segment's Q tiles
                 // (the G heads x L rows of a KV group are consecutive rows of q).
                 const bool first = x == piece_start;
                 const bool ok = mbar_wait_warp(&empty[stage], phase ^ 1u, misc, a.err);
                 if (ok && (nbox > 0 || first)) {
                     const uint32_t bytes =
                         uint32_t(nbox) * box * 128u * Lay::kKVHalves * 2u +
-                        (first ? uint32_t(Lay::kHalves * Lay::kQHalfBytes) : 0u);
+                        (first ? uint32_t(q_tiles * Lay::kHalves * Lay::kQHalfBytes) : 0u);
                     if (lane == 0) {
                         mbar_arrive_expect_tx(&full[stage], bytes);
                         if (first) {
-                            const int qrow = (sp.b * a.H_q + sp.h * a.G) * a.L + sp.mt * kDecodeRows;
+                            for (int t = 0; t < q_tiles; ++t) {
+                                const int qrow = (sp.b * a.H_q + sp.h * a.G) * a.L +
+                                                 (sp.ms * TG + t) * kDecodeRows;
 #pragma unroll
-                            for (int hf = 0; hf < Lay::kHalves; ++hf)
-                                tma_load_2d(smem + Lay::kQ + (stage * Lay::kHalves + hf) * Lay::kQHalfBytes,
-                                            &q_map, hf * 64, qrow, &full[stage], policy);
+                                for (int hf = 0; hf < Lay::kHalves; ++hf)
+                                    tma_load_2d(smem + Lay::kQ + stage * Lay::kQStageBytes +
+                                                    (t * Lay::kHalves + hf) * Lay::kQHalfBytes,
+                                                &q_map, hf * 64, qrow, &full[stage], policy);
+                            }
                         }
                     }
                     __syncwarp();
@@ -433,24 +446,33 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ===================== consumer warps ===================================
-    // Consumer warp w owns output columns [w * D/4, (w + 1) * D/4). Every
-    // warp computes the scores of all 64 tokens of a granule (identical in all
-    // four warps, so the softmax state needs no exchange) and P V for its own
-    // columns; a segment's result never has to be merged across warps.
-    constexpr int kCols = D / kConsumerWarps;  // output columns per warp
+    // The TG row tiles of a segment are spread over the four consumer warps:
+    // kWPT = 4 / TG warps per tile, each owning D / kWPT output columns. Every
+    // warp computes the scores of all 64 tokens of a granule for its tile's
+    // rows (identical in the kWPT warps of a tile, so the softmax state needs
+    // no exchange) and P V for its own columns; a segment's result never has
+    // to be merged across warps. (e4m3 pages: TG = 1, see below.)
+    constexpr int kWPT = kConsumerWarps / TG;  // warps per row tile
+    constexpr int kCols = D / kWPT;            // output columns per warp
     constexpr int kON = kCols / 8;             // output n-tiles per warp
     constexpr int kSN = kDecodeTokens / 8;     // score n-tiles per granule
     const int swz = a.swz;        // stage layout: chunk ^ (row & 7) when swizzled
     const int row0 = lane >> 2;   // fragment rows row0 and row0 + 8
     const int quad = lane & 3;
-    const int col0 = warp * kCols;
+    const int tw = warp / kWPT;   // this warp's row tile within a segment
+    const int col0 = (warp % kWPT) * kCols;
     int stage = 0;
     uint32_t phase = 0;
-    constexpr int kSlotFloats = kDecodeRows * (D + 2);
+    constexpr int kTileFloats = kDecodeRows * (D + 2);   // m[16], l[16], acc[16][D]
+    constexpr int kSlotFloats = TG * kTileFloats;
 
+    // Row of this warp's tile of a segment, in the (request, KV head) rows
+    auto tile_row = [&](const SegmentPos& p, int rw) -> int {
+        return (p.ms * TG + tw) * kDecodeRows + rw;
+    };
     // Output row index of fragment row rw of a segment, or -1 for padding.
     auto out_row = [&](const SegmentPos& p, int rw) -> int64_t {
-        const int rg = p.mt * kDecodeRows + rw;
+        const int rg = tile_row(p, rw);
         if (rg >= a.R)
             return -1;
         const int g = rg / a.L, i = rg - g * a.L;
@@ -487,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int r_lo = warp * kWT;
         int64_t x = x_begin;
         while (x < x_end) {
-            const SegmentPos sp = locate(pre, a.B, per_req, a.MT, x);
+            const SegmentPos sp = locate(pre, a.B, per_req, a.MS, x);
             const int64_t piece_end = min(x_end, sp.seg_start + sp.seg_len);
             const int n = clamp_context(a.context_lens[sp.b], cap, a.err);
             uint32_t qa[kKS][4];
@@ -495,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             int lim[2];
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-                const int rg = sp.mt * kDecodeRows + row0 + rr * 8;
+                const int rg = tile_row(sp, row0 + rr * 8);
                 const int i = rg < a.R ? rg % a.L : a.L - 1;
                 lim[rr] = a.causal ? min(n - a.L + i, n - 1) : n - 1;
             }
@@ -512,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int nvalid = min(kDecodeTokens, n - t0);
                 const bool ok = mbar_wait_warp(&full[stage], phase, misc, a.err);
                 if (need_q) {
-                    const uint8_t* qs = smem + Lay::kQ + stage * Lay::kHalves * Lay::kQHalfBytes;
+                    const uint8_t* qs = smem + Lay::kQ + stage * Lay::kQStageBytes;
 #pragma unroll
                     for (int kk = 0; kk < kKS; ++kk) {
                         const int d = 16 * kk + 4 * quad;
@@ -751,20 +773,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     } else {
     int64_t x = x_begin;
     while (x < x_end) {
-        const SegmentPos sp = locate(pre, a.B, per_req, a.MT, x);
+        const SegmentPos sp = locate(pre, a.B, per_req, a.MS, x);
         const int64_t piece_end = min(x_end, sp.seg_start + sp.seg_len);
         const int n = clamp_context(a.context_lens[sp.b], cap, a.err);
 
         // Q fragments of the piece: from the stage of its first granule,
-        // loaded (ldmatrix) once that stage has landed.
+        // loaded (ldmatrix) once that stage has landed. A tile past the
+        // segment's rows (a group of 3 tiles in a slot of 4) computes nothing.
         uint32_t qa[kKS][4];
-        bool need_q = true;
+        const bool live_tile = tile_row(sp, 0) < a.R;
+        bool need_q = live_tile;
 
         // Last visible position of this thread's two fragment rows.
         int lim[2];
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
-            const int rg = sp.mt * kDecodeRows + row0 + rr * 8;
+            const int rg = tile_row(sp, row0 + rr * 8);
             const int i = rg < a.R ? rg % a.L : a.L - 1;
             lim[rr] = a.causal ? min(n - a.L + i, n - 1) : n - 1;
         }
@@ -782,7 +806,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int nvalid = min(kDecodeTokens, n - t0);
             const bool ok = mbar_wait_warp(&full[stage], phase, misc, a.err);
             if (need_q) {
-                const uint8_t* qs = smem + Lay::kQ + stage * Lay::kHalves * Lay::kQHalfBytes;
+                const uint8_t* qs = smem + Lay::kQ + stage * Lay::kQStageBytes +
+                                    tw * Lay::kHalves * Lay::kQHalfBytes;
 #pragma unroll
                 for (int kk = 0; kk < kKS; ++kk) {
                     const int r = lane & 15;
@@ -794,22 +819,43 @@ __global__ void __launch_bounds__(kThreads, 2)
                 need_q = false;
             }
             bool wrote = false;
-            if (ok && nvalid > 0) {
-                if (nvalid < kDecodeTokens) {
-                    // Zero this warp's V columns of the rows past the context:
-                    // P is 0 there, but 0 * NaN is not.
-                    constexpr int kChunks = kCols / 8;  // 16-byte chunks per row
-                    const int nz = (kDecodeTokens - nvalid) * kChunks;
-                    for (int idx = lane; idx < nz; idx += 32) {
-                        const int r = nvalid + idx / kChunks;
-                        const int ch = col0 / 8 + idx % kChunks;
-                        *reinterpret_cast<uint4*>(v_half(stage, ch >> 3) + r * 128 +
-                                                  (((ch & 7) ^ (r & swz)) << 4)) =
-                            make_uint4(0, 0, 0, 0);
+            if (nvalid > 0 && nvalid < kDecodeTokens) {
+                // Zero the V rows past the context: P is 0 there, but 0 * NaN
+                // is not. One row tile per segment: each warp zeroes its own
+                // columns. Several: the warps of different tiles read the same
+                // columns, so the four warps zero disjoint chunks and meet at a
+                // barrier (reached by all of them, whatever their waits gave).
+                if constexpr (TG == 1) {
+                    if (ok) {
+                        constexpr int kChunks = kCols / 8;  // 16-byte chunks per row
+                        const int nz = (kDecodeTokens - nvalid) * kChunks;
+                        for (int idx = lane; idx < nz; idx += 32) {
+                            const int r = nvalid + idx / kChunks;
+                            const int ch = col0 / 8 + idx % kChunks;
+                            *reinterpret_cast<uint4*>(v_half(stage, ch >> 3) + r * 128 +
+                                                      (((ch & 7) ^ (r & swz)) << 4)) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        wrote = true;
                     }
-                    wrote = true;
                     __syncwarp();
+                } else {
+                    if (ok) {
+                        constexpr int kChunks = D / 8;
+                        const int nz = (kDecodeTokens - nvalid) * kChunks;
+                        for (int idx = threadIdx.x; idx < nz; idx += kConsumerThreads) {
+                            const int r = nvalid + idx / kChunks;
+                            const int ch = idx % kChunks;
+                            *reinterpret_cast<uint4*>(v_half(stage, ch >> 3) + r * 128 +
+                                                      (((ch & 7) ^ (r & swz)) << 4)) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        wrote = true;
+                    }
+                    named_barrier_sync(1, kConsumerThreads);
                 }
+            }
+            if (ok && nvalid > 0 && live_tile) {
                 // S = Q K^T for all 64 tokens (8 n-tiles of 8 tokens).
                 float sc[kSN][4];
 #pragma unroll
@@ -955,14 +1001,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         } else if (!aborted) {
             // A segment that straddles blocks: leave this block's partial
-            // (m, l, acc) for the merge pass.
-            float* slot = a.partials + (int64_t(sp.seg) + cta) * kSlotFloats;
+            // (m, l, acc) of every row tile for the merge pass.
+            float* slot = a.partials + (int64_t(sp.seg) + cta) * kSlotFloats + tw * kTileFloats;
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 const int rw = row0 + rr * 8;
                 if (out_row(sp, rw) < 0)
                     continue;  // padding rows of the tile carry nothing
-                if (warp == 0 && quad == 0) {
+                if (warp % kWPT == 0 && quad == 0) {
                     slot[rw] = m_run[rr];
                     slot[kDecodeRows + rw] = l_run[rr];
                 }
@@ -982,16 +1028,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 // segment (blocks of the other segments return at once). Its per-segment
 // arithmetic repeats the decode kernel's partition, on the inputs only; the
 // partial states are read after the decode grid has completed.
-// Thread -> (row tid / 8, columns c0 .. c0 + D/8): M = max m_k,
-// l = sum l_k 2^(m_k - M), o = sum acc_k 2^(m_k - M) / l, as one running pass.
+// Thread -> (row tid / 8, columns c0 .. c0 + D/8) of each of the segment's
+// row tiles in turn: M = max m_k, l = sum l_k 2^(m_k - M),
+// o = sum acc_k 2^(m_k - M) / l, as one running pass.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int decode_grid)
 {
-    constexpr int kSlotFloats = kDecodeRows * (D + 2);
+    constexpr int kTileFloats = kDecodeRows * (D + 2);
+    const int64_t slot_floats = int64_t(a.TG) * kTileFloats;
     __shared__ long long red[2][4];
     const int tid = threadIdx.x;
     const int seg = blockIdx.x;
-    const int per_req = a.H_kv * a.MT;
+    const int per_req = a.H_kv * a.MS;
     const int b = seg / per_req, hm = seg - b * per_req;
     const int cap = a.max_pages * a.ps;
     auto granules = [&](int q) {
@@ -1031,102 +1079,133 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
 
     const int r = tid >> 3;
     const int c0 = (tid & 7) * (D / 8);
-    const int rg = (hm % a.MT) * kDecodeRows + r;
-    if (rg >= a.R)
-        return;
-    const int g = rg / a.L, i = rg - g * a.L;
-    const int64_t orow = (int64_t(b) * a.H_q + (hm / a.MT) * a.G + g) * a.L + i;
-    const float* base = a.partials + (int64_t(seg) + first) * kSlotFloats;
+    const int ms = hm % a.MS, h = hm / a.MS;
     const int np = int(last - first) + 1;
-    // One pass over the pieces, four in flight, with a running maximum:
-    // M' = max(M, m_k), l = l 2^(M - M') + l_k 2^(m_k - M'), likewise o
-    // (the pieces in order, so repeated calls give the same bits).
-    float Mx = -INFINITY, L2 = 0.f;
-    float fin[D / 8];
+    for (int t = 0; t < a.TG; ++t) {
+        const int rg = (ms * a.TG + t) * kDecodeRows + r;
+        if (rg >= a.R)
+            break;   // this and every later tile row are padding
+        const int g = rg / a.L, i = rg - g * a.L;
+        const int64_t orow = (int64_t(b) * a.H_q + h * a.G + g) * a.L + i;
+        const float* base = a.partials + (int64_t(seg) + first) * slot_floats + t * kTileFloats;
+        // One pass over the pieces, four in flight, with a running maximum:
+        // M' = max(M, m_k), l = l 2^(M - M') + l_k 2^(m_k - M'), likewise o
+        // (the pieces in order, so repeated calls give the same bits).
+        float Mx = -INFINITY, L2 = 0.f;
+        float fin[D / 8];
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c)
-        fin[c] = 0.f;
-    for (int k0 = 0; k0 < np; k0 += 4) {
-        float mk[4], lk[4];
-        float4 v[4][D / 32];
+        for (int c = 0; c < D / 8; ++c)
+            fin[c] = 0.f;
+        for (int k0 = 0; k0 < np; k0 += 4) {
+            float mk[4], lk[4];
+            float4 v[4][D / 32];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const bool live = k0 + u < np;
-            const float* sk = base + int64_t(live ? k0 + u : 0) * kSlotFloats;
-            mk[u] = live ? __ldcg(sk + r) : -INFINITY;
-            lk[u] = live ? __ldcg(sk + kDecodeRows + r) : 0.f;
-            const float4* src = reinterpret_cast<const float4*>(sk + 2 * kDecodeRows + r * D + c0);
+            for (int u = 0; u < 4; ++u) {
+                const bool live = k0 + u < np;
+                const float* sk = base + int64_t(live ? k0 + u : 0) * slot_floats;
+                mk[u] = live ? __ldcg(sk + r) : -INFINITY;
+                lk[u] = live ? __ldcg(sk + kDecodeRows + r) : 0.f;
+                const float4* src =
+                    reinterpret_cast<const float4*>(sk + 2 * kDecodeRows + r * D + c0);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c)
-                v[u][c] = live ? __ldcg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+                for (int c = 0; c < D / 32; ++c)
+                    v[u][c] = live ? __ldcg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (mk[u] == -INFINITY)
-                continue;  // absent piece, or no visible key in it
-            const float Mn = fmaxf(Mx, mk[u]);
-            const float co = Mx == -INFINITY ? 0.f : fast_exp2(Mx - Mn);
-            const float cn = fast_exp2(mk[u] - Mn);
-            Mx = Mn;
-            L2 = L2 * co + lk[u] * cn;
+            for (int u = 0; u < 4; ++u) {
+                if (mk[u] == -INFINITY)
+                    continue;  // absent piece, or no visible key in it
+                const float Mn = fmaxf(Mx, mk[u]);
+                const float co = Mx == -INFINITY ? 0.f : fast_exp2(Mx - Mn);
+                const float cn = fast_exp2(mk[u] - Mn);
+                Mx = Mn;
+                L2 = L2 * co + lk[u] * cn;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                fin[4 * c] = fin[4 * c] * co + cn * v[u][c].x;
-                fin[4 * c + 1] = fin[4 * c + 1] * co + cn * v[u][c].y;
-                fin[4 * c + 2] = fin[4 * c + 2] * co + cn * v[u][c].z;
-                fin[4 * c + 3] = fin[4 * c + 3] * co + cn * v[u][c].w;
+                for (int c = 0; c < D / 32; ++c) {
+                    fin[4 * c] = fin[4 * c] * co + cn * v[u][c].x;
+                    fin[4 * c + 1] = fin[4 * c + 1] * co + cn * v[u][c].y;
+                    fin[4 * c + 2] = fin[4 * c + 2] * co + cn * v[u][c].z;
+                    fin[4 * c + 3] = fin[4 * c + 3] * co + cn * v[u][c].w;
+                }
             }
         }
-    }
-    const float inv = L2 > 0.f ? 1.f / L2 : 0.f;
-    uint16_t* dst = a.out + orow * D + c0;
+        const float inv = L2 > 0.f ? 1.f / L2 : 0.f;
+        uint16_t* dst = a.out + orow * D + c0;
 #pragma unroll
-    for (int c = 0; c < D / 8; c += 8) {
-        uint4 w4;
-        w4.x = pack_bf16x2(fin[c + 0] * inv, fin[c + 1] * inv);
-        w4.y = pack_bf16x2(fin[c + 2] * inv, fin[c + 3] * inv);
-        w4.z = pack_bf16x2(fin[c + 4] * inv, fin[c + 5] * inv);
-        w4.w = pack_bf16x2(fin[c + 6] * inv, fin[c + 7] * inv);
-        *reinterpret_cast<uint4*>(dst + c) = w4;
+        for (int c = 0; c < D / 8; c += 8) {
+            uint4 w4;
+            w4.x = pack_bf16x2(fin[c + 0] * inv, fin[c + 1] * inv);
+            w4.y = pack_bf16x2(fin[c + 2] * inv, fin[c + 3] * inv);
+            w4.z = pack_bf16x2(fin[c + 4] * inv, fin[c + 5] * inv);
+            w4.w = pack_bf16x2(fin[c + 6] * inv, fin[c + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + c) = w4;
+        }
     }
 }
 
 }  // namespace
 
-size_t decode_smem_bytes(int D, int B, bool fp8)
+size_t decode_smem_bytes(int D, int B, bool fp8, int TG)
 {
-    return fp8 ? Layout<128, true>::bytes(B) : D == 64 ? Layout<64>::bytes(B) : Layout<128>::bytes(B);
+    if (fp8)
+        return Layout<128, true>::bytes(B);
+    if (D == 64)
+        return TG == 4 ? Layout<64, false, 4>::bytes(B)
+             : TG == 2 ? Layout<64, false, 2>::bytes(B) : Layout<64>::bytes(B);
+    return TG == 4 ? Layout<128, false, 4>::bytes(B)
+         : TG == 2 ? Layout<128, false, 2>::bytes(B) : Layout<128>::bytes(B);
 }
 
 int decode_max_grid(int sm_count) { return 2 * sm_count; }
 
-size_t decode_workspace_bytes(int64_t nseg, int grid_max, int D)
+size_t decode_workspace_bytes(int64_t nseg, int grid_max, int D, int TG)
 {
     const size_t slots = size_t(nseg) + size_t(grid_max);
-    return slots * kDecodeRows * (D + 2) * 4;
+    return slots * size_t(TG) * kDecodeRows * (D + 2) * 4;
 }
+
+namespace {
+
+using DecodeKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, DecodeArgs);
+
+// The instantiation for (head_dim, e4m3 pages, row tiles per segment), with
+// its index in the table of raised shared-memory limits.
+DecodeKernel decode_kernel_for(int D, bool fp8, int TG, int* index)
+{
+    if (fp8) {
+        *index = 0;
+        return decode_kernel<128, true>;
+    }
+    const int t = TG == 4 ? 2 : TG == 2 ? 1 : 0;
+    *index = 1 + (D == 64 ? 0 : 3) + t;
+    if (D == 64)
+        return t == 2 ? decode_kernel<64, false, 4> : t == 1 ? decode_kernel<64, false, 2>
+                                                              : decode_kernel<64>;
+    return t == 2 ? decode_kernel<128, false, 4> : t == 1 ? decode_kernel<128, false, 2>
+                                                           : decode_kernel<128>;
+}
+
+}  // namespace
 
 cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_map,
                           const CUtensorMap& q_map, const DecodeArgs& a, int grid, int device,
                           cudaStream_t stream)
 {
-    // The dynamic shared-memory limit is raised once per (device, head_dim)
+    // The dynamic shared-memory limit is raised once per (device, kernel)
     // and only grows.
     constexpr int kMaxDev = 64;
-    static std::atomic<int> smem_set[kMaxDev][3];
+    static std::atomic<int> smem_set[kMaxDev][7];
     const bool fp8 = a.fp8 != 0;
-    if (fp8 && a.D != 128)
+    if ((fp8 && (a.D != 128 || a.TG != 1)) || (a.TG != 1 && a.TG != 2 && a.TG != 4))
         return cudaErrorInvalidValue;
-    const int smem = int(decode_smem_bytes(a.D, a.B, fp8));
-    const int di = fp8 ? 2 : a.D == 64 ? 0 : 1;
+    const int smem = int(decode_smem_bytes(a.D, a.B, fp8, a.TG));
+    int di = 0;
+    const DecodeKernel kern = decode_kernel_for(a.D, fp8, a.TG, &di);
     if (device < 0 || device >= kMaxDev)
         return cudaErrorInvalidDevice;
     if (smem_set[device][di].load(std::memory_order_relaxed) < smem) {
-        const void* fn = fp8 ? reinterpret_cast<const void*>(decode_kernel<128, true>)
-                       : a.D == 64 ? reinterpret_cast<const void*>(decode_kernel<64>)
-                                   : reinterpret_cast<const void*>(decode_kernel<128>);
-        cudaError_t e =
-            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
         smem_set[device][di].store(smem, std::memory_order_relaxed);
@@ -1144,16 +1223,13 @@ cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_m
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e =
-        fp8 ? cudaLaunchKernelEx(&cfg, decode_kernel<128, true>, key_map, value_map, q_map, a)
-        : a.D == 64 ? cudaLaunchKernelEx(&cfg, decode_kernel<64>, key_map, value_map, q_map, a)
-                    : cudaLaunchKernelEx(&cfg, decode_kernel<128>, key_map, value_map, q_map, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, key_map, value_map, q_map, a);
     if (e != cudaSuccess || a.whole_segments)
         return e;
     DecodeArgs ma = a;
     ma.piece_units = piece_units(fp8);
     cudaLaunchConfig_t mcfg = cfg;
-    mcfg.gridDim = dim3(unsigned(int64_t(a.B) * a.H_kv * a.MT));
+    mcfg.gridDim = dim3(unsigned(int64_t(a.B) * a.H_kv * a.MS));
     mcfg.blockDim = dim3(128);
     mcfg.dynamicSmemBytes = 0;
     return a.D == 64 ? cudaLaunchKernelEx(&mcfg, decode_merge_kernel<64>, ma, grid)

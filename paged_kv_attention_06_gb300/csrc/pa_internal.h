@@ -55,28 +55,44 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream);
 // ---------------------------------------------------------------------------
 // Split-KV attention (decode schedule)
 
-// Work decomposition: a "segment" is (request b, KV head h, tile mt of 16
-// query rows); its keys are cut into granules of kDecodeTokens tokens. All
-// granules of all segments form one stream that the grid splits evenly; a
-// segment that straddles blocks leaves one partial state per block, merged
-// by a second, small kernel.
+// Work decomposition: the G * L query rows of a (request b, KV head h) are
+// cut into tiles of 16 rows, and a "segment" is (b, h, group of TG
+// consecutive row tiles); its keys are cut into granules of kDecodeTokens
+// tokens, and every K/V granule loaded serves all TG tiles. All granules of
+// all segments form one stream that the grid splits evenly; a segment that
+// straddles blocks leaves one partial state per block, merged by a second,
+// small kernel.
 constexpr int kDecodeTokens = 64;
 constexpr int kDecodeRows = 16;
 
-// At most this many segments per call (request x KV head x 16-row tile).
+// At most this many (request x KV head x 16-row tile) per call.
 constexpr int64_t kMaxSegments = 65536;
+
+// Row tiles per segment and segment count of a decode call: one tile per
+// segment when the rows fit one tile (and always on e4m3 pools), otherwise
+// 2 tiles (2 tiles of rows) or 4 (3 or more; a group of 3 tiles leaves the
+// fourth slot empty).
+struct DecodePlan {
+    int32_t MT;      // 16-row tiles per (request, KV head): ceil(G * L / 16)
+    int32_t TG;      // row tiles per segment: 1, 2 or 4
+    int32_t MS;      // segments per (request, KV head): ceil(MT / TG)
+    int64_t nseg;    // B * H_kv * MS
+};
+DecodePlan decode_plan(const pa_shape& s, bool fp8);
 
 struct DecodeArgs {
     const uint16_t* q;            // [B, H_q, L, D]
     uint16_t* out;                // [B, H_q, L, D]
     const int32_t* block_table;   // [B, max_pages]
     const int32_t* context_lens;  // [B]
-    float* partials;              // [slots][m[16], l[16], acc[16][D]]
+    float* partials;              // [slots][TG][m[16], l[16], acc[16][D]]
     unsigned* err;
     int32_t B, H_q, H_kv, L, D, ps, max_pages, num_pages;
     int32_t G;          // H_q / H_kv
     int32_t R;          // G * L query rows per (request, KV head)
-    int32_t MT;         // ceil(R / 16) row tiles
+    int32_t MS;         // segments per (request, KV head): ceil(ceil(R / 16) / TG)
+    int32_t TG;         // 16-row tiles per segment (1, 2 or 4); tile t of segment
+                        // ms holds rows [16 (ms TG + t), 16 (ms TG + t) + 16) of R
     int32_t box_rows;   // rows per TMA box: min(ps, 64)
     int32_t swz;        // 7: 128B-swizzled stage layout (box_rows >= 8); 0: linear
     int32_t whole_segments;  // 1: every block takes whole segments (no partials)
@@ -92,9 +108,9 @@ struct DecodeArgs {
                                // that nothing arrives at (times out, flags)
 };
 
-size_t decode_smem_bytes(int D, int B, bool fp8 = false);
+size_t decode_smem_bytes(int D, int B, bool fp8 = false, int TG = 1);
 int decode_max_grid(int sm_count);
-size_t decode_workspace_bytes(int64_t nseg, int grid_max, int D);
+size_t decode_workspace_bytes(int64_t nseg, int grid_max, int D, int TG);
 cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_map,
                           const CUtensorMap& q_map, const DecodeArgs& a, int grid, int device,
                           cudaStream_t stream);

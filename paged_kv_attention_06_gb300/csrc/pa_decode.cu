@@ -84,8 +84,9 @@ struct Layout {
     static constexpr int kWorkBytes = F8 ? kConsumerWarps * kDecodeRows * D * 2 : 0;
     static constexpr int kBar = kWork + kWorkBytes;
     static constexpr int kMisc = kBar + 2 * kStages * 8;     // abort flag, test barrier
-    static constexpr int kPrefix = kMisc + 32;               // [B + 1] int32
-    static size_t bytes(int B) { return kPrefix + size_t(B + 1) * 4 + 1024; }
+    // [B + 1] int32 granule prefix, then [B] int32 granules per segment
+    static constexpr int kPrefix = kMisc + 32;
+    static size_t bytes(int B) { return kPrefix + size_t(2 * B + 1) * 4 + 1024; }
 };
 
 __device__ __forceinline__ int clamp_context(int n, int cap, unsigned* err)
@@ -103,29 +104,51 @@ struct SegmentPos {
     int seg_len;        // granules in the segment
 };
 
-// Locates granule x of the stream. pre[b] = first granule of request b.
-__device__ __forceinline__ SegmentPos locate(const int32_t* pre, int B, int per_req, int MS,
-                                             int64_t x)
+// The segment hm (0 <= hm < per_req) of request b. pre[b] = first granule of
+// request b, gbr[b] = granules in each of its segments.
+__device__ __forceinline__ SegmentPos segment_at(const int32_t* pre, const int32_t* gbr,
+                                                 int per_req, int MS, int b, int hm)
 {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {  // largest b with pre[b] <= x
-        int mid = (lo + hi + 1) >> 1;
-        if (pre[mid] <= x)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
     SegmentPos s;
-    s.b = lo;
-    const int gb = (pre[lo + 1] - pre[lo]) / per_req;
-    const int r = int(x - pre[lo]);
-    const int hm = r / gb;
-    s.h = hm / MS;
+    s.b = b;
+    s.h = MS == 1 ? hm : hm / MS;
     s.ms = hm - s.h * MS;
-    s.seg = lo * per_req + hm;
-    s.seg_start = pre[lo] + int64_t(hm) * gb;
-    s.seg_len = gb;
+    s.seg = b * per_req + hm;
+    s.seg_len = gbr[b];
+    s.seg_start = pre[b] + int64_t(hm) * s.seg_len;
     return s;
+}
+
+// The segment after s in the stream (segments are in (request, KV head, row
+// tile group) order and none is empty).
+__device__ __forceinline__ SegmentPos next_segment(const int32_t* pre, const int32_t* gbr,
+                                                   int per_req, int MS, const SegmentPos& s)
+{
+    const int hm = s.seg - s.b * per_req + 1;
+    return hm < per_req ? segment_at(pre, gbr, per_req, MS, s.b, hm)
+                        : segment_at(pre, gbr, per_req, MS, s.b + 1, 0);
+}
+
+// Largest b in [0, B) with key(b) <= u, for a non-decreasing key with
+// key(0) <= u, by the whole warp: each round samples 32 evenly spaced
+// candidates of the remaining range and keeps the last one at or below u, so
+// B <= 32 takes one round (one shared-memory read per lane and a ballot)
+// instead of log2(B) dependent reads.
+template <class Key>
+__device__ __forceinline__ int warp_last_at_most(int B, int64_t u, Key key)
+{
+    const int lane = threadIdx.x & 31;
+    int lo = 0, n = B;
+    while (n > 32) {
+        const int stride = (n + 31) >> 5;
+        const int idx = lo + lane * stride;
+        const bool ok = lane * stride < n && key(idx) <= u;
+        const int last = 31 - __clz(__ballot_sync(0xffffffffu, ok));
+        lo += last * stride;
+        n = min(stride, n - last * stride);
+    }
+    const bool ok = lane < n && key(lo + lane) <= u;
+    return lo + 31 - __clz(__ballot_sync(0xffffffffu, ok));
 }
 
 // The split over blocks weighs each segment as its granules plus pu units
@@ -142,34 +165,43 @@ __device__ __forceinline__ SegmentPos locate(const int32_t* pre, int B, int per_
 // with 3).
 __host__ __device__ constexpr int piece_units(bool f8) { return f8 ? 3 : 1; }
 
+// a / b for 0 <= a, 0 < b: one 32-bit division when both fit (the usual
+// case); a 64-bit integer division is a long dependent instruction sequence,
+// and the block prologue and piece ends lie on the call's critical path.
+__device__ __forceinline__ int64_t udiv64(int64_t a, int64_t b)
+{
+    if (uint64_t(a) <= 0xffffffffull && uint64_t(b) <= 0xffffffffull)
+        return int64_t(uint32_t(a) / uint32_t(b));
+    return a / b;
+}
+
 // Block index that processes the granule at unit position u.
 __device__ __forceinline__ int64_t block_of_unit(int64_t u, int64_t units, int64_t grid)
 {
-    return ((u + 1) * grid - 1) / units;
+    return udiv64((u + 1) * grid - 1, units);
 }
 
-// First granule whose unit position is >= u (granule count if none).
-// pre[b] = first granule of request b; every segment of request b has the
-// same number of granules.
-__device__ __forceinline__ int64_t granule_at_unit(const int32_t* pre, int B, int per_req,
-                                                   int64_t u, int64_t units, int pu)
+// First granule whose unit position is >= u (the granule count if none),
+// and the request b and segment hm within it that hold that granule (b = B
+// if none). Called by whole warps.
+struct StreamPoint {
+    int64_t x;
+    int b, hm;
+};
+__device__ __forceinline__ StreamPoint granule_at_unit(const int32_t* pre, const int32_t* gbr,
+                                                       int B, int per_req, int64_t u,
+                                                       int64_t units, int pu)
 {
     if (u >= units)
-        return pre[B];
-    auto pre_u = [&](int b) { return int64_t(pre[b]) + int64_t(pu) * per_req * b; };
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {  // largest b whose first unit is <= u
-        const int mid = (lo + hi + 1) >> 1;
-        if (pre_u(mid) <= u)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    const int gb = (pre[lo + 1] - pre[lo]) / per_req;
+        return StreamPoint{pre[B], B, 0};
+    const int64_t per_b = int64_t(pu) * per_req;
+    auto pre_u = [&](int b) { return int64_t(pre[b]) + per_b * b; };
+    const int lo = warp_last_at_most(B, u, pre_u);   // request whose units hold u
+    const int gb = gbr[lo];
     const int64_t r = u - pre_u(lo);
-    const int64_t hm = r / (gb + pu);
+    const int64_t hm = udiv64(r, gb + pu);
     const int64_t in = r - hm * (gb + pu) - pu;
-    return pre[lo] + hm * gb + (in > 0 ? in : 0);
+    return StreamPoint{pre[lo] + hm * gb + (in > 0 ? in : 0), lo, int(hm)};
 }
 
 template <int D, bool F8 = false, int TG = 1>
@@ -188,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int32_t* pre = reinterpret_cast<int32_t*>(smem + Lay::kPrefix);
+    int32_t* gbr = pre + a.B + 1;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
     uint64_t* empty = full + kStages;
     volatile int* misc = reinterpret_cast<volatile int*>(smem + Lay::kMisc);
@@ -196,6 +229,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int lane = threadIdx.x & 31;
     const int per_req = a.H_kv * a.MS;
     const int cap = a.max_pages * a.ps;
+
+    // Set-up that reads no input runs before the wait below, overlapping the
+    // tail of the previous kernel in the stream: the pipeline barriers and
+    // the tensor-map prefetch.
+    uint64_t* never = reinterpret_cast<uint64_t*>(smem + Lay::kMisc + 16);
+    if (threadIdx.x == 0) {
+        misc[0] = 0;
+        misc[1] = 0;
+        misc[2] = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        mbar_init(never, 1);
+        fence_barrier_init();
+    }
+    if (warp == kConsumerWarps && lane == 0) {
+        prefetch_tensormap(&key_map);
+        prefetch_tensormap(&value_map);
+        prefetch_tensormap(&q_map);
+    }
 
     // Inputs may come from the previous kernel in the stream (e.g. the append
     // of this step): wait for it before reading any of them, and let the
@@ -213,7 +267,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             int g = 0;
             if (b < a.B) {
                 const int n = clamp_context(a.context_lens[b], cap, a.err);
-                g = max(1, (n + kDecodeTokens - 1) / kDecodeTokens) * per_req;
+                const int gs = max(1, (n + kDecodeTokens - 1) / kDecodeTokens);
+                gbr[b] = gs;
+                g = gs * per_req;
             }
             int incl = g;
 #pragma unroll
@@ -227,17 +283,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             carry += __shfl_sync(0xffffffffu, incl, 31);
         }
     }
-    uint64_t* never = reinterpret_cast<uint64_t*>(smem + Lay::kMisc + 16);
     if (threadIdx.x == 0) {
-        misc[0] = 0;
-        misc[1] = 0;
-        misc[2] = 0;
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
-        }
-        mbar_init(never, 1);
-        fence_barrier_init();
         if (a.debug_unset_wait && blockIdx.x == 0) {
             // Test support: a wait on a barrier nothing arrives at must run
             // out, record the timeout bit and let the kernel finish normally.
@@ -265,25 +311,34 @@ __global__ void __launch_bounds__(kThreads, 2)
                                           : (int64_t(gridDim.x) < units ? int64_t(gridDim.x) : units);
     if (cta >= grid)
         return;
+    // The block's granules [x_begin, x_end) and the segment of x_begin.
     int64_t x_begin, x_end;
+    SegmentPos first;
     if (a.whole_segments) {
         // Whole segments per block: segments [s0, s1) of nseg.
         const int64_t nseg = int64_t(a.B) * per_req;
-        const int64_t s0 = cta * nseg / grid, s1 = (cta + 1) * nseg / grid;
+        const int64_t s0 = udiv64(cta * nseg, grid), s1 = udiv64((cta + 1) * nseg, grid);
         if (s0 >= s1)
             return;
-        auto seg_first = [&](int64_t s) -> int64_t {
-            if (s >= nseg)
-                return total;
-            const int b = int(s / per_req), hm = int(s % per_req);
-            const int gb = (pre[b + 1] - pre[b]) / per_req;
-            return pre[b] + int64_t(hm) * gb;
-        };
-        x_begin = seg_first(s0);
-        x_end = seg_first(s1);
+        const int b0 = int(udiv64(s0, per_req));
+        first = segment_at(pre, gbr, per_req, a.MS, b0, int(s0 - int64_t(b0) * per_req));
+        x_begin = first.seg_start;
+        if (s1 >= nseg) {
+            x_end = total;
+        } else {
+            const int b1 = int(udiv64(s1, per_req));
+            x_end = pre[b1] + (s1 - int64_t(b1) * per_req) * gbr[b1];
+        }
     } else {
-        x_begin = granule_at_unit(pre, a.B, per_req, cta * units / grid, units, kPU);
-        x_end = granule_at_unit(pre, a.B, per_req, (cta + 1) * units / grid, units, kPU);
+        const StreamPoint p0 =
+            granule_at_unit(pre, gbr, a.B, per_req, udiv64(cta * units, grid), units, kPU);
+        const StreamPoint p1 =
+            granule_at_unit(pre, gbr, a.B, per_req, udiv64((cta + 1) * units, grid), units, kPU);
+        x_begin = p0.x;
+        x_end = p1.x;
+        if (x_begin >= x_end)
+            return;
+        first = segment_at(pre, gbr, per_req, a.MS, p0.b, p0.hm);
     }
     if (x_begin >= x_end)
         return;
@@ -297,11 +352,6 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == kConsumerWarps) {
         // ===================== producer warp: page walk + TMA =================
-        if (lane == 0) {
-            prefetch_tensormap(&key_map);
-            prefetch_tensormap(&value_map);
-            prefetch_tensormap(&q_map);
-        }
         const uint64_t policy = l2_policy_evict_first();
         const int box = a.box_rows;
         int stage = 0;
@@ -312,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         // and the next granule's is issued as soon as this one's copies are
         // out, so its loads overlap the wait for a free stage.
         int64_t x = x_begin;
-        while (x < x_end) {
-            const SegmentPos sp = locate(pre, a.B, per_req, a.MS, x);
+        for (SegmentPos sp = first; x < x_end;
+             sp = next_segment(pre, gbr, per_req, a.MS, sp)) {
             const int64_t piece_start = x;
             const int64_t piece_end =
                 x_end < sp.seg_start + sp.seg_len ? x_end : sp.seg_start + sp.seg_len;
@@ -508,8 +558,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint16_t* wtile = reinterpret_cast<uint16_t*>(smem + Lay::kWork);  // [warp][16 rows][D] f16
         const int r_lo = warp * kWT;
         int64_t x = x_begin;
-        while (x < x_end) {
-            const SegmentPos sp = locate(pre, a.B, per_req, a.MS, x);
+        for (SegmentPos sp = first; x < x_end;
+             sp = next_segment(pre, gbr, per_req, a.MS, sp)) {
             const int64_t piece_end = min(x_end, sp.seg_start + sp.seg_len);
             const int n = clamp_context(a.context_lens[sp.b], cap, a.err);
             uint32_t qa[kKS][4];
@@ -731,11 +781,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             named_barrier_sync(1, kConsumerThreads);   // the tile may be refilled
 
-            const bool single =
-                a.whole_segments ||
-                block_of_unit(sp.seg_start + int64_t(kPU) * (sp.seg + 1), units, grid) ==
-                    block_of_unit(sp.seg_start + sp.seg_len - 1 + int64_t(kPU) * (sp.seg + 1),
-                                  units, grid);
+            // The segment lies inside this block's range: no other block
+            // holds a piece of it.
+            const bool single = a.whole_segments ||
+                                (sp.seg_start >= x_begin && sp.seg_start + sp.seg_len <= x_end);
             const bool aborted = misc[0] != 0;
             if (!aborted && single) {
 #pragma unroll
@@ -772,8 +821,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
     int64_t x = x_begin;
-    while (x < x_end) {
-        const SegmentPos sp = locate(pre, a.B, per_req, a.MS, x);
+    for (SegmentPos sp = first; x < x_end; sp = next_segment(pre, gbr, per_req, a.MS, sp)) {
         const int64_t piece_end = min(x_end, sp.seg_start + sp.seg_len);
         const int n = clamp_context(a.context_lens[sp.b], cap, a.err);
 
@@ -979,11 +1027,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
             l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
         }
-        const bool single =
-            a.whole_segments ||
-            block_of_unit(sp.seg_start + int64_t(kPU) * (sp.seg + 1), units, grid) ==
-                block_of_unit(sp.seg_start + sp.seg_len - 1 + int64_t(kPU) * (sp.seg + 1), units,
-                              grid);
+        // The segment lies inside this block's range: no other block holds a
+        // piece of it.
+        const bool single = a.whole_segments ||
+                            (sp.seg_start >= x_begin && sp.seg_start + sp.seg_len <= x_end);
         const bool aborted = misc[0] != 0;
 
         if (!aborted && single) {
@@ -1037,6 +1084,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
     constexpr int kTileFloats = kDecodeRows * (D + 2);
     const int64_t slot_floats = int64_t(a.TG) * kTileFloats;
     __shared__ long long red[2][4];
+    // The next kernel in the stream may be scheduled now; it still waits for
+    // this one to complete before it reads or writes anything.
+    grid_launch_dependents();
     const int tid = threadIdx.x;
     const int seg = blockIdx.x;
     const int per_req = a.H_kv * a.MS;

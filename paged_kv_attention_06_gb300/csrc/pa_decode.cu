@@ -129,28 +129,6 @@ __device__ __forceinline__ SegmentPos next_segment(const int32_t* pre, const int
                         : segment_at(pre, gbr, per_req, MS, s.b + 1, 0);
 }
 
-// Largest b in [0, B) with key(b) <= u, for a non-decreasing key with
-// key(0) <= u, by the whole warp: each round samples 32 evenly spaced
-// candidates of the remaining range and keeps the last one at or below u, so
-// B <= 32 takes one round (one shared-memory read per lane and a ballot)
-// instead of log2(B) dependent reads.
-template <class Key>
-__device__ __forceinline__ int warp_last_at_most(int B, int64_t u, Key key)
-{
-    const int lane = threadIdx.x & 31;
-    int lo = 0, n = B;
-    while (n > 32) {
-        const int stride = (n + 31) >> 5;
-        const int idx = lo + lane * stride;
-        const bool ok = lane * stride < n && key(idx) <= u;
-        const int last = 31 - __clz(__ballot_sync(0xffffffffu, ok));
-        lo += last * stride;
-        n = min(stride, n - last * stride);
-    }
-    const bool ok = lane < n && key(lo + lane) <= u;
-    return lo + 31 - __clz(__ballot_sync(0xffffffffu, ok));
-}
-
 // The split over blocks weighs each segment as its granules plus pu units
 // (DecodeArgs::piece_units): a piece costs a block more than its granules (the
 // first granule's Q tile, the partial tail granule, the epilogue; for e4m3
@@ -165,11 +143,27 @@ __device__ __forceinline__ int warp_last_at_most(int B, int64_t u, Key key)
 // with 3).
 __host__ __device__ constexpr int piece_units(bool f8) { return f8 ? 3 : 1; }
 
-// a / b for 0 <= a, 0 < b: one 32-bit division when both fit (the usual
-// case); a 64-bit integer division is a long dependent instruction sequence,
-// and the block prologue and piece ends lie on the call's critical path.
+// a / b for 0 <= a, 0 < b. When both are below 2^24 (the usual case) the
+// quotient comes from one fp32 division (a and b are exact in fp32, the
+// estimate is within a few units of a / b) and is then corrected to the exact
+// floor; an integer division is a long dependent instruction sequence (about
+// 230 cycles for 32 bits, measured), and the block prologue and the piece
+// ends lie on the call's critical path.
 __device__ __forceinline__ int64_t udiv64(int64_t a, int64_t b)
 {
+    if (uint64_t(a) < (1ull << 24) && uint64_t(b) < (1ull << 24)) {
+        int32_t q = int32_t(__fdividef(float(a), float(b)));
+        int32_t r = int32_t(a) - q * int32_t(b);
+        while (r < 0) {
+            --q;
+            r += int32_t(b);
+        }
+        while (r >= int32_t(b)) {
+            ++q;
+            r -= int32_t(b);
+        }
+        return q;
+    }
     if (uint64_t(a) <= 0xffffffffull && uint64_t(b) <= 0xffffffffull)
         return int64_t(uint32_t(a) / uint32_t(b));
     return a / b;
@@ -183,25 +177,52 @@ __device__ __forceinline__ int64_t block_of_unit(int64_t u, int64_t units, int64
 
 // First granule whose unit position is >= u (the granule count if none),
 // and the request b and segment hm within it that hold that granule (b = B
-// if none). Called by whole warps.
+// if none), for the two unit positions u0 <= u1 at once (the two searches
+// and their divisions interleave). Called by whole warps.
 struct StreamPoint {
     int64_t x;
     int b, hm;
 };
-__device__ __forceinline__ StreamPoint granule_at_unit(const int32_t* pre, const int32_t* gbr,
-                                                       int B, int per_req, int64_t u,
-                                                       int64_t units, int pu)
+__device__ __forceinline__ void granules_at_units(const int32_t* pre, const int32_t* gbr, int B,
+                                                  int per_req, int64_t u0, int64_t u1,
+                                                  int64_t units, int pu, StreamPoint& p0,
+                                                  StreamPoint& p1)
 {
-    if (u >= units)
-        return StreamPoint{pre[B], B, 0};
+    const int lane = threadIdx.x & 31;
     const int64_t per_b = int64_t(pu) * per_req;
     auto pre_u = [&](int b) { return int64_t(pre[b]) + per_b * b; };
-    const int lo = warp_last_at_most(B, u, pre_u);   // request whose units hold u
-    const int gb = gbr[lo];
-    const int64_t r = u - pre_u(lo);
-    const int64_t hm = udiv64(r, gb + pu);
-    const int64_t in = r - hm * (gb + pu) - pu;
-    return StreamPoint{pre[lo] + hm * gb + (in > 0 ? in : 0), lo, int(hm)};
+    // largest b with pre_u(b) <= u, for both u (pre_u(0) = 0 <= u); each
+    // round samples 32 evenly spaced candidates of the remaining range, so
+    // B <= 32 takes one round of one shared-memory read per lane
+    int lo0 = 0, n0 = B, lo1 = 0, n1 = B;
+    while (n0 > 32 || n1 > 32) {
+        const int s0 = (n0 + 31) >> 5, s1 = (n1 + 31) >> 5;
+        const bool ok0 = lane * s0 < n0 && pre_u(lo0 + lane * s0) <= u0;
+        const bool ok1 = lane * s1 < n1 && pre_u(lo1 + lane * s1) <= u1;
+        const int l0 = 31 - __clz(__ballot_sync(0xffffffffu, ok0));
+        const int l1 = 31 - __clz(__ballot_sync(0xffffffffu, ok1));
+        lo0 += l0 * s0;
+        n0 = min(s0, n0 - l0 * s0);
+        lo1 += l1 * s1;
+        n1 = min(s1, n1 - l1 * s1);
+    }
+    const bool ok0 = lane < n0 && pre_u(lo0 + lane) <= u0;
+    const bool ok1 = lane < n1 && pre_u(lo1 + lane) <= u1;
+    lo0 += 31 - __clz(__ballot_sync(0xffffffffu, ok0));
+    lo1 += 31 - __clz(__ballot_sync(0xffffffffu, ok1));
+    auto finish = [&](int lo, int64_t u, StreamPoint& p) {
+        if (u >= units) {
+            p = StreamPoint{pre[B], B, 0};
+            return;
+        }
+        const int gb = gbr[lo];
+        const int64_t r = u - pre_u(lo);
+        const int64_t hm = udiv64(r, gb + pu);
+        const int64_t in = r - hm * (gb + pu) - pu;
+        p = StreamPoint{pre[lo] + hm * gb + (in > 0 ? in : 0), lo, int(hm)};
+    };
+    finish(lo0, u0, p0);
+    finish(lo1, u1, p1);
 }
 
 template <int D, bool F8 = false, int TG = 1>
@@ -251,40 +272,57 @@ __global__ void __launch_bounds__(kThreads, 2)
         prefetch_tensormap(&q_map);
     }
 
-    // Inputs may come from the previous kernel in the stream (e.g. the append
-    // of this step): wait for it before reading any of them, and let the
-    // merge pass that follows this kernel be scheduled right away.
-    grid_dependency_wait();
-    grid_launch_dependents();
-
-    // ---- granule prefix over requests (one warp) ---------------------------
-    if (warp == 0) {
-        int carry = 0;
-        if (lane == 0)
-            pre[0] = 0;
-        for (int base = 0; base < a.B; base += 32) {
-            const int b = base + lane;
-            int g = 0;
-            if (b < a.B) {
-                const int n = clamp_context(a.context_lens[b], cap, a.err);
-                const int gs = max(1, (n + kDecodeTokens - 1) / kDecodeTokens);
-                gbr[b] = gs;
-                g = gs * per_req;
-            }
-            int incl = g;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o)
-                    incl += v;
-            }
-            if (b < a.B)
-                pre[b + 1] = carry + incl;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
+    // The prologue below (granule prefix, this block's range and first
+    // segment) runs twice: first on made-up context lengths (64 granules
+    // each), before the wait for the previous kernel, so that its code
+    // is fetched into the instruction caches while that kernel drains; then,
+    // after the wait, on the real inputs. Only the second pass's results are
+    // used.
+    constexpr int kPU = piece_units(F8);
+    int64_t total = 0, units = 0, grid = 0;
+    const int64_t cta = blockIdx.x;
+    // The block's granules [x_begin, x_end) and the segment of x_begin.
+    int64_t x_begin = 0, x_end = 0;
+    SegmentPos first;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool real = pass == 1;
+        if (real) {
+            // Inputs may come from the previous kernel in the stream (e.g. the
+            // append of this step): wait for it before reading any of them,
+            // and let the merge pass that follows this kernel be scheduled
+            // right away.
+            grid_dependency_wait();
+            grid_launch_dependents();
         }
-    }
-    if (threadIdx.x == 0) {
-        if (a.debug_unset_wait && blockIdx.x == 0) {
+        // ---- granule prefix over requests (one warp) -----------------------
+        if (warp == 0) {
+            int carry = 0;
+            if (lane == 0)
+                pre[0] = 0;
+            for (int base = 0; base < a.B; base += 32) {
+                const int b = base + lane;
+                int g = 0;
+                if (b < a.B) {
+                    const int n =
+                        real ? clamp_context(a.context_lens[b], cap, a.err) : 64 * kDecodeTokens;
+                    const int gs = max(1, (n + kDecodeTokens - 1) / kDecodeTokens);
+                    gbr[b] = gs;
+                    g = gs * per_req;
+                }
+                int incl = g;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o)
+                        incl += v;
+                }
+                if (b < a.B)
+                    pre[b + 1] = carry + incl;
+                carry += __shfl_sync(0xffffffffu, incl, 31);
+            }
+        }
+        if (real && threadIdx.x == 0 && a.debug_unset_wait && blockIdx.x == 0) {
             // Test support: a wait on a barrier nothing arrives at must run
             // out, record the timeout bit and let the kernel finish normally.
             // The whole block waits for it below, before any copy is issued.
@@ -296,49 +334,45 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         }
-    }
-    __syncthreads();
+        __syncthreads();
 
-    constexpr int kPU = piece_units(F8);
-    const int64_t total = pre[a.B];
-    const int64_t units = total + int64_t(kPU) * a.B * per_req;
-    const int64_t cta = blockIdx.x;
-    // The unit stream is split over min(gridDim.x, units) blocks so that every
-    // block in use owns at least one unit; a segment whose granules span
-    // blocks first..last then has exactly last - first + 1 pieces (every
-    // block in between owns units inside the segment's granules).
-    const int64_t grid = a.whole_segments ? int64_t(gridDim.x)
-                                          : (int64_t(gridDim.x) < units ? int64_t(gridDim.x) : units);
-    if (cta >= grid)
-        return;
-    // The block's granules [x_begin, x_end) and the segment of x_begin.
-    int64_t x_begin, x_end;
-    SegmentPos first;
-    if (a.whole_segments) {
-        // Whole segments per block: segments [s0, s1) of nseg.
-        const int64_t nseg = int64_t(a.B) * per_req;
-        const int64_t s0 = udiv64(cta * nseg, grid), s1 = udiv64((cta + 1) * nseg, grid);
-        if (s0 >= s1)
-            return;
-        const int b0 = int(udiv64(s0, per_req));
-        first = segment_at(pre, gbr, per_req, a.MS, b0, int(s0 - int64_t(b0) * per_req));
-        x_begin = first.seg_start;
-        if (s1 >= nseg) {
-            x_end = total;
-        } else {
-            const int b1 = int(udiv64(s1, per_req));
-            x_end = pre[b1] + (s1 - int64_t(b1) * per_req) * gbr[b1];
+        total = pre[a.B];
+        units = total + int64_t(kPU) * a.B * per_req;
+        // The unit stream is split over min(gridDim.x, units) blocks so that
+        // every block in use owns at least one unit; a segment whose granules
+        // span blocks first..last then has exactly last - first + 1 pieces
+        // (every block in between owns units inside the segment's granules).
+        grid = a.whole_segments ? int64_t(gridDim.x)
+                                : (int64_t(gridDim.x) < units ? int64_t(gridDim.x) : units);
+        x_begin = x_end = 0;
+        if (cta < grid) {
+            if (a.whole_segments) {
+                // Whole segments per block: segments [s0, s1) of nseg.
+                const int64_t nseg = int64_t(a.B) * per_req;
+                const int64_t s0 = udiv64(cta * nseg, grid), s1 = udiv64((cta + 1) * nseg, grid);
+                if (s0 < s1) {
+                    const int b0 = int(udiv64(s0, per_req));
+                    first = segment_at(pre, gbr, per_req, a.MS, b0, int(s0 - int64_t(b0) * per_req));
+                    x_begin = first.seg_start;
+                    if (s1 >= nseg) {
+                        x_end = total;
+                    } else {
+                        const int b1 = int(udiv64(s1, per_req));
+                        x_end = pre[b1] + (s1 - int64_t(b1) * per_req) * gbr[b1];
+                    }
+                }
+            } else {
+                StreamPoint p0, p1;
+                granules_at_units(pre, gbr, a.B, per_req, udiv64(cta * units, grid),
+                                  udiv64((cta + 1) * units, grid), units, kPU, p0, p1);
+                x_begin = p0.x;
+                x_end = p1.x;
+                if (x_begin < x_end)
+                    first = segment_at(pre, gbr, per_req, a.MS, p0.b, p0.hm);
+            }
         }
-    } else {
-        const StreamPoint p0 =
-            granule_at_unit(pre, gbr, a.B, per_req, udiv64(cta * units, grid), units, kPU);
-        const StreamPoint p1 =
-            granule_at_unit(pre, gbr, a.B, per_req, udiv64((cta + 1) * units, grid), units, kPU);
-        x_begin = p0.x;
-        x_end = p1.x;
-        if (x_begin >= x_end)
-            return;
-        first = segment_at(pre, gbr, per_req, a.MS, p0.b, p0.hm);
+        if (!real)
+            __syncthreads();   // pass 0's tables are read by every warp before pass 1 rewrites them
     }
     if (x_begin >= x_end)
         return;
@@ -1075,15 +1109,20 @@ __global__ void __launch_bounds__(kThreads, 2)
 // segment (blocks of the other segments return at once). Its per-segment
 // arithmetic repeats the decode kernel's partition, on the inputs only; the
 // partial states are read after the decode grid has completed.
-// Thread -> (row tid / 8, columns c0 .. c0 + D/8) of each of the segment's
+// Thread -> (row tid / 16, columns c0 .. c0 + D/16) of each of the segment's
 // row tiles in turn: M = max m_k, l = sum l_k 2^(m_k - M),
-// o = sum acc_k 2^(m_k - M) / l, as one running pass.
+// o = sum acc_k 2^(m_k - M) / l, as one running pass over the pieces with
+// up to eight of them in flight.
+constexpr int kMergeThreads = 256;
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, int decode_grid)
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeArgs a, int decode_grid)
 {
     constexpr int kTileFloats = kDecodeRows * (D + 2);
+    constexpr int kCols = D / 16;              // output columns per thread (4 or 8)
+    constexpr int kVec = kCols / 4;            // float4 per piece and thread
+    constexpr int kFly = 8;                    // pieces in flight
     const int64_t slot_floats = int64_t(a.TG) * kTileFloats;
-    __shared__ long long red[2][4];
+    __shared__ long long red[2][kMergeThreads / 32];
     // The next kernel in the stream may be scheduled now; it still waits for
     // this one to complete before it reads or writes anything.
     grid_launch_dependents();
@@ -1114,8 +1153,12 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
         red[1][tid >> 5] = before;
     }
     __syncthreads();
-    total = red[0][0] + red[0][1] + red[0][2] + red[0][3];
-    before = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+    total = before = 0;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) {
+        total += red[0][w];
+        before += red[1][w];
+    }
     const int gb = granules(b);
     const int64_t seg_start = before + int64_t(hm) * gb;
     const int64_t units = total + int64_t(a.piece_units) * a.B * per_req;
@@ -1127,8 +1170,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
         return;  // finished and written by one decode block
     grid_dependency_wait();  // the decode grid has completed: its partials are visible
 
-    const int r = tid >> 3;
-    const int c0 = (tid & 7) * (D / 8);
+    const int r = tid >> 4;
+    const int c0 = (tid & 15) * kCols;
     const int ms = hm % a.MS, h = hm / a.MS;
     const int np = int(last - first) + 1;
     for (int t = 0; t < a.TG; ++t) {
@@ -1138,19 +1181,18 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
         const int g = rg / a.L, i = rg - g * a.L;
         const int64_t orow = (int64_t(b) * a.H_q + h * a.G + g) * a.L + i;
         const float* base = a.partials + (int64_t(seg) + first) * slot_floats + t * kTileFloats;
-        // One pass over the pieces, four in flight, with a running maximum:
         // M' = max(M, m_k), l = l 2^(M - M') + l_k 2^(m_k - M'), likewise o
         // (the pieces in order, so repeated calls give the same bits).
         float Mx = -INFINITY, L2 = 0.f;
-        float fin[D / 8];
+        float fin[kCols];
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c)
+        for (int c = 0; c < kCols; ++c)
             fin[c] = 0.f;
-        for (int k0 = 0; k0 < np; k0 += 4) {
-            float mk[4], lk[4];
-            float4 v[4][D / 32];
+        for (int k0 = 0; k0 < np; k0 += kFly) {
+            float mk[kFly], lk[kFly];
+            float4 v[kFly][kVec];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kFly; ++u) {
                 const bool live = k0 + u < np;
                 const float* sk = base + int64_t(live ? k0 + u : 0) * slot_floats;
                 mk[u] = live ? __ldcg(sk + r) : -INFINITY;
@@ -1158,11 +1200,11 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
                 const float4* src =
                     reinterpret_cast<const float4*>(sk + 2 * kDecodeRows + r * D + c0);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c)
+                for (int c = 0; c < kVec; ++c)
                     v[u][c] = live ? __ldcg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kFly; ++u) {
                 if (mk[u] == -INFINITY)
                     continue;  // absent piece, or no visible key in it
                 const float Mn = fmaxf(Mx, mk[u]);
@@ -1171,7 +1213,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
                 Mx = Mn;
                 L2 = L2 * co + lk[u] * cn;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < kVec; ++c) {
                     fin[4 * c] = fin[4 * c] * co + cn * v[u][c].x;
                     fin[4 * c + 1] = fin[4 * c + 1] * co + cn * v[u][c].y;
                     fin[4 * c + 2] = fin[4 * c + 2] * co + cn * v[u][c].z;
@@ -1182,14 +1224,10 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a, i
         const float inv = L2 > 0.f ? 1.f / L2 : 0.f;
         uint16_t* dst = a.out + orow * D + c0;
 #pragma unroll
-        for (int c = 0; c < D / 8; c += 8) {
-            uint4 w4;
-            w4.x = pack_bf16x2(fin[c + 0] * inv, fin[c + 1] * inv);
-            w4.y = pack_bf16x2(fin[c + 2] * inv, fin[c + 3] * inv);
-            w4.z = pack_bf16x2(fin[c + 4] * inv, fin[c + 5] * inv);
-            w4.w = pack_bf16x2(fin[c + 6] * inv, fin[c + 7] * inv);
-            *reinterpret_cast<uint4*>(dst + c) = w4;
-        }
+        for (int c = 0; c < kCols; c += 4)   // 4 bf16 (8 bytes) at a time
+            *reinterpret_cast<uint2*>(dst + c) =
+                make_uint2(pack_bf16x2(fin[c + 0] * inv, fin[c + 1] * inv),
+                           pack_bf16x2(fin[c + 2] * inv, fin[c + 3] * inv));
     }
 }
 
@@ -1280,7 +1318,7 @@ cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_m
     ma.piece_units = piece_units(fp8);
     cudaLaunchConfig_t mcfg = cfg;
     mcfg.gridDim = dim3(unsigned(int64_t(a.B) * a.H_kv * a.MS));
-    mcfg.blockDim = dim3(128);
+    mcfg.blockDim = dim3(kMergeThreads);
     mcfg.dynamicSmemBytes = 0;
     return a.D == 64 ? cudaLaunchKernelEx(&mcfg, decode_merge_kernel<64>, ma, grid)
                      : cudaLaunchKernelEx(&mcfg, decode_merge_kernel<128>, ma, grid);

@@ -392,11 +392,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait(kPVDone, j & 1))
                     break;
                 tc_fence_after();
-                if (more)
+                if (more) {
                     s_mmas(0, j + 1);
-                ok = wait(kPFull + 1, j & 1);
-                if (more)
                     commit(kSFull);
+                }
+                ok = wait(kPFull + 1, j & 1);
                 if (!ok)
                     break;
                 // head 1: P_1 V_j, then S_1 for tile j + 1
@@ -409,11 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (more) {
                     tc_fence_after();
                     s_mmas(1, j + 1);
-                    // the next tile's V and the tile after's K, before the commit
-                    ok = wait(kVFull + ((j + 1) & 1), ((j + 1) >> 1) & 1) &&
-                         (j + 2 >= nt || wait(kKFull + (j & 1), ((j + 2) >> 1) & 1));
                     commit(kSFull + 1);
                     commit(kKEmpty + ((j + 1) & 1));
+                    // the next tile's V and the tile after's K
+                    ok = wait(kVFull + ((j + 1) & 1), ((j + 1) >> 1) & 1) &&
+                         (j + 2 >= nt || wait(kKFull + (j & 1), ((j + 2) >> 1) & 1));
                 }
             }
             // Every MMA issued completes before the block ends.

@@ -143,11 +143,12 @@ __device__ __forceinline__ int combo_tiles(const SplitPrefillArgs& a, int m, int
 
 // Units of the stream: a K/V tile weighs kTileUnits, and an item adds
 // kItemUnits ahead of its first tile for what a piece costs besides its
-// tiles (its Q tiles, the epilogue, the restart of the chain); an item with
-// no visible key weighs kEmptyUnits. A tile belongs to the block whose range
+// tiles (its Q tiles, the epilogue, the restart of the chain: about two
+// tiles' time, measured per piece on the 512-row batch); an item with no
+// visible key weighs kEmptyUnits. A tile belongs to the block whose range
 // holds its first unit.
 constexpr int kTileUnits = 4;
-constexpr int kItemUnits = 3;
+constexpr int kItemUnits = 8;
 constexpr int kEmptyUnits = 1;
 
 __device__ __forceinline__ int64_t item_units(int nt)

@@ -891,8 +891,9 @@ def bench_decode_config(name, pa, binding, torch, device, stream, steps, warmup=
     return res
 
 
-def dispatch_sweep(torch, device, Ls=(1, 2, 4, 8, 12, 16, 24, 32, 64), ctxs=(1024, 4096),
-                   groups=((28, 4), (32, 8)), B=32, page_size=16, copies=4, calls=16):
+def dispatch_sweep(torch, device, Ls=(1, 2, 4, 8, 12, 16, 24, 32, 48, 64, 96, 128),
+                   ctxs=(1024, 4096), groups=((28, 4), (32, 8), (8, 8)), B=32, page_size=16,
+                   copies=4, calls=16):
     """Time pa_decode and pa_prefill on the same inputs for query chunks of L
     rows (both are correct for every L): the data behind the L threshold of
     pa_attention_route. Each timing is a CUDA graph of `calls` calls over

@@ -289,9 +289,9 @@ pa_status pa_prefill_fp8(const void *query, const void *key_pages, const void *v
                          size_t workspace_bytes, void *stream);
 
 /*
- * The dispatch of pa_attention for e4m3 pools: pa_decode_fp8 where
- * pa_attention_route gives 0 (query rows <= 8), pa_prefill_fp8 otherwise,
- * with the same arguments. The workspace is the one that call takes, at
+ * The dispatch of pa_attention for e4m3 pools: pa_decode_fp8 for query rows
+ * L <= 8 (the page's rule: the e4m3 decode reads K/V once per 16-row tile of
+ * a KV group), pa_prefill_fp8 otherwise, with the same arguments. The workspace is the one that call takes, at
  * least pa_attention_fp8_workspace_bytes(shape, max_context_len) bytes,
  * 256-byte aligned (0 bytes: invalid shape or head_dim other than 128).
  */
@@ -344,7 +344,11 @@ pa_status pa_prefill_split(const void *query, const void *key_pages,
  * Route chosen by pa_attention for these sizes: 0 = decode, 1 = prefill.
  * The rule sits at this boundary (Week 3 Day 4, "Choose a Schedule for Each
  * Query Shape": short queries take the vector decode schedule, long ones the
- * page-walking prefill; no dense fallback). Returns -1 on invalid shapes.
+ * page-walking prefill; no dense fallback). The thresholds are this
+ * library's, set by timing both kernels on GB300 (the page's own rule,
+ * L <= 8, was set on other hardware): decode for L <= 16, and for L <= 32
+ * when num_q_heads / num_kv_heads >= 4; prefill otherwise. Returns -1 on
+ * invalid shapes.
  */
 int32_t pa_attention_route(pa_shape shape, int32_t max_context_len);
 

@@ -647,9 +647,23 @@ pa_status pa_prefill_fp8(const void* query, const void* key_pages, const void* v
                           p.split_bytes ? w + p.split_off : nullptr, p.split_bytes, v_scale);
 }
 
+namespace {
+
+// Route of pa_attention_fp8: the e4m3 decode kernel carries one 16-row tile
+// per segment (its K/V are read once per tile), so it takes query chunks of
+// at most 8 rows per request, the rule of Week 3 Day 4, "Task 2".
+int32_t route_fp8(const pa_shape& shape)
+{
+    if (shape.q_len <= 0)
+        return -1;
+    return shape.q_len <= 8 ? 0 : 1;
+}
+
+}  // namespace
+
 size_t pa_attention_fp8_workspace_bytes(pa_shape shape, int32_t max_context_len)
 {
-    const int32_t route = pa_attention_route(shape, max_context_len);
+    const int32_t route = route_fp8(shape);
     if (route < 0 || shape.head_dim != 128)
         return 0;
     return route == 0 ? pa_decode_workspace_bytes(shape)
@@ -662,7 +676,7 @@ pa_status pa_attention_fp8(const void* query, const void* key_pages, const void*
                            int causal, void* out, pa_shape shape, int32_t max_context_len,
                            void* workspace, size_t workspace_bytes, void* stream)
 {
-    const int32_t route = pa_attention_route(shape, max_context_len);
+    const int32_t route = route_fp8(shape);
     if (route < 0)
         return PA_ERR_INVALID_ARG;
     if (route == 0)
@@ -884,9 +898,16 @@ pa_status pa_prefill_split(const void* query, const void* key_pages, const void*
 int32_t pa_attention_route(pa_shape shape, int32_t max_context_len)
 {
     (void)max_context_len;
-    if (shape.q_len <= 0)
+    if (shape.q_len <= 0 || shape.num_q_heads <= 0 || shape.num_kv_heads <= 0)
         return -1;
-    return shape.q_len <= 8 ? 0 : 1;
+    // The split-KV decode reads a KV group's K/V once per 64 of its query
+    // rows (four 16-row tiles per segment), the tile prefill once per 128-row
+    // tile of each head pair at a fixed cost per tile. Measured crossover on
+    // GB300 (32 requests, contexts of 1k and 4k tokens, page size 16): decode
+    // is faster up to 16 rows per request for every group size, and up to 32
+    // rows when a KV group has 4 or more query heads.
+    const int32_t G = shape.num_q_heads / shape.num_kv_heads;
+    return shape.q_len <= 16 || (shape.q_len <= 32 && G >= 4) ? 0 : 1;
 }
 
 pa_status pa_attention(const void* query, const void* key_pages, const void* value_pages,

@@ -117,3 +117,19 @@ def test_prefill_route_head_dim64_whole_segments(L, causal):
     check_no_device_error()
     kp, vp = oracle_pages(b)
     assert_close(host_f64(out), oracle_out(b, kp, vp), f"prefill D=64 L={L}")
+
+
+@pytest.mark.parametrize("L,H_q,H_kv", [(12, 28, 4), (24, 28, 4), (32, 32, 8), (16, 8, 8)])
+def test_attention_routes_short_chunks_to_decode(L, H_q, H_kv):
+    """pa_attention sends these chunk lengths to the decode schedule (the
+    GB300 thresholds: L <= 16, or L <= 32 with 4 or more query heads per KV
+    group) and the result matches the oracle on every row."""
+    import paged_kv_attention_06_gb300 as pa
+    b = _batch(16, H_q, H_kv, 128, L, True, B=6, seed=L)
+    db = DeviceBatch(b)
+    shape = pa.make_shape(db.query.shape, db.key_pages.shape, db.block_table.shape[1])
+    assert int(pa.binding._lib.pa_attention_route(shape, int(b.context_lens.max()))) == 0
+    out = gpu_step(db, route="attention")
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), f"pa_attention L={L} G={H_q // H_kv}")

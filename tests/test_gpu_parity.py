@@ -114,7 +114,7 @@ def test_prefill_lengths(L, causal, ps):
     b = wl.build_batch("prefill", B=B, H_q=8, H_kv=2, D=128, page_size=ps, L=L,
                        context_lens=lens, seed=3 * L + ps, causal=causal, placement="churn")
     db = DeviceBatch(b)
-    out = gpu_step(db)            # pa_attention routes L > 8 to prefill
+    out = gpu_step(db, route="prefill")
     check_no_device_error()
     kp, vp = oracle_pages(b)
     assert_close(host_f64(out), oracle_out(b, kp, vp), f"prefill L={L} ps={ps}")

@@ -339,7 +339,7 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
         if (e == cudaErrorCooperativeLaunchTooLarge && !pending)
             (void)cudaGetLastError();
     }
-    cudaError_t e = pairs ? launch_prefill_pairs(qmap, kmap, vmap, a, dev->id, stream)
+    cudaError_t e = pairs ? launch_prefill_pairs(qmap, kmap, vmap, a, dev->id, dev->sm_count, stream)
                           : launch_prefill(qmap, kmap, vmap, a, dev->id, stream);
     if (pairs && e == cudaErrorNotSupported)   // register split not available: one head per block
         e = launch_prefill(qmap, kmap, vmap, a, dev->id, stream);

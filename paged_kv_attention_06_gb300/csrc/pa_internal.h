@@ -188,7 +188,7 @@ size_t prefill_smem_bytes();
 size_t prefill_pairs_smem_bytes();
 cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& key_map,
                                  const CUtensorMap& value_map, const PrefillArgs& a, int device,
-                                 cudaStream_t stream);
+                                 int sm_count, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& q_map, const CUtensorMap& key_map,
                            const CUtensorMap& value_map, const PrefillArgs& a, int device,
                            cudaStream_t stream);

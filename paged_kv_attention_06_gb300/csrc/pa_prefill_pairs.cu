@@ -14,19 +14,27 @@
 // one K/V tile serves two independent 128-row score tiles, and the MMAs of
 // one head run while the other head's softmax works.
 //
-// Schedule (one block per (request, pair of query heads of one KV group,
-// tile of 128 query rows), tiles with the most K/V tiles launched first):
-//   * warps 0, 2, 3 (loaders): TMA loads of both Q tiles (once) and of K and
-//     V tiles of 128 keys page by page (one box of min(page_size, 128) rows x
-//     64 columns per page and half, the boxes split over the three warps),
-//     two K and two V stages released separately;
+// Schedule: an item is (request, pair of query heads of one KV group, tile of
+// 128 query rows). Items are ranked by the number of K/V tiles they visit,
+// most first, and one block per SM takes them in that order as a snake
+// (block c takes ranks c, 2G - 1 - c, 2G + c, ...; G blocks), the
+// longest-first packing, keeping one pipeline running across its items: the
+// next item's Q and K/V tiles load while the current item's last tiles are
+// in flight, and its first scores are computed while the softmax warps write
+// out the current item.
+//   * warps 0, 2, 3 (loaders): per item, the K and V tiles of 128 keys page by
+//     page (one box of min(page_size, 128) rows x 64 columns per page and
+//     half, the boxes split over the three warps), two K and two V stages
+//     released separately and shared by all items; warps 0 and 2 also load
+//     head 0's and head 1's Q tile of each item, into a buffer per head that
+//     is free once that head's last S of the item before has completed;
 //   * warp 1 (one thread): tcgen05.mma kind::f16, M = 128, fp32 accumulate:
 //     S_h = Q_h K^T (N = 128 keys; an N = 64 MMA takes as long as N = 128)
 //     into head h's score buffer in TMEM, and O_h += P_h V (N = 128 =
 //     head_dim) with P_h read from TMEM. An MMA issue returns only about as
 //     fast as the tensor core executes it, so every wait of this thread is
 //     time the tensor core idles; the order per tile j is P_0 V_j, S_0 for
-//     tile j + 1, P_1 V_j, S_1 for tile j + 1;
+//     tile j + 1, P_1 V_j, S_1 for tile j + 1, each S committed at once;
 //   * warps 4-7 (head 0) and 8-11 (head 1): one thread per query row (TMEM
 //     lane), the online-softmax fold with a lazily moved maximum (O and the
 //     running sum are rescaled only when a tile's maximum exceeds the one in
@@ -34,13 +42,15 @@
 //     so the result is the same softmax). P (bf16, two per 32-bit column) is
 //     written over the upper 64 columns of the head's score buffer. V rows
 //     past the context are zeroed (by head 0's warps) before either P V. At
-//     the end O / l -> bf16.
+//     the end of an item O / l -> bf16, through a staging buffer per warp.
 //
 // TMEM (512 columns): S_0 [0, 128), S_1 [128, 256), O_0 [256, 384),
 // O_1 [384, 512). A score buffer holds P_h(j) until P_h(j) V_j completes;
 // S_h(j + 1) is issued only after that completion has been observed, and
 // its commit also covers P_h(j) V_j, so a softmax thread that sees S_h(j + 1)
-// may rescale O_h without another wait.
+// may rescale O_h without another wait. An item's first P_h V overwrites O_h;
+// it is issued after the softmax warps of head h arrive for that tile, which
+// they do after writing out the item before.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -68,29 +78,43 @@ __host__ __device__ constexpr uint32_t col_s(int head) { return uint32_t(head * 
 __host__ __device__ constexpr uint32_t col_o(int head) { return uint32_t(256 + head * 128); }
 constexpr uint32_t kPCol = 64;        // P_h: columns [64, 128) of head h's score buffer
 
+// Items a block can take; the host sizes the grid so that no block gets more.
+constexpr int kMaxItems = 32;
+
 struct Layout {
     static constexpr int kHalf = 128 * 128;        // 128 rows x 64 bf16 (128 B)
     static constexpr int kMat = 2 * kHalf;         // 128 x 128 bf16, [half][row][128 B]
     static constexpr int kQ = 0;                   // [head] matrices
     static constexpr int kK = kQ + 2 * kMat;       // 2 stages
     static constexpr int kV = kK + 2 * kMat;       // 2 stages
-    static constexpr int kBar = kV + 2 * kMat;
-    static constexpr int kNumBars = 16;
+    // output staging, 4 KiB per softmax warp (the item ranking uses it first)
+    static constexpr int kStage = kV + 2 * kMat;
+    static constexpr int kStageWarp = 4096;
+    static constexpr int kItems = kStage + 8 * kStageWarp;   // [kMaxItems][8] int32
+    static constexpr int kBar = kItems + kMaxItems * 8 * 4;
+    static constexpr int kNumBars = 20;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kMisc = kTmemSlot + 16;
     static constexpr int kBytes = kMisc + 16 + 1024;   // + alignment slack
 };
 
 // Barrier indices.
-constexpr int kQFull = 0;
-constexpr int kKFull = 1;     // + stage (2)
-constexpr int kKEmpty = 3;    // + stage
-constexpr int kVFull = 5;     // + stage
-constexpr int kVEmpty = 7;    // + stage
-constexpr int kSFull = 9;     // + head (2)
-constexpr int kPFull = 11;    // + head
-constexpr int kPVDone = 13;   // + head
-constexpr int kMmaDone = 15;
+constexpr int kQFull = 0;     // + head (2)
+constexpr int kQEmpty = 2;    // + head
+constexpr int kKFull = 4;     // + stage (2)
+constexpr int kKEmpty = 6;    // + stage
+constexpr int kVFull = 8;     // + stage
+constexpr int kVEmpty = 10;   // + stage
+constexpr int kSFull = 12;    // + head (2)
+constexpr int kPFull = 14;    // + head
+constexpr int kPVDone = 16;   // + head
+constexpr int kMmaDone = 18;
+static_assert(kMmaDone < Layout::kNumBars, "barrier count");
+
+// Item table entry: request, query tile, the two query heads, the KV head,
+// the (clamped) context length, K/V tiles visited, whether head 1 repeats
+// head 0.
+enum { kEB = 0, kET, kEH0, kEH1, kEHK, kEN, kENT, kEDup };
 
 // Operand descriptors (128B swizzle). K-major [half][128 rows][128 B] (Q, K):
 // k-step kk (16 elements along K) starts kmajor_off(kk) bytes in. MN-major
@@ -121,40 +145,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Layout::kBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Layout::kTmemSlot);
     volatile int* misc = reinterpret_cast<volatile int*>(smem + Layout::kMisc);
+    int32_t* items = reinterpret_cast<int32_t*>(smem + Layout::kItems);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- which tile -----------------------------------------------------------
-    // Blocks go out in order of rank: the (request, query tile) pairs sorted by
-    // the number of K/V tiles they visit, most first (the longest-job-first
-    // order for the block scheduler), then the head pairs of each. Every block
-    // ranks all pairs itself (one thread per pair) when there are at most
+    // ---- this block's items ---------------------------------------------------
+    // Items in rank order: the (request, query tile) pairs sorted by the number
+    // of K/V tiles they visit, most first, then the head pairs of each. Every
+    // block ranks all pairs itself (one thread per pair) when there are at most
     // kThreads of them; beyond that, query tiles are taken last to first.
     // Head pairs: ceil(G / 2) per KV group; with an odd group size the last
     // pair of each group holds its last head twice (computed by both softmax
-    // warpgroups, written by the first only).
+    // warpgroups, written by the first only). Block c takes the items of rank
+    // c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... (G blocks).
     const int per_group = kOdd ? (a.G + 1) / 2 : a.G / 2;
     const int pairs = a.H_kv * per_group;
     const int cap = a.max_pages * a.ps;
-    const int rank = int(blockIdx.x / pairs);
-    const int hp = int(blockIdx.x % pairs);
     const int M = a.B * a.n_qtiles;
-    int b, t;
+    const int64_t n_all = int64_t(M) * pairs;
+    const int64_t nblk = gridDim.x, c = blockIdx.x;
+    auto item_at = [&](int k) -> int64_t {   // k-th item of this block
+        const int64_t w = k >> 1;
+        return (k & 1) ? (2 * w + 2) * nblk - 1 - c : 2 * w * nblk + c;
+    };
+    int n_items = 0;
+    while (n_items < kMaxItems && item_at(n_items) < n_all)
+        ++n_items;
+    auto tiles_for = [&](int bb, int tt, int* n_out) {
+        int nn = a.context_lens[bb];
+        nn = nn < 0 ? 0 : (nn > cap ? cap : nn);
+        const int r0 = tt * kRows;
+        const int pl = nn - a.L + r0 + min(kRows, a.L - r0) - 1;
+        int nk = a.causal ? min(nn, pl + 1) : nn;
+        nk = nk < 0 ? 0 : nk;
+        *n_out = nn;
+        return (nk + kKeys - 1) / kKeys;
+    };
+    int* order = reinterpret_cast<int*>(smem + Layout::kStage);   // scratch until the epilogues
     if (M <= kThreads) {
-        __shared__ int tiles_of[kThreads];
-        __shared__ int order[kThreads];
-        auto tiles_for = [&](int bb, int tt) {
-            int nn = a.context_lens[bb];
-            nn = nn < 0 ? 0 : (nn > cap ? cap : nn);
-            const int r0 = tt * kRows;
-            const int pl = nn - a.L + r0 + min(kRows, a.L - r0) - 1;
-            int nk = a.causal ? min(nn, pl + 1) : nn;
-            nk = nk < 0 ? 0 : nk;
-            return (nk + kKeys - 1) / kKeys;
-        };
+        int* tiles_of = order + kThreads;
         const int m = threadIdx.x;
+        int nn;
         if (m < M)
-            tiles_of[m] = tiles_for(m / a.n_qtiles, m % a.n_qtiles);
+            tiles_of[m] = tiles_for(m / a.n_qtiles, m % a.n_qtiles, &nn);
         __syncthreads();
         if (m < M) {
             const int w = tiles_of[m];
@@ -166,36 +199,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             order[rk] = m;
         }
         __syncthreads();
-        const int combo = order[rank];
-        b = combo / a.n_qtiles;
-        t = combo - b * a.n_qtiles;
-    } else {
-        t = a.n_qtiles - 1 - rank / a.B;
-        b = rank - (rank / a.B) * a.B;
     }
-    int hk, hq0;
-    if constexpr (kOdd) {
-        hk = hp / per_group;                     // KV group
-        hq0 = hk * a.G + 2 * (hp - hk * per_group);
-    } else {
-        hq0 = 2 * hp;
-        hk = hq0 / a.G;
-    }
-    const bool dup = kOdd && hq0 + 1 == (hk + 1) * a.G;  // odd group: one head, twice
-    const int hq1 = dup ? hq0 : hq0 + 1;         // heads hq0, hq1 (same KV group)
-    int n = a.context_lens[b];
-    if (n < 0 || n > cap) {
-        if (threadIdx.x == 0)
+    if (int(threadIdx.x) < n_items) {
+        const int64_t i = item_at(int(threadIdx.x));
+        const int rank = int(i / pairs);
+        const int hp = int(i - int64_t(rank) * pairs);
+        int b, t;
+        if (M <= kThreads) {
+            const int combo = order[rank];
+            b = combo / a.n_qtiles;
+            t = combo - b * a.n_qtiles;
+        } else {
+            t = a.n_qtiles - 1 - rank / a.B;
+            b = rank - (rank / a.B) * a.B;
+        }
+        int hk, hq0;
+        if constexpr (kOdd) {
+            hk = hp / per_group;
+            hq0 = hk * a.G + 2 * (hp - hk * per_group);
+        } else {
+            hq0 = 2 * hp;
+            hk = hq0 / a.G;
+        }
+        const bool dup = kOdd && hq0 + 1 == (hk + 1) * a.G;   // odd group: one head, twice
+        const int raw = a.context_lens[b];
+        if (raw < 0 || raw > cap)
             atomicOr(a.err, PA_DEVERR_CONTEXT_LEN_BIT);
-        n = n < 0 ? 0 : cap;
+        int n;
+        const int nt = tiles_for(b, t, &n);
+        int32_t* e = items + threadIdx.x * 8;
+        e[kEB] = b;
+        e[kET] = t;
+        e[kEH0] = hq0;
+        e[kEH1] = dup ? hq0 : hq0 + 1;
+        e[kEHK] = hk;
+        e[kEN] = n;
+        e[kENT] = nt;
+        e[kEDup] = dup ? 1 : 0;
     }
-    const int row0 = t * kRows;
-    const int rows = min(kRows, a.L - row0);
-    const int p_last = n - a.L + row0 + rows - 1;   // position of the tile's last row
-    int n_keys = a.causal ? min(n, p_last + 1) : n;
-    if (n_keys < 0)
-        n_keys = 0;
-    const int nt = (n_keys + kKeys - 1) / kKeys;     // K/V tiles to visit
 
     const uint32_t sQ = smem_u32(smem + Layout::kQ);
     const uint32_t sK = smem_u32(smem + Layout::kK);
@@ -203,7 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         misc[0] = 0;
-        mbar_init(&bar[kQFull], 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&bar[kQFull + h], 1);
+            mbar_init(&bar[kQEmpty + h], 1);
+        }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar[kKFull + s], 3);   // one arrival per loader warp
             mbar_init(&bar[kKEmpty + s], 1);
@@ -232,10 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // top of its warpgroup's branch, so that the branch is compiled to it.
     if (warp < 4) {
         setmaxnreg_dec<kRegsProducer>();
-        if (warp != 1 && nt > 0) {
+        if (warp != 1) {
             // ===================== loaders =====================================
             // Box k of a tile goes to loader k mod 3; each loader arrives on the
-            // stage barrier with its own byte count.
+            // stage barrier with its own byte count. Loader h < 2 also loads
+            // head h's Q tile of each item.
             const int li = warp == 0 ? 0 : warp - 1;     // 0, 1, 2
             // K/V tiles are read again by the other query tiles and head pairs
             // of the same request and KV group: keep them in L2.
@@ -244,93 +289,116 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prefetch_tensormap(&q_map);
                 prefetch_tensormap(&key_map);
                 prefetch_tensormap(&value_map);
-                mbar_arrive_expect_tx(&bar[kQFull], 2u * Layout::kMat);
-                for (int h = 0; h < 2; ++h) {
-                    const int qrow = (b * a.H_q + (h == 0 ? hq0 : hq1)) * a.L + row0;
-                    uint8_t* d = smem + Layout::kQ + h * Layout::kMat;
-                    tma_load_2d(d, &q_map, 0, qrow, &bar[kQFull], policy);
-                    tma_load_2d(d + Layout::kHalf, &q_map, 64, qrow, &bar[kQFull], policy);
-                }
             }
             const int box = a.box_rows;                  // min(ps, 128)
-            const int32_t* bt = a.block_table + int64_t(b) * a.max_pages;
             const int my_box = li + 3 * lane;
-            auto n_boxes = [&](int j) {
-                const int key0 = j * kKeys;
-                return (min(n, key0 + kKeys) - key0 + box - 1) / box;
-            };
-            // Raw block-table entry of this lane's box in tile j, loaded ahead
-            // of use and checked at use. The load is unconditional (entry 0 when
-            // the box does not exist) so that nothing waits for it before use.
-            auto fetch_page = [&](int j) -> int {
-                const bool live = j < nt && my_box < n_boxes(j);
-                return bt[live ? (j * kKeys + my_box * box) / a.ps : 0];
-            };
-            auto pool_row = [&](int j, int phys) -> int {
-                if (unsigned(phys) >= unsigned(a.num_pages)) {
-                    atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
-                    phys = 0;
-                }
-                const int tok = j * kKeys + my_box * box;
-                return (phys * a.H_kv + hk) * a.ps + (tok - (tok / a.ps) * a.ps);
-            };
-            auto load = [&](int j, bool is_v, int phys) {
-                const int nbox = n_boxes(j);
-                const int mine = nbox > li ? (nbox - li + 2) / 3 : 0;
-                const int s = j & 1;
-                const int full = (is_v ? kVFull : kKFull) + s;
-                const int empty = (is_v ? kVEmpty : kKEmpty) + s;
-                const bool ok = mbar_wait_warp(&bar[empty], ((j >> 1) & 1) ^ 1u, misc, a.err);
-                if (ok) {
-                    if (lane == 0)
-                        mbar_arrive_expect_tx(&bar[full], uint32_t(mine) * box * 128u * 2u);
+            int g = 0;                                   // tiles of the block before this item
+            int qk = 0;                                  // items with tiles before this one
+            for (int it = 0; it < n_items; ++it) {
+                const int32_t* e = items + it * 8;
+                const int nt = e[kENT];
+                if (nt == 0)
+                    continue;
+                const int b = e[kEB], n = e[kEN], hk = e[kEHK];
+                const int32_t* bt = a.block_table + int64_t(b) * a.max_pages;
+                auto n_boxes = [&](int j) {
+                    const int key0 = j * kKeys;
+                    return (min(n, key0 + kKeys) - key0 + box - 1) / box;
+                };
+                // Raw block-table entry of this lane's box in tile j, loaded
+                // ahead of use and checked at use (entry 0 when the box does
+                // not exist, so that nothing waits for it before use).
+                auto fetch_page = [&](int j) -> int {
+                    const bool live = j < nt && my_box < n_boxes(j);
+                    return bt[live ? (j * kKeys + my_box * box) / a.ps : 0];
+                };
+                auto pool_row = [&](int j, int phys) -> int {
+                    if (unsigned(phys) >= unsigned(a.num_pages)) {
+                        atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
+                        phys = 0;
+                    }
+                    const int tok = j * kKeys + my_box * box;
+                    return (phys * a.H_kv + hk) * a.ps + (tok - (tok / a.ps) * a.ps);
+                };
+                auto load = [&](int j, bool is_v, int phys) {
+                    const int nbox = n_boxes(j);
+                    const int mine = nbox > li ? (nbox - li + 2) / 3 : 0;
+                    const int gj = g + j;
+                    const int s = gj & 1;
+                    const int full = (is_v ? kVFull : kKFull) + s;
+                    const int empty = (is_v ? kVEmpty : kKEmpty) + s;
+                    const bool ok = mbar_wait_warp(&bar[empty], ((gj >> 1) & 1) ^ 1u, misc, a.err);
+                    if (ok) {
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&bar[full], uint32_t(mine) * box * 128u * 2u);
+                        __syncwarp();
+                        if (my_box < nbox) {
+                            const int row = pool_row(j, phys);
+                            uint8_t* d = smem + (is_v ? Layout::kV : Layout::kK) + s * Layout::kMat +
+                                         my_box * box * 128;
+                            const CUtensorMap* m = is_v ? &value_map : &key_map;
+                            tma_load_2d(d, m, 0, row, &bar[full], policy);
+                            tma_load_2d(d + Layout::kHalf, m, 64, row, &bar[full], policy);
+                        }
+                    }
                     __syncwarp();
-                    if (my_box < nbox) {
-                        const int row = pool_row(j, phys);
-                        uint8_t* d = smem + (is_v ? Layout::kV : Layout::kK) + s * Layout::kMat +
-                                     my_box * box * 128;
-                        const CUtensorMap* m = is_v ? &value_map : &key_map;
-                        tma_load_2d(d, m, 0, row, &bar[full], policy);
-                        tma_load_2d(d + Layout::kHalf, m, 64, row, &bar[full], policy);
+                };
+                // Order of need: K_0 (its stage frees early), then this head's
+                // Q (free once the item before has issued its last S), then
+                // V_0, K_1, V_1, ... Page ids are fetched two tiles ahead in a
+                // ring of three registers, the loop unrolled over the ring so
+                // that no pending load result is ever copied.
+                auto load_q = [&]() {
+                    const bool ok = mbar_wait_warp(&bar[kQEmpty + li], (qk & 1) ^ 1u, misc, a.err);
+                    if (ok && lane == 0) {
+                        mbar_arrive_expect_tx(&bar[kQFull + li], uint32_t(Layout::kMat));
+                        const int qrow = (b * a.H_q + e[li == 0 ? kEH0 : kEH1]) * a.L + e[kET] * kRows;
+                        uint8_t* d = smem + Layout::kQ + li * Layout::kMat;
+                        tma_load_2d(d, &q_map, 0, qrow, &bar[kQFull + li], policy);
+                        tma_load_2d(d + Layout::kHalf, &q_map, 64, qrow, &bar[kQFull + li], policy);
                     }
-                }
-                __syncwarp();
-            };
-            // Order of need: K_0, V_0, K_1, V_1, ... (S for tile j + 1 follows
-            // P V of tile j). K runs one tile ahead of V. Page ids are fetched
-            // two tiles ahead in a ring of three registers, the loop unrolled
-            // over the ring so that no pending load result is ever copied.
-            int pg[3];
-            pg[0] = fetch_page(0);
-            pg[1] = fetch_page(1);
-            load(0, false, pg[0]);
-            for (int j0 = 0; j0 < nt; j0 += 3) {
+                    __syncwarp();
+                };
+                int pg[3];
+                pg[0] = fetch_page(0);
+                pg[1] = fetch_page(1);
+                // The block's first item: its Q buffers are free, so Q goes out
+                // while the page ids of K_0 are still loading.
+                if (li < 2 && qk == 0)
+                    load_q();
+                load(0, false, pg[0]);
+                if (li < 2 && qk > 0)
+                    load_q();
+                for (int j0 = 0; j0 < nt; j0 += 3) {
     #pragma unroll
-                for (int u = 0; u < 3; ++u) {
-                    const int j = j0 + u;
-                    if (j < nt) {
-                        pg[(u + 2) % 3] = fetch_page(j + 2);
-                        load(j, true, pg[u]);
-                        if (j + 1 < nt)
-                            load(j + 1, false, pg[(u + 1) % 3]);
+                    for (int u = 0; u < 3; ++u) {
+                        const int j = j0 + u;
+                        if (j < nt) {
+                            pg[(u + 2) % 3] = fetch_page(j + 2);
+                            load(j, true, pg[u]);
+                            if (j + 1 < nt)
+                                load(j + 1, false, pg[(u + 1) % 3]);
+                        }
                     }
                 }
+                g += nt;
+                ++qk;
             }
             // No copy may still be landing when the block exits: wait (bounded)
-            // for the last two stages of both streams.
-            for (int j = max(0, nt - 2); j < nt; ++j) {
-                mbar_wait_bounded(&bar[kKFull + (j & 1)], (j >> 1) & 1, misc, a.err);
-                mbar_wait_bounded(&bar[kVFull + (j & 1)], (j >> 1) & 1, misc, a.err);
+            // for the last two stages of both streams and the last Q.
+            for (int gj = max(0, g - 2); gj < g; ++gj) {
+                mbar_wait_bounded(&bar[kKFull + (gj & 1)], (gj >> 1) & 1, misc, a.err);
+                mbar_wait_bounded(&bar[kVFull + (gj & 1)], (gj >> 1) & 1, misc, a.err);
             }
-        } else if (warp == 1 && nt > 0) {
+            if (li < 2 && qk > 0)
+                mbar_wait_bounded(&bar[kQFull + li], (qk - 1) & 1, misc, a.err);
+        } else {
             // ===================== MMA issue (one elected thread) ==============
             // The whole warp runs the loop (waits are warp-uniform, which costs
             // less than branches in a lone lane); one elected lane issues. The
             // first wait after a tcgen05.commit costs about 0.1 us even on a
             // completed phase, so the waits that are normally already satisfied
-            // (the other head's P, the next K and V tiles) are taken right after
-            // a wait that has to take that long anyway (P_h V done), or before a
-            // commit.
+            // (the next K and V tiles) are taken after the commits of a tile.
             const bool leader = elect_one();
             const uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
             const uint32_t idesc_pv = idesc_bf16_f32(kRows, 128, 1);
@@ -338,10 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dq0 = kmajor_base(sQ), dq1 = desc_advance(dq0, Layout::kMat);
             const uint64_t dk0 = kmajor_base(sK), dk1 = desc_advance(dk0, Layout::kMat);
             const uint64_t dv0 = mnmajor_base(sV), dv1 = desc_advance(dv0, Layout::kMat);
-            auto s_mmas = [&](int h, int j) {
+            auto s_mmas = [&](int h, int gj) {
                 if (leader) {
                     const uint64_t da = h ? dq1 : dq0;
-                    const uint64_t db = (j & 1) ? dk1 : dk0;
+                    const uint64_t db = (gj & 1) ? dk1 : dk0;
                     const uint32_t d = tmem + col_s(h);
     #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
@@ -350,15 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             };
-            auto pv_mmas = [&](int h, int j) {
+            auto pv_mmas = [&](int h, int gj, bool first) {
                 if (leader) {
-                    const uint64_t db = (j & 1) ? dv1 : dv0;
+                    const uint64_t db = (gj & 1) ? dv1 : dv0;
                     const uint32_t d = tmem + col_o(h);
                     const uint32_t pa = tmem + col_s(h) + kPCol;
     #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         tc_mma_bf16_ts(d, pa + 8u * kk, desc_advance(db, mnmajor_off(kk)), idesc_pv,
-                                       (j > 0 || kk > 0) ? 1u : 0u);
+                                       (!first || kk > 0) ? 1u : 0u);
                 }
                 __syncwarp();
             };
@@ -370,51 +438,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto wait = [&](int b, uint32_t parity) {
                 return __all_sync(0xffffffffu, mbar_wait_lean(&bar[b], parity, misc, a.err));
             };
-            bool ok = wait(kQFull, 0) && wait(kKFull, 0);
-            if (ok) {
-                tc_fence_after();
-                s_mmas(0, 0);
-                commit(kSFull);
-                s_mmas(1, 0);
-                ok = wait(kVFull, 0) && (nt < 2 || wait(kKFull + 1, 0));
-                commit(kSFull + 1);
-                commit(kKEmpty);
-            }
-            for (int j = 0; j < nt && ok; ++j) {
-                const bool more = j + 1 < nt;
-                // head 0: P_0 V_j, then S_0 for tile j + 1 once P_0 V_j is done
-                // (S_0 overwrites P_0)
-                if (!wait(kPFull, j & 1))
-                    break;
-                tc_fence_after();
-                pv_mmas(0, j);
-                commit(kPVDone);
-                if (!wait(kPVDone, j & 1))
-                    break;
-                tc_fence_after();
-                if (more) {
-                    s_mmas(0, j + 1);
-                    commit(kSFull);
-                }
-                ok = wait(kPFull + 1, j & 1);
+            int g = 0, qk = 0;
+            bool ok = true;
+            for (int it = 0; it < n_items && ok; ++it) {
+                const int nt = items[it * 8 + kENT];
+                if (nt == 0)
+                    continue;
+                // The item's first scores: both score buffers are free (the
+                // last P_h V of the item before was waited for).
+                ok = wait(kQFull, qk & 1) && wait(kKFull + (g & 1), (g >> 1) & 1);
                 if (!ok)
                     break;
-                // head 1: P_1 V_j, then S_1 for tile j + 1
                 tc_fence_after();
-                pv_mmas(1, j);
-                commit(kPVDone + 1);
-                commit(kVEmpty + (j & 1));
-                if (!wait(kPVDone + 1, j & 1))
+                s_mmas(0, g);
+                if (nt == 1)
+                    commit(kQEmpty);
+                commit(kSFull);
+                if (!(ok = wait(kQFull + 1, qk & 1)))
                     break;
-                if (more) {
+                tc_fence_after();
+                s_mmas(1, g);
+                if (nt == 1)
+                    commit(kQEmpty + 1);
+                commit(kSFull + 1);
+                commit(kKEmpty + (g & 1));
+                ok = wait(kVFull + (g & 1), (g >> 1) & 1) &&
+                     (nt < 2 || wait(kKFull + ((g + 1) & 1), ((g + 1) >> 1) & 1));
+                for (int j = 0; j < nt && ok; ++j) {
+                    const int gj = g + j;
+                    const bool more = j + 1 < nt;
+                    const bool last_s = j + 2 == nt;   // S for tile j + 1 is the item's last
+                    // head 0: P_0 V_j, then S_0 for tile j + 1 once P_0 V_j is
+                    // done (S_0 overwrites P_0)
+                    if (!(ok = wait(kPFull, gj & 1)))
+                        break;
                     tc_fence_after();
-                    s_mmas(1, j + 1);
-                    commit(kSFull + 1);
-                    commit(kKEmpty + ((j + 1) & 1));
-                    // the next tile's V and the tile after's K
-                    ok = wait(kVFull + ((j + 1) & 1), ((j + 1) >> 1) & 1) &&
-                         (j + 2 >= nt || wait(kKFull + (j & 1), ((j + 2) >> 1) & 1));
+                    pv_mmas(0, gj, j == 0);
+                    commit(kPVDone);
+                    if (!(ok = wait(kPVDone, gj & 1)))
+                        break;
+                    tc_fence_after();
+                    if (more) {
+                        s_mmas(0, gj + 1);
+                        if (last_s)
+                            commit(kQEmpty);
+                        commit(kSFull);
+                    }
+                    if (!(ok = wait(kPFull + 1, gj & 1)))
+                        break;
+                    // head 1: P_1 V_j, then S_1 for tile j + 1
+                    tc_fence_after();
+                    pv_mmas(1, gj, j == 0);
+                    commit(kPVDone + 1);
+                    commit(kVEmpty + (gj & 1));
+                    if (!(ok = wait(kPVDone + 1, gj & 1)))
+                        break;
+                    if (more) {
+                        tc_fence_after();
+                        s_mmas(1, gj + 1);
+                        if (last_s)
+                            commit(kQEmpty + 1);
+                        commit(kSFull + 1);
+                        commit(kKEmpty + ((gj + 1) & 1));
+                        // the next tile's V and the tile after's K
+                        ok = wait(kVFull + ((gj + 1) & 1), ((gj + 1) >> 1) & 1) &&
+                             (j + 2 >= nt || wait(kKFull + (gj & 1), ((gj + 2) >> 1) & 1));
+                    }
                 }
+                g += nt;
+                ++qk;
             }
             // Every MMA issued completes before the block ends.
             commit(kMmaDone);
@@ -429,178 +521,188 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t trow = tmem + (uint32_t(w4 * 32) << 16);
         const uint32_t ts = trow + col_s(head);
         const uint32_t to = trow + col_o(head);
-        const int i = row0 + r;
-        const int lim = a.causal ? min(n - a.L + i, n - 1) : n - 1;  // last visible key
-        float m_used = -INFINITY;
-        float l = 0.f;
         const float c = a.scale_log2;
-
-        for (int j = 0; j < nt; ++j) {
-            mbar_wait_warp(&bar[kSFull + head], j & 1, misc, a.err);
-            tc_fence_after();
-            // Scores in two halves of 64 columns (64 registers at a time): the
-            // maximum over both, then the exponentials of the upper half (still
-            // in registers), P of keys 64..127 over columns 96..127 (scores
-            // already read), the lower half read again, P of keys 0..63 over
-            // columns 64..95. Columns 0..63 are never written, so every score
-            // is read before anything overwrites it.
-            const int key0 = j * kKeys;
-            const bool edge = key0 + kKeys - 1 > lim;
-            uint32_t sv[64];
-            float* s = reinterpret_cast<float*>(sv);
-            auto load_half = [&](int hf) {
-                tmem_ld32(ts + 64u * hf, sv);
-                tmem_ld32(ts + 64u * hf + 32u, sv + 32);
-                tmem_wait_ld();
-                if (edge) {
-                    // Keys past this row's last visible key -> -inf (by select).
-#pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        const int nv = lim - (key0 + 64 * hf + 32 * w) + 1;   // visible keys
-                        const uint32_t vis = nv >= 32 ? 0xffffffffu : nv <= 0 ? 0u : (1u << nv) - 1u;
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            s[32 * w + k] = (vis >> k) & 1u ? s[32 * w + k] : -INFINITY;
-                    }
-                }
-            };
-            float m8[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                m8[u] = -INFINITY;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                load_half(hf);
-#pragma unroll
-                for (int k = 0; k < 64; k += 8)
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        m8[u] = fmaxf(m8[u], s[k + u]);
-            }
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            const float mxs = mx * c;
-            const bool need =
-                mxs > m_used + kRescaleLog2 || (m_used == -INFINITY && mxs > -INFINITY);
-            float factor = 1.f;
-            if (need) {
-                factor = m_used == -INFINITY ? 0.f : fast_exp2(m_used - mxs);
-                m_used = mxs;
-                l *= factor;
-            }
-            const float mu = m_used == -INFINITY ? 0.f : m_used;
-            // Exponent arguments and the running sum two at a time (packed
-            // fp32x2 FMA and add): half the instructions of the scalar forms.
-            const float2 c2 = make_float2(c, c), nmu2 = make_float2(-mu, -mu);
-            float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                              make_float2(0.f, 0.f)};
-            auto exp_store = [&](int hf) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float2 x = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), c2, nmu2);
-                    const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                    lsum[k & 3] = __fadd2_rn(lsum[k & 3], pp);
-                    pk[k] = pack_bf16x2(pp.x, pp.y);
-                }
-                tmem_st32(ts + kPCol + 32u * hf, pk);
-            };
-            exp_store(1);        // upper half, still in registers
-            load_half(0);
-            exp_store(0);
-            {
-                const float2 t2 = __fadd2_rn(__fadd2_rn(lsum[0], lsum[1]), __fadd2_rn(lsum[2], lsum[3]));
-                l += t2.x + t2.y;
-            }
-            // O_h holds P_h(j-1) V_{j-1} complete (the commit of S_h(j) covers
-            // it): rescale it if the maximum moved (after P, when the scores
-            // no longer occupy registers).
-            if (j >= 1 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t ov[32];
-                    tmem_ld32(to + 32u * q4, ov);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        ov[k] = __float_as_uint(__uint_as_float(ov[k]) * factor);
-                    tmem_st32(to + 32u * q4, ov);
-                }
-            }
-            tmem_wait_st();
-            // V rows past the context hold stale bytes: zero them (P is 0
-            // there, but 0 * NaN is not) before either head's P V.
-            if (head == 0 && n < key0 + kKeys) {
-                mbar_wait_bounded(&bar[kVFull + (j & 1)], (j >> 1) & 1, misc, a.err);
-                const int z0 = max(0, n - key0);
-                const int nz = (kKeys - z0) * 16;    // 16-byte chunks
-                uint8_t* vb = smem + Layout::kV + (j & 1) * Layout::kMat;
-                for (int idx = r; idx < nz; idx += 128) {
-                    const int zr = z0 + idx / 16, ch = idx % 16;
-                    *reinterpret_cast<uint4*>(vb + (ch >> 3) * Layout::kHalf + zr * 128 +
-                                              (((ch & 7) ^ (zr & 7)) << 4)) = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&bar[kPFull + head]);
-        }
-        // ---- epilogue: O / l -> bf16 ----------------------------------------
-        const float inv = l > 0.f ? a.out_scale / l : 0.f;
-        if (nt > 0) {
-            mbar_wait_warp(&bar[kPVDone + head], (nt - 1) & 1, misc, a.err);
-            tc_fence_after();
-        }
         // Output rows go through a 4 KiB staging buffer per warp, 16-byte
         // chunks swizzled by row, so that a warp stores four whole 128-byte row
-        // segments per instruction instead of 32 scattered 16-byte pieces. The
-        // buffer is the head's Q tile: the wait above covers every MMA issued
-        // before the last P V, the last read of Q among them (with no visible
-        // key nothing was loaded into it).
-        uint8_t* stage = smem + Layout::kQ + head * Layout::kMat + w4 * 4096;
-        uint16_t* out_warp =
-            a.out + ((int64_t(b) * a.H_q + (head == 0 ? hq0 : hq1)) * a.L + row0 + w4 * 32) * 128;
-        int rows_ok = rows - w4 * 32;
-        rows_ok = rows_ok > 32 ? 32 : rows_ok;
-        if (misc[0] != 0 || (head == 1 && dup))
-            rows_ok = 0;                          // a wait gave up, or the duplicate head
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            uint32_t pk[32];                      // columns 64 hf .. 64 hf + 63 of this row
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                uint32_t ov[32];
-                if (nt > 0) {
-                    tmem_ld32(to + 32u * (2 * hf + q), ov);
+        // segments per instruction instead of 32 scattered 16-byte pieces.
+        uint8_t* stage = smem + Layout::kStage + (warp - 4) * Layout::kStageWarp;
+        int g = 0;                                   // tiles of the block before this item
+        for (int it = 0; it < n_items; ++it) {
+            const int32_t* e = items + it * 8;
+            const int nt = e[kENT], n = e[kEN];
+            const int row0 = e[kET] * kRows;
+            const int rows = min(kRows, a.L - row0);
+            const int i = row0 + r;
+            const int lim = a.causal ? min(n - a.L + i, n - 1) : n - 1;  // last visible key
+            float m_used = -INFINITY;
+            float l = 0.f;
+
+            for (int j = 0; j < nt; ++j) {
+                const int gj = g + j;
+                mbar_wait_warp(&bar[kSFull + head], gj & 1, misc, a.err);
+                tc_fence_after();
+                // Scores in two halves of 64 columns (64 registers at a time):
+                // the maximum over both, then the exponentials of the upper half
+                // (still in registers), P of keys 64..127 over columns 96..127
+                // (scores already read), the lower half read again, P of keys
+                // 0..63 over columns 64..95. Columns 0..63 are never written, so
+                // every score is read before anything overwrites it.
+                const int key0 = j * kKeys;
+                const bool edge = key0 + kKeys - 1 > lim;
+                uint32_t sv[64];
+                float* s = reinterpret_cast<float*>(sv);
+                auto load_half = [&](int hf) {
+                    tmem_ld32(ts + 64u * hf, sv);
+                    tmem_ld32(ts + 64u * hf + 32u, sv + 32);
                     tmem_wait_ld();
-                } else {
+                    if (edge) {
+                        // Keys past this row's last visible key -> -inf (by select).
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        ov[k] = 0u;
+                        for (int w = 0; w < 2; ++w) {
+                            const int nv = lim - (key0 + 64 * hf + 32 * w) + 1;   // visible keys
+                            const uint32_t vis = nv >= 32 ? 0xffffffffu : nv <= 0 ? 0u : (1u << nv) - 1u;
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                s[32 * w + k] = (vis >> k) & 1u ? s[32 * w + k] : -INFINITY;
+                        }
+                    }
+                };
+                float m8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    m8[u] = -INFINITY;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    load_half(hf);
+#pragma unroll
+                    for (int k = 0; k < 64; k += 8)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            m8[u] = fmaxf(m8[u], s[k + u]);
+                }
+                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                const float mxs = mx * c;
+                const bool need =
+                    mxs > m_used + kRescaleLog2 || (m_used == -INFINITY && mxs > -INFINITY);
+                float factor = 1.f;
+                if (need) {
+                    factor = m_used == -INFINITY ? 0.f : fast_exp2(m_used - mxs);
+                    m_used = mxs;
+                    l *= factor;
+                }
+                const float mu = m_used == -INFINITY ? 0.f : m_used;
+                // Exponent arguments and the running sum two at a time (packed
+                // fp32x2 FMA and add): half the instructions of the scalar forms.
+                const float2 c2 = make_float2(c, c), nmu2 = make_float2(-mu, -mu);
+                float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                  make_float2(0.f, 0.f)};
+                auto exp_store = [&](int hf) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const float2 x = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), c2, nmu2);
+                        const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        lsum[k & 3] = __fadd2_rn(lsum[k & 3], pp);
+                        pk[k] = pack_bf16x2(pp.x, pp.y);
+                    }
+                    tmem_st32(ts + kPCol + 32u * hf, pk);
+                };
+                exp_store(1);        // upper half, still in registers
+                load_half(0);
+                exp_store(0);
+                {
+                    const float2 t2 =
+                        __fadd2_rn(__fadd2_rn(lsum[0], lsum[1]), __fadd2_rn(lsum[2], lsum[3]));
+                    l += t2.x + t2.y;
+                }
+                // O_h holds P_h(j-1) V_{j-1} complete (the commit of S_h(j)
+                // covers it): rescale it if the maximum moved (after P, when the
+                // scores no longer occupy registers).
+                if (j >= 1 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t ov[32];
+                        tmem_ld32(to + 32u * q4, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            ov[k] = __float_as_uint(__uint_as_float(ov[k]) * factor);
+                        tmem_st32(to + 32u * q4, ov);
+                    }
+                }
+                tmem_wait_st();
+                // V rows past the context hold stale bytes: zero them (P is 0
+                // there, but 0 * NaN is not) before either head's P V.
+                if (head == 0 && n < key0 + kKeys) {
+                    mbar_wait_bounded(&bar[kVFull + (gj & 1)], (gj >> 1) & 1, misc, a.err);
+                    const int z0 = max(0, n - key0);
+                    const int nz = (kKeys - z0) * 16;    // 16-byte chunks
+                    uint8_t* vb = smem + Layout::kV + (gj & 1) * Layout::kMat;
+                    for (int idx = r; idx < nz; idx += 128) {
+                        const int zr = z0 + idx / 16, ch = idx % 16;
+                        *reinterpret_cast<uint4*>(vb + (ch >> 3) * Layout::kHalf + zr * 128 +
+                                                  (((ch & 7) ^ (zr & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bar[kPFull + head]);
+            }
+            // ---- epilogue of the item: O / l -> bf16 ----------------------------
+            const float inv = l > 0.f ? a.out_scale / l : 0.f;
+            if (nt > 0) {
+                mbar_wait_warp(&bar[kPVDone + head], (g + nt - 1) & 1, misc, a.err);
+                tc_fence_after();
+            }
+            uint16_t* out_warp =
+                a.out + ((int64_t(e[kEB]) * a.H_q + e[head == 0 ? kEH0 : kEH1]) * a.L + row0 + w4 * 32) *
+                            128;
+            int rows_ok = rows - w4 * 32;
+            rows_ok = rows_ok > 32 ? 32 : rows_ok;
+            if (misc[0] != 0 || (head == 1 && e[kEDup]))
+                rows_ok = 0;                      // a wait gave up, or the duplicate head
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t pk[32];                  // columns 64 hf .. 64 hf + 63 of this row
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t ov[32];
+                    if (nt > 0) {
+                        tmem_ld32(to + 32u * (2 * hf + q), ov);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            ov[k] = 0u;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2)
+                        pk[16 * q + k / 2] =
+                            pack_bf16x2(__uint_as_float(ov[k]) * inv, __uint_as_float(ov[k + 1]) * inv);
                 }
 #pragma unroll
-                for (int k = 0; k < 32; k += 2)
-                    pk[16 * q + k / 2] =
-                        pack_bf16x2(__uint_as_float(ov[k]) * inv, __uint_as_float(ov[k + 1]) * inv);
-            }
+                for (int cq = 0; cq < 8; ++cq)
+                    *reinterpret_cast<uint4*>(stage + lane * 128 + ((cq ^ (lane & 7)) << 4)) =
+                        make_uint4(pk[4 * cq], pk[4 * cq + 1], pk[4 * cq + 2], pk[4 * cq + 3]);
+                __syncwarp();
 #pragma unroll
-            for (int cq = 0; cq < 8; ++cq)
-                *reinterpret_cast<uint4*>(stage + lane * 128 + ((cq ^ (lane & 7)) << 4)) =
-                    make_uint4(pk[4 * cq], pk[4 * cq + 1], pk[4 * cq + 2], pk[4 * cq + 3]);
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int idx = j * 32 + lane;
-                const int rw = idx >> 3, cq = idx & 7;
-                const uint4 v = *reinterpret_cast<const uint4*>(stage + rw * 128 + ((cq ^ (rw & 7)) << 4));
-                if (rw < rows_ok)
-                    *reinterpret_cast<uint4*>(out_warp + int64_t(rw) * 128 + hf * 64 + cq * 8) = v;
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int idx = jj * 32 + lane;
+                    const int rw = idx >> 3, cq = idx & 7;
+                    const uint4 v = *reinterpret_cast<const uint4*>(stage + rw * 128 + ((cq ^ (rw & 7)) << 4));
+                    if (rw < rows_ok)
+                        *reinterpret_cast<uint4*>(out_warp + int64_t(rw) * 128 + hf * 64 + cq * 8) = v;
+                }
+                __syncwarp();
             }
-            __syncwarp();
+            // the O reads above are ordered before the next item's first P V
+            // (issued once this warp arrives for that tile)
+            tc_fence_before();
+            g += nt;
         }
-        tc_fence_before();
     }
 
     __syncthreads();
@@ -616,7 +718,7 @@ size_t prefill_pairs_smem_bytes() { return size_t(Layout::kBytes); }
 
 cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& key_map,
                                  const CUtensorMap& value_map, const PrefillArgs& a, int device,
-                                 cudaStream_t stream)
+                                 int sm_count, cudaStream_t stream)
 {
     constexpr int kMaxDev = 64;
     static std::atomic<int> smem_set[kMaxDev][2];
@@ -650,7 +752,15 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
             return e;
         smem_set[device][odd].store(smem, std::memory_order_relaxed);
     }
-    const int64_t grid = int64_t(a.B) * a.H_kv * ((a.G + 1) / 2) * a.n_qtiles;
+    // One block per SM (one fits), each taking whole items; more blocks only
+    // when an SM would get more than kMaxItems items.
+    const int64_t n_items = int64_t(a.B) * a.H_kv * ((a.G + 1) / 2) * a.n_qtiles;
+    int64_t grid = n_items < sm_count ? n_items : sm_count;
+    const int64_t min_grid = (n_items + kMaxItems - 1) / kMaxItems;
+    if (grid < min_grid)
+        grid = min_grid;
+    if (grid < 1 || grid >= (int64_t(1) << 31))
+        return cudaErrorInvalidValue;
     // Programmatic stream serialization: the blocks may be scheduled while the
     // previous kernel in the stream finishes; each waits for it
     // (griddepcontrol.wait) before reading anything.

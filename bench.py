@@ -468,6 +468,12 @@ def main(argv=None):
                     help="time direct paged decode against gather + dense decode and exit")
     ap.add_argument("--dispatch-sweep", action="store_true",
                     help="time decode vs prefill over query chunk lengths and exit")
+    ap.add_argument("--sweep-L", default=None,
+                    help="with --dispatch-sweep: comma-separated query chunk lengths only")
+    ap.add_argument("--sweep-ctx", default=None,
+                    help="with --dispatch-sweep: comma-separated context lengths only")
+    ap.add_argument("--sweep-group", default=None,
+                    help="with --dispatch-sweep: one head shape only, as H_qxH_kv (e.g. 28x4)")
     ap.add_argument("--no-other-decode", action="store_true",
                     help="skip the other decode workloads (secondary entries)")
     args = ap.parse_args(argv)
@@ -506,7 +512,15 @@ def main(argv=None):
                                     "median of 4"}))
         return 0
     if args.dispatch_sweep:
-        print(json.dumps({"dispatch_sweep": dispatch_sweep(torch, device),
+        kw = {}
+        if args.sweep_L:
+            kw["Ls"] = tuple(int(x) for x in args.sweep_L.split(","))
+        if args.sweep_ctx:
+            kw["ctxs"] = tuple(int(x) for x in args.sweep_ctx.split(","))
+        if args.sweep_group:
+            hq, hkv = (int(x) for x in args.sweep_group.lower().split("x"))
+            kw["groups"] = ((hq, hkv),)
+        print(json.dumps({"dispatch_sweep": dispatch_sweep(torch, device, **kw),
                           "timing": "CUDA graph of 16 calls over 4 rotating pool copies, "
                                     "replayed 3 times, events around the replays"}))
         return 0

@@ -17,12 +17,14 @@ extern "C" {
 #endif
 
 /*
- * Test support for failure detection. The next pa_decode, pa_prefill or
- * pa_attention call made by the calling host thread runs one extra wait, in
- * its first block, on a barrier that nothing ever arrives at. That wait runs
- * out after its bounded limit (about one second), records PA_DEVERR_TIMEOUT
- * in the device error word, and the kernel then finishes normally with the
- * correct result. Nothing faults or hangs; the CUDA context stays usable.
+ * Test support for failure detection. The next call made by the calling
+ * host thread that runs the split-KV kernel (pa_decode, pa_decode_noalloc,
+ * pa_attention routed to decode, and the prefill of head_dim 64 or of pages
+ * under 8 tokens) runs one extra wait, in its first block, on a barrier that
+ * nothing ever arrives at. That wait runs out after its bounded limit (about
+ * one second), records PA_DEVERR_TIMEOUT in the device error word, and the
+ * kernel then finishes normally with the correct result. Nothing faults or
+ * hangs; the CUDA context stays usable.
  */
 void pa_debug_arm_wait_timeout(void);
 

@@ -171,8 +171,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n_items = 0;
     while (n_items < kMaxItems && item_at(n_items) < n_all)
         ++n_items;
+    // Context length of request bb (clamped; an entry out of range is
+    // recorded) and the K/V tiles its query tile tt visits.
     auto tiles_for = [&](int bb, int tt, int* n_out) {
         int nn = a.context_lens[bb];
+        if (nn < 0 || nn > cap)
+            atomicOr(a.err, PA_DEVERR_CONTEXT_LEN_BIT);
         nn = nn < 0 ? 0 : (nn > cap ? cap : nn);
         const int r0 = tt * kRows;
         const int pl = nn - a.L + r0 + min(kRows, a.L - r0) - 1;
@@ -181,13 +185,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         *n_out = nn;
         return (nk + kKeys - 1) / kKeys;
     };
-    int* order = reinterpret_cast<int*>(smem + Layout::kStage);   // scratch until the epilogues
+    // scratch until the epilogues: the ranking, and the tiles and context
+    // length of each (request, query tile) pair
+    int* order = reinterpret_cast<int*>(smem + Layout::kStage);
+    int* tiles_of = order + kThreads;
+    int* n_of = tiles_of + kThreads;
     if (M <= kThreads) {
-        int* tiles_of = order + kThreads;
         const int m = threadIdx.x;
-        int nn;
         if (m < M)
-            tiles_of[m] = tiles_for(m / a.n_qtiles, m % a.n_qtiles, &nn);
+            tiles_of[m] = tiles_for(m / a.n_qtiles, m % a.n_qtiles, &n_of[m]);
         __syncthreads();
         if (m < M) {
             const int w = tiles_of[m];
@@ -204,14 +210,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t i = item_at(int(threadIdx.x));
         const int rank = int(i / pairs);
         const int hp = int(i - int64_t(rank) * pairs);
-        int b, t;
+        int b, t, n, nt;
         if (M <= kThreads) {
             const int combo = order[rank];
             b = combo / a.n_qtiles;
             t = combo - b * a.n_qtiles;
+            n = n_of[combo];
+            nt = tiles_of[combo];
         } else {
             t = a.n_qtiles - 1 - rank / a.B;
             b = rank - (rank / a.B) * a.B;
+            nt = tiles_for(b, t, &n);
         }
         int hk, hq0;
         if constexpr (kOdd) {
@@ -222,11 +231,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             hk = hq0 / a.G;
         }
         const bool dup = kOdd && hq0 + 1 == (hk + 1) * a.G;   // odd group: one head, twice
-        const int raw = a.context_lens[b];
-        if (raw < 0 || raw > cap)
-            atomicOr(a.err, PA_DEVERR_CONTEXT_LEN_BIT);
-        int n;
-        const int nt = tiles_for(b, t, &n);
         int32_t* e = items + threadIdx.x * 8;
         e[kEB] = b;
         e[kET] = t;

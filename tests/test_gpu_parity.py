@@ -448,6 +448,22 @@ def test_split_prefill_workspace_contents_and_repeat():
     assert_close(host_f64(outs[0]), oracle_out(b, kp, vp), "split workspace contents")
 
 
+def test_split_prefill_ragged_items_with_empty_rows():
+    """Ragged contexts from 0 to 5000 tokens (the longest items cut over many
+    blocks, the shortest with no visible key at all) in one split launch:
+    sampled rows of every request against the oracle, and the rows at
+    negative positions exactly zero."""
+    lens = [0, 5000, 130, 2100, 7, 900, 3333, 256, 1]
+    b = wl.build_batch("splitragged", B=len(lens), H_q=16, H_kv=4, D=128, page_size=16, L=256,
+                       context_lens=lens, seed=25, L_new=0, placement="churn")
+    out = host_f64(gpu_step(DeviceBatch(b), route="prefill_split"))
+    check_no_device_error()
+    assert np.all(out[0] == 0) and np.all(out[4, :, :249] == 0) and np.all(out[8, :, :255] == 0)
+    rows = _sampled_rows(b, np.random.default_rng(5))
+    got = out[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(got, oracle_out(b, b.key_pages, b.value_pages, rows=rows), "split ragged")
+
+
 def test_split_prefill_rejects_small_workspace():
     import paged_kv_attention_06_gb300 as pa
     b = wl.build_batch("splitsmallws", B=1, H_q=4, H_kv=2, D=128, page_size=16, L=64,

@@ -16,39 +16,34 @@
 namespace pa {
 namespace {
 
-// Thread t of the flat index: vector c of row (b, h, i) (i fastest among
-// the rows). Returns false past the end.
+// Thread t of the flat index (t below the thread count): vector c of row
+// (b, h, i) (i fastest among the rows); its source is element t * 8 of key /
+// value.
 struct AppendPos {
-    int64_t src;      // element offset of the vector in key / value
     int64_t dst;      // element offset in the page pool, or -1: skip
 };
 
-__device__ __forceinline__ bool append_pos(const AppendArgs& a, int64_t t, int vshift,
+__device__ __forceinline__ void append_pos(const AppendArgs& a, int64_t t, int vshift,
                                            AppendPos& p)
 {
-    const int64_t rows = int64_t(a.B) * a.H_kv * a.L_new;
     const int64_t r = t >> vshift;
-    if (r >= rows)
-        return false;
     const int c = int(t & ((1 << vshift) - 1));
     const int64_t bh = udiv64(r, a.L_new);
     const int i = int(r - bh * a.L_new);
     const int b = int(udiv64(bh, a.H_kv));
     const int h = int(bh - int64_t(b) * a.H_kv);
-    p.src = t * 8;
     p.dst = -1;
     const int64_t slot = a.slot_mapping[int64_t(b) * a.L_new + i];
     if (slot < 0)
-        return true;  // padding token
+        return;  // padding token
     const int64_t page = udiv64(slot, a.ps);
     const int64_t off = slot - page * a.ps;
     if (page >= a.num_pages) {
         if (c == 0 && h == 0)
             atomicOr(a.err, PA_DEVERR_SLOT_BIT);
-        return true;
+        return;
     }
     p.dst = ((page * a.H_kv + h) * a.ps + off) * a.D + c * 8;
-    return true;
 }
 
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a)
@@ -59,15 +54,17 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a)
     grid_dependency_wait();
     grid_launch_dependents();
     const int vshift = a.D == 128 ? 4 : 3;   // 16-byte vectors per row: 16 or 8
-    for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;;
+    const int64_t total = (int64_t(a.B) * a.H_kv * a.L_new) << vshift;
+    for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
          t += int64_t(gridDim.x) * blockDim.x) {
+        // The source rows do not depend on the slot: their loads are in
+        // flight together with the slot_mapping load.
+        const uint4 k = *reinterpret_cast<const uint4*>(a.key + t * 8);
+        const uint4 v = *reinterpret_cast<const uint4*>(a.value + t * 8);
         AppendPos p;
-        if (!append_pos(a, t, vshift, p))
-            break;
+        append_pos(a, t, vshift, p);
         if (p.dst < 0)
             continue;
-        const uint4 k = *reinterpret_cast<const uint4*>(a.key + p.src);
-        const uint4 v = *reinterpret_cast<const uint4*>(a.value + p.src);
         *reinterpret_cast<uint4*>(a.key_pages + p.dst) = k;
         *reinterpret_cast<uint4*>(a.value_pages + p.dst) = v;
     }
@@ -83,11 +80,13 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const AppendArgs a)
     const int vshift = a.D == 128 ? 4 : 3;
     uint8_t* const kp = reinterpret_cast<uint8_t*>(a.key_pages);
     uint8_t* const vp = reinterpret_cast<uint8_t*>(a.value_pages);
-    for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;;
+    const int64_t total = (int64_t(a.B) * a.H_kv * a.L_new) << vshift;
+    for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
          t += int64_t(gridDim.x) * blockDim.x) {
+        const uint4 k = *reinterpret_cast<const uint4*>(a.key + t * 8);
+        const uint4 v = *reinterpret_cast<const uint4*>(a.value + t * 8);
         AppendPos p;
-        if (!append_pos(a, t, vshift, p))
-            break;
+        append_pos(a, t, vshift, p);
         if (p.dst < 0)
             continue;
         auto q2 = [&](uint32_t w, float sc) {   // two bf16 -> two e4m3 codes (16 bits)
@@ -97,8 +96,6 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const AppendArgs a)
         auto q8 = [&](uint4 x, float sc) {
             return make_uint2(q2(x.x, sc) | (q2(x.y, sc) << 16), q2(x.z, sc) | (q2(x.w, sc) << 16));
         };
-        const uint4 k = *reinterpret_cast<const uint4*>(a.key + p.src);
-        const uint4 v = *reinterpret_cast<const uint4*>(a.value + p.src);
         *reinterpret_cast<uint2*>(kp + p.dst) = q8(k, a.k_scale);
         *reinterpret_cast<uint2*>(vp + p.dst) = q8(v, a.v_scale);
     }

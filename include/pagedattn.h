@@ -346,9 +346,9 @@ pa_status pa_prefill_split(const void *query, const void *key_pages,
  * Query Shape": short queries take the vector decode schedule, long ones the
  * page-walking prefill; no dense fallback). The thresholds are this
  * library's, set by timing both kernels on GB300 (the page's own rule,
- * L <= 8, was set on other hardware): decode for L <= 16, and for L <= 32
- * when num_q_heads / num_kv_heads >= 4; prefill otherwise. Returns -1 on
- * invalid shapes.
+ * L <= 8, was set on other hardware): decode for L <= 24, and for L <= 32
+ * when max_context_len >= 3072; prefill otherwise. Returns -1 on invalid
+ * shapes.
  */
 int32_t pa_attention_route(pa_shape shape, int32_t max_context_len);
 

@@ -897,17 +897,16 @@ pa_status pa_prefill_split(const void* query, const void* key_pages, const void*
 
 int32_t pa_attention_route(pa_shape shape, int32_t max_context_len)
 {
-    (void)max_context_len;
     if (shape.q_len <= 0 || shape.num_q_heads <= 0 || shape.num_kv_heads <= 0)
         return -1;
     // The split-KV decode reads a KV group's K/V once per 64 of its query
-    // rows (four 16-row tiles per segment), the tile prefill once per 128-row
-    // tile of each head pair at a fixed cost per tile. Measured crossover on
-    // GB300 (32 requests, contexts of 1k and 4k tokens, page size 16): decode
-    // is faster up to 16 rows per request for every group size, and up to 32
-    // rows when a KV group has 4 or more query heads.
-    const int32_t G = shape.num_q_heads / shape.num_kv_heads;
-    return shape.q_len <= 16 || (shape.q_len <= 32 && G >= 4) ? 0 : 1;
+    // rows (four 16-row tiles per segment) and its cost grows with the rows;
+    // the persistent tile prefill pays a fixed cost per 128-row tile.
+    // Measured crossover on GB300 (32 requests, contexts of 1k to 4k tokens,
+    // page size 16, 1, 4 and 7 query heads per KV group): decode is faster up
+    // to 24 rows per request (within 3 % at 1k contexts), the two tie at 32
+    // rows from about 3k-token contexts on, and prefill is faster beyond.
+    return shape.q_len <= 24 || (shape.q_len <= 32 && max_context_len >= 3072) ? 0 : 1;
 }
 
 pa_status pa_attention(const void* query, const void* key_pages, const void* value_pages,

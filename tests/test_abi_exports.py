@@ -62,18 +62,19 @@ class Shape(ctypes.Structure):
 def test_dispatch_route_rule(lib):
     """Short queries take the decode schedule, long ones the prefill one
     (Week 3 Day 4, "Choose a Schedule for Each Query Shape"), with the
-    GB300 thresholds: L <= 16, or L <= 32 when a KV group has >= 4 heads."""
+    GB300 thresholds: L <= 24, or L <= 32 when max_context_len >= 3072,
+    whatever the group size."""
     lib.pa_attention_route.argtypes = [Shape, ctypes.c_int32]
     lib.pa_attention_route.restype = ctypes.c_int32
-    for L in range(1, 33):     # G = 4
-        assert lib.pa_attention_route(Shape(2, 8, 2, 128, L, 16, 4), 4096) == 0
-    for L in (33, 48, 64, 512):
-        assert lib.pa_attention_route(Shape(2, 8, 2, 128, L, 16, 4), 4096) == 1
-    for L in range(1, 17):     # G = 1 and G = 2
-        assert lib.pa_attention_route(Shape(2, 8, 8, 128, L, 16, 4), 4096) == 0
-        assert lib.pa_attention_route(Shape(2, 8, 4, 128, L, 16, 4), 4096) == 0
-    for L in (17, 24, 32, 64):
-        assert lib.pa_attention_route(Shape(2, 8, 8, 128, L, 16, 4), 4096) == 1
-        assert lib.pa_attention_route(Shape(2, 8, 4, 128, L, 16, 4), 4096) == 1
+    for H_kv in (2, 4, 8):     # G = 4, 2, 1
+        for L in range(1, 25):
+            assert lib.pa_attention_route(Shape(2, 8, H_kv, 128, L, 16, 4), 1024) == 0
+        for L in range(25, 33):
+            assert lib.pa_attention_route(Shape(2, 8, H_kv, 128, L, 16, 4), 4096) == 0
+            assert lib.pa_attention_route(Shape(2, 8, H_kv, 128, L, 16, 4), 3072) == 0
+            assert lib.pa_attention_route(Shape(2, 8, H_kv, 128, L, 16, 4), 3071) == 1
+            assert lib.pa_attention_route(Shape(2, 8, H_kv, 128, L, 16, 4), 0) == 1
+        for L in (33, 48, 64, 512):
+            assert lib.pa_attention_route(Shape(2, 8, H_kv, 128, L, 16, 4), 1 << 20) == 1
     assert lib.pa_attention_route(Shape(2, 8, 2, 128, 0, 16, 4), 0) == -1
     assert lib.pa_attention_route(Shape(2, 8, 0, 128, 4, 16, 4), 0) == -1

@@ -119,13 +119,14 @@ def test_prefill_route_head_dim64_whole_segments(L, causal):
     assert_close(host_f64(out), oracle_out(b, kp, vp), f"prefill D=64 L={L}")
 
 
-@pytest.mark.parametrize("L,H_q,H_kv", [(12, 28, 4), (24, 28, 4), (32, 32, 8), (16, 8, 8)])
-def test_attention_routes_short_chunks_to_decode(L, H_q, H_kv):
+@pytest.mark.parametrize("L,H_q,H_kv,max_len", [(12, 28, 4, 3000), (24, 28, 4, 3000),
+                                                 (24, 8, 8, 3000), (32, 32, 8, 5000)])
+def test_attention_routes_short_chunks_to_decode(L, H_q, H_kv, max_len):
     """pa_attention sends these chunk lengths to the decode schedule (the
-    GB300 thresholds: L <= 16, or L <= 32 with 4 or more query heads per KV
-    group) and the result matches the oracle on every row."""
+    GB300 thresholds: L <= 24, or L <= 32 with contexts of 3072 tokens or
+    more) and the result matches the oracle on every row."""
     import paged_kv_attention_06_gb300 as pa
-    b = _batch(16, H_q, H_kv, 128, L, True, B=6, seed=L)
+    b = _batch(16, H_q, H_kv, 128, L, True, max_len=max_len, B=6, seed=L)
     db = DeviceBatch(b)
     shape = pa.make_shape(db.query.shape, db.key_pages.shape, db.block_table.shape[1])
     assert int(pa.binding._lib.pa_attention_route(shape, int(b.context_lens.max()))) == 0

@@ -503,7 +503,8 @@ def main(argv=None):
         return 0
     if args.serving_trace:
         serving_trace(torch, device)            # warm-up run (builds, first calls)
-        print(json.dumps({"serving_trace": serving_trace(torch, device)}))
+        print(json.dumps({"serving_trace": serving_trace(torch, device),
+                          "serving_trace_python_issue": serving_trace(torch, device, native=False)}))
         return 0
     if args.dense_gather:
         print(json.dumps({"dense_gather": dense_gather_bench(torch, device),
@@ -1054,7 +1055,7 @@ def dense_gather_bench(torch, device, ctxs=(128, 1024), batches=(1, 32), H_q=32,
 
 
 def serving_trace(torch, device, n_seqs=16, batch=4, prompt=(128, 1024), output=(32, 128),
-                  chunk=128, H_q=32, H_kv=8, D=128, page_size=16, seed=2024):
+                  chunk=128, H_q=32, H_kv=8, D=128, page_size=16, seed=2024, native=True):
     """A synthetic serving trace shaped like the pages' (16 requests, at most
     4 active, prompts U[128, 1024], outputs U[32, 128], prefill in chunks of
     128 tokens) through one attention layer: every step the C++ pa_kv_cache
@@ -1062,7 +1063,10 @@ def serving_trace(torch, device, n_seqs=16, batch=4, prompt=(128, 1024), output=
     tables go to the device from pinned buffers, the new K/V rows are
     appended, and attention runs (all decoding requests in one call with
     L = 1; each prefilling request's chunk in its own call). K/V rows and
-    queries are seeded normal values (no model)."""
+    queries are seeded normal values (no model). native: each call is one
+    pa_kv_cache_step (plan into pinned memory, one table copy, append and
+    attention in one C call); otherwise plan, three copies, append and
+    attention are issued from Python one by one."""
     import paged_kv_attention_06_gb300 as pa
     rng = np.random.default_rng(seed)
     prompts = rng.integers(prompt[0], prompt[1], size=n_seqs, endpoint=True)
@@ -1086,6 +1090,28 @@ def serving_trace(torch, device, n_seqs=16, batch=4, prompt=(128, 1024), output=
     d_bt = torch.empty((batch * max_pages,), dtype=torch.int32, device=device)
     d_cl = torch.empty((batch,), dtype=torch.int32, device=device)
     d_sm = torch.empty((batch * chunk,), dtype=torch.int32, device=device)
+    # native steps: packed tables, one pinned region per call of a step
+    tab_bytes = pa.KVCache.step_table_bytes(batch, max_pages, chunk)
+    h_tab = torch.empty((regions, tab_bytes), dtype=torch.uint8).pin_memory()
+    d_tab = torch.empty((regions, tab_bytes), dtype=torch.uint8, device=device)
+    o_flat = torch.empty((batch * H_q * chunk * D,), dtype=torch.bfloat16, device=device)
+    ws, _ = pa.decode_workspace(pa.pa_shape(batch, H_q, H_kv, D, 1, num_pages, max_pages), device)
+    pws, _ = pa.prefill_workspace(pa.pa_shape(1, H_q, H_kv, D, chunk, num_pages, max_pages),
+                                  page_size, device)
+    if pws is not None and pws.numel() > ws.numel():
+        ws = pws
+
+    def step_native(r, ids, toks, l_new, is_decode):
+        n = len(ids)
+        kv = (n, H_kv, l_new, D)
+        e0, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        cache.step(ids, toks, l_new, max_pages, h_tab[r], d_tab[r],
+                   k_flat[:n * H_kv * l_new * D].view(kv), v_flat[:n * H_kv * l_new * D].view(kv),
+                   q_flat[:n * H_q * l_new * D].view(n, H_q, l_new, D), kp, vp,
+                   out=o_flat[:n * H_q * l_new * D].view(n, H_q, l_new, D), workspace=ws)
+        e2.record()
+        events.append((e0, e0, e2, is_decode))
 
     def step(r, ids, toks, l_new, is_decode):
         bt, cl, sm = cache.plan(ids, toks, max_pages, l_new)
@@ -1124,9 +1150,10 @@ def serving_trace(torch, device, n_seqs=16, batch=4, prompt=(128, 1024), output=
         dec = [s_id for s_id, (p_, o_) in active.items() if p_ >= prompts[s_id]]
         pre = [s_id for s_id, (p_, o_) in active.items() if p_ < prompts[s_id]]
         # decode group: one token each, one attention call
+        run = step_native if native else step
         if dec:
             t0 = time.perf_counter()
-            step(0, dec, [1] * len(dec), 1, True)
+            run(0, dec, [1] * len(dec), 1, True)
             host_s += time.perf_counter() - t0
             decode_tokens += len(dec)
             for s_id in dec:
@@ -1135,7 +1162,7 @@ def serving_trace(torch, device, n_seqs=16, batch=4, prompt=(128, 1024), output=
         for r, s_id in enumerate(pre, start=1):
             take = int(min(chunk, prompts[s_id] - active[s_id][0]))
             t0 = time.perf_counter()
-            step(r, [s_id], [take], take, False)
+            run(r, [s_id], [take], take, False)
             host_s += time.perf_counter() - t0
             prefill_tokens += take
             active[s_id][0] += take
@@ -1168,8 +1195,11 @@ def serving_trace(torch, device, n_seqs=16, batch=4, prompt=(128, 1024), output=
             "pages_left_held": int(leaked),
             "shape": {"H_q": H_q, "H_kv": H_kv, "D": D, "page_size": page_size, "chunk": chunk,
                       "prompt": list(prompt), "output": list(output)},
+            "issue": "native pa_kv_cache_step per call" if native else
+                     "plan, table copies, append and attention issued from Python",
             "timing": "wall clock over the whole trace (one device sync per step); device "
-                      "times from CUDA events around each append and attention call"}
+                      "times from CUDA events around each append and attention call (native: "
+                      "around each whole step call, reported under the attention kind; append 0)"}
 
 
 PREFILL_SHAPES = [

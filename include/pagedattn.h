@@ -442,6 +442,47 @@ pa_status pa_kv_cache_snapshot_take(const pa_kv_cache *cache, pa_kv_cache_snapsh
 pa_status pa_kv_cache_restore(pa_kv_cache *cache, const pa_kv_cache_snapshot *snapshot);
 void pa_kv_cache_snapshot_destroy(pa_kv_cache_snapshot *snapshot);
 
+/*
+ * One scheduler step run from the host in a single call (Week 3 Day 4,
+ * "Decode Metadata": the batch's page metadata prepared once per step):
+ * pa_kv_cache_plan writes the three tables, packed as block_table [n,
+ * max_pages], then context_lens [n], then slot_mapping [n, l_new] (int32),
+ * into `host_tables`; one asynchronous copy moves them to `device_tables`;
+ * then pa_append_kv writes the new K/V rows and pa_attention (causal, with
+ * max_context_len = the largest planned context length) runs over the step,
+ * all on `stream`.
+ *   host_tables    pinned host memory of at least
+ *                  pa_kv_cache_step_table_bytes(n, max_pages, l_new) bytes.
+ *                  The copy is asynchronous: the caller must not rewrite this
+ *                  region (for example by the next step) before the copy has
+ *                  run (use one region per step in flight, or synchronise).
+ *   device_tables  device memory of the same size, 4-byte aligned; the
+ *                  kernels of this step read it.
+ *   key_new, value_new  [n, num_kv_heads, l_new, head_dim] bf16 (device);
+ *                  rows past a request's new_tokens[i] are not written.
+ *   query, out     [n, num_q_heads, l_new, head_dim] bf16 (device); a request
+ *                  with fewer than l_new new tokens has its new tokens in its
+ *                  last new_tokens[i] rows (bottom-right causal alignment);
+ *                  its earlier rows attend as tokens already cached.
+ *   key_pages, value_pages  the layer's pool [num_pages, num_kv_heads,
+ *                  page_size, head_dim] bf16, num_pages and page_size as
+ *                  given to pa_kv_cache_create.
+ *   workspace      as pa_attention (required when the step takes the decode
+ *                  route, L <= pa_attention_route's threshold).
+ * Returns the plan's status (nothing changed on failure), PA_ERR_CUDA if the
+ * copy could not be issued, or the status of pa_append_kv / pa_attention; in
+ * the last two cases the plan stays applied and a snapshot taken before the
+ * call undoes it.
+ */
+size_t pa_kv_cache_step_table_bytes(int32_t n, int32_t max_pages, int32_t l_new);
+pa_status pa_kv_cache_step(pa_kv_cache *cache, int32_t n, const int64_t *seq_ids,
+                           const int32_t *new_tokens, int32_t l_new, int32_t max_pages,
+                           void *host_tables, void *device_tables, size_t table_bytes,
+                           const void *key_new, const void *value_new, const void *query,
+                           void *key_pages, void *value_pages, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, float scale, void *out,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *pa_status_string(pa_status status);
 

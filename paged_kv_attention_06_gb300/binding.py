@@ -97,6 +97,11 @@ def _load() -> ctypes.CDLL:
     lib.pa_kv_cache_context_len.restype = i32
     lib.pa_kv_cache_plan.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp]
     lib.pa_kv_cache_plan.restype = ctypes.c_int
+    lib.pa_kv_cache_step_table_bytes.argtypes = [i32, i32, i32]
+    lib.pa_kv_cache_step_table_bytes.restype = sz
+    lib.pa_kv_cache_step.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, sz, vp, vp, vp, vp, vp,
+                                     i32, i32, i32, ctypes.c_float, vp, vp, sz, vp]
+    lib.pa_kv_cache_step.restype = ctypes.c_int
     lib.pa_kv_cache_snapshot_take.argtypes = [vp, ctypes.POINTER(vp)]
     lib.pa_kv_cache_snapshot_take.restype = ctypes.c_int
     lib.pa_kv_cache_restore.argtypes = [vp, vp]
@@ -637,6 +642,51 @@ class KVCache:
                                    int(l_new), bt.ctypes.data, cl.ctypes.data, sm.ctypes.data)
         _check(st, "pa_kv_cache_plan")
         return bt, cl, sm[:, :int(l_new)]
+
+    @staticmethod
+    def step_table_bytes(n: int, max_pages: int, l_new: int) -> int:
+        """Bytes of the packed tables of one pa_kv_cache_step."""
+        return int(_lib.pa_kv_cache_step_table_bytes(int(n), int(max_pages), int(l_new)))
+
+    def step(self, seq_ids, new_tokens, l_new: int, max_pages: int, host_tables, device_tables,
+             key_new, value_new, query, key_pages, value_pages, out=None,
+             scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
+             stream=None) -> torch.Tensor:
+        """One whole step in one native call (pa_kv_cache_step): plan into the
+        pinned `host_tables`, one copy to `device_tables`, append, attention.
+        Returns out [n, H_q, l_new, D]. `host_tables` must not be rewritten
+        (by a later step) before this step's copy has run."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        toks = np.ascontiguousarray(new_tokens, dtype=np.int32)
+        n = int(ids.shape[0])
+        if n != query.shape[0] or n != key_new.shape[0] or int(l_new) != query.shape[2]:
+            raise ValueError("query / key_new must be [n, heads, l_new, D] for the n requests")
+        if not host_tables.is_pinned() or not device_tables.is_cuda:
+            raise ValueError("host_tables must be pinned host memory, device_tables on the GPU")
+        nbytes = min(host_tables.numel() * host_tables.element_size(),
+                     device_tables.numel() * device_tables.element_size())
+        _, H_q, _, D = (int(x) for x in query.shape)
+        H_kv = int(key_new.shape[1])
+        if out is None:
+            out = torch.empty_like(query)
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        if workspace is None:
+            shape = pa_shape(n, H_q, H_kv, D, int(l_new), int(key_pages.shape[0]), int(max_pages))
+            workspace, _ = decode_workspace(shape, query.device)
+            pws, _ = prefill_workspace(shape, self.page_size, query.device)
+            if pws is not None and pws.numel() > workspace.numel():
+                workspace = pws
+        st = _lib.pa_kv_cache_step(
+            self._h, n, ids.ctypes.data, toks.ctypes.data, int(l_new), int(max_pages),
+            host_tables.data_ptr(), device_tables.data_ptr(), nbytes,
+            _dev_ptr(key_new, torch.bfloat16, "key_new"), _dev_ptr(value_new, torch.bfloat16, "value_new"),
+            _dev_ptr(query, torch.bfloat16, "query"), _dev_ptr(key_pages, torch.bfloat16, "key_pages"),
+            _dev_ptr(value_pages, torch.bfloat16, "value_pages"), H_q, H_kv, D, float(scale),
+            _dev_ptr(out, torch.bfloat16, "out"), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+        _check(st, "pa_kv_cache_step")
+        return out
 
 
 class KVCacheSnapshot:

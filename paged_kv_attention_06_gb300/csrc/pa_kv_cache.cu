@@ -9,10 +9,14 @@
 // allocate; release every page of a finished request exactly once; restore
 // the pool when a write fails).
 //
+// pa_kv_cache_step runs a whole step from the host in one call: the plan,
+// one copy of the packed tables, the append and the attention launch.
+//
 // The allocator hands out a freed page first (free list, last freed first)
 // and otherwise the lowest never-used page id. A step is all-or-nothing: the
 // allocations it made are undone, in reverse, when any request of the step
 // cannot be placed, so a failed step leaves the cache exactly as it was.
+#include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -229,5 +233,57 @@ pa_status pa_kv_cache_restore(pa_kv_cache* cache, const pa_kv_cache_snapshot* sn
 }
 
 void pa_kv_cache_snapshot_destroy(pa_kv_cache_snapshot* snapshot) { delete snapshot; }
+
+size_t pa_kv_cache_step_table_bytes(int32_t n, int32_t max_pages, int32_t l_new)
+{
+    if (n <= 0 || max_pages <= 0 || l_new <= 0)
+        return 0;
+    return size_t(n) * size_t(max_pages + 1 + l_new) * sizeof(int32_t);
+}
+
+pa_status pa_kv_cache_step(pa_kv_cache* cache, int32_t n, const int64_t* seq_ids,
+                           const int32_t* new_tokens, int32_t l_new, int32_t max_pages,
+                           void* host_tables, void* device_tables, size_t table_bytes,
+                           const void* key_new, const void* value_new, const void* query,
+                           void* key_pages, void* value_pages, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, float scale, void* out,
+                           void* workspace, size_t workspace_bytes, void* stream)
+{
+    const size_t need = pa_kv_cache_step_table_bytes(n, max_pages, l_new);
+    if (!cache || need == 0 || !host_tables || !device_tables || table_bytes < need)
+        return PA_ERR_INVALID_ARG;
+    // The three tables, packed: block_table [n, max_pages], context_lens [n],
+    // slot_mapping [n, l_new].
+    int32_t* h_bt = static_cast<int32_t*>(host_tables);
+    int32_t* h_cl = h_bt + int64_t(n) * max_pages;
+    int32_t* h_sm = h_cl + n;
+    pa_status st = pa_kv_cache_plan(cache, n, seq_ids, new_tokens, max_pages, l_new, h_bt, h_cl,
+                                    h_sm);
+    if (st != PA_OK)
+        return st;
+    int32_t max_len = 0;
+    for (int32_t i = 0; i < n; ++i)
+        max_len = h_cl[i] > max_len ? h_cl[i] : max_len;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(device_tables, host_tables, need, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    const int32_t* d_bt = static_cast<const int32_t*>(device_tables);
+    const int32_t* d_cl = d_bt + int64_t(n) * max_pages;
+    const int32_t* d_sm = d_cl + n;
+    pa_shape shape;
+    shape.batch = n;
+    shape.num_q_heads = num_q_heads;
+    shape.num_kv_heads = num_kv_heads;
+    shape.head_dim = head_dim;
+    shape.q_len = l_new;
+    shape.num_pages = cache->num_pages;
+    shape.max_pages = max_pages;
+    st = pa_append_kv(key_new, value_new, key_pages, value_pages, d_sm, cache->page_size, shape,
+                      stream);
+    if (st != PA_OK)
+        return st;
+    return pa_attention(query, key_pages, value_pages, d_bt, d_cl, cache->page_size, scale, 1, out,
+                        shape, max_len, workspace, workspace_bytes, stream);
+}
 
 }  // extern "C"

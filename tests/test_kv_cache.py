@@ -146,3 +146,43 @@ def test_snapshot_restore_rolls_back_a_step():
     with pytest.raises(pa.PagedAttentionError):       # snapshot of another cache
         other.restore(snap)
     snap.close()
+
+
+def test_native_step_checks_before_any_device_work():
+    """pa_kv_cache_step: the packed table size, and the argument checks and
+    plan failures that return before anything reaches the GPU (the cache is
+    left unchanged)."""
+    import ctypes
+    pa = _pa()
+    lib = pa.binding._lib
+    assert lib.pa_kv_cache_step_table_bytes(3, 10, 4) == 3 * (10 + 1 + 4) * 4
+    assert lib.pa_kv_cache_step_table_bytes(0, 10, 4) == 0
+    assert lib.pa_kv_cache_step_table_bytes(3, 10, 0) == 0
+    c = pa.KVCache(8, 4)
+    c.add(1)
+    ids = np.array([1], dtype=np.int64)
+    toks = np.array([3], dtype=np.int32)
+    host = (ctypes.c_int32 * 64)()
+    need = lib.pa_kv_cache_step_table_bytes(1, 4, 3)
+
+    def step(ids_, toks_, host_ptr, nbytes, max_pages=4):
+        return lib.pa_kv_cache_step(c._h, len(ids_), ids_.ctypes.data, toks_.ctypes.data, 3,
+                                    max_pages, host_ptr, ctypes.addressof(host), nbytes,
+                                    None, None, None, None, None, 4, 2, 128, 0.1, None, None, 0,
+                                    None)
+
+    assert step(ids, toks, None, need) == pa.PA_ERR_INVALID_ARG           # no host tables
+    assert step(ids, toks, ctypes.addressof(host), need - 4) == pa.PA_ERR_INVALID_ARG
+    bad = np.array([2], dtype=np.int64)                                   # unknown request
+    assert step(bad, toks, ctypes.addressof(host), need) == pa.PA_ERR_INVALID_ARG
+    c2 = pa.KVCache(1, 4)                                                 # one page: 3 + 3 tokens do not fit
+    c2.add(1)
+    c2.plan([1], [3], 4, 3)
+    assert lib.pa_kv_cache_step(c2._h, 1, ids.ctypes.data, toks.ctypes.data, 3, 4,
+                                ctypes.addressof(host), ctypes.addressof(host), need,
+                                None, None, None, None, None, 4, 2, 128, 0.1, None, None, 0,
+                                None) == pa.PA_ERR_NO_PAGES
+    assert c.context_len(1) == 0 and c.free_pages == 8
+    assert c2.context_len(1) == 3 and c2.free_pages == 0
+    c.close()
+    c2.close()

@@ -242,10 +242,11 @@ size_t split_prefill_need(const pa_shape& s, int32_t page_size, const DeviceInfo
     return prefill_split_workspace_bytes(dev->sm_count);
 }
 
-// Prefill on tcgen05 (D = 128, page_size >= 8). With a workspace of at least
-// split_prefill_need bytes: the split kernel (K/V tiles spread evenly over
-// one block per SM); otherwise one block per (request, query head or head
-// pair, tile of 128 query rows).
+// Prefill on tcgen05 (D = 128, or D = 64 with at least two query heads per
+// KV group; page_size >= 8). With a workspace of at least split_prefill_need
+// bytes: the split kernel (K/V tiles spread evenly over one block per SM);
+// otherwise the persistent pairs kernel (whole (request, head pair, 128-row
+// query tile) items) or one block per (request, query head, query tile).
 pa_status run_prefill_tc(const void* query, const void* key_pages, const void* value_pages,
                          const int32_t* block_table, const int32_t* context_lens,
                          int32_t page_size, float scale, int causal, void* out,
@@ -268,10 +269,14 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     // us; with 256 pair items the pairs kernel is 22-33 % faster).
     const int g = s.num_q_heads / s.num_kv_heads;
     const int64_t pair_items = prefill_pair_items(s);
-    bool pairs = t_prefill_variant != 1 && g >= 2 &&
-                 (g % 2 == 0 || t_prefill_variant == 2 || pair_items >= dev->sm_count);
-    if (pairs && prefill_pairs_smem_bytes() > size_t(dev->max_smem_optin))
+    const bool d64 = s.head_dim == 64;   // only the pairs kernel has the 64-column form
+    bool pairs = g >= 2 && (d64 || (t_prefill_variant != 1 &&
+                                    (g % 2 == 0 || t_prefill_variant == 2 ||
+                                     pair_items >= dev->sm_count)));
+    if (pairs && prefill_pairs_smem_bytes(s.head_dim) > size_t(dev->max_smem_optin))
         pairs = false;
+    if (d64 && !pairs)
+        return PA_ERR_UNSUPPORTED;
     if (!pairs && prefill_smem_bytes() > size_t(dev->max_smem_optin))
         return PA_ERR_UNSUPPORTED;
     const int64_t n_qtiles = (int64_t(s.q_len) + 127) / 128;
@@ -282,9 +287,10 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     const uint32_t box = uint32_t(page_size < 128 ? page_size : 128);
     CUtensorMap qmap, kmap, vmap;
     const uint64_t kv_rows = uint64_t(s.num_pages) * s.num_kv_heads * page_size;
-    if ((st = encode_rows_map(&qmap, query, uint64_t(q_rows), 128u)) != PA_OK ||
-        (st = encode_rows_map(&kmap, key_pages, kv_rows, box)) != PA_OK ||
-        (st = encode_rows_map(&vmap, value_pages, kv_rows, box)) != PA_OK)
+    const uint32_t cols = uint32_t(s.head_dim);
+    if ((st = encode_rows_map(&qmap, query, uint64_t(q_rows), 128u, cols)) != PA_OK ||
+        (st = encode_rows_map(&kmap, key_pages, kv_rows, box, cols)) != PA_OK ||
+        (st = encode_rows_map(&vmap, value_pages, kv_rows, box, cols)) != PA_OK)
         return st;
     PrefillArgs a;
     memset(&a, 0, sizeof a);
@@ -305,6 +311,7 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     a.scale_log2 = scale * 1.4426950408889634f;
     a.causal = causal ? 1 : 0;
     a.out_scale = out_scale;
+    a.D = s.head_dim;
     if (split) {
         SplitPrefillArgs sa;
         memset(&sa, 0, sizeof sa);
@@ -341,8 +348,11 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     }
     cudaError_t e = pairs ? launch_prefill_pairs(qmap, kmap, vmap, a, dev->id, dev->sm_count, stream)
                           : launch_prefill(qmap, kmap, vmap, a, dev->id, stream);
-    if (pairs && e == cudaErrorNotSupported)   // register split not available: one head per block
-        e = launch_prefill(qmap, kmap, vmap, a, dev->id, stream);
+    if (pairs && e == cudaErrorNotSupported) {   // register split not available
+        if (d64)
+            return PA_ERR_UNSUPPORTED;
+        e = launch_prefill(qmap, kmap, vmap, a, dev->id, stream);   // one head per block
+    }
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -853,12 +863,16 @@ pa_status pa_prefill(const void* query, const void* key_pages, const void* value
                                    page_size, scale, out, shape);
     if (st != PA_OK)
         return st;
-    if (shape.head_dim == 128 && page_size >= 8)
-        return run_prefill_tc(query, key_pages, value_pages, block_table, context_lens,
-                              page_size, scale, causal, out, shape,
-                              static_cast<cudaStream_t>(stream));
-    // D = 64 or pages smaller than 8 tokens: the split-KV kernel with whole
-    // segments per block.
+    const bool d64_pairs = shape.head_dim == 64 && shape.num_q_heads >= 2 * shape.num_kv_heads;
+    if ((shape.head_dim == 128 || d64_pairs) && page_size >= 8) {
+        st = run_prefill_tc(query, key_pages, value_pages, block_table, context_lens, page_size,
+                            scale, causal, out, shape, static_cast<cudaStream_t>(stream));
+        if (st != PA_ERR_UNSUPPORTED || shape.head_dim == 128)
+            return st;
+    }
+    // Pages smaller than 8 tokens, or D = 64 with one query head per KV group
+    // (or without the pairs kernel's register split): the split-KV kernel
+    // with whole segments per block.
     return run_split_kv(query, key_pages, value_pages, block_table, context_lens, page_size,
                         scale, causal, out, shape, 0, nullptr, 0, 1,
                         static_cast<cudaStream_t>(stream));

@@ -119,7 +119,7 @@ cudaError_t launch_decode(const CUtensorMap& key_map, const CUtensorMap& value_m
 // Prefill on the 5th-generation tensor cores (D = 128, page_size >= 8)
 
 struct PrefillArgs {
-    uint16_t* out;                // [B, H_q, L, 128]
+    uint16_t* out;                // [B, H_q, L, D]
     const int32_t* block_table;   // [B, max_pages]
     const int32_t* context_lens;  // [B]
     unsigned* err;
@@ -130,6 +130,7 @@ struct PrefillArgs {
     float scale_log2;
     int32_t causal;
     float out_scale;    // the output is out_scale * softmax . V (e4m3 copies: v_scale)
+    int32_t D;          // head_dim: 128 (64 on the pairs kernel only)
 };
 
 // Prefill over e4m3 pools: bf16 copies of the visible K/V tokens, in pages
@@ -185,7 +186,7 @@ cudaError_t launch_prefill_split(const CUtensorMap& q_map, const CUtensorMap& ke
                                  void* workspace, int device, cudaStream_t stream);
 
 size_t prefill_smem_bytes();
-size_t prefill_pairs_smem_bytes();
+size_t prefill_pairs_smem_bytes(int D);
 cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& key_map,
                                  const CUtensorMap& value_map, const PrefillArgs& a, int device,
                                  int sm_count, cudaStream_t stream);

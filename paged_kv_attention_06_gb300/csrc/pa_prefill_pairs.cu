@@ -81,9 +81,12 @@ constexpr uint32_t kPCol = 64;        // P_h: columns [64, 128) of head h's scor
 // Items a block can take; the host sizes the grid so that no block gets more.
 constexpr int kMaxItems = 32;
 
+// kD: head_dim, 128 or 64 (two or one 64-column halves per matrix row).
+template <int kD>
 struct Layout {
     static constexpr int kHalf = 128 * 128;        // 128 rows x 64 bf16 (128 B)
-    static constexpr int kMat = 2 * kHalf;         // 128 x 128 bf16, [half][row][128 B]
+    static constexpr int kHalves = kD / 64;
+    static constexpr int kMat = kHalves * kHalf;   // 128 x kD bf16, [half][row][128 B]
     static constexpr int kQ = 0;                   // [head] matrices
     static constexpr int kK = kQ + 2 * kMat;       // 2 stages
     static constexpr int kV = kK + 2 * kMat;       // 2 stages
@@ -109,7 +112,7 @@ constexpr int kSFull = 12;    // + head (2)
 constexpr int kPFull = 14;    // + head
 constexpr int kPVDone = 16;   // + head
 constexpr int kMmaDone = 18;
-static_assert(kMmaDone < Layout::kNumBars, "barrier count");
+static_assert(kMmaDone < Layout<128>::kNumBars, "barrier count");
 
 // Item table entry: request, query tile, the two query heads, the KV head,
 // the (clamped) context length, K/V tiles visited, whether head 1 repeats
@@ -121,23 +124,27 @@ enum { kEB = 0, kET, kEH0, kEH1, kEHK, kEN, kENT, kEDup };
 // [d half][128 keys][128 B] (V): k-step kk (16 keys) starts 16 rows in.
 __host__ __device__ constexpr uint32_t kmajor_off(int kk)
 {
-    return uint32_t(kk >> 2) * Layout::kHalf + uint32_t(kk & 3) * 32u;
+    return uint32_t(kk >> 2) * Layout<128>::kHalf + uint32_t(kk & 3) * 32u;
 }
 __host__ __device__ constexpr uint32_t mnmajor_off(int kk) { return uint32_t(kk) * 16u * 128u; }
 __device__ __forceinline__ uint64_t kmajor_base(uint32_t saddr) { return smem_desc_sw128(saddr, 16u, 1024u); }
 __device__ __forceinline__ uint64_t mnmajor_base(uint32_t saddr)
 {
-    return smem_desc_sw128(saddr, uint32_t(Layout::kHalf), 1024u);
+    return smem_desc_sw128(saddr, uint32_t(Layout<128>::kHalf), 1024u);
 }
 
 // kOdd: the group size is odd and the last pair of each group repeats its
 // last head (a separate instantiation, so that even groups keep their code).
-template <bool kOdd>
+// kD: head_dim (128, or 64: one 64-column half per Q, K and V row, four
+// k-steps for S, N = 64 for P V and 64 of O's TMEM columns).
+template <bool kOdd, int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pairs_kernel(const __grid_constant__ CUtensorMap q_map,
                          const __grid_constant__ CUtensorMap key_map,
                          const __grid_constant__ CUtensorMap value_map, const PrefillArgs a)
 {
+    using Layout = pa::Layout<kD>;
+    constexpr int kKSteps = kD / 16;                 // k-steps of S = Q K^T
     grid_dependency_wait();  // the previous kernel's outputs are visible from here on
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -334,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool ok = mbar_wait_warp(&bar[empty], ((gj >> 1) & 1) ^ 1u, misc, a.err);
                     if (ok) {
                         if (lane == 0)
-                            mbar_arrive_expect_tx(&bar[full], uint32_t(mine) * box * 128u * 2u);
+                            mbar_arrive_expect_tx(&bar[full], uint32_t(mine) * box * 128u * Layout::kHalves);
                         __syncwarp();
                         if (my_box < nbox) {
                             const int row = pool_row(j, phys);
@@ -342,7 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          my_box * box * 128;
                             const CUtensorMap* m = is_v ? &value_map : &key_map;
                             tma_load_2d(d, m, 0, row, &bar[full], policy);
-                            tma_load_2d(d + Layout::kHalf, m, 64, row, &bar[full], policy);
+                            if constexpr (kD == 128)
+                                tma_load_2d(d + Layout::kHalf, m, 64, row, &bar[full], policy);
                         }
                     }
                     __syncwarp();
@@ -359,7 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int qrow = (b * a.H_q + e[li == 0 ? kEH0 : kEH1]) * a.L + e[kET] * kRows;
                         uint8_t* d = smem + Layout::kQ + li * Layout::kMat;
                         tma_load_2d(d, &q_map, 0, qrow, &bar[kQFull + li], policy);
-                        tma_load_2d(d + Layout::kHalf, &q_map, 64, qrow, &bar[kQFull + li], policy);
+                        if constexpr (kD == 128)
+                            tma_load_2d(d + Layout::kHalf, &q_map, 64, qrow, &bar[kQFull + li], policy);
                     }
                     __syncwarp();
                 };
@@ -405,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (the next K and V tiles) are taken after the commits of a tile.
             const bool leader = elect_one();
             const uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0);
-            const uint32_t idesc_pv = idesc_bf16_f32(kRows, 128, 1);
+            const uint32_t idesc_pv = idesc_bf16_f32(kRows, kD, 1);
             // Base descriptors built once; every k-step is one add.
             const uint64_t dq0 = kmajor_base(sQ), dq1 = desc_advance(dq0, Layout::kMat);
             const uint64_t dk0 = kmajor_base(sK), dk1 = desc_advance(dk0, Layout::kMat);
@@ -416,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t db = (gj & 1) ? dk1 : dk0;
                     const uint32_t d = tmem + col_s(h);
     #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
+                    for (int kk = 0; kk < kKSteps; ++kk)
                         tc_mma_bf16(d, desc_advance(da, kmajor_off(kk)), desc_advance(db, kmajor_off(kk)),
                                     idesc_s, kk > 0);
                 }
@@ -625,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // scores no longer occupy registers).
                 if (j >= 1 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
+                    for (int q4 = 0; q4 < kD / 32; ++q4) {
                         uint32_t ov[32];
                         tmem_ld32(to + 32u * q4, ov);
                         tmem_wait_ld();
@@ -641,10 +650,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (head == 0 && n < key0 + kKeys) {
                     mbar_wait_bounded(&bar[kVFull + (gj & 1)], (gj >> 1) & 1, misc, a.err);
                     const int z0 = max(0, n - key0);
-                    const int nz = (kKeys - z0) * 16;    // 16-byte chunks
+                    constexpr int kRowChunks = kD / 8;    // 16-byte chunks per V row
+                    const int nz = (kKeys - z0) * kRowChunks;
                     uint8_t* vb = smem + Layout::kV + (gj & 1) * Layout::kMat;
                     for (int idx = r; idx < nz; idx += 128) {
-                        const int zr = z0 + idx / 16, ch = idx % 16;
+                        const int zr = z0 + idx / kRowChunks, ch = idx % kRowChunks;
                         *reinterpret_cast<uint4*>(vb + (ch >> 3) * Layout::kHalf + zr * 128 +
                                                   (((ch & 7) ^ (zr & 7)) << 4)) = make_uint4(0, 0, 0, 0);
                     }
@@ -663,13 +673,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint16_t* out_warp =
                 a.out + ((int64_t(e[kEB]) * a.H_q + e[head == 0 ? kEH0 : kEH1]) * a.L + row0 + w4 * 32) *
-                            128;
+                            kD;
             int rows_ok = rows - w4 * 32;
             rows_ok = rows_ok > 32 ? 32 : rows_ok;
             if (misc[0] != 0 || (head == 1 && e[kEDup]))
                 rows_ok = 0;                      // a wait gave up, or the duplicate head
 #pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
+            for (int hf = 0; hf < Layout::kHalves; ++hf) {
                 uint32_t pk[32];                  // columns 64 hf .. 64 hf + 63 of this row
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
@@ -698,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int rw = idx >> 3, cq = idx & 7;
                     const uint4 v = *reinterpret_cast<const uint4*>(stage + rw * 128 + ((cq ^ (rw & 7)) << 4));
                     if (rw < rows_ok)
-                        *reinterpret_cast<uint4*>(out_warp + int64_t(rw) * 128 + hf * 64 + cq * 8) = v;
+                        *reinterpret_cast<uint4*>(out_warp + int64_t(rw) * kD + hf * 64 + cq * 8) = v;
                 }
                 __syncwarp();
             }
@@ -718,26 +728,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t prefill_pairs_smem_bytes() { return size_t(Layout::kBytes); }
+size_t prefill_pairs_smem_bytes(int D)
+{
+    return D == 64 ? size_t(Layout<64>::kBytes) : size_t(Layout<128>::kBytes);
+}
 
-cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& key_map,
-                                 const CUtensorMap& value_map, const PrefillArgs& a, int device,
-                                 int sm_count, cudaStream_t stream)
+namespace {
+
+// Register split and shared-memory limit checked once per device and
+// instantiation, then the launch.
+template <bool kOdd, int kD>
+cudaError_t launch_pairs(const cudaLaunchConfig_t& cfg_in, const CUtensorMap& q_map,
+                         const CUtensorMap& key_map, const CUtensorMap& value_map,
+                         const PrefillArgs& a, int device)
 {
     constexpr int kMaxDev = 64;
-    static std::atomic<int> smem_set[kMaxDev][2];
+    static std::atomic<int> smem_set[kMaxDev];
+    static std::atomic<int> regs_ok[kMaxDev];
     if (device < 0 || device >= kMaxDev)
         return cudaErrorInvalidDevice;
-    const bool odd = a.G % 2 != 0;
-    const void* fn = odd ? reinterpret_cast<const void*>(prefill_pairs_kernel<true>)
-                         : reinterpret_cast<const void*>(prefill_pairs_kernel<false>);
-    const int smem = Layout::kBytes;
+    const void* fn = reinterpret_cast<const void*>(prefill_pairs_kernel<kOdd, kD>);
+    const int smem = Layout<kD>::kBytes;
     // The register split needs 128 x kRegsProducer + 256 x kRegsSoftmax
     // registers out of the launch's own 384 x numRegs, a launch count no
     // higher than kRegsSoftmax (the increase must be one) and no lower than
     // kRegsProducer; otherwise the increase would wait forever.
-    static std::atomic<int> regs_ok[kMaxDev][2];
-    int rk = regs_ok[device][odd].load(std::memory_order_relaxed);
+    int rk = regs_ok[device].load(std::memory_order_relaxed);
     if (rk == 0) {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, fn);
@@ -746,16 +762,29 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
         const bool fits = fa.numRegs >= kRegsProducer && fa.numRegs <= kRegsSoftmax &&
                           128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * fa.numRegs;
         rk = fits ? 1 : 2;
-        regs_ok[device][odd].store(rk, std::memory_order_relaxed);
+        regs_ok[device].store(rk, std::memory_order_relaxed);
     }
     if (rk != 1)
         return cudaErrorNotSupported;
-    if (smem_set[device][odd].load(std::memory_order_relaxed) < smem) {
+    if (smem_set[device].load(std::memory_order_relaxed) < smem) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        smem_set[device][odd].store(smem, std::memory_order_relaxed);
+        smem_set[device].store(smem, std::memory_order_relaxed);
     }
+    cudaLaunchConfig_t cfg = cfg_in;
+    cfg.dynamicSmemBytes = size_t(smem);
+    return cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<kOdd, kD>, q_map, key_map, value_map, a);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& key_map,
+                                 const CUtensorMap& value_map, const PrefillArgs& a, int device,
+                                 int sm_count, cudaStream_t stream)
+{
+    if (a.D != 64 && a.D != 128)
+        return cudaErrorInvalidValue;
     // One block per SM (one fits), each taking whole items; more blocks only
     // when an SM would get more than kMaxItems items.
     const int64_t n_items = int64_t(a.B) * a.H_kv * ((a.G + 1) / 2) * a.n_qtiles;
@@ -774,14 +803,15 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = size_t(smem);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e =
-        odd ? cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<true>, q_map, key_map, value_map, a)
-            : cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<false>, q_map, key_map, value_map, a);
-    return e;
+    const bool odd = a.G % 2 != 0;
+    if (a.D == 64)
+        return odd ? launch_pairs<true, 64>(cfg, q_map, key_map, value_map, a, device)
+                   : launch_pairs<false, 64>(cfg, q_map, key_map, value_map, a, device);
+    return odd ? launch_pairs<true, 128>(cfg, q_map, key_map, value_map, a, device)
+               : launch_pairs<false, 128>(cfg, q_map, key_map, value_map, a, device);
 }
 
 }  // namespace pa

@@ -107,9 +107,9 @@ def test_multirow_workspace_contents_and_relabelling():
 
 
 @pytest.mark.parametrize("L,causal", [(40, True), (100, False), (257, True)])
-def test_prefill_route_head_dim64_whole_segments(L, causal):
-    """head_dim 64 prefill runs the split-KV kernel with whole segments per
-    block; with G L / 16 tiles per KV group it now takes four per segment."""
+def test_prefill_route_head_dim64(L, causal):
+    """head_dim 64 prefill through pa_prefill at several lengths, causal and
+    not (the pairs kernel's 64-column form at G = 4)."""
     b = wl.build_batch("prefill64", B=3, H_q=8, H_kv=2, D=64, page_size=16, L=L,
                        context_lens=[L, L + 100, L + 700], seed=L, causal=causal)
     db = DeviceBatch(b)
@@ -117,6 +117,19 @@ def test_prefill_route_head_dim64_whole_segments(L, causal):
     check_no_device_error()
     kp, vp = oracle_pages(b)
     assert_close(host_f64(out), oracle_out(b, kp, vp), f"prefill D=64 L={L}")
+
+
+@pytest.mark.parametrize("L", [40, 257])
+def test_prefill_head_dim64_one_head_per_group_whole_segments(L):
+    """head_dim 64 with one query head per KV group has no pairs: the split-KV
+    kernel with whole segments per block (four row tiles per segment)."""
+    b = wl.build_batch("prefill64g1", B=3, H_q=4, H_kv=4, D=64, page_size=16, L=L,
+                       context_lens=[L, L + 100, L + 700], seed=L + 1, causal=True)
+    db = DeviceBatch(b)
+    out = gpu_step(db, route="prefill")
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), f"prefill D=64 G=1 L={L}")
 
 
 @pytest.mark.parametrize("L,H_q,H_kv,max_len", [(12, 28, 4, 3000), (24, 28, 4, 3000),

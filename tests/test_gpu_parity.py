@@ -301,6 +301,23 @@ def test_tc_prefill_page_sizes(ps, causal, H_q, H_kv, prefill_variant):
     assert_close(host_f64(out), oracle_out(b, kp, vp), f"tc prefill ps={ps} causal={causal}")
 
 
+@pytest.mark.parametrize("ps", [8, 16, 128, 256])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("H_q,H_kv", [(8, 2), (6, 2), (4, 1)])   # groups of 4 / 3 / 4
+def test_tc_prefill_head_dim64(ps, causal, H_q, H_kv):
+    """head_dim 64 on the pairs kernel (one 64-column half per row, four
+    k-steps for the scores, N = 64 for P V): several query tiles, a ragged
+    last tile, contexts across page boundaries, odd and even groups."""
+    lens = [200, 129, 700, 300]
+    b = wl.build_batch("tcprefill64", B=4, H_q=H_q, H_kv=H_kv, D=64, page_size=ps, L=129,
+                       context_lens=lens, seed=ps + 3 * int(causal) + H_q, causal=causal,
+                       placement="churn")
+    out = gpu_step(DeviceBatch(b), route="prefill")
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), f"tc prefill D=64 ps={ps} causal={causal}")
+
+
 @pytest.mark.parametrize("H_q,H_kv", [(28, 4), (10, 2)])   # groups of 7 / 5
 def test_tc_prefill_odd_groups(H_q, H_kv, prefill_variant):
     """Odd group sizes: the head-pairs kernel runs each group's last head in a

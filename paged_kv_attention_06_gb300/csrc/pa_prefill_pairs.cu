@@ -145,7 +145,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using Layout = pa::Layout<kD>;
     constexpr int kKSteps = kD / 16;                 // k-steps of S = Q K^T
-    grid_dependency_wait();  // the previous kernel's outputs are visible from here on
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -155,6 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t* items = reinterpret_cast<int32_t*>(smem + Layout::kItems);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+
+    grid_dependency_wait();  // the previous kernel's outputs are visible from here on
 
     // ---- this block's items ---------------------------------------------------
     // Items in rank order: the (request, query tile) pairs sorted by the number
@@ -272,6 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bar[kMmaDone], 1);
         fence_barrier_init();
+        prefetch_tensormap(&q_map);
+        prefetch_tensormap(&key_map);
+        prefetch_tensormap(&value_map);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
@@ -281,6 +285,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The Q tiles of the block's first item with K/V tiles go out now, while
+    // the loaders still fetch its first page ids (the loaders load every later
+    // item's Q).
+    if (threadIdx.x == 0) {
+        int it0 = 0;
+        while (it0 < n_items && items[it0 * 8 + kENT] == 0)
+            ++it0;
+        if (it0 < n_items) {
+            const int32_t* e = items + it0 * 8;
+            const uint64_t policy = l2_policy_evict_last();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                mbar_arrive_expect_tx(&bar[kQFull + h], uint32_t(Layout::kMat));
+                const int qrow = (e[kEB] * a.H_q + e[h == 0 ? kEH0 : kEH1]) * a.L + e[kET] * kRows;
+                uint8_t* d = smem + Layout::kQ + h * Layout::kMat;
+                tma_load_2d(d, &q_map, 0, qrow, &bar[kQFull + h], policy);
+                if constexpr (kD == 128)
+                    tma_load_2d(d + Layout::kHalf, &q_map, 64, qrow, &bar[kQFull + h], policy);
+            }
+        }
+    }
     // Registers from the loader / MMA warpgroup (warps 0-3) to the two softmax
     // warpgroups: 128 x kRegsProducer + 256 x kRegsSoftmax <= 384 x the launch
     // count (checked on the host before every launch). Each change sits at the
@@ -296,11 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // K/V tiles are read again by the other query tiles and head pairs
             // of the same request and KV group: keep them in L2.
             const uint64_t policy = l2_policy_evict_last();
-            if (lane == 0 && li == 0) {
-                prefetch_tensormap(&q_map);
-                prefetch_tensormap(&key_map);
-                prefetch_tensormap(&value_map);
-            }
             const int box = a.box_rows;                  // min(ps, 128)
             const int my_box = li + 3 * lane;
             int g = 0;                                   // tiles of the block before this item
@@ -375,12 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int pg[3];
                 pg[0] = fetch_page(0);
                 pg[1] = fetch_page(1);
-                // The block's first item: its Q buffers are free, so Q goes out
-                // while the page ids of K_0 are still loading.
-                if (li < 2 && qk == 0)
-                    load_q();
                 load(0, false, pg[0]);
-                if (li < 2 && qk > 0)
+                if (li < 2 && qk > 0)    // the first item's Q went out at the start
                     load_q();
                 for (int j0 = 0; j0 < nt; j0 += 3) {
     #pragma unroll

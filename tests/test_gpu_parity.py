@@ -318,6 +318,24 @@ def test_tc_prefill_head_dim64(ps, causal, H_q, H_kv):
     assert_close(host_f64(out), oracle_out(b, kp, vp), f"tc prefill D=64 ps={ps} causal={causal}")
 
 
+@pytest.mark.parametrize("H_q,H_kv", [(4, 2), (6, 2), (16, 2)])   # 1600 / 3200 / 6400 items
+def test_tc_prefill_many_query_tiles_unranked(H_q, H_kv):
+    """More (request, query tile) pairs than the pairs kernel ranks (384):
+    400 requests of two query tiles take the tiles last to first without the
+    ranking, and more items than 32 per SM grow the grid; every request's
+    first, boundary and last rows against the oracle."""
+    rng = np.random.default_rng(31)
+    lens = [int(x) for x in rng.integers(130, 420, 400)]
+    b = wl.build_batch("manytiles", B=400, H_q=H_q, H_kv=H_kv, D=128, page_size=16, L=130,
+                       context_lens=lens, seed=32, L_new=0, placement="churn")
+    out = host_f64(gpu_step(DeviceBatch(b), route="prefill"))
+    check_no_device_error()
+    rows = np.asarray([(r, h, i) for r in range(b.B) for h in range(b.H_q)
+                       for i in (0, 127, 128, 129)], dtype=np.int32)
+    got = out[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(got, oracle_out(b, b.key_pages, b.value_pages, rows=rows), "tc prefill 800 tiles")
+
+
 @pytest.mark.parametrize("H_q,H_kv", [(28, 4), (10, 2)])   # groups of 7 / 5
 def test_tc_prefill_odd_groups(H_q, H_kv, prefill_variant):
     """Odd group sizes: the head-pairs kernel runs each group's last head in a

@@ -336,6 +336,18 @@ def test_tc_prefill_many_query_tiles_unranked(H_q, H_kv):
     assert_close(got, oracle_out(b, b.key_pages, b.value_pages, rows=rows), "tc prefill 800 tiles")
 
 
+def test_tc_prefill_head_dim64_rows_without_keys():
+    """head_dim 64 on the pairs kernel: contexts of 0, 50 and 199 tokens under
+    200 query rows (rows at negative positions see no key: zeros), page size 8."""
+    b = wl.build_batch("tcempty64", B=3, H_q=8, H_kv=2, D=64, page_size=8, L=200,
+                       context_lens=[0, 50, 199], seed=41, L_new=0)
+    out = host_f64(gpu_step(DeviceBatch(b), route="prefill"))
+    check_no_device_error()
+    assert np.all(out[0] == 0)
+    assert np.all(out[1, :, :150] == 0) and np.all(out[2, :, :1] == 0)
+    assert_close(out, oracle_out(b, b.key_pages, b.value_pages), "tc prefill D=64 empty rows")
+
+
 @pytest.mark.parametrize("H_q,H_kv", [(28, 4), (10, 2)])   # groups of 7 / 5
 def test_tc_prefill_odd_groups(H_q, H_kv, prefill_variant):
     """Odd group sizes: the head-pairs kernel runs each group's last head in a

@@ -243,8 +243,8 @@ pa_status pa_append_kv_fp8(const void *key, const void *value, void *key_pages,
  * bf16 pools) and multiplies on the tensor cores in f16, into which e4m3
  * values convert exactly; the query is taken in f16 too, so its elements
  * must have magnitudes within f16's range (below 65504; below 2^-14 they keep
- * fewer bits). A NaN code in a visible slot reads as 480 (times the scale),
- * not NaN; slots past a request's context are never read. Any query length;
+ * fewer bits). A NaN code in a visible slot gives NaN; slots past a
+ * request's context are never read. Any query length;
  * for prefill chunks pa_prefill_fp8 is the faster call.
  */
 pa_status pa_decode_fp8(const void *query, const void *key_pages, const void *value_pages,

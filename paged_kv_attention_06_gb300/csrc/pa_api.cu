@@ -451,11 +451,12 @@ pa_status run_split_kv(const void* query, const void* key_pages, const void* val
     a.swz = a.box_rows >= 8 ? 7 : 0;
     a.whole_segments = whole_segments;
     a.dense = dense;
-    // e4m3 pages: the kernel's K and V fragments hold code values / 256
-    a.scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_scale * 256.f : 1.f);
+    // e4m3 pages: the kernel's K and V fragments hold the code values; the
+    // per-tensor scales go into the softmax scale and the output
+    a.scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
     a.causal = causal ? 1 : 0;
     a.fp8 = fp8 ? 1 : 0;
-    a.v_scale = fp8 ? v_scale * 256.f : 1.f;
+    a.v_scale = fp8 ? v_scale : 1.f;
     a.debug_unset_wait = t_arm_unset_wait ? 1 : 0;
     t_arm_unset_wait = false;
     CUtensorMap qmap;

@@ -548,8 +548,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         // o = sum l_w 2^(m_w - M) (O_w / l_w). Every warp then
         // holds its D/4 columns, as in the bf16 schedule, and the same
         // epilogue follows.
-        //   * Codes become f16 holding value / 256 by moving their bits into
-        //     the f16 fields (exact); the host folds the 256 into the scales.
+        //   * Codes become f16 (exact) two at a time with one conversion
+        //     instruction; k_scale and v_scale stay in the softmax scale and
+        //     the output.
         //   * K: ldmatrix (no transpose) of 8 byte rows gives lane (row0,
         //     quad) the codes of token row0 at d = 16 kk + 4 quad .. + 3; their
         //     two halves are the two f16 B registers when the head dimension
@@ -642,8 +643,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                             for (int u = 0; u < 4; ++u)
                                 mma_f16_16816(sc[u & 1], qa[kp + (u >> 1)],
-                                              e4m3_spread_to_f16x2_div256(__byte_perm(r4[u], 0u, 0x4140u)),
-                                              e4m3_spread_to_f16x2_div256(__byte_perm(r4[u], 0u, 0x4342u)));
+                                              e4m3x2_to_f16x2(r4[u]),
+                                              e4m3x2_to_f16x2(r4[u] >> 16));
                         }
                     }
                     if (t0 + r_lo + kWT - 1 > lim_min) {
@@ -712,11 +713,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                                 const int c = cp + u;
                                 const uint32_t lo = r4[2 * u], hi = r4[2 * u + 1];
                                 mma_f16_16816(o[2 * c], pa,
-                                              e4m3_spread_to_f16x2_div256(__byte_perm(lo, 0u, 0x4240u)),
-                                              e4m3_spread_to_f16x2_div256(__byte_perm(hi, 0u, 0x4240u)));
+                                              e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0020u)),
+                                              e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0020u)));
                                 mma_f16_16816(o[2 * c + 1], pa,
-                                              e4m3_spread_to_f16x2_div256(__byte_perm(lo, 0u, 0x4341u)),
-                                              e4m3_spread_to_f16x2_div256(__byte_perm(hi, 0u, 0x4341u)));
+                                              e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0031u)),
+                                              e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0031u)));
                             }
                         }
                     }

@@ -269,13 +269,15 @@ __device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint3
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two e4m3 codes, in bytes 0 and 2 of y, -> two f16 holding value / 256, for
-// every finite code exactly: the code's exponent and mantissa bits are moved
-// into the f16 fields, and the f16 bias (15, against 7) divides by 2^8;
-// e4m3 subnormals land on f16 subnormals. A NaN code reads as 480 / 256.
-__device__ __forceinline__ uint32_t e4m3_spread_to_f16x2_div256(uint32_t y)
+// Two e4m3 codes (bits 0-7 and 8-15 of w) -> two f16, the first in the lower
+// half: one conversion instruction, exact for every code (every e4m3 value,
+// subnormals included, is an f16 value; a NaN code gives NaN).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w)
 {
-    return ((y << 7) & 0x3F803F80u) | ((y << 8) & 0x80008000u);
+    uint32_t r;
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n}"
+        : "=r"(r) : "r"(w));
+    return r;
 }
 
 // Two fp32 -> two e4m3 codes (round to nearest even, saturated to +-448),

@@ -644,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                             for (int u = 0; u < 4; ++u)
                                 mma_f16_16816(sc[u & 1], qa[kp + (u >> 1)],
                                               e4m3x2_to_f16x2(r4[u]),
-                                              e4m3x2_to_f16x2(r4[u] >> 16));
+                                              e4m3x2_hi_to_f16x2(r4[u]));
                         }
                     }
                     if (t0 + r_lo + kWT - 1 > lim_min) {

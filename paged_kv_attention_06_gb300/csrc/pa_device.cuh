@@ -279,6 +279,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w)
         : "=r"(r) : "r"(w));
     return r;
 }
+// The same for the codes in bits 16-31 of w.
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w)
+{
+    uint32_t r;
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.rn.f16x2.e4m3x2 %0, hi;\n}"
+        : "=r"(r) : "r"(w));
+    return r;
+}
 
 // Two fp32 -> two e4m3 codes (round to nearest even, saturated to +-448),
 // the first in the lower byte.

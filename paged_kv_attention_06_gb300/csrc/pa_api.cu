@@ -220,6 +220,25 @@ pa_status encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uin
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// 3-D bf16 tensor map over the attention output [B * H_q, L, cols]: boxes of
+// 64 columns x 32 rows of one (request, head), 128-byte swizzle (the pairs
+// prefill kernel's output stores; rows past L are outside the map).
+pa_status encode_out_map(CUtensorMap* map, void* base, uint64_t heads, uint64_t L, uint32_t cols)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    pa_status st = get_encoder(&enc);
+    if (st != PA_OK)
+        return st;
+    const cuuint64_t dims[3] = {cuuint64_t(cols), cuuint64_t(L), cuuint64_t(heads)};
+    const cuuint64_t strides[2] = {cuuint64_t(cols) * 2, cuuint64_t(cols) * 2 * L};
+    const cuuint32_t box[3] = {64u, 32u, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 // Workspace the split prefill kernel needs for this shape on this device, or
 // 0 when the shape takes another prefill kernel (head_dim 64, pages of fewer
 // than 8 tokens, one query head per KV group, or shared memory too small).
@@ -288,9 +307,12 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     CUtensorMap qmap, kmap, vmap;
     const uint64_t kv_rows = uint64_t(s.num_pages) * s.num_kv_heads * page_size;
     const uint32_t cols = uint32_t(s.head_dim);
+    CUtensorMap omap;
     if ((st = encode_rows_map(&qmap, query, uint64_t(q_rows), 128u, cols)) != PA_OK ||
         (st = encode_rows_map(&kmap, key_pages, kv_rows, box, cols)) != PA_OK ||
-        (st = encode_rows_map(&vmap, value_pages, kv_rows, box, cols)) != PA_OK)
+        (st = encode_rows_map(&vmap, value_pages, kv_rows, box, cols)) != PA_OK ||
+        (st = encode_out_map(&omap, out, uint64_t(s.batch) * s.num_q_heads, uint64_t(s.q_len), cols)) !=
+            PA_OK)
         return st;
     PrefillArgs a;
     memset(&a, 0, sizeof a);
@@ -346,7 +368,7 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
         if (e == cudaErrorCooperativeLaunchTooLarge && !pending)
             (void)cudaGetLastError();
     }
-    cudaError_t e = pairs ? launch_prefill_pairs(qmap, kmap, vmap, a, dev->id, dev->sm_count, stream)
+    cudaError_t e = pairs ? launch_prefill_pairs(qmap, kmap, vmap, omap, a, dev->id, dev->sm_count, stream)
                           : launch_prefill(qmap, kmap, vmap, a, dev->id, stream);
     if (pairs && e == cudaErrorNotSupported) {   // register split not available
         if (d64)

@@ -187,9 +187,11 @@ cudaError_t launch_prefill_split(const CUtensorMap& q_map, const CUtensorMap& ke
 
 size_t prefill_smem_bytes();
 size_t prefill_pairs_smem_bytes(int D);
+// out_map: the output as a 3-D bf16 tensor {D, L, B * H_q}, boxes of 64
+// columns x 32 rows, 128-byte swizzle (the kernel stores through it).
 cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& key_map,
-                                 const CUtensorMap& value_map, const PrefillArgs& a, int device,
-                                 int sm_count, cudaStream_t stream);
+                                 const CUtensorMap& value_map, const CUtensorMap& out_map,
+                                 const PrefillArgs& a, int device, int sm_count, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& q_map, const CUtensorMap& key_map,
                            const CUtensorMap& value_map, const PrefillArgs& a, int device,
                            cudaStream_t stream);

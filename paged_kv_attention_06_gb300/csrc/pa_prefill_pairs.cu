@@ -42,7 +42,8 @@
 //     so the result is the same softmax). P (bf16, two per 32-bit column) is
 //     written over the upper 64 columns of the head's score buffer. V rows
 //     past the context are zeroed (by head 0's warps) before either P V. At
-//     the end of an item O / l -> bf16, through a staging buffer per warp.
+//     the end of an item O / l -> bf16, through a staging buffer per warp
+//     and a TMA store of each 32-row x 64-column box.
 //
 // TMEM (512 columns): S_0 [0, 128), S_1 [128, 256), O_0 [256, 384),
 // O_1 [384, 512). A score buffer holds P_h(j) until P_h(j) V_j completes;
@@ -141,7 +142,8 @@ template <bool kOdd, int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pairs_kernel(const __grid_constant__ CUtensorMap q_map,
                          const __grid_constant__ CUtensorMap key_map,
-                         const __grid_constant__ CUtensorMap value_map, const PrefillArgs a)
+                         const __grid_constant__ CUtensorMap value_map,
+                         const __grid_constant__ CUtensorMap out_map, const PrefillArgs a)
 {
     using Layout = pa::Layout<kD>;
     constexpr int kKSteps = kD / 16;                 // k-steps of S = Q K^T
@@ -276,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&q_map);
         prefetch_tensormap(&key_map);
         prefetch_tensormap(&value_map);
+        prefetch_tensormap(&out_map);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
@@ -552,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t to = trow + col_o(head);
         const float c = a.scale_log2;
         // Output rows go through a 4 KiB staging buffer per warp, 16-byte
-        // chunks swizzled by row, so that a warp stores four whole 128-byte row
-        // segments per instruction instead of 32 scattered 16-byte pieces.
+        // chunks swizzled by row as the output map's 128-byte swizzle wants;
+        // one lane then stores the warp's 32 rows x 64 columns by TMA.
         uint8_t* stage = smem + Layout::kStage + (warp - 4) * Layout::kStageWarp;
         int g = 0;                                   // tiles of the block before this item
         for (int it = 0; it < n_items; ++it) {
@@ -687,18 +690,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_warp(&bar[kPVDone + head], (g + nt - 1) & 1, misc, a.err);
                 tc_fence_after();
             }
-            uint16_t* out_warp =
-                a.out + ((int64_t(e[kEB]) * a.H_q + e[head == 0 ? kEH0 : kEH1]) * a.L + row0 + w4 * 32) *
-                            kD;
-            int rows_ok = rows - w4 * 32;
-            rows_ok = rows_ok > 32 ? 32 : rows_ok;
-            if (misc[0] != 0 || (head == 1 && e[kEDup]))
-                rows_ok = 0;                      // a wait gave up, or the duplicate head
+            // This warp's 32 rows: one TMA store of 32 rows x 64 columns per
+            // half from the staging buffer (rows past L are outside the output
+            // map's L extent and are not written).
+            const int oz = e[kEB] * a.H_q + e[head == 0 ? kEH0 : kEH1];
+            const bool write = rows - w4 * 32 > 0 && misc[0] == 0 && !(head == 1 && e[kEDup]);
 #pragma unroll 1
             for (int hf = 0; hf < Layout::kHalves; ++hf) {
-                uint32_t pk[32];                  // columns 64 hf .. 64 hf + 63 of this row
+                // the staging buffer's previous store has read it
+                if (lane == 0)
+                    tma_store_wait_read();
+                __syncwarp();
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
+                for (int q = 0; q < 2; ++q) {     // columns 64 hf + 32 q .. + 31 of this row
                     uint32_t ov[32];
                     if (nt > 0) {
                         tmem_ld32(to + 32u * (2 * hf + q), ov);
@@ -709,30 +713,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ov[k] = 0u;
                     }
 #pragma unroll
-                    for (int k = 0; k < 32; k += 2)
-                        pk[16 * q + k / 2] =
-                            pack_bf16x2(__uint_as_float(ov[k]) * inv, __uint_as_float(ov[k + 1]) * inv);
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int cq = 4 * q + c4;
+                        const uint32_t* o = ov + 8 * c4;
+                        *reinterpret_cast<uint4*>(stage + lane * 128 + ((cq ^ (lane & 7)) << 4)) = make_uint4(
+                            pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv),
+                            pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv),
+                            pack_bf16x2(__uint_as_float(o[4]) * inv, __uint_as_float(o[5]) * inv),
+                            pack_bf16x2(__uint_as_float(o[6]) * inv, __uint_as_float(o[7]) * inv));
+                    }
                 }
-#pragma unroll
-                for (int cq = 0; cq < 8; ++cq)
-                    *reinterpret_cast<uint4*>(stage + lane * 128 + ((cq ^ (lane & 7)) << 4)) =
-                        make_uint4(pk[4 * cq], pk[4 * cq + 1], pk[4 * cq + 2], pk[4 * cq + 3]);
+                fence_proxy_async_smem();
                 __syncwarp();
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int idx = jj * 32 + lane;
-                    const int rw = idx >> 3, cq = idx & 7;
-                    const uint4 v = *reinterpret_cast<const uint4*>(stage + rw * 128 + ((cq ^ (rw & 7)) << 4));
-                    if (rw < rows_ok)
-                        *reinterpret_cast<uint4*>(out_warp + int64_t(rw) * kD + hf * 64 + cq * 8) = v;
+                if (lane == 0 && write) {
+                    tma_store_3d(&out_map, stage, hf * 64, row0 + w4 * 32, oz);
+                    tma_store_commit();
                 }
-                __syncwarp();
             }
             // the O reads above are ordered before the next item's first P V
             // (issued once this warp arrives for that tile)
             tc_fence_before();
             g += nt;
         }
+        if (lane == 0)
+            tma_store_wait_all();     // every output store has landed
+        __syncwarp();
     }
 
     __syncthreads();
@@ -756,7 +761,7 @@ namespace {
 template <bool kOdd, int kD>
 cudaError_t launch_pairs(const cudaLaunchConfig_t& cfg_in, const CUtensorMap& q_map,
                          const CUtensorMap& key_map, const CUtensorMap& value_map,
-                         const PrefillArgs& a, int device)
+                         const CUtensorMap& out_map, const PrefillArgs& a, int device)
 {
     constexpr int kMaxDev = 64;
     static std::atomic<int> smem_set[kMaxDev];
@@ -790,14 +795,15 @@ cudaError_t launch_pairs(const cudaLaunchConfig_t& cfg_in, const CUtensorMap& q_
     }
     cudaLaunchConfig_t cfg = cfg_in;
     cfg.dynamicSmemBytes = size_t(smem);
-    return cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<kOdd, kD>, q_map, key_map, value_map, a);
+    return cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<kOdd, kD>, q_map, key_map, value_map, out_map,
+                              a);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& key_map,
-                                 const CUtensorMap& value_map, const PrefillArgs& a, int device,
-                                 int sm_count, cudaStream_t stream)
+                                 const CUtensorMap& value_map, const CUtensorMap& out_map,
+                                 const PrefillArgs& a, int device, int sm_count, cudaStream_t stream)
 {
     if (a.D != 64 && a.D != 128)
         return cudaErrorInvalidValue;
@@ -824,10 +830,10 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
     cfg.numAttrs = 1;
     const bool odd = a.G % 2 != 0;
     if (a.D == 64)
-        return odd ? launch_pairs<true, 64>(cfg, q_map, key_map, value_map, a, device)
-                   : launch_pairs<false, 64>(cfg, q_map, key_map, value_map, a, device);
-    return odd ? launch_pairs<true, 128>(cfg, q_map, key_map, value_map, a, device)
-               : launch_pairs<false, 128>(cfg, q_map, key_map, value_map, a, device);
+        return odd ? launch_pairs<true, 64>(cfg, q_map, key_map, value_map, out_map, a, device)
+                   : launch_pairs<false, 64>(cfg, q_map, key_map, value_map, out_map, a, device);
+    return odd ? launch_pairs<true, 128>(cfg, q_map, key_map, value_map, out_map, a, device)
+               : launch_pairs<false, 128>(cfg, q_map, key_map, value_map, out_map, a, device);
 }
 
 }  // namespace pa

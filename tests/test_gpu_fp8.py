@@ -166,9 +166,12 @@ def _run_prefill(b, kc, vc, k_scale, v_scale, rows=None, max_context_len=None):
     return got, ref
 
 
-@pytest.mark.parametrize("ps", [16, 1, 128])
+@pytest.mark.parametrize("ps", [16, 1, 2, 128, 256])
 @pytest.mark.parametrize("L,causal", [(64, True), (130, True), (257, False)])
 def test_prefill_fp8_matches_oracle(ps, L, causal):
+    """Pool pages of 1, 2, 16, 128 and 256 tokens (the copy gathers every
+    size into 128-token pages; at 256 a copy page is half a pool page); row
+    tiles with a ragged tail; causal and not."""
     lens = [L, L + 300, 700, 2 * L + 5]
     b, kc, vc = _fp8_batch("fp8pre", 4, 8, 2, ps, L, lens, seed=300 + L + ps, causal=causal)
     got, ref = _run_prefill(b, kc, vc, 0.05, 0.04)
@@ -176,7 +179,7 @@ def test_prefill_fp8_matches_oracle(ps, L, causal):
     assert_close(got, ref, f"fp8 prefill ps={ps} L={L} causal={causal}")
 
 
-@pytest.mark.parametrize("H_q,H_kv", [(6, 2), (4, 4)])   # group of 3 (pairs, last head repeated) / 1 (one head)
+@pytest.mark.parametrize("H_q,H_kv", [(6, 2), (4, 4), (14, 2)])   # groups of 3 and 7 (pairs, last head repeated) / 1 (one head)
 def test_prefill_fp8_odd_groups(H_q, H_kv):
     b, kc, vc = _fp8_batch("fp8pre1", 3, H_q, H_kv, 16, 100, [100, 333, 1000], seed=61)
     got, ref = _run_prefill(b, kc, vc, 0.02, 0.09)
@@ -205,6 +208,21 @@ def test_prefill_fp8_short_and_empty_contexts():
     assert np.all(got[0] == 0)                 # no keys at all
     assert np.all(got[1, :, :33] == 0)         # rows before the first key
     assert_close(got, ref, "fp8 prefill short contexts")
+
+
+def test_prefill_fp8_nan_code_in_a_visible_slot():
+    """A NaN code among the keys a row sees makes that row NaN; rows and
+    requests that do not see it stay finite."""
+    b, kc, vc = _fp8_batch("fp8nan", 2, 8, 2, 16, 40, [300, 200], seed=67)
+    kc = kc.copy()
+    pos = 270                                  # visible to rows 10.. of request 0 (causal)
+    kc[b.block_table[0, pos // 16], 1, pos % 16, 5] = 0x7F
+    got, _ = _run_prefill(b, kc, vc, 0.05, 0.05)
+    check_no_device_error()
+    first = pos - (300 - 40)                   # first row of request 0 that sees it
+    assert np.all(np.isnan(got[0, 4:8, first:]).any(axis=-1))   # heads of KV head 1
+    assert np.all(np.isfinite(got[0, 4:8, :first]))
+    assert np.all(np.isfinite(got[0, :4])) and np.all(np.isfinite(got[1]))
 
 
 def test_prefill_fp8_agrees_with_decode_kernel():

@@ -573,45 +573,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int gj = g + j;
                 mbar_wait_warp(&bar[kSFull + head], gj & 1, misc, a.err);
                 tc_fence_after();
-                // Scores in two halves of 64 columns (64 registers at a time):
-                // the maximum over both, then the exponentials of the upper half
-                // (still in registers), P of keys 64..127 over columns 96..127
-                // (scores already read), the lower half read again, P of keys
-                // 0..63 over columns 64..95. Columns 0..63 are never written, so
-                // every score is read before anything overwrites it.
+                // All 128 scores of the row in registers (four loads, one wait),
+                // their maximum, then P of keys 64..127 over columns 96..127 and
+                // of keys 0..63 over columns 64..95 (every score is read before
+                // P overwrites any). Reading the two 64-column halves one after
+                // the other, the lower half twice, was 0.9 us per call slower on
+                // the 512-row batch.
                 const int key0 = j * kKeys;
                 const bool edge = key0 + kKeys - 1 > lim;
-                uint32_t sv[64];
+                uint32_t sv[128];
                 float* s = reinterpret_cast<float*>(sv);
-                auto load_half = [&](int hf) {
-                    tmem_ld32(ts + 64u * hf, sv);
-                    tmem_ld32(ts + 64u * hf + 32u, sv + 32);
-                    tmem_wait_ld();
-                    if (edge) {
-                        // Keys past this row's last visible key -> -inf (by select).
 #pragma unroll
-                        for (int w = 0; w < 2; ++w) {
-                            const int nv = lim - (key0 + 64 * hf + 32 * w) + 1;   // visible keys
-                            const uint32_t vis = nv >= 32 ? 0xffffffffu : nv <= 0 ? 0u : (1u << nv) - 1u;
+                for (int w = 0; w < 4; ++w)
+                    tmem_ld32(ts + 32u * w, sv + 32 * w);
+                tmem_wait_ld();
+                if (edge) {
+                    // Keys past this row's last visible key -> -inf (by select).
 #pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                s[32 * w + k] = (vis >> k) & 1u ? s[32 * w + k] : -INFINITY;
-                        }
+                    for (int w = 0; w < 4; ++w) {
+                        const int nv = lim - (key0 + 32 * w) + 1;   // visible keys
+                        const uint32_t vis = nv >= 32 ? 0xffffffffu : nv <= 0 ? 0u : (1u << nv) - 1u;
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            s[32 * w + k] = (vis >> k) & 1u ? s[32 * w + k] : -INFINITY;
                     }
-                };
+                }
                 float m8[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     m8[u] = -INFINITY;
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    load_half(hf);
+                for (int k = 0; k < 128; k += 8)
 #pragma unroll
-                    for (int k = 0; k < 64; k += 8)
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            m8[u] = fmaxf(m8[u], s[k + u]);
-                }
+                    for (int u = 0; u < 8; ++u)
+                        m8[u] = fmaxf(m8[u], s[k + u]);
                 const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                        fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
                 const float mxs = mx * c;
@@ -633,15 +628,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        const float2 x = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), c2, nmu2);
+                        const float2 x = __ffma2_rn(make_float2(s[64 * hf + 2 * k], s[64 * hf + 2 * k + 1]), c2, nmu2);
                         const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                         lsum[k & 3] = __fadd2_rn(lsum[k & 3], pp);
                         pk[k] = pack_bf16x2(pp.x, pp.y);
                     }
                     tmem_st32(ts + kPCol + 32u * hf, pk);
                 };
-                exp_store(1);        // upper half, still in registers
-                load_half(0);
+                exp_store(1);
                 exp_store(0);
                 {
                     const float2 t2 =

@@ -719,36 +719,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int key0 = k * kKeys;
                 const bool edge = key0 + kKeys - 1 > lim;
-                uint32_t sv[64];
+                // All 128 scores of the row in registers (four loads, one wait).
+                uint32_t sv[128];
                 float* sc = reinterpret_cast<float*>(sv);
-                auto load_half = [&](int hf) {
-                    tmem_ld32(ts + 64u * hf, sv);
-                    tmem_ld32(ts + 64u * hf + 32u, sv + 32);
-                    tmem_wait_ld();
-                    if (edge) {
 #pragma unroll
-                        for (int w = 0; w < 2; ++w) {
-                            const int nv = lim - (key0 + 64 * hf + 32 * w) + 1;
-                            const uint32_t vis = nv >= 32 ? 0xffffffffu : nv <= 0 ? 0u : (1u << nv) - 1u;
+                for (int w = 0; w < 4; ++w)
+                    tmem_ld32(ts + 32u * w, sv + 32 * w);
+                tmem_wait_ld();
+                if (edge) {
 #pragma unroll
-                            for (int kq = 0; kq < 32; ++kq)
-                                sc[32 * w + kq] = (vis >> kq) & 1u ? sc[32 * w + kq] : -INFINITY;
-                        }
+                    for (int w = 0; w < 4; ++w) {
+                        const int nv = lim - (key0 + 32 * w) + 1;
+                        const uint32_t vis = nv >= 32 ? 0xffffffffu : nv <= 0 ? 0u : (1u << nv) - 1u;
+#pragma unroll
+                        for (int kq = 0; kq < 32; ++kq)
+                            sc[32 * w + kq] = (vis >> kq) & 1u ? sc[32 * w + kq] : -INFINITY;
                     }
-                };
+                }
                 float m8[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     m8[u] = -INFINITY;
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    load_half(hf);
+                for (int kq = 0; kq < 128; kq += 8)
 #pragma unroll
-                    for (int kq = 0; kq < 64; kq += 8)
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            m8[u] = fmaxf(m8[u], sc[kq + u]);
-                }
+                    for (int u = 0; u < 8; ++u)
+                        m8[u] = fmaxf(m8[u], sc[kq + u]);
                 const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                        fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
                 const float mxs = mx * c2l;
@@ -768,7 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[32];
 #pragma unroll
                     for (int kq = 0; kq < 32; ++kq) {
-                        const float2 x = __ffma2_rn(make_float2(sc[2 * kq], sc[2 * kq + 1]), cc, nmu2);
+                        const float2 x =
+                            __ffma2_rn(make_float2(sc[64 * hf + 2 * kq], sc[64 * hf + 2 * kq + 1]), cc, nmu2);
                         const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                         lsum[kq & 3] = __fadd2_rn(lsum[kq & 3], pp);
                         pk[kq] = pack_bf16x2(pp.x, pp.y);
@@ -776,7 +773,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(ts + kPCol + 32u * hf, pk);
                 };
                 exp_store(1);
-                load_half(0);
                 exp_store(0);
                 {
                     const float2 t2 =

@@ -361,7 +361,14 @@ int32_t pa_attention_route(pa_shape shape, int32_t max_context_len);
  * workspace of at least pa_prefill_workspace_bytes (256-byte aligned), it
  * runs pa_prefill_split when the shape has fewer than 1.5 (request, head
  * pair, 128-row query tile) items per SM, where whole blocks would leave
- * SMs idle; otherwise (or with NULL / a smaller workspace) pa_prefill.
+ * SMs idle; otherwise pa_prefill's kernel, and with one to two items per SM
+ * (head_dim 128) that kernel balances the blocks through the workspace: a
+ * block holding two items hands the last K/V tiles of its second item to a
+ * block holding one, which runs them first and leaves their softmax state
+ * (O / l in bf16, the maximum and the sum in fp32) for the first block to
+ * merge at its end (a cooperative launch, so every block is resident; every
+ * wait is bounded). The output is the same softmax up to rounding. With NULL
+ * or a smaller workspace: pa_prefill as it is.
  */
 pa_status pa_attention(const void *query, const void *key_pages,
                        const void *value_pages, const int32_t *block_table,

@@ -37,7 +37,14 @@ void pa_debug_arm_wait_timeout(void);
  *   2  two query heads of one KV group per block when the group size
  *      (num_q_heads / num_kv_heads) is at least 2; with an odd group size
  *      the last pair of each group computes its last head twice and writes
- *      it once. A group of 1 takes 1.
+ *      it once. A group of 1 takes 1;
+ *   4  as 2 on a grid of two thirds of the (request, head pair, query
+ *      tile) items, so that a third of the blocks hold one item and the rest
+ *      two; pa_attention given a prefill workspace then balances them with
+ *      tail pieces (a block runs the last tiles of another's second item
+ *      first and leaves their state, which that block merges), as it does by
+ *      itself with 1 to 2 items per SM. For tests of the pieces on small
+ *      shapes.
  * Settings 1 and 2 also hold for pa_prefill_split and for pa_attention given
  * a prefill workspace (the workspace is then not used). Any other value is
  * taken as 0. Returns the previous setting. Results agree

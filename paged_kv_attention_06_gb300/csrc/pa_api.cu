@@ -270,7 +270,8 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
                          const int32_t* block_table, const int32_t* context_lens,
                          int32_t page_size, float scale, int causal, void* out,
                          const pa_shape& s, cudaStream_t stream, void* workspace = nullptr,
-                         size_t workspace_bytes = 0, float out_scale = 1.f)
+                         size_t workspace_bytes = 0, float out_scale = 1.f,
+                         void* piece_ws = nullptr, size_t piece_ws_bytes = 0)
 {
     DeviceInfo* dev;
     pa_status st = device_info(&dev);
@@ -290,7 +291,7 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     const int64_t pair_items = prefill_pair_items(s);
     const bool d64 = s.head_dim == 64;   // only the pairs kernel has the 64-column form
     bool pairs = g >= 2 && (d64 || (t_prefill_variant != 1 &&
-                                    (g % 2 == 0 || t_prefill_variant == 2 ||
+                                    (g % 2 == 0 || t_prefill_variant >= 2 ||
                                      pair_items >= dev->sm_count)));
     if (pairs && prefill_pairs_smem_bytes(s.head_dim) > size_t(dev->max_smem_optin))
         pairs = false;
@@ -368,7 +369,14 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
         if (e == cudaErrorCooperativeLaunchTooLarge && !pending)
             (void)cudaGetLastError();
     }
-    cudaError_t e = pairs ? launch_prefill_pairs(qmap, kmap, vmap, omap, a, dev->id, dev->sm_count, stream)
+    // The pairs kernel's tail pieces use the caller's workspace (pa_attention's).
+    // Test setting 4: a grid of two thirds of the items, so that small shapes
+    // have blocks of one item and of two, and get pieces.
+    const bool small_grid = t_prefill_variant == 4;
+    const int grid_cap = small_grid ? int((2 * pair_items + 2) / 3) : dev->sm_count;
+    cudaError_t e = pairs ? launch_prefill_pairs(qmap, kmap, vmap, omap, a, dev->id, grid_cap,
+                                                 t_prefill_variant == 0 || small_grid ? piece_ws : nullptr,
+                                                 piece_ws_bytes, stream)
                           : launch_prefill(qmap, kmap, vmap, a, dev->id, stream);
     if (pairs && e == cudaErrorNotSupported) {   // register split not available
         if (d64)
@@ -878,9 +886,14 @@ pa_status pa_decode_dense(const void* query, const void* key_dense, const void* 
                         static_cast<cudaStream_t>(stream), 1);
 }
 
-pa_status pa_prefill(const void* query, const void* key_pages, const void* value_pages,
-                     const int32_t* block_table, const int32_t* context_lens, int32_t page_size,
-                     float scale, int causal, void* out, pa_shape shape, void* stream)
+namespace {
+
+// pa_prefill; piece_ws: room for the pairs kernel's tail pieces (pa_attention's
+// workspace), or null.
+pa_status prefill_route(const void* query, const void* key_pages, const void* value_pages,
+                        const int32_t* block_table, const int32_t* context_lens, int32_t page_size,
+                        float scale, int causal, void* out, pa_shape shape, void* stream,
+                        void* piece_ws, size_t piece_ws_bytes)
 {
     pa_status st = check_attention(query, key_pages, value_pages, block_table, context_lens,
                                    page_size, scale, out, shape);
@@ -889,7 +902,8 @@ pa_status pa_prefill(const void* query, const void* key_pages, const void* value
     const bool d64_pairs = shape.head_dim == 64 && shape.num_q_heads >= 2 * shape.num_kv_heads;
     if ((shape.head_dim == 128 || d64_pairs) && page_size >= 8) {
         st = run_prefill_tc(query, key_pages, value_pages, block_table, context_lens, page_size,
-                            scale, causal, out, shape, static_cast<cudaStream_t>(stream));
+                            scale, causal, out, shape, static_cast<cudaStream_t>(stream), nullptr, 0,
+                            1.f, piece_ws, piece_ws_bytes);
         if (st != PA_ERR_UNSUPPORTED || shape.head_dim == 128)
             return st;
     }
@@ -899,6 +913,16 @@ pa_status pa_prefill(const void* query, const void* key_pages, const void* value
     return run_split_kv(query, key_pages, value_pages, block_table, context_lens, page_size,
                         scale, causal, out, shape, 0, nullptr, 0, 1,
                         static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+pa_status pa_prefill(const void* query, const void* key_pages, const void* value_pages,
+                     const int32_t* block_table, const int32_t* context_lens, int32_t page_size,
+                     float scale, int causal, void* out, pa_shape shape, void* stream)
+{
+    return prefill_route(query, key_pages, value_pages, block_table, context_lens, page_size, scale,
+                         causal, out, shape, stream, nullptr, 0);
 }
 
 size_t pa_prefill_workspace_bytes(pa_shape shape, int32_t page_size)
@@ -959,7 +983,7 @@ pa_status pa_attention(const void* query, const void* key_pages, const void* val
         return pa_decode(query, key_pages, value_pages, block_table, context_lens, page_size,
                          scale, causal, out, shape, max_context_len, workspace, workspace_bytes,
                          stream);
-    if (workspace) {
+    if (workspace && t_prefill_variant != 4) {
         // The split kernel pays for its balance at every piece boundary; it
         // is the faster one when the (request, head pair, query tile) items
         // are too few to fill the SMs in whole waves (measured: 1.75x on one
@@ -977,8 +1001,10 @@ pa_status pa_attention(const void* query, const void* key_pages, const void* val
                                     page_size, scale, causal, out, shape, workspace,
                                     workspace_bytes, stream);
     }
-    return pa_prefill(query, key_pages, value_pages, block_table, context_lens, page_size, scale,
-                      causal, out, shape, stream);
+    // the pairs kernel, which balances one to two items per block with tail
+    // pieces in the workspace
+    return prefill_route(query, key_pages, value_pages, block_table, context_lens, page_size, scale,
+                         causal, out, shape, stream, workspace, workspace_bytes);
 }
 
 pa_status pa_get_device_error(void* stream, uint32_t* flags)
@@ -1024,7 +1050,7 @@ void pa_debug_arm_wait_timeout(void) { t_arm_unset_wait = true; }
 int pa_debug_prefill_variant(int variant)
 {
     const int prev = t_prefill_variant;
-    t_prefill_variant = (variant == 1 || variant == 2) ? variant : 0;
+    t_prefill_variant = (variant == 1 || variant == 2 || variant == 4) ? variant : 0;
     return prev;
 }
 

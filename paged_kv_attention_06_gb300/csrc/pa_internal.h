@@ -131,6 +131,14 @@ struct PrefillArgs {
     int32_t causal;
     float out_scale;    // the output is out_scale * softmax . V (e4m3 copies: v_scale)
     int32_t D;          // head_dim: 128 (64 on the pairs kernel only)
+    // Pairs kernel, tail pieces (head_dim 128; state == nullptr: none): per
+    // block slot and head, O / l of a piece in bf16 [16 chunks of 8
+    // columns][128 rows], (m, l) per row, and one flag per softmax warp that
+    // holds the launch's stamp once the slot is written.
+    uint4* state;                 // [grid][2][16][128]
+    float2* state_ml;             // [grid][2][128]
+    unsigned long long* flags;    // [grid][2][4]
+    uint64_t stamp;               // this launch's stamp (never 0)
 };
 
 // Prefill over e4m3 pools: bf16 copies of the visible K/V tokens, in pages
@@ -187,11 +195,17 @@ cudaError_t launch_prefill_split(const CUtensorMap& q_map, const CUtensorMap& ke
 
 size_t prefill_smem_bytes();
 size_t prefill_pairs_smem_bytes(int D);
+// Workspace of the pairs kernel's tail pieces on a grid of `grid` blocks.
+size_t prefill_pairs_workspace_bytes(int grid);
 // out_map: the output as a 3-D bf16 tensor {D, L, B * H_q}, boxes of 64
 // columns x 32 rows, 128-byte swizzle (the kernel stores through it).
+// grid_cap: blocks at most (the SM count). workspace (optional, 256-byte
+// aligned, any contents): room for tail pieces (prefill_pairs_workspace_bytes
+// of the grid); without it, whole items only.
 cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& key_map,
                                  const CUtensorMap& value_map, const CUtensorMap& out_map,
-                                 const PrefillArgs& a, int device, int sm_count, cudaStream_t stream);
+                                 const PrefillArgs& a, int device, int grid_cap, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& q_map, const CUtensorMap& key_map,
                            const CUtensorMap& value_map, const PrefillArgs& a, int device,
                            cudaStream_t stream);

@@ -94,8 +94,8 @@ struct Layout {
     // output staging, 4 KiB per softmax warp (the item ranking uses it first)
     static constexpr int kStage = kV + 2 * kMat;
     static constexpr int kStageWarp = 4096;
-    static constexpr int kItems = kStage + 8 * kStageWarp;   // [kMaxItems][8] int32
-    static constexpr int kBar = kItems + kMaxItems * 8 * 4;
+    static constexpr int kItems = kStage + 8 * kStageWarp;   // [kMaxItems][12] int32
+    static constexpr int kBar = kItems + kMaxItems * 12 * 4;
     static constexpr int kNumBars = 20;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kMisc = kTmemSlot + 16;
@@ -118,7 +118,27 @@ static_assert(kMmaDone < Layout<128>::kNumBars, "barrier count");
 // Item table entry: request, query tile, the two query heads, the KV head,
 // the (clamped) context length, K/V tiles visited, whether head 1 repeats
 // head 0.
-enum { kEB = 0, kET, kEH0, kEH1, kEHK, kEN, kENT, kEDup };
+enum { kEB = 0, kET, kEH0, kEH1, kEHK, kEN, kENT, kEDup, kEK0, kERole, kESlot, kEntry = 12 };
+// Item roles: the whole item here; the item's last tiles here, state left
+// for its first block (run first on the receiving block); the item's first
+// tiles here, merged at the end with the state its last tiles left.
+enum { kWhole = 0, kPublish = 1, kMerge = 2 };
+
+// Tail pieces, with at most two items per block (N items on G blocks, G < N
+// <= 2G; the R = 2G - N blocks c < R hold one item): block c >= max(R, G - R)
+// hands the last d tiles of its second item (position 2G - 1 - c) to block
+// j = G - 1 - c, which runs them before its own item and leaves their state;
+// block c merges that state into its own part of the item at the end. Loads in
+// quarter tiles: 4 per K/V tile, kWItem per item (its Q, the pipeline restart,
+// the epilogue), kWPiece more for a piece that leaves its state, kWMerge for the
+// merge. d balances the two blocks: floor((L_c + kWMerge - L_j - kWItem -
+// kWPiece) / 8), at most the item's tiles less one, none when below one. The
+// weights are measured: on 4 requests of 512 rows after ragged prefixes (the
+// busiest blocks at two items of 14 tiles, the idlest at one of 17) they give
+// d = 6, 52.6 us per call; d = 4 / 5 / 7 / 8 gave 55.0 / 53.8 / 54.5 / 56.5.
+constexpr int kWItem = 4;
+constexpr int kWPiece = 0;
+constexpr int kWMerge = 8;
 
 // Operand descriptors (128B swizzle). K-major [half][128 rows][128 B] (Q, K):
 // k-step kk (16 elements along K) starts kmajor_off(kk) bytes in. MN-major
@@ -132,6 +152,17 @@ __device__ __forceinline__ uint64_t kmajor_base(uint32_t saddr) { return smem_de
 __device__ __forceinline__ uint64_t mnmajor_base(uint32_t saddr)
 {
     return smem_desc_sw128(saddr, uint32_t(Layout<128>::kHalf), 1024u);
+}
+
+// Hands a piece's state over: this warp's stores are made visible at GPU scope
+// before lane 0 writes the launch's stamp into the warp's flag. Not inlined:
+// inside the softmax loop an inlined copy costs the loop registers.
+__device__ __noinline__ void publish_state(unsigned long long* flag, unsigned long long stamp, int lane)
+{
+    __threadfence();
+    __syncwarp();
+    if (lane == 0)
+        st_release_gpu(flag, stamp);
 }
 
 // kOdd: the group size is odd and the last pair of each group repeats its
@@ -178,9 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t w = k >> 1;
         return (k & 1) ? (2 * w + 2) * nblk - 1 - c : 2 * w * nblk + c;
     };
-    int n_items = 0;
-    while (n_items < kMaxItems && item_at(n_items) < n_all)
-        ++n_items;
+    int n_own = 0;
+    while (n_own < kMaxItems - 1 && item_at(n_own) < n_all)
+        ++n_own;
     // Context length of request bb (clamped; an entry out of range is
     // recorded) and the K/V tiles its query tile tt visits.
     auto tiles_for = [&](int bb, int tt, int* n_out) {
@@ -216,8 +247,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
     }
+    // Tail pieces (kWItem): with the state buffers, the ranking in shared
+    // memory and between one and two items per block.
+    const bool pieces =
+        kD == 128 && a.state != nullptr && M <= kThreads && n_all > nblk && n_all <= 2 * nblk;
+    auto size_at = [&](int64_t p) { return tiles_of[order[int(p / pairs)]]; };
+    auto donated = [&](int dc) -> int {       // tiles block dc hands over
+        const int s2 = size_at(2 * nblk - 1 - dc);
+        const int lc = 4 * (size_at(dc) + s2) + 2 * kWItem;
+        const int lj = 4 * size_at(nblk - 1 - dc) + kWItem;
+        const int d = min((lc + kWMerge - lj - kWItem - kWPiece) / 8, s2 - 1);
+        return d > 0 ? d : 0;
+    };
+    int my_cut = 0, my_piece = 0;             // tiles handed over / taken over
+    if (pieces) {
+        const int R = int(2 * nblk - n_all);
+        const int c_lo = max(R, int(nblk) - R);
+        if (c >= c_lo)
+            my_cut = donated(int(c));
+        else if (c < R && int(nblk) - 1 - int(c) >= c_lo)
+            my_piece = donated(int(nblk) - 1 - int(c));
+    }
+    const int n_items = n_own + (my_piece > 0 ? 1 : 0);
     if (int(threadIdx.x) < n_items) {
-        const int64_t i = item_at(int(threadIdx.x));
+        // entry 0 of a receiving block is the piece (the donor's second item)
+        const int slot = my_piece > 0 ? int(nblk) - 1 - int(c) : int(c);
+        const int own = int(threadIdx.x) - (my_piece > 0 ? 1 : 0);
+        const int64_t i = own < 0 ? nblk + c : item_at(own);
         const int rank = int(i / pairs);
         const int hp = int(i - int64_t(rank) * pairs);
         int b, t, n, nt;
@@ -241,15 +297,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             hk = hq0 / a.G;
         }
         const bool dup = kOdd && hq0 + 1 == (hk + 1) * a.G;   // odd group: one head, twice
-        int32_t* e = items + threadIdx.x * 8;
+        int32_t* e = items + threadIdx.x * kEntry;
         e[kEB] = b;
         e[kET] = t;
         e[kEH0] = hq0;
         e[kEH1] = dup ? hq0 : hq0 + 1;
         e[kEHK] = hk;
         e[kEN] = n;
-        e[kENT] = nt;
         e[kEDup] = dup ? 1 : 0;
+        e[kESlot] = slot;
+        if (own < 0) {                        // the piece: the last my_piece tiles
+            e[kEK0] = nt - my_piece;
+            e[kENT] = my_piece;
+            e[kERole] = kPublish;
+        } else if (own == 1 && my_cut > 0) {  // the first tiles of the second item
+            e[kEK0] = 0;
+            e[kENT] = nt - my_cut;
+            e[kERole] = kMerge;
+        } else {
+            e[kEK0] = 0;
+            e[kENT] = nt;
+            e[kERole] = kWhole;
+        }
     }
 
     const uint32_t sQ = smem_u32(smem + Layout::kQ);
@@ -293,10 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // item's Q).
     if (threadIdx.x == 0) {
         int it0 = 0;
-        while (it0 < n_items && items[it0 * 8 + kENT] == 0)
+        while (it0 < n_items && items[it0 * kEntry + kENT] == 0)
             ++it0;
         if (it0 < n_items) {
-            const int32_t* e = items + it0 * 8;
+            const int32_t* e = items + it0 * kEntry;
             const uint64_t policy = l2_policy_evict_last();
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -329,14 +398,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             int g = 0;                                   // tiles of the block before this item
             int qk = 0;                                  // items with tiles before this one
             for (int it = 0; it < n_items; ++it) {
-                const int32_t* e = items + it * 8;
-                const int nt = e[kENT];
+                const int32_t* e = items + it * kEntry;
+                const int nt = e[kENT], k0 = e[kEK0];
                 if (nt == 0)
                     continue;
                 const int b = e[kEB], n = e[kEN], hk = e[kEHK];
                 const int32_t* bt = a.block_table + int64_t(b) * a.max_pages;
+                // tile j of the piece is the item's K/V tile k0 + j
                 auto n_boxes = [&](int j) {
-                    const int key0 = j * kKeys;
+                    const int key0 = (k0 + j) * kKeys;
                     return (min(n, key0 + kKeys) - key0 + box - 1) / box;
                 };
                 // Raw block-table entry of this lane's box in tile j, loaded
@@ -344,14 +414,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // not exist, so that nothing waits for it before use).
                 auto fetch_page = [&](int j) -> int {
                     const bool live = j < nt && my_box < n_boxes(j);
-                    return bt[live ? (j * kKeys + my_box * box) / a.ps : 0];
+                    return bt[live ? ((k0 + j) * kKeys + my_box * box) / a.ps : 0];
                 };
                 auto pool_row = [&](int j, int phys) -> int {
                     if (unsigned(phys) >= unsigned(a.num_pages)) {
                         atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
                         phys = 0;
                     }
-                    const int tok = j * kKeys + my_box * box;
+                    const int tok = (k0 + j) * kKeys + my_box * box;
                     return (phys * a.H_kv + hk) * a.ps + (tok - (tok / a.ps) * a.ps);
                 };
                 auto load = [&](int j, bool is_v, int phys) {
@@ -473,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int g = 0, qk = 0;
             bool ok = true;
             for (int it = 0; it < n_items && ok; ++it) {
-                const int nt = items[it * 8 + kENT];
+                const int nt = items[it * kEntry + kENT];
                 if (nt == 0)
                     continue;
                 // The item's first scores: both score buffers are free (the
@@ -558,10 +628,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // chunks swizzled by row as the output map's 128-byte swizzle wants;
         // one lane then stores the warp's 32 rows x 64 columns by TMA.
         uint8_t* stage = smem + Layout::kStage + (warp - 4) * Layout::kStageWarp;
+        // A piece's state is handed over by its flag, raised by this warp one
+        // tile after the state's stores (or at the end), when they have drained.
+        int64_t flag_slot = -1;
+        auto raise_flag = [&]() {
+            publish_state(a.flags + flag_slot * 4 + w4, a.stamp, lane);
+            flag_slot = -1;
+        };
         int g = 0;                                   // tiles of the block before this item
         for (int it = 0; it < n_items; ++it) {
-            const int32_t* e = items + it * 8;
-            const int nt = e[kENT], n = e[kEN];
+            const int32_t* e = items + it * kEntry;
+            const int nt = e[kENT], n = e[kEN], k0 = e[kEK0], role = e[kERole];
             const int row0 = e[kET] * kRows;
             const int rows = min(kRows, a.L - row0);
             const int i = row0 + r;
@@ -579,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // P overwrites any). Reading the two 64-column halves one after
                 // the other, the lower half twice, was 0.9 us per call slower on
                 // the 512-row batch.
-                const int key0 = j * kKeys;
+                const int key0 = (k0 + j) * kKeys;
                 const bool edge = key0 + kKeys - 1 > lim;
                 uint32_t sv[128];
                 float* s = reinterpret_cast<float*>(sv);
@@ -677,29 +754,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&bar[kPFull + head]);
+                if (flag_slot >= 0)
+                    raise_flag();
             }
-            // ---- epilogue of the item: O / l -> bf16 ----------------------------
-            const float inv = l > 0.f ? a.out_scale / l : 0.f;
+            // ---- epilogue of the item ---------------------------------------------
             if (nt > 0) {
                 mbar_wait_warp(&bar[kPVDone + head], (g + nt - 1) & 1, misc, a.err);
                 tc_fence_after();
             }
-            // This warp's 32 rows: one TMA store of 32 rows x 64 columns per
-            // half from the staging buffer (rows past L are outside the output
-            // map's L extent and are not written).
-            const int oz = e[kEB] * a.H_q + e[head == 0 ? kEH0 : kEH1];
-            const bool write = rows - w4 * 32 > 0 && misc[0] == 0 && !(head == 1 && e[kEDup]);
+            const int64_t sl = int64_t(e[kESlot]) * 2 + head;     // a piece's state slot
+            if (role == kPublish) {
+                // The item's last tiles: O / l in bf16 as [16 chunks of 8
+                // columns][128 rows] (a warp's stores contiguous) and (m, l) per
+                // row, for the block that holds the item's first tiles; the
+                // flag is raised one tile later, once the stores have drained.
+                uint4* st_o = a.state + sl * 16 * 128 + r;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-            for (int hf = 0; hf < Layout::kHalves; ++hf) {
-                // the staging buffer's previous store has read it
-                if (lane == 0)
-                    tma_store_wait_read();
-                __syncwarp();
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {     // columns 64 hf + 32 q .. + 31 of this row
+                for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t ov[32];
                     if (nt > 0) {
-                        tmem_ld32(to + 32u * (2 * hf + q), ov);
+                        tmem_ld32(to + 32u * q4, ov);
                         tmem_wait_ld();
                     } else {
 #pragma unroll
@@ -707,21 +782,104 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ov[k] = 0u;
                     }
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const int cq = 4 * q + c4;
-                        const uint32_t* o = ov + 8 * c4;
-                        *reinterpret_cast<uint4*>(stage + lane * 128 + ((cq ^ (lane & 7)) << 4)) = make_uint4(
-                            pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv),
-                            pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv),
-                            pack_bf16x2(__uint_as_float(o[4]) * inv, __uint_as_float(o[5]) * inv),
-                            pack_bf16x2(__uint_as_float(o[6]) * inv, __uint_as_float(o[7]) * inv));
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const uint32_t* o = ov + 8 * ch;
+                        __stcg(st_o + (q4 * 4 + ch) * 128,
+                               make_uint4(pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv),
+                                          pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv),
+                                          pack_bf16x2(__uint_as_float(o[4]) * inv, __uint_as_float(o[5]) * inv),
+                                          pack_bf16x2(__uint_as_float(o[6]) * inv, __uint_as_float(o[7]) * inv)));
                     }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && write) {
-                    tma_store_3d(&out_map, stage, hf * 64, row0 + w4 * 32, oz);
-                    tma_store_commit();
+                __stcg(a.state_ml + sl * 128 + r, make_float2(m_used, l));
+                flag_slot = sl;
+            } else {
+                // O / l -> bf16; merged first with the state the item's last
+                // tiles left: M = max(m, m_t), l' = l 2^(m - M) + l_t 2^(m_t - M),
+                // o = (O 2^(m - M) + O_t / l_t l_t 2^(m_t - M)) / l'.
+                float a_own = l > 0.f ? a.out_scale / l : 0.f;
+                float w_t = 0.f;
+                const uint4* st_t = nullptr;
+                if (role == kMerge) {
+                    const unsigned long long* f = a.flags + sl * 4 + w4;
+                    bool got = ld_acquire_gpu(f) == a.stamp;
+                    if (!got) {
+                        const uint64_t t0 = global_timer_ns();
+                        const uint64_t limit = misc[0] ? kShortWaitLimitNs : kWaitLimitNs;
+                        for (uint32_t w = 1; !got; ++w) {
+                            got = ld_acquire_gpu(f) == a.stamp;
+                            if (!got && (w & 15u) == 0 && global_timer_ns() - t0 > limit)
+                                break;
+                        }
+                    }
+                    if (!__all_sync(0xffffffffu, got) && lane == 0 && !misc[0]) {
+                        misc[0] = 1;
+                        atomicOr(a.err, PA_DEVERR_TIMEOUT_BIT);
+                    }
+                    __syncwarp();
+                    const float2 ml = __ldcg(a.state_ml + sl * 128 + r);
+                    const float mx = fmaxf(m_used, ml.x);
+                    const float f_own = m_used == -INFINITY ? 0.f : fast_exp2(m_used - mx);
+                    const float f_t = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mx);
+                    const float lt = l * f_own + ml.y * f_t;
+                    const float inv = lt > 0.f ? a.out_scale / lt : 0.f;
+                    a_own = f_own * inv;
+                    w_t = ml.y * f_t * inv;
+                    st_t = a.state + sl * 16 * 128 + r;
+                }
+                // This warp's 32 rows: one TMA store of 32 rows x 64 columns per
+                // half from the staging buffer (rows past L are outside the output
+                // map's L extent and are not written).
+                const int oz = e[kEB] * a.H_q + e[head == 0 ? kEH0 : kEH1];
+                const bool write = rows - w4 * 32 > 0 && misc[0] == 0 && !(head == 1 && e[kEDup]);
+#pragma unroll 1
+                for (int hf = 0; hf < Layout::kHalves; ++hf) {
+                    // the staging buffer's previous store has read it
+                    if (lane == 0)
+                        tma_store_wait_read();
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {     // columns 64 hf + 32 q .. + 31 of this row
+                        uint32_t ov[32];
+                        if (nt > 0) {
+                            tmem_ld32(to + 32u * (2 * hf + q), ov);
+                            tmem_wait_ld();
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                ov[k] = 0u;
+                        }
+                        float* o = reinterpret_cast<float*>(ov);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            o[k] *= a_own;
+                        if (st_t != nullptr) {
+#pragma unroll
+                            for (int c4 = 0; c4 < 4; ++c4) {
+                                const uint4 v = __ldcg(st_t + (8 * hf + 4 * q + c4) * 128);
+                                const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    o[8 * c4 + 2 * k] += w_t * __uint_as_float(vw[k] << 16);
+                                    o[8 * c4 + 2 * k + 1] += w_t * __uint_as_float(vw[k] & 0xffff0000u);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const int cq = 4 * q + c4;
+                            const float* oc = o + 8 * c4;
+                            *reinterpret_cast<uint4*>(stage + lane * 128 + ((cq ^ (lane & 7)) << 4)) =
+                                make_uint4(pack_bf16x2(oc[0], oc[1]), pack_bf16x2(oc[2], oc[3]),
+                                           pack_bf16x2(oc[4], oc[5]), pack_bf16x2(oc[6], oc[7]));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && write) {
+                        tma_store_3d(&out_map, stage, hf * 64, row0 + w4 * 32, oz);
+                        tma_store_commit();
+                    }
                 }
             }
             // the O reads above are ordered before the next item's first P V
@@ -729,6 +887,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             g += nt;
         }
+        if (flag_slot >= 0)
+            raise_flag();
         if (lane == 0)
             tma_store_wait_all();     // every output store has landed
         __syncwarp();
@@ -746,6 +906,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t prefill_pairs_smem_bytes(int D)
 {
     return D == 64 ? size_t(Layout<64>::kBytes) : size_t(Layout<128>::kBytes);
+}
+
+namespace {
+constexpr size_t kPieceState = 2 * 16 * 128 * sizeof(uint4);      // per block: O / l, both heads
+constexpr size_t kPieceMl = 2 * 128 * sizeof(float2);             // (m, l) per row and head
+constexpr size_t kPieceFlags = 2 * 4 * sizeof(unsigned long long);
+}  // namespace
+
+size_t prefill_pairs_workspace_bytes(int grid)
+{
+    return size_t(grid) * (kPieceState + kPieceMl + kPieceFlags);
 }
 
 namespace {
@@ -797,15 +968,22 @@ cudaError_t launch_pairs(const cudaLaunchConfig_t& cfg_in, const CUtensorMap& q_
 
 cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& key_map,
                                  const CUtensorMap& value_map, const CUtensorMap& out_map,
-                                 const PrefillArgs& a, int device, int sm_count, cudaStream_t stream)
+                                 const PrefillArgs& a_in, int device, int grid_cap, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream)
 {
+    PrefillArgs a = a_in;
+    a.state = nullptr;
+    a.state_ml = nullptr;
+    a.flags = nullptr;
+    a.stamp = 0;
     if (a.D != 64 && a.D != 128)
         return cudaErrorInvalidValue;
-    // One block per SM (one fits), each taking whole items; more blocks only
-    // when an SM would get more than kMaxItems items.
+    // One block per SM (grid_cap: the SM count; one block fits per SM); more
+    // blocks only when one would get more than kMaxItems - 1 items (one entry
+    // stays free for a piece).
     const int64_t n_items = int64_t(a.B) * a.H_kv * ((a.G + 1) / 2) * a.n_qtiles;
-    int64_t grid = n_items < sm_count ? n_items : sm_count;
-    const int64_t min_grid = (n_items + kMaxItems - 1) / kMaxItems;
+    int64_t grid = n_items < grid_cap ? n_items : grid_cap;
+    const int64_t min_grid = (n_items + kMaxItems - 2) / (kMaxItems - 1);
     if (grid < min_grid)
         grid = min_grid;
     if (grid < 1 || grid >= (int64_t(1) << 31))
@@ -813,9 +991,11 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
     // Programmatic stream serialization: the blocks may be scheduled while the
     // previous kernel in the stream finishes; each waits for it
     // (griddepcontrol.wait) before reading anything.
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
     cfg.blockDim = dim3(kThreads);
@@ -823,11 +1003,41 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const bool odd = a.G % 2 != 0;
-    if (a.D == 64)
-        return odd ? launch_pairs<true, 64>(cfg, q_map, key_map, value_map, out_map, a, device)
-                   : launch_pairs<false, 64>(cfg, q_map, key_map, value_map, out_map, a, device);
-    return odd ? launch_pairs<true, 128>(cfg, q_map, key_map, value_map, out_map, a, device)
-               : launch_pairs<false, 128>(cfg, q_map, key_map, value_map, out_map, a, device);
+    auto launch = [&]() {
+        if (a.D == 64)
+            return odd ? launch_pairs<true, 64>(cfg, q_map, key_map, value_map, out_map, a, device)
+                       : launch_pairs<false, 64>(cfg, q_map, key_map, value_map, out_map, a, device);
+        return odd ? launch_pairs<true, 128>(cfg, q_map, key_map, value_map, out_map, a, device)
+                   : launch_pairs<false, 128>(cfg, q_map, key_map, value_map, out_map, a, device);
+    };
+    // Tail pieces (a block waits for another's state): with a workspace, one
+    // or two items per block, the ranking in shared memory, and a cooperative
+    // launch so that every block is resident; otherwise whole items.
+    const int64_t M = int64_t(a.B) * a.n_qtiles;
+    if (workspace && a.D == 128 && M <= kThreads && n_items > grid && n_items <= 2 * grid &&
+        workspace_bytes >= prefill_pairs_workspace_bytes(int(grid)) &&
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0) {
+        uint8_t* w = static_cast<uint8_t*>(workspace);
+        a.state = reinterpret_cast<uint4*>(w);
+        a.state_ml = reinterpret_cast<float2*>(w + size_t(grid) * kPieceState);
+        a.flags = reinterpret_cast<unsigned long long*>(w + size_t(grid) * (kPieceState + kPieceMl));
+        a.stamp = next_launch_stamp();
+        cfg.numAttrs = 2;
+        // An error the caller left pending is not ours to clear: note it, so
+        // that only a refused cooperative launch of this call is cleared.
+        const bool pending = cudaPeekAtLastError() != cudaSuccess;
+        const cudaError_t e = launch();
+        if (e != cudaErrorCooperativeLaunchTooLarge)
+            return e;
+        if (!pending)
+            (void)cudaGetLastError();
+        a.state = nullptr;                      // not every block could be resident
+        a.state_ml = nullptr;
+        a.flags = nullptr;
+        a.stamp = 0;
+        cfg.numAttrs = 1;
+    }
+    return launch();
 }
 
 }  // namespace pa

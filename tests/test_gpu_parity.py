@@ -208,6 +208,27 @@ def test_empty_contexts_and_rows_without_keys():
         assert_close(out, ref, route)
 
 
+@pytest.mark.parametrize("ps,L,route", [(16, 1, "decode"), (16, 200, "prefill"), (128, 1, "decode"),
+                                        (128, 130, "prefill"), (16, 130, "prefill_split")])
+def test_full_tables_in_a_full_pool(ps, L, route):
+    """Every block-table row full (each context a whole number of pages, the
+    longest filling max_pages), every page of the pool in use (no slack, so
+    the pool's last page is read too): the edge where a page walk ends exactly
+    at the table's and the pool's last entries."""
+    n_full = 12 * ps
+    lens = [n_full, n_full, 6 * ps, n_full]
+    b = wl.build_batch(f"full_{ps}_{L}", B=4, H_q=16, H_kv=4, D=128, page_size=ps, L=L,
+                       context_lens=lens, seed=ps + L, L_new=min(L, 2), pool_slack=0.0)
+    assert b.num_pages == sum(n // ps for n in lens)
+    assert int((b.block_table >= 0).sum()) == b.num_pages
+    db = DeviceBatch(b)
+    out = gpu_step(db, route=route)
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert np.array_equal(host_bits(db.key_pages), kp)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), f"full tables ps={ps} L={L} {route}")
+
+
 def test_decode_and_prefill_routes_agree():
     b = wl.build_batch("routes", B=8, H_q=32, H_kv=8, D=128, page_size=16, L=4,
                        context_lens=[5, 77, 300, 1000, 2047, 16, 17, 4096], seed=21, L_new=0)
@@ -274,16 +295,17 @@ def test_non_default_stream():
 # The tensor-core prefill path (head_dim 128, page_size >= 8) at its edges
 
 
-@pytest.fixture(params=[1, 2, 0], ids=["one_head", "head_pairs", "split"])
+@pytest.fixture(params=[1, 2, 0, 4], ids=["one_head", "head_pairs", "split", "tail_pieces"])
 def prefill_variant(request):
     """Runs the test under each tensor-core prefill kernel (pairs need an even
     group size; odd groups take the one-head kernel under either setting; the
     split kernel runs through pa_prefill_split with a workspace, and odd
-    groups there also fall back to the one-head kernel). Yields the route for
-    gpu_step."""
+    groups there also fall back to the one-head kernel; the pairs kernel with
+    tail pieces runs through pa_attention with its workspace on a grid of two
+    thirds of the items). Yields the route for gpu_step."""
     import paged_kv_attention_06_gb300 as pa
     prev = pa.pa_debug_prefill_variant(request.param)
-    yield "prefill_split" if request.param == 0 else "prefill"
+    yield {0: "prefill_split", 4: "attention"}.get(request.param, "prefill")
     pa.pa_debug_prefill_variant(prev)
 
 
@@ -493,6 +515,59 @@ def test_split_prefill_workspace_contents_and_repeat():
     kp, vp = b.key_pages.copy(), b.value_pages.copy()
     oracle.append_kv(b.key_new, b.value_new, kp, vp, b.slot_mapping, b.page_size)
     assert_close(host_f64(outs[0]), oracle_out(b, kp, vp), "split workspace contents")
+
+
+@pytest.fixture
+def tail_pieces():
+    """pa_attention's pairs kernel on a grid of two thirds of the items, so
+    that the blocks with two items hand the last tiles of their second one to
+    blocks with one (test setting 4)."""
+    import paged_kv_attention_06_gb300 as pa
+    prev = pa.pa_debug_prefill_variant(4)
+    yield
+    pa.pa_debug_prefill_variant(prev)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("H_q,H_kv", [(8, 2), (6, 2)])     # groups of 4 / 3
+def test_tail_pieces_every_row(causal, H_q, H_kv, tail_pieces):
+    """Ragged prefixes (items of 1 to 21 K/V tiles): the donors' second items
+    are cut, their last tiles run first on the receiving blocks, and the
+    donors merge the states at their ends. Every row against the oracle."""
+    b = wl.build_batch("pieces", B=4, H_q=H_q, H_kv=H_kv, D=128, page_size=16, L=512,
+                       context_lens=[1866, 2285, 710, 2052], seed=31 + H_q + int(causal),
+                       causal=causal, placement="churn", L_new=4)
+    db = DeviceBatch(b)
+    out = gpu_step(db, route="attention")
+    check_no_device_error()
+    kp, vp = oracle_pages(b)
+    assert_close(host_f64(out), oracle_out(b, kp, vp), f"tail pieces G={H_q // H_kv} causal={causal}")
+
+
+def test_tail_pieces_workspace_contents_and_repeat(tail_pieces):
+    """Any workspace contents (stale flags included) give the same bits."""
+    import paged_kv_attention_06_gb300 as pa
+    b = wl.build_batch("piecesws", B=4, H_q=8, H_kv=2, D=128, page_size=16, L=512,
+                       context_lens=[1866, 2285, 710, 2052], seed=37, placement="churn", L_new=0)
+    db = DeviceBatch(b)
+    shape = pa.make_shape(db.query.shape, db.key_pages.shape, db.block_table.shape[1])
+    need = pa.pa_prefill_workspace_bytes(shape, b.page_size)
+    assert need > 0
+    outs = []
+    for fill in (0x00, 0xFF, 0x5A, None):
+        ws = torch.full((need,), fill if fill is not None else 0, dtype=torch.uint8, device="cuda")
+        if fill is None:      # the same buffer twice: the first launch's flags are stale
+            pa.pa_attention(db.query, db.key_pages, db.value_pages, db.block_table,
+                            db.context_lens, b.page_size, scale=b.scale, causal=b.causal,
+                            max_context_len=int(b.context_lens.max()), workspace=ws)
+        outs.append(pa.pa_attention(db.query, db.key_pages, db.value_pages, db.block_table,
+                                    db.context_lens, b.page_size, scale=b.scale,
+                                    causal=b.causal, max_context_len=int(b.context_lens.max()),
+                                    workspace=ws))
+        check_no_device_error()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert_close(host_f64(outs[0]), oracle_out(b, b.key_pages, b.value_pages), "pieces workspace")
 
 
 def test_split_prefill_ragged_items_with_empty_rows():

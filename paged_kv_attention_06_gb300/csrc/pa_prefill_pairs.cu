@@ -154,9 +154,32 @@ __device__ __forceinline__ uint64_t mnmajor_base(uint32_t saddr)
     return smem_desc_sw128(saddr, uint32_t(Layout<128>::kHalf), 1024u);
 }
 
+// This block's part in the tail pieces (kWItem): (tiles it hands over, tiles
+// it takes over). order / tiles_of: the ranking of the (request, query tile)
+// pairs; item p (rank order) has tiles_of[order[p / pairs]] tiles.
+__device__ __forceinline__ int2 plan_piece(const int* order, const int* tiles_of, int pairs, int n_all,
+                                        int nblk, int c)
+{
+    auto size_at = [&](int p) { return tiles_of[order[p / pairs]]; };
+    auto donated = [&](int dc) -> int {       // tiles block dc hands over
+        const int s2 = size_at(2 * nblk - 1 - dc);
+        const int lc = 4 * (size_at(dc) + s2) + 2 * kWItem;
+        const int lj = 4 * size_at(nblk - 1 - dc) + kWItem;
+        const int d = min((lc + kWMerge - lj - kWItem - kWPiece) / 8, s2 - 1);
+        return d > 0 ? d : 0;
+    };
+    const int R = 2 * nblk - n_all;
+    const int c_lo = max(R, nblk - R);
+    if (c >= c_lo)
+        return make_int2(donated(c), 0);
+    if (c < R && nblk - 1 - c >= c_lo)
+        return make_int2(0, donated(nblk - 1 - c));
+    return make_int2(0, 0);
+}
+
 // Hands a piece's state over: this warp's stores are made visible at GPU scope
 // before lane 0 writes the launch's stamp into the warp's flag. Not inlined:
-// inside the softmax loop an inlined copy costs the loop registers.
+// an inlined copy costs the softmax loop registers.
 __device__ __noinline__ void publish_state(unsigned long long* flag, unsigned long long stamp, int lane)
 {
     __threadfence();
@@ -168,8 +191,11 @@ __device__ __noinline__ void publish_state(unsigned long long* flag, unsigned lo
 // kOdd: the group size is odd and the last pair of each group repeats its
 // last head (a separate instantiation, so that even groups keep their code).
 // kD: head_dim (128, or 64: one 64-column half per Q, K and V row, four
-// k-steps for S, N = 64 for P V and 64 of O's TMEM columns).
-template <bool kOdd, int kD>
+// k-steps for S, N = 64 for P V and 64 of O's TMEM columns). kPieces: the
+// tail pieces' planning and epilogues (head_dim 128; a separate instantiation,
+// so that the whole-item kernel's code and registers stay as they are: with
+// the piece code compiled in, whole items ran 2-3 us per call slower).
+template <bool kOdd, int kD, bool kPieces>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pairs_kernel(const __grid_constant__ CUtensorMap q_map,
                          const __grid_constant__ CUtensorMap key_map,
@@ -250,23 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Tail pieces (kWItem): with the state buffers, the ranking in shared
     // memory and between one and two items per block.
     const bool pieces =
-        kD == 128 && a.state != nullptr && M <= kThreads && n_all > nblk && n_all <= 2 * nblk;
-    auto size_at = [&](int64_t p) { return tiles_of[order[int(p / pairs)]]; };
-    auto donated = [&](int dc) -> int {       // tiles block dc hands over
-        const int s2 = size_at(2 * nblk - 1 - dc);
-        const int lc = 4 * (size_at(dc) + s2) + 2 * kWItem;
-        const int lj = 4 * size_at(nblk - 1 - dc) + kWItem;
-        const int d = min((lc + kWMerge - lj - kWItem - kWPiece) / 8, s2 - 1);
-        return d > 0 ? d : 0;
-    };
+        kPieces && kD == 128 && a.state != nullptr && M <= kThreads && n_all > nblk && n_all <= 2 * nblk;
     int my_cut = 0, my_piece = 0;             // tiles handed over / taken over
     if (pieces) {
-        const int R = int(2 * nblk - n_all);
-        const int c_lo = max(R, int(nblk) - R);
-        if (c >= c_lo)
-            my_cut = donated(int(c));
-        else if (c < R && int(nblk) - 1 - int(c) >= c_lo)
-            my_piece = donated(int(nblk) - 1 - int(c));
+        const int2 cp = plan_piece(order, tiles_of, pairs, int(n_all), int(nblk), int(c));
+        my_cut = cp.x;
+        my_piece = cp.y;
     }
     const int n_items = n_own + (my_piece > 0 ? 1 : 0);
     if (int(threadIdx.x) < n_items) {
@@ -472,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (li < 2 && qk > 0)    // the first item's Q went out at the start
                     load_q();
                 for (int j0 = 0; j0 < nt; j0 += 3) {
-    #pragma unroll
+#pragma unroll
                     for (int u = 0; u < 3; ++u) {
                         const int j = j0 + u;
                         if (j < nt) {
@@ -513,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t da = h ? dq1 : dq0;
                     const uint64_t db = (gj & 1) ? dk1 : dk0;
                     const uint32_t d = tmem + col_s(h);
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < kKSteps; ++kk)
                         tc_mma_bf16(d, desc_advance(da, kmajor_off(kk)), desc_advance(db, kmajor_off(kk)),
                                     idesc_s, kk > 0);
@@ -525,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t db = (gj & 1) ? dv1 : dv0;
                     const uint32_t d = tmem + col_o(h);
                     const uint32_t pa = tmem + col_s(h) + kPCol;
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         tc_mma_bf16_ts(d, pa + 8u * kk, desc_advance(db, mnmajor_off(kk)), idesc_pv,
                                        (!first || kk > 0) ? 1u : 0u);
@@ -628,13 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // chunks swizzled by row as the output map's 128-byte swizzle wants;
         // one lane then stores the warp's 32 rows x 64 columns by TMA.
         uint8_t* stage = smem + Layout::kStage + (warp - 4) * Layout::kStageWarp;
-        // A piece's state is handed over by its flag, raised by this warp one
-        // tile after the state's stores (or at the end), when they have drained.
-        int64_t flag_slot = -1;
-        auto raise_flag = [&]() {
-            publish_state(a.flags + flag_slot * 4 + w4, a.stamp, lane);
-            flag_slot = -1;
-        };
+        int64_t flag_slot = -1;                      // a piece's slot whose flag is due
         int g = 0;                                   // tiles of the block before this item
         for (int it = 0; it < n_items; ++it) {
             const int32_t* e = items + it * kEntry;
@@ -754,84 +763,144 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&bar[kPFull + head]);
-                if (flag_slot >= 0)
-                    raise_flag();
+                if (kPieces && flag_slot >= 0) {
+                    publish_state(a.flags + flag_slot * 4 + w4, a.stamp, lane);
+                    flag_slot = -1;
+                }
             }
             // ---- epilogue of the item ---------------------------------------------
             if (nt > 0) {
                 mbar_wait_warp(&bar[kPVDone + head], (g + nt - 1) & 1, misc, a.err);
                 tc_fence_after();
             }
-            const int64_t sl = int64_t(e[kESlot]) * 2 + head;     // a piece's state slot
-            if (role == kPublish) {
-                // The item's last tiles: O / l in bf16 as [16 chunks of 8
-                // columns][128 rows] (a warp's stores contiguous) and (m, l) per
-                // row, for the block that holds the item's first tiles; the
-                // flag is raised one tile later, once the stores have drained.
-                uint4* st_o = a.state + sl * 16 * 128 + r;
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+            if constexpr (kPieces) {
+                const int64_t sl = int64_t(e[kESlot]) * 2 + head;     // a piece's state slot
+                if (role == kPublish) {
+                    // The item's last tiles: O / l in bf16 as [16 chunks of 8
+                    // columns][128 rows] (a warp's stores contiguous) and (m, l) per
+                    // row, for the block that holds the item's first tiles; the
+                    // flag is raised one tile later, once the stores have drained.
+                    uint4* st_o = a.state + sl * 16 * 128 + r;
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t ov[32];
-                    if (nt > 0) {
-                        tmem_ld32(to + 32u * q4, ov);
-                        tmem_wait_ld();
-                    } else {
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t ov[32];
+                        if (nt > 0) {
+                            tmem_ld32(to + 32u * q4, ov);
+                            tmem_wait_ld();
+                        } else {
 #pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            ov[k] = 0u;
-                    }
+                            for (int k = 0; k < 32; ++k)
+                                ov[k] = 0u;
+                        }
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        const uint32_t* o = ov + 8 * ch;
-                        __stcg(st_o + (q4 * 4 + ch) * 128,
-                               make_uint4(pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv),
-                                          pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv),
-                                          pack_bf16x2(__uint_as_float(o[4]) * inv, __uint_as_float(o[5]) * inv),
-                                          pack_bf16x2(__uint_as_float(o[6]) * inv, __uint_as_float(o[7]) * inv)));
-                    }
-                }
-                __stcg(a.state_ml + sl * 128 + r, make_float2(m_used, l));
-                flag_slot = sl;
-            } else {
-                // O / l -> bf16; merged first with the state the item's last
-                // tiles left: M = max(m, m_t), l' = l 2^(m - M) + l_t 2^(m_t - M),
-                // o = (O 2^(m - M) + O_t / l_t l_t 2^(m_t - M)) / l'.
-                float a_own = l > 0.f ? a.out_scale / l : 0.f;
-                float w_t = 0.f;
-                const uint4* st_t = nullptr;
-                if (role == kMerge) {
-                    const unsigned long long* f = a.flags + sl * 4 + w4;
-                    bool got = ld_acquire_gpu(f) == a.stamp;
-                    if (!got) {
-                        const uint64_t t0 = global_timer_ns();
-                        const uint64_t limit = misc[0] ? kShortWaitLimitNs : kWaitLimitNs;
-                        for (uint32_t w = 1; !got; ++w) {
-                            got = ld_acquire_gpu(f) == a.stamp;
-                            if (!got && (w & 15u) == 0 && global_timer_ns() - t0 > limit)
-                                break;
+                        for (int ch = 0; ch < 4; ++ch) {
+                            const uint32_t* o = ov + 8 * ch;
+                            __stcg(st_o + (q4 * 4 + ch) * 128,
+                                   make_uint4(pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv),
+                                              pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv),
+                                              pack_bf16x2(__uint_as_float(o[4]) * inv, __uint_as_float(o[5]) * inv),
+                                              pack_bf16x2(__uint_as_float(o[6]) * inv, __uint_as_float(o[7]) * inv)));
                         }
                     }
-                    if (!__all_sync(0xffffffffu, got) && lane == 0 && !misc[0]) {
-                        misc[0] = 1;
-                        atomicOr(a.err, PA_DEVERR_TIMEOUT_BIT);
+                    __stcg(a.state_ml + sl * 128 + r, make_float2(m_used, l));
+                    flag_slot = sl;
+                } else {
+                    // O / l -> bf16; merged first with the state the item's last
+                    // tiles left: M = max(m, m_t), l' = l 2^(m - M) + l_t 2^(m_t - M),
+                    // o = (O 2^(m - M) + O_t / l_t l_t 2^(m_t - M)) / l'.
+                    float a_own = l > 0.f ? a.out_scale / l : 0.f;
+                    float w_t = 0.f;
+                    const uint4* st_t = nullptr;
+                    if (role == kMerge) {
+                        const unsigned long long* f = a.flags + sl * 4 + w4;
+                        bool got = ld_acquire_gpu(f) == a.stamp;
+                        if (!got) {
+                            const uint64_t t0 = global_timer_ns();
+                            const uint64_t limit = misc[0] ? kShortWaitLimitNs : kWaitLimitNs;
+                            for (uint32_t w = 1; !got; ++w) {
+                                got = ld_acquire_gpu(f) == a.stamp;
+                                if (!got && (w & 15u) == 0 && global_timer_ns() - t0 > limit)
+                                    break;
+                            }
+                        }
+                        if (!__all_sync(0xffffffffu, got) && lane == 0 && !misc[0]) {
+                            misc[0] = 1;
+                            atomicOr(a.err, PA_DEVERR_TIMEOUT_BIT);
+                        }
+                        __syncwarp();
+                        const float2 ml = __ldcg(a.state_ml + sl * 128 + r);
+                        const float mx = fmaxf(m_used, ml.x);
+                        const float f_own = m_used == -INFINITY ? 0.f : fast_exp2(m_used - mx);
+                        const float f_t = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mx);
+                        const float lt = l * f_own + ml.y * f_t;
+                        const float inv = lt > 0.f ? a.out_scale / lt : 0.f;
+                        a_own = f_own * inv;
+                        w_t = ml.y * f_t * inv;
+                        st_t = a.state + sl * 16 * 128 + r;
                     }
-                    __syncwarp();
-                    const float2 ml = __ldcg(a.state_ml + sl * 128 + r);
-                    const float mx = fmaxf(m_used, ml.x);
-                    const float f_own = m_used == -INFINITY ? 0.f : fast_exp2(m_used - mx);
-                    const float f_t = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mx);
-                    const float lt = l * f_own + ml.y * f_t;
-                    const float inv = lt > 0.f ? a.out_scale / lt : 0.f;
-                    a_own = f_own * inv;
-                    w_t = ml.y * f_t * inv;
-                    st_t = a.state + sl * 16 * 128 + r;
+                    // This warp's 32 rows: one TMA store of 32 rows x 64 columns per
+                    // half from the staging buffer (rows past L are outside the output
+                    // map's L extent and are not written).
+                    const int oz = e[kEB] * a.H_q + e[head == 0 ? kEH0 : kEH1];
+                    const bool write = rows - w4 * 32 > 0 && misc[0] == 0 && !(head == 1 && e[kEDup]);
+#pragma unroll 1
+                    for (int hf = 0; hf < Layout::kHalves; ++hf) {
+                        // the staging buffer's previous store has read it
+                        if (lane == 0)
+                            tma_store_wait_read();
+                        __syncwarp();
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {     // columns 64 hf + 32 q .. + 31 of this row
+                            uint32_t ov[32];
+                            if (nt > 0) {
+                                tmem_ld32(to + 32u * (2 * hf + q), ov);
+                                tmem_wait_ld();
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 32; ++k)
+                                    ov[k] = 0u;
+                            }
+                            float* o = reinterpret_cast<float*>(ov);
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                o[k] *= a_own;
+                            if (st_t != nullptr) {
+#pragma unroll
+                                for (int c4 = 0; c4 < 4; ++c4) {
+                                    const uint4 v = __ldcg(st_t + (8 * hf + 4 * q + c4) * 128);
+                                    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                                    for (int k = 0; k < 4; ++k) {
+                                        o[8 * c4 + 2 * k] += w_t * __uint_as_float(vw[k] << 16);
+                                        o[8 * c4 + 2 * k + 1] += w_t * __uint_as_float(vw[k] & 0xffff0000u);
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int c4 = 0; c4 < 4; ++c4) {
+                                const int cq = 4 * q + c4;
+                                const float* oc = o + 8 * c4;
+                                *reinterpret_cast<uint4*>(stage + lane * 128 + ((cq ^ (lane & 7)) << 4)) =
+                                    make_uint4(pack_bf16x2(oc[0], oc[1]), pack_bf16x2(oc[2], oc[3]),
+                                               pack_bf16x2(oc[4], oc[5]), pack_bf16x2(oc[6], oc[7]));
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && write) {
+                            tma_store_3d(&out_map, stage, hf * 64, row0 + w4 * 32, oz);
+                            tma_store_commit();
+                        }
+                    }
                 }
-                // This warp's 32 rows: one TMA store of 32 rows x 64 columns per
-                // half from the staging buffer (rows past L are outside the output
-                // map's L extent and are not written).
+            } else {
                 const int oz = e[kEB] * a.H_q + e[head == 0 ? kEH0 : kEH1];
                 const bool write = rows - w4 * 32 > 0 && misc[0] == 0 && !(head == 1 && e[kEDup]);
+                const float inv = l > 0.f ? a.out_scale / l : 0.f;
+                // This warp's 32 rows: one TMA store of 32 rows x 64 columns per
+                // half from the staging buffer (rows past L are outside the
+                // output map's L extent and are not written).
 #pragma unroll 1
                 for (int hf = 0; hf < Layout::kHalves; ++hf) {
                     // the staging buffer's previous store has read it
@@ -849,29 +918,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int k = 0; k < 32; ++k)
                                 ov[k] = 0u;
                         }
-                        float* o = reinterpret_cast<float*>(ov);
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            o[k] *= a_own;
-                        if (st_t != nullptr) {
-#pragma unroll
-                            for (int c4 = 0; c4 < 4; ++c4) {
-                                const uint4 v = __ldcg(st_t + (8 * hf + 4 * q + c4) * 128);
-                                const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                                for (int k = 0; k < 4; ++k) {
-                                    o[8 * c4 + 2 * k] += w_t * __uint_as_float(vw[k] << 16);
-                                    o[8 * c4 + 2 * k + 1] += w_t * __uint_as_float(vw[k] & 0xffff0000u);
-                                }
-                            }
-                        }
 #pragma unroll
                         for (int c4 = 0; c4 < 4; ++c4) {
                             const int cq = 4 * q + c4;
-                            const float* oc = o + 8 * c4;
-                            *reinterpret_cast<uint4*>(stage + lane * 128 + ((cq ^ (lane & 7)) << 4)) =
-                                make_uint4(pack_bf16x2(oc[0], oc[1]), pack_bf16x2(oc[2], oc[3]),
-                                           pack_bf16x2(oc[4], oc[5]), pack_bf16x2(oc[6], oc[7]));
+                            const uint32_t* o = ov + 8 * c4;
+                            *reinterpret_cast<uint4*>(stage + lane * 128 + ((cq ^ (lane & 7)) << 4)) = make_uint4(
+                                pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv),
+                                pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv),
+                                pack_bf16x2(__uint_as_float(o[4]) * inv, __uint_as_float(o[5]) * inv),
+                                pack_bf16x2(__uint_as_float(o[6]) * inv, __uint_as_float(o[7]) * inv));
                         }
                     }
                     fence_proxy_async_smem();
@@ -887,8 +942,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             g += nt;
         }
-        if (flag_slot >= 0)
-            raise_flag();
+        if (kPieces && flag_slot >= 0)
+            publish_state(a.flags + flag_slot * 4 + w4, a.stamp, lane);
         if (lane == 0)
             tma_store_wait_all();     // every output store has landed
         __syncwarp();
@@ -923,7 +978,7 @@ namespace {
 
 // Register split and shared-memory limit checked once per device and
 // instantiation, then the launch.
-template <bool kOdd, int kD>
+template <bool kOdd, int kD, bool kPieces>
 cudaError_t launch_pairs(const cudaLaunchConfig_t& cfg_in, const CUtensorMap& q_map,
                          const CUtensorMap& key_map, const CUtensorMap& value_map,
                          const CUtensorMap& out_map, const PrefillArgs& a, int device)
@@ -933,7 +988,7 @@ cudaError_t launch_pairs(const cudaLaunchConfig_t& cfg_in, const CUtensorMap& q_
     static std::atomic<int> regs_ok[kMaxDev];
     if (device < 0 || device >= kMaxDev)
         return cudaErrorInvalidDevice;
-    const void* fn = reinterpret_cast<const void*>(prefill_pairs_kernel<kOdd, kD>);
+    const void* fn = reinterpret_cast<const void*>(prefill_pairs_kernel<kOdd, kD, kPieces>);
     const int smem = Layout<kD>::kBytes;
     // The register split needs 128 x kRegsProducer + 256 x kRegsSoftmax
     // registers out of the launch's own 384 x numRegs, a launch count no
@@ -960,8 +1015,8 @@ cudaError_t launch_pairs(const cudaLaunchConfig_t& cfg_in, const CUtensorMap& q_
     }
     cudaLaunchConfig_t cfg = cfg_in;
     cfg.dynamicSmemBytes = size_t(smem);
-    return cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<kOdd, kD>, q_map, key_map, value_map, out_map,
-                              a);
+    return cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<kOdd, kD, kPieces>, q_map, key_map, value_map,
+                              out_map, a);
 }
 
 }  // namespace
@@ -1005,10 +1060,13 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
     const bool odd = a.G % 2 != 0;
     auto launch = [&]() {
         if (a.D == 64)
-            return odd ? launch_pairs<true, 64>(cfg, q_map, key_map, value_map, out_map, a, device)
-                       : launch_pairs<false, 64>(cfg, q_map, key_map, value_map, out_map, a, device);
-        return odd ? launch_pairs<true, 128>(cfg, q_map, key_map, value_map, out_map, a, device)
-                   : launch_pairs<false, 128>(cfg, q_map, key_map, value_map, out_map, a, device);
+            return odd ? launch_pairs<true, 64, false>(cfg, q_map, key_map, value_map, out_map, a, device)
+                       : launch_pairs<false, 64, false>(cfg, q_map, key_map, value_map, out_map, a, device);
+        if (a.state != nullptr)
+            return odd ? launch_pairs<true, 128, true>(cfg, q_map, key_map, value_map, out_map, a, device)
+                       : launch_pairs<false, 128, true>(cfg, q_map, key_map, value_map, out_map, a, device);
+        return odd ? launch_pairs<true, 128, false>(cfg, q_map, key_map, value_map, out_map, a, device)
+                   : launch_pairs<false, 128, false>(cfg, q_map, key_map, value_map, out_map, a, device);
     };
     // Tail pieces (a block waits for another's state): with a workspace, one
     // or two items per block, the ranking in shared memory, and a cooperative

@@ -260,7 +260,8 @@ pa_status pa_decode_fp8(const void *query, const void *key_pages, const void *va
  * (batch * ceil(max_context_len / 128) pages of num_kv_heads * 128 * 128
  * elements each, 64 KiB per page and KV head for K and V together), their
  * page table, and the split prefill's workspace when pa_prefill_fp8 takes
- * that kernel for the shape (the same rule as pa_attention's prefill route).
+ * that kernel for the shape, or the pairs kernel's tail pieces' (the same
+ * rules as pa_attention's prefill route).
  */
 size_t pa_prefill_fp8_workspace_bytes(pa_shape shape, int32_t max_context_len);
 
@@ -272,7 +273,8 @@ size_t pa_prefill_fp8_workspace_bytes(pa_shape shape, int32_t max_context_len);
  *   1. the K/V tokens each request can see are copied into bf16 pages of
  *      128 tokens in the workspace, each code converted to its exact value
  *      (e4m3 values are bf16 values; a NaN code stays NaN);
- *   2. pa_prefill's kernels (or pa_prefill_split's, by pa_attention's rule)
+ *   2. the kernels of pa_attention's prefill route (pa_prefill's, with tail
+ *      pieces at 1.5 to 2 items per SM, or pa_prefill_split's below 1.5)
  *      attend over the copies, with scale * k_scale as the softmax scale and
  *      the output multiplied by v_scale, so the scaled values are never
  *      rounded.

@@ -597,7 +597,7 @@ namespace {
 struct Fp8PrefillPlan {
     int64_t P2 = 0;
     pa_shape copy{};
-    size_t kv_bytes = 0, table_off = 0, split_off = 0, split_bytes = 0, total = 0;
+    size_t kv_bytes = 0, table_off = 0, split_off = 0, split_bytes = 0, piece_bytes = 0, total = 0;
 };
 
 pa_status plan_prefill_fp8(const pa_shape& s, int32_t max_context_len, DeviceInfo* dev,
@@ -618,10 +618,15 @@ pa_status plan_prefill_fp8(const pa_shape& s, int32_t max_context_len, DeviceInf
     const size_t table_bytes = size_t(pages) * 4;
     p->split_off = (p->table_off + table_bytes + 255) & ~size_t(255);
     // the kernel choice of pa_attention's prefill route (split below 1.5
-    // items per SM)
+    // items per SM; from there to 2 items per SM the pairs kernel's tail
+    // pieces, in the same place)
     const int64_t items = prefill_pair_items(s);
-    p->split_bytes = 2 * items < 3 * int64_t(dev->sm_count) ? split_prefill_need(p->copy, 128, dev) : 0;
-    p->total = p->split_off + p->split_bytes;
+    const bool few = 2 * items < 3 * int64_t(dev->sm_count);
+    p->split_bytes = few ? split_prefill_need(p->copy, 128, dev) : 0;
+    p->piece_bytes = !few && items <= 2 * int64_t(dev->sm_count) && split_prefill_need(p->copy, 128, dev) > 0
+                         ? prefill_pairs_workspace_bytes(dev->sm_count)
+                         : 0;
+    p->total = p->split_off + (p->split_bytes > p->piece_bytes ? p->split_bytes : p->piece_bytes);
     return PA_OK;
 }
 
@@ -685,7 +690,8 @@ pa_status pa_prefill_fp8(const void* query, const void* key_pages, const void* v
     // k_scale into the softmax scale, v_scale into the output normalisation
     return run_prefill_tc(query, c.key_out, c.value_out, c.table_out, context_lens, 128,
                           scale * k_scale, causal, out, p.copy, s,
-                          p.split_bytes ? w + p.split_off : nullptr, p.split_bytes, v_scale);
+                          p.split_bytes ? w + p.split_off : nullptr, p.split_bytes, v_scale,
+                          p.piece_bytes ? w + p.split_off : nullptr, p.piece_bytes);
 }
 
 namespace {

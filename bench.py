@@ -463,6 +463,8 @@ def main(argv=None):
     ap.add_argument("--prefill-shapes", action="store_true",
                     help="time both prefill kernels on chunked-prefill shapes and exit")
     ap.add_argument("--shape", default=None, help="with --prefill-shapes: only this shape")
+    ap.add_argument("--shapes-heads", default="32x8",
+                    help="with --prefill-shapes: query heads x KV heads, e.g. 28x4")
     ap.add_argument("--serving-trace", action="store_true",
                     help="run the synthetic serving trace through pa_kv_cache and exit")
     ap.add_argument("--dense-gather", action="store_true",
@@ -500,7 +502,9 @@ def main(argv=None):
                                                          stream, args.steps, args.warmup)}))
         return 0
     if args.prefill_shapes:
-        print(json.dumps({"prefill_shapes": prefill_shapes(torch, device, args.shape)}))
+        hq, hkv = (int(x) for x in args.shapes_heads.split("x"))
+        print(json.dumps({"prefill_shapes": prefill_shapes(torch, device, args.shape,
+                                                           heads=(hq, hkv))}))
         return 0
     if args.serving_trace:
         serving_trace(torch, device)            # warm-up run (builds, first calls)
@@ -1215,12 +1219,14 @@ PREFILL_SHAPES = [
 ]
 
 
-def prefill_shapes(torch, device, only=None, steps=15):
-    """Both tensor-core prefill kernels (pa_prefill: one block per request x
-    head pair x query tile; pa_prefill_split: K/V tiles spread over one block
-    per SM) on chunked-prefill shapes with few and many query-tile items,
-    L2 flushed before every call, CUDA events. Inputs: seeded N(0,1) K/V
-    already in the pages (no append), random page permutation."""
+def prefill_shapes(torch, device, only=None, steps=15, heads=(32, 8)):
+    """The tensor-core prefill paths (pa_attention with its workspace, as the
+    product calls it; pa_prefill: whole request x head pair x query tile items
+    on one block per SM; pa_prefill_split: K/V tiles spread over one block per
+    SM; pa_prefill_fp8 on e4m3 pools) on chunked-prefill shapes with few and
+    many query-tile items, L2 flushed before every call, CUDA events. Inputs:
+    seeded N(0,1) K/V already in the pages (no append), random page
+    permutation."""
     import paged_kv_attention_06_gb300 as pa
     flush = torch.empty(int(2 * torch.cuda.get_device_properties(device).L2_cache_size),
                         dtype=torch.uint8, device=device)
@@ -1248,7 +1254,7 @@ def prefill_shapes(torch, device, only=None, steps=15):
     for name, B, L, lens in PREFILL_SHAPES:
         if only and name != only:
             continue
-        b = wl.build_batch(name, B=B, H_q=32, H_kv=8, D=128, page_size=16, L=L,
+        b = wl.build_batch(name, B=B, H_q=heads[0], H_kv=heads[1], D=128, page_size=16, L=L,
                            context_lens=lens, seed=5, L_new=0, placement="permutation")
         q, kp, vp = to_dev(b.query), to_dev(b.key_pages), to_dev(b.value_pages)
         bt, cl = to_dev(b.block_table), to_dev(b.context_lens)
@@ -1257,6 +1263,16 @@ def prefill_shapes(torch, device, only=None, steps=15):
                                                causal=True, out=out))
         t_split = timeit(lambda: pa.pa_prefill_split(q, kp, vp, bt, cl, b.page_size,
                                                      scale=b.scale, causal=True, out=out))
+        # the product path: pa_attention with its prefill workspace (split
+        # kernel, pairs kernel with tail pieces, or whole items, by its rule)
+        ws_att = torch.empty(max(1, pa.pa_prefill_workspace_bytes(
+            pa.make_shape(q.shape, kp.shape, bt.shape[1]), b.page_size)), dtype=torch.uint8,
+            device=device)
+        mcl_att = int(b.context_lens.max())
+        t_att = timeit(lambda: pa.pa_attention(q, kp, vp, bt, cl, b.page_size, scale=b.scale,
+                                               causal=True, out=out, max_context_len=mcl_att,
+                                               workspace=ws_att))
+        del ws_att
         rng = np.random.default_rng(6)
         kc = torch.from_numpy(wl.random_e4m3_codes(rng, b.key_pages.shape)).to(device)
         vc = torch.from_numpy(wl.random_e4m3_codes(rng, b.value_pages.shape)).to(device)
@@ -1268,14 +1284,17 @@ def prefill_shapes(torch, device, only=None, steps=15):
                                                  max_context_len=mcl, workspace=ws8))
         del ws8
         fl = prefill_flops(b)
-        items = B * ((L + 127) // 128) * 16
+        items = B * ((L + 127) // 128) * heads[1] * ((heads[0] // heads[1] + 1) // 2)
         rows.append({"shape": name, "items": items, "items_per_sm": round(items / sms, 2),
                      "gflop": round(fl / 1e9, 2),
+                     "attention_us": round(t_att, 2),
+                     "attention_tflops": round(fl / t_att / 1e6, 1),
                      "pairs_us": round(t_pairs, 2), "split_us": round(t_split, 2),
                      "pairs_tflops": round(fl / t_pairs / 1e6, 1),
                      "split_tflops": round(fl / t_split / 1e6, 1),
                      "fp8_pages_us": round(t_fp8, 2), "fp8_pages_tflops": round(fl / t_fp8 / 1e6, 1),
-                     "attention_picks": "split" if 2 * items < 3 * sms else "pairs"})
+                     "attention_picks": ("split" if 2 * items < 3 * sms else
+                                         "pairs, tail pieces" if items <= 2 * sms else "pairs")})
     st, flags = pa.pa_get_device_error()
     if st:
         raise RuntimeError(f"device error in the prefill shapes: {flags:#x}")

@@ -367,10 +367,11 @@ int32_t pa_attention_route(pa_shape shape, int32_t max_context_len);
  * (head_dim 128) that kernel balances the blocks through the workspace: a
  * block holding two items hands the last K/V tiles of its second item to a
  * block holding one, which runs them first and leaves their softmax state
- * (O / l in bf16, the maximum and the sum in fp32) for the first block to
- * merge at its end (a cooperative launch, so every block is resident; every
- * wait is bounded). The output is the same softmax up to rounding. With NULL
- * or a smaller workspace: pa_prefill as it is.
+ * (O / l in bf16, the maximum and the sum in fp32); the first block merges it
+ * at its end. No block waits for another: the side that arrives second merges
+ * (normally the first block), and both sides merge with the same arithmetic,
+ * so the bits do not depend on the order. The output is the same softmax up
+ * to rounding. With NULL or a smaller workspace: pa_prefill as it is.
  */
 pa_status pa_attention(const void *query, const void *key_pages,
                        const void *value_pages, const int32_t *block_table,

@@ -44,7 +44,11 @@ void pa_debug_arm_wait_timeout(void);
  *      tail pieces (a block runs the last tiles of another's second item
  *      first and leaves their state, which that block merges), as it does by
  *      itself with 1 to 2 items per SM. For tests of the pieces on small
- *      shapes.
+ *      shapes;
+ *   5  as 4, with the receiving blocks running the piece after their own
+ *      item, so that the donors usually finish first and the receiving
+ *      blocks write the merged rows (the path taken when a receiving block
+ *      starts late).
  * Settings 1 and 2 also hold for pa_prefill_split and for pa_attention given
  * a prefill workspace (the workspace is then not used). Any other value is
  * taken as 0. Returns the previous setting. Results agree

@@ -258,7 +258,10 @@ size_t split_prefill_need(const pa_shape& s, int32_t page_size, const DeviceInfo
         return 0;
     if (prefill_split_smem_bytes() > size_t(dev->max_smem_optin))
         return 0;
-    return prefill_split_workspace_bytes(dev->sm_count);
+    // the same workspace serves the pairs kernel's tail pieces
+    const size_t split = prefill_split_workspace_bytes(dev->sm_count);
+    const size_t pieces = prefill_pairs_workspace_bytes(dev->sm_count);
+    return split > pieces ? split : pieces;
 }
 
 // Prefill on tcgen05 (D = 128, or D = 64 with at least two query heads per
@@ -335,6 +338,7 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     a.causal = causal ? 1 : 0;
     a.out_scale = out_scale;
     a.D = s.head_dim;
+    a.piece_last = t_prefill_variant == 5 ? 1 : 0;
     if (split) {
         SplitPrefillArgs sa;
         memset(&sa, 0, sizeof sa);
@@ -372,7 +376,7 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     // The pairs kernel's tail pieces use the caller's workspace (pa_attention's).
     // Test setting 4: a grid of two thirds of the items, so that small shapes
     // have blocks of one item and of two, and get pieces.
-    const bool small_grid = t_prefill_variant == 4;
+    const bool small_grid = t_prefill_variant == 4 || t_prefill_variant == 5;
     const int grid_cap = small_grid ? int((2 * pair_items + 2) / 3) : dev->sm_count;
     cudaError_t e = pairs ? launch_prefill_pairs(qmap, kmap, vmap, omap, a, dev->id, grid_cap,
                                                  t_prefill_variant == 0 || small_grid ? piece_ws : nullptr,
@@ -989,7 +993,7 @@ pa_status pa_attention(const void* query, const void* key_pages, const void* val
         return pa_decode(query, key_pages, value_pages, block_table, context_lens, page_size,
                          scale, causal, out, shape, max_context_len, workspace, workspace_bytes,
                          stream);
-    if (workspace && t_prefill_variant != 4) {
+    if (workspace && t_prefill_variant != 4 && t_prefill_variant != 5) {
         // The split kernel pays for its balance at every piece boundary; it
         // is the faster one when the (request, head pair, query tile) items
         // are too few to fill the SMs in whole waves (measured: 1.75x on one
@@ -1056,7 +1060,7 @@ void pa_debug_arm_wait_timeout(void) { t_arm_unset_wait = true; }
 int pa_debug_prefill_variant(int variant)
 {
     const int prev = t_prefill_variant;
-    t_prefill_variant = (variant == 1 || variant == 2 || variant == 4) ? variant : 0;
+    t_prefill_variant = (variant == 1 || variant == 2 || variant == 4 || variant == 5) ? variant : 0;
     return prev;
 }
 

@@ -132,13 +132,15 @@ struct PrefillArgs {
     float out_scale;    // the output is out_scale * softmax . V (e4m3 copies: v_scale)
     int32_t D;          // head_dim: 128 (64 on the pairs kernel only)
     // Pairs kernel, tail pieces (head_dim 128; state == nullptr: none): per
-    // block slot and head, O / l of a piece in bf16 [16 chunks of 8
-    // columns][128 rows], (m, l) per row, and one flag per softmax warp that
-    // holds the launch's stamp once the slot is written.
-    uint4* state;                 // [grid][2][16][128]
-    float2* state_ml;             // [grid][2][128]
-    unsigned long long* flags;    // [grid][2][4]
+    // donor block slot, part (0: the item's last tiles, 1: its first tiles)
+    // and head, O / l in bf16 [16 chunks of 8 columns][128 rows] and (m, l)
+    // per row; per slot, head and softmax warp one arrival word (the launch's
+    // stamp in the high 32 bits, the arrivals in the low 32).
+    uint4* state;                 // [grid][2][2][16][128]
+    float2* state_ml;             // [grid][2][2][128]
+    unsigned long long* arrive;   // [grid][2][4]
     uint64_t stamp;               // this launch's stamp (never 0)
+    int32_t piece_last;           // test setting: receiving blocks run the piece last
 };
 
 // Prefill over e4m3 pools: bf16 copies of the visible K/V tokens, in pages

@@ -177,15 +177,173 @@ __device__ __forceinline__ int2 plan_piece(const int* order, const int* tiles_of
     return make_int2(0, 0);
 }
 
-// Hands a piece's state over: this warp's stores are made visible at GPU scope
-// before lane 0 writes the launch's stamp into the warp's flag. Not inlined:
-// an inlined copy costs the softmax loop registers.
-__device__ __noinline__ void publish_state(unsigned long long* flag, unsigned long long stamp, int lane)
+// Block t's load (quarter tiles) with whole items and with the pieces.
+__device__ __forceinline__ int2 block_loads(const int* order, const int* tiles_of, int pairs, int n_all,
+                                            int nblk, int t)
+{
+    auto size_at = [&](int p) { return tiles_of[order[p / pairs]]; };
+    int before = 4 * size_at(t) + kWItem;
+    if (2 * nblk - 1 - t < n_all)
+        before += 4 * size_at(2 * nblk - 1 - t) + kWItem;
+    const int2 cp = plan_piece(order, tiles_of, pairs, n_all, nblk, t);
+    const int after = before - 4 * cp.x + (cp.x > 0 ? kWMerge : 0) +
+                      (cp.y > 0 ? 4 * cp.y + kWItem + kWPiece : 0);
+    return make_int2(before, after);
+}
+
+// This block's (tiles handed over, tiles taken over), the same in every thread
+// and every block: only when the pieces lower the busiest block's load by a
+// tile or more (with more overloaded blocks than blocks of one item, the ones
+// left out keep the makespan and the pieces would only add their costs).
+// red: 2 x kThreads / 32 ints of scratch. Called by every thread of the
+// block (it synchronises them).
+__device__ __forceinline__ int2 plan_tail_pieces(const int* order, const int* tiles_of, int* red, int pairs,
+                                              int n_all, int nblk, int c)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int2 ld = make_int2(0, 0);
+    if (int(threadIdx.x) < nblk)
+        ld = block_loads(order, tiles_of, pairs, n_all, nblk, int(threadIdx.x));
+    const int mb = __reduce_max_sync(0xffffffffu, ld.x), ma = __reduce_max_sync(0xffffffffu, ld.y);
+    if (lane == 0) {
+        red[warp] = mb;
+        red[kThreads / 32 + warp] = ma;
+    }
+    __syncthreads();
+    int max_before = 0, max_after = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        max_before = max(max_before, red[w]);
+        max_after = max(max_after, red[kThreads / 32 + w]);
+    }
+    if (max_after + 4 > max_before)
+        return make_int2(0, 0);
+    return plan_piece(order, tiles_of, pairs, n_all, nblk, c);
+}
+
+// A piece's hand-over needs no wait. Each side of an item cut in two (its
+// last tiles, run first by the receiving block; its first tiles, run by the
+// donor at its end) arrives once per softmax warp at a word holding the
+// launch's stamp and the arrivals so far. The donor normally finds the other
+// side arrived and merges that side's state into its own O (in TMEM). If it
+// comes first, it leaves its own state and arrives, and the receiving block,
+// arriving second, merges the two states from memory. So no block ever waits
+// for another, and no launch needs every block resident at once.
+
+// Index of a piece's state: donor slot, part (0: last tiles, 1: first), head.
+__device__ __forceinline__ int64_t piece_state(int slot, int part, int head)
+{
+    return (int64_t(slot) * 2 + part) * 2 + head;
+}
+
+// Arrival at a piece's word: the arrivals before this one in this launch (a
+// word holding another launch's stamp counts as none). Two parties at most,
+// so the loop retries at most a few times.
+__device__ __forceinline__ unsigned arrive_piece(unsigned long long* w, uint32_t stamp32)
+{
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(w);
+    for (;;) {
+        const bool mine = uint32_t(old >> 32) == stamp32;
+        const unsigned long long want =
+            (uint64_t(stamp32) << 32) | (mine ? (old & 0xffffffffull) + 1 : 1ull);
+        const unsigned long long got = atomicCAS(w, old, want);
+        if (got == old)
+            return mine ? unsigned(old) : 0u;
+        old = got;
+    }
+}
+
+// The merge of an item's two parts, each held as O / l (bf16) with its (m, l):
+// out = w0 (O_0 / l_0) + w1 (O_1 / l_1), w_k = l_k 2^(m_k - M) out_scale / l,
+// M = max(m_0, m_1), l = l_0 2^(m_0 - M) + l_1 2^(m_1 - M). Whichever block
+// merges computes exactly this, in this order (no contraction), so the output
+// bits do not depend on which one it was.
+__device__ __forceinline__ float2 merge_weights(float2 ml0, float2 ml1, float out_scale)
+{
+    const float mx = fmaxf(ml0.x, ml1.x);
+    const float f0 = ml0.x == -INFINITY ? 0.f : fast_exp2(ml0.x - mx);
+    const float f1 = ml1.x == -INFINITY ? 0.f : fast_exp2(ml1.x - mx);
+    const float p0 = __fmul_rn(ml0.y, f0), p1 = __fmul_rn(ml1.y, f1);
+    const float lt = __fadd_rn(p0, p1);
+    const float inv = lt > 0.f ? __fdiv_rn(out_scale, lt) : 0.f;
+    return make_float2(__fmul_rn(p0, inv), __fmul_rn(p1, inv));
+}
+__device__ __forceinline__ float merge_one(float2 w, float a0, float a1)
+{
+    return __fmaf_rn(w.y, a1, __fmul_rn(w.x, a0));
+}
+// O / l as a piece's state holds it (the same rounding on both sides).
+__device__ __forceinline__ float piece_inv(float l) { return l > 0.f ? __fdiv_rn(1.f, l) : 0.f; }
+
+// This warp's 32 rows of a piece's O / l -> bf16 [16 chunks of 8 columns][128
+// rows] at st (row r = lane already added), (m, l) at ml.
+__device__ __forceinline__ void store_piece_state(uint4* st, float2* ml, uint32_t to, bool has_tiles,
+                                                  float m_used, float l)
+{
+    const float inv = piece_inv(l);
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t ov[32];
+        if (has_tiles) {
+            tmem_ld32(to + 32u * q4, ov);
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                ov[k] = 0u;
+        }
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+            const uint32_t* o = ov + 8 * ch;
+            __stcg(st + (q4 * 4 + ch) * 128,
+                   make_uint4(pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv),
+                              pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv),
+                              pack_bf16x2(__uint_as_float(o[4]) * inv, __uint_as_float(o[5]) * inv),
+                              pack_bf16x2(__uint_as_float(o[6]) * inv, __uint_as_float(o[7]) * inv)));
+        }
+    }
+    __stcg(ml, make_float2(m_used, l));
+}
+
+// The receiving block's arrival, one tile after its piece's state was stored
+// (the stores have drained by then). If the donor arrived first, this warp
+// writes its 32 rows of the item from the two states (rare):
+// M = max(m_0, m_1), l = l_0 2^(m_0 - M) + l_1 2^(m_1 - M),
+// o = (O_0 / l_0 l_0 2^(m_0 - M) + O_1 / l_1 l_1 2^(m_1 - M)) / l.
+__device__ __forceinline__ void piece_arrive_receiver(const uint4* state, const float2* state_ml,
+                                                   unsigned long long* arrive, uint64_t stamp, int slot,
+                                                   int head, int w4, int lane, uint16_t* out_row,
+                                                   bool write, float out_scale)
 {
     __threadfence();
     __syncwarp();
+    unsigned old = 0;
     if (lane == 0)
-        st_release_gpu(flag, stamp);
+        old = arrive_piece(arrive + (int64_t(slot) * 2 + head) * 4 + w4, uint32_t(stamp));
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old == 0)
+        return;                                // the donor merges
+    __threadfence();                           // the donor's state, stored before its arrival
+    __syncwarp();
+    const int r = w4 * 32 + lane;
+    const int64_t i0 = piece_state(slot, 0, head), i1 = piece_state(slot, 1, head);
+    const float2 w = merge_weights(__ldcg(state_ml + i0 * 128 + r), __ldcg(state_ml + i1 * 128 + r),
+                                   out_scale);
+    const uint4* s0 = state + i0 * 16 * 128 + r;
+    const uint4* s1 = state + i1 * 16 * 128 + r;
+#pragma unroll 1
+    for (int ch = 0; ch < 16; ++ch) {
+        const uint4 v0 = __ldcg(s0 + ch * 128), v1 = __ldcg(s1 + ch * 128);
+        const uint32_t a0[4] = {v0.x, v0.y, v0.z, v0.w}, a1[4] = {v1.x, v1.y, v1.z, v1.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            o[k] = pack_bf16x2(merge_one(w, __uint_as_float(a0[k] << 16), __uint_as_float(a1[k] << 16)),
+                               merge_one(w, __uint_as_float(a0[k] & 0xffff0000u),
+                                         __uint_as_float(a1[k] & 0xffff0000u)));
+        if (write)
+            *reinterpret_cast<uint4*>(out_row + ch * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
 }
 
 // kOdd: the group size is odd and the last pair of each group repeats its
@@ -279,15 +437,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         kPieces && kD == 128 && a.state != nullptr && M <= kThreads && n_all > nblk && n_all <= 2 * nblk;
     int my_cut = 0, my_piece = 0;             // tiles handed over / taken over
     if (pieces) {
-        const int2 cp = plan_piece(order, tiles_of, pairs, int(n_all), int(nblk), int(c));
+        const int2 cp = plan_tail_pieces(order, tiles_of, n_of + kThreads, pairs, int(n_all), int(nblk),
+                                         int(c));
         my_cut = cp.x;
         my_piece = cp.y;
     }
     const int n_items = n_own + (my_piece > 0 ? 1 : 0);
     if (int(threadIdx.x) < n_items) {
-        // entry 0 of a receiving block is the piece (the donor's second item)
+        // entry 0 of a receiving block is the piece (the donor's second item);
+        // the last one under the test setting that makes the donors finish
+        // first
         const int slot = my_piece > 0 ? int(nblk) - 1 - int(c) : int(c);
-        const int own = int(threadIdx.x) - (my_piece > 0 ? 1 : 0);
+        const int pe = a.piece_last ? n_items - 1 : 0;    // the piece's entry
+        const int own = my_piece > 0 ? (int(threadIdx.x) == pe ? -1 : int(threadIdx.x) - (pe == 0 ? 1 : 0))
+                                     : int(threadIdx.x);
         const int64_t i = own < 0 ? nblk + c : item_at(own);
         const int rank = int(i / pairs);
         const int hp = int(i - int64_t(rank) * pairs);
@@ -643,7 +806,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // chunks swizzled by row as the output map's 128-byte swizzle wants;
         // one lane then stores the warp's 32 rows x 64 columns by TMA.
         uint8_t* stage = smem + Layout::kStage + (warp - 4) * Layout::kStageWarp;
-        int64_t flag_slot = -1;                      // a piece's slot whose flag is due
+        int pend_it = -1;                            // a published piece whose arrival is due
+        // the receiving block's arrival for the piece of item pend_it (rows
+        // of this warp); writes them too if the donor came first
+        auto arrive_pending = [&]() {
+            const int32_t* pe = items + pend_it * kEntry;
+            const int prow0 = pe[kET] * kRows;
+            const bool pwrite = prow0 + r < a.L && misc[0] == 0 && !(head == 1 && pe[kEDup]);
+            uint16_t* out_row =
+                a.out + ((int64_t(pe[kEB]) * a.H_q + pe[head == 0 ? kEH0 : kEH1]) * a.L + prow0 + r) * 128;
+            piece_arrive_receiver(a.state, a.state_ml, a.arrive, a.stamp, pe[kESlot], head, w4, lane,
+                                  out_row, pwrite, a.out_scale);
+            pend_it = -1;
+        };
         int g = 0;                                   // tiles of the block before this item
         for (int it = 0; it < n_items; ++it) {
             const int32_t* e = items + it * kEntry;
@@ -763,10 +938,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&bar[kPFull + head]);
-                if (kPieces && flag_slot >= 0) {
-                    publish_state(a.flags + flag_slot * 4 + w4, a.stamp, lane);
-                    flag_slot = -1;
-                }
+                if (kPieces && pend_it >= 0)
+                    arrive_pending();
             }
             // ---- epilogue of the item ---------------------------------------------
             if (nt > 0) {
@@ -774,76 +947,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
             }
             if constexpr (kPieces) {
-                const int64_t sl = int64_t(e[kESlot]) * 2 + head;     // a piece's state slot
+                const int slot = e[kESlot];
                 if (role == kPublish) {
-                    // The item's last tiles: O / l in bf16 as [16 chunks of 8
-                    // columns][128 rows] (a warp's stores contiguous) and (m, l) per
-                    // row, for the block that holds the item's first tiles; the
-                    // flag is raised one tile later, once the stores have drained.
-                    uint4* st_o = a.state + sl * 16 * 128 + r;
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t ov[32];
-                        if (nt > 0) {
-                            tmem_ld32(to + 32u * q4, ov);
-                            tmem_wait_ld();
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                ov[k] = 0u;
-                        }
-#pragma unroll
-                        for (int ch = 0; ch < 4; ++ch) {
-                            const uint32_t* o = ov + 8 * ch;
-                            __stcg(st_o + (q4 * 4 + ch) * 128,
-                                   make_uint4(pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv),
-                                              pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv),
-                                              pack_bf16x2(__uint_as_float(o[4]) * inv, __uint_as_float(o[5]) * inv),
-                                              pack_bf16x2(__uint_as_float(o[6]) * inv, __uint_as_float(o[7]) * inv)));
-                        }
-                    }
-                    __stcg(a.state_ml + sl * 128 + r, make_float2(m_used, l));
-                    flag_slot = sl;
+                    // The item's last tiles: their state (part 0) for the block
+                    // that holds the item's first tiles; this warp arrives one
+                    // tile later, once the stores have drained.
+                    const int64_t i0 = piece_state(slot, 0, head);
+                    store_piece_state(a.state + i0 * 16 * 128 + r, a.state_ml + i0 * 128 + r, to, nt > 0,
+                                      m_used, l);
+                    pend_it = it;
                 } else {
                     // O / l -> bf16; merged first with the state the item's last
                     // tiles left: M = max(m, m_t), l' = l 2^(m - M) + l_t 2^(m_t - M),
                     // o = (O 2^(m - M) + O_t / l_t l_t 2^(m_t - M)) / l'.
-                    float a_own = l > 0.f ? a.out_scale / l : 0.f;
-                    float w_t = 0.f;
+                    const float a_own = l > 0.f ? a.out_scale / l : 0.f;
+                    float2 w_m = make_float2(0.f, 0.f);   // merge weights (last tiles, these)
+                    const float inv_own = piece_inv(l);
                     const uint4* st_t = nullptr;
+                    bool skip = false;                 // the receiving block writes these rows
                     if (role == kMerge) {
-                        const unsigned long long* f = a.flags + sl * 4 + w4;
-                        bool got = ld_acquire_gpu(f) == a.stamp;
-                        if (!got) {
-                            const uint64_t t0 = global_timer_ns();
-                            const uint64_t limit = misc[0] ? kShortWaitLimitNs : kWaitLimitNs;
-                            for (uint32_t w = 1; !got; ++w) {
-                                got = ld_acquire_gpu(f) == a.stamp;
-                                if (!got && (w & 15u) == 0 && global_timer_ns() - t0 > limit)
-                                    break;
-                            }
+                        // Normally the last tiles' state is long there; if not,
+                        // this part's state is left and the receiving block,
+                        // arriving second, writes the rows (no wait either way).
+                        unsigned long long* w = a.arrive + (int64_t(slot) * 2 + head) * 4 + w4;
+                        bool got = false;
+                        if (lane == 0) {
+                            const unsigned long long v = ld_acquire_gpu(w);
+                            got = uint32_t(v >> 32) == uint32_t(a.stamp) && uint32_t(v) >= 1u;
                         }
-                        if (!__all_sync(0xffffffffu, got) && lane == 0 && !misc[0]) {
-                            misc[0] = 1;
-                            atomicOr(a.err, PA_DEVERR_TIMEOUT_BIT);
+                        got = __shfl_sync(0xffffffffu, got, 0);
+                        if (!got) {
+                            const int64_t i1 = piece_state(slot, 1, head);
+                            store_piece_state(a.state + i1 * 16 * 128 + r, a.state_ml + i1 * 128 + r, to,
+                                              nt > 0, m_used, l);
+                            __threadfence();
+                            __syncwarp();
+                            unsigned old = 0;
+                            if (lane == 0)
+                                old = arrive_piece(w, uint32_t(a.stamp));
+                            old = __shfl_sync(0xffffffffu, old, 0);
+                            skip = old == 0;
+                            __threadfence();
                         }
                         __syncwarp();
-                        const float2 ml = __ldcg(a.state_ml + sl * 128 + r);
-                        const float mx = fmaxf(m_used, ml.x);
-                        const float f_own = m_used == -INFINITY ? 0.f : fast_exp2(m_used - mx);
-                        const float f_t = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mx);
-                        const float lt = l * f_own + ml.y * f_t;
-                        const float inv = lt > 0.f ? a.out_scale / lt : 0.f;
-                        a_own = f_own * inv;
-                        w_t = ml.y * f_t * inv;
-                        st_t = a.state + sl * 16 * 128 + r;
+                        const int64_t i0 = piece_state(slot, 0, head);
+                        w_m = merge_weights(__ldcg(a.state_ml + i0 * 128 + r), make_float2(m_used, l),
+                                            a.out_scale);
+                        st_t = a.state + i0 * 16 * 128 + r;
                     }
                     // This warp's 32 rows: one TMA store of 32 rows x 64 columns per
                     // half from the staging buffer (rows past L are outside the output
                     // map's L extent and are not written).
                     const int oz = e[kEB] * a.H_q + e[head == 0 ? kEH0 : kEH1];
-                    const bool write = rows - w4 * 32 > 0 && misc[0] == 0 && !(head == 1 && e[kEDup]);
+                    const bool write =
+                        !skip && rows - w4 * 32 > 0 && misc[0] == 0 && !(head == 1 && e[kEDup]);
 #pragma unroll 1
                     for (int hf = 0; hf < Layout::kHalves; ++hf) {
                         // the staging buffer's previous store has read it
@@ -862,18 +1019,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     ov[k] = 0u;
                             }
                             float* o = reinterpret_cast<float*>(ov);
+                            if (st_t == nullptr) {
 #pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                o[k] *= a_own;
-                            if (st_t != nullptr) {
+                                for (int k = 0; k < 32; ++k)
+                                    o[k] *= a_own;
+                            } else {
+                                // this part's O / l rounded as its state would be, then
+                                // the merge with the last tiles' state
 #pragma unroll
                                 for (int c4 = 0; c4 < 4; ++c4) {
                                     const uint4 v = __ldcg(st_t + (8 * hf + 4 * q + c4) * 128);
                                     const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                                     for (int k = 0; k < 4; ++k) {
-                                        o[8 * c4 + 2 * k] += w_t * __uint_as_float(vw[k] << 16);
-                                        o[8 * c4 + 2 * k + 1] += w_t * __uint_as_float(vw[k] & 0xffff0000u);
+                                        const uint32_t own = pack_bf16x2(o[8 * c4 + 2 * k] * inv_own,
+                                                                         o[8 * c4 + 2 * k + 1] * inv_own);
+                                        o[8 * c4 + 2 * k] = merge_one(w_m, __uint_as_float(vw[k] << 16),
+                                                                      __uint_as_float(own << 16));
+                                        o[8 * c4 + 2 * k + 1] =
+                                            merge_one(w_m, __uint_as_float(vw[k] & 0xffff0000u),
+                                                      __uint_as_float(own & 0xffff0000u));
                                     }
                                 }
                             }
@@ -942,8 +1107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             g += nt;
         }
-        if (kPieces && flag_slot >= 0)
-            publish_state(a.flags + flag_slot * 4 + w4, a.stamp, lane);
+        if (kPieces && pend_it >= 0)
+            arrive_pending();
         if (lane == 0)
             tma_store_wait_all();     // every output store has landed
         __syncwarp();
@@ -964,14 +1129,16 @@ size_t prefill_pairs_smem_bytes(int D)
 }
 
 namespace {
-constexpr size_t kPieceState = 2 * 16 * 128 * sizeof(uint4);      // per block: O / l, both heads
-constexpr size_t kPieceMl = 2 * 128 * sizeof(float2);             // (m, l) per row and head
-constexpr size_t kPieceFlags = 2 * 4 * sizeof(unsigned long long);
+// per block slot: O / l of both parts and heads, (m, l) per row, part and
+// head, one arrival word per head and softmax warp
+constexpr size_t kPieceState = 2 * 2 * 16 * 128 * sizeof(uint4);
+constexpr size_t kPieceMl = 2 * 2 * 128 * sizeof(float2);
+constexpr size_t kPieceArrive = 2 * 4 * sizeof(unsigned long long);
 }  // namespace
 
 size_t prefill_pairs_workspace_bytes(int grid)
 {
-    return size_t(grid) * (kPieceState + kPieceMl + kPieceFlags);
+    return size_t(grid) * (kPieceState + kPieceMl + kPieceArrive);
 }
 
 namespace {
@@ -1029,7 +1196,7 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
     PrefillArgs a = a_in;
     a.state = nullptr;
     a.state_ml = nullptr;
-    a.flags = nullptr;
+    a.arrive = nullptr;
     a.stamp = 0;
     if (a.D != 64 && a.D != 128)
         return cudaErrorInvalidValue;
@@ -1046,11 +1213,9 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
     // Programmatic stream serialization: the blocks may be scheduled while the
     // previous kernel in the stream finishes; each waits for it
     // (griddepcontrol.wait) before reading anything.
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeCooperative;
-    attr[1].val.cooperative = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
     cfg.blockDim = dim3(kThreads);
@@ -1068,9 +1233,9 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
         return odd ? launch_pairs<true, 128, false>(cfg, q_map, key_map, value_map, out_map, a, device)
                    : launch_pairs<false, 128, false>(cfg, q_map, key_map, value_map, out_map, a, device);
     };
-    // Tail pieces (a block waits for another's state): with a workspace, one
-    // or two items per block, the ranking in shared memory, and a cooperative
-    // launch so that every block is resident; otherwise whole items.
+    // Tail pieces: with a workspace, one or two items per block and the
+    // ranking in shared memory; otherwise whole items. No block waits for
+    // another (the second to arrive merges), so the launch is an ordinary one.
     const int64_t M = int64_t(a.B) * a.n_qtiles;
     if (workspace && a.D == 128 && M <= kThreads && n_items > grid && n_items <= 2 * grid &&
         workspace_bytes >= prefill_pairs_workspace_bytes(int(grid)) &&
@@ -1078,22 +1243,8 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
         uint8_t* w = static_cast<uint8_t*>(workspace);
         a.state = reinterpret_cast<uint4*>(w);
         a.state_ml = reinterpret_cast<float2*>(w + size_t(grid) * kPieceState);
-        a.flags = reinterpret_cast<unsigned long long*>(w + size_t(grid) * (kPieceState + kPieceMl));
+        a.arrive = reinterpret_cast<unsigned long long*>(w + size_t(grid) * (kPieceState + kPieceMl));
         a.stamp = next_launch_stamp();
-        cfg.numAttrs = 2;
-        // An error the caller left pending is not ours to clear: note it, so
-        // that only a refused cooperative launch of this call is cleared.
-        const bool pending = cudaPeekAtLastError() != cudaSuccess;
-        const cudaError_t e = launch();
-        if (e != cudaErrorCooperativeLaunchTooLarge)
-            return e;
-        if (!pending)
-            (void)cudaGetLastError();
-        a.state = nullptr;                      // not every block could be resident
-        a.state_ml = nullptr;
-        a.flags = nullptr;
-        a.stamp = 0;
-        cfg.numAttrs = 1;
     }
     return launch();
 }

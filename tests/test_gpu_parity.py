@@ -517,13 +517,14 @@ def test_split_prefill_workspace_contents_and_repeat():
     assert_close(host_f64(outs[0]), oracle_out(b, kp, vp), "split workspace contents")
 
 
-@pytest.fixture
-def tail_pieces():
+@pytest.fixture(params=[4, 5], ids=["receiver_first", "donor_first"])
+def tail_pieces(request):
     """pa_attention's pairs kernel on a grid of two thirds of the items, so
     that the blocks with two items hand the last tiles of their second one to
-    blocks with one (test setting 4)."""
+    blocks with one (test setting 4; setting 5 runs the pieces last, so that
+    the donors usually arrive first and the receiving blocks merge)."""
     import paged_kv_attention_06_gb300 as pa
-    prev = pa.pa_debug_prefill_variant(4)
+    prev = pa.pa_debug_prefill_variant(request.param)
     yield
     pa.pa_debug_prefill_variant(prev)
 

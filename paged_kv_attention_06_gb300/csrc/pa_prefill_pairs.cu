@@ -116,8 +116,9 @@ constexpr int kMmaDone = 18;
 static_assert(kMmaDone < Layout<128>::kNumBars, "barrier count");
 
 // Item table entry: request, query tile, the two query heads, the KV head,
-// the (clamped) context length, K/V tiles visited, whether head 1 repeats
-// head 0.
+// the (clamped) context length, K/V tiles run here, whether head 1 repeats
+// head 0, the first K/V tile run here, the role (below), the tail piece's
+// state slot (its donor block).
 enum { kEB = 0, kET, kEH0, kEH1, kEHK, kEN, kENT, kEDup, kEK0, kERole, kESlot, kEntry = 12 };
 // Item roles: the whole item here; the item's last tiles here, state left
 // for its first block (run first on the receiving block); the item's first
@@ -135,7 +136,8 @@ enum { kWhole = 0, kPublish = 1, kMerge = 2 };
 // kWPiece) / 8), at most the item's tiles less one, none when below one. The
 // weights are measured: on 4 requests of 512 rows after ragged prefixes (the
 // busiest blocks at two items of 14 tiles, the idlest at one of 17) they give
-// d = 6, 52.6 us per call; d = 4 / 5 / 7 / 8 gave 55.0 / 53.8 / 54.5 / 56.5.
+// d = 6, 52.6 us per call back to back; d = 4 / 5 / 7 / 8 gave 55.0 / 53.8 /
+// 54.5 / 56.5 (with an earlier hand-over that waited for a flag).
 constexpr int kWItem = 4;
 constexpr int kWPiece = 0;
 constexpr int kWMerge = 8;

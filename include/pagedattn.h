@@ -207,8 +207,9 @@ pa_status pa_decode_dense(const void *query, const void *key_dense,
  * block_table (Week 3 Day 4, "Task 2", the long-query page-walking
  * schedule), causal by default with the bottom-right offset above. Needs no
  * workspace. Tensor-core kernels (tcgen05, TMEM) for page_size >= 8 with
- * head_dim 128, and with head_dim 64 when a KV group has at least two query
- * heads; other shapes run the split-KV kernel with whole segments per block.
+ * head_dim 128 or 64 (head_dim 64 with one query head per KV group computes
+ * that head in both halves of a two-head block); smaller pages run the
+ * split-KV kernel with whole segments per block.
  */
 pa_status pa_prefill(const void *query, const void *key_pages,
                      const void *value_pages, const int32_t *block_table,

@@ -264,8 +264,7 @@ size_t split_prefill_need(const pa_shape& s, int32_t page_size, const DeviceInfo
     return split > pieces ? split : pieces;
 }
 
-// Prefill on tcgen05 (D = 128, or D = 64 with at least two query heads per
-// KV group; page_size >= 8). With a workspace of at least split_prefill_need
+// Prefill on tcgen05 (D = 128 or 64; page_size >= 8). With a workspace of at least split_prefill_need
 // bytes: the split kernel (K/V tiles spread evenly over one block per SM);
 // otherwise the persistent pairs kernel (whole (request, head pair, 128-row
 // query tile) items) or one block per (request, query head, query tile).
@@ -292,10 +291,11 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     // us; with 256 pair items the pairs kernel is 22-33 % faster).
     const int g = s.num_q_heads / s.num_kv_heads;
     const int64_t pair_items = prefill_pair_items(s);
-    const bool d64 = s.head_dim == 64;   // only the pairs kernel has the 64-column form
-    bool pairs = g >= 2 && (d64 || (t_prefill_variant != 1 &&
-                                    (g % 2 == 0 || t_prefill_variant >= 2 ||
-                                     pair_items >= dev->sm_count)));
+    // Only the pairs kernel has the 64-column form. With one query head per KV
+    // group it takes that head twice, as an odd group's last pair.
+    const bool d64 = s.head_dim == 64;
+    bool pairs = d64 || (g >= 2 && t_prefill_variant != 1 &&
+                         (g % 2 == 0 || t_prefill_variant >= 2 || pair_items >= dev->sm_count));
     if (pairs && prefill_pairs_smem_bytes(s.head_dim) > size_t(dev->max_smem_optin))
         pairs = false;
     if (d64 && !pairs)
@@ -909,17 +909,15 @@ pa_status prefill_route(const void* query, const void* key_pages, const void* va
                                    page_size, scale, out, shape);
     if (st != PA_OK)
         return st;
-    const bool d64_pairs = shape.head_dim == 64 && shape.num_q_heads >= 2 * shape.num_kv_heads;
-    if ((shape.head_dim == 128 || d64_pairs) && page_size >= 8) {
+    if ((shape.head_dim == 128 || shape.head_dim == 64) && page_size >= 8) {
         st = run_prefill_tc(query, key_pages, value_pages, block_table, context_lens, page_size,
                             scale, causal, out, shape, static_cast<cudaStream_t>(stream), nullptr, 0,
                             1.f, piece_ws, piece_ws_bytes);
         if (st != PA_ERR_UNSUPPORTED || shape.head_dim == 128)
             return st;
     }
-    // Pages smaller than 8 tokens, or D = 64 with one query head per KV group
-    // (or without the pairs kernel's register split): the split-KV kernel
-    // with whole segments per block.
+    // Pages smaller than 8 tokens, or D = 64 without the pairs kernel's
+    // register split: the split-KV kernel with whole segments per block.
     return run_split_kv(query, key_pages, value_pages, block_table, context_lens, page_size,
                         scale, causal, out, shape, 0, nullptr, 0, 1,
                         static_cast<cudaStream_t>(stream));

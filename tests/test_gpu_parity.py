@@ -325,11 +325,12 @@ def test_tc_prefill_page_sizes(ps, causal, H_q, H_kv, prefill_variant):
 
 @pytest.mark.parametrize("ps", [8, 16, 128, 256])
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("H_q,H_kv", [(8, 2), (6, 2), (4, 1)])   # groups of 4 / 3 / 4
+@pytest.mark.parametrize("H_q,H_kv", [(8, 2), (6, 2), (4, 1), (4, 4)])   # groups of 4 / 3 / 4 / 1
 def test_tc_prefill_head_dim64(ps, causal, H_q, H_kv):
     """head_dim 64 on the pairs kernel (one 64-column half per row, four
     k-steps for the scores, N = 64 for P V): several query tiles, a ragged
-    last tile, contexts across page boundaries, odd and even groups."""
+    last tile, contexts across page boundaries, odd and even groups, and one
+    query head per KV group (that head in both halves of a block)."""
     lens = [200, 129, 700, 300]
     b = wl.build_batch("tcprefill64", B=4, H_q=H_q, H_kv=H_kv, D=64, page_size=ps, L=129,
                        context_lens=lens, seed=ps + 3 * int(causal) + H_q, causal=causal,

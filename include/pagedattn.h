@@ -206,10 +206,10 @@ pa_status pa_decode_dense(const void *query, const void *key_dense,
  * Prefill attention: query rows in tiles, every K/V tile resolved through
  * block_table (Week 3 Day 4, "Task 2", the long-query page-walking
  * schedule), causal by default with the bottom-right offset above. Needs no
- * workspace. Tensor-core kernels (tcgen05, TMEM) for page_size >= 8 with
- * head_dim 128 or 64 (head_dim 64 with one query head per KV group computes
- * that head in both halves of a two-head block); smaller pages run the
- * split-KV kernel with whole segments per block.
+ * workspace. Tensor-core kernels (tcgen05, TMEM) for head_dim 128 or 64 and
+ * every page size. A KV group of one query head computes that head in both
+ * halves of a two-head block. Pages of fewer than 8 tokens are copied into
+ * shared memory row by row instead of one TMA box per page.
  */
 pa_status pa_prefill(const void *query, const void *key_pages,
                      const void *value_pages, const int32_t *block_table,

@@ -264,7 +264,8 @@ size_t split_prefill_need(const pa_shape& s, int32_t page_size, const DeviceInfo
     return split > pieces ? split : pieces;
 }
 
-// Prefill on tcgen05 (D = 128 or 64; page_size >= 8). With a workspace of at least split_prefill_need
+// Prefill on tcgen05 (D = 128 or 64; pages of fewer than 8 tokens on the
+// pairs kernel, whose loaders then copy K/V row by row). With a workspace of at least split_prefill_need
 // bytes: the split kernel (K/V tiles spread evenly over one block per SM);
 // otherwise the persistent pairs kernel (whole (request, head pair, 128-row
 // query tile) items) or one block per (request, query head, query tile).
@@ -291,14 +292,17 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     // us; with 256 pair items the pairs kernel is 22-33 % faster).
     const int g = s.num_q_heads / s.num_kv_heads;
     const int64_t pair_items = prefill_pair_items(s);
-    // Only the pairs kernel has the 64-column form. With one query head per KV
-    // group it takes that head twice, as an odd group's last pair.
+    // Only the pairs kernel has the 64-column form and the row-by-row loads of
+    // small pages. With one query head per KV group it takes that head twice,
+    // as an odd group's last pair.
     const bool d64 = s.head_dim == 64;
-    bool pairs = d64 || (g >= 2 && t_prefill_variant != 1 &&
-                         (g % 2 == 0 || t_prefill_variant >= 2 || pair_items >= dev->sm_count));
+    const bool small_pages = page_size < 8;
+    bool pairs = d64 || small_pages ||
+                 (g >= 2 && t_prefill_variant != 1 &&
+                  (g % 2 == 0 || t_prefill_variant >= 2 || pair_items >= dev->sm_count));
     if (pairs && prefill_pairs_smem_bytes(s.head_dim) > size_t(dev->max_smem_optin))
         pairs = false;
-    if (d64 && !pairs)
+    if ((d64 || small_pages) && !pairs)
         return PA_ERR_UNSUPPORTED;
     if (!pairs && prefill_smem_bytes() > size_t(dev->max_smem_optin))
         return PA_ERR_UNSUPPORTED;
@@ -338,6 +342,8 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
     a.causal = causal ? 1 : 0;
     a.out_scale = out_scale;
     a.D = s.head_dim;
+    a.key_pages = static_cast<const uint16_t*>(key_pages);
+    a.value_pages = static_cast<const uint16_t*>(value_pages);
     a.piece_last = t_prefill_variant == 5 ? 1 : 0;
     if (split) {
         SplitPrefillArgs sa;
@@ -383,7 +389,7 @@ pa_status run_prefill_tc(const void* query, const void* key_pages, const void* v
                                                  piece_ws_bytes, stream)
                           : launch_prefill(qmap, kmap, vmap, a, dev->id, stream);
     if (pairs && e == cudaErrorNotSupported) {   // register split not available
-        if (d64)
+        if (d64 || small_pages)
             return PA_ERR_UNSUPPORTED;
         e = launch_prefill(qmap, kmap, vmap, a, dev->id, stream);   // one head per block
     }
@@ -909,15 +915,15 @@ pa_status prefill_route(const void* query, const void* key_pages, const void* va
                                    page_size, scale, out, shape);
     if (st != PA_OK)
         return st;
-    if ((shape.head_dim == 128 || shape.head_dim == 64) && page_size >= 8) {
+    if (shape.head_dim == 128 || shape.head_dim == 64) {
         st = run_prefill_tc(query, key_pages, value_pages, block_table, context_lens, page_size,
                             scale, causal, out, shape, static_cast<cudaStream_t>(stream), nullptr, 0,
                             1.f, piece_ws, piece_ws_bytes);
         if (st != PA_ERR_UNSUPPORTED || shape.head_dim == 128)
             return st;
     }
-    // Pages smaller than 8 tokens, or D = 64 without the pairs kernel's
-    // register split: the split-KV kernel with whole segments per block.
+    // Without the pairs kernel's register split (head_dim 64, or pages of
+    // fewer than 8 tokens): the split-KV kernel with whole segments per block.
     return run_split_kv(query, key_pages, value_pages, block_table, context_lens, page_size,
                         scale, causal, out, shape, 0, nullptr, 0, 1,
                         static_cast<cudaStream_t>(stream));

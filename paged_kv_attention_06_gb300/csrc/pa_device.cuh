@@ -150,6 +150,20 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
     return __all_sync(0xffffffffu, ok);
 }
 
+// 16 bytes global -> shared without a register round trip (cp.async, L2
+// only); src_bytes < 16 fills the rest with zeros (0: no read at all).
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+                 "l"(gmem_src), "r"(src_bytes)
+                 : "memory");
+}
+// Waits until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) accesses of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem()

@@ -131,6 +131,10 @@ struct PrefillArgs {
     int32_t causal;
     float out_scale;    // the output is out_scale * softmax . V (e4m3 copies: v_scale)
     int32_t D;          // head_dim: 128 (64 on the pairs kernel only)
+    // The pools, read row by row on the pairs kernel when a page holds fewer
+    // than 8 tokens (otherwise through the tensor maps).
+    const uint16_t* key_pages;    // [P, H_kv, ps, D]
+    const uint16_t* value_pages;
     // Pairs kernel, tail pieces (head_dim 128; state == nullptr: none): per
     // donor block slot, part (0: the item's last tiles, 1: its first tiles)
     // and head, O / l in bf16 [16 chunks of 8 columns][128 rows] and (m, l)

@@ -355,7 +355,12 @@ __device__ __forceinline__ void piece_arrive_receiver(const uint4* state, const 
 // tail pieces' planning and epilogues (head_dim 128; a separate instantiation,
 // so that the whole-item kernel's code and registers stay as they are: with
 // the piece code compiled in, whole items ran 2-3 us per call slower).
-template <bool kOdd, int kD, bool kPieces>
+// kSmall: pages of fewer than 8 tokens. A TMA box of one page would start
+// inside a 128-byte swizzle atom (8 rows), so the loaders copy the K/V rows
+// one by one instead (cp.async into the swizzled layout, rows past the
+// context zero-filled), wait for their own copies and fence them to the
+// tensor cores' proxy before they arrive.
+template <bool kOdd, int kD, bool kPieces, bool kSmall>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pairs_kernel(const __grid_constant__ CUtensorMap q_map,
                          const __grid_constant__ CUtensorMap key_map,
@@ -604,6 +609,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int tok = (k0 + j) * kKeys + my_box * box;
                     return (phys * a.H_kv + hk) * a.ps + (tok - (tok / a.ps) * a.ps);
                 };
+                // Pages of fewer than 8 tokens: row r of tile j (row r of
+                // each 64-column half at r * 128 bytes, its 16-byte chunk c at
+                // chunk c ^ (r mod 8), the 128-byte swizzle) from its page.
+                auto load_rows = [&](int j, bool is_v) {
+                    const int gj = g + j;
+                    const int s = gj & 1;
+                    const int full = (is_v ? kVFull : kKFull) + s;
+                    const int empty = (is_v ? kVEmpty : kKEmpty) + s;
+                    const bool ok = mbar_wait_warp(&bar[empty], ((gj >> 1) & 1) ^ 1u, misc, a.err);
+                    if (ok) {
+                        const int key0 = (k0 + j) * kKeys;
+                        uint8_t* dst = smem + (is_v ? Layout::kV : Layout::kK) + s * Layout::kMat;
+                        const uint16_t* pool = is_v ? a.value_pages : a.key_pages;
+                        for (int r = li * 32 + lane; r < kKeys; r += 96) {
+                            const int key = key0 + r;
+                            const bool live = key < n;
+                            int64_t row = 0;
+                            if (live) {
+                                int phys = bt[key / a.ps];
+                                if (unsigned(phys) >= unsigned(a.num_pages)) {
+                                    atomicOr(a.err, PA_DEVERR_PAGE_ID_BIT);
+                                    phys = 0;
+                                }
+                                row = (int64_t(phys) * a.H_kv + hk) * a.ps + (key - (key / a.ps) * a.ps);
+                            }
+                            const uint8_t* src = reinterpret_cast<const uint8_t*>(pool + row * kD);
+                            uint8_t* drow = dst + r * 128;
+#pragma unroll
+                            for (int h = 0; h < Layout::kHalves; ++h)
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    cp_async_16(drow + h * Layout::kHalf + ((c ^ (r & 7)) << 4),
+                                                src + h * 128 + c * 16, live ? 16u : 0u);
+                        }
+                        cp_async_wait_all();
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&bar[full], 0u);
+                    }
+                    __syncwarp();
+                };
                 auto load = [&](int j, bool is_v, int phys) {
                     const int nbox = n_boxes(j);
                     const int mine = nbox > li ? (nbox - li + 2) / 3 : 0;
@@ -645,21 +692,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                 };
-                int pg[3];
-                pg[0] = fetch_page(0);
-                pg[1] = fetch_page(1);
-                load(0, false, pg[0]);
-                if (li < 2 && qk > 0)    // the first item's Q went out at the start
-                    load_q();
-                for (int j0 = 0; j0 < nt; j0 += 3) {
+                if constexpr (kSmall) {
+                    load_rows(0, false);
+                    if (li < 2 && qk > 0)    // the first item's Q went out at the start
+                        load_q();
+                    for (int j = 0; j < nt; ++j) {
+                        load_rows(j, true);
+                        if (j + 1 < nt)
+                            load_rows(j + 1, false);
+                    }
+                } else {
+                    int pg[3];
+                    pg[0] = fetch_page(0);
+                    pg[1] = fetch_page(1);
+                    load(0, false, pg[0]);
+                    if (li < 2 && qk > 0)    // the first item's Q went out at the start
+                        load_q();
+                    for (int j0 = 0; j0 < nt; j0 += 3) {
 #pragma unroll
-                    for (int u = 0; u < 3; ++u) {
-                        const int j = j0 + u;
-                        if (j < nt) {
-                            pg[(u + 2) % 3] = fetch_page(j + 2);
-                            load(j, true, pg[u]);
-                            if (j + 1 < nt)
-                                load(j + 1, false, pg[(u + 1) % 3]);
+                        for (int u = 0; u < 3; ++u) {
+                            const int j = j0 + u;
+                            if (j < nt) {
+                                pg[(u + 2) % 3] = fetch_page(j + 2);
+                                load(j, true, pg[u]);
+                                if (j + 1 < nt)
+                                    load(j + 1, false, pg[(u + 1) % 3]);
+                            }
                         }
                     }
                 }
@@ -1147,7 +1205,7 @@ namespace {
 
 // Register split and shared-memory limit checked once per device and
 // instantiation, then the launch.
-template <bool kOdd, int kD, bool kPieces>
+template <bool kOdd, int kD, bool kPieces, bool kSmall>
 cudaError_t launch_pairs(const cudaLaunchConfig_t& cfg_in, const CUtensorMap& q_map,
                          const CUtensorMap& key_map, const CUtensorMap& value_map,
                          const CUtensorMap& out_map, const PrefillArgs& a, int device)
@@ -1157,7 +1215,7 @@ cudaError_t launch_pairs(const cudaLaunchConfig_t& cfg_in, const CUtensorMap& q_
     static std::atomic<int> regs_ok[kMaxDev];
     if (device < 0 || device >= kMaxDev)
         return cudaErrorInvalidDevice;
-    const void* fn = reinterpret_cast<const void*>(prefill_pairs_kernel<kOdd, kD, kPieces>);
+    const void* fn = reinterpret_cast<const void*>(prefill_pairs_kernel<kOdd, kD, kPieces, kSmall>);
     const int smem = Layout<kD>::kBytes;
     // The register split needs 128 x kRegsProducer + 256 x kRegsSoftmax
     // registers out of the launch's own 384 x numRegs, a launch count no
@@ -1184,7 +1242,7 @@ cudaError_t launch_pairs(const cudaLaunchConfig_t& cfg_in, const CUtensorMap& q_
     }
     cudaLaunchConfig_t cfg = cfg_in;
     cfg.dynamicSmemBytes = size_t(smem);
-    return cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<kOdd, kD, kPieces>, q_map, key_map, value_map,
+    return cudaLaunchKernelEx(&cfg, prefill_pairs_kernel<kOdd, kD, kPieces, kSmall>, q_map, key_map, value_map,
                               out_map, a);
 }
 
@@ -1225,21 +1283,29 @@ cudaError_t launch_prefill_pairs(const CUtensorMap& q_map, const CUtensorMap& ke
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const bool odd = a.G % 2 != 0;
+    const bool small = a.ps < 8;
     auto launch = [&]() {
+        if (small) {
+            if (a.D == 64)
+                return odd ? launch_pairs<true, 64, false, true>(cfg, q_map, key_map, value_map, out_map, a, device)
+                           : launch_pairs<false, 64, false, true>(cfg, q_map, key_map, value_map, out_map, a, device);
+            return odd ? launch_pairs<true, 128, false, true>(cfg, q_map, key_map, value_map, out_map, a, device)
+                       : launch_pairs<false, 128, false, true>(cfg, q_map, key_map, value_map, out_map, a, device);
+        }
         if (a.D == 64)
-            return odd ? launch_pairs<true, 64, false>(cfg, q_map, key_map, value_map, out_map, a, device)
-                       : launch_pairs<false, 64, false>(cfg, q_map, key_map, value_map, out_map, a, device);
+            return odd ? launch_pairs<true, 64, false, false>(cfg, q_map, key_map, value_map, out_map, a, device)
+                       : launch_pairs<false, 64, false, false>(cfg, q_map, key_map, value_map, out_map, a, device);
         if (a.state != nullptr)
-            return odd ? launch_pairs<true, 128, true>(cfg, q_map, key_map, value_map, out_map, a, device)
-                       : launch_pairs<false, 128, true>(cfg, q_map, key_map, value_map, out_map, a, device);
-        return odd ? launch_pairs<true, 128, false>(cfg, q_map, key_map, value_map, out_map, a, device)
-                   : launch_pairs<false, 128, false>(cfg, q_map, key_map, value_map, out_map, a, device);
+            return odd ? launch_pairs<true, 128, true, false>(cfg, q_map, key_map, value_map, out_map, a, device)
+                       : launch_pairs<false, 128, true, false>(cfg, q_map, key_map, value_map, out_map, a, device);
+        return odd ? launch_pairs<true, 128, false, false>(cfg, q_map, key_map, value_map, out_map, a, device)
+                   : launch_pairs<false, 128, false, false>(cfg, q_map, key_map, value_map, out_map, a, device);
     };
     // Tail pieces: with a workspace, one or two items per block and the
     // ranking in shared memory; otherwise whole items. No block waits for
     // another (the second to arrive merges), so the launch is an ordinary one.
     const int64_t M = int64_t(a.B) * a.n_qtiles;
-    if (workspace && a.D == 128 && M <= kThreads && n_items > grid && n_items <= 2 * grid &&
+    if (workspace && !small && a.D == 128 && M <= kThreads && n_items > grid && n_items <= 2 * grid &&
         workspace_bytes >= prefill_pairs_workspace_bytes(int(grid)) &&
         (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0) {
         uint8_t* w = static_cast<uint8_t*>(workspace);

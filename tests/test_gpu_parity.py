@@ -309,7 +309,7 @@ def prefill_variant(request):
     pa.pa_debug_prefill_variant(prev)
 
 
-@pytest.mark.parametrize("ps", [8, 16, 64, 128, 256])
+@pytest.mark.parametrize("ps", [1, 2, 4, 8, 16, 64, 128, 256])   # below 8: rows copied one by one
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("H_q,H_kv", [(8, 2), (6, 2)])   # group of 4 / 3
 def test_tc_prefill_page_sizes(ps, causal, H_q, H_kv, prefill_variant):
@@ -323,7 +323,7 @@ def test_tc_prefill_page_sizes(ps, causal, H_q, H_kv, prefill_variant):
     assert_close(host_f64(out), oracle_out(b, kp, vp), f"tc prefill ps={ps} causal={causal}")
 
 
-@pytest.mark.parametrize("ps", [8, 16, 128, 256])
+@pytest.mark.parametrize("ps", [1, 4, 8, 16, 128, 256])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("H_q,H_kv", [(8, 2), (6, 2), (4, 1), (4, 4)])   # groups of 4 / 3 / 4 / 1
 def test_tc_prefill_head_dim64(ps, causal, H_q, H_kv):

@@ -137,10 +137,12 @@ enum { kWhole = 0, kPublish = 1, kMerge = 2 };
 // weights are measured: on 4 requests of 512 rows after ragged prefixes (the
 // busiest blocks at two items of 14 tiles, the idlest at one of 17) they give
 // d = 6, 52.6 us per call back to back; d = 4 / 5 / 7 / 8 gave 55.0 / 53.8 /
-// 54.5 / 56.5 (with an earlier hand-over that waited for a flag).
+// 54.5 / 56.5 (with an earlier hand-over that waited for a flag). A merge
+// weight of 4 gives the same d there and measured 0.3 us faster than 8 on the
+// whole batch (12 and 16: 0.7 and 1.7 us slower).
 constexpr int kWItem = 4;
 constexpr int kWPiece = 0;
-constexpr int kWMerge = 8;
+constexpr int kWMerge = 4;
 
 // Operand descriptors (128B swizzle). K-major [half][128 rows][128 B] (Q, K):
 // k-step kk (16 elements along K) starts kmajor_off(kk) bytes in. MN-major

@@ -19,10 +19,10 @@ extern "C" {
 /*
  * Test support for failure detection. The next call made by the calling
  * host thread that runs the split-KV kernel (pa_decode, pa_decode_noalloc,
- * pa_attention routed to decode, and the prefill of head_dim 64 or of pages
- * under 8 tokens) runs one extra wait, in its first block, on a barrier that
- * nothing ever arrives at. That wait runs out after its bounded limit (about
- * one second), records PA_DEVERR_TIMEOUT in the device error word, and the
+ * pa_decode_dense, pa_attention routed to decode) runs one extra wait, in
+ * its first block, on a barrier that nothing ever arrives at. That wait runs
+ * out after its bounded limit (about one second), records PA_DEVERR_TIMEOUT
+ * in the device error word, and the
  * kernel then finishes normally with the correct result. Nothing faults or
  * hangs; the CUDA context stays usable.
  */
@@ -30,7 +30,9 @@ void pa_debug_arm_wait_timeout(void);
 
 /*
  * Test and tuning support: which tensor-core prefill kernel the calling host
- * thread's pa_prefill / pa_attention calls use (head_dim 128, page_size >= 8).
+ * thread's pa_prefill / pa_attention calls use (head_dim 128 and pages of 8
+ * tokens or more; head_dim 64 and smaller pages always take the two-head
+ * kernel).
  *   0  automatic (the default): as 2, except that a group size that is odd
  *      with fewer (request, head pair, query tile) items than SMs takes 1;
  *   1  one query head per block;

@@ -158,10 +158,17 @@ __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src
                  "l"(gmem_src), "r"(src_bytes)
                  : "memory");
 }
-// Waits until every cp.async this thread issued has landed.
-__device__ __forceinline__ void cp_async_wait_all()
+// Closes the group of this thread's cp.async issued since the last commit.
+__device__ __forceinline__ void cp_async_commit()
 {
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most kPending of this thread's committed groups (the most
+// recent ones) are still landing.
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait_group()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later

@@ -360,8 +360,9 @@ __device__ __forceinline__ void piece_arrive_receiver(const uint4* state, const 
 // kSmall: pages of fewer than 8 tokens. A TMA box of one page would start
 // inside a 128-byte swizzle atom (8 rows), so the loaders copy the K/V rows
 // one by one instead (cp.async into the swizzled layout, rows past the
-// context zero-filled), wait for their own copies and fence them to the
-// tensor cores' proxy before they arrive.
+// context zero-filled). Each loader warp waits for its own copies of a stage
+// once it has issued the next stage's, fences them to the tensor cores'
+// proxy and then arrives.
 template <bool kOdd, int kD, bool kPieces, bool kSmall>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pairs_kernel(const __grid_constant__ CUtensorMap q_map,
@@ -584,6 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int my_box = li + 3 * lane;
             int g = 0;                                   // tiles of the block before this item
             int qk = 0;                                  // items with tiles before this one
+            int pend_full = -1;                          // pages under 8 tokens: the stage whose
+            bool pend_ok = false;                        // copies are pending (its full barrier)
             for (int it = 0; it < n_items; ++it) {
                 const int32_t* e = items + it * kEntry;
                 const int nt = e[kENT], k0 = e[kEK0];
@@ -614,6 +617,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Pages of fewer than 8 tokens: row r of tile j (row r of
                 // each 64-column half at r * 128 bytes, its 16-byte chunk c at
                 // chunk c ^ (r mod 8), the 128-byte swizzle) from its page.
+                // One stage's copies stay pending while the next stage's are
+                // issued; then the pending stage is waited for, fenced and
+                // arrived at. (Its consumer comes after the next stage's
+                // empty barrier in the MMA order: K_j after the P V that frees
+                // V_j, V_j after the S that frees K_j+1.)
+                auto land_pending = [&](bool keep_one) {
+                    if (keep_one)
+                        cp_async_wait_group<1>();
+                    else
+                        cp_async_wait_group<0>();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (pend_ok && lane == 0)
+                        mbar_arrive_expect_tx(&bar[pend_full], 0u);
+                    __syncwarp();
+                    pend_full = -1;
+                };
                 auto load_rows = [&](int j, bool is_v) {
                     const int gj = g + j;
                     const int s = gj & 1;
@@ -645,13 +665,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     cp_async_16(drow + h * Layout::kHalf + ((c ^ (r & 7)) << 4),
                                                 src + h * 128 + c * 16, live ? 16u : 0u);
                         }
-                        cp_async_wait_all();
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive_expect_tx(&bar[full], 0u);
                     }
-                    __syncwarp();
+                    cp_async_commit();
+                    if (pend_full >= 0)
+                        land_pending(true);
+                    pend_full = full;
+                    pend_ok = ok;
                 };
                 auto load = [&](int j, bool is_v, int phys) {
                     const int nbox = n_boxes(j);
@@ -703,6 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (j + 1 < nt)
                             load_rows(j + 1, false);
                     }
+                    land_pending(false);
                 } else {
                     int pg[3];
                     pg[0] = fetch_page(0);

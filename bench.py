@@ -463,6 +463,10 @@ def main(argv=None):
     ap.add_argument("--prefill-shapes", action="store_true",
                     help="time both prefill kernels on chunked-prefill shapes and exit")
     ap.add_argument("--shape", default=None, help="with --prefill-shapes: only this shape")
+    ap.add_argument("--shapes-page-size", type=int, default=16,
+                    help="with --prefill-shapes: tokens per page")
+    ap.add_argument("--shapes-head-dim", type=int, default=128,
+                    help="with --prefill-shapes: head_dim (128 or 64)")
     ap.add_argument("--shapes-heads", default="32x8",
                     help="with --prefill-shapes: query heads x KV heads, e.g. 28x4")
     ap.add_argument("--serving-trace", action="store_true",
@@ -503,8 +507,9 @@ def main(argv=None):
         return 0
     if args.prefill_shapes:
         hq, hkv = (int(x) for x in args.shapes_heads.split("x"))
-        print(json.dumps({"prefill_shapes": prefill_shapes(torch, device, args.shape,
-                                                           heads=(hq, hkv))}))
+        print(json.dumps({"prefill_shapes": prefill_shapes(
+            torch, device, args.shape, heads=(hq, hkv), page_size=args.shapes_page_size,
+            head_dim=args.shapes_head_dim)}))
         return 0
     if args.serving_trace:
         serving_trace(torch, device)            # warm-up run (builds, first calls)
@@ -1219,14 +1224,17 @@ PREFILL_SHAPES = [
 ]
 
 
-def prefill_shapes(torch, device, only=None, steps=15, heads=(32, 8)):
+def prefill_shapes(torch, device, only=None, steps=15, heads=(32, 8), page_size=16,
+                   head_dim=128):
     """The tensor-core prefill paths (pa_attention with its workspace, as the
     product calls it; pa_prefill: whole request x head pair x query tile items
     on one block per SM; pa_prefill_split: K/V tiles spread over one block per
     SM; pa_prefill_fp8 on e4m3 pools) on chunked-prefill shapes with few and
     many query-tile items, L2 flushed before every call, CUDA events. Inputs:
     seeded N(0,1) K/V already in the pages (no append), random page
-    permutation."""
+    permutation. With head_dim 64 or pages of fewer than 8 tokens (the pairs
+    kernel only, no e4m3 pools) the split-KV kernel (pa_decode) is timed
+    beside it instead."""
     import paged_kv_attention_06_gb300 as pa
     flush = torch.empty(int(2 * torch.cuda.get_device_properties(device).L2_cache_size),
                         dtype=torch.uint8, device=device)
@@ -1254,8 +1262,10 @@ def prefill_shapes(torch, device, only=None, steps=15, heads=(32, 8)):
     for name, B, L, lens in PREFILL_SHAPES:
         if only and name != only:
             continue
-        b = wl.build_batch(name, B=B, H_q=heads[0], H_kv=heads[1], D=128, page_size=16, L=L,
-                           context_lens=lens, seed=5, L_new=0, placement="permutation")
+        b = wl.build_batch(name, B=B, H_q=heads[0], H_kv=heads[1], D=head_dim,
+                           page_size=page_size, L=L, context_lens=lens, seed=5, L_new=0,
+                           placement="permutation")
+        pairs_only = head_dim != 128 or page_size < 8
         q, kp, vp = to_dev(b.query), to_dev(b.key_pages), to_dev(b.value_pages)
         bt, cl = to_dev(b.block_table), to_dev(b.context_lens)
         out = torch.empty_like(q)
@@ -1273,6 +1283,21 @@ def prefill_shapes(torch, device, only=None, steps=15, heads=(32, 8)):
                                                causal=True, out=out, max_context_len=mcl_att,
                                                workspace=ws_att))
         del ws_att
+        fl = prefill_flops(b)
+        items = B * ((L + 127) // 128) * heads[1] * ((heads[0] // heads[1] + 1) // 2)
+        if pairs_only:
+            ws_dec, _ = pa.decode_workspace(pa.make_shape(q.shape, kp.shape, bt.shape[1]), device)
+            t_dec = timeit(lambda: pa.pa_decode(q, kp, vp, bt, cl, b.page_size, scale=b.scale,
+                                                causal=True, out=out, max_context_len=mcl_att,
+                                                workspace=ws_dec))
+            del ws_dec
+            rows.append({"shape": name, "items": items, "items_per_sm": round(items / sms, 2),
+                         "gflop": round(fl / 1e9, 2), "page_size": page_size,
+                         "head_dim": head_dim, "attention_us": round(t_att, 2),
+                         "attention_tflops": round(fl / t_att / 1e6, 1),
+                         "split_kv_decode_us": round(t_dec, 2),
+                         "attention_picks": "pairs"})
+            continue
         rng = np.random.default_rng(6)
         kc = torch.from_numpy(wl.random_e4m3_codes(rng, b.key_pages.shape)).to(device)
         vc = torch.from_numpy(wl.random_e4m3_codes(rng, b.value_pages.shape)).to(device)
@@ -1283,8 +1308,6 @@ def prefill_shapes(torch, device, only=None, steps=15, heads=(32, 8)):
                                                  scale=b.scale, causal=True, out=out,
                                                  max_context_len=mcl, workspace=ws8))
         del ws8
-        fl = prefill_flops(b)
-        items = B * ((L + 127) // 128) * heads[1] * ((heads[0] // heads[1] + 1) // 2)
         rows.append({"shape": name, "items": items, "items_per_sm": round(items / sms, 2),
                      "gflop": round(fl / 1e9, 2),
                      "attention_us": round(t_att, 2),

@@ -587,10 +587,12 @@ def main(argv=None):
             raise RuntimeError(f"native step loop failed with status {st}")
         return float(total.value)
 
-    # The K timed steps run as up to four blocks, each bracketed by events
-    # (none inside a block); the step time is their sum over K, and the blocks'
-    # own per-step times give the repeat spread.
-    n_blocks = 4 if args.steps >= 8 else 1
+    # The K timed steps run as up to four blocks of at least 25 steps, each
+    # bracketed by events (none inside a block); the step time is their sum
+    # over K, and the blocks' own per-step times give the repeat spread. A
+    # block boundary breaks the kernels' launch overlap once, so short runs
+    # take one block.
+    n_blocks = max(1, min(4, args.steps // 25))
     block_sizes = [args.steps // n_blocks + (1 if i < args.steps % n_blocks else 0)
                    for i in range(n_blocks)]
 
